@@ -1,0 +1,246 @@
+"""CPU oracle of the qwen3moe MoE FFN over GGUF k-quant experts (double precision).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's
+CPU-baseline leg may import this package; the product path never does.  It
+shares no code with the CUDA path; both take their inputs from ``synth``.
+
+The arithmetic lives in ``qmoe_oracle.c`` (plain C, every quantity in double,
+serial sums in index order).  ``dequant_np`` is a second, independent numpy
+dequantiser used only to cross-check the C one.
+
+Sources: aprender issue "qwen3moe (Qwen3-30B-A3B, Qwen3-Coder-30B-A3B, Q4_K_M)
+has NO working CUDA path" (sections "File facts", "Gaps ... G3"); aprender issue
+"Qwen3 GPU inference produces garbage output" ("Fix Applied"); aprender PR
+"apply per-head Q/K RMSNorm in forward_qwen3_moe" ("The fix"); SharpInference
+issue "Forward-pass divergence on Qwen3-Coder 30B-A3B" (closing comment).
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test (closed
+forms, library routines, brute force, invariants); the 48-layer composition as a
+whole is pinned only through its pinned parts.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmoe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libqmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+Q4_K, Q6_K = 1, 2
+QCODE = {"Q4_K": Q4_K, "Q6_K": Q6_K}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _p(a, t):
+    return None if a is None else a.ctypes.data_as(C.POINTER(t))
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = C.CDLL(_LIB)
+            dp, fp, ip, up8, u16 = (C.POINTER(C.c_double), C.POINTER(C.c_float),
+                                    C.POINTER(C.c_int32), C.POINTER(C.c_uint8),
+                                    C.POINTER(C.c_uint16))
+            L.qo_half_to_double.argtypes = [C.c_uint16]
+            L.qo_half_to_double.restype = C.c_double
+            L.qo_double_to_half.argtypes = [C.c_double]
+            L.qo_double_to_half.restype = C.c_uint16
+            L.qo_block_bytes.argtypes = [C.c_int]
+            L.qo_expert_stride.argtypes = [C.c_int, C.c_long, C.c_long]
+            L.qo_expert_stride.restype = C.c_long
+            L.qo_dequant_block.argtypes = [C.c_int, up8, dp]
+            L.qo_dequant_matrix.argtypes = [C.c_int, up8, C.c_long, C.c_long, dp]
+            L.qo_router.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, fp, fp, ip,
+                                    fp, ip, dp, dp]
+            L.qo_moe_ffn.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, dp, ip, dp,
+                                     up8, C.c_int, up8, C.c_int, up8, C.c_int, dp, dp, dp]
+            L.qo_rmsnorm.argtypes = [C.c_long, dp, fp, C.c_double, dp]
+            L.qo_rope_neox.argtypes = [C.c_int, dp, C.c_int, C.c_double]
+            L.qo_attend.argtypes = [C.c_int, dp, u16, u16, C.c_int, dp]
+            L.qo_decode_layer.argtypes = (
+                [C.c_int] * 8 + [C.c_double, C.c_double, C.c_int, dp] + [fp] * 4 + [up8] * 4
+                + [fp, up8, up8, up8, C.c_int, u16, u16, ip, fp, ip, dp, dp, dp])
+            _lib = L
+    return _lib
+
+
+def _u8(a):
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+# ----------------------------------------------------------------------------- fp16 / dequant
+
+def half_to_double(bits: int) -> float:
+    return lib().qo_half_to_double(int(bits))
+
+
+def double_to_half_bits(v: float) -> int:
+    return lib().qo_double_to_half(float(v))
+
+
+def expert_stride(qtype: str, rows: int, cols: int) -> int:
+    return lib().qo_expert_stride(QCODE[qtype], rows, cols)
+
+
+def dequant_block(qtype: str, blk: np.ndarray) -> np.ndarray:
+    blk = _u8(blk).reshape(-1)
+    out = np.empty(256, dtype=np.float64)
+    rc = lib().qo_dequant_block(QCODE[qtype], _p(blk, C.c_uint8), _p(out, C.c_double))
+    if rc:
+        raise ValueError("bad qtype")
+    return out
+
+
+def dequant_matrix(qtype: str, data: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    data = _u8(data).reshape(-1)
+    out = np.empty((rows, cols), dtype=np.float64)
+    rc = lib().qo_dequant_matrix(QCODE[qtype], _p(data, C.c_uint8), rows, cols, _p(out, C.c_double))
+    if rc:
+        raise ValueError("dequant_matrix failed")
+    return out
+
+
+# ----------------------------------------------------------------------------- router / FFN
+
+def route(x, router, K, bias=None, norm_topk=True, force=None):
+    """Returns (logits f32 [T][E], ids int32 [T][K], w f64 [T][K], probs f64 [T][E])."""
+    x = _f64(np.atleast_2d(x))
+    T, H = x.shape
+    E = router.shape[0]
+    router = _f32(router)
+    bias = _f32(bias)
+    force = None if force is None else np.ascontiguousarray(force, dtype=np.int32)
+    logits = np.empty((T, E), dtype=np.float32)
+    ids = np.empty((T, K), dtype=np.int32)
+    w = np.empty((T, K), dtype=np.float64)
+    probs = np.empty((T, E), dtype=np.float64)
+    rc = lib().qo_router(T, H, E, K, int(bool(norm_topk)), _p(x, C.c_double), _p(router, C.c_float),
+                         _p(bias, C.c_float), _p(force, C.c_int32), _p(logits, C.c_float),
+                         _p(ids, C.c_int32), _p(w, C.c_double), _p(probs, C.c_double))
+    if rc:
+        raise ValueError("router failed")
+    return logits, ids, w, probs
+
+
+def moe_ffn(x, ids, w, gate, up, down, gate_t, up_t, down_t, F, E, res=None, want_act=False):
+    """out [T][H] (f64) = res + sum_j w_j * Wd(silu(Wg x) * Wu x); optional act [T][K][F]."""
+    x = _f64(np.atleast_2d(x))
+    T, H = x.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    K = ids.shape[1]
+    w = _f64(w)
+    res = None if res is None else _f64(np.atleast_2d(res))
+    out = np.empty((T, H), dtype=np.float64)
+    act = np.empty((T, K, F), dtype=np.float64) if want_act else None
+    g8, u8, d8 = _u8(gate).reshape(-1), _u8(up).reshape(-1), _u8(down).reshape(-1)
+    rc = lib().qo_moe_ffn(T, H, F, E, K, _p(x, C.c_double), _p(res, C.c_double), _p(ids, C.c_int32),
+                          _p(w, C.c_double), _p(g8, C.c_uint8), QCODE[gate_t], _p(u8, C.c_uint8),
+                          QCODE[up_t], _p(d8, C.c_uint8), QCODE[down_t], _p(out, C.c_double),
+                          _p(act, C.c_double), None)
+    if rc:
+        raise ValueError(f"moe_ffn failed rc={rc}")
+    return (out, act) if want_act else out
+
+
+def moe_forward(inp: dict, norm_topk=True, force=None):
+    """out = x + MoE(x) for one layer's synthetic inputs (see ``synth.moe_inputs``)."""
+    logits, ids, w, probs = route(inp["x"], inp["router"], inp["K"], inp.get("bias"), norm_topk,
+                                  force)
+    out = moe_ffn(inp["x"], ids, w, inp["gate"], inp["up"], inp["down"], inp["gate_t"],
+                  inp["up_t"], inp["down_t"], inp["F"], inp["E"])
+    return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
+
+
+# ----------------------------------------------------------------------------- decoder layer
+
+def rmsnorm(x, w, eps):
+    x = _f64(x)
+    out = np.empty_like(x)
+    lib().qo_rmsnorm(x.size, _p(x, C.c_double), _p(_f32(w), C.c_float), eps, _p(out, C.c_double))
+    return out
+
+
+def rope_neox(v, pos, base):
+    v = _f64(v).copy()
+    lib().qo_rope_neox(v.size, _p(v, C.c_double), int(pos), float(base))
+    return v
+
+
+def attend(q, k_cache, v_cache, pos):
+    """k_cache/v_cache: fp16 [ctx][hd] of one kv head."""
+    q = _f64(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.float16).view(np.uint16)
+    vc = np.ascontiguousarray(v_cache, dtype=np.float16).view(np.uint16)
+    out = np.empty(q.size, dtype=np.float64)
+    lib().qo_attend(q.size, _p(q, C.c_double), _p(kc, C.c_uint16), _p(vc, C.c_uint16), int(pos),
+                    _p(out, C.c_double))
+    return out
+
+
+def decode_layer(geo: dict, small: dict, experts: dict, h, pos, force=None, debug=False):
+    """One decoder layer on hidden h (f64 [H]).
+
+    Returns dict(h, ids, w, logits, k_cache, v_cache[, q, att]).  The caller's
+    caches are not modified: the layer writes slot ``pos`` of copies.
+    """
+    h = _f64(h).copy()
+    kc = np.ascontiguousarray(small["k_cache"], dtype=np.float16).copy()
+    vc = np.ascontiguousarray(small["v_cache"], dtype=np.float16).copy()
+    K, E = geo["K"], geo["E"]
+    ids = np.empty(K, dtype=np.int32)
+    w = np.empty(K, dtype=np.float64)
+    logits = np.empty(E, dtype=np.float32)
+    force = None if force is None else np.ascontiguousarray(force, dtype=np.int32)
+    args = [geo["H"], E, K, geo["F"], geo["n_heads"], geo["n_kv"], geo["head_dim"], geo["ctx"],
+            geo["eps"], geo["rope_base"], int(pos), _p(h, C.c_double)]
+    norms = [_f32(small[n]) for n in ("attn_norm", "q_norm", "k_norm", "ffn_norm")]
+    args += [_p(a, C.c_float) for a in norms]
+    keep = [_u8(small[n]).reshape(-1) for n in ("wq", "wk", "wv", "wo")]
+    args += [_p(a, C.c_uint8) for a in keep]
+    ex = [_u8(experts[n]).reshape(-1) for n in ("gate", "up", "down")]
+    router = _f32(small["router"])
+    args += [_p(router, C.c_float)] + [_p(a, C.c_uint8) for a in ex]
+    args += [QCODE[small["down_t"]], _p(kc.view(np.uint16), C.c_uint16),
+             _p(vc.view(np.uint16), C.c_uint16), _p(force, C.c_int32), _p(logits, C.c_float),
+             _p(ids, C.c_int32), _p(w, C.c_double)]
+    qd = geo["n_heads"] * geo["head_dim"]
+    q = np.empty(qd, dtype=np.float64) if debug else None
+    att = np.empty(qd, dtype=np.float64) if debug else None
+    args += [_p(q, C.c_double), _p(att, C.c_double)]
+    rc = lib().qo_decode_layer(*args)
+    if rc:
+        raise ValueError(f"decode_layer failed rc={rc}")
+    out = dict(h=h, ids=ids, w=w, logits=logits, k_cache=kc, v_cache=vc)
+    if debug:
+        out.update(q=q, att=att)
+    return out

@@ -1,0 +1,416 @@
+/*
+ * qmoe_oracle.c -- plain CPU oracle of the qwen3moe MoE FFN over GGUF k-quant
+ * expert weights, and of one qwen3moe decoder layer at decode time.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the package's smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code with the CUDA path.
+ *
+ * Every quantity is computed in double from the exact stored fields, with no
+ * blocking, fusion or reordering beyond the definitions cited next to each
+ * function.  Threads (OpenMP) only split independent outer loops (experts,
+ * heads); every reduction is a plain serial sum in index order.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [P2] aprender issue "qwen3moe (Qwen3-30B-A3B, Qwen3-Coder-30B-A3B, Q4_K_M)
+ *       has NO working CUDA path", sections "File facts" (geometry, 144 B Q4_K /
+ *       210 B Q6_K superblocks, 884,736 / 1,290,240 B per expert, base + e*stride
+ *       addressing), "Gaps ... G3" (router GEMV, per-qtype expert GEMVs, fused
+ *       SwiGLU, weighted sum, residual add, softmax/top-8/renorm).
+ *  [P1] aprender issue "Qwen3 GPU inference produces garbage output", section
+ *       "Fix Applied" (head_dim 128 independent of hidden/heads, GQA uses head_dim,
+ *       per-head Q/K RMSNorm).
+ *  [P4] aprender PR "apply per-head Q/K RMSNorm in forward_qwen3_moe", section
+ *       "The fix" (Q/K norm after bias, before RoPE).
+ *  [P5] SharpInference issue "Forward-pass divergence on Qwen3-Coder 30B-A3B",
+ *       closing comment (NEOX RoPE: rotated pairs offset by head_dim/2).
+ *  The bit layout inside a Q4_K / Q6_K superblock is the public GGUF k-quant
+ *  format; the pages fix only the superblock sizes and field order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QO_QK 256
+#define QO_Q4_K 1
+#define QO_Q6_K 2
+
+/* ------------------------------------------------------------------ fp16 */
+
+/* IEEE 754 binary16 -> double, exact for every finite pattern incl. subnormals. */
+double qo_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 31;
+    int man = h & 1023;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)man, -24);             /* man * 2^-24 */
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + man), ex - 25); /* (1 + man/1024) * 2^(ex-15) */
+    return sign ? -v : v;
+}
+
+/* double -> binary16 with round-to-nearest-even (used for the KV-cache write). */
+uint16_t qo_double_to_half(double v) {
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return 0x7e00;
+    if (a >= 65520.0) return sign | 0x7c00;      /* rounds past the largest finite half */
+    if (a < ldexp(1.0, -14)) {                    /* subnormal range: multiples of 2^-24 */
+        double r = nearbyint(ldexp(a, 24));
+        return sign | (uint16_t)r;                /* r == 1024 is the smallest normal */
+    }
+    int e;
+    double f = frexp(a, &e);                      /* a = f * 2^e, f in [0.5, 1) */
+    double r = nearbyint(ldexp(f, 11));           /* 11 significant bits, in [1024, 2048] */
+    int E = e - 1 + 15;
+    if (r == 2048.0) { r = 1024.0; E += 1; }
+    if (E >= 31) return sign | 0x7c00;
+    return sign | (uint16_t)(E << 10) | (uint16_t)((int)r - 1024);
+}
+
+static double half_at(const uint8_t* p) {
+    return qo_half_to_double((uint16_t)(p[0] | (p[1] << 8)));
+}
+
+/* ------------------------------------------------------------------ k-quant blocks */
+
+int qo_block_bytes(int qtype) {
+    return qtype == QO_Q4_K ? 144 : qtype == QO_Q6_K ? 210 : -1;
+}
+
+/* Q4_K sub-block j (0..7) scale s_j and min m_j, both 6-bit, packed in 12 bytes:
+ * j < 4 : low 6 bits of byte j (scale) and of byte j+4 (min);
+ * j >= 4: low nibble / high nibble of byte j+4 give the 4 low bits of scale /
+ *         min, the top 2 bits of byte j-4 / byte j give their 2 high bits. */
+static void q4k_scale_min(const uint8_t* sc, int j, int* s, int* m) {
+    if (j < 4) {
+        *s = sc[j] & 63;
+        *m = sc[j + 4] & 63;
+    } else {
+        *s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+        *m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+    }
+}
+
+/* Element i (0..255) of a 144-byte Q4_K superblock:
+ * bytes 0-1 d (fp16), 2-3 dmin (fp16), 4-15 packed scales/mins, 16-143 nibbles.
+ * Element i lies in sub-block j = i/32 at position l = i%32; the nibbles form
+ * four 32-byte chunks, chunk c holding sub-block 2c in its low nibbles and
+ * sub-block 2c+1 in its high nibbles (byte l of the chunk -> position l).
+ * value = d * s_j * q - dmin * m_j. */
+double qo_q4k_element(const uint8_t* blk, int i) {
+    double d = half_at(blk), dmin = half_at(blk + 2);
+    const uint8_t* sc = blk + 4;
+    const uint8_t* qs = blk + 16;
+    int j = i / 32, l = i % 32;
+    int q = (qs[32 * (j / 2) + l] >> (4 * (j % 2))) & 15;
+    int s, m;
+    q4k_scale_min(sc, j, &s, &m);
+    return d * s * q - dmin * m;
+}
+
+/* Element i (0..255) of a 210-byte Q6_K superblock:
+ * bytes 0-127 ql (low 4 bits), 128-191 qh (high 2 bits), 192-207 int8 scales,
+ * 208-209 d (fp16).  i = 128n + 32g + l (half n, group g, position l):
+ * low 4 bits from ql[64n + l + 32*(g%2)] (low nibble for g<2, high for g>=2),
+ * high 2 bits = bits 2g..2g+1 of qh[32n + l], scale sc[8n + l/16 + 2g],
+ * value = d * sc * (q6 - 32). */
+double qo_q6k_element(const uint8_t* blk, int i) {
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    const int8_t* sc = (const int8_t*)(blk + 192);
+    double d = half_at(blk + 208);
+    int n = i / 128, g = (i % 128) / 32, l = i % 32;
+    int lo = (ql[64 * n + l + 32 * (g % 2)] >> (4 * (g / 2))) & 15;
+    int hi = (qh[32 * n + l] >> (2 * g)) & 3;
+    int q = (lo | (hi << 4)) - 32;
+    return d * (double)sc[8 * n + l / 16 + 2 * g] * (double)q;
+}
+
+int qo_dequant_block(int qtype, const uint8_t* blk, double* out) {
+    for (int i = 0; i < QO_QK; ++i) {
+        if (qtype == QO_Q4_K) out[i] = qo_q4k_element(blk, i);
+        else if (qtype == QO_Q6_K) out[i] = qo_q6k_element(blk, i);
+        else return -1;
+    }
+    return 0;
+}
+
+/* A matrix with `rows` outputs and `cols` inputs is stored row after row; a row
+ * is cols/256 consecutive superblocks ([P2] "File facts"). */
+int qo_dequant_matrix(int qtype, const uint8_t* data, long rows, long cols, double* out) {
+    int bb = qo_block_bytes(qtype);
+    if (bb < 0 || cols % QO_QK) return -1;
+    long nb = cols / QO_QK;
+    for (long r = 0; r < rows; ++r)
+        for (long b = 0; b < nb; ++b)
+            if (qo_dequant_block(qtype, data + (r * nb + b) * bb, out + r * cols + b * QO_QK)) return -1;
+    return 0;
+}
+
+/* Byte stride between experts of a 3-D expert tensor: expert e starts at
+ * base + e * rows * (cols/256) * block_bytes ([P2] "File facts"). */
+long qo_expert_stride(int qtype, long rows, long cols) {
+    int bb = qo_block_bytes(qtype);
+    if (bb < 0 || cols % QO_QK) return -1;
+    return rows * (cols / QO_QK) * bb;
+}
+
+/* ------------------------------------------------------------------ router */
+
+/* Router for one token ([P2] "Gaps ... G3": router GEMV, softmax, top-k, renorm):
+ * logit_e = sum_h Wr[e][h] x[h] (+ bias_e), accumulated in double and delivered
+ * as an F32 vector (the router output the pages move is 128 x f32);
+ * S = the k largest F32 logits, ties to the lower expert index, ordered by
+ * descending logit then ascending index;
+ * p = softmax(logits) in double; w_j = p_{S_j} / sum_{i in S} p_i (norm_topk)
+ * or p_{S_j}.  If `force` is given, S = force (weights still from p). */
+static void route_one(int H, int E, int K, int norm_topk, const double* x, const float* wr,
+                      const float* bias, const int32_t* force, float* logits, int32_t* ids,
+                      double* w, double* probs) {
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h) acc += (double)wr[(long)e * H + h] * x[h];
+        if (bias) acc += (double)bias[e];
+        logits[e] = (float)acc;
+    }
+    if (force) {
+        for (int j = 0; j < K; ++j) ids[j] = force[j];
+    } else {
+        char* taken = (char*)calloc((size_t)E, 1);
+        for (int j = 0; j < K; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || logits[e] > logits[best])) best = e;
+            taken[best] = 1;
+            ids[j] = best;
+        }
+        free(taken);
+    }
+    double mx = logits[0];
+    for (int e = 1; e < E; ++e) if (logits[e] > mx) mx = logits[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp((double)logits[e] - mx);
+    double ps = 0.0;
+    for (int j = 0; j < K; ++j) ps += exp((double)logits[ids[j]] - mx) / z;
+    for (int j = 0; j < K; ++j) {
+        double p = exp((double)logits[ids[j]] - mx) / z;
+        w[j] = norm_topk ? p / ps : p;
+    }
+    if (probs)
+        for (int e = 0; e < E; ++e) probs[e] = exp((double)logits[e] - mx) / z;
+}
+
+int qo_router(int T, int H, int E, int K, int norm_topk, const double* x, const float* wr,
+              const float* bias, const int32_t* force, float* logits, int32_t* ids, double* w,
+              double* probs) {
+    if (K < 1 || K > E) return -1;
+    for (int t = 0; t < T; ++t)
+        route_one(H, E, K, norm_topk, x + (long)t * H, wr, bias, force ? force + (long)t * K : NULL,
+                  logits + (long)t * E, ids + (long)t * K, w + (long)t * K,
+                  probs ? probs + (long)t * E : NULL);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ MoE FFN */
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* y = W x for a dense double matrix [rows][cols]. */
+static void matvec(const double* W, long rows, long cols, const double* x, double* y) {
+    for (long r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (long c = 0; c < cols; ++c) acc += W[r * cols + c] * x[c];
+        y[r] = acc;
+    }
+}
+
+/* MoE FFN of T tokens ([P2] "Gaps ... G3"): for each token t and slot j with
+ * expert e = ids[t][j]:
+ *   g = Wg_e x_t, u = Wu_e x_t           (Q4_K gate/up, [F][H], dequantised)
+ *   a = silu(g) * u                      (fused SwiGLU)
+ *   y_tj = Wd_e a                        (Q6_K or Q4_K down, [H][F])
+ *   out_t = res_t + sum_j w[t][j] y_tj   (weighted sum into the residual,
+ *                                         summed in slot order j = 0..K-1)
+ * Expert e of each 3-D tensor is read in place at base + e*stride.
+ * act (nullable) receives a [T][K][F]; ys (nullable) receives y [T][K][H]. */
+int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double* res,
+               const int32_t* ids, const double* w,
+               const uint8_t* gate, int gate_t, const uint8_t* up, int up_t,
+               const uint8_t* down, int down_t, double* out, double* act, double* ys) {
+    long sg = qo_expert_stride(gate_t, F, H), su = qo_expert_stride(up_t, F, H);
+    long sd = qo_expert_stride(down_t, H, F);
+    if (sg < 0 || su < 0 || sd < 0) return -1;
+    for (long p = 0; p < (long)T * K; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return -2;
+    double* Y = (double*)malloc(sizeof(double) * (size_t)T * K * H);
+    if (!Y) return -3;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e) {
+        int used = 0;
+        for (long p = 0; p < (long)T * K; ++p) used |= (ids[p] == e);
+        if (!used) continue;
+        double* Wg = (double*)malloc(sizeof(double) * (size_t)F * H);
+        double* Wu = (double*)malloc(sizeof(double) * (size_t)F * H);
+        double* Wd = (double*)malloc(sizeof(double) * (size_t)H * F);
+        double* g = (double*)malloc(sizeof(double) * (size_t)F);
+        double* u = (double*)malloc(sizeof(double) * (size_t)F);
+        double* a = (double*)malloc(sizeof(double) * (size_t)F);
+        if (!Wg || !Wu || !Wd || !g || !u || !a) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            qo_dequant_matrix(gate_t, gate + (long)e * sg, F, H, Wg);
+            qo_dequant_matrix(up_t, up + (long)e * su, F, H, Wu);
+            qo_dequant_matrix(down_t, down + (long)e * sd, H, F, Wd);
+            for (long p = 0; p < (long)T * K; ++p) {
+                if (ids[p] != e) continue;
+                long t = p / K;
+                matvec(Wg, F, H, x + t * H, g);
+                matvec(Wu, F, H, x + t * H, u);
+                for (long f = 0; f < F; ++f) a[f] = silu(g[f]) * u[f];
+                if (act) memcpy(act + p * F, a, sizeof(double) * (size_t)F);
+                matvec(Wd, H, F, a, Y + p * H);
+            }
+        }
+        free(Wg); free(Wu); free(Wd); free(g); free(u); free(a);
+    }
+    if (err) { free(Y); return -3; }
+    for (long t = 0; t < T; ++t)
+        for (long h = 0; h < H; ++h) {
+            double acc = res ? res[t * H + h] : x[t * H + h];
+            for (long j = 0; j < K; ++j) acc += w[t * K + j] * Y[(t * K + j) * H + h];
+            out[t * H + h] = acc;
+        }
+    if (ys) memcpy(ys, Y, sizeof(double) * (size_t)T * K * H);
+    free(Y);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ decoder layer pieces */
+
+/* RMSNorm: x / sqrt(mean(x^2) + eps) * w. */
+void qo_rmsnorm(long n, const double* x, const float* w, double eps, double* out) {
+    double ss = 0.0;
+    for (long i = 0; i < n; ++i) ss += x[i] * x[i];
+    double r = 1.0 / sqrt(ss / (double)n + eps);
+    for (long i = 0; i < n; ++i) out[i] = x[i] * r * (double)w[i];
+}
+
+/* NEOX rotary embedding of one head ([P5] closing comment): the rotated pairs
+ * are (i, i + hd/2) for i < hd/2, angle pos * base^(-2i/hd). */
+void qo_rope_neox(int hd, double* v, int pos, double base) {
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double th = (double)pos * pow(base, -2.0 * (double)i / (double)hd);
+        double c = cos(th), s = sin(th);
+        double a = v[i], b = v[i + half];
+        v[i] = a * c - b * s;
+        v[i + half] = b * c + a * s;
+    }
+}
+
+/* Single-query attention of one q head over cache positions 0..pos of its kv
+ * head: softmax(q . K_p / sqrt(hd)) . V_p.  The cache holds fp16. */
+void qo_attend(int hd, const double* q, const uint16_t* Kc, const uint16_t* Vc, int pos,
+               double* out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(pos + 1));
+    double scale = 1.0 / sqrt((double)hd), mx = -INFINITY;
+    for (int p = 0; p <= pos; ++p) {
+        double acc = 0.0;
+        for (int i = 0; i < hd; ++i) acc += q[i] * qo_half_to_double(Kc[(long)p * hd + i]);
+        s[p] = acc * scale;
+        if (s[p] > mx) mx = s[p];
+    }
+    double z = 0.0;
+    for (int p = 0; p <= pos; ++p) { s[p] = exp(s[p] - mx); z += s[p]; }
+    for (int i = 0; i < hd; ++i) out[i] = 0.0;
+    for (int p = 0; p <= pos; ++p)
+        for (int i = 0; i < hd; ++i) out[i] += (s[p] / z) * qo_half_to_double(Vc[(long)p * hd + i]);
+    free(s);
+}
+
+/* One qwen3moe decoder layer at decode time (batch 1), on hidden state h (in/out):
+ *  B1 x = RMSNorm(h) * attn_norm
+ *  B2 q = Wq x [nq*hd], k = Wk x [nkv*hd], v = Wv x [nkv*hd]   (no bias, [P1])
+ *  B3 per-head RMSNorm of q (q_norm) and k (k_norm), after bias, before RoPE ([P4])
+ *  B4 NEOX RoPE at position pos, base rope_base ([P5])
+ *  B5 k, v rounded to fp16 and written to cache slot pos
+ *  B6 GQA: q head hq reads kv head hq / (nq/nkv) over positions 0..pos ([P1])
+ *  B7 h += Wo attn
+ *  B8 x2 = RMSNorm(h) * ffn_norm
+ *  B9 h += MoE(x2) (router + experts, as qo_router / qo_moe_ffn)
+ * Caches are [nkv][ctx][hd] fp16; entries before pos are used as stored.
+ * q_out / att_out (nullable) receive q after norm+RoPE and the attention output. */
+int qo_decode_layer(int H, int E, int K, int F, int nq, int nkv, int hd, int ctx, double eps,
+                    double rope_base, int pos, double* h,
+                    const float* attn_norm, const float* q_norm, const float* k_norm,
+                    const float* ffn_norm, const uint8_t* wq, const uint8_t* wk,
+                    const uint8_t* wv, const uint8_t* wo, const float* router,
+                    const uint8_t* gate, const uint8_t* up, const uint8_t* down, int down_t,
+                    uint16_t* k_cache, uint16_t* v_cache, const int32_t* force,
+                    float* logits_out, int32_t* ids_out, double* w_out, double* q_out,
+                    double* att_out) {
+    if (pos < 0 || pos >= ctx || nq % nkv || hd % 2) return -1;
+    long qd = (long)nq * hd, kvd = (long)nkv * hd;
+    double* x = (double*)malloc(sizeof(double) * H);
+    double* q = (double*)malloc(sizeof(double) * qd);
+    double* k = (double*)malloc(sizeof(double) * kvd);
+    double* v = (double*)malloc(sizeof(double) * kvd);
+    double* att = (double*)malloc(sizeof(double) * qd);
+    double* Wbuf = (double*)malloc(sizeof(double) * (size_t)(qd > kvd ? qd : kvd) * (size_t)H);
+    double* o = (double*)malloc(sizeof(double) * H);
+    double* tmp = (double*)malloc(sizeof(double) * hd);
+    if (!x || !q || !k || !v || !att || !Wbuf || !o || !tmp) return -3;
+
+    qo_rmsnorm(H, h, attn_norm, eps, x);                              /* B1 */
+    qo_dequant_matrix(QO_Q4_K, wq, qd, H, Wbuf); matvec(Wbuf, qd, H, x, q);   /* B2 */
+    qo_dequant_matrix(QO_Q4_K, wk, kvd, H, Wbuf); matvec(Wbuf, kvd, H, x, k);
+    qo_dequant_matrix(QO_Q4_K, wv, kvd, H, Wbuf); matvec(Wbuf, kvd, H, x, v);
+    for (int hh = 0; hh < nq; ++hh) {                                 /* B3 + B4 */
+        qo_rmsnorm(hd, q + (long)hh * hd, q_norm, eps, tmp);
+        memcpy(q + (long)hh * hd, tmp, sizeof(double) * hd);
+        qo_rope_neox(hd, q + (long)hh * hd, pos, rope_base);
+    }
+    for (int hh = 0; hh < nkv; ++hh) {
+        qo_rmsnorm(hd, k + (long)hh * hd, k_norm, eps, tmp);
+        memcpy(k + (long)hh * hd, tmp, sizeof(double) * hd);
+        qo_rope_neox(hd, k + (long)hh * hd, pos, rope_base);
+    }
+    for (int hh = 0; hh < nkv; ++hh)                                  /* B5 */
+        for (int i = 0; i < hd; ++i) {
+            k_cache[((long)hh * ctx + pos) * hd + i] = qo_double_to_half(k[(long)hh * hd + i]);
+            v_cache[((long)hh * ctx + pos) * hd + i] = qo_double_to_half(v[(long)hh * hd + i]);
+        }
+    int group = nq / nkv;
+#pragma omp parallel for schedule(static)
+    for (int hh = 0; hh < nq; ++hh) {                                 /* B6 */
+        int kvh = hh / group;
+        qo_attend(hd, q + (long)hh * hd, k_cache + (long)kvh * ctx * hd,
+                  v_cache + (long)kvh * ctx * hd, pos, att + (long)hh * hd);
+    }
+    if (q_out) memcpy(q_out, q, sizeof(double) * qd);
+    if (att_out) memcpy(att_out, att, sizeof(double) * qd);
+    qo_dequant_matrix(QO_Q4_K, wo, H, qd, Wbuf); matvec(Wbuf, H, qd, att, o);  /* B7 */
+    for (int i = 0; i < H; ++i) h[i] += o[i];
+    qo_rmsnorm(H, h, ffn_norm, eps, x);                               /* B8 */
+    double* w = (double*)malloc(sizeof(double) * K);                  /* B9 */
+    int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * K);
+    float* lg = (float*)malloc(sizeof(float) * E);
+    qo_router(1, H, E, K, 1, x, router, NULL, force, lg, ids, w, NULL);
+    double* out = (double*)malloc(sizeof(double) * H);
+    int rc = qo_moe_ffn(1, H, F, E, K, x, h, ids, w, gate, QO_Q4_K, up, QO_Q4_K, down, down_t,
+                        out, NULL, NULL);
+    if (rc == 0) memcpy(h, out, sizeof(double) * H);
+    if (logits_out) memcpy(logits_out, lg, sizeof(float) * E);
+    if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * K);
+    if (w_out) memcpy(w_out, w, sizeof(double) * K);
+    free(x); free(q); free(k); free(v); free(att); free(Wbuf); free(o); free(tmp);
+    free(w); free(ids); free(lg); free(out);
+    return rc;
+}

@@ -1,0 +1,172 @@
+"""Seeded synthetic inputs for the qwen3moe MoE FFN (no method arithmetic here).
+
+This module only draws random numbers and lays them out in the byte formats the
+method consumes; it computes nothing the method computes.  Both the CPU oracle
+(``oracle/``) and the CUDA path take their inputs from here, so that parity is
+checked on identical bytes.
+
+Shapes and value distributions follow the Qwen3-30B-A3B file facts given in the
+aprender issue "qwen3moe ... has NO working CUDA path" (section "File facts"):
+hidden 2048, 128 experts, top-8, expert FFN width 768, router ``ffn_gate_inp``
+F32 [128 x 2048], gate/up experts Q4_K, down experts Q6_K or Q4_K, 32 q heads /
+4 kv heads, head_dim 128, rope base 1e7, 48 layers.
+
+Recipe (every array is drawn with numpy ``Generator(PCG64(seed))``):
+
+* router weights ~ N(0, 0.02) as float32 [E][H]
+* optional per-expert router bias ~ N(0, 1.5) as float32 [E] (prefill workload)
+* every k-quant tensor: uniform random bytes for the whole superblock, then the
+  fp16 super-scales are overwritten with fp16(|N(0,1)| * 1e-3)
+  (Q4_K: d and dmin; Q6_K: d).  Q6_K's int8 sub-block scales stay uniform bytes.
+* activations ~ N(0, 1) as float32.
+* decode-step extras: norm weights 1 + 0.1 N(0,1); KV cache entries fp16(N(0,1)).
+
+Expert tensors are drawn expert by expert from a stream keyed by
+(seed, tensor tag, expert), so that one expert's bytes can be regenerated alone
+(the oracle of a 48-layer step regenerates only the experts it routes to).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QK_K = 256
+BLOCK_BYTES = {"Q4_K": 144, "Q6_K": 210}
+QTYPE_CODE = {"Q4_K": 1, "Q6_K": 2}
+
+# tensor tags used to key the per-expert streams
+_TAG = {"gate": 1, "up": 2, "down": 3, "wq": 11, "wk": 12, "wv": 13, "wo": 14}
+
+
+def row_bytes(qtype: str, cols: int) -> int:
+    """Bytes of one stored row: cols/256 consecutive superblocks."""
+    assert cols % QK_K == 0
+    return (cols // QK_K) * BLOCK_BYTES[qtype]
+
+
+def matrix_bytes(qtype: str, rows: int, cols: int) -> int:
+    return rows * row_bytes(qtype, cols)
+
+
+def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int) -> np.ndarray:
+    bb = BLOCK_BYTES[qtype]
+    raw = np.frombuffer(rng.bytes(nblocks * bb), dtype=np.uint8).reshape(nblocks, bb).copy()
+    d = (np.abs(rng.standard_normal(nblocks)) * 1e-3).astype(np.float16)
+    if qtype == "Q4_K":
+        dmin = (np.abs(rng.standard_normal(nblocks)) * 1e-3).astype(np.float16)
+        raw[:, 0:2] = d.view(np.uint8).reshape(nblocks, 2)
+        raw[:, 2:4] = dmin.view(np.uint8).reshape(nblocks, 2)
+    else:
+        raw[:, 208:210] = d.view(np.uint8).reshape(nblocks, 2)
+    return raw
+
+
+def kquant_matrix(seed: int, tag: int, index: int, qtype: str, rows: int, cols: int) -> np.ndarray:
+    """One quantised matrix [rows][cols] as uint8 [rows][row_bytes]."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
+    nblk = rows * (cols // QK_K)
+    return _fill_kquant(rng, qtype, nblk).reshape(rows, row_bytes(qtype, cols))
+
+
+def expert_slice(seed: int, which: str, e: int, qtype: str, rows: int, cols: int) -> np.ndarray:
+    return kquant_matrix(seed, _TAG[which], e, qtype, rows, cols)
+
+
+def expert_tensor(seed: int, which: str, n_experts: int, qtype: str, rows: int, cols: int) -> np.ndarray:
+    """3-D expert tensor: expert e's slice starts at e * rows * row_bytes (contiguous)."""
+    out = np.empty((n_experts, rows, row_bytes(qtype, cols)), dtype=np.uint8)
+    for e in range(n_experts):
+        out[e] = expert_slice(seed, which, e, qtype, rows, cols)
+    return out
+
+
+# --------------------------------------------------------------------------- MoE FFN workloads
+
+MOE_CONFIGS = {
+    1: dict(name="tiny", H=256, E=8, K=2, F=256, T=4, gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K",
+            seed=0, bias_std=None),
+    2: dict(name="qwen3moe-30b-a3b layer decode T=1", H=2048, E=128, K=8, F=768, T=1,
+            gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K", seed=1, bias_std=None),
+    3: dict(name="qwen3moe-30b-a3b layer decode T=8, Q4_K down", H=2048, E=128, K=8, F=768, T=8,
+            gate_t="Q4_K", up_t="Q4_K", down_t="Q4_K", seed=2, bias_std=None),
+    4: dict(name="qwen3moe-30b-a3b layer prefill T=512, biased router", H=2048, E=128, K=8, F=768,
+            T=512, gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K", seed=3, bias_std=1.5),
+}
+
+
+def moe_inputs(cfg: dict, T: int | None = None) -> dict:
+    """All inputs of one MoE-FFN layer call, drawn in a fixed order.
+
+    Order: router, bias (if any), input activations from the main stream; expert
+    tensors from their own per-expert streams.
+    """
+    H, E, F = cfg["H"], cfg["E"], cfg["F"]
+    T = cfg["T"] if T is None else T
+    seed = cfg["seed"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    router = rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32)
+    bias = None
+    if cfg.get("bias_std"):
+        bias = rng.normal(0.0, cfg["bias_std"], size=E).astype(np.float32)
+    x = rng.normal(0.0, 1.0, size=(T, H)).astype(np.float32)
+    gate = expert_tensor(seed, "gate", E, cfg["gate_t"], F, H)
+    up = expert_tensor(seed, "up", E, cfg["up_t"], F, H)
+    down = expert_tensor(seed, "down", E, cfg["down_t"], H, F)
+    return dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=bias, x=x,
+                gate=gate, up=up, down=down,
+                gate_t=cfg["gate_t"], up_t=cfg["up_t"], down_t=cfg["down_t"])
+
+
+# --------------------------------------------------------------------------- 48-layer decode step
+
+STEP_DEFAULT = dict(n_layers=48, H=2048, E=128, K=8, F=768, n_heads=32, n_kv=4, head_dim=128,
+                    ctx=4096, rope_base=1.0e7, eps=1e-6, seed0=100, input_seed=5000)
+
+
+def step_down_qtype(layer: int) -> str:
+    """Down-projection quant type of layer i: Q6_K on even layers, Q4_K on odd ones."""
+    return "Q6_K" if layer % 2 == 0 else "Q4_K"
+
+
+def step_layer_small(geo: dict, layer: int) -> dict:
+    """Everything of layer i except its expert tensors (norms, attention, router, KV)."""
+    H, E = geo["H"], geo["E"]
+    hd, nq, nkv, ctx = geo["head_dim"], geo["n_heads"], geo["n_kv"], geo["ctx"]
+    seed = geo["seed0"] + layer
+    rng = np.random.Generator(np.random.PCG64(seed))
+    attn_norm = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    q_norm = (1.0 + 0.1 * rng.standard_normal(hd)).astype(np.float32)
+    k_norm = (1.0 + 0.1 * rng.standard_normal(hd)).astype(np.float32)
+    ffn_norm = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    router = rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32)
+    k_cache = rng.standard_normal((nkv, ctx, hd)).astype(np.float16)
+    v_cache = rng.standard_normal((nkv, ctx, hd)).astype(np.float16)
+    wq = kquant_matrix(seed, _TAG["wq"], 0, "Q4_K", nq * hd, H)
+    wk = kquant_matrix(seed, _TAG["wk"], 0, "Q4_K", nkv * hd, H)
+    wv = kquant_matrix(seed, _TAG["wv"], 0, "Q4_K", nkv * hd, H)
+    wo = kquant_matrix(seed, _TAG["wo"], 0, "Q4_K", H, nq * hd)
+    return dict(attn_norm=attn_norm, q_norm=q_norm, k_norm=k_norm, ffn_norm=ffn_norm,
+                router=router, k_cache=k_cache, v_cache=v_cache, wq=wq, wk=wk, wv=wv, wo=wo,
+                down_t=step_down_qtype(layer))
+
+
+def step_layer_experts(geo: dict, layer: int) -> dict:
+    H, E, F = geo["H"], geo["E"], geo["F"]
+    seed = geo["seed0"] + layer
+    dt = step_down_qtype(layer)
+    return dict(gate=expert_tensor(seed, "gate", E, "Q4_K", F, H),
+                up=expert_tensor(seed, "up", E, "Q4_K", F, H),
+                down=expert_tensor(seed, "down", E, dt, H, F))
+
+
+def step_layer_expert(geo: dict, layer: int, which: str, e: int) -> np.ndarray:
+    """Regenerate one expert slice of one layer (identical to the full tensor's slice)."""
+    H, F = geo["H"], geo["F"]
+    seed = geo["seed0"] + layer
+    if which == "down":
+        return expert_slice(seed, "down", e, step_down_qtype(layer), H, F)
+    return expert_slice(seed, which, e, "Q4_K", F, H)
+
+
+def step_input(geo: dict) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(geo["input_seed"]))
+    return rng.standard_normal(geo["H"]).astype(np.float32)

@@ -1,0 +1,186 @@
+/*
+ * qmoe.h -- C ABI of the GB300 (sm_103a) qwen3moe Mixture-of-Experts FFN over
+ * GGUF k-quant expert weights.
+ *
+ * The operation (aprender issue "qwen3moe (Qwen3-30B-A3B, Qwen3-Coder-30B-A3B,
+ * Q4_K_M) has NO working CUDA path", sections "File facts" and "Gaps ... G3"):
+ *
+ *   logits = Wr x (+ bias)                        F32 router GEMV [E x H]
+ *   S, w   = top-k(softmax(logits)), renormalised  ("softmax, top-8, renorm")
+ *   for each selected expert e (addressed in place as base + e * stride):
+ *     g = Wg_e x, u = Wu_e x                      Q4_K gate / up dequant-GEMV
+ *     a = silu(g) * u                             fused SwiGLU
+ *     y_e = Wd_e a                                Q6_K or Q4_K down dequant-GEMV
+ *   out = residual + sum_j w_j y_{S_j}            weighted sum into the residual
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is a DEVICE pointer that the caller allocated and owns
+ *    (except qmoe_forward_host, whose activations are host pointers).  The
+ *    library never copies, repacks or frees caller memory.
+ *  - Quantised tensors are raw GGUF superblocks: Q4_K = 144 B per 256 weights
+ *    (fp16 d, fp16 dmin, 12 B packed 6-bit scales/mins, 128 B nibbles); Q6_K =
+ *    210 B per 256 weights (128 B ql, 64 B qh, 16 int8 scales, fp16 d).  A
+ *    matrix with R outputs and C inputs is R rows of C/256 consecutive
+ *    superblocks; expert e of a 3-D expert tensor starts at
+ *    base + e * R * (C/256) * block_bytes.
+ *  - F32 activations are row-major [n_tokens][hidden].
+ *  - Work is enqueued asynchronously on the context's stream; no call below
+ *    synchronises the host, allocates memory or copies weights, except
+ *    qmoe_create / qmoe_destroy (allocate / free the workspace),
+ *    qmoe_forward_host (copies activations and synchronises) and
+ *    qmoe_get_status (synchronises).
+ *  - Errors are returned as qmoe_status; no exception crosses the ABI.
+ *    Argument errors are detected on the host before anything is enqueued.
+ *    qmoe_last_error() gives a one-line description of the last failure.
+ *  - A context is not thread-safe: one host thread at a time, and calls that
+ *    share a context must be ordered on its stream (they share the workspace).
+ */
+#ifndef QMOE_H
+#define QMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QMOE_OK = 0,
+    QMOE_ERR_INVALID_ARG = 1,       /* null pointer, bad size or count */
+    QMOE_ERR_MISALIGNED = 2,        /* a base pointer is not 16-byte aligned */
+    QMOE_ERR_UNSUPPORTED_QTYPE = 3, /* qtype not allowed for that tensor */
+    QMOE_ERR_SHAPE = 4,             /* hidden/ffn not a multiple of 256, n_tokens > max */
+    QMOE_ERR_NO_MEMORY = 5,         /* workspace does not fit; message names the bytes */
+    QMOE_ERR_CUDA = 6,              /* a CUDA runtime call failed; message names it */
+    QMOE_ERR_TIMEOUT = 7,           /* a bounded device-side wait gave up */
+    QMOE_ERR_DEVICE_CHECK = 8       /* a device-side index check failed */
+} qmoe_status;
+
+typedef enum { QMOE_Q4_K = 1, QMOE_Q6_K = 2 } qmoe_qtype;
+
+typedef struct qmoe_ctx qmoe_ctx;
+
+/* Geometry fixed at create time.  The MoE part (hidden, n_experts, top_k, ffn)
+ * is required; the attention part is needed only by qmoe_decode_step and may
+ * be all zero otherwise (Qwen3-30B-A3B: 32 q heads, 4 kv heads, head_dim 128,
+ * rope base 1e7, RMSNorm eps 1e-6; head_dim is NOT hidden / n_heads -- aprender
+ * issue "Qwen3 GPU inference produces garbage output", "Fix Applied"). */
+typedef struct {
+    int hidden;          /* H, multiple of 256 */
+    int n_experts;       /* E, 1..1024 */
+    int top_k;           /* k, 1..min(E, 16) */
+    int ffn;             /* F, expert FFN width, multiple of 256 */
+    int norm_topk_prob;  /* 1: renormalise the k selected probabilities (qwen3moe) */
+    int max_tokens;      /* largest n_tokens any call will pass (workspace size) */
+    int n_heads;         /* attention q heads (decode step only, else 0) */
+    int n_kv_heads;      /* attention kv heads, divides n_heads */
+    int head_dim;        /* 128 for qwen3moe (even, <= 256) */
+    int max_ctx;         /* KV-cache positions per layer */
+    float rope_base;     /* NEOX RoPE base */
+    float rms_eps;       /* RMSNorm epsilon (all four norms) */
+    void* stream;        /* cudaStream_t the work is enqueued on (NULL = legacy default) */
+} qmoe_config;
+
+/* Create a context on the current CUDA device and allocate its workspace
+ * (router logits, expert ids / weights, per-expert pair lists, intermediate
+ * activations, all sized by max_tokens).  Returns QMOE_ERR_NO_MEMORY with a
+ * message giving the bytes needed and free, instead of failing later.
+ * On success *out owns the workspace until qmoe_destroy. */
+qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out);
+
+/* Free the workspace (synchronises the context's stream first).  NULL is a no-op. */
+void qmoe_destroy(qmoe_ctx* ctx);
+
+/* Change the stream later calls enqueue on. */
+qmoe_status qmoe_set_stream(qmoe_ctx* ctx, void* stream);
+
+/* hidden_out = hidden_in + MoE(hidden_in) for n_tokens tokens.
+ *  hidden_in, hidden_out : F32 [n_tokens][H] (device).  They may alias only
+ *                          when n_tokens <= 8 (decode); otherwise -> INVALID_ARG.
+ *  router_w              : F32 [E][H] (device), the ffn_gate_inp tensor.
+ *  gate_exps, up_exps    : [E][F rows][H/256 superblocks], Q4_K (or Q6_K).
+ *  down_exps             : [E][H rows][F/256 superblocks], Q6_K or Q4_K.
+ *  All base pointers 16-byte aligned.  n_tokens in 1..max_tokens.
+ * Expert ids are selected on the F32 logits, ties to the lower index. */
+qmoe_status qmoe_forward(qmoe_ctx* ctx, const float* hidden_in, const float* router_w,
+                         const void* gate_exps, const void* up_exps, const void* down_exps,
+                         qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
+                         int n_tokens, float* hidden_out);
+
+/* General form:  out = residual + MoE(ffn_in), router logits += router_bias.
+ *  residual     : F32 [n_tokens][H] or NULL (then residual = ffn_in).
+ *  router_bias  : F32 [E] or NULL.
+ *  ids_out      : int32 [n_tokens][k] or NULL -- selected experts, ordered by
+ *                 descending logit (ties: lower index first).
+ *  weights_out  : F32 [n_tokens][k] or NULL -- their routing weights.
+ * out may alias residual (not ffn_in) when n_tokens <= 8. */
+qmoe_status qmoe_forward_ex(qmoe_ctx* ctx, const float* ffn_in, const float* residual,
+                            const float* router_bias, const float* router_w,
+                            const void* gate_exps, const void* up_exps, const void* down_exps,
+                            qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
+                            int n_tokens, float* out, int32_t* ids_out, float* weights_out);
+
+/* Same as qmoe_forward, but hidden_in / hidden_out are HOST pointers (pinned
+ * memory gives asynchronous copies).  Copies the activations to the device
+ * workspace, runs the layer, copies the result back and synchronises the
+ * stream before returning.  Weights stay device pointers. */
+qmoe_status qmoe_forward_host(qmoe_ctx* ctx, const float* hidden_in_host, const float* router_w,
+                              const void* gate_exps, const void* up_exps, const void* down_exps,
+                              qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
+                              int n_tokens, float* hidden_out_host);
+
+/* Weights of one qwen3moe decoder layer (all device pointers). */
+typedef struct {
+    const float* attn_norm;  /* [H] input RMSNorm weight */
+    const void* wq;          /* [n_heads*head_dim rows][H], Q4_K */
+    const void* wk;          /* [n_kv*head_dim rows][H], Q4_K */
+    const void* wv;          /* [n_kv*head_dim rows][H], Q4_K */
+    const void* wo;          /* [H rows][n_heads*head_dim], Q4_K */
+    const float* q_norm;     /* [head_dim] per-head Q RMSNorm weight */
+    const float* k_norm;     /* [head_dim] per-head K RMSNorm weight */
+    const float* ffn_norm;   /* [H] post-attention RMSNorm weight */
+    const float* router_w;   /* [E][H] F32 */
+    const void* gate_exps;   /* MoE experts as in qmoe_forward */
+    const void* up_exps;
+    const void* down_exps;
+    qmoe_qtype down_t;       /* Q6_K or Q4_K (per layer) */
+    void* k_cache;           /* fp16 [n_kv][max_ctx][head_dim]; slot pos is written */
+    void* v_cache;           /* fp16 [n_kv][max_ctx][head_dim]; slot pos is written */
+} qmoe_layer_weights;
+
+/* One batch-1 decode step through n_layers qwen3moe decoder layers, in place on
+ * hidden (F32 [H], device).  Per layer: x = RMSNorm(h)*attn_norm; q,k,v = Wq/Wk/Wv x;
+ * per-head RMSNorm of q and k (q_norm, k_norm), then NEOX RoPE at position pos
+ * (pairs (i, i + head_dim/2)); k, v rounded to fp16 into cache slot pos; GQA
+ * attention of q head h over kv head h / (n_heads/n_kv_heads), positions
+ * 0..pos, scale 1/sqrt(head_dim); h += Wo attn; h += MoE(RMSNorm(h)*ffn_norm).
+ * Sources: aprender issue "Qwen3 GPU inference produces garbage output" (Fix
+ * Applied), aprender PR "apply per-head Q/K RMSNorm in forward_qwen3_moe" (The
+ * fix), SharpInference issue "Forward-pass divergence on Qwen3-Coder 30B-A3B"
+ * (NEOX RoPE).  ids_out (nullable): int32 [n_layers][k] selected experts.
+ * Requires the attention geometry in the config; 0 <= pos < max_ctx. */
+qmoe_status qmoe_decode_step(qmoe_ctx* ctx, const qmoe_layer_weights* layers, int n_layers,
+                             int pos, float* hidden, int32_t* ids_out);
+
+/* Synchronise the stream and read the device status word (bounded-wait
+ * timeouts, device index checks).  A non-OK status is sticky until read:
+ * reading it clears it. */
+qmoe_status qmoe_get_status(qmoe_ctx* ctx);
+
+/* One-line description of the last error on this context ("" if none).  The
+ * string is owned by the context and valid until the next call on it. */
+const char* qmoe_last_error(qmoe_ctx* ctx);
+
+/* Bytes of workspace a context with this config allocates (0 on bad config). */
+size_t qmoe_workspace_bytes(const qmoe_config* cfg);
+
+/* Byte stride between consecutive experts of a 3-D expert tensor whose
+ * matrices have `rows` outputs and `cols` inputs (0 on bad arguments). */
+size_t qmoe_expert_stride(qmoe_qtype qtype, int rows, int cols);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMOE_H */

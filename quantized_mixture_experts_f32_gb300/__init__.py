@@ -1,0 +1,168 @@
+"""GB300 (sm_103a) qwen3moe MoE FFN over GGUF k-quant experts -- Python binding.
+
+A thin ctypes layer over the C ABI in ``include/qmoe.h`` (library
+``_build/libqmoe.so``, built by ``build.py``).  It only marshals arguments:
+every step of the MoE FFN runs in the library's CUDA kernels.  Tensors are
+passed as raw device pointers; PyTorch is used by callers for device memory
+and streams only.
+
+Importing this package loads the library and fails loudly if it has not been
+built: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libqmoe.so")
+
+QMOE_OK = 0
+STATUS_NAMES = {0: "QMOE_OK", 1: "QMOE_ERR_INVALID_ARG", 2: "QMOE_ERR_MISALIGNED",
+                3: "QMOE_ERR_UNSUPPORTED_QTYPE", 4: "QMOE_ERR_SHAPE", 5: "QMOE_ERR_NO_MEMORY",
+                6: "QMOE_ERR_CUDA", 7: "QMOE_ERR_TIMEOUT", 8: "QMOE_ERR_DEVICE_CHECK"}
+QMOE_Q4_K, QMOE_Q6_K = 1, 2
+QTYPE = {"Q4_K": QMOE_Q4_K, "Q6_K": QMOE_Q6_K}
+
+EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
+            "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
+            "qmoe_workspace_bytes", "qmoe_expert_stride"]
+
+
+class qmoe_config(C.Structure):
+    _fields_ = [("hidden", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
+                ("ffn", C.c_int), ("norm_topk_prob", C.c_int), ("max_tokens", C.c_int),
+                ("n_heads", C.c_int), ("n_kv_heads", C.c_int), ("head_dim", C.c_int),
+                ("max_ctx", C.c_int), ("rope_base", C.c_float), ("rms_eps", C.c_float),
+                ("stream", C.c_void_p)]
+
+
+class qmoe_layer_weights(C.Structure):
+    _fields_ = [("attn_norm", C.c_void_p), ("wq", C.c_void_p), ("wk", C.c_void_p),
+                ("wv", C.c_void_p), ("wo", C.c_void_p), ("q_norm", C.c_void_p),
+                ("k_norm", C.c_void_p), ("ffn_norm", C.c_void_p), ("router_w", C.c_void_p),
+                ("gate_exps", C.c_void_p), ("up_exps", C.c_void_p), ("down_exps", C.c_void_p),
+                ("down_t", C.c_int), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p)]
+
+
+class QmoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libqmoe is not built ({LIB_PATH} missing); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` -- there is no CPU fallback")
+    L = C.CDLL(LIB_PATH)
+    vp, i, ip, fp = C.c_void_p, C.c_int, C.c_void_p, C.c_void_p
+    L.qmoe_create.argtypes = [C.POINTER(qmoe_config), C.POINTER(C.c_void_p)]
+    L.qmoe_create.restype = i
+    L.qmoe_destroy.argtypes = [vp]
+    L.qmoe_destroy.restype = None
+    L.qmoe_set_stream.argtypes = [vp, vp]
+    L.qmoe_set_stream.restype = i
+    L.qmoe_forward.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp]
+    L.qmoe_forward.restype = i
+    L.qmoe_forward_ex.argtypes = [vp, fp, fp, fp, fp, vp, vp, vp, i, i, i, i, fp, ip, fp]
+    L.qmoe_forward_ex.restype = i
+    L.qmoe_forward_host.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp]
+    L.qmoe_forward_host.restype = i
+    L.qmoe_decode_step.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, fp, ip]
+    L.qmoe_decode_step.restype = i
+    L.qmoe_get_status.argtypes = [vp]
+    L.qmoe_get_status.restype = i
+    L.qmoe_last_error.argtypes = [vp]
+    L.qmoe_last_error.restype = C.c_char_p
+    L.qmoe_workspace_bytes.argtypes = [C.POINTER(qmoe_config)]
+    L.qmoe_workspace_bytes.restype = C.c_size_t
+    L.qmoe_expert_stride.argtypes = [i, i, i]
+    L.qmoe_expert_stride.restype = C.c_size_t
+    return L
+
+
+lib = _load()
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor-like object, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _check(ctx, status):
+    if status != QMOE_OK:
+        msg = lib.qmoe_last_error(ctx).decode() if ctx else ""
+        raise QmoeError(status, msg)
+
+
+# ---------------------------------------------------------------------------- C names
+
+def qmoe_create(cfg: qmoe_config):
+    h = C.c_void_p()
+    st = lib.qmoe_create(C.byref(cfg), C.byref(h))
+    if st != QMOE_OK:
+        raise QmoeError(st, "qmoe_create failed (details on stderr)")
+    return h
+
+
+def qmoe_destroy(ctx):
+    lib.qmoe_destroy(ctx)
+
+
+def qmoe_set_stream(ctx, stream: int):
+    _check(ctx, lib.qmoe_set_stream(ctx, stream))
+
+
+def qmoe_forward(ctx, hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t, up_t, down_t,
+                 n_tokens, hidden_out):
+    _check(ctx, lib.qmoe_forward(ctx, _ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
+                                 _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t, n_tokens,
+                                 _ptr(hidden_out)))
+
+
+def qmoe_forward_ex(ctx, ffn_in, residual, router_bias, router_w, gate_exps, up_exps, down_exps,
+                    gate_t, up_t, down_t, n_tokens, out, ids_out=None, weights_out=None):
+    _check(ctx, lib.qmoe_forward_ex(ctx, _ptr(ffn_in), _ptr(residual), _ptr(router_bias),
+                                    _ptr(router_w), _ptr(gate_exps), _ptr(up_exps),
+                                    _ptr(down_exps), gate_t, up_t, down_t, n_tokens, _ptr(out),
+                                    _ptr(ids_out), _ptr(weights_out)))
+
+
+def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,
+                      down_t, n_tokens, hidden_out_host):
+    _check(ctx, lib.qmoe_forward_host(ctx, _ptr(hidden_in_host), _ptr(router_w), _ptr(gate_exps),
+                                      _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t,
+                                      n_tokens, _ptr(hidden_out_host)))
+
+
+def qmoe_decode_step(ctx, layers, n_layers, pos, hidden, ids_out=None):
+    _check(ctx, lib.qmoe_decode_step(ctx, layers, n_layers, pos, _ptr(hidden), _ptr(ids_out)))
+
+
+def qmoe_get_status(ctx) -> int:
+    return lib.qmoe_get_status(ctx)
+
+
+def qmoe_last_error(ctx) -> str:
+    return lib.qmoe_last_error(ctx).decode()
+
+
+def qmoe_workspace_bytes(cfg: qmoe_config) -> int:
+    return lib.qmoe_workspace_bytes(C.byref(cfg))
+
+
+def qmoe_expert_stride(qtype: int, rows: int, cols: int) -> int:
+    return lib.qmoe_expert_stride(qtype, rows, cols)
+
+
+def make_config(hidden, n_experts, top_k, ffn, max_tokens, norm_topk_prob=1, stream=0,
+                n_heads=0, n_kv_heads=0, head_dim=0, max_ctx=0, rope_base=0.0,
+                rms_eps=0.0) -> qmoe_config:
+    return qmoe_config(hidden, n_experts, top_k, ffn, norm_topk_prob, max_tokens, n_heads,
+                       n_kv_heads, head_dim, max_ctx, rope_base, rms_eps, stream or None)

@@ -1,0 +1,326 @@
+// qmoe_api.cu -- the C ABI (include/qmoe.h): argument checks, workspace, and the
+// launch sequence of one MoE-FFN layer call on the context's stream.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/qmoe.h"
+#include "qmoe_internal.h"
+
+struct qmoe_ctx {
+    qmoe_config cfg;
+    cudaStream_t stream;
+    int device;
+    char err[512];
+    void* ws;
+    size_t ws_bytes;
+    qmoe::Route route;
+    float* act;       // [P][F]
+    float* y;         // [P][H]
+    float* hin;       // [T][H] staging for qmoe_forward_host
+    float* hout;      // [T][H]
+    int* status;      // device status word
+    // decode-step scratch
+    float* xs;        // [H] normed hidden
+    float* q;         // [nq*hd]
+    float* kv;        // [2*nkv*hd]
+    float* att;       // [nq*hd]
+    float* attn_part; // split-K partials
+    int attn_splits;
+};
+
+namespace {
+
+constexpr int DECODE_ALIAS_MAX = 8;
+
+qmoe_status fail(qmoe_ctx* c, qmoe_status s, const char* fmt, ...) {
+    if (c) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(c->err, sizeof(c->err), fmt, ap);
+        va_end(ap);
+    }
+    return s;
+}
+
+qmoe_status cuda_fail(qmoe_ctx* c, cudaError_t e, const char* what) {
+    return fail(c, QMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
+
+struct Layout {
+    size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
+        status, xs, q, kv, att, attn_part, total;
+    int attn_splits;
+};
+
+bool config_ok(const qmoe_config* c, char* why, size_t n) {
+    if (!c) { snprintf(why, n, "config is NULL"); return false; }
+    if (c->hidden <= 0 || c->hidden % 256) { snprintf(why, n, "hidden=%d is not a positive multiple of 256", c->hidden); return false; }
+    if (c->ffn <= 0 || c->ffn % 256) { snprintf(why, n, "ffn=%d is not a positive multiple of 256", c->ffn); return false; }
+    if (c->n_experts < 1 || c->n_experts > 1024) { snprintf(why, n, "n_experts=%d outside 1..1024", c->n_experts); return false; }
+    if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) { snprintf(why, n, "top_k=%d outside 1..min(n_experts,16)", c->top_k); return false; }
+    if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) { snprintf(why, n, "max_tokens=%d outside 1..2^20", c->max_tokens); return false; }
+    const bool attn = c->n_heads || c->n_kv_heads || c->head_dim || c->max_ctx;
+    if (attn) {
+        if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) { snprintf(why, n, "n_heads=%d must be a positive multiple of n_kv_heads=%d", c->n_heads, c->n_kv_heads); return false; }
+        if (c->head_dim < 2 || c->head_dim > 256 || c->head_dim % 32) { snprintf(why, n, "head_dim=%d must be a multiple of 32 in 32..256", c->head_dim); return false; }
+        if ((c->n_heads * c->head_dim) % 256) { snprintf(why, n, "n_heads*head_dim=%d is not a multiple of 256", c->n_heads * c->head_dim); return false; }
+        if ((c->n_kv_heads * c->head_dim) % 256 && c->n_kv_heads * c->head_dim % 32) { snprintf(why, n, "bad kv dim"); return false; }
+        if (c->max_ctx < 1) { snprintf(why, n, "max_ctx=%d must be >= 1", c->max_ctx); return false; }
+        if (!(c->rope_base > 0.f) || !(c->rms_eps > 0.f)) { snprintf(why, n, "rope_base and rms_eps must be positive"); return false; }
+    }
+    return true;
+}
+
+Layout layout(const qmoe_config* c) {
+    Layout L{};
+    const size_t T = c->max_tokens, E = c->n_experts, K = c->top_k, F = c->ffn, H = c->hidden;
+    const size_t P = T * K;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    L.logits = take(sizeof(float) * T * E);
+    L.ids = take(sizeof(int32_t) * P);
+    L.wts = take(sizeof(float) * P);
+    L.n_used = take(sizeof(int32_t) * 4);
+    L.used_expert = take(sizeof(int32_t) * E);
+    L.used_first = take(sizeof(int32_t) * (E + 1));
+    L.pair_list = take(sizeof(int32_t) * P);
+    L.act = take(sizeof(float) * P * F);
+    L.y = take(sizeof(float) * P * H);
+    L.hin = take(sizeof(float) * T * H);
+    L.hout = take(sizeof(float) * T * H);
+    L.status = take(sizeof(int) * 16);
+    const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
+    L.attn_splits = c->max_ctx > 0 ? (c->max_ctx + 255) / 256 : 0;
+    L.xs = take(sizeof(float) * H);
+    L.q = take(sizeof(float) * (qd ? qd : 1));
+    L.kv = take(sizeof(float) * (2 * kvd + 1));
+    L.att = take(sizeof(float) * (qd ? qd : 1));
+    L.attn_part = take(sizeof(float) * (size_t)c->n_heads * L.attn_splits * (c->head_dim + 2) + 4);
+    L.total = off;
+    return L;
+}
+
+qmoe_status check_forward(qmoe_ctx* c, const float* in, const float* router_w, const void* g,
+                          const void* u, const void* d, int gt, int ut, int dt, int T,
+                          const float* out) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    if (!in || !router_w || !g || !u || !d || !out)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null tensor pointer");
+    if (T < 1 || T > c->cfg.max_tokens)
+        return fail(c, QMOE_ERR_SHAPE, "n_tokens=%d outside 1..max_tokens=%d", T, c->cfg.max_tokens);
+    if (!valid_qtype(gt) || !valid_qtype(ut) || !valid_qtype(dt))
+        return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "qtypes gate=%d up=%d down=%d (allowed: 1=Q4_K, 2=Q6_K)", gt, ut, dt);
+    if (!aligned16(in) || !aligned16(router_w) || !aligned16(g) || !aligned16(u) || !aligned16(d) || !aligned16(out))
+        return fail(c, QMOE_ERR_MISALIGNED, "every tensor base pointer must be 16-byte aligned");
+    return QMOE_OK;
+}
+
+qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* bias,
+                    const float* router_w, const void* gate, const void* up, const void* down,
+                    int gt, int ut, int dt, int T, float* out, int32_t* ids_out, float* w_out) {
+    const qmoe_config& k = c->cfg;
+    qmoe::MoeShape s{T, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    cudaError_t e = qmoe::launch_route(s, x, router_w, bias, c->route, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    e = qmoe::launch_gateup(s, x, static_cast<const uint8_t*>(gate), gt,
+                            static_cast<const uint8_t*>(up), ut, c->route, c->act, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "gate/up launch");
+    e = qmoe::launch_down(s, c->act, static_cast<const uint8_t*>(down), dt, c->route, c->y, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "down launch");
+    e = qmoe::launch_combine(s, c->y, c->route, res ? res : x, out, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    if (ids_out || w_out) {
+        e = qmoe::copy_route_out(s, c->route, ids_out, w_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmoe_workspace_bytes(const qmoe_config* cfg) {
+    char why[256];
+    if (!config_ok(cfg, why, sizeof(why))) return 0;
+    return layout(cfg).total;
+}
+
+size_t qmoe_expert_stride(qmoe_qtype qtype, int rows, int cols) {
+    if (!valid_qtype(qtype) || rows < 1 || cols < 256 || cols % 256) return 0;
+    return (size_t)rows * qmoe::row_bytes(qtype, cols);
+}
+
+qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
+    if (!out) return QMOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    qmoe_ctx* c = new (std::nothrow) qmoe_ctx();
+    if (!c) return QMOE_ERR_NO_MEMORY;
+    if (!config_ok(cfg, c->err, sizeof(c->err))) {
+        // keep the message readable through a throwaway context is impossible; print it
+        fprintf(stderr, "qmoe_create: %s\n", c->err);
+        delete c;
+        return QMOE_ERR_INVALID_ARG;
+    }
+    c->cfg = *cfg;
+    c->stream = static_cast<cudaStream_t>(cfg->stream);
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: cudaGetDevice: %s\n", cudaGetErrorString(e));
+        delete c;
+        return QMOE_ERR_CUDA;
+    }
+    const Layout L = layout(cfg);
+    size_t free_b = 0, total_b = 0;
+    e = cudaMemGetInfo(&free_b, &total_b);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: cudaMemGetInfo: %s\n", cudaGetErrorString(e));
+        delete c;
+        return QMOE_ERR_CUDA;
+    }
+    if (L.total > free_b) {
+        fprintf(stderr, "qmoe_create: workspace needs %zu bytes (%.1f MiB) but only %zu bytes (%.1f MiB) of %zu are free\n",
+                L.total, L.total / 1048576.0, free_b, free_b / 1048576.0, total_b);
+        delete c;
+        return QMOE_ERR_NO_MEMORY;
+    }
+    e = cudaMalloc(&c->ws, L.total);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: cudaMalloc(%zu): %s\n", L.total, cudaGetErrorString(e));
+        delete c;
+        return QMOE_ERR_NO_MEMORY;
+    }
+    c->ws_bytes = L.total;
+    char* b = static_cast<char*>(c->ws);
+    c->route.logits = reinterpret_cast<float*>(b + L.logits);
+    c->route.ids = reinterpret_cast<int32_t*>(b + L.ids);
+    c->route.wts = reinterpret_cast<float*>(b + L.wts);
+    c->route.n_used = reinterpret_cast<int32_t*>(b + L.n_used);
+    c->route.used_expert = reinterpret_cast<int32_t*>(b + L.used_expert);
+    c->route.used_first = reinterpret_cast<int32_t*>(b + L.used_first);
+    c->route.pair_list = reinterpret_cast<int32_t*>(b + L.pair_list);
+    c->act = reinterpret_cast<float*>(b + L.act);
+    c->y = reinterpret_cast<float*>(b + L.y);
+    c->hin = reinterpret_cast<float*>(b + L.hin);
+    c->hout = reinterpret_cast<float*>(b + L.hout);
+    c->status = reinterpret_cast<int*>(b + L.status);
+    c->xs = reinterpret_cast<float*>(b + L.xs);
+    c->q = reinterpret_cast<float*>(b + L.q);
+    c->kv = reinterpret_cast<float*>(b + L.kv);
+    c->att = reinterpret_cast<float*>(b + L.att);
+    c->attn_part = reinterpret_cast<float*>(b + L.attn_part);
+    c->attn_splits = L.attn_splits;
+    e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: workspace clear: %s\n", cudaGetErrorString(e));
+        cudaFree(c->ws);
+        delete c;
+        return QMOE_ERR_CUDA;
+    }
+    *out = c;
+    return QMOE_OK;
+}
+
+void qmoe_destroy(qmoe_ctx* c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->stream);
+    cudaFree(c->ws);
+    delete c;
+}
+
+qmoe_status qmoe_set_stream(qmoe_ctx* c, void* stream) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    c->stream = static_cast<cudaStream_t>(stream);
+    c->cfg.stream = stream;
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_forward(qmoe_ctx* c, const float* hidden_in, const float* router_w,
+                         const void* gate_exps, const void* up_exps, const void* down_exps,
+                         qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t, int n_tokens,
+                         float* hidden_out) {
+    qmoe_status s = check_forward(c, hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t,
+                                  up_t, down_t, n_tokens, hidden_out);
+    if (s != QMOE_OK) return s;
+    if (hidden_in == hidden_out && n_tokens > DECODE_ALIAS_MAX)
+        return fail(c, QMOE_ERR_INVALID_ARG, "hidden_out may alias hidden_in only for n_tokens <= %d", DECODE_ALIAS_MAX);
+    return run_moe(c, hidden_in, nullptr, nullptr, router_w, gate_exps, up_exps, down_exps, gate_t,
+                   up_t, down_t, n_tokens, hidden_out, nullptr, nullptr);
+}
+
+qmoe_status qmoe_forward_ex(qmoe_ctx* c, const float* ffn_in, const float* residual,
+                            const float* router_bias, const float* router_w,
+                            const void* gate_exps, const void* up_exps, const void* down_exps,
+                            qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t, int n_tokens,
+                            float* out, int32_t* ids_out, float* weights_out) {
+    qmoe_status s = check_forward(c, ffn_in, router_w, gate_exps, up_exps, down_exps, gate_t,
+                                  up_t, down_t, n_tokens, out);
+    if (s != QMOE_OK) return s;
+    if ((residual && !aligned16(residual)) || (router_bias && !aligned16(router_bias)))
+        return fail(c, QMOE_ERR_MISALIGNED, "residual / router_bias must be 16-byte aligned");
+    if (out == ffn_in && n_tokens > DECODE_ALIAS_MAX)
+        return fail(c, QMOE_ERR_INVALID_ARG, "out may alias ffn_in only for n_tokens <= %d", DECODE_ALIAS_MAX);
+    if (residual && out == residual && n_tokens > DECODE_ALIAS_MAX)
+        return fail(c, QMOE_ERR_INVALID_ARG, "out may alias residual only for n_tokens <= %d", DECODE_ALIAS_MAX);
+    return run_moe(c, ffn_in, residual, router_bias, router_w, gate_exps, up_exps, down_exps,
+                   gate_t, up_t, down_t, n_tokens, out, ids_out, weights_out);
+}
+
+qmoe_status qmoe_forward_host(qmoe_ctx* c, const float* hin, const float* router_w,
+                              const void* gate_exps, const void* up_exps, const void* down_exps,
+                              qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t, int n_tokens,
+                              float* hout) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    if (!hin || !hout) return fail(c, QMOE_ERR_INVALID_ARG, "null host activation pointer");
+    qmoe_status s = check_forward(c, c->hin, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,
+                                  down_t, n_tokens, c->hout);
+    if (s != QMOE_OK) return s;
+    const size_t bytes = sizeof(float) * (size_t)n_tokens * c->cfg.hidden;
+    cudaError_t e = cudaMemcpyAsync(c->hin, hin, bytes, cudaMemcpyHostToDevice, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "host->device copy");
+    s = run_moe(c, c->hin, nullptr, nullptr, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,
+                down_t, n_tokens, c->hout, nullptr, nullptr);
+    if (s != QMOE_OK) return s;
+    e = cudaMemcpyAsync(hout, c->hout, bytes, cudaMemcpyDeviceToHost, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "device->host copy");
+    e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "stream synchronize");
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int n_layers, int pos,
+                             float* hidden, int32_t* ids_out) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    (void)layers; (void)n_layers; (void)pos; (void)hidden; (void)ids_out;
+    return fail(c, QMOE_ERR_INVALID_ARG, "decode step is not available in this build");
+}
+
+qmoe_status qmoe_get_status(qmoe_ctx* c) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "stream synchronize");
+    int st = 0;
+    e = cudaMemcpy(&st, c->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "status read");
+    if (st != 0) {
+        cudaMemset(c->status, 0, sizeof(int) * 16);
+        return fail(c, static_cast<qmoe_status>(st), "device reported status %d", st);
+    }
+    return QMOE_OK;
+}
+
+const char* qmoe_last_error(qmoe_ctx* c) { return c ? c->err : "null context"; }
+
+}  // extern "C"

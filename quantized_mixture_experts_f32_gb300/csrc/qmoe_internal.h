@@ -1,0 +1,51 @@
+// qmoe_internal.h -- launchers shared between the C-ABI layer and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qmoe {
+
+// Routing results of one layer call, all in the context workspace (device).
+// Pairs p = t*K + j (token t, slot j).  The per-expert pair lists group the
+// pairs of each used expert, experts in ascending id order, pairs in ascending
+// p inside an expert: pair_list[used_first[u] .. used_first[u+1]) belong to
+// expert used_expert[u], for u < *n_used.
+struct Route {
+    float* logits;        // [T][E]
+    int32_t* ids;         // [T*K]
+    float* wts;           // [T*K]
+    int32_t* n_used;      // [1]
+    int32_t* used_expert; // [E]
+    int32_t* used_first;  // [E+1]
+    int32_t* pair_list;   // [T*K]
+};
+
+struct MoeShape {
+    int T, H, E, K, F;
+    int norm_topk;
+};
+
+// A1 + A2 + A3: router logits, softmax / top-k / renorm, per-expert pair lists.
+cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
+                         const float* bias, const Route& r, cudaStream_t st);
+
+// A4 + A5: act[p][f] = silu(Wg_e x_t)[f] * (Wu_e x_t)[f] for every pair p.
+cudaError_t launch_gateup(const MoeShape& s, const float* x, const uint8_t* gate, int gate_t,
+                          const uint8_t* up, int up_t, const Route& r, float* act,
+                          cudaStream_t st);
+
+// A6: y[p][h] = (Wd_e act_p)[h] for every pair p.
+cudaError_t launch_down(const MoeShape& s, const float* act, const uint8_t* down, int down_t,
+                        const Route& r, float* y, cudaStream_t st);
+
+// A7: out[t][h] = res[t][h] + sum_j wts[t][j] * y[t*K+j][h].
+cudaError_t launch_combine(const MoeShape& s, const float* y, const Route& r, const float* res,
+                           float* out, cudaStream_t st);
+
+// Copy the routing results out (ids int32, weights f32), async.
+cudaError_t copy_route_out(const MoeShape& s, const Route& r, int32_t* ids_out, float* w_out,
+                           cudaStream_t st);
+
+size_t row_bytes(int qtype, int cols);
+
+}  // namespace qmoe

@@ -1,0 +1,68 @@
+"""Helpers shared by the GPU parity tests: upload seeded inputs, call the C ABI,
+compare against the oracle with the comparator in tests/compare.py."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from tests.compare import TOL_W, ids_match, rel_err, tie_bound_f32
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(dev())
+
+
+def upload(inp: dict) -> dict:
+    d = {n: to_dev(inp[n]) for n in ("x", "router", "gate", "up", "down")}
+    d["bias"] = None if inp.get("bias") is None else to_dev(inp["bias"])
+    return d
+
+
+def make_ctx(q, inp, max_tokens=None, norm=1):
+    stream = torch.cuda.current_stream(dev())
+    return q.qmoe_create(q.make_config(inp["H"], inp["E"], inp["K"], inp["F"],
+                                       max_tokens or inp["T"], norm, stream.cuda_stream))
+
+
+def run(q, ctx, inp, d, T=None, x=None, residual=None, bias="auto", out=None):
+    T = inp["T"] if T is None else T
+    x = d["x"] if x is None else x
+    bias = d["bias"] if bias == "auto" else bias
+    out = torch.empty((T, inp["H"]), dtype=torch.float32, device=dev()) if out is None else out
+    ids = torch.full((T, inp["K"]), -1, dtype=torch.int32, device=dev())
+    w = torch.full((T, inp["K"]), -1.0, dtype=torch.float32, device=dev())
+    q.qmoe_forward_ex(ctx, x, residual, bias, d["router"], d["gate"], d["up"], d["down"],
+                      q.QTYPE[inp["gate_t"]], q.QTYPE[inp["up_t"]], q.QTYPE[inp["down_t"]], T,
+                      out, ids, w)
+    st = q.qmoe_get_status(ctx)
+    assert st == q.QMOE_OK, q.qmoe_last_error(ctx)
+    return dict(out=out.cpu().numpy(), ids=ids.cpu().numpy(), w=w.cpu().numpy())
+
+
+def check(inp, got, tol, ref=None, residual=None, norm=True):
+    """Assert parity of one call; returns (rel_err, near-tie tokens, min gap)."""
+    from tests.compare import min_gap
+    ref = ref if ref is not None else oracle.moe_forward(inp, norm_topk=norm)
+    bound = tie_bound_f32(inp["router"], inp["x"], inp.get("bias"))
+    ok, ties = ids_match(got["ids"], ref["ids"], ref["logits"], bound)
+    assert ok, f"expert ids differ beyond near-ties:\n{got['ids']}\n{ref['ids']}"
+    if ties:
+        # both selections are valid F32-router results: compare against the oracle
+        # evaluated on the kernel's selection
+        ref = oracle.moe_forward(inp, norm_topk=norm, force=got["ids"])
+    dw = np.abs(got["w"] - ref["w"]).max()
+    assert dw <= TOL_W, f"routing weights differ by {dw:.3e}"
+    want = ref["out"]
+    if residual is not None:
+        want = want - inp["x"].astype(np.float64) + residual.astype(np.float64)
+    err = rel_err(got["out"], want)
+    assert err <= tol, f"max relative error {err:.3e} > {tol:.1e}"
+    return err, ties, min_gap(ref["logits"], inp["K"])

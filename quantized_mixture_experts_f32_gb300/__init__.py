@@ -24,6 +24,10 @@ STATUS_NAMES = {0: "QMOE_OK", 1: "QMOE_ERR_INVALID_ARG", 2: "QMOE_ERR_MISALIGNED
 QMOE_Q4_K, QMOE_Q6_K = 1, 2
 QTYPE = {"Q4_K": QMOE_Q4_K, "Q6_K": QMOE_Q6_K}
 
+# kernels one qmoe_forward enqueues on the decode path (n_tokens <= 8): the
+# whole layer is one fused cooperative kernel
+LAUNCHES_PER_DECODE_FORWARD = 1
+
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride"]

@@ -23,6 +23,8 @@ struct qmoe_ctx {
     float* hin;       // [T][H] staging for qmoe_forward_host
     float* hout;      // [T][H]
     int* status;      // device status word
+    unsigned* bar;    // grid-barrier counters of the fused kernel
+    int num_sms;
     // decode-step scratch
     float* xs;        // [H] normed hidden
     float* q;         // [nq*hd]
@@ -58,7 +60,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, xs, q, kv, att, attn_part, total;
+        status, bar, xs, q, kv, att, attn_part, total;
     int attn_splits;
 };
 
@@ -99,6 +101,7 @@ Layout layout(const qmoe_config* c) {
     L.hin = take(sizeof(float) * T * H);
     L.hout = take(sizeof(float) * T * H);
     L.status = take(sizeof(int) * 16);
+    L.bar = take(sizeof(unsigned) * 16);
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
     L.attn_splits = c->max_ctx > 0 ? (c->max_ctx + 255) / 256 : 0;
     L.xs = take(sizeof(float) * H);
@@ -130,6 +133,17 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
                     int gt, int ut, int dt, int T, float* out, int32_t* ids_out, float* w_out) {
     const qmoe_config& k = c->cfg;
     qmoe::MoeShape s{T, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    qmoe::FusedPlan plan;
+    if (qmoe::fused_decode_plan(s, gt, ut, dt, c->num_sms, &plan)) {
+        // decode: the whole layer is one cooperative kernel
+        cudaError_t e = qmoe::launch_fused_decode(
+            s, plan, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
+            static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out,
+            w_out, c->route.logits, c->act, c->bar, c->status, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
+        c->err[0] = 0;
+        return QMOE_OK;
+    }
     cudaError_t e = qmoe::launch_route(s, x, router_w, bias, c->route, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
     e = qmoe::launch_gateup(s, x, static_cast<const uint8_t*>(gate), gt,
@@ -195,6 +209,18 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
         delete c;
         return QMOE_ERR_NO_MEMORY;
     }
+    e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: cudaDeviceGetAttribute: %s\n", cudaGetErrorString(e));
+        delete c;
+        return QMOE_ERR_CUDA;
+    }
+    e = qmoe::fused_prepare();
+    if (e != cudaSuccess) {
+        fprintf(stderr, "qmoe_create: fused kernel set-up: %s\n", cudaGetErrorString(e));
+        delete c;
+        return QMOE_ERR_CUDA;
+    }
     e = cudaMalloc(&c->ws, L.total);
     if (e != cudaSuccess) {
         fprintf(stderr, "qmoe_create: cudaMalloc(%zu): %s\n", L.total, cudaGetErrorString(e));
@@ -215,6 +241,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->hin = reinterpret_cast<float*>(b + L.hin);
     c->hout = reinterpret_cast<float*>(b + L.hout);
     c->status = reinterpret_cast<int*>(b + L.status);
+    c->bar = reinterpret_cast<unsigned*>(b + L.bar);
     c->xs = reinterpret_cast<float*>(b + L.xs);
     c->q = reinterpret_cast<float*>(b + L.q);
     c->kv = reinterpret_cast<float*>(b + L.kv);

@@ -48,4 +48,28 @@ cudaError_t copy_route_out(const MoeShape& s, const Route& r, int32_t* ids_out, 
 
 size_t row_bytes(int qtype, int cols);
 
+// Fused single-kernel decode path (T <= 8): launch plan chosen once per shape.
+struct FusedPlan {
+    int grid;          // CTAs (one per SM, cooperative)
+    int smem;          // dynamic shared memory bytes
+    const void* fn;    // kernel variant
+    int rows_max;      // ceil(H / grid)
+    int slot_bytes;    // ring slot size
+    int asum_bytes;    // act group-sum table size
+    int cf;            // f rows per gate/up chunk
+    bool stage_act;    // act copied to shared memory for the down phase
+};
+
+bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int num_sms,
+                       FusedPlan* plan);
+
+cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const float* x,
+                                const float* res, const float* bias, const float* router,
+                                const uint8_t* gate, const uint8_t* up, const uint8_t* down,
+                                float* out, int32_t* ids_out, float* w_out, float* logits,
+                                float* act, unsigned* bar, int* status, cudaStream_t st);
+
+int fused_threads();
+cudaError_t fused_prepare();
+
 }  // namespace qmoe

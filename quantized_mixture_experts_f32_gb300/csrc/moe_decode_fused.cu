@@ -62,7 +62,7 @@ enum { M_NUSED = 0, M_NCH, M_NGU, M_GUDONE, M_ABORT, M_H0, M_NROWS, M_GULO, M_NR
 
 struct SmemLayout {
     int off_bar, off_misc, off_red, off_ids, off_wts, off_used, off_first, off_pairs,
-        off_x, off_xsum, off_ybuf, off_ring, total, slot_bytes, rows_max, act_stage;
+        off_x, off_xsum, off_xscale, off_ybuf, off_ring, total, slot_bytes, rows_max, act_stage;
 };
 
 __host__ __device__ inline int al(int v, int a) { return (v + a - 1) / a * a; }
@@ -87,6 +87,7 @@ __host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, i
     o = al(o, 16);
     L.off_x = o;        o += al(T * H * 4 > asum_bytes ? T * H * 4 : asum_bytes, 16);
     L.off_xsum = o;     o += al(T * (H / 16) * 4, 16);
+    L.off_xscale = o;   o += al(T * (H / 16) * 4, 16);
     L.off_ybuf = o;     o += al(P * rows_max * 4, 16);
     o = al(o, 128);
     L.off_ring = o;     o += NSLOT * slot_bytes;
@@ -148,6 +149,45 @@ __device__ __forceinline__ void q4_piece_regs(uint4 q, const float4 (&xa)[4], co
     PB = b0 + b1;
 }
 
+// Exact integer form of one 16-byte Q4_K piece.  The 16 x values paired with the
+// low nibbles are n_l * scaleA with n_l a 24-bit integer split into three
+// signed byte planes (n = p2*2^16 + p1*2^8 + p0); the nibble bytes of the
+// piece are the other dp4a operand, so sum_l q_l n_l is formed exactly in
+// int32 with no per-weight float conversion.  Returns sum q*x for the low
+// (SA) and high (SB) nibbles.
+__device__ __forceinline__ void q4_piece_dp4a(uint4 q, const int (&xa)[3][4], const int (&xb)[3][4],
+                                              float scaleA, float scaleB, float& SA, float& SB) {
+    int a0 = 0, a1 = 0, a2 = 0, b0 = 0, b1 = 0, b2 = 0;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int lo = (int)(w[i] & 0x0F0F0F0Fu), hi = (int)((w[i] >> 4) & 0x0F0F0F0Fu);
+        a0 = __dp4a(lo, xa[0][i], a0);
+        a1 = __dp4a(lo, xa[1][i], a1);
+        a2 = __dp4a(lo, xa[2][i], a2);
+        b0 = __dp4a(hi, xb[0][i], b0);
+        b1 = __dp4a(hi, xb[1][i], b1);
+        b2 = __dp4a(hi, xb[2][i], b2);
+    }
+    SA = scaleA * fmaf((float)a2, 65536.f, (float)(a1 * 256 + a0));
+    SB = scaleB * fmaf((float)b2, 65536.f, (float)(b1 * 256 + b0));
+}
+
+// contribution of a piece given the exact sums QA = sum q x, QB, and the x sums
+__device__ __forceinline__ float q4_piece_finish_exact(uint4 hdr, int pc, float QA, float QB,
+                                                       float XA, float XB) {
+    int sA, mA, sB, mB;
+    q4_scales(hdr.y, hdr.z, hdr.w, pc >> 1, sA, mA, sB, mB);
+    const float d = half_bits(hdr.x), dmin = half_bits(hdr.x >> 16);
+    float r = (d * (float)sA) * QA - (dmin * (float)mA) * XA;
+    r = fmaf(d * (float)sB, QB, r) - (dmin * (float)mB) * XB;
+    return r;
+}
+
+// 24-bit exact-integer quantiser limit: |n| <= 2^23 - 2^16 keeps the top byte
+// plane in [-127, 127]
+constexpr float XQ_LIM = 8323072.f;
+
 // ----------------------------------------------------------------------------- the kernel
 
 template <int NSB_G, int NSB_D, int DQT>
@@ -172,6 +212,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     int32_t* pairs = reinterpret_cast<int32_t*>(sm + L.off_pairs);
     float* x_s = reinterpret_cast<float*>(sm + L.off_x);
     float* xsum = reinterpret_cast<float*>(sm + L.off_xsum);
+    float* xscale = reinterpret_cast<float*>(sm + L.off_xscale);
+    int32_t* xq = reinterpret_cast<int32_t*>(x_s);                 // byte planes, after the router
     float* ybuf = reinterpret_cast<float*>(sm + L.off_ybuf);
     uint8_t* ring = sm + L.off_ring;
     const int SB = L.slot_bytes;
@@ -244,6 +286,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         }
         __syncthreads();
     }
+    // x -> per-16-column scale and three signed byte planes, in place (the
+    // router, the only fp32 reader of x_s, is done)
+    {
+        constexpr int GPT = 2;                                     // 16-col groups per thread
+        int pw[GPT][12];
+        float psc[GPT];
+        const int ng = T * (H / 16);
+#pragma unroll
+        for (int gi = 0; gi < GPT; ++gi) {
+            const int g = tid + gi * NTHREADS;
+            if (g < ng) {
+                const float* xv = x_s + 16 * g;
+                float mx = 0.f;
+#pragma unroll
+                for (int z = 0; z < 16; ++z) mx = fmaxf(mx, fabsf(xv[z]));
+                const float inv = mx > 0.f ? XQ_LIM / mx : 0.f;
+                psc[gi] = mx / XQ_LIM;
+#pragma unroll
+                for (int w4 = 0; w4 < 4; ++w4) {
+                    uint32_t p0 = 0, p1 = 0, p2 = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int n = __float2int_rn(xv[4 * w4 + b] * inv);
+                        const int d0 = ((n + 128) & 255) - 128;
+                        const int n1 = (n - d0) >> 8;
+                        const int d1 = ((n1 + 128) & 255) - 128;
+                        const int d2 = (n1 - d1) >> 8;
+                        p0 |= (uint32_t)(d0 & 255) << (8 * b);
+                        p1 |= (uint32_t)(d1 & 255) << (8 * b);
+                        p2 |= (uint32_t)(d2 & 255) << (8 * b);
+                    }
+                    pw[gi][w4] = (int)p0;
+                    pw[gi][4 + w4] = (int)p1;
+                    pw[gi][8 + w4] = (int)p2;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int gi = 0; gi < GPT; ++gi) {
+            const int g = tid + gi * NTHREADS;
+            if (g < ng) {
+#pragma unroll
+                for (int z = 0; z < 12; ++z) xq[12 * g + z] = pw[gi][z];
+                xscale[g] = psc[gi];
+            }
+        }
+    }
     if (tid == 0) {
         QMOE_TRACE(1);
         grid_arrive(&p.bar[0]);
@@ -266,20 +356,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     if (tid < 32) bitmap[tid] = 0u;
     for (int i = tid; i < P; i += NTHREADS) sel[i] = 0;
     __syncthreads();
-    if (!abort_b)
-        for (int i = tid; i < T * E; i += NTHREADS) {
-            const int t = i / E, e = i - t * E;
+    if (!abort_b) {
+        // rank of every logit among its token's E (ties: lower index first);
+        // tpe consecutive lanes share one logit's E comparisons
+        const int nel = T * E;
+        int tpe = NTHREADS / nel;
+        tpe = tpe >= 32 ? 32 : tpe >= 16 ? 16 : tpe >= 8 ? 8 : tpe >= 4 ? 4 : tpe >= 2 ? 2 : 1;
+        if (tpe > 1) {
+            const int i = tid / tpe, sub = tid - (tid / tpe) * tpe;
+            const bool valid = i < nel;
+            const int t = valid ? i / E : 0, e = valid ? i - t * E : 0;
             const float* l = lg_s + t * E;
             const float v = l[e];
             int rank = 0;
-            for (int e2 = 0; e2 < E; ++e2) {
+            for (int e2 = sub; e2 < E; e2 += tpe) {
                 const float w = l[e2];
                 rank += (w > v) || (w == v && e2 < e);
             }
-            if (rank < K) sel[t * K + rank] = e;
+            for (int o = tpe >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+            if (valid && sub == 0 && rank < K) sel[t * K + rank] = e;
+        } else {
+            for (int i = tid; i < nel; i += NTHREADS) {
+                const int t = i / E, e = i - t * E;
+                const float* l = lg_s + t * E;
+                const float v = l[e];
+                int rank = 0;
+                for (int e2 = 0; e2 < E; ++e2) {
+                    const float w = l[e2];
+                    rank += (w > v) || (w == v && e2 < e);
+                }
+                if (rank < K) sel[t * K + rank] = e;
+            }
         }
+    }
     if (tid == 0) QMOE_TRACE(11);
     __syncthreads();
+    // softmax weights (warp t) and, in parallel, each pair's place in the
+    // expert-sorted pair list (threads 256.. ; ids are the selection itself)
     if (!abort_b && warp < T) {
         const float* l = lg_s + warp * E;
         const float vmax = l[sel[warp * K]];
@@ -292,27 +405,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             set_status(p.status, ST_DEVICE_CHECK);
         }
         const float pj = lane < K ? expf(l[id] - vmax) / z : 0.f;
-        float psel = 0.f;
-        for (int j = 0; j < K; ++j) psel += __shfl_sync(0xffffffffu, pj, j);
+        const float psel = warp_sum(pj);
         if (lane < K) {
             ids_s[warp * K + lane] = id;
             wts_s[warp * K + lane] = p.norm ? pj / psel : pj;
         }
     }
-    __syncthreads();
-    if (tid == 0) QMOE_TRACE(12);
-    if (!abort_b && tid < P) {
-        const int e = ids_s[tid];
+    const int pt = tid - NTHREADS / 2;
+    if (!abort_b && pt >= 0 && pt < P) {
+        int e = sel[pt];
+        e = (e < 0 || e >= E) ? 0 : e;
         int pos = 0;
         for (int q = 0; q < P; ++q) {
-            const int e2 = ids_s[q];
-            pos += (e2 < e) || (e2 == e && q < tid);
+            int e2 = sel[q];
+            e2 = (e2 < 0 || e2 >= E) ? 0 : e2;
+            pos += (e2 < e) || (e2 == e && q < pt);
         }
-        pairs[pos] = tid;
+        pairs[pos] = pt;
         se[pos] = e;
         atomicOr(&bitmap[e >> 5], 1u << (e & 31));
     }
     __syncthreads();
+    if (tid == 0) QMOE_TRACE(12);
     if (!abort_b && tid < P) {
         const int e = se[tid];
         if (tid == 0 || se[tid - 1] != e) {
@@ -322,39 +436,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             used_first[u] = tid;
         }
     }
-    if (tid == 0) {
-        int nu = 0;
-        for (int w = 0; w < 32; ++w) nu += __popc(bitmap[w]);
-        misc[M_NUSED] = abort_b ? 0 : nu;
-        used_first[abort_b ? 0 : nu] = P;
+    if (warp == NCW - 1) {
+        int nu = __popc(bitmap[lane]);
+        for (int o = 16; o > 0; o >>= 1) nu += __shfl_xor_sync(0xffffffffu, nu, o);
+        if (abort_b) nu = 0;
+        if (lane == 0) {
+            misc[M_NUSED] = nu;
+            used_first[nu] = P;
+            // Work of this CTA, in closed form.  Gate/up: the used experts' f rows
+            // are cut into global chunks of CF consecutive f (CF divides F); CTA c
+            // owns global chunks [c*NG/G, (c+1)*NG/G).  Down: rows [h0, h1) of
+            // every used expert, RPC rows per chunk.
+            const int CF = p.cf, CPE = F / CF;
+            const int NG = nu * CPE;                             // < 2^17, NG * G < 2^31
+            const int lo = NG * c / G, hi = NG * (c + 1) / G;
+            const int h0 = H * c / G, h1 = H * (c + 1) / G;
+            const int RPC = (SB - 32) / RBD;
+            const int nrc = (h1 - h0 + RPC - 1) / RPC;
+            misc[M_GULO] = lo;
+            misc[M_NGU] = hi - lo;
+            misc[M_GUWARPS] = hi - lo < NCW ? hi - lo : NCW;      // warps with gate/up work
+            misc[M_NRC] = nrc;
+            misc[M_NCH] = (hi - lo) + nu * nrc;
+            misc[M_H0] = h0;
+            misc[M_NROWS] = h1 - h0;
+            if (hi - lo == 0) grid_arrive(&p.bar[1]);
+        }
     }
+    __syncthreads();
     if (tid == 0) QMOE_TRACE(13);
-    if (tid == 0) {
-        // Work of this CTA, in closed form.  Gate/up: the used experts' f rows are
-        // cut into global chunks of CF consecutive f (CF divides F); CTA c owns
-        // global chunks [c*NG/G, (c+1)*NG/G).  Down: rows [h0, h1) of every used
-        // expert, RPC rows per chunk.
-        const int nu = abort_b ? 0 : misc[M_NUSED];
-        const int CF = p.cf, CPE = F / CF;
-        const int NG = nu * CPE;                                 // < 2^17, NG * G < 2^31
-        const int lo = NG * c / G, hi = NG * (c + 1) / G;
-        const int h0 = H * c / G, h1 = H * (c + 1) / G;
-        const int RPC = (SB - 32) / RBD;
-        const int nrc = (h1 - h0 + RPC - 1) / RPC;
-        misc[M_GULO] = lo;
-        misc[M_NGU] = hi - lo;
-        misc[M_GUWARPS] = hi - lo < NCW ? hi - lo : NCW;          // warps with gate/up work
-        misc[M_NRC] = nrc;
-        misc[M_NCH] = (hi - lo) + nu * nrc;
-        misc[M_H0] = h0;
-        misc[M_NROWS] = h1 - h0;
-        if (hi - lo == 0) grid_arrive(&p.bar[1]);
-    }
     if (c == 0 && tid < P && !abort_b) {
         if (p.ids_out) p.ids_out[tid] = ids_s[tid];
         if (p.w_out) p.w_out[tid] = wts_s[tid];
     }
-    __syncthreads();
     if (tid == 0) QMOE_TRACE(3);
     const int n_ch = misc[M_NCH], n_gu = misc[M_NGU];
     const int gu_lo = misc[M_GULO], nrc = misc[M_NRC];
@@ -408,8 +522,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     }
     {
         // ---------------- phase C: gate/up + SwiGLU
-        float4 xa[NTG][4], xb[NTG][4];
-        float XA[NTG], XB[NTG];
+        int xa[NTG][3][4], xb[NTG][3][4];
+        float XA[NTG], XB[NTG], SXA[NTG], SXB[NTG];
         int xtok = -1;
         int j = 0;
         for (; warp + NCW * j < n_gu; ++j) {
@@ -438,57 +552,58 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                             const int sb = tsk >> 3, pc = tsk & 7;
                             if (tsk < 8 * NSB_G) {
                                 const int col = QK * sb + 64 * (pc >> 1) + 16 * (pc & 1);
-                                const float4* xp = reinterpret_cast<const float4*>(x_s + t * H + col);
+                                const int ga = t * (H / 16) + col / 16, gb = ga + 2;
+                                const int4* pa = reinterpret_cast<const int4*>(xq + 12 * ga);
+                                const int4* pb = reinterpret_cast<const int4*>(xq + 12 * gb);
 #pragma unroll
-                                for (int z = 0; z < 4; ++z) { xa[jt][z] = xp[z]; xb[jt][z] = xp[8 + z]; }
-                                XA[jt] = xsum[t * (H / 16) + col / 16];
-                                XB[jt] = xsum[t * (H / 16) + col / 16 + 2];
+                                for (int pl = 0; pl < 3; ++pl) {
+                                    const int4 va = pa[pl], vb = pb[pl];
+                                    xa[jt][pl][0] = va.x; xa[jt][pl][1] = va.y; xa[jt][pl][2] = va.z; xa[jt][pl][3] = va.w;
+                                    xb[jt][pl][0] = vb.x; xb[jt][pl][1] = vb.y; xb[jt][pl][2] = vb.z; xb[jt][pl][3] = vb.w;
+                                }
+                                XA[jt] = xsum[ga];
+                                XB[jt] = xsum[gb];
+                                SXA[jt] = xscale[ga];
+                                SXB[jt] = xscale[gb];
                             }
                         }
                     }
                     if (lane == 0 && warp == 0 && j == 0) QMOE_TRACE(10);
-                    for (int i = 0; i < nf; i += 2) {
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int i = 0; i < nf; ++i) {
+                        // gate row i and up row i, all of this lane's pieces at once
+                        float g = 0.f, v = 0.f;
+                        uint4 hd[2 * NTG], qd[2 * NTG];
 #pragma unroll
-                        for (int jt = 0; jt < NTG; ++jt) {
-                            const int tsk = lane + 32 * jt;
+                        for (int z = 0; z < 2 * NTG; ++z) {
+                            const int jt = z >> 1, tsk = lane + 32 * jt;
                             if (tsk < 8 * NSB_G) {
                                 const int sb = tsk >> 3, pc = tsk & 7;
-                                uint4 hd[4], qd[4];
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) {
-                                    const int row = (r < 2 ? i + r : nf + i + r - 2);
-                                    const uint8_t* b = slot + row * RBG + sb * Q4K_BYTES;
-                                    hd[r] = *reinterpret_cast<const uint4*>(b);
-                                    qd[r] = *reinterpret_cast<const uint4*>(b + 16 + 16 * pc);
-                                }
-#ifdef QMOE_ROLLED
-#pragma unroll 1
-#else
-#pragma unroll
-#endif
-                                for (int r = 0; r < 4; ++r) {
-                                    float PA, PB;
-                                    q4_piece_regs(qd[r], xa[jt], xb[jt], PA, PB);
-                                    acc[r] += q4_piece_finish(hd[r], pc, PA, PB, XA[jt], XB[jt]);
-                                }
+                                const int row = (z & 1) ? nf + i : i;
+                                const uint8_t* b = slot + row * RBG + sb * Q4K_BYTES;
+                                hd[z] = *reinterpret_cast<const uint4*>(b);
+                                qd[z] = *reinterpret_cast<const uint4*>(b + 16 + 16 * pc);
                             }
                         }
-                        // lanes with bits (4,3) = (a, b) end with the sum of acc[2a + b]
-                        const bool h16 = lane & 16, h8 = lane & 8;
-                        const float r0 = __shfl_xor_sync(0xffffffffu, h16 ? acc[0] : acc[2], 16);
-                        const float r1 = __shfl_xor_sync(0xffffffffu, h16 ? acc[1] : acc[3], 16);
-                        const float k0 = (h16 ? acc[2] : acc[0]) + r0;
-                        const float k1 = (h16 ? acc[3] : acc[1]) + r1;
-                        float m = (h8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+#pragma unroll
+                        for (int z = 0; z < 2 * NTG; ++z) {
+                            const int jt = z >> 1, tsk = lane + 32 * jt;
+                            if (tsk < 8 * NSB_G) {
+                                const int pc = tsk & 7;
+                                float QA, QB;
+                                q4_piece_dp4a(qd[z], xa[jt], xb[jt], SXA[jt], SXB[jt], QA, QB);
+                                const float c = q4_piece_finish_exact(hd[z], pc, QA, QB, XA[jt], XB[jt]);
+                                if (z & 1) v += c; else g += c;
+                            }
+                        }
+                        // lanes 0-15 end with the gate sum, lanes 16-31 with the up sum
+                        const bool h16 = lane & 16;
+                        float m = (h16 ? v : g) + __shfl_xor_sync(0xffffffffu, h16 ? g : v, 16);
+                        m += __shfl_xor_sync(0xffffffffu, m, 8);
                         m += __shfl_xor_sync(0xffffffffu, m, 4);
                         m += __shfl_xor_sync(0xffffffffu, m, 2);
                         m += __shfl_xor_sync(0xffffffffu, m, 1);
-                        const float upv = __shfl_down_sync(0xffffffffu, m, 16);   // up of the same f
-                        if (lane == 0 || lane == 8) {
-                            const float g = m;
-                            p.act[(size_t)pr * F + f0 + i + (lane >> 3)] = g / (1.f + expf(-g)) * upv;
-                        }
+                        const float upv = __shfl_down_sync(0xffffffffu, m, 16);
+                        if (lane == 0) p.act[(size_t)pr * F + f0 + i] = m / (1.f + expf(-m)) * upv;
                     }
                 }
             }
@@ -680,7 +795,7 @@ int slot_bytes_for(int H, int F, int down_t) {
     const int rbg = (H / QK) * Q4K_BYTES;
     const int rbd = (F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
     int sb = SLOT_BYTES_TARGET;
-    if (sb < 4 * rbg) sb = 4 * rbg;                       // at least two f per gate/up chunk
+    if (sb < 2 * rbg) sb = 2 * rbg;                       // at least one f per gate/up chunk
     if (sb < rbd + 32) sb = al(rbd + 32, 16);
     return al(sb, 128);
 }
@@ -709,13 +824,17 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
     plan->stage_act = stage;
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    int cf = sb / (2 * rbg);                 // largest power of two <= that divides F
+    // f rows per gate/up chunk: one when a row pair is already >= 2 KB (finer
+    // split of a CTA's share over its warps), else the largest power of two
+    // that fits the slot and divides F
+    int cf = sb / (2 * rbg);
     int p2 = 1;
     while (p2 * 2 <= cf && s.F % (p2 * 2) == 0) p2 *= 2;
-    cf = p2;
-    if (cf < 2 || (sb - 32) / rbd < 1) return false;
+    cf = rbg >= 1024 ? 1 : p2;
+    if (cf < 1 || (sb - 32) / rbd < 1) return false;
     plan->cf = cf;
     if (s.E > 1024) return false;
+    if (s.T * (s.H / 16) > 2 * NTHREADS) return false;       // x byte-plane conversion share
     plan->grid = G;
     plan->smem = L.total;
     plan->fn = v->fn;

@@ -163,6 +163,37 @@ typedef struct {
 qmoe_status qmoe_decode_step(qmoe_ctx* ctx, const qmoe_layer_weights* layers, int n_layers,
                              int pos, float* hidden, int32_t* ids_out);
 
+/* Allocation-free variant of qmoe_forward for decode-sized calls.  The pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory: processes whose device memory is owned by their own
+ * pool (a host framework's allocator, a plugin inside such a process), or
+ * latency-critical loops that must not run a cudaMalloc, with its implicit
+ * device synchronisation, after start-up.  It needs no context and allocates
+ * nothing: its scratch (router logits, SwiGLU activations, grid-barrier
+ * counters, status word) is one fixed device array inside the library, about
+ * 288 KiB, which every GPU that loads the library holds until the process exits.
+ *  - Computes the same as qmoe_forward (hidden_out = hidden_in + MoE(hidden_in))
+ *    with the same argument meaning, layout and alignment rules, on `stream`
+ *    (a cudaStream_t; NULL = legacy default stream).
+ *  - Served shapes: those of the fused single-kernel decode path -- n_tokens
+ *    <= 8, gate/up Q4_K, hidden in {256, 2048}, ffn in {256, 768} -- and within
+ *    the scratch capacity n_tokens*n_experts <= 8192, n_tokens*top_k*ffn <=
+ *    65536.  Anything else returns QMOE_ERR_SHAPE and enqueues nothing.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
+ *    first call before any stream capture.
+ *  - All calls share the one scratch array and it keeps the last call's
+ *    contents; each call clears the counters it needs.  Calls whose execution
+ *    overlaps on the GPU (other streams, other host threads) race on it and
+ *    give wrong results: order them.
+ *  - Returns launch / argument errors only; device-side status is not reported. */
+qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float* router_w,
+                                 const void* gate_exps, const void* up_exps,
+                                 const void* down_exps, qmoe_qtype gate_t, qmoe_qtype up_t,
+                                 qmoe_qtype down_t, int hidden, int n_experts, int top_k,
+                                 int ffn, int norm_topk_prob, int n_tokens, float* hidden_out,
+                                 void* stream);
+
 /* Synchronise the stream and read the device status word (bounded-wait
  * timeouts, device index checks).  A non-OK status is sticky until read:
  * reading it clears it. */

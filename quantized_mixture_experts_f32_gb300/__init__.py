@@ -30,7 +30,7 @@ LAUNCHES_PER_DECODE_FORWARD = 1
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
-            "qmoe_workspace_bytes", "qmoe_expert_stride"]
+            "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc"]
 
 
 class qmoe_config(C.Structure):
@@ -84,6 +84,8 @@ def _load():
     L.qmoe_workspace_bytes.restype = C.c_size_t
     L.qmoe_expert_stride.argtypes = [i, i, i]
     L.qmoe_expert_stride.restype = C.c_size_t
+    L.qmoe_forward_noalloc.argtypes = [fp, fp, vp, vp, vp, i, i, i, i, i, i, i, i, i, fp, vp]
+    L.qmoe_forward_noalloc.restype = i
     return L
 
 
@@ -147,6 +149,16 @@ def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_ex
 
 def qmoe_decode_step(ctx, layers, n_layers, pos, hidden, ids_out=None):
     _check(ctx, lib.qmoe_decode_step(ctx, layers, n_layers, pos, _ptr(hidden), _ptr(ids_out)))
+
+
+def qmoe_forward_noalloc(hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,
+                         down_t, hidden, n_experts, top_k, ffn, norm_topk_prob, n_tokens,
+                         hidden_out, stream=0) -> int:
+    """Allocation-free decode-size forward; returns the qmoe_status code."""
+    return lib.qmoe_forward_noalloc(_ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
+                                    _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t, hidden,
+                                    n_experts, top_k, ffn, norm_topk_prob, n_tokens,
+                                    _ptr(hidden_out), stream or None)
 
 
 def qmoe_get_status(ctx) -> int:

@@ -1,0 +1,110 @@
+// qmoe_noalloc.cu -- qmoe_forward_noalloc: the decode-size MoE-FFN layer for
+// callers that cannot allocate device memory.
+//
+// Some callers own every byte of device memory through their own pool (a host
+// framework whose allocator must not be bypassed, a plugin loaded into such a
+// process), or run latency-critical loops in which a cudaMalloc, with its
+// implicit device synchronisation, is not acceptable after start-up.  For them
+// this entry point needs no context and performs no allocation: the scratch of
+// the fused decode kernel (router logits, SwiGLU activations, grid-barrier
+// counters and the device status word) lives in one file-scope device array of
+// fixed size, which every GPU that loads this library keeps until the process
+// exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/qmoe.h"
+#include "qmoe_internal.h"
+
+namespace {
+
+// Capacity of the shared scratch (elements).
+constexpr size_t NA_LOGITS = 8 * 1024;        // n_tokens * n_experts
+constexpr size_t NA_ACT = 64 * 1024;          // n_tokens * top_k * ffn
+constexpr size_t NA_HEAD = 256;               // barrier counters + status word (bytes)
+constexpr size_t NA_BYTES = NA_HEAD + (NA_LOGITS + NA_ACT) * sizeof(float);
+
+constexpr int NA_MAX_DEVICES = 64;
+
+struct DeviceSetup {
+    bool ready = false;
+    unsigned char* scratch = nullptr;  // device address of g_qmoe_noalloc_scratch
+    int num_sms = 0;
+};
+
+DeviceSetup g_setup[NA_MAX_DEVICES];
+std::mutex g_setup_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// symbol, never a device address: the address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_qmoe_noalloc_scratch[NA_BYTES];
+
+extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float* router_w,
+                                            const void* gate_exps, const void* up_exps,
+                                            const void* down_exps, qmoe_qtype gate_t,
+                                            qmoe_qtype up_t, qmoe_qtype down_t, int hidden,
+                                            int n_experts, int top_k, int ffn,
+                                            int norm_topk_prob, int n_tokens,
+                                            float* hidden_out, void* stream) {
+    if (!hidden_in || !router_w || !gate_exps || !up_exps || !down_exps || !hidden_out)
+        return QMOE_ERR_INVALID_ARG;
+    if (hidden <= 0 || hidden % 256 || ffn <= 0 || ffn % 256 || n_experts < 1 ||
+        n_experts > 1024 || top_k < 1 || top_k > 16 || top_k > n_experts || n_tokens < 1)
+        return QMOE_ERR_SHAPE;
+    if ((gate_t != QMOE_Q4_K && gate_t != QMOE_Q6_K) || (up_t != QMOE_Q4_K && up_t != QMOE_Q6_K) ||
+        (down_t != QMOE_Q4_K && down_t != QMOE_Q6_K))
+        return QMOE_ERR_UNSUPPORTED_QTYPE;
+    if (!aligned16(hidden_in) || !aligned16(router_w) || !aligned16(gate_exps) ||
+        !aligned16(up_exps) || !aligned16(down_exps) || !aligned16(hidden_out))
+        return QMOE_ERR_MISALIGNED;
+    // capacity of the shared scratch
+    if ((size_t)n_tokens * n_experts > NA_LOGITS ||
+        (size_t)n_tokens * top_k * ffn > NA_ACT)
+        return QMOE_ERR_SHAPE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES)
+        return QMOE_ERR_CUDA;
+    DeviceSetup* su = &g_setup[dev];
+    {
+        // first call on this device: look up the scratch's device address and
+        // prepare the kernel (no allocation happens here either)
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        if (!su->ready) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_qmoe_noalloc_scratch) != cudaSuccess)
+                return QMOE_ERR_CUDA;
+            if (qmoe::fused_prepare() != cudaSuccess) return QMOE_ERR_CUDA;
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return QMOE_ERR_CUDA;
+            su->scratch = static_cast<unsigned char*>(ptr);
+            su->num_sms = sms;
+            su->ready = true;
+        }
+    }
+
+    qmoe::MoeShape s{n_tokens, hidden, n_experts, top_k, ffn, norm_topk_prob ? 1 : 0};
+    qmoe::FusedPlan plan;
+    if (!qmoe::fused_decode_plan(s, gate_t, up_t, down_t, su->num_sms, &plan))
+        return QMOE_ERR_SHAPE;                 // only the fused decode shapes are served
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned* bar = reinterpret_cast<unsigned*>(su->scratch);
+    int* status = reinterpret_cast<int*>(su->scratch + 128);
+    float* logits = reinterpret_cast<float*>(su->scratch + NA_HEAD);
+    float* act = logits + NA_LOGITS;
+    // the scratch keeps the previous call's contents: the barrier counters and
+    // the status word must start at zero
+    if (cudaMemsetAsync(su->scratch, 0, NA_HEAD, st) != cudaSuccess) return QMOE_ERR_CUDA;
+    cudaError_t e = qmoe::launch_fused_decode(
+        s, plan, hidden_in, nullptr, nullptr, router_w, static_cast<const uint8_t*>(gate_exps),
+        static_cast<const uint8_t*>(up_exps), static_cast<const uint8_t*>(down_exps), hidden_out,
+        nullptr, nullptr, logits, act, bar, status, st);
+    return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
+}

@@ -24,6 +24,9 @@ struct qmoe_ctx {
     float* hout;      // [T][H]
     int* status;      // device status word
     unsigned* bar;    // grid-barrier counters of the fused kernel
+    __half* xp;       // [P][H] fp16 gathered x (prefill)
+    __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
+    int32_t* inv_pos; // [P] pair -> position in the expert-sorted list
     int num_sms;
     // decode-step scratch
     float* xs;        // [H] normed hidden
@@ -60,7 +63,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xs, q, kv, att, attn_part, total;
+        status, bar, xp, actp, inv_pos, xs, q, kv, att, attn_part, total;
     int attn_splits;
 };
 
@@ -102,6 +105,9 @@ Layout layout(const qmoe_config* c) {
     L.hout = take(sizeof(float) * T * H);
     L.status = take(sizeof(int) * 16);
     L.bar = take(sizeof(unsigned) * 16);
+    L.xp = take(sizeof(__half) * P * H);
+    L.actp = take(sizeof(__half) * P * F);
+    L.inv_pos = take(sizeof(int32_t) * P);
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
     L.attn_splits = c->max_ctx > 0 ? (c->max_ctx + 255) / 256 : 0;
     L.xs = take(sizeof(float) * H);
@@ -146,6 +152,19 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
     }
     cudaError_t e = qmoe::launch_route(s, x, router_w, bias, c->route, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    if (qmoe::prefill_supported(s, gt, ut, dt)) {
+        // many tokens: grouped GEMMs on the tensor cores
+        e = qmoe::launch_prefill(s, x, res ? res : x, static_cast<const uint8_t*>(gate),
+                                 static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down),
+                                 dt, c->route, c->xp, c->actp, c->y, c->inv_pos, out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "prefill launch");
+        if (ids_out || w_out) {
+            e = qmoe::copy_route_out(s, c->route, ids_out, w_out, c->stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
+        }
+        c->err[0] = 0;
+        return QMOE_OK;
+    }
     e = qmoe::launch_gateup(s, x, static_cast<const uint8_t*>(gate), gt,
                             static_cast<const uint8_t*>(up), ut, c->route, c->act, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "gate/up launch");
@@ -242,6 +261,9 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->hout = reinterpret_cast<float*>(b + L.hout);
     c->status = reinterpret_cast<int*>(b + L.status);
     c->bar = reinterpret_cast<unsigned*>(b + L.bar);
+    c->xp = reinterpret_cast<__half*>(b + L.xp);
+    c->actp = reinterpret_cast<__half*>(b + L.actp);
+    c->inv_pos = reinterpret_cast<int32_t*>(b + L.inv_pos);
     c->xs = reinterpret_cast<float*>(b + L.xs);
     c->q = reinterpret_cast<float*>(b + L.q);
     c->kv = reinterpret_cast<float*>(b + L.kv);

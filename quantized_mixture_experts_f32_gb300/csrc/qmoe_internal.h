@@ -1,5 +1,6 @@
 // qmoe_internal.h -- launchers shared between the C-ABI layer and the kernels.
 #pragma once
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,5 +72,12 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
 
 int fused_threads();
 cudaError_t fused_prepare();
+
+// Prefill path (T > 8): tcgen05 grouped GEMMs with on-the-fly dequantisation.
+bool prefill_supported(const MoeShape& s, int gate_t, int up_t, int down_t);
+cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
+                           const uint8_t* gate, const uint8_t* up, const uint8_t* down, int down_t,
+                           const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
+                           float* out, cudaStream_t st);
 
 }  // namespace qmoe

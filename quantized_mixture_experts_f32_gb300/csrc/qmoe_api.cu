@@ -109,7 +109,7 @@ Layout layout(const qmoe_config* c) {
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
-    L.attn_splits = c->max_ctx > 0 ? (c->max_ctx + 255) / 256 : 0;
+    L.attn_splits = c->max_ctx > 0 ? qmoe::attn_splits(c->max_ctx) : 0;
     L.xs = take(sizeof(float) * H);
     L.q = take(sizeof(float) * (qd ? qd : 1));
     L.kv = take(sizeof(float) * (2 * kvd + 1));
@@ -352,8 +352,56 @@ qmoe_status qmoe_forward_host(qmoe_ctx* c, const float* hin, const float* router
 qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int n_layers, int pos,
                              float* hidden, int32_t* ids_out) {
     if (!c) return QMOE_ERR_INVALID_ARG;
-    (void)layers; (void)n_layers; (void)pos; (void)hidden; (void)ids_out;
-    return fail(c, QMOE_ERR_INVALID_ARG, "decode step is not available in this build");
+    const qmoe_config& k = c->cfg;
+    if (k.n_heads < 1 || k.max_ctx < 1)
+        return fail(c, QMOE_ERR_INVALID_ARG, "context was created without attention geometry");
+    if (!layers || n_layers < 1 || !hidden)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null layers / hidden or n_layers < 1");
+    if (pos < 0 || pos >= k.max_ctx)
+        return fail(c, QMOE_ERR_SHAPE, "pos=%d outside 0..max_ctx-1=%d", pos, k.max_ctx - 1);
+    if (!aligned16(hidden)) return fail(c, QMOE_ERR_MISALIGNED, "hidden must be 16-byte aligned");
+    for (int l = 0; l < n_layers; ++l) {
+        const qmoe_layer_weights& w = layers[l];
+        if (!w.attn_norm || !w.wq || !w.wk || !w.wv || !w.wo || !w.q_norm || !w.k_norm ||
+            !w.ffn_norm || !w.router_w || !w.gate_exps || !w.up_exps || !w.down_exps ||
+            !w.k_cache || !w.v_cache)
+            return fail(c, QMOE_ERR_INVALID_ARG, "layer %d: null pointer", l);
+        if (!aligned16(w.wq) || !aligned16(w.wk) || !aligned16(w.wv) || !aligned16(w.wo) ||
+            !aligned16(w.router_w) || !aligned16(w.gate_exps) || !aligned16(w.up_exps) ||
+            !aligned16(w.down_exps) || !aligned16(w.k_cache) || !aligned16(w.v_cache) ||
+            !aligned16(w.attn_norm) || !aligned16(w.ffn_norm))
+            return fail(c, QMOE_ERR_MISALIGNED, "layer %d: a base pointer is not 16-byte aligned", l);
+        if (!valid_qtype(w.down_t))
+            return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "layer %d: down qtype %d", l, (int)w.down_t);
+    }
+    qmoe::AttnShape a{k.hidden, k.n_heads, k.n_kv_heads, k.head_dim, k.max_ctx, pos, k.rms_eps,
+                      k.rope_base};
+    for (int l = 0; l < n_layers; ++l) {
+        const qmoe_layer_weights& w = layers[l];
+        qmoe::LayerAttn la{w.attn_norm,
+                           static_cast<const uint8_t*>(w.wq),
+                           static_cast<const uint8_t*>(w.wk),
+                           static_cast<const uint8_t*>(w.wv),
+                           static_cast<const uint8_t*>(w.wo),
+                           w.q_norm,
+                           w.k_norm,
+                           static_cast<__half*>(w.k_cache),
+                           static_cast<__half*>(w.v_cache)};
+        // B1-B7: h += Wo attn(...)
+        cudaError_t e = qmoe::launch_attention_block(a, la, hidden, c->xs, c->q, c->kv, c->att,
+                                                     c->attn_part, hidden, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
+        // B8: x2 = RMSNorm(h) * ffn_norm
+        e = qmoe::launch_rmsnorm(hidden, w.ffn_norm, k.rms_eps, k.hidden, c->xs, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "ffn norm launch");
+        // B9: h = h + MoE(x2)
+        qmoe_status st = run_moe(c, c->xs, hidden, nullptr, w.router_w, w.gate_exps, w.up_exps,
+                                 w.down_exps, QMOE_Q4_K, QMOE_Q4_K, w.down_t, 1, hidden,
+                                 ids_out ? ids_out + (size_t)l * k.top_k : nullptr, nullptr);
+        if (st != QMOE_OK) return st;
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
 }
 
 qmoe_status qmoe_get_status(qmoe_ctx* c) {

@@ -73,6 +73,30 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
 int fused_threads();
 cudaError_t fused_prepare();
 
+// Attention half of a decoder layer at decode time (batch 1).
+struct AttnShape {
+    int H, nq, nkv, hd, max_ctx, pos;
+    float eps, rope_base;
+};
+struct LayerAttn {
+    const float* attn_norm;
+    const uint8_t* wq;
+    const uint8_t* wk;
+    const uint8_t* wv;
+    const uint8_t* wo;
+    const float* q_norm;
+    const float* k_norm;
+    __half* k_cache;
+    __half* v_cache;
+};
+// h_out = h + Wo attn(RoPE(norm(Wq x)), cache), x = RMSNorm(h); writes slot pos
+cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const float* h,
+                                   float* xs, float* q, float* kv, float* att, float* part,
+                                   float* h_out, cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* h, const float* w, float eps, int n, float* out,
+                           cudaStream_t st);
+int attn_splits(int max_ctx);
+
 // Prefill path (T > 8): tcgen05 grouped GEMMs with on-the-fly dequantisation.
 bool prefill_supported(const MoeShape& s, int gate_t, int up_t, int down_t);
 cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,

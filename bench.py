@@ -1,26 +1,29 @@
 """Benchmark: qwen3moe MoE-FFN tokens/s/layer and expert-weight HBM GB/s on GB300.
 
-Workload: one Qwen3-30B-A3B MoE layer at decode (hidden 2048, 128 experts,
-top-8 renormalised, expert FFN 768, one token, Q4_K gate/up, Q6_K down),
-seeded synthetic weights.  A step is one full MoE-FFN layer call for one token
-(router, top-k, per-expert pair lists, gate/up + SwiGLU, down, weighted
-combine into the residual) through the C ABI.
+Default workload (``--workload decode``): one Qwen3-30B-A3B MoE layer at decode
+(hidden 2048, 128 experts, top-8 renormalised, expert FFN 768, one token, Q4_K
+gate/up, Q6_K down) on seeded synthetic weights.  A step is one full MoE-FFN
+layer call (router, top-k, per-expert pair lists, gate/up + SwiGLU, down,
+weighted combine into the residual) through the C ABI.  Other workloads:
+``batch8`` (8 tokens, Q4_K down), ``prefill`` (512 tokens, biased router, the
+tensor-core path) and ``step48`` (a full 48-layer decode step at context 4096).
 
 Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and a device synchronise, timed with CUDA events on the
-launching stream.  Every step reads a different device copy of the layer's
-weights; the copies rotate over more than 4x the L2 size, so weight bytes come
-from HBM.  ``value`` = tokens/s/layer summed over ranks (each rank runs its own
-replica; weak scaling).
+launching stream.  Every step reads a different device copy of the weights and
+the copies together touch more than 4x the L2 size, so weight bytes come from
+HBM.  ``value`` is summed over ranks (each rank runs its own replica).
 
-``--impl reference`` times the CPU oracle (the reference arm of this repo) on
-the same workload and unit.
+``--impl reference`` times the CPU oracle (the reference arm) on the same
+workload and unit.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -33,22 +36,45 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-WORKLOAD_CFG = 2
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "qwen3moe MoE-FFN tokens/s/layer; expert-weight HBM GB/s vs GB300 peak"
+
+WORKLOADS = {
+    "decode": dict(cfg=2, copies=32, e2e=2000, steps=20000, warmup=200,
+                   desc="qwen3moe-30b-a3b MoE layer decode, T=1, Q4_K gate/up, Q6_K down"),
+    "batch8": dict(cfg=3, copies=6, e2e=500, steps=4000, warmup=40,
+                   desc="qwen3moe-30b-a3b MoE layer decode batch, T=8, Q4_K gate/up, Q4_K down"),
+    "prefill": dict(cfg=4, copies=3, e2e=20, steps=300, warmup=6,
+                    desc="qwen3moe-30b-a3b MoE layer prefill, T=512, biased router, Q6_K down"),
+    "step48": dict(cfg=None, copies=1, e2e=10, steps=400, warmup=3,
+                   desc="qwen3moe-30b-a3b 48-layer decode step, T=1, context 4096"),
+}
+
+# kernels whose summary under profiles/ carries a DRAM traffic figure
+PROFILE_FOR = {"decode": "moe_decode_fused_decode_T1.md", "batch8": None, "prefill": None,
+               "step48": None}
+FUSED_SOURCES = ["moe_decode_fused.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--copies", type=int, default=32, help="weight copies in the rotation")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--copies", type=int, default=None, help="weight copies in the rotation")
+    ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    a = ap.parse_args()
+    w = WORKLOADS[a.workload]
+    a.steps = w["steps"] if a.steps is None else a.steps
+    a.warmup = w["warmup"] if a.warmup is None else a.warmup
+    a.copies = w["copies"] if a.copies is None else a.copies
+    a.e2e_steps = w["e2e"] if a.e2e_steps is None else a.e2e_steps
+    return a
 
 
 def peaks():
@@ -57,11 +83,36 @@ def peaks():
         try:
             j = json.load(open(p))
             hbm = j.get("hbm_gbs") or j.get("hbm_GBps")
+            tf = j.get("bf16_tflops")
             if hbm:
-                return float(hbm), "measured", j
+                return float(hbm), float(tf) if tf else FALLBACK_BF16_TFLOPS, "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback", None
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def fused_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        h.update(open(os.path.join(ROOT, "quantized_mixture_experts_f32_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    name = PROFILE_FOR.get(workload)
+    if not name:
+        return None
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+    if not m_src or not m_tr or m_src.group(1) != fused_source_hash():
+        return None
+    return int(m_tr.group(1))
 
 
 class ClockSampler:
@@ -122,34 +173,109 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def algorithmic_bytes(inp, ids) -> dict:
-    """Bytes the method must read: the distinct selected experts' gate+up+down slices."""
-    H, F = inp["H"], inp["F"]
-    per = (synth.matrix_bytes(inp["gate_t"], F, H) + synth.matrix_bytes(inp["up_t"], F, H)
-           + synth.matrix_bytes(inp["down_t"], H, F))
-    distinct = len(np.unique(ids))
-    return dict(expert=distinct * per, router=inp["E"] * H * 4,
-                act=inp["T"] * H * 4 * 2, distinct=distinct)
+def expert_bytes(H, F, gate_t, up_t, down_t):
+    return (synth.matrix_bytes(gate_t, F, H) + synth.matrix_bytes(up_t, F, H)
+            + synth.matrix_bytes(down_t, H, F))
 
 
-def cpu_baseline(inp, seconds: float) -> dict:
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_sample_layer(inp, seconds: float, max_tokens: int):
+    """The oracle on a bounded sample of the layer workload: tokens/s/layer."""
     import oracle
     oracle.build()
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    T = inp["T"]
+    n = min(T, max_tokens)
     one = dict(inp)
+    one["x"] = inp["x"][:n]
+    one["T"] = n
     done, t0 = 0, time.perf_counter()
-    rng = np.random.default_rng(123)
     while True:
-        one["x"] = rng.standard_normal((1, inp["H"])).astype(np.float32)
         oracle.moe_forward(one)
         done += 1
         el = time.perf_counter() - t0
-        if el >= seconds and done >= 3:
+        if el >= seconds and done >= 1:
             break
-    return {"value": done / el, "unit": "tokens/s/layer", "cores": cores, "kind": "oracle",
-            "sample": f"{done} single-token MoE-FFN layer calls of the decode workload "
-                      f"(router + top-8 + 8 experts in double), {el:.1f} s"}
+        if el >= 3 * seconds:
+            break
+    return done * n / el, f"{done} oracle calls of {n} tokens of this layer workload, {el:.1f} s"
 
+
+def cpu_sample_step(geo, seconds: float):
+    import oracle
+    oracle.build()
+    h = synth.step_input(geo).astype(np.float64)
+    pos = geo["ctx"] - 1
+    layers, t0 = 0, time.perf_counter()
+    while True:
+        small = synth.step_layer_small(geo, layers)
+        ex = synth.step_layer_experts(geo, layers)
+        tl = time.perf_counter()
+        r = oracle.decode_layer(geo, small, ex, h, pos)
+        h = r["h"]
+        layers += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or layers >= geo["n_layers"]:
+            break
+    return layers / el, f"{layers} oracle decoder layers of the 48-layer step (context 4096), {el:.1f} s"
+
+
+def cores():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    budget = 150.0
+    if w["cfg"] is not None:
+        inp = synth.moe_inputs(synth.MOE_CONFIGS[w["cfg"]])
+        sample = min(inp["T"], 8)
+        one = dict(inp)
+        one["x"] = inp["x"][:sample]
+        one["T"] = sample
+        step = lambda: oracle.moe_forward(one)  # noqa: E731
+        tokens_per_step = sample
+        what = f"{sample} tokens of the {args.workload} layer workload per step"
+    else:
+        geo = dict(synth.STEP_DEFAULT)
+        small = synth.step_layer_small(geo, 0)
+        ex = synth.step_layer_experts(geo, 0)
+        h = synth.step_input(geo).astype(np.float64)
+        step = lambda: oracle.decode_layer(geo, small, ex, h, geo["ctx"] - 1)  # noqa: E731
+        tokens_per_step = 1
+        what = "one decoder layer of the 48-layer step per step"
+    t0 = time.perf_counter()
+    step()
+    est = time.perf_counter() - t0
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        step()
+    k = max(3, min(args.steps, int(budget / max(est, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(k):
+        step()
+    el = time.perf_counter() - t0
+    val = k * tokens_per_step / el
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s/layer",
+            "n_gpus": args.gpus, "steps": k, "requested_steps": args.steps, "warmup": warm,
+            "ms_per_step": 1000 * el / k, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w["desc"]},
+            "cpu_baseline": {"value": val, "unit": "tokens/s/layer", "cores": cores(),
+                             "kind": "oracle",
+                             "sample": f"{k} steps of {what} (steps capped to ~{budget:.0f} s)"},
+            "e2e": {"value": val, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
 
 def dist_init():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -157,127 +283,49 @@ def dist_init():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     pg = None
     if ws > 1:
-        import torch.distributed as dist
         import torch
+        import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
         pg = dist
     return ws, rank, local, pg
 
 
-def run_reference(args):
-    ws, rank, local, pg = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None
-    if rank != 0:
-        return 0
-    import oracle
-    oracle.build()
-    cfg = synth.MOE_CONFIGS[WORKLOAD_CFG]
-    inp = synth.moe_inputs(cfg)
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    rng = np.random.default_rng(7)
-    xs = [rng.standard_normal((1, inp["H"])).astype(np.float32) for _ in range(8)]
-
-    def step(i):
-        one = dict(inp)
-        one["x"] = xs[i % len(xs)]
-        oracle.moe_forward(one)
-
-    t0 = time.perf_counter()
-    step(0)
-    est = time.perf_counter() - t0
-    warm = min(args.warmup, 2)
-    for i in range(warm):
-        step(i)
-    budget = 150.0
-    k = max(3, min(args.steps, int(budget / max(est, 1e-6))))
-    t0 = time.perf_counter()
-    for i in range(k):
-        step(i)
-    el = time.perf_counter() - t0
-    val = k / el
-    line = {"impl": "reference", "metric": "qwen3moe MoE-FFN tokens/s/layer", "value": val,
-            "unit": "tokens/s/layer", "n_gpus": args.gpus, "steps": k, "requested_steps": args.steps,
-            "warmup": warm, "ms_per_step": 1000 * el / k, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "qwen3moe-30b-a3b MoE layer decode, T=1, Q4_K gate/up, Q6_K down",
-                       "hidden": 2048, "n_experts": 128, "top_k": 8, "ffn": 768, "tokens": 1},
-            "cpu_baseline": {"value": val, "unit": "tokens/s/layer", "cores": cores,
-                             "kind": "oracle",
-                             "sample": f"{k} single-token layer calls (steps capped to ~{budget:.0f} s)"},
-            "e2e": {"value": val, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
-
-
-def main():
-    args = parse()
-    if args.impl == "reference":
-        return run_reference(args)
-    import torch
-    ws, rank, local, pg = dist_init()
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
-    import quantized_mixture_experts_f32_gb300 as q
-
-    cfg = synth.MOE_CONFIGS[WORKLOAD_CFG]
-    inp = synth.moe_inputs(cfg)
-    T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
-    gt, ut, dt = q.QTYPE[inp["gate_t"]], q.QTYPE[inp["up_t"]], q.QTYPE[inp["down_t"]]
-    x = torch.from_numpy(inp["x"]).to(dev)
-    base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev)
-            for n in ("router", "gate", "up", "down")}
-    R = args.copies
-    copies = [base] + [{n: t.clone() for n, t in base.items()} for _ in range(R - 1)]
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    out = torch.empty((T, H), dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(dev)
-    ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream))
-
-    def call(c):
-        q.qmoe_forward(ctx, x, c["router"], c["gate"], c["up"], c["down"], gt, ut, dt, T, out)
-
-    # routing of this input (same for every copy): for the algorithmic bytes
-    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index):
+    """Capture one graph over the rotation of `calls`, replay for exactly
+    `steps` steps after `warmup`; returns (ms, clocks)."""
+    R = len(calls)
     with torch.cuda.stream(stream):
-        q.qmoe_forward_ex(ctx, x, None, None, base["router"], base["gate"], base["up"],
-                          base["down"], gt, ut, dt, T, out, ids, None)
-    stream.synchronize()
-    ab = algorithmic_bytes(inp, ids.cpu().numpy())
-    touched = (ab["expert"] + ab["router"]) * R
-
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            call(copies[i % R])
+        for i in range(min(3, R)):
+            calls[i]()
         stream.synchronize()
         g_full = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_full, stream=stream):
-            for i in range(R):
-                call(copies[i])
-        rem = args.steps % R
+            for c in calls:
+                c()
+        rem = steps % R
         g_rem = None
         if rem:
             g_rem = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_rem, stream=stream):
-                for i in range(rem):
-                    call(copies[i])
-        # warm-up: W steps
-        for _ in range(args.warmup // R):
+                for c in calls[:rem]:
+                    c()
+        for _ in range(warmup // R):
             g_full.replay()
-        for i in range(args.warmup % R):
-            call(copies[i])
+        for c in calls[:warmup % R]:
+            c()
         stream.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(sampler_index)
     sampler.start()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps // R):
+        for _ in range(steps // R):
             g_full.replay()
         if g_rem is not None:
             g_rem.replay()
@@ -293,18 +341,46 @@ def main():
         tt = torch.tensor([ms], device=dev)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         ms = float(tt.item())
-    secs = ms / 1e3
-    tokens = T * args.steps * ws
-    value = tokens / secs
-    step_s = secs / args.steps
-    gbs = ab["expert"] / step_s / 1e9
+    return ms, clocks
 
-    # e2e: the public host-buffer entry point, copies + sync inside every step
+
+def bench_layer(args, torch, q, dev, stream, ws, pg, local):
+    w = WORKLOADS[args.workload]
+    inp = synth.moe_inputs(synth.MOE_CONFIGS[w["cfg"]])
+    T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
+    gt, ut, dt = q.QTYPE[inp["gate_t"]], q.QTYPE[inp["up_t"]], q.QTYPE[inp["down_t"]]
+    x = torch.from_numpy(inp["x"]).to(dev)
+    bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev)
+    base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev)
+            for n in ("router", "gate", "up", "down")}
+    R = args.copies
+    copies = [base] + [{n: t.clone() for n, t in base.items()} for _ in range(R - 1)]
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream))
+
+    def mk(c):
+        return lambda: q.qmoe_forward_ex(ctx, x, None, bias, c["router"], c["gate"], c["up"],
+                                         c["down"], gt, ut, dt, T, out)
+
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        q.qmoe_forward_ex(ctx, x, None, bias, base["router"], base["gate"], base["up"],
+                          base["down"], gt, ut, dt, T, out, ids, None)
+    stream.synchronize()
+    distinct = len(np.unique(ids.cpu().numpy()))
+    ebytes = distinct * expert_bytes(H, F, inp["gate_t"], inp["up_t"], inp["down_t"])
+    rbytes = E * H * 4
+    ms, clocks = timed_graphs(torch, stream, [mk(c) for c in copies], args.steps, args.warmup,
+                              pg, dev, local)
+    secs = ms / 1e3
+    step_s = secs / args.steps
+    # e2e: host buffers through qmoe_forward_host (copies + sync inside every step)
     hin = torch.from_numpy(inp["x"].copy()).pin_memory()
     hout = torch.empty_like(hin).pin_memory()
-    for i in range(5):
-        q.qmoe_forward_host(ctx, hin, copies[i % R]["router"], copies[i % R]["gate"],
-                            copies[i % R]["up"], copies[i % R]["down"], gt, ut, dt, T, hout)
+    for i in range(3):
+        c = copies[i % R]
+        q.qmoe_forward_host(ctx, hin, c["router"], c["gate"], c["up"], c["down"], gt, ut, dt, T,
+                            hout)
     if pg:
         pg.barrier()
     te0 = time.perf_counter()
@@ -317,36 +393,164 @@ def main():
         tt = torch.tensor([te], device=dev)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         te = float(tt.item())
-    e2e_val = T * args.e2e_steps * ws / te
+    q.qmoe_destroy(ctx)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = (ebytes + rbytes) * R
+    res = dict(
+        value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
+        ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
+        e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
+        launches=(q.LAUNCHES_PER_DECODE_FORWARD if T <= 8 else q.LAUNCHES_PER_PREFILL_FORWARD),
+        config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
+                "tokens": T, "distinct_experts": distinct,
+                "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
+                      f"per rotation vs L2 {l2 / 1e6:.0f} MB"},
+        kernel=("moe_decode_fused (the whole layer is one kernel)" if T <= 8
+                else "whole layer call (routing, gather, grouped GEMMs, combine)"))
+    if T > 8:
+        flops = T * K * 2 * (2 * F * H + H * F)
+        res["tensor_tflops"] = flops / step_s / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        val, sample = cpu_sample_layer(inp, args.cpu_seconds, 8 if T <= 8 else 16)
+        cpu = {"value": val, "unit": "tokens/s/layer", "cores": cores(), "kind": "oracle",
+               "sample": sample}
+    return res, cpu
 
-    peak, peak_kind, _ = peaks()
-    roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-            "peak_kind": peak_kind, "traffic": None,
-            "kernel": "whole MoE-FFN layer call (all kernels of one step)",
-            "algorithmic_bytes_per_launch": ab["expert"]}
+
+def bench_step48(args, torch, q, dev, stream, ws, pg, local):
+    geo = dict(synth.STEP_DEFAULT)
+    L, H, E, K, F = geo["n_layers"], geo["H"], geo["E"], geo["K"], geo["F"]
+    pos = geo["ctx"] - 1
+    keep, structs = [], []
+    ebytes = attn_bytes = kv_bytes = rbytes = 0
+    for l in range(L):
+        small = synth.step_layer_small(geo, l)
+        ex = synth.step_layer_experts(geo, l)
+        d = {}
+        for n in ("attn_norm", "q_norm", "k_norm", "ffn_norm", "router", "wq", "wk", "wv", "wo"):
+            d[n] = torch.from_numpy(np.ascontiguousarray(small[n])).to(dev)
+        for n in ("k_cache", "v_cache"):
+            d[n] = torch.from_numpy(np.ascontiguousarray(small[n]).view(np.uint16)).to(dev)
+        for n in ("gate", "up", "down"):
+            d[n] = torch.from_numpy(ex[n]).to(dev)
+        keep.append(d)
+        structs.append(q.qmoe_layer_weights(
+            d["attn_norm"].data_ptr(), d["wq"].data_ptr(), d["wk"].data_ptr(), d["wv"].data_ptr(),
+            d["wo"].data_ptr(), d["q_norm"].data_ptr(), d["k_norm"].data_ptr(),
+            d["ffn_norm"].data_ptr(), d["router"].data_ptr(), d["gate"].data_ptr(),
+            d["up"].data_ptr(), d["down"].data_ptr(), q.QTYPE[small["down_t"]],
+            d["k_cache"].data_ptr(), d["v_cache"].data_ptr()))
+        attn_bytes += sum(small[n].nbytes for n in ("wq", "wk", "wv", "wo"))
+        kv_bytes += 2 * geo["n_kv"] * (pos + 1) * geo["head_dim"] * 2
+        rbytes += small["router"].nbytes
+        per = expert_bytes(H, F, "Q4_K", "Q4_K", small["down_t"])
+        del ex
+        keep[-1]["_per"] = per
+    arr = (q.qmoe_layer_weights * L)(*structs)
+    h0 = torch.from_numpy(synth.step_input(geo)).to(dev)
+    hidden = torch.empty_like(h0)
+    ids = torch.empty((L, K), dtype=torch.int32, device=dev)
+    ctx = q.qmoe_create(q.make_config(H, E, K, F, 1, 1, stream.cuda_stream, n_heads=geo["n_heads"],
+                                      n_kv_heads=geo["n_kv"], head_dim=geo["head_dim"],
+                                      max_ctx=geo["ctx"], rope_base=geo["rope_base"],
+                                      rms_eps=geo["eps"]))
+    with torch.cuda.stream(stream):
+        hidden.copy_(h0)
+        q.qmoe_decode_step(ctx, arr, L, pos, hidden, ids)
+    stream.synchronize()
+    idn = ids.cpu().numpy()
+    for l in range(L):
+        ebytes += len(np.unique(idn[l])) * keep[l]["_per"]
+
+    def step():
+        hidden.copy_(h0)
+        q.qmoe_decode_step(ctx, arr, L, pos, hidden)
+
+    ms, clocks = timed_graphs(torch, stream, [step], args.steps, args.warmup, pg, dev, local)
+    secs = ms / 1e3
+    step_s = secs / args.steps
+    hin = torch.from_numpy(synth.step_input(geo)).pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    if pg:
+        pg.barrier()
+    te0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        with torch.cuda.stream(stream):
+            hidden.copy_(hin, non_blocking=True)
+            q.qmoe_decode_step(ctx, arr, L, pos, hidden)
+            hout.copy_(hidden, non_blocking=True)
+        stream.synchronize()
+    te = time.perf_counter() - te0
+    q.qmoe_destroy(ctx)
+    res = dict(
+        value=L * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
+        ebytes=ebytes, other_bytes=attn_bytes + kv_bytes + rbytes,
+        e2e=L * args.e2e_steps * ws / te, h2d=H * 4, d2h=H * 4,
+        launches=L * q.LAUNCHES_PER_DECODE_LAYER,
+        config={"workload": WORKLOADS["step48"]["desc"], "hidden": H, "n_experts": E,
+                "top_k": K, "ffn": F, "layers": L, "context": geo["ctx"], "tokens": 1,
+                "l2": f"one step touches {(ebytes + attn_bytes + kv_bytes + rbytes) / 1e9:.2f} GB "
+                      "vs a 136 MB L2"},
+        kernel="whole 48-layer decode step",
+        tokens_per_s=args.steps * ws / secs,
+        bytes_split={"experts": ebytes, "attention_weights": attn_bytes, "kv_cache": kv_bytes,
+                     "routers": rbytes})
+    cpu = None
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        val, sample = cpu_sample_step(geo, args.cpu_seconds)
+        cpu = {"value": val, "unit": "tokens/s/layer", "cores": cores(), "kind": "oracle",
+               "sample": sample}
+    return res, cpu
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    ws, rank, local, pg = dist_init()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import quantized_mixture_experts_f32_gb300 as q
+    stream = torch.cuda.Stream(dev)
+    if args.workload == "step48":
+        res, cpu = bench_step48(args, torch, q, dev, stream, ws, pg, local)
+    else:
+        res, cpu = bench_layer(args, torch, q, dev, stream, ws, pg, local)
+    hbm, tf, kind = peaks()
+    step_s = res["step_s"]
+    gbs = res["ebytes"] / step_s / 1e9
+    all_gbs = (res["ebytes"] + res["other_bytes"]) / step_s / 1e9
+    traffic = profiled_traffic(args.workload)
+    roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+            "peak_kind": kind, "traffic": traffic, "kernel": res["kernel"],
+            "algorithmic_bytes_per_launch": res["ebytes"],
+            "achieved_all_bytes": all_gbs, "frac_all_bytes": all_gbs / hbm,
+            "frac_of_nominal_8tbs": gbs / 8000.0}
     line = {
-        "metric": "qwen3moe MoE-FFN tokens/s/layer; expert-weight HBM GB/s vs GB300 peak",
-        "value": value, "unit": "tokens/s/layer", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "qwen3moe-30b-a3b MoE layer decode, T=1, Q4_K gate/up, Q6_K down",
-                   "hidden": H, "n_experts": E, "top_k": K, "ffn": F, "tokens": T,
-                   "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
-                         f"per rotation vs L2 {l2 / 1e6:.0f} MB",
-                   "parallelism": f"replicas x{ws}"},
-        "expert_weight_gbs": gbs,
-        "expert_bytes_per_step": ab["expert"], "router_bytes_per_step": ab["router"],
-        "roofline": roof,
-        "e2e": {"value": e2e_val, "unit": "tokens/s/layer",
-                "h2d_bytes_per_step": T * H * 4, "d2h_bytes_per_step": T * H * 4},
-        "gpu_launches": args.steps * q.LAUNCHES_PER_DECODE_FORWARD,
-        "clocks": clocks,
+        "metric": METRIC, "value": res["value"], "unit": "tokens/s/layer", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(res["config"], parallelism=f"replicas x{ws}"),
+        "expert_weight_gbs": gbs, "roofline": roof,
+        "e2e": {"value": res["e2e"], "unit": "tokens/s/layer", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": args.steps * res["launches"],
+        "clocks": res["clocks"],
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if "tensor_tflops" in res:
+        line["dtype"] = "f16 tensor-core operands, f32 accumulate"
+        line["tensor"] = {"achieved_tflops": res["tensor_tflops"], "peak_tflops": tf,
+                          "frac": res["tensor_tflops"] / tf, "peak_kind": kind}
+    if "bytes_split" in res:
+        line["tokens_per_s"] = res["tokens_per_s"]
+        line["bytes_per_step"] = res["bytes_split"]
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
-    q.qmoe_destroy(ctx)
     if pg:
         pg.destroy_process_group()
     return 0

@@ -5,10 +5,12 @@
 // section "Gaps ... G3": router = F32 GEMV of ffn_gate_inp [E x H]; softmax,
 // top-8 and renorm (planned device kernel K1 in G8).  Everything stays on the
 // device: no logits copy, no host sync, so the layer is graph-capturable.
+#include <climits>
 #include <float.h>
 #include <math.h>
 
 #include "kquant.cuh"
+
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -55,6 +57,16 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ x
     }
 }
 
+// Integer key with the order of the float comparison (-0 folded into +0); NaN
+// gets an extreme key, so the ranks in this file stay a permutation whatever the input.
+__device__ __forceinline__ int order_key(float v) {
+    const int b = __float_as_int(v + 0.f);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+
+// the map is its own inverse
+__device__ __forceinline__ float key_value(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+
 constexpr int TK_MAXV = 32;   // logits per lane (E <= 1024)
 
 // Per token (one warp): top-K of the F32 logits (ties -> lower index), softmax
@@ -72,19 +84,20 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
     const int nwarps = blockDim.x >> 5;
     const int nv = (E + 31) / 32;
     for (int t = warp; t < T; t += nwarps) {
-        float v[TK_MAXV];
+        int v[TK_MAXV];                           // order keys; INT_MIN pads
 #pragma unroll
         for (int i = 0; i < TK_MAXV; ++i) {
             const int e = lane + 32 * i;
-            v[i] = (i < nv && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+            v[i] = (i < nv && e < E) ? order_key(logits[(size_t)t * E + e]) : INT_MIN;
         }
         uint32_t taken = 0u;                      // bit i: v[i] selected
         float vmax = 0.f, psel = 0.f;
         int sel_id[16];
         float sel_v[16];
         for (int j = 0; j < K; ++j) {
-            // lane-local best among not-taken (ascending index order inside a lane)
-            float bv = -INFINITY;
+            // lane-local best among not-taken (ascending index order inside a lane);
+            // (key, lower index) is a total order, so every lane agrees on the result
+            int bv = INT_MIN;
             int bi = 0x7fffffff;
 #pragma unroll
             for (int i = 0; i < TK_MAXV; ++i) {
@@ -94,20 +107,20 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int ov = __shfl_xor_sync(0xffffffffu, bv, o);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
                 if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
             }
             if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
             sel_id[j] = bi;
-            sel_v[j] = bv;
-            if (j == 0) vmax = bv;
+            sel_v[j] = key_value(bv);
+            if (j == 0) vmax = sel_v[0];
         }
         float z = 0.f;
 #pragma unroll
         for (int i = 0; i < TK_MAXV; ++i) {
             const int e = lane + 32 * i;
-            if (i < nv && e < E) z += expf(v[i] - vmax);
+            if (i < nv && e < E) z += expf(key_value(v[i]) - vmax);
         }
         z = warp_sum(z);
         for (int j = 0; j < K; ++j) psel += expf(sel_v[j] - vmax) / z;
@@ -169,7 +182,207 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
     }
 }
 
+// ---------------------------------------------------------------------------- many tokens
+
+constexpr int RG_T = 64, RG_E = 64, RG_K = 128;    // router tile: tokens x experts x k-slice
+constexpr int RG_THREADS = 256;                    // 4 tokens x 4 experts per thread
+constexpr int RG_LD = RG_K + 4;                    // padded smem row (floats)
+
+// Split-k router GEMM: part[z][t][e] = sum over k in slice z of X[t][k] Wr[e][k].
+// Slices are summed in a fixed order by topk_rank, so the result is deterministic.
+// Grid (ceil(E/64), ceil(T/64), H/128); H is a multiple of 128.
+__global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restrict__ x,
+                                                          const float* __restrict__ wr, int T,
+                                                          int H, int E,
+                                                          float* __restrict__ part) {
+    extern __shared__ float4 rg_smem4[];
+    float* xs = reinterpret_cast<float*>(rg_smem4);              // [RG_T][RG_LD]
+    float* ws = xs + RG_T * RG_LD;                               // [RG_E][RG_LD]
+    const int e0 = blockIdx.x * RG_E, t0 = blockIdx.y * RG_T, k0 = blockIdx.z * RG_K;
+    const int tid = threadIdx.x;
+    // 64 rows x 32 float4 per operand, 8 float4 per thread each, all in flight
+    float4 vx[8], vw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int f = tid + i * RG_THREADS, r = f >> 5, c = (f & 31) * 4;
+        vx[i] = t0 + r < T ? __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + r) * H + k0 + c))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        vw[i] = e0 + r < E ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + r) * H + k0 + c))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int f = tid + i * RG_THREADS, r = f >> 5, c = (f & 31) * 4;
+        *reinterpret_cast<float4*>(xs + r * RG_LD + c) = vx[i];
+        *reinterpret_cast<float4*>(ws + r * RG_LD + c) = vw[i];
+    }
+    __syncthreads();
+    const int tx = tid & 15, ty = tid >> 4;      // experts tx + 16j, tokens ty + 16i
+    float acc[4][4] = {};
+#pragma unroll 4
+    for (int k = 0; k < RG_K; k += 4) {
+        float4 a[4], w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(xs + (ty + 16 * i) * RG_LD + k);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const float4*>(ws + (tx + 16 * j) * RG_LD + k);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[i][j] = fmaf(a[i].x, w[j].x, acc[i][j]);
+                acc[i][j] = fmaf(a[i].y, w[j].y, acc[i][j]);
+                acc[i][j] = fmaf(a[i].z, w[j].z, acc[i][j]);
+                acc[i][j] = fmaf(a[i].w, w[j].w, acc[i][j]);
+            }
+    }
+    float* dst = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = t0 + ty + 16 * i, e = e0 + tx + 16 * j;
+            if (t < T && e < E) dst[(size_t)t * E + e] = acc[i][j];
+        }
+}
+
+// one warp per token: rank every logit (ties: lower index first), keep the top
+// K in descending order, softmax over E, renormalise over the selection
+__global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part, int S,
+                                                 const float* __restrict__ bias, int T, int E,
+                                                 int K, int norm, float* __restrict__ logits,
+                                                 int32_t* __restrict__ ids,
+                                                 float* __restrict__ wts) {
+    extern __shared__ float lsm[];                 // 8 warps x (E logits + 16 selection slots)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    float* l = lsm + warp * (E + 16);
+    int* sel = reinterpret_cast<int*>(l + E);
+    for (int e = lane; e < E; e += 32) {
+        float v = 0.f;
+        for (int z = 0; z < S; ++z) v += part[((size_t)z * T + t) * E + e];
+        v += bias ? bias[e] : 0.f;
+        l[e] = v;
+        logits[(size_t)t * E + e] = v;
+    }
+    if (lane < 16) reinterpret_cast<int*>(l + E)[lane] = 0;
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) {
+        const int v = order_key(l[e]);
+        int rank = 0;
+        for (int e2 = 0; e2 < E; ++e2) {
+            const int w = order_key(l[e2]);
+            rank += (w > v) || (w == v && e2 < e);
+        }
+        if (rank < K) sel[rank] = e;
+    }
+    __syncwarp();
+    const float vmax = l[sel[0]];
+    float z = 0.f;
+    for (int e = lane; e < E; e += 32) z += expf(l[e] - vmax);
+    z = warp_sum(z);
+    const int id = lane < K ? sel[lane] : 0;
+    const float pj = lane < K ? expf(l[id] - vmax) / z : 0.f;
+    const float psel = warp_sum(pj);
+    if (lane < K) {
+        ids[(size_t)t * K + lane] = id;
+        wts[(size_t)t * K + lane] = norm ? pj / psel : pj;
+    }
+}
+
+// One CTA: pairs p = t*K + j sorted by (expert, p).  A token selects an expert
+// at most once, so the rank of pair (t, e) inside expert e's list is the number
+// of earlier tokens that selected e: a popcount prefix over a per-expert token
+// bitmap.  Also emits the used-expert list.
+__global__ void __launch_bounds__(1024) sort_pairs(const int32_t* __restrict__ ids, int T, int E,
+                                                   int K, int32_t* __restrict__ n_used,
+                                                   int32_t* __restrict__ used_expert,
+                                                   int32_t* __restrict__ used_first,
+                                                   int32_t* __restrict__ pair_list) {
+    extern __shared__ uint32_t bm[];               // E * W bitmap words, then counts, offsets
+    const int W = (T + 31) / 32;
+    int32_t* counts = reinterpret_cast<int32_t*>(bm + (size_t)E * W);
+    int32_t* offs = counts + E;
+    const int P = T * K;
+    for (int i = threadIdx.x; i < E * W; i += blockDim.x) bm[i] = 0u;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p], t = p / K;
+        atomicOr(&bm[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+        atomicAdd(&counts[e], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int run = 0, used = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = e < E ? counts[e] : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const uint32_t nz = __ballot_sync(0xffffffffu, c > 0);
+            if (e < E) offs[e] = run + incl - c;
+            if (c > 0) {
+                const int slot = used + __popc(nz & ((1u << lane) - 1u));
+                used_expert[slot] = e;
+                used_first[slot] = run + incl - c;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+            used += __popc(nz);
+        }
+        if (lane == 0) { *n_used = used; used_first[used] = P; }
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int e = ids[p], t = p / K;
+        const uint32_t* row = bm + (size_t)e * W;
+        int r = __popc(row[t >> 5] & ((1u << (t & 31)) - 1u));
+        for (int w = 0; w < (t >> 5); ++w) r += __popc(row[w]);
+        pair_list[offs[e] + r] = p;
+    }
+}
+
+constexpr size_t kSortSmemMax = 200 * 1024;
+
+size_t sort_pairs_smem(int T, int E) {
+    return sizeof(uint32_t) * (size_t)E * ((T + 31) / 32) + sizeof(int32_t) * 2 * E;
+}
+
 }  // namespace
+
+cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* router_w,
+                              const float* bias, const Route& r, cudaStream_t st) {
+    const size_t rg_smem = sizeof(float) * (RG_T + RG_E) * RG_LD;
+    dim3 g1((s.E + RG_E - 1) / RG_E, (s.T + RG_T - 1) / RG_T, s.H / RG_K);
+    router_gemm<<<g1, RG_THREADS, rg_smem, st>>>(x, router_w, s.T, s.H, s.E, r.logits_part);
+    topk_rank<<<(s.T + 7) / 8, 256, sizeof(float) * 8 * (s.E + 16), st>>>(
+        r.logits_part, s.H / RG_K, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts);
+    sort_pairs<<<1, 1024, sort_pairs_smem(s.T, s.E), st>>>(r.ids, s.T, s.E, s.K, r.n_used, r.used_expert, r.used_first,
+                                    r.pair_list);
+    return cudaGetLastError();
+}
+
+size_t route_many_part_floats(int T, int H, int E) { return (size_t)(H / RG_K) * T * E; }
+
+bool route_many_supported(const MoeShape& s, const Route& r) {
+    return r.logits_part && s.H % RG_K == 0 && sort_pairs_smem(s.T, s.E) <= kSortSmemMax;
+}
+
+// Raise the dynamic shared-memory limits once per device context.
+cudaError_t route_prepare() {
+    cudaError_t e = cudaFuncSetAttribute(router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(float) * (RG_T + RG_E) * RG_LD));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sort_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSortSmemMax);
+    return e;
+}
 
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
                          const float* bias, const Route& r, cudaStream_t st) {

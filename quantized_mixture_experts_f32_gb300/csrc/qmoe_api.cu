@@ -63,7 +63,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, xs, q, kv, att, attn_part, total;
+        status, bar, xp, actp, inv_pos, logits_part, xs, q, kv, att, attn_part, total;
     int attn_splits;
 };
 
@@ -108,6 +108,7 @@ Layout layout(const qmoe_config* c) {
     L.xp = take(sizeof(__half) * P * H);
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
+    L.logits_part = take(sizeof(float) * qmoe::route_many_part_floats((int)T, (int)H, (int)E));
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
     L.attn_splits = c->max_ctx > 0 ? qmoe::attn_splits(c->max_ctx) : 0;
     L.xs = take(sizeof(float) * H);
@@ -150,9 +151,11 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
         c->err[0] = 0;
         return QMOE_OK;
     }
-    cudaError_t e = qmoe::launch_route(s, x, router_w, bias, c->route, c->stream);
+    const bool many = qmoe::prefill_supported(s, gt, ut, dt) && qmoe::route_many_supported(s, c->route);
+    cudaError_t e = many ? qmoe::launch_route_many(s, x, router_w, bias, c->route, c->stream)
+                         : qmoe::launch_route(s, x, router_w, bias, c->route, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
-    if (qmoe::prefill_supported(s, gt, ut, dt)) {
+    if (many) {
         // many tokens: grouped GEMMs on the tensor cores
         e = qmoe::launch_prefill(s, x, res ? res : x, static_cast<const uint8_t*>(gate),
                                  static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down),
@@ -235,6 +238,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
         return QMOE_ERR_CUDA;
     }
     e = qmoe::fused_prepare();
+    if (e == cudaSuccess) e = qmoe::route_prepare();
     if (e != cudaSuccess) {
         fprintf(stderr, "qmoe_create: fused kernel set-up: %s\n", cudaGetErrorString(e));
         delete c;
@@ -255,6 +259,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.used_expert = reinterpret_cast<int32_t*>(b + L.used_expert);
     c->route.used_first = reinterpret_cast<int32_t*>(b + L.used_first);
     c->route.pair_list = reinterpret_cast<int32_t*>(b + L.pair_list);
+    c->route.logits_part = reinterpret_cast<float*>(b + L.logits_part);
     c->act = reinterpret_cast<float*>(b + L.act);
     c->y = reinterpret_cast<float*>(b + L.y);
     c->hin = reinterpret_cast<float*>(b + L.hin);

@@ -19,6 +19,7 @@ struct Route {
     int32_t* used_expert; // [E]
     int32_t* used_first;  // [E+1]
     int32_t* pair_list;   // [T*K]
+    float* logits_part;   // [H/128][T][E] split-k router partials (many-token path), or null
 };
 
 struct MoeShape {
@@ -29,6 +30,14 @@ struct MoeShape {
 // A1 + A2 + A3: router logits, softmax / top-k / renorm, per-expert pair lists.
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
                          const float* bias, const Route& r, cudaStream_t st);
+
+// The same for many tokens (tiled router GEMM, per-token rank top-k, bitmap
+// stable sort); requires route_many_supported().
+cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* router_w,
+                              const float* bias, const Route& r, cudaStream_t st);
+bool route_many_supported(const MoeShape& s, const Route& r);
+size_t route_many_part_floats(int T, int H, int E);
+cudaError_t route_prepare();
 
 // A4 + A5: act[p][f] = silu(Wg_e x_t)[f] * (Wu_e x_t)[f] for every pair p.
 cudaError_t launch_gateup(const MoeShape& s, const float* x, const uint8_t* gate, int gate_t,

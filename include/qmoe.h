@@ -206,6 +206,14 @@ const char* qmoe_last_error(qmoe_ctx* ctx);
 /* Bytes of workspace a context with this config allocates (0 on bad config). */
 size_t qmoe_workspace_bytes(const qmoe_config* cfg);
 
+/* 1 when qmoe_forward / qmoe_forward_ex on this context would run a layer of
+ * n_tokens tokens with these expert qtypes as the single fused decode kernel
+ * (one launch: router, top-k, gate/up, SwiGLU, down and combine), 0 when it
+ * would take the multi-kernel path (tensor-core prefill or the SIMT path).
+ * Pure host query; no device work. */
+int qmoe_fused_decode_available(const qmoe_ctx* ctx, int n_tokens, qmoe_qtype gate_t,
+                                qmoe_qtype up_t, qmoe_qtype down_t);
+
 /* Byte stride between consecutive experts of a 3-D expert tensor whose
  * matrices have `rows` outputs and `cols` inputs (0 on bad arguments). */
 size_t qmoe_expert_stride(qmoe_qtype qtype, int rows, int cols);

@@ -35,7 +35,8 @@ LAUNCHES_PER_DECODE_LAYER = 8
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
-            "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc"]
+            "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
+            "qmoe_fused_decode_available"]
 
 
 class qmoe_config(C.Structure):
@@ -87,6 +88,8 @@ def _load():
     L.qmoe_last_error.restype = C.c_char_p
     L.qmoe_workspace_bytes.argtypes = [C.POINTER(qmoe_config)]
     L.qmoe_workspace_bytes.restype = C.c_size_t
+    L.qmoe_fused_decode_available.argtypes = [vp, i, i, i, i]
+    L.qmoe_fused_decode_available.restype = i
     L.qmoe_expert_stride.argtypes = [i, i, i]
     L.qmoe_expert_stride.restype = C.c_size_t
     L.qmoe_forward_noalloc.argtypes = [fp, fp, vp, vp, vp, i, i, i, i, i, i, i, i, i, fp, vp]
@@ -176,6 +179,10 @@ def qmoe_last_error(ctx) -> str:
 
 def qmoe_workspace_bytes(cfg: qmoe_config) -> int:
     return lib.qmoe_workspace_bytes(C.byref(cfg))
+
+
+def qmoe_fused_decode_available(ctx, n_tokens: int, gate_t: int, up_t: int, down_t: int) -> bool:
+    return bool(lib.qmoe_fused_decode_available(ctx, n_tokens, gate_t, up_t, down_t))
 
 
 def qmoe_expert_stride(qtype: int, rows: int, cols: int) -> int:

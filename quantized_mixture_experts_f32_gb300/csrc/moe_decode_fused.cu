@@ -9,22 +9,28 @@
 // launches per expert for the weighted sum; here the layer is one launch with
 // no host involvement and is graph-capturable.
 //
-// Structure (G CTAs of 16 warps):
+// Structure (G CTAs of 16 warps, all co-resident: cooperative launch).  Values
+// that cross CTAs travel as 64-bit words {value, launch tag}: a reader polls
+// until the word carries this launch's tag, so no grid barrier, fence or
+// counter sits between the phases (the tag is one more than the one the last
+// CTA of the previous launch published).
 //  A  every CTA stages x in shared memory; CTA c computes the router logits of
-//     experts c, c+G, ... (fixed-order reductions) -> grid barrier 1.
-//  B  every CTA redoes the (cheap, deterministic) top-k of all T tokens and
-//     builds the same per-expert pair lists; it then owns a contiguous share of
-//     the (expert, f) gate/up rows and a contiguous range of down rows of every
-//     used expert, cut into chunks of a few KB.
+//     experts c, c+G, ... (fixed-order reductions) and stores them tagged.
+//  B  every CTA waits for the T*E logits, redoes the (cheap, deterministic)
+//     top-k of all T tokens and builds the same per-expert pair lists; it then
+//     owns a contiguous share of the (expert, f) gate/up rows and a contiguous
+//     share of the used experts' down rows (rows weighted by 1 + the expert's
+//     pair count, so a few experts at most), cut into chunks of a few KB.
 //  C  warp w handles chunks w, w+16, ... and streams them itself with bulk async
-//     copies (TMA) into its two shared-memory slots, one chunk ahead of the one
-//     it computes (one issuing thread per CTA cannot keep HBM busy; sixteen
-//     can).  Gate/up chunks produce act[p][f] = silu(g)*u (fp32); a warp's
-//     first down chunks are already in flight while it finishes gate/up.
-//  -  grid barrier 2 (all act written).
-//  D  down chunks: y = Wd_e act for this CTA's rows of every used expert, then
-//     out[t][h] = res[t][h] + sum_j w[t][j] y_j[h] in slot order j = 0..K-1
-//     (deterministic, no atomics on values).
+//     copies (TMA) into its ring slots, several chunks ahead of the one it
+//     computes (one issuing thread per CTA cannot keep HBM busy; sixteen can).
+//     Gate/up chunks produce act[p][f] = silu(g)*u, stored tagged; the down
+//     chunks are already in flight meanwhile.
+//  D  the CTA waits for act of its down experts only, then y[p][h] = Wd_e act
+//     for its down rows, stored tagged.
+//  E  CTA c owns out rows [H*c/G, H*(c+1)/G): out[t][h] = res[t][h] + sum_j
+//     w[t][j] y[t*K+j][h] in slot order j = 0..K-1 (deterministic, no atomics
+//     on values).
 // Every wait is bounded (%globaltimer); on expiry the kernel records
 // QMOE_ERR_TIMEOUT, stops computing, drains its own copies and exits.
 #include <math.h>
@@ -52,29 +58,33 @@ namespace {
 
 constexpr int NCW = 16;                     // warps; each streams its own chunks
 constexpr int NTHREADS = NCW * 32;
-constexpr int NSLOT = 2 * NCW;              // two ring slots per warp
+constexpr int NSMAX = 8;                    // ring slots per warp, at most
+constexpr int NSLOT = NSMAX * NCW;
 constexpr int MAXT = 8;
 constexpr int MAXP = 128;
 
 // misc int slots
-enum { M_NUSED = 0, M_NCH, M_NGU, M_GUDONE, M_ABORT, M_H0, M_NROWS, M_GULO, M_NRC, M_GUWARPS,
-       M_COUNT = 16 };
+constexpr int MAXSEG = 8;                   // experts a CTA's down rows may span
+enum { M_NUSED = 0, M_NCH, M_NGU, M_ABORT, M_GULO, M_TAG, M_NSEG, M_QBASE, M_NLOC,
+       M_SEG = 16,                          // + 4*s: expert slot u, first row, rows, first chunk
+       M_COUNT = M_SEG + 4 * MAXSEG };
 
 struct SmemLayout {
     int off_bar, off_misc, off_red, off_ids, off_wts, off_used, off_first, off_pairs,
-        off_x, off_xsum, off_xscale, off_ybuf, off_ring, total, slot_bytes, rows_max, act_stage;
+        off_x, off_xsum, off_xscale, off_ring, total, slot_bytes, ns, asum_off;
 };
 
 __host__ __device__ inline int al(int v, int a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, int rows_max,
-                                                   int slot_bytes, int asum_bytes, bool stage_act) {
+// nloc_max: pairs of the experts one CTA's down rows can touch
+__host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, int nloc_max,
+                                                   int slot_bytes, int ns) {
     SmemLayout L;
     const int P = T * K;
-    // the x region is reused in the down phase for the act group sums and,
-    // when it fits, a copy of act itself
-    const int act_bytes = stage_act ? P * F * 4 : 0;
-    asum_bytes = al(asum_bytes, 16) + act_bytes;
+    // after gate/up the x region holds act of this CTA's down experts and the
+    // group sums of act (groups of 8 or 16; sized for 8)
+    const int act_bytes = al(nloc_max * F * 4, 16);
+    const int asum_bytes = al(nloc_max * (F / 8) * 4, 16);
     int o = 0;
     L.off_bar = o;      o += NSLOT * 8;
     L.off_misc = o;     o += M_COUNT * 4;
@@ -85,16 +95,15 @@ __host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, i
     L.off_first = o;    o += al(P + 1, 4) * 4;
     L.off_pairs = o;    o += al(P, 4) * 4;
     o = al(o, 16);
-    L.off_x = o;        o += al(T * H * 4 > asum_bytes ? T * H * 4 : asum_bytes, 16);
+    L.off_x = o;        o += al(T * H * 4 > act_bytes + asum_bytes ? T * H * 4 : act_bytes + asum_bytes, 16);
     L.off_xsum = o;     o += al(T * (H / 16) * 4, 16);
     L.off_xscale = o;   o += al(T * (H / 16) * 4, 16);
-    L.off_ybuf = o;     o += al(P * rows_max * 4, 16);
     o = al(o, 128);
-    L.off_ring = o;     o += NSLOT * slot_bytes;
+    L.off_ring = o;     o += NCW * ns * slot_bytes;
     L.total = o;
     L.slot_bytes = slot_bytes;
-    L.rows_max = rows_max;
-    L.act_stage = act_bytes ? al(asum_bytes - act_bytes, 16) : -1;   // byte offset in the x region
+    L.ns = ns;
+    L.asum_off = act_bytes;
     return L;
 }
 
@@ -109,11 +118,13 @@ struct FusedParams {
     float* out;
     int32_t* ids_out;
     float* w_out;
-    float* logits;
-    float* act;
-    unsigned* bar;
+    unsigned long long* lg;     // [T][E] tagged router logits
+    unsigned long long* act;    // [P][F] tagged silu(g)*u
+    unsigned long long* y;      // [P][H] tagged down outputs
+    unsigned long long* xflag;  // [G] tagged "x staged" marks (only when out aliases x)
+    unsigned* ctl;              // [0] exit counter, [1] tag of the last completed launch
     int* status;
-    int T, H, E, K, F, norm;
+    int T, H, E, K, F, norm, x_alias;
     int cf;          // f rows per gate/up chunk (divides F)
     SmemLayout L;
 };
@@ -121,6 +132,39 @@ struct FusedParams {
 // ----------------------------------------------------------------------------- small helpers
 
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// N tagged values base[first + z*stride] (those below n): all loads in flight
+// together, then the ones not yet carrying `tag` are reloaded together until
+// they do (bounded).  Missing values read as 0; false if the wait timed out.
+template <int N>
+__device__ __forceinline__ bool load_tagged(const unsigned long long* base, int n, int first,
+                                            int stride, unsigned tag, float (&v)[N]) {
+    uint32_t pend = 0u;                                   // bit z: value z still to come
+#pragma unroll
+    for (int z = 0; z < N; ++z) {
+        v[z] = 0.f;
+        if (first + z * stride < n) pend |= 1u << z;
+    }
+    unsigned long long t0 = 0ull;
+    for (int round = 0; pend; ++round) {
+        if (round == 1) t0 = globaltimer();
+        if (round > 1) {
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+            __nanosleep(32);
+        }
+        unsigned long long w[N];
+#pragma unroll
+        for (int z = 0; z < N; ++z)
+            w[z] = (pend >> z) & 1u ? ld_relaxed_u64(base + first + z * stride) : 0ull;
+#pragma unroll
+        for (int z = 0; z < N; ++z)
+            if (((pend >> z) & 1u) && (unsigned)(w[z] >> 32) == tag) {
+                v[z] = __uint_as_float((unsigned)w[z]);
+                pend &= ~(1u << z);
+            }
+    }
+    return true;
+}
 
 // 8 bytes at an even shared-memory address (three aligned words, funnel shift)
 __device__ __forceinline__ uint2 lds8_a2(const uint8_t* p) {
@@ -201,6 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     constexpr int BBD = DQT == 1 ? Q4K_BYTES : Q6K_BYTES;
     constexpr int RBD = NSB_D * BBD;                              // down row bytes
     constexpr int NTG = (8 * NSB_G + 31) / 32;                    // gate/up tasks per lane
+    constexpr int GS = DQT == 1 ? 16 : 8;                         // act group of one down scale
 
     uint64_t* fullb = reinterpret_cast<uint64_t*>(sm + L.off_bar);
     int* misc = reinterpret_cast<int*>(sm + L.off_misc);
@@ -214,11 +259,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     float* xsum = reinterpret_cast<float*>(sm + L.off_xsum);
     float* xscale = reinterpret_cast<float*>(sm + L.off_xscale);
     int32_t* xq = reinterpret_cast<int32_t*>(x_s);                 // byte planes, after the router
-    float* ybuf = reinterpret_cast<float*>(sm + L.off_ybuf);
+    float* act_s = x_s;                                            // after gate/up: act, group sums
+    float* asum = reinterpret_cast<float*>(sm + L.off_x + L.asum_off);
     uint8_t* ring = sm + L.off_ring;
     const int SB = L.slot_bytes;
+    const int NS = L.ns;
 
-    // ---------------- phase A: stage x, barriers, router slice
+    // ---------------- phase A: stage x, router slice -> tagged logits
     if (tid == 0) QMOE_TRACE(0);
     // this warp's router columns of the first expert row, loaded before x so
     // that both loads are in flight together
@@ -233,11 +280,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     for (int i = tid; i < T * H / 4; i += NTHREADS)
         reinterpret_cast<float4*>(x_s)[i] = __ldg(reinterpret_cast<const float4*>(p.x) + i);
     if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) mbar_init(&fullb[s], 1);
+        for (int s = 0; s < NCW * NS; ++s) mbar_init(&fullb[s], 1);
         for (int i = 0; i < M_COUNT; ++i) misc[i] = 0;
+        misc[M_TAG] = (int)(ld_acquire_gpu(p.ctl + 1) + 1u);   // this launch's tag
         fence_barrier_init();
     }
     __syncthreads();
+    const unsigned tag = (unsigned)misc[M_TAG];
+    if (p.x_alias && tid == 0) st_relaxed_u64(p.xflag + c, tag_pack(0.f, tag));   // x is staged
     for (int i = tid; i < T * (H / 16); i += NTHREADS) {
         const float4* q = reinterpret_cast<const float4*>(x_s + 16 * i);
         float s = 0.f;
@@ -282,7 +332,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         if (tid < T) {
             float s = 0.f;
             for (int w = 0; w < NCW; ++w) s += red[w * MAXT + tid];
-            p.logits[(size_t)tid * E + e] = s + (p.bias ? p.bias[e] : 0.f);
+            st_relaxed_u64(p.lg + (size_t)tid * E + e, tag_pack(s + (p.bias ? p.bias[e] : 0.f), tag));
         }
         __syncthreads();
     }
@@ -334,28 +384,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             }
         }
     }
-    if (tid == 0) {
-        QMOE_TRACE(1);
-        grid_arrive(&p.bar[0]);
-        if (!grid_wait(&p.bar[0], (unsigned)G)) {
+    if (tid == 0) QMOE_TRACE(1);
+
+    // ---------------- phase B: routing (identical in every CTA).  Wait for all
+    // logits of this launch, rank every logit, then in parallel the softmax
+    // weights (warp t), each pair's place in the expert-sorted pair list
+    // (threads 256..) and, in the last warp, the used-expert list and this
+    // CTA's share of the work, so that the weight copies start right after.
+    float* lg_s = reinterpret_cast<float*>(ring);                 // ring is idle until phase C
+    int32_t* sel = reinterpret_cast<int32_t*>(lg_s + T * E);      // [T][K]
+    {
+        constexpr int LPT = 2;                                     // logits per thread (T*E <= 1024)
+        float v[LPT];
+        if (!load_tagged<LPT>(p.lg, T * E, tid, NTHREADS, tag, v)) {
             set_status(p.status, ST_TIMEOUT);
             misc[M_ABORT] = 1;
         }
+#pragma unroll
+        for (int z = 0; z < LPT; ++z)
+            if (tid + z * NTHREADS < T * E) lg_s[tid + z * NTHREADS] = v[z];
     }
-    __syncthreads();
-
-    // ---------------- phase B: routing (identical in every CTA), all threads in
-    // parallel: rank of every logit, softmax weights, pairs sorted by expert
-    if (tid == 0) QMOE_TRACE(2);
-    const bool abort_b = misc[M_ABORT] != 0;
-    float* lg_s = reinterpret_cast<float*>(ring);                 // ring is idle until phase C
-    int32_t* sel = reinterpret_cast<int32_t*>(lg_s + T * E);      // [T][K]
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(sel + P);      // used experts, E <= 1024
-    int32_t* se = reinterpret_cast<int32_t*>(bitmap + 32);        // experts in pair order
-    for (int i = tid; i < T * E; i += NTHREADS) lg_s[i] = __ldcg(p.logits + i);
-    if (tid < 32) bitmap[tid] = 0u;
     for (int i = tid; i < P; i += NTHREADS) sel[i] = 0;
     __syncthreads();
+    if (tid == 0) QMOE_TRACE(2);
+    const bool abort_b = misc[M_ABORT] != 0;
     if (!abort_b) {
         // rank of every logit among its token's E (ties: lower index first);
         // tpe consecutive lanes share one logit's E comparisons
@@ -391,8 +443,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     }
     if (tid == 0) QMOE_TRACE(11);
     __syncthreads();
-    // softmax weights (warp t) and, in parallel, each pair's place in the
-    // expert-sorted pair list (threads 256.. ; ids are the selection itself)
     if (!abort_b && warp < T) {
         const float* l = lg_s + warp * E;
         const float vmax = l[sel[warp * K]];
@@ -422,45 +472,109 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             pos += (e2 < e) || (e2 == e && q < pt);
         }
         pairs[pos] = pt;
-        se[pos] = e;
-        atomicOr(&bitmap[e >> 5], 1u << (e & 31));
-    }
-    __syncthreads();
-    if (tid == 0) QMOE_TRACE(12);
-    if (!abort_b && tid < P) {
-        const int e = se[tid];
-        if (tid == 0 || se[tid - 1] != e) {
-            int u = __popc(bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-            for (int w = 0; w < (e >> 5); ++w) u += __popc(bitmap[w]);
-            used_e[u] = e;
-            used_first[u] = tid;
-        }
     }
     if (warp == NCW - 1) {
-        int nu = __popc(bitmap[lane]);
-        for (int o = 16; o > 0; o >>= 1) nu += __shfl_xor_sync(0xffffffffu, nu, o);
-        if (abort_b) nu = 0;
-        if (lane == 0) {
-            misc[M_NUSED] = nu;
-            used_first[nu] = P;
-            // Work of this CTA, in closed form.  Gate/up: the used experts' f rows
-            // are cut into global chunks of CF consecutive f (CF divides F); CTA c
-            // owns global chunks [c*NG/G, (c+1)*NG/G).  Down: rows [h0, h1) of
-            // every used expert, RPC rows per chunk.
-            const int CF = p.cf, CPE = F / CF;
-            const int NG = nu * CPE;                             // < 2^17, NG * G < 2^31
-            const int lo = NG * c / G, hi = NG * (c + 1) / G;
-            const int h0 = H * c / G, h1 = H * (c + 1) / G;
-            const int RPC = (SB - 32) / RBD;
-            const int nrc = (h1 - h0 + RPC - 1) / RPC;
-            misc[M_GULO] = lo;
-            misc[M_NGU] = hi - lo;
-            misc[M_GUWARPS] = hi - lo < NCW ? hi - lo : NCW;      // warps with gate/up work
-            misc[M_NRC] = nrc;
-            misc[M_NCH] = (hi - lo) + nu * nrc;
-            misc[M_H0] = h0;
-            misc[M_NROWS] = h1 - h0;
-            if (hi - lo == 0) grid_arrive(&p.bar[1]);
+        // used experts in ascending id order: lane owns bitmap word `lane` (E <= 1024)
+        uint32_t word = 0u;
+        if (!abort_b)
+            for (int q = 0; q < P; ++q) {
+                int e = sel[q];
+                e = (e < 0 || e >= E) ? 0 : e;
+                if ((e >> 5) == lane) word |= 1u << (e & 31);
+            }
+        const int cw = __popc(word);
+        int incl = cw;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        const int nu = __shfl_sync(0xffffffffu, incl, 31);
+        int u = incl - cw;
+        for (uint32_t w = word; w; w &= w - 1u) used_e[u++] = lane * 32 + __ffs(w) - 1;
+        __syncwarp();
+        // first pair of used expert u = number of pairs with a smaller expert id
+        for (int uu = lane; uu < nu; uu += 32) {
+            const int e = used_e[uu];
+            int before = 0;
+            for (int q = 0; q < P; ++q) {
+                int e2 = sel[q];
+                e2 = (e2 < 0 || e2 >= E) ? 0 : e2;
+                before += e2 < e;
+            }
+            used_first[uu] = before;
+        }
+        if (lane == 0) used_first[nu] = P;
+        __syncwarp();
+        // Work of this CTA, in closed form.  Gate/up: the used experts' f rows
+        // are cut into global chunks of CF consecutive f (CF divides F); CTA c
+        // owns global chunks [c*NG/G, (c+1)*NG/G).  Down: the used experts'
+        // rows in expert order, each weighted by 1 + the expert's pair count
+        // (one row load, one dot product per pair); CTA c owns the rows whose
+        // weighted position falls in [c*W/G, (c+1)*W/G): a few experts at most.
+        const int RPC = (SB - 32) / RBD;
+        {
+            const long long W = (long long)H * (P + nu);
+            const long long wlo = W * c / G, whi = W * (c + 1) / G;
+            long long base = 0;
+            int nseg = 0;
+            bool over = false;
+            for (int u0 = 0; u0 < nu; u0 += 32) {
+                const int u = u0 + lane;
+                const int wu = u < nu ? used_first[u + 1] - used_first[u] + 1 : 0;
+                const long long len = (long long)H * wu;
+                long long incl = len;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                const long long U = base + incl - len;
+                const bool hit = u < nu && U < whi && U + len > wlo;
+                const uint32_t hm = __ballot_sync(0xffffffffu, hit);
+                if (hit) {
+                    const long long a = (wlo > U ? wlo : U) - U, b = (whi < U + len ? whi : U + len) - U;
+                    const int ra = (int)((a + wu - 1) / wu), rb = (int)((b + wu - 1) / wu);
+                    const int slot = nseg + __popc(hm & ((1u << lane) - 1u));
+                    if (slot < MAXSEG) {
+                        int* sg = misc + M_SEG + 4 * slot;
+                        sg[0] = u;
+                        sg[1] = ra;
+                        sg[2] = rb - ra;
+                    } else {
+                        over = true;
+                    }
+                }
+                nseg += __popc(hm);
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (over) set_status(p.status, ST_DEVICE_CHECK);      // host bound broken
+            __syncwarp();
+            if (lane == 0) {
+                misc[M_NUSED] = nu;
+                if (nseg > MAXSEG) nseg = MAXSEG;
+                int ndc = 0, keep = 0;
+                for (int sgi = 0; sgi < nseg; ++sgi) {
+                    int* sg = misc + M_SEG + 4 * sgi;
+                    if (sg[2] <= 0) continue;                     // a range too short for a row
+                    int* dst = misc + M_SEG + 4 * keep;
+                    dst[0] = sg[0]; dst[1] = sg[1]; dst[2] = sg[2];
+                    dst[3] = ndc;
+                    ndc += (dst[2] + RPC - 1) / RPC;
+                    ++keep;
+                }
+                const int CF = p.cf, CPE = F / CF;
+                const int NG = nu * CPE;                             // < 2^17, NG * G < 2^31
+                const int lo = NG * c / G, hi = NG * (c + 1) / G;
+                misc[M_GULO] = lo;
+                misc[M_NGU] = hi - lo;
+                misc[M_NCH] = (hi - lo) + ndc;
+                misc[M_NSEG] = keep;
+                const int qb = keep ? used_first[misc[M_SEG]] : 0;
+                const int qe = keep ? used_first[misc[M_SEG + 4 * (keep - 1)] + 1] : 0;
+                misc[M_QBASE] = qb;
+                misc[M_NLOC] = qe - qb;
+            }
         }
     }
     __syncthreads();
@@ -471,9 +585,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     }
     if (tid == 0) QMOE_TRACE(3);
     const int n_ch = misc[M_NCH], n_gu = misc[M_NGU];
-    const int gu_lo = misc[M_GULO], nrc = misc[M_NRC];
+    const int gu_lo = misc[M_GULO], nseg = misc[M_NSEG];
     const int CPE = F / p.cf, RPC = (SB - 32) / RBD;
-    const int H0c = misc[M_H0], H1c = H0c + misc[M_NROWS];
     // chunk k -> (is_gu, used index u, start row, row count)
     auto decode = [&](int k, int& u, int& start, int& cnt) -> bool {
         if (k < n_gu) {
@@ -484,19 +597,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             return true;
         }
         const int kd = k - n_gu;
-        u = kd / nrc;
-        start = H0c + (kd - u * nrc) * RPC;
-        cnt = min(RPC, H1c - start);
+        int sgi = 0;
+        while (sgi + 1 < nseg && misc[M_SEG + 4 * (sgi + 1) + 3] <= kd) ++sgi;
+        const int* sg = misc + M_SEG + 4 * sgi;
+        u = sg[0];
+        start = sg[1] + (kd - sg[3]) * RPC;
+        cnt = min(RPC, sg[1] + sg[2] - start);
         return false;
     };
 
     // ---------------- phases C and D: warp w streams and computes chunks w, w+16, ...
-    // chunk j of this warp lives in slot warp + 16*(j&1); it is issued two
+    // chunk j of this warp lives in slot warp + 16*(j%NS); it is issued NS
     // chunks ahead, right after the chunk that used the slot before it
     auto issue = [&](int j) {                                    // lane 0 only
         const int k = warp + NCW * j;
         if (k >= n_ch) return;
-        const int s = warp + NCW * (j & 1);
+        const int s = warp + NCW * (j % NS);
         int u, start, cnt;
         const bool is_gu = decode(k, u, start, cnt);
         const int e = used_e[u];
@@ -517,8 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         }
     };
     if (lane == 0) {
-        issue(0);
-        issue(1);
+        for (int j = 0; j < NS; ++j) issue(j);
     }
     {
         // ---------------- phase C: gate/up + SwiGLU
@@ -528,8 +643,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         int j = 0;
         for (; warp + NCW * j < n_gu; ++j) {
             const int k = warp + NCW * j;
-            const int s = warp + NCW * (j & 1);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&fullb[s], (uint32_t)(j >> 1) & 1u));
+            const int s = warp + NCW * (j % NS);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&fullb[s], (uint32_t)(j / NS) & 1u));
             if (lane == 0 && j == 0) QMOE_TRACE(32 + warp);
             if (!ok) { if (lane == 0) { set_status(p.status, ST_TIMEOUT); misc[M_ABORT] = 1; } }
             const bool run = __all_sync(0xffffffffu, ok && misc[M_ABORT] == 0);
@@ -603,64 +718,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                         m += __shfl_xor_sync(0xffffffffu, m, 2);
                         m += __shfl_xor_sync(0xffffffffu, m, 1);
                         const float upv = __shfl_down_sync(0xffffffffu, m, 16);
-                        if (lane == 0) p.act[(size_t)pr * F + f0 + i] = m / (1.f + expf(-m)) * upv;
+                        if (lane == 0)
+                            st_relaxed_u64(p.act + (size_t)pr * F + f0 + i,
+                                           tag_pack(m / (1.f + expf(-m)) * upv, tag));
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) {
                 if (warp == 0 && j == 0) QMOE_TRACE(9);
-                issue(j + 2);
+                issue(j + NS);
             }
         }
-        // this warp's act rows are written: publish them once (every writing lane
-        // fences its own stores), then count the warp in; the last warp of the
-        // CTA arrives at the grid barrier
-        if (j > 0) {
-            __threadfence();
-            __syncwarp();
-            if (lane == 0 && atomicAdd(&misc[M_GUDONE], 1) == misc[M_GUWARPS] - 1)
-                grid_arrive(&p.bar[1]);
-        }
         if (lane == 0) QMOE_TRACE(16 + warp);
-        named_bar(1, NCW * 32);
+        named_bar(1, NCW * 32);                                  // x planes no longer read
         if (tid == 0) QMOE_TRACE(4);
-        if (tid == 0 && misc[M_ABORT] == 0) {
-            if (!grid_wait(&p.bar[1], (unsigned)G)) {
+
+        // ---------------- phase D prologue: act of this CTA's down experts (all
+        // gate/up work of the grid contributes) and its group sums (8 for Q6_K,
+        // 16 for Q4_K)
+        const int qbase = misc[M_QBASE], nloc = misc[M_NLOC];
+        if (misc[M_ABORT] == 0) {
+            bool ok = true;
+            for (int i = tid; i < nloc * (F / GS); i += NCW * 32) {
+                const int lp = i / (F / GS), g = i - lp * (F / GS);
+                const int pr = pairs[qbase + lp];
+                float v[GS];
+                ok = load_tagged<GS>(p.act + (size_t)pr * F + g * GS, GS, 0, 1, tag, v) && ok;
+                float s = 0.f;
+#pragma unroll
+                for (int z = 0; z < GS; ++z) s += v[z];
+#pragma unroll
+                for (int z = 0; z < GS; z += 4)
+                    *reinterpret_cast<float4*>(act_s + (size_t)lp * F + g * GS + z) =
+                        make_float4(v[z], v[z + 1], v[z + 2], v[z + 3]);
+                asum[i] = s;
+            }
+            if (!ok) {
                 set_status(p.status, ST_TIMEOUT);
                 misc[M_ABORT] = 1;
             }
         }
         named_bar(1, NCW * 32);
-        if (tid == 0) QMOE_TRACE(5);
-
-        // ---------------- phase D prologue: group sums of act (8 for Q6_K, 16 for Q4_K)
-        constexpr int GS = DQT == 1 ? 16 : 8;
-        float* asum = x_s;                                       // x is no longer needed
-        const bool live = misc[M_ABORT] == 0;
-        float* act_s = L.act_stage >= 0 ? reinterpret_cast<float*>(sm + L.off_x + L.act_stage) : nullptr;
-        if (live)
-            for (int i = tid; i < P * (F / GS); i += NCW * 32) {
-                const float4* a4 = reinterpret_cast<const float4*>(p.act + (size_t)i * GS);
-                float s = 0.f;
-#pragma unroll
-                for (int z = 0; z < GS / 4; ++z) {
-                    const float4 q = a4[z];
-                    s += (q.x + q.y) + (q.z + q.w);
-                    if (act_s) reinterpret_cast<float4*>(act_s + (size_t)i * GS)[z] = q;
-                }
-                asum[i] = s;
-            }
-        named_bar(1, NCW * 32);
         if (tid == 0) QMOE_TRACE(6);
 
-        // ---------------- phase D: down rows of every used expert
-        const int H0 = misc[M_H0];
+        // ---------------- phase D: down rows -> tagged y
         const int rr = lane >> 3, kk = lane & 7;
         for (; warp + NCW * j < n_ch; ++j) {
             const int k = warp + NCW * j;
-            const int s = warp + NCW * (j & 1);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&fullb[s], (uint32_t)(j >> 1) & 1u));
+            const int s = warp + NCW * (j % NS);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&fullb[s], (uint32_t)(j / NS) & 1u));
             if (!ok) { if (lane == 0) { set_status(p.status, ST_TIMEOUT); misc[M_ABORT] = 1; } }
             if (__all_sync(0xffffffffu, ok && misc[M_ABORT] == 0)) {
                 int u, r0, nr;
@@ -671,8 +778,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                 const int q0 = used_first[u], q1 = used_first[u + 1];
                 for (int qi = q0; qi < q1; ++qi) {
                     const int pr = pairs[qi];
-                    const float* a = (act_s ? act_s : p.act) + (size_t)pr * F;
-                    const float* as = asum + (size_t)pr * (F / GS);
+                    const float* a = act_s + (size_t)(qi - qbase) * F;
+                    const float* as = asum + (size_t)(qi - qbase) * (F / GS);
                     for (int rb = 0; rb < nr; rb += 4) {
                         const int r = rb + rr;
                         float acc = 0.f;
@@ -733,39 +840,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                         acc += __shfl_xor_sync(0xffffffffu, acc, 4);
                         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
                         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                        if (r < nr && kk == 0) ybuf[pr * L.rows_max + (r0 - H0) + r] = acc;
+                        if (r < nr && kk == 0)
+                            st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(acc, tag));
                     }
                 }
             }
             __syncwarp();
             if (lane == 0 && warp == 0) QMOE_TRACE(15);
-            if (lane == 0) issue(j + 2);
+            if (lane == 0) issue(j + NS);
         }
         if (lane == 0) QMOE_TRACE(48 + warp);
-        named_bar(1, NCW * 32);
-        if (tid == 0) QMOE_TRACE(7);
-        // ---------------- combine into the residual
-        if (misc[M_ABORT] == 0) {
-            const int nrows = misc[M_NROWS];
-            const float* res = p.res ? p.res : p.x;
-            for (int i = tid; i < T * nrows; i += NCW * 32) {
-                const int t = i / nrows, r = i % nrows, h = H0 + r;
-                float acc = res[(size_t)t * H + h];
-                for (int jj = 0; jj < K; ++jj)
-                    acc = fmaf(wts_s[t * K + jj], ybuf[(t * K + jj) * L.rows_max + r], acc);
-                p.out[(size_t)t * H + h] = acc;
-            }
+    }
+
+    // ---------------- phase E: out rows [H*c/G, H*(c+1)/G) = residual + sum over
+    // slots j (in order) of w[t][j] * y[t*K+j]
+    if (p.x_alias) {
+        // out aliases x: every CTA must have staged x before any row is written
+        bool ok = true;
+        for (int i = tid; i < G; i += NCW * 32) {
+            float v;
+            ok = poll_tagged(p.xflag + i, tag, v) && ok;
         }
+        if (!ok) { set_status(p.status, ST_TIMEOUT); misc[M_ABORT] = 1; }
+        __syncthreads();
+    }
+    if (tid == 0) QMOE_TRACE(7);
+    if (misc[M_ABORT] == 0) {
+        const int h0 = H * c / G, nrows = H * (c + 1) / G - h0;
+        const float* res = p.res ? p.res : p.x;
+        bool ok = true;
+        for (int i = tid; i < T * nrows; i += NCW * 32) {
+            const int t = i / nrows, h = h0 + (i - t * nrows);
+            float yv[16];
+            ok = load_tagged<16>(p.y + (size_t)t * K * H + h, K * H, 0, H, tag, yv) && ok;
+            float acc = res[(size_t)t * H + h];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+                if (jj < K) acc = fmaf(wts_s[t * K + jj], yv[jj], acc);
+            p.out[(size_t)t * H + h] = acc;
+        }
+        if (!ok) set_status(p.status, ST_TIMEOUT);
     }
     __syncthreads();
     if (tid == 0) QMOE_TRACE(8);
     if (tid == 0) {
-        // the last CTA out resets the grid-barrier counters for the next launch
-        __threadfence();
-        if (atomicAdd(&p.bar[2], 1u) == (unsigned)G - 1) {
-            atomicExch(&p.bar[0], 0u);
-            atomicExch(&p.bar[1], 0u);
-            atomicExch(&p.bar[2], 0u);
+        // the last CTA out resets the exit counter and publishes this launch's
+        // tag, which the next launch increments
+        if (atomicAdd(&p.ctl[0], 1u) == (unsigned)G - 1) {
+            atomicExch(&p.ctl[0], 0u);
+            atomicExch(&p.ctl[1], tag);
         }
     }
 }
@@ -789,12 +912,14 @@ const Variant* find_variant(int H, int F, int down_t) {
     return nullptr;
 }
 
-constexpr int SLOT_BYTES_TARGET = 4608;
-
-int slot_bytes_for(int H, int F, int down_t) {
+// Ring slot size: 4608 B (two gate+up row pairs at hidden 2048); measured
+// against 2304 B slots, which put a one-token CTA's whole share in flight at
+// once but double the number of copies and chunk hand-offs.
+int slot_bytes_for(int T, int H, int F, int down_t) {
+    (void)T;
     const int rbg = (H / QK) * Q4K_BYTES;
     const int rbd = (F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    int sb = SLOT_BYTES_TARGET;
+    int sb = 4608;
     if (sb < 2 * rbg) sb = 2 * rbg;                       // at least one f per gate/up chunk
     if (sb < rbd + 32) sb = al(rbd + 32, 16);
     return al(sb, 128);
@@ -809,55 +934,84 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
     if (gate_t != 1 || up_t != 1) return false;
     const Variant* v = find_variant(s.H, s.F, down_t);
     if (!v) return false;
+    if (s.E > 1024 || s.T * s.E > 2 * NTHREADS) return false;   // logits per thread in phase B
+    if (s.T * (s.H / 16) > 2 * NTHREADS) return false;          // x byte-plane conversion share
     const int G = num_sms;
-    const int rows_max = (s.H + G - 1) / G;
-    const int sb = slot_bytes_for(s.H, s.F, down_t);
-    const int gs = down_t == 1 ? 16 : 8;
-    const int asum_bytes = s.T * s.K * (s.F / gs) * 4;
-    bool stage = true;
-    SmemLayout L = fused_layout(s.T, s.H, s.K, s.F, rows_max, sb, asum_bytes, stage);
-    if (L.total > 227 * 1024) {
-        stage = false;
-        L = fused_layout(s.T, s.H, s.K, s.F, rows_max, sb, asum_bytes, stage);
-    }
-    if (L.total > 227 * 1024) return false;
-    plan->stage_act = stage;
+    if (G < 1 || G > 1024) return false;                      // size of the "x staged" marks
+    const int P = s.T * s.K;
+    // experts (and their pairs) that one CTA's share of the down rows can touch
+    const int nu_max = s.E < P ? s.E : P;
+    // a CTA's weighted share is at most ceil(H*(P+nu)/G); an expert weighs at
+    // least 2H, so the share touches at most (P+nu)/(2G) + 2 experts
+    int span = (P + nu_max + 2 * G - 1) / (2 * G) + 2;
+    if (span > nu_max) span = nu_max;
+    if (span > MAXSEG) return false;
+    // pairs of the touched experts: the two end experts hold at most T each and
+    // the fully covered ones weigh H*(pairs+1) each, at most (P+nu)/G pairs in all
+    int nloc_max = 2 * s.T + (P + nu_max) / G + 1;
+    if (nloc_max > P) nloc_max = P;
+    const int sb = slot_bytes_for(s.T, s.H, s.F, down_t);
+    // as many ring slots per warp as fit, up to NSMAX
+    constexpr int SMEM_MAX = 227 * 1024;
+    int ns = NSMAX;
+    SmemLayout L = fused_layout(s.T, s.H, s.K, s.F, nloc_max, sb, ns);
+    while (L.total > SMEM_MAX && ns > 2) L = fused_layout(s.T, s.H, s.K, s.F, nloc_max, sb, --ns);
+    if (L.total > SMEM_MAX) return false;
+    if (s.T * s.E * 4 + P * 4 > NCW * ns * sb) return false;   // routing scratch in the ring
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    // f rows per gate/up chunk: one when a row pair is already >= 2 KB (finer
-    // split of a CTA's share over its warps), else the largest power of two
-    // that fits the slot and divides F
-    int cf = sb / (2 * rbg);
-    int p2 = 1;
-    while (p2 * 2 <= cf && s.F % (p2 * 2) == 0) p2 *= 2;
-    cf = rbg >= 1024 ? 1 : p2;
+    // f rows per gate/up chunk: the largest power of two that fits the slot and
+    // divides F
+    int cf = 1;
+    while (2 * (2 * cf) * rbg <= sb && s.F % (2 * cf) == 0) cf *= 2;
     if (cf < 1 || (sb - 32) / rbd < 1) return false;
     plan->cf = cf;
-    if (s.E > 1024) return false;
-    if (s.T * (s.H / 16) > 2 * NTHREADS) return false;       // x byte-plane conversion share
+    plan->ns = ns;
+    plan->nloc_max = nloc_max;
     plan->grid = G;
     plan->smem = L.total;
     plan->fn = v->fn;
-    plan->rows_max = rows_max;
     plan->slot_bytes = sb;
-    plan->asum_bytes = asum_bytes;
     return true;
+}
+
+size_t fused_bufs_bytes(int T, int H, int E, int K, int F, int grid) {
+    const size_t P = (size_t)T * K;
+    auto a = [](size_t v) { return (v + 255) / 256 * 256; };
+    return a(8 * (size_t)T * E) + a(8 * P * F) + a(8 * P * H) + a(8 * (size_t)grid);
+}
+
+FusedBufs fused_bufs_carve(unsigned char* base, int T, int H, int E, int K, int F, int grid,
+                           unsigned* ctl, int* status) {
+    const size_t P = (size_t)T * K;
+    auto a = [](size_t v) { return (v + 255) / 256 * 256; };
+    FusedBufs b;
+    b.lg = reinterpret_cast<unsigned long long*>(base);
+    b.act = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E));
+    b.y = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E) + a(8 * P * F));
+    b.xflag = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E) + a(8 * P * F) +
+                                                    a(8 * P * H));
+    b.ctl = ctl;
+    b.status = status;
+    return b;
 }
 
 cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const float* x,
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
-                                float* out, int32_t* ids_out, float* w_out, float* logits,
-                                float* act, unsigned* bar, int* status, cudaStream_t st) {
+                                float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
+                                cudaStream_t st) {
     FusedParams p;
     p.x = x; p.res = res; p.bias = bias; p.router = router;
     p.gate = gate; p.up = up; p.down = down;
     p.out = out; p.ids_out = ids_out; p.w_out = w_out;
-    p.logits = logits; p.act = act; p.bar = bar; p.status = status;
+    p.lg = b.lg; p.act = b.act; p.y = b.y; p.xflag = b.xflag; p.ctl = b.ctl; p.status = b.status;
     p.T = s.T; p.H = s.H; p.E = s.E; p.K = s.K; p.F = s.F; p.norm = s.norm_topk;
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), o0 = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t n = sizeof(float) * (uintptr_t)s.T * s.H;
+    p.x_alias = (x0 < o0 + n && o0 < x0 + n) ? 1 : 0;
     p.cf = plan.cf;
-    p.L = fused_layout(s.T, s.H, s.K, s.F, plan.rows_max, plan.slot_bytes, plan.asum_bytes,
-                       plan.stage_act);
+    p.L = fused_layout(s.T, s.H, s.K, s.F, plan.nloc_max, plan.slot_bytes, plan.ns);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(NTHREADS);

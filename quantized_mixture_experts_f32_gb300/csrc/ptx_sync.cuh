@@ -93,6 +93,42 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// Tagged values: a float and the tag of the launch that wrote it, in one
+// 64-bit word that is stored and loaded in one access.  A reader that sees its
+// own launch's tag has the value itself, so no fence or counter is needed to
+// pass single values between CTAs of a co-resident grid.
+__device__ __forceinline__ unsigned long long tag_pack(float v, unsigned tag) {
+    return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *p carries `tag`; false on timeout (v is then 0).
+__device__ __forceinline__ bool poll_tagged(const unsigned long long* p, unsigned tag, float& v) {
+    unsigned long long w = ld_relaxed_u64(p);
+    if ((unsigned)(w >> 32) != tag) {
+        const unsigned long long t0 = globaltimer();
+        do {
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                v = 0.f;
+                return false;
+            }
+            __nanosleep(32);
+            w = ld_relaxed_u64(p);
+        } while ((unsigned)(w >> 32) != tag);
+    }
+    v = __uint_as_float((unsigned)w);
+    return true;
+}
+
 // Grid-wide arrival: called by one thread of each CTA after its writes.
 __device__ __forceinline__ void grid_arrive(unsigned* counter) {
     __threadfence();

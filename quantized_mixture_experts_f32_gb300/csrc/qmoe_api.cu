@@ -23,7 +23,8 @@ struct qmoe_ctx {
     float* hin;       // [T][H] staging for qmoe_forward_host
     float* hout;      // [T][H]
     int* status;      // device status word
-    unsigned* bar;    // grid-barrier counters of the fused kernel
+    unsigned* bar;    // fused kernel control words (exit counter, launch tag)
+    qmoe::FusedBufs fb; // tagged values passed between the fused kernel's CTAs
     __half* xp;       // [P][H] fp16 gathered x (prefill)
     __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
     int32_t* inv_pos; // [P] pair -> position in the expert-sorted list
@@ -40,6 +41,7 @@ struct qmoe_ctx {
 namespace {
 
 constexpr int DECODE_ALIAS_MAX = 8;
+constexpr int FUSED_GRID_MAX = 1024;     // largest grid of the fused decode kernel
 
 qmoe_status fail(qmoe_ctx* c, qmoe_status s, const char* fmt, ...) {
     if (c) {
@@ -63,7 +65,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, logits_part, xs, q, kv, att, attn_part, total;
+        status, bar, xp, actp, inv_pos, logits_part, ftag, xs, q, kv, att, attn_part, total;
     int attn_splits;
 };
 
@@ -109,6 +111,8 @@ Layout layout(const qmoe_config* c) {
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
     L.logits_part = take(sizeof(float) * qmoe::route_many_part_floats((int)T, (int)H, (int)E));
+    const int Tf = (int)(T < 8 ? T : 8);                 // the fused decode kernel serves T <= 8
+    L.ftag = take(qmoe::fused_bufs_bytes(Tf, (int)H, (int)E, (int)K, (int)F, FUSED_GRID_MAX));
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
     L.attn_splits = c->max_ctx > 0 ? qmoe::attn_splits(c->max_ctx) : 0;
     L.xs = take(sizeof(float) * H);
@@ -146,7 +150,7 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
         cudaError_t e = qmoe::launch_fused_decode(
             s, plan, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
             static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out,
-            w_out, c->route.logits, c->act, c->bar, c->status, c->stream);
+            w_out, c->fb, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
         c->err[0] = 0;
         return QMOE_OK;
@@ -191,6 +195,16 @@ size_t qmoe_workspace_bytes(const qmoe_config* cfg) {
     char why[256];
     if (!config_ok(cfg, why, sizeof(why))) return 0;
     return layout(cfg).total;
+}
+
+int qmoe_fused_decode_available(const qmoe_ctx* c, int n_tokens, qmoe_qtype gate_t,
+                                qmoe_qtype up_t, qmoe_qtype down_t) {
+    if (!c || n_tokens < 1 || n_tokens > c->cfg.max_tokens) return 0;
+    if (!valid_qtype(gate_t) || !valid_qtype(up_t) || !valid_qtype(down_t)) return 0;
+    const qmoe_config& k = c->cfg;
+    qmoe::MoeShape s{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    qmoe::FusedPlan plan;
+    return qmoe::fused_decode_plan(s, gate_t, up_t, down_t, c->num_sms, &plan) ? 1 : 0;
 }
 
 size_t qmoe_expert_stride(qmoe_qtype qtype, int rows, int cols) {
@@ -266,6 +280,11 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->hout = reinterpret_cast<float*>(b + L.hout);
     c->status = reinterpret_cast<int*>(b + L.status);
     c->bar = reinterpret_cast<unsigned*>(b + L.bar);
+    {
+        const int Tf = c->cfg.max_tokens < 8 ? c->cfg.max_tokens : 8;
+        c->fb = qmoe::fused_bufs_carve(reinterpret_cast<unsigned char*>(b + L.ftag), Tf, c->cfg.hidden, c->cfg.n_experts,
+                                       c->cfg.top_k, c->cfg.ffn, FUSED_GRID_MAX, c->bar, c->status);
+    }
     c->xp = reinterpret_cast<__half*>(b + L.xp);
     c->actp = reinterpret_cast<__half*>(b + L.actp);
     c->inv_pos = reinterpret_cast<int32_t*>(b + L.inv_pos);

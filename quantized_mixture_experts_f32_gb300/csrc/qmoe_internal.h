@@ -63,12 +63,25 @@ struct FusedPlan {
     int grid;          // CTAs (one per SM, cooperative)
     int smem;          // dynamic shared memory bytes
     const void* fn;    // kernel variant
-    int rows_max;      // ceil(H / grid)
     int slot_bytes;    // ring slot size
-    int asum_bytes;    // act group-sum table size
     int cf;            // f rows per gate/up chunk
-    bool stage_act;    // act copied to shared memory for the down phase
+    int ns;            // ring slots per warp
+    int nloc_max;      // pairs of the experts one CTA's down rows can touch
 };
+
+// Values passed between the CTAs of the fused kernel, each tagged with its
+// launch (zero-initialised once; never shared with other kernels).
+struct FusedBufs {
+    unsigned long long* lg;     // [T][E] router logits
+    unsigned long long* act;    // [T*K][F] silu(gate)*up
+    unsigned long long* y;      // [T*K][H] down outputs
+    unsigned long long* xflag;  // [grid] "x staged" marks
+    unsigned* ctl;              // [0] exit counter, [1] tag of the last launch
+    int* status;
+};
+size_t fused_bufs_bytes(int T, int H, int E, int K, int F, int grid);
+FusedBufs fused_bufs_carve(unsigned char* base, int T, int H, int E, int K, int F, int grid,
+                           unsigned* ctl, int* status);
 
 bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int num_sms,
                        FusedPlan* plan);
@@ -76,8 +89,8 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
 cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const float* x,
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
-                                float* out, int32_t* ids_out, float* w_out, float* logits,
-                                float* act, unsigned* bar, int* status, cudaStream_t st);
+                                float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
+                                cudaStream_t st);
 
 int fused_threads();
 cudaError_t fused_prepare();

@@ -6,10 +6,12 @@
 // process), or run latency-critical loops in which a cudaMalloc, with its
 // implicit device synchronisation, is not acceptable after start-up.  For them
 // this entry point needs no context and performs no allocation: the scratch of
-// the fused decode kernel (router logits, SwiGLU activations, grid-barrier
-// counters and the device status word) lives in one file-scope device array of
-// fixed size, which every GPU that loads this library keeps until the process
-// exits.
+// the fused decode kernel (the tagged router logits, SwiGLU activations and
+// down outputs it passes between CTAs, its two control words and the device
+// status word) lives in one file-scope device array of fixed size, which every
+// GPU that loads this library keeps until the process exits.  The array starts
+// zeroed with the module and the control words carry over from call to call
+// (they count launches), so only the status word is cleared per call.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -19,11 +21,10 @@
 
 namespace {
 
-// Capacity of the shared scratch (elements).
-constexpr size_t NA_LOGITS = 8 * 1024;        // n_tokens * n_experts
-constexpr size_t NA_ACT = 64 * 1024;          // n_tokens * top_k * ffn
-constexpr size_t NA_HEAD = 256;               // barrier counters + status word (bytes)
-constexpr size_t NA_BYTES = NA_HEAD + (NA_LOGITS + NA_ACT) * sizeof(float);
+// Capacity of the shared scratch (bytes).
+constexpr size_t NA_HEAD = 256;               // control words at 0, status word at 128
+constexpr size_t NA_TAGGED = 2u << 20;        // tagged logits, act, down outputs, marks
+constexpr size_t NA_BYTES = NA_HEAD + NA_TAGGED;
 
 constexpr int NA_MAX_DEVICES = 64;
 
@@ -62,10 +63,6 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
     if (!aligned16(hidden_in) || !aligned16(router_w) || !aligned16(gate_exps) ||
         !aligned16(up_exps) || !aligned16(down_exps) || !aligned16(hidden_out))
         return QMOE_ERR_MISALIGNED;
-    // capacity of the shared scratch
-    if ((size_t)n_tokens * n_experts > NA_LOGITS ||
-        (size_t)n_tokens * top_k * ffn > NA_ACT)
-        return QMOE_ERR_SHAPE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES)
@@ -93,18 +90,20 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
     qmoe::FusedPlan plan;
     if (!qmoe::fused_decode_plan(s, gate_t, up_t, down_t, su->num_sms, &plan))
         return QMOE_ERR_SHAPE;                 // only the fused decode shapes are served
+    // capacity of the shared scratch
+    if (qmoe::fused_bufs_bytes(n_tokens, hidden, n_experts, top_k, ffn, plan.grid) > NA_TAGGED)
+        return QMOE_ERR_SHAPE;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    unsigned* bar = reinterpret_cast<unsigned*>(su->scratch);
+    unsigned* ctl = reinterpret_cast<unsigned*>(su->scratch);
     int* status = reinterpret_cast<int*>(su->scratch + 128);
-    float* logits = reinterpret_cast<float*>(su->scratch + NA_HEAD);
-    float* act = logits + NA_LOGITS;
-    // the scratch keeps the previous call's contents: the barrier counters and
-    // the status word must start at zero
-    if (cudaMemsetAsync(su->scratch, 0, NA_HEAD, st) != cudaSuccess) return QMOE_ERR_CUDA;
+    const qmoe::FusedBufs fb = qmoe::fused_bufs_carve(su->scratch + NA_HEAD, n_tokens, hidden,
+                                                      n_experts, top_k, ffn, plan.grid, ctl, status);
+    // the status word reports this call only
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return QMOE_ERR_CUDA;
     cudaError_t e = qmoe::launch_fused_decode(
         s, plan, hidden_in, nullptr, nullptr, router_w, static_cast<const uint8_t*>(gate_exps),
         static_cast<const uint8_t*>(up_exps), static_cast<const uint8_t*>(down_exps), hidden_out,
-        nullptr, nullptr, logits, act, bar, status, st);
+        nullptr, nullptr, fb, st);
     return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }

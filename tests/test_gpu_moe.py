@@ -55,6 +55,24 @@ def test_decode_configs_match_oracle(q, cfg_id):
     print(f"config {cfg_id}: rel err {err:.2e}, near-tie tokens {ties}, min 8/9 gap {gap:.3e}")
 
 
+def test_decode_sizes_take_the_fused_kernel(q):
+    """Decode-size layers (T = 1 and T = 8 at the qwen3moe shape, both down
+    qtypes) run as the single fused kernel; the T = 512 prefill does not."""
+    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    ctx = G.make_ctx(q, inp, max_tokens=512)
+    try:
+        for T in (1, 2, 4, 8):
+            for dt in ("Q4_K", "Q6_K"):
+                assert q.qmoe_fused_decode_available(ctx, T, q.QTYPE["Q4_K"], q.QTYPE["Q4_K"],
+                                                     q.QTYPE[dt]), (T, dt)
+        assert not q.qmoe_fused_decode_available(ctx, 9, q.QTYPE["Q4_K"], q.QTYPE["Q4_K"],
+                                                 q.QTYPE["Q6_K"])
+        assert not q.qmoe_fused_decode_available(ctx, 512, q.QTYPE["Q4_K"], q.QTYPE["Q4_K"],
+                                                 q.QTYPE["Q6_K"])
+    finally:
+        q.qmoe_destroy(ctx)
+
+
 def test_prefill_config_matches_oracle(q):
     inp, got = _case(q, 4)
     err, ties, gap = G.check(inp, got, TOL_BF16)

@@ -75,7 +75,7 @@ typedef struct {
     int max_tokens;      /* largest n_tokens any call will pass (workspace size) */
     int n_heads;         /* attention q heads (decode step only, else 0) */
     int n_kv_heads;      /* attention kv heads, divides n_heads */
-    int head_dim;        /* 128 for qwen3moe (even, <= 256) */
+    int head_dim;        /* 128 for qwen3moe (a multiple of 64, <= 256) */
     int max_ctx;         /* KV-cache positions per layer */
     float rope_base;     /* NEOX RoPE base */
     float rms_eps;       /* RMSNorm epsilon (all four norms) */

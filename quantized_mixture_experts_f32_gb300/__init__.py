@@ -27,11 +27,13 @@ QTYPE = {"Q4_K": QMOE_Q4_K, "Q6_K": QMOE_Q6_K}
 # kernels one qmoe_forward enqueues on the decode path (n_tokens <= 8): the
 # whole layer is one fused cooperative kernel
 LAUNCHES_PER_DECODE_FORWARD = 1
-# n_tokens > 8: router, top-k + pair lists, gather, gate/up GEMM, down GEMM, combine
-LAUNCHES_PER_PREFILL_FORWARD = 6
-# one decoder layer of qmoe_decode_step: RMSNorm, Q/K/V GEMV, Q/K norm + RoPE + KV
-# append, attention partials, attention merge, O GEMV, RMSNorm, fused MoE layer
-LAUNCHES_PER_DECODE_LAYER = 8
+# n_tokens > 8 (tensor-core path): router GEMM, top-k, pair sort, gather, gate/up
+# GEMM, down GEMM, combine
+LAUNCHES_PER_PREFILL_FORWARD = 7
+# one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
+# Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
+# its RMSNorm)
+LAUNCHES_PER_DECODE_LAYER = 5
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",

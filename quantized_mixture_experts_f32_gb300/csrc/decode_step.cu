@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(512) rmsnorm_kernel(const float* __restrict__ 
     for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = h[i] * r * w[i];
 }
 
-constexpr int GV_ROWS = 8;      // rows per CTA (one per warp)
+constexpr int GV_WARPS = 8;
 
 struct GemvSeg {
     const uint8_t* W;   // Q4_K [rows][cols/256 superblocks]
@@ -48,131 +48,269 @@ struct GemvArgs {
     int nseg;
     int cols;
     const float* x;
+    const float* norm_w;   // nullable: x is first RMS-normalised and scaled by norm_w
+    float eps;
 };
 
-// y = W x (+ res) for up to three Q4_K matrices sharing the same x; one warp per
-// row, 16-byte pieces decoded in registers, x and its 16-column sums in smem
-__global__ void __launch_bounds__(256) q4k_gemv(const GemvArgs a) {
+// y = W x (+ res) for up to three Q4_K matrices sharing the same x (optionally
+// x = RMSNorm(x) * norm_w, recomputed by every CTA).  Each warp owns RPW
+// consecutive rows and issues all their loads before any arithmetic (16-byte
+// pieces, NT per lane and row), so a CTA keeps ~RPW*9 KB in flight; x and its
+// 16-column sums sit in shared memory.
+// x sits in shared memory with 4 floats of padding after every 64 (column c
+// at c + 4*(c/64)): the 16-float runs the 8 lanes of one superblock read at
+// once then fall in 8 different bank groups instead of 2.
+__device__ __forceinline__ int xpad(int c) { return c + 4 * (c >> 6); }
+
+template <int RPW, int NT>
+__global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
     extern __shared__ float sx[];
-    float* xsum = sx + a.cols;
-    for (int i = threadIdx.x; i < a.cols / 4; i += blockDim.x)
-        reinterpret_cast<float4*>(sx)[i] = reinterpret_cast<const float4*>(a.x)[i];
+    float* xsum = sx + xpad(a.cols);
+    __shared__ float red[GV_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // this warp's weight pieces first: they stream in while x is staged
+    const int npieces = 8 * (a.cols / QK);
+    const int r0 = (blockIdx.x * GV_WARPS + warp) * RPW;
+    uint4 hd[RPW][NT], qd[RPW][NT];
+    const uint8_t* wp[RPW];
+    float* yp[RPW];
+    const float* rp[RPW];
+    int rr[RPW];
+    const int n0 = a.seg[0].rows, n1 = a.nseg > 1 ? a.seg[1].rows : 0,
+              n2 = a.nseg > 2 ? a.seg[2].rows : 0;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        // segment of row r0 + i, selected without indexing the parameter array
+        const int r_ = r0 + i;
+        const int s_ = r_ < n0 ? 0 : r_ < n0 + n1 ? 1 : r_ < n0 + n1 + n2 ? 2 : 3;
+        wp[i] = s_ == 0 ? a.seg[0].W : s_ == 1 ? a.seg[1].W : s_ == 2 ? a.seg[2].W : nullptr;
+        yp[i] = s_ == 0 ? a.seg[0].y : s_ == 1 ? a.seg[1].y : a.seg[2].y;
+        rp[i] = s_ == 0 ? a.seg[0].res : s_ == 1 ? a.seg[1].res : a.seg[2].res;
+        rr[i] = r_ - (s_ >= 1 ? n0 : 0) - (s_ >= 2 ? n1 : 0);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int task = lane + 32 * t;
+            if (wp[i] && task < npieces) {
+                const uint8_t* b = wp[i] + ((size_t)rr[i] * (a.cols / QK) + (task >> 3)) * Q4K_BYTES;
+                hd[i][t] = __ldg(reinterpret_cast<const uint4*>(b));
+                qd[i][t] = __ldg(reinterpret_cast<const uint4*>(b + 16 + 16 * (task & 7)));
+            }
+        }
+    }
+    float r = 1.f;
+    if (a.norm_w) {
+        float ss = 0.f;
+        for (int i = threadIdx.x; i < a.cols / 4; i += blockDim.x) {
+            const float4 v = reinterpret_cast<const float4*>(a.x)[i];
+            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < GV_WARPS; ++i) tot += red[i];
+        r = rsqrtf(tot / (float)a.cols + a.eps);
+    }
+    for (int i = threadIdx.x; i < a.cols / 4; i += blockDim.x) {
+        float4 v = reinterpret_cast<const float4*>(a.x)[i];
+        if (a.norm_w) {
+            const float4 w = reinterpret_cast<const float4*>(a.norm_w)[i];
+            v = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+        }
+        *reinterpret_cast<float4*>(sx + xpad(4 * i)) = v;
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < a.cols / 16; i += blockDim.x) {
-        const float4* q = reinterpret_cast<const float4*>(sx + 16 * i);
+        const float4* q = reinterpret_cast<const float4*>(sx + xpad(16 * i));
         float s = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) s += (q[j].x + q[j].y) + (q[j].z + q[j].w);
         xsum[i] = s;
     }
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int r = blockIdx.x * GV_ROWS + warp;
-    int sidx = 0;
-    while (sidx < a.nseg && r >= a.seg[sidx].rows) { r -= a.seg[sidx].rows; ++sidx; }
-    if (sidx >= a.nseg) return;
-    const GemvSeg& sg = a.seg[sidx];
-    const int nsb = a.cols / QK;
-    const uint8_t* row = sg.W + (size_t)r * nsb * Q4K_BYTES;
-    float acc = 0.f;
-    for (int t = lane; t < 8 * nsb; t += 32) {
-        const int s = t >> 3, pc = t & 7;
-        const uint8_t* sb = row + (size_t)s * Q4K_BYTES;
-        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(sb));
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(sb + 16 + 16 * pc));
-        const int col = QK * s + 64 * (pc >> 1) + 16 * (pc & 1);
-        float PA, PB;
-        q4_piece_dot(q, reinterpret_cast<const float4*>(sx + col),
-                     reinterpret_cast<const float4*>(sx + col + 32), PA, PB);
-        acc += q4_piece_finish(hdr, pc, PA, PB, xsum[col / 16], xsum[col / 16 + 2]);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int task = lane + 32 * t;
+            if (wp[i] && task < npieces) {
+                const int pc = task & 7;
+                const int col = QK * (task >> 3) + 64 * (pc >> 1) + 16 * (pc & 1);
+                float PA, PB;
+                q4_piece_dot(qd[i][t], reinterpret_cast<const float4*>(sx + xpad(col)),
+                             reinterpret_cast<const float4*>(sx + xpad(col + 32)), PA, PB);
+                acc += q4_piece_finish(hd[i][t], pc, PA, PB, xsum[col / 16], xsum[col / 16 + 2]);
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0 && wp[i]) yp[i][rr[i]] = acc + (rp[i] ? rp[i][rr[i]] : 0.f);
     }
-    acc = warp_sum(acc);
-    if (lane == 0) sg.y[r] = acc + (sg.res ? sg.res[r] : 0.f);
 }
 
-// Per head: RMSNorm (q with q_norm, k with k_norm), NEOX RoPE at pos, then k and
-// v rounded to fp16 into cache slot pos.  blocks: nq + nkv, threads: hd
-__global__ void qk_norm_rope_append(float* __restrict__ q, const float* __restrict__ k,
-                                    const float* __restrict__ v, const float* __restrict__ q_norm,
-                                    const float* __restrict__ k_norm, float eps, int pos,
-                                    float rope_base, int hd, int nq, int nkv, int max_ctx,
-                                    __half* __restrict__ k_cache, __half* __restrict__ v_cache) {
-    extern __shared__ float buf[];        // hd values + 32 partials
-    float* part = buf + hd;
-    const int head = blockIdx.x, i = threadIdx.x;
-    const bool is_q = head < nq;
-    const int kvh = head - nq;
-    const float* src = is_q ? q + (size_t)head * hd : k + (size_t)kvh * hd;
-    const float val = src[i];
-    float ss = warp_sum(val * val);
-    if ((i & 31) == 0) part[i >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int j = 0; j < hd / 32; ++j) tot += part[j];
-    const float nv = val * rsqrtf(tot / (float)hd + eps) * (is_q ? q_norm[i] : k_norm[i]);
-    buf[i] = nv;
-    __syncthreads();
-    // NEOX: pairs (j, j + hd/2), angle pos * base^(-2j/hd); the angle and its
-    // sine/cosine in double (angles reach thousands of radians)
-    const int half = hd / 2;
-    const int j = i < half ? i : i - half;
-    const double th = (double)pos * pow((double)rope_base, -2.0 * (double)j / (double)hd);
-    double sn, cs;
-    sincos(th, &sn, &cs);
-    const float a = buf[j], b = buf[j + half];
-    const float rot = i < half ? (float)((double)a * cs - (double)b * sn)
-                               : (float)((double)b * cs + (double)a * sn);
-    if (is_q) {
-        q[(size_t)head * hd + i] = rot;
+// launch with RPW rows per warp chosen so that the grid still covers the SMs
+// (and the per-lane registers stay bounded: RPW * NT <= 8)
+cudaError_t launch_gemv(const GemvArgs& g, int total_rows, cudaStream_t st) {
+    const int nt = (8 * (g.cols / QK) + 31) / 32;
+    const size_t smem = sizeof(float) * (g.cols + g.cols / 16 + g.cols / 16);
+    auto blocks = [&](int rpw) { return (total_rows + GV_WARPS * rpw - 1) / (GV_WARPS * rpw); };
+    const int rpw_max = nt <= 2 ? 4 : 2;
+    const int rpw = rpw_max >= 4 && blocks(4) >= 148 ? 4 : blocks(2) >= 148 ? 2 : 1;
+    dim3 grid(blocks(rpw)), thr(GV_WARPS * 32);
+#define QMOE_GEMV(R, N) q4k_gemv<R, N><<<grid, thr, smem, st>>>(g)
+    if (nt == 1) {
+        if (rpw == 4) QMOE_GEMV(4, 1); else if (rpw == 2) QMOE_GEMV(2, 1); else QMOE_GEMV(1, 1);
+    } else if (nt == 2) {
+        if (rpw == 4) QMOE_GEMV(4, 2); else if (rpw == 2) QMOE_GEMV(2, 2); else QMOE_GEMV(1, 2);
+    } else if (nt <= 4) {
+        if (rpw == 2) QMOE_GEMV(2, 4); else QMOE_GEMV(1, 4);
     } else {
-        k_cache[((size_t)kvh * max_ctx + pos) * hd + i] = __float2half_rn(rot);
-        v_cache[((size_t)kvh * max_ctx + pos) * hd + i] = __float2half_rn(v[(size_t)kvh * hd + i]);
+        return cudaErrorInvalidValue;
+    }
+#undef QMOE_GEMV
+    return cudaGetLastError();
+}
+
+constexpr int ATT_CHUNK = 64;         // positions per split
+constexpr int ATT_THREADS = 256;
+constexpr int ATT_HPT = 8;            // q heads per thread in the score pass, at most
+constexpr int ATT_DPL = 8;            // head dims per lane in the norm/RoPE pass, at most
+
+// Per-head RMSNorm (weights nw) and NEOX RoPE at pos of one head vector held by
+// a warp: lane owns dims lane + 32 i, i < hd/32, so the rotated pairs (d,
+// d + hd/2) sit in the same lane.  inv_freq[j] = base^(-2j/hd) (host, double);
+// the angle pos * inv_freq[j] (thousands of radians) is formed and reduced to
+// [-pi, pi] in double, the rotation itself is float.
+__device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
+                                               const float* __restrict__ nw, float eps, int hd,
+                                               int pos, const double* __restrict__ inv_freq,
+                                               float (&o)[ATT_DPL]) {
+    const int lane = threadIdx.x & 31, n = hd / 32;
+    float v[ATT_DPL];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < ATT_DPL; ++i) {
+        v[i] = i < n ? src[lane + 32 * i] : 0.f;
+        ss = fmaf(v[i], v[i], ss);
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)hd + eps);
+#pragma unroll
+    for (int i = 0; i < ATT_DPL; ++i)
+        if (i < n) v[i] = v[i] * r * nw[lane + 32 * i];
+    constexpr double TWO_PI = 6.283185307179586476925286766559;
+#pragma unroll
+    for (int i = 0; i < ATT_DPL / 2; ++i) {
+        if (i < n / 2) {
+            const int j = lane + 32 * i;                        // pair (j, j + hd/2)
+            const double th = (double)pos * inv_freq[j];
+            const double red = fma(-rint(th * (1.0 / TWO_PI)), TWO_PI, th);
+            float sn, cs;
+            sincosf((float)red, &sn, &cs);
+            const float a = v[i], b = v[i + n / 2];
+            o[i] = a * cs - b * sn;
+            o[i + n / 2] = b * cs + a * sn;
+        }
     }
 }
 
-constexpr int ATT_CHUNK = 128;        // positions per split
-constexpr int ATT_THREADS = 256;
-
-// Split-K (flash-decoding) GQA attention: block (kv head, chunk) handles the
-// `group` q heads of that kv head over positions [c*CH, min((c+1)*CH, pos+1)).
-// Writes per (q head, chunk): running max, sum of exp, unnormalised acc[hd].
+// Split-K (flash-decoding) GQA attention with the per-head Q/K RMSNorm, RoPE
+// and the fp16 KV append fused in: block (kv head, chunk) normalises and
+// rotates the `group` q heads of that kv head, and the block whose chunk holds
+// position pos also normalises and rotates k, rounds k and v to fp16 and writes
+// them to cache slot pos (and into its staged tile).  It then attends over
+// positions [c*CH, min((c+1)*CH, pos+1)).  The chunk's K and V rows
+// (contiguous in the cache) are staged in shared memory with coalesced 16-byte
+// loads; K rows padded to an odd number of words so that one thread per
+// position reads them without bank conflicts.  Writes per (q head, chunk):
+// running max, sum of exp, unnormalised acc[hd].
 __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
-    const float* __restrict__ q, const __half* __restrict__ k_cache,
-    const __half* __restrict__ v_cache, int pos, int hd, int nq, int nkv, int max_ctx, int nsplit,
-    float* __restrict__ part) {
-    extern __shared__ float sm[];
+    const float* __restrict__ q_raw, const float* __restrict__ k_raw,
+    const float* __restrict__ v_raw, const float* __restrict__ q_norm,
+    const float* __restrict__ k_norm, float eps, const double* __restrict__ inv_freq,
+    __half* __restrict__ k_cache, __half* __restrict__ v_cache, int pos, int hd, int nq, int nkv,
+    int max_ctx, int nsplit, float* __restrict__ part) {
+    extern __shared__ __align__(16) float sm[];
     const int kvh = blockIdx.x, c = blockIdx.y;
     const int group = nq / nkv;
     const int p0 = c * ATT_CHUNK, p1 = min(p0 + ATT_CHUNK, pos + 1);
     const int np = p1 - p0;
-    float* qs = sm;                        // group * hd
-    float* sc = qs + group * hd;           // group * CHUNK
-    const float scale = rsqrtf((float)hd);
-    for (int i = threadIdx.x; i < group * hd; i += blockDim.x)
-        qs[i] = q[(size_t)(kvh * group) * hd + i];
-    __syncthreads();
-    const __half* K = k_cache + ((size_t)kvh * max_ctx + p0) * hd;
-    const __half* V = v_cache + ((size_t)kvh * max_ctx + p0) * hd;
-    for (int i = threadIdx.x; i < group * ATT_CHUNK; i += blockDim.x) {
-        const int g = i / ATT_CHUNK, pp = i % ATT_CHUNK;
-        float s = -INFINITY;
-        if (pp < np) {
-            const __half2* kr = reinterpret_cast<const __half2*>(K + (size_t)pp * hd);
-            const float* qg = qs + g * hd;
-            float a = 0.f;
-            for (int d = 0; d < hd / 2; ++d) {
-                const float2 kv = __half22float2(kr[d]);
-                a = fmaf(qg[2 * d], kv.x, a);
-                a = fmaf(qg[2 * d + 1], kv.y, a);
+    const int kw = hd / 2 + 1;                         // padded K row, 32-bit words
+    float* qs = sm;                                    // group * hd
+    float* sc = qs + group * hd;                       // group * CHUNK
+    uint32_t* ks = reinterpret_cast<uint32_t*>(sc + group * ATT_CHUNK);   // CHUNK * kw
+    __half* vs = reinterpret_cast<__half*>(ks + ((ATT_CHUNK * kw + 3) & ~3));
+    __shared__ float mx_s[32], sum_s[32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = ATT_THREADS >> 5;
+    const uint4* K = reinterpret_cast<const uint4*>(k_cache + ((size_t)kvh * max_ctx + p0) * hd);
+    const uint4* V = reinterpret_cast<const uint4*>(v_cache + ((size_t)kvh * max_ctx + p0) * hd);
+    const int vpr = hd / 8;                            // uint4 per row
+    for (int i = tid; i < np * vpr; i += ATT_THREADS) {
+        const int row = i / vpr, cc = i - row * vpr;
+        const uint4 kq = __ldg(K + i), vq = __ldg(V + i);
+        uint32_t* kd = ks + row * kw + 4 * cc;
+        kd[0] = kq.x; kd[1] = kq.y; kd[2] = kq.z; kd[3] = kq.w;
+        reinterpret_cast<uint4*>(vs)[i] = vq;
+    }
+    // q heads of this kv head: RMSNorm + RoPE (warp per head)
+    for (int g = warp; g < group; g += nw) {
+        float o[ATT_DPL];
+        norm_rope_warp(q_raw + (size_t)(kvh * group + g) * hd, q_norm, eps, hd, pos, inv_freq, o);
+#pragma unroll
+        for (int i = 0; i < ATT_DPL; ++i)
+            if (i < hd / 32) qs[g * hd + lane + 32 * i] = o[i];
+    }
+    __syncthreads();                                   // tile staged (row pos - p0 is stale)
+    if (pos >= p0 && pos < p1 && warp == 0) {
+        // the new token's k and v: cache slot pos and tile row pos - p0
+        float o[ATT_DPL];
+        norm_rope_warp(k_raw + (size_t)kvh * hd, k_norm, eps, hd, pos, inv_freq, o);
+        __half* kc = k_cache + ((size_t)kvh * max_ctx + pos) * hd;
+        __half* vc = v_cache + ((size_t)kvh * max_ctx + pos) * hd;
+        __half* kt = reinterpret_cast<__half*>(ks + (pos - p0) * kw);
+        __half* vt = vs + (size_t)(pos - p0) * hd;
+#pragma unroll
+        for (int i = 0; i < ATT_DPL; ++i) {
+            if (i < hd / 32) {
+                const int d = lane + 32 * i;
+                const __half kh = __float2half_rn(o[i]);
+                const __half vh = __float2half_rn(v_raw[(size_t)kvh * hd + d]);
+                kc[d] = kh;
+                vc[d] = vh;
+                kt[d] = kh;
+                vt[d] = vh;
             }
-            s = a * scale;
         }
-        sc[i] = s;
+    }
+    __syncthreads();
+    // scores: thread -> position pp, heads [hg*hpt, (hg+1)*hpt)
+    const float scale = rsqrtf((float)hd);
+    const int hpt = (group * ATT_CHUNK + ATT_THREADS - 1) / ATT_THREADS;
+    {
+        const int pp = tid % ATT_CHUNK, hg = tid / ATT_CHUNK;
+        float acc[ATT_HPT];
+#pragma unroll
+        for (int g = 0; g < ATT_HPT; ++g) acc[g] = 0.f;
+        if (hg * hpt < group && pp < np) {
+            const uint32_t* kr = ks + pp * kw;
+            for (int d2 = 0; d2 < hd / 2; ++d2) {
+                const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(kr + d2));
+#pragma unroll
+                for (int g = 0; g < ATT_HPT; ++g) {
+                    if (g < hpt) {
+                        const float2 qv = *reinterpret_cast<const float2*>(qs + (hg * hpt + g) * hd + 2 * d2);
+                        acc[g] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, acc[g]));
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < ATT_HPT; ++g)
+            if (g < hpt && hg * hpt + g < group)
+                sc[(hg * hpt + g) * ATT_CHUNK + pp] = pp < np ? acc[g] * scale : -INFINITY;
     }
     __syncthreads();
     // per q head (one warp each, warps loop over heads): max and sum of exp
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    __shared__ float mx_s[32], sum_s[32];
     for (int g = warp; g < group; g += nw) {
         float m = -INFINITY;
         for (int pp = lane; pp < np; pp += 32) m = fmaxf(m, sc[g * ATT_CHUNK + pp]);
@@ -187,32 +325,76 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
         if (lane == 0) { mx_s[g] = m; sum_s[g] = l; }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < group * hd; i += blockDim.x) {
-        const int g = i / hd, d = i % hd;
-        float a = 0.f;
-        for (int pp = 0; pp < np; ++pp)
-            a = fmaf(sc[g * ATT_CHUNK + pp], __half2float(V[(size_t)pp * hd + d]), a);
+    // P V: thread -> (head g, 4 consecutive dims)
+    const int dq = hd / 4;
+    for (int i = tid; i < group * dq; i += ATT_THREADS) {
+        const int g = i / dq, d4 = i - g * dq;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        const float* pg = sc + g * ATT_CHUNK;
+        for (int pp = 0; pp < np; ++pp) {
+            const float w = pg[pp];
+            const uint2 vv = *reinterpret_cast<const uint2*>(vs + (size_t)pp * hd + 4 * d4);
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&vv.x));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&vv.y));
+            a0 = fmaf(w, v01.x, a0);
+            a1 = fmaf(w, v01.y, a1);
+            a2 = fmaf(w, v23.x, a2);
+            a3 = fmaf(w, v23.y, a3);
+        }
         float* o = part + ((size_t)(kvh * group + g) * nsplit + c) * (hd + 2);
-        o[2 + d] = a;
-        if (d == 0) { o[0] = mx_s[g]; o[1] = sum_s[g]; }
+        *reinterpret_cast<float2*>(o + 2 + 4 * d4) = make_float2(a0, a1);
+        *reinterpret_cast<float2*>(o + 4 + 4 * d4) = make_float2(a2, a3);
+        if (d4 == 0) { o[0] = mx_s[g]; o[1] = sum_s[g]; }
     }
 }
 
-// merge the splits of one q head (block per q head, hd threads)
-__global__ void attn_merge(const float* __restrict__ part, int nsplit, int nvalid, int hd,
-                           float* __restrict__ out) {
-    const int h = blockIdx.x, d = threadIdx.x;
+size_t attn_smem(int group, int hd) {
+    const size_t kwords = (size_t)ATT_CHUNK * (hd / 2 + 1);
+    return sizeof(float) * (group * hd + group * ATT_CHUNK) + 4 * ((kwords + 3) & ~(size_t)3) +
+           sizeof(__half) * ATT_CHUNK * hd;
+}
+
+// merge the splits of one q head (block per q head): split weights
+// exp(m_c - M) once in shared memory, then each thread sums a slice of the
+// splits for one dim with all its loads in flight, slices combined in order
+constexpr int MRG_THREADS = 256;
+
+__global__ void __launch_bounds__(MRG_THREADS) attn_merge(const float* __restrict__ part,
+                                                          int nsplit, int nvalid, int hd,
+                                                          float* __restrict__ out) {
+    extern __shared__ float wsh[];                     // nvalid weights, then slice sums
+    __shared__ float tot_s[2];
+    const int h = blockIdx.x, tid = threadIdx.x;
     const float* ph = part + (size_t)h * nsplit * (hd + 2);
-    float m = -INFINITY;
-    for (int c = 0; c < nvalid; ++c) m = fmaxf(m, ph[(size_t)c * (hd + 2)]);
-    float l = 0.f, a = 0.f;
-    for (int c = 0; c < nvalid; ++c) {
-        const float* pc = ph + (size_t)c * (hd + 2);
-        const float w = expf(pc[0] - m);
-        l = fmaf(w, pc[1], l);
-        a = fmaf(w, pc[2 + d], a);
+    float* acc_s = wsh + nvalid;
+    if (tid < 32) {
+        float m = -INFINITY;
+        for (int c = tid; c < nvalid; c += 32) m = fmaxf(m, ph[(size_t)c * (hd + 2)]);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int c = tid; c < nvalid; c += 32) {
+            const float w = expf(ph[(size_t)c * (hd + 2)] - m);
+            wsh[c] = w;
+            l = fmaf(w, ph[(size_t)c * (hd + 2) + 1], l);
+        }
+        l = warp_sum(l);
+        if (tid == 0) tot_s[0] = l;
     }
-    out[(size_t)h * hd + d] = a / l;
+    __syncthreads();
+    const int S = MRG_THREADS / hd;                    // slices of splits
+    const int d = tid % hd, sl = tid / hd;
+    if (sl < S) {
+        float a = 0.f;
+#pragma unroll 8
+        for (int c = sl; c < nvalid; c += S) a = fmaf(wsh[c], ph[(size_t)c * (hd + 2) + 2 + d], a);
+        acc_s[sl * hd + d] = a;
+    }
+    __syncthreads();
+    if (tid < hd) {
+        float a = 0.f;
+        for (int k = 0; k < S; ++k) a += acc_s[k * hd + tid];
+        out[(size_t)h * hd + tid] = a / tot_s[0];
+    }
 }
 
 }  // namespace
@@ -226,41 +408,57 @@ cudaError_t launch_rmsnorm(const float* h, const float* w, float eps, int n, flo
 cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const float* h,
                                    float* xs, float* q, float* kv, float* att, float* part,
                                    float* h_out, cudaStream_t st) {
+    (void)xs;
     const int qd = a.nq * a.hd, kvd = a.nkv * a.hd;
     cudaError_t e;
-    // B1: x = RMSNorm(h) * attn_norm
-    rmsnorm_kernel<<<1, 512, 0, st>>>(h, L.attn_norm, a.eps, a.H, xs);
-    // B2: q, k, v = Wq x, Wk x, Wv x  (no bias)
+    // B1 + B2: q, k, v = Wq x, Wk x, Wv x with x = RMSNorm(h) * attn_norm (no bias)
     GemvArgs g{};
     g.seg[0] = GemvSeg{L.wq, q, nullptr, qd};
     g.seg[1] = GemvSeg{L.wk, kv, nullptr, kvd};
     g.seg[2] = GemvSeg{L.wv, kv + kvd, nullptr, kvd};
     g.nseg = 3;
     g.cols = a.H;
-    g.x = xs;
-    const size_t gsm = sizeof(float) * (a.H + a.H / 16);
-    q4k_gemv<<<(qd + 2 * kvd + GV_ROWS - 1) / GV_ROWS, 256, gsm, st>>>(g);
-    // B3-B5: per-head Q/K RMSNorm, NEOX RoPE, fp16 KV append at pos
-    qk_norm_rope_append<<<a.nq + a.nkv, a.hd, sizeof(float) * (a.hd + 32), st>>>(
-        q, kv, kv + kvd, L.q_norm, L.k_norm, a.eps, a.pos, a.rope_base, a.hd, a.nq, a.nkv,
-        a.max_ctx, L.k_cache, L.v_cache);
-    // B6: GQA attention over positions 0..pos
+    g.x = h;
+    g.norm_w = L.attn_norm;
+    g.eps = a.eps;
+    e = launch_gemv(g, qd + 2 * kvd, st);
+    if (e != cudaSuccess) return e;
+    // B3-B6: per-head Q/K RMSNorm, NEOX RoPE, fp16 KV append at pos (all fused
+    // into the split-K attention), GQA attention over positions 0..pos
     const int nsplit = (a.max_ctx + ATT_CHUNK - 1) / ATT_CHUNK;
     const int nvalid = a.pos / ATT_CHUNK + 1;
     const int group = a.nq / a.nkv;
     dim3 ga(a.nkv, nvalid);
-    attn_partial<<<ga, ATT_THREADS, sizeof(float) * group * (a.hd + ATT_CHUNK), st>>>(
-        q, L.k_cache, L.v_cache, a.pos, a.hd, a.nq, a.nkv, a.max_ctx, nsplit, part);
-    attn_merge<<<a.nq, a.hd, 0, st>>>(part, nsplit, nvalid, a.hd, att);
+    attn_partial<<<ga, ATT_THREADS, attn_smem(group, a.hd), st>>>(
+        q, kv, kv + kvd, L.q_norm, L.k_norm, a.eps, a.inv_freq, L.k_cache, L.v_cache, a.pos, a.hd,
+        a.nq, a.nkv, a.max_ctx, nsplit, part);
+    attn_merge<<<a.nq, MRG_THREADS, sizeof(float) * (nvalid + MRG_THREADS), st>>>(
+        part, nsplit, nvalid, a.hd, att);
     // B7: h_out = h + Wo att
     GemvArgs go{};
     go.seg[0] = GemvSeg{L.wo, h_out, h, a.H};
     go.nseg = 1;
     go.cols = qd;
     go.x = att;
-    q4k_gemv<<<(a.H + GV_ROWS - 1) / GV_ROWS, 256, sizeof(float) * (qd + qd / 16), st>>>(go);
-    e = cudaGetLastError();
-    return e;
+    e = launch_gemv(go, a.H, st);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// Shared memory limit of the attention kernel (once per device context) and
+// the shapes it serves: at most 2 * ATT_HPT q heads per kv head, head_dim a
+// multiple of 64 up to 256 with the staged chunk inside ATT_SMEM_MAX.
+constexpr int ATT_SMEM_MAX = 200 * 1024;     // dynamic; the kernel also has 256 B static
+
+cudaError_t decode_step_prepare() {
+    return cudaFuncSetAttribute(attn_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ATT_SMEM_MAX);
+}
+
+bool attention_supported(int nq, int nkv, int hd) {
+    if (nkv < 1 || nq % nkv || nq / nkv > 2 * ATT_HPT) return false;
+    if (hd < 64 || hd > 32 * ATT_DPL || hd % 64) return false;     // RoPE pairs within a lane
+    return attn_smem(nq / nkv, hd) <= (size_t)ATT_SMEM_MAX;
 }
 
 int attn_splits(int max_ctx) { return (max_ctx + ATT_CHUNK - 1) / ATT_CHUNK; }

@@ -54,6 +54,14 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Integer key with the order of the float comparison (-0 folded into +0); NaN
+// gets an extreme key, so ranks taken on it stay a permutation whatever the
+// input (routing top-k).
+__device__ __forceinline__ int order_key(float v) {
+    const int b = __float_as_int(v + 0.f);
+    return b ^ ((b >> 31) & 0x7fffffff);
+}
+
 // Sum over four consecutive 32-bit words of (0.5 + nibble/256) * x for the low
 // nibbles (PA) and the high nibbles (PB) of 16 bytes; xa/xb point at the 16 x
 // values paired with the low / high nibbles.

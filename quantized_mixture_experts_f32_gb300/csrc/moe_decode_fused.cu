@@ -124,6 +124,8 @@ struct FusedParams {
     unsigned long long* xflag;  // [G] tagged "x staged" marks (only when out aliases x)
     unsigned* ctl;              // [0] exit counter, [1] tag of the last completed launch
     int* status;
+    const float* norm_w;        // nullable: x is RMS-normalised per token and scaled first
+    float eps;
     int T, H, E, K, F, norm, x_alias;
     int cf;          // f rows per gate/up chunk (divides F)
     SmemLayout L;
@@ -288,6 +290,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     __syncthreads();
     const unsigned tag = (unsigned)misc[M_TAG];
     if (p.x_alias && tid == 0) st_relaxed_u64(p.xflag + c, tag_pack(0.f, tag));   // x is staged
+    if (p.norm_w) {
+        // x = x / sqrt(mean(x^2) + eps) * norm_w, per token (every CTA redoes it)
+        for (int t = 0; t < T; ++t) {
+            float ss = 0.f;
+            for (int i = tid; i < H; i += NTHREADS) ss = fmaf(x_s[t * H + i], x_s[t * H + i], ss);
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp * MAXT + t] = ss;
+        }
+        __syncthreads();
+        for (int i = tid; i < T * H; i += NTHREADS) {
+            const int t = i / H;
+            float tot = 0.f;
+            for (int w = 0; w < NCW; ++w) tot += red[w * MAXT + t];
+            x_s[i] = x_s[i] * rsqrtf(tot / (float)H + p.eps) * p.norm_w[i - t * H];
+        }
+        __syncthreads();
+    }
     for (int i = tid; i < T * (H / 16); i += NTHREADS) {
         const float4* q = reinterpret_cast<const float4*>(x_s + 16 * i);
         float s = 0.f;
@@ -419,10 +438,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             const bool valid = i < nel;
             const int t = valid ? i / E : 0, e = valid ? i - t * E : 0;
             const float* l = lg_s + t * E;
-            const float v = l[e];
+            const int v = order_key(l[e]);
             int rank = 0;
             for (int e2 = sub; e2 < E; e2 += tpe) {
-                const float w = l[e2];
+                const int w = order_key(l[e2]);
                 rank += (w > v) || (w == v && e2 < e);
             }
             for (int o = tpe >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
@@ -431,10 +450,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             for (int i = tid; i < nel; i += NTHREADS) {
                 const int t = i / E, e = i - t * E;
                 const float* l = lg_s + t * E;
-                const float v = l[e];
+                const int v = order_key(l[e]);
                 int rank = 0;
                 for (int e2 = 0; e2 < E; ++e2) {
-                    const float w = l[e2];
+                    const int w = order_key(l[e2]);
                     rank += (w > v) || (w == v && e2 < e);
                 }
                 if (rank < K) sel[t * K + rank] = e;
@@ -1000,8 +1019,10 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
                                 float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
-                                cudaStream_t st) {
+                                const float* norm_w, float eps, cudaStream_t st) {
     FusedParams p;
+    p.norm_w = norm_w;
+    p.eps = eps;
     p.x = x; p.res = res; p.bias = bias; p.router = router;
     p.gate = gate; p.up = up; p.down = down;
     p.out = out; p.ids_out = ids_out; p.w_out = w_out;

@@ -57,13 +57,6 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ x
     }
 }
 
-// Integer key with the order of the float comparison (-0 folded into +0); NaN
-// gets an extreme key, so the ranks in this file stay a permutation whatever the input.
-__device__ __forceinline__ int order_key(float v) {
-    const int b = __float_as_int(v + 0.f);
-    return b ^ ((b >> 31) & 0x7fffffff);
-}
-
 // the map is its own inverse
 __device__ __forceinline__ float key_value(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
 

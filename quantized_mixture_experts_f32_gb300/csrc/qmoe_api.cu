@@ -1,6 +1,7 @@
 // qmoe_api.cu -- the C ABI (include/qmoe.h): argument checks, workspace, and the
 // launch sequence of one MoE-FFN layer call on the context's stream.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -35,6 +36,7 @@ struct qmoe_ctx {
     float* kv;        // [2*nkv*hd]
     float* att;       // [nq*hd]
     float* attn_part; // split-K partials
+    double* inv_freq; // [head_dim/2] RoPE frequencies
     int attn_splits;
 };
 
@@ -65,7 +67,8 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, logits_part, ftag, xs, q, kv, att, attn_part, total;
+        status, bar, xp, actp, inv_pos, logits_part, ftag, xs, q, kv, att, attn_part, inv_freq,
+        total;
     int attn_splits;
 };
 
@@ -79,11 +82,12 @@ bool config_ok(const qmoe_config* c, char* why, size_t n) {
     const bool attn = c->n_heads || c->n_kv_heads || c->head_dim || c->max_ctx;
     if (attn) {
         if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) { snprintf(why, n, "n_heads=%d must be a positive multiple of n_kv_heads=%d", c->n_heads, c->n_kv_heads); return false; }
-        if (c->head_dim < 2 || c->head_dim > 256 || c->head_dim % 32) { snprintf(why, n, "head_dim=%d must be a multiple of 32 in 32..256", c->head_dim); return false; }
+        if (c->head_dim < 64 || c->head_dim > 256 || c->head_dim % 64) { snprintf(why, n, "head_dim=%d must be a multiple of 64 in 64..256", c->head_dim); return false; }
         if ((c->n_heads * c->head_dim) % 256) { snprintf(why, n, "n_heads*head_dim=%d is not a multiple of 256", c->n_heads * c->head_dim); return false; }
         if ((c->n_kv_heads * c->head_dim) % 256 && c->n_kv_heads * c->head_dim % 32) { snprintf(why, n, "bad kv dim"); return false; }
         if (c->max_ctx < 1) { snprintf(why, n, "max_ctx=%d must be >= 1", c->max_ctx); return false; }
         if (!(c->rope_base > 0.f) || !(c->rms_eps > 0.f)) { snprintf(why, n, "rope_base and rms_eps must be positive"); return false; }
+        if (!qmoe::attention_supported(c->n_heads, c->n_kv_heads, c->head_dim)) { snprintf(why, n, "attention shape n_heads=%d n_kv_heads=%d head_dim=%d not served (at most 16 q heads per kv head)", c->n_heads, c->n_kv_heads, c->head_dim); return false; }
     }
     return true;
 }
@@ -120,6 +124,7 @@ Layout layout(const qmoe_config* c) {
     L.kv = take(sizeof(float) * (2 * kvd + 1));
     L.att = take(sizeof(float) * (qd ? qd : 1));
     L.attn_part = take(sizeof(float) * (size_t)c->n_heads * L.attn_splits * (c->head_dim + 2) + 4);
+    L.inv_freq = take(sizeof(double) * (c->head_dim > 0 ? c->head_dim / 2 : 1));
     L.total = off;
     return L;
 }
@@ -150,7 +155,7 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
         cudaError_t e = qmoe::launch_fused_decode(
             s, plan, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
             static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out,
-            w_out, c->fb, c->stream);
+            w_out, c->fb, nullptr, 0.f, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
         c->err[0] = 0;
         return QMOE_OK;
@@ -253,8 +258,9 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     }
     e = qmoe::fused_prepare();
     if (e == cudaSuccess) e = qmoe::route_prepare();
+    if (e == cudaSuccess) e = qmoe::decode_step_prepare();
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: fused kernel set-up: %s\n", cudaGetErrorString(e));
+        fprintf(stderr, "qmoe_create: kernel set-up: %s\n", cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_CUDA;
     }
@@ -294,6 +300,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->att = reinterpret_cast<float*>(b + L.att);
     c->attn_part = reinterpret_cast<float*>(b + L.attn_part);
     c->attn_splits = L.attn_splits;
+    c->inv_freq = reinterpret_cast<double*>(b + L.inv_freq);
     e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
@@ -301,6 +308,20 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
         cudaFree(c->ws);
         delete c;
         return QMOE_ERR_CUDA;
+    }
+    if (c->cfg.head_dim > 0) {
+        // RoPE frequencies base^(-2j/head_dim), j < head_dim/2, in double
+        const int half = c->cfg.head_dim / 2;
+        double f[128];
+        for (int j = 0; j < half; ++j)
+            f[j] = pow((double)c->cfg.rope_base, -2.0 * (double)j / (double)c->cfg.head_dim);
+        e = cudaMemcpy(c->inv_freq, f, sizeof(double) * half, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            fprintf(stderr, "qmoe_create: RoPE table upload: %s\n", cudaGetErrorString(e));
+            cudaFree(c->ws);
+            delete c;
+            return QMOE_ERR_CUDA;
+        }
     }
     *out = c;
     return QMOE_OK;
@@ -399,7 +420,7 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
             return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "layer %d: down qtype %d", l, (int)w.down_t);
     }
     qmoe::AttnShape a{k.hidden, k.n_heads, k.n_kv_heads, k.head_dim, k.max_ctx, pos, k.rms_eps,
-                      k.rope_base};
+                      k.rope_base, c->inv_freq};
     for (int l = 0; l < n_layers; ++l) {
         const qmoe_layer_weights& w = layers[l];
         qmoe::LayerAttn la{w.attn_norm,
@@ -415,14 +436,26 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
         cudaError_t e = qmoe::launch_attention_block(a, la, hidden, c->xs, c->q, c->kv, c->att,
                                                      c->attn_part, hidden, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
-        // B8: x2 = RMSNorm(h) * ffn_norm
-        e = qmoe::launch_rmsnorm(hidden, w.ffn_norm, k.rms_eps, k.hidden, c->xs, c->stream);
-        if (e != cudaSuccess) return cuda_fail(c, e, "ffn norm launch");
-        // B9: h = h + MoE(x2)
-        qmoe_status st = run_moe(c, c->xs, hidden, nullptr, w.router_w, w.gate_exps, w.up_exps,
-                                 w.down_exps, QMOE_Q4_K, QMOE_Q4_K, w.down_t, 1, hidden,
-                                 ids_out ? ids_out + (size_t)l * k.top_k : nullptr, nullptr);
-        if (st != QMOE_OK) return st;
+        // B8 + B9: h = h + MoE(RMSNorm(h) * ffn_norm); the fused decode kernel
+        // normalises x itself, other paths take a separate normalisation
+        int32_t* ids_l = ids_out ? ids_out + (size_t)l * k.top_k : nullptr;
+        qmoe::MoeShape ms{1, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+        qmoe::FusedPlan plan;
+        if (qmoe::fused_decode_plan(ms, QMOE_Q4_K, QMOE_Q4_K, w.down_t, c->num_sms, &plan)) {
+            e = qmoe::launch_fused_decode(
+                ms, plan, hidden, hidden, nullptr, w.router_w,
+                static_cast<const uint8_t*>(w.gate_exps), static_cast<const uint8_t*>(w.up_exps),
+                static_cast<const uint8_t*>(w.down_exps), hidden, ids_l, nullptr, c->fb,
+                w.ffn_norm, k.rms_eps, c->stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
+        } else {
+            e = qmoe::launch_rmsnorm(hidden, w.ffn_norm, k.rms_eps, k.hidden, c->xs, c->stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "ffn norm launch");
+            qmoe_status st = run_moe(c, c->xs, hidden, nullptr, w.router_w, w.gate_exps,
+                                     w.up_exps, w.down_exps, QMOE_Q4_K, QMOE_Q4_K, w.down_t, 1,
+                                     hidden, ids_l, nullptr);
+            if (st != QMOE_OK) return st;
+        }
     }
     c->err[0] = 0;
     return QMOE_OK;

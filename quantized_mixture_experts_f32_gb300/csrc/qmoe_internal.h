@@ -90,7 +90,7 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
                                 float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
-                                cudaStream_t st);
+                                const float* norm_w, float eps, cudaStream_t st);
 
 int fused_threads();
 cudaError_t fused_prepare();
@@ -99,6 +99,7 @@ cudaError_t fused_prepare();
 struct AttnShape {
     int H, nq, nkv, hd, max_ctx, pos;
     float eps, rope_base;
+    const double* inv_freq;   // [hd/2] rope_base^(-2j/hd), device
 };
 struct LayerAttn {
     const float* attn_norm;
@@ -118,6 +119,8 @@ cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const
 cudaError_t launch_rmsnorm(const float* h, const float* w, float eps, int n, float* out,
                            cudaStream_t st);
 int attn_splits(int max_ctx);
+cudaError_t decode_step_prepare();
+bool attention_supported(int nq, int nkv, int hd);
 
 // Prefill path (T > 8): tcgen05 grouped GEMMs with on-the-fly dequantisation.
 bool prefill_supported(const MoeShape& s, int gate_t, int up_t, int down_t);

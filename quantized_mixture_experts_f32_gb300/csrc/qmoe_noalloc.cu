@@ -104,6 +104,6 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
     cudaError_t e = qmoe::launch_fused_decode(
         s, plan, hidden_in, nullptr, nullptr, router_w, static_cast<const uint8_t*>(gate_exps),
         static_cast<const uint8_t*>(up_exps), static_cast<const uint8_t*>(down_exps), hidden_out,
-        nullptr, nullptr, fb, st);
+        nullptr, nullptr, fb, nullptr, 0.f, st);
     return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }

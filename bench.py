@@ -487,7 +487,7 @@ def bench_step48(args, torch, q, dev, stream, ws, pg, local):
         value=L * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
         ebytes=ebytes, other_bytes=attn_bytes + kv_bytes + rbytes,
         e2e=L * args.e2e_steps * ws / te, h2d=H * 4, d2h=H * 4,
-        launches=L * q.LAUNCHES_PER_DECODE_LAYER,
+        launches=L * q.LAUNCHES_PER_DECODE_LAYER + q.LAUNCHES_PER_DECODE_STEP,
         config={"workload": WORKLOADS["step48"]["desc"], "hidden": H, "n_experts": E,
                 "top_k": K, "ffn": F, "layers": L, "context": geo["ctx"], "tokens": 1,
                 "l2": f"one step touches {(ebytes + attn_bytes + kv_bytes + rbytes) / 1e9:.2f} GB "

@@ -34,6 +34,8 @@ LAUNCHES_PER_PREFILL_FORWARD = 7
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
 # its RMSNorm)
 LAUNCHES_PER_DECODE_LAYER = 5
+# plus, once per qmoe_decode_step: the RoPE cos/sin table at the step's position
+LAUNCHES_PER_DECODE_STEP = 1
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",

@@ -97,12 +97,27 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
             }
         }
     }
+    // x (and the norm weights) in flight at once: cols <= 4096, 4 float4 per thread
+    constexpr int XLD = 4096 / 4 / (GV_WARPS * 32);
+    float4 xv[XLD], wv[XLD];
+#pragma unroll
+    for (int j = 0; j < XLD; ++j) {
+        const int i = threadIdx.x + j * GV_WARPS * 32;
+        if (i < a.cols / 4) {
+            xv[j] = reinterpret_cast<const float4*>(a.x)[i];
+            wv[j] = a.norm_w ? reinterpret_cast<const float4*>(a.norm_w)[i] : make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+    }
     float r = 1.f;
     if (a.norm_w) {
         float ss = 0.f;
-        for (int i = threadIdx.x; i < a.cols / 4; i += blockDim.x) {
-            const float4 v = reinterpret_cast<const float4*>(a.x)[i];
-            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+#pragma unroll
+        for (int j = 0; j < XLD; ++j) {
+            const int i = threadIdx.x + j * GV_WARPS * 32;
+            if (i < a.cols / 4) {
+                const float4 v = xv[j];
+                ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+            }
         }
         ss = warp_sum(ss);
         if (lane == 0) red[warp] = ss;
@@ -111,13 +126,17 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
         for (int i = 0; i < GV_WARPS; ++i) tot += red[i];
         r = rsqrtf(tot / (float)a.cols + a.eps);
     }
-    for (int i = threadIdx.x; i < a.cols / 4; i += blockDim.x) {
-        float4 v = reinterpret_cast<const float4*>(a.x)[i];
-        if (a.norm_w) {
-            const float4 w = reinterpret_cast<const float4*>(a.norm_w)[i];
-            v = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+#pragma unroll
+    for (int j = 0; j < XLD; ++j) {
+        const int i = threadIdx.x + j * GV_WARPS * 32;
+        if (i < a.cols / 4) {
+            float4 v = xv[j];
+            if (a.norm_w) {
+                const float4 w = wv[j];
+                v = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+            }
+            *reinterpret_cast<float4*>(sx + xpad(4 * i)) = v;
         }
-        *reinterpret_cast<float4*>(sx + xpad(4 * i)) = v;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < a.cols / 16; i += blockDim.x) {
@@ -176,14 +195,28 @@ constexpr int ATT_THREADS = 256;
 constexpr int ATT_HPT = 8;            // q heads per thread in the score pass, at most
 constexpr int ATT_DPL = 8;            // head dims per lane in the norm/RoPE pass, at most
 
-// Per-head RMSNorm (weights nw) and NEOX RoPE at pos of one head vector held by
-// a warp: lane owns dims lane + 32 i, i < hd/32, so the rotated pairs (d,
-// d + hd/2) sit in the same lane.  inv_freq[j] = base^(-2j/hd) (host, double);
+// cos/sin of the NEOX RoPE angles at one position, shared by every head and
+// every layer of a decode step: inv_freq[j] = base^(-2j/hd) (host, double);
 // the angle pos * inv_freq[j] (thousands of radians) is formed and reduced to
-// [-pi, pi] in double, the rotation itself is float.
+// [-pi, pi] in double, then cos and sin are taken in float.  One block.
+__global__ void rope_table(const double* __restrict__ inv_freq, int half, int pos,
+                           float2* __restrict__ cs) {
+    constexpr double TWO_PI = 6.283185307179586476925286766559;
+    for (int j = threadIdx.x; j < half; j += blockDim.x) {
+        const double th = (double)pos * inv_freq[j];
+        const double red = fma(-rint(th * (1.0 / TWO_PI)), TWO_PI, th);
+        float sn, c;
+        sincosf((float)red, &sn, &c);
+        cs[j] = make_float2(c, sn);
+    }
+}
+
+// Per-head RMSNorm (weights nw) and NEOX RoPE (table cs) of one head vector
+// held by a warp: lane owns dims lane + 32 i, i < hd/32, so the rotated pairs
+// (d, d + hd/2) sit in the same lane.
 __device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
                                                const float* __restrict__ nw, float eps, int hd,
-                                               int pos, const double* __restrict__ inv_freq,
+                                               const float2* __restrict__ cs,
                                                float (&o)[ATT_DPL]) {
     const int lane = threadIdx.x & 31, n = hd / 32;
     float v[ATT_DPL];
@@ -198,18 +231,13 @@ __device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
 #pragma unroll
     for (int i = 0; i < ATT_DPL; ++i)
         if (i < n) v[i] = v[i] * r * nw[lane + 32 * i];
-    constexpr double TWO_PI = 6.283185307179586476925286766559;
 #pragma unroll
     for (int i = 0; i < ATT_DPL / 2; ++i) {
         if (i < n / 2) {
-            const int j = lane + 32 * i;                        // pair (j, j + hd/2)
-            const double th = (double)pos * inv_freq[j];
-            const double red = fma(-rint(th * (1.0 / TWO_PI)), TWO_PI, th);
-            float sn, cs;
-            sincosf((float)red, &sn, &cs);
+            const float2 t = cs[lane + 32 * i];               // pair (j, j + hd/2)
             const float a = v[i], b = v[i + n / 2];
-            o[i] = a * cs - b * sn;
-            o[i + n / 2] = b * cs + a * sn;
+            o[i] = a * t.x - b * t.y;
+            o[i + n / 2] = b * t.x + a * t.y;
         }
     }
 }
@@ -224,10 +252,11 @@ __device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
 // loads; K rows padded to an odd number of words so that one thread per
 // position reads them without bank conflicts.  Writes per (q head, chunk):
 // running max, sum of exp, unnormalised acc[hd].
+template <int HPT>
 __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
     const float* __restrict__ q_raw, const float* __restrict__ k_raw,
     const float* __restrict__ v_raw, const float* __restrict__ q_norm,
-    const float* __restrict__ k_norm, float eps, const double* __restrict__ inv_freq,
+    const float* __restrict__ k_norm, float eps, const float2* __restrict__ rope_cs,
     __half* __restrict__ k_cache, __half* __restrict__ v_cache, int pos, int hd, int nq, int nkv,
     int max_ctx, int nsplit, float* __restrict__ part) {
     extern __shared__ __align__(16) float sm[];
@@ -245,17 +274,33 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
     const uint4* K = reinterpret_cast<const uint4*>(k_cache + ((size_t)kvh * max_ctx + p0) * hd);
     const uint4* V = reinterpret_cast<const uint4*>(v_cache + ((size_t)kvh * max_ctx + p0) * hd);
     const int vpr = hd / 8;                            // uint4 per row
-    for (int i = tid; i < np * vpr; i += ATT_THREADS) {
-        const int row = i / vpr, cc = i - row * vpr;
-        const uint4 kq = __ldg(K + i), vq = __ldg(V + i);
-        uint32_t* kd = ks + row * kw + 4 * cc;
-        kd[0] = kq.x; kd[1] = kq.y; kd[2] = kq.z; kd[3] = kq.w;
-        reinterpret_cast<uint4*>(vs)[i] = vq;
+    {
+        // every thread's share of the tile in flight at once, then stored
+        constexpr int NLD = ATT_CHUNK * 32 / ATT_THREADS;   // uint4 per thread at hd = 256
+        uint4 kq[NLD], vq[NLD];
+#pragma unroll
+        for (int j = 0; j < NLD; ++j) {
+            const int i = tid + j * ATT_THREADS;
+            if (i < np * vpr) {
+                kq[j] = __ldg(K + i);
+                vq[j] = __ldg(V + i);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NLD; ++j) {
+            const int i = tid + j * ATT_THREADS;
+            if (i < np * vpr) {
+                const int row = i / vpr, cc = i - row * vpr;
+                uint32_t* kd = ks + row * kw + 4 * cc;
+                kd[0] = kq[j].x; kd[1] = kq[j].y; kd[2] = kq[j].z; kd[3] = kq[j].w;
+                reinterpret_cast<uint4*>(vs)[i] = vq[j];
+            }
+        }
     }
     // q heads of this kv head: RMSNorm + RoPE (warp per head)
     for (int g = warp; g < group; g += nw) {
         float o[ATT_DPL];
-        norm_rope_warp(q_raw + (size_t)(kvh * group + g) * hd, q_norm, eps, hd, pos, inv_freq, o);
+        norm_rope_warp(q_raw + (size_t)(kvh * group + g) * hd, q_norm, eps, hd, rope_cs, o);
 #pragma unroll
         for (int i = 0; i < ATT_DPL; ++i)
             if (i < hd / 32) qs[g * hd + lane + 32 * i] = o[i];
@@ -264,7 +309,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
     if (pos >= p0 && pos < p1 && warp == 0) {
         // the new token's k and v: cache slot pos and tile row pos - p0
         float o[ATT_DPL];
-        norm_rope_warp(k_raw + (size_t)kvh * hd, k_norm, eps, hd, pos, inv_freq, o);
+        norm_rope_warp(k_raw + (size_t)kvh * hd, k_norm, eps, hd, rope_cs, o);
         __half* kc = k_cache + ((size_t)kvh * max_ctx + pos) * hd;
         __half* vc = v_cache + ((size_t)kvh * max_ctx + pos) * hd;
         __half* kt = reinterpret_cast<__half*>(ks + (pos - p0) * kw);
@@ -283,31 +328,31 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
         }
     }
     __syncthreads();
-    // scores: thread -> position pp, heads [hg*hpt, (hg+1)*hpt)
+    // scores: thread -> position pp, heads [hg*HPT, (hg+1)*HPT)
     const float scale = rsqrtf((float)hd);
-    const int hpt = (group * ATT_CHUNK + ATT_THREADS - 1) / ATT_THREADS;
     {
         const int pp = tid % ATT_CHUNK, hg = tid / ATT_CHUNK;
-        float acc[ATT_HPT];
+        float acc[HPT];
 #pragma unroll
-        for (int g = 0; g < ATT_HPT; ++g) acc[g] = 0.f;
-        if (hg * hpt < group && pp < np) {
+        for (int g = 0; g < HPT; ++g) acc[g] = 0.f;
+        if (hg * HPT < group && pp < np) {
             const uint32_t* kr = ks + pp * kw;
-            for (int d2 = 0; d2 < hd / 2; ++d2) {
-                const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(kr + d2));
+            const float* qh = qs + hg * HPT * hd;
+#pragma unroll 4
+            for (int d2 = 0; d2 < hd / 2; d2 += 2) {
+                const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(kr + d2));
+                const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(kr + d2 + 1));
 #pragma unroll
-                for (int g = 0; g < ATT_HPT; ++g) {
-                    if (g < hpt) {
-                        const float2 qv = *reinterpret_cast<const float2*>(qs + (hg * hpt + g) * hd + 2 * d2);
-                        acc[g] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, acc[g]));
-                    }
+                for (int g = 0; g < HPT; ++g) {
+                    const float4 qv = *reinterpret_cast<const float4*>(qh + g * hd + 2 * d2);
+                    acc[g] = fmaf(qv.x, k0.x, fmaf(qv.y, k0.y, fmaf(qv.z, k1.x, fmaf(qv.w, k1.y, acc[g]))));
                 }
             }
         }
 #pragma unroll
-        for (int g = 0; g < ATT_HPT; ++g)
-            if (g < hpt && hg * hpt + g < group)
-                sc[(hg * hpt + g) * ATT_CHUNK + pp] = pp < np ? acc[g] * scale : -INFINITY;
+        for (int g = 0; g < HPT; ++g)
+            if (hg * HPT + g < group)
+                sc[(hg * HPT + g) * ATT_CHUNK + pp] = pp < np ? acc[g] * scale : -INFINITY;
     }
     __syncthreads();
     // per q head (one warp each, warps loop over heads): max and sum of exp
@@ -429,9 +474,13 @@ cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const
     const int nvalid = a.pos / ATT_CHUNK + 1;
     const int group = a.nq / a.nkv;
     dim3 ga(a.nkv, nvalid);
-    attn_partial<<<ga, ATT_THREADS, attn_smem(group, a.hd), st>>>(
-        q, kv, kv + kvd, L.q_norm, L.k_norm, a.eps, a.inv_freq, L.k_cache, L.v_cache, a.pos, a.hd,
-        a.nq, a.nkv, a.max_ctx, nsplit, part);
+    const int hpt = (group * ATT_CHUNK + ATT_THREADS - 1) / ATT_THREADS;
+#define QMOE_ATT(N)                                                                        \
+    attn_partial<N><<<ga, ATT_THREADS, attn_smem(group, a.hd), st>>>(                      \
+        q, kv, kv + kvd, L.q_norm, L.k_norm, a.eps, a.rope_cs, L.k_cache, L.v_cache, a.pos, \
+        a.hd, a.nq, a.nkv, a.max_ctx, nsplit, part)
+    if (hpt <= 1) QMOE_ATT(1); else if (hpt <= 2) QMOE_ATT(2); else if (hpt <= 4) QMOE_ATT(4); else QMOE_ATT(8);
+#undef QMOE_ATT
     attn_merge<<<a.nq, MRG_THREADS, sizeof(float) * (nvalid + MRG_THREADS), st>>>(
         part, nsplit, nvalid, a.hd, att);
     // B7: h_out = h + Wo att
@@ -446,17 +495,32 @@ cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const
 }
 
 // Shared memory limit of the attention kernel (once per device context) and
-// the shapes it serves: at most 2 * ATT_HPT q heads per kv head, head_dim a
-// multiple of 64 up to 256 with the staged chunk inside ATT_SMEM_MAX.
+// the shapes it serves: at most ATT_HPT * ATT_THREADS / ATT_CHUNK (32) q heads
+// per kv head, head_dim a multiple of 64 up to 256 with the staged chunk inside
+// ATT_SMEM_MAX.
 constexpr int ATT_SMEM_MAX = 200 * 1024;     // dynamic; the kernel also has 256 B static
 
 cudaError_t decode_step_prepare() {
-    return cudaFuncSetAttribute(attn_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                ATT_SMEM_MAX);
+    const void* fns[] = {reinterpret_cast<const void*>(&attn_partial<1>),
+                         reinterpret_cast<const void*>(&attn_partial<2>),
+                         reinterpret_cast<const void*>(&attn_partial<4>),
+                         reinterpret_cast<const void*>(&attn_partial<8>)};
+    for (const void* f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             ATT_SMEM_MAX);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_rope_table(const double* inv_freq, int hd, int pos, float2* cs,
+                              cudaStream_t st) {
+    rope_table<<<1, 128, 0, st>>>(inv_freq, hd / 2, pos, cs);
+    return cudaGetLastError();
 }
 
 bool attention_supported(int nq, int nkv, int hd) {
-    if (nkv < 1 || nq % nkv || nq / nkv > 2 * ATT_HPT) return false;
+    if (nkv < 1 || nq % nkv || (nq / nkv) * ATT_CHUNK > ATT_HPT * ATT_THREADS) return false;
     if (hd < 64 || hd > 32 * ATT_DPL || hd % 64) return false;     // RoPE pairs within a lane
     return attn_smem(nq / nkv, hd) <= (size_t)ATT_SMEM_MAX;
 }

@@ -37,6 +37,7 @@ struct qmoe_ctx {
     float* att;       // [nq*hd]
     float* attn_part; // split-K partials
     double* inv_freq; // [head_dim/2] RoPE frequencies
+    float2* rope_cs;  // [head_dim/2] cos/sin at the current position
     int attn_splits;
 };
 
@@ -68,7 +69,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
         status, bar, xp, actp, inv_pos, logits_part, ftag, xs, q, kv, att, attn_part, inv_freq,
-        total;
+        rope_cs, total;
     int attn_splits;
 };
 
@@ -87,7 +88,8 @@ bool config_ok(const qmoe_config* c, char* why, size_t n) {
         if ((c->n_kv_heads * c->head_dim) % 256 && c->n_kv_heads * c->head_dim % 32) { snprintf(why, n, "bad kv dim"); return false; }
         if (c->max_ctx < 1) { snprintf(why, n, "max_ctx=%d must be >= 1", c->max_ctx); return false; }
         if (!(c->rope_base > 0.f) || !(c->rms_eps > 0.f)) { snprintf(why, n, "rope_base and rms_eps must be positive"); return false; }
-        if (!qmoe::attention_supported(c->n_heads, c->n_kv_heads, c->head_dim)) { snprintf(why, n, "attention shape n_heads=%d n_kv_heads=%d head_dim=%d not served (at most 16 q heads per kv head)", c->n_heads, c->n_kv_heads, c->head_dim); return false; }
+        if (c->hidden > 4096 || c->n_heads * c->head_dim > 4096) { snprintf(why, n, "decode step serves hidden and n_heads*head_dim up to 4096"); return false; }
+        if (!qmoe::attention_supported(c->n_heads, c->n_kv_heads, c->head_dim)) { snprintf(why, n, "attention shape n_heads=%d n_kv_heads=%d head_dim=%d not served (at most 32 q heads per kv head)", c->n_heads, c->n_kv_heads, c->head_dim); return false; }
     }
     return true;
 }
@@ -125,6 +127,7 @@ Layout layout(const qmoe_config* c) {
     L.att = take(sizeof(float) * (qd ? qd : 1));
     L.attn_part = take(sizeof(float) * (size_t)c->n_heads * L.attn_splits * (c->head_dim + 2) + 4);
     L.inv_freq = take(sizeof(double) * (c->head_dim > 0 ? c->head_dim / 2 : 1));
+    L.rope_cs = take(sizeof(float2) * (c->head_dim > 0 ? c->head_dim / 2 : 1));
     L.total = off;
     return L;
 }
@@ -301,6 +304,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->attn_part = reinterpret_cast<float*>(b + L.attn_part);
     c->attn_splits = L.attn_splits;
     c->inv_freq = reinterpret_cast<double*>(b + L.inv_freq);
+    c->rope_cs = reinterpret_cast<float2*>(b + L.rope_cs);
     e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
@@ -420,7 +424,12 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
             return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "layer %d: down qtype %d", l, (int)w.down_t);
     }
     qmoe::AttnShape a{k.hidden, k.n_heads, k.n_kv_heads, k.head_dim, k.max_ctx, pos, k.rms_eps,
-                      k.rope_base, c->inv_freq};
+                      k.rope_base, c->inv_freq, c->rope_cs};
+    {
+        // cos/sin of the RoPE angles at pos: one table for every layer
+        cudaError_t e = qmoe::launch_rope_table(c->inv_freq, k.head_dim, pos, c->rope_cs, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
+    }
     for (int l = 0; l < n_layers; ++l) {
         const qmoe_layer_weights& w = layers[l];
         qmoe::LayerAttn la{w.attn_norm,

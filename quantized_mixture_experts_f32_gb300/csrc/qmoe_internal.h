@@ -100,6 +100,7 @@ struct AttnShape {
     int H, nq, nkv, hd, max_ctx, pos;
     float eps, rope_base;
     const double* inv_freq;   // [hd/2] rope_base^(-2j/hd), device
+    const float2* rope_cs;    // [hd/2] cos/sin of the angles at pos (launch_rope_table)
 };
 struct LayerAttn {
     const float* attn_norm;
@@ -120,6 +121,8 @@ cudaError_t launch_rmsnorm(const float* h, const float* w, float eps, int n, flo
                            cudaStream_t st);
 int attn_splits(int max_ctx);
 cudaError_t decode_step_prepare();
+cudaError_t launch_rope_table(const double* inv_freq, int hd, int pos, float2* cs,
+                              cudaStream_t st);
 bool attention_supported(int nq, int nkv, int hd);
 
 // Prefill path (T > 8): tcgen05 grouped GEMMs with on-the-fly dequantisation.

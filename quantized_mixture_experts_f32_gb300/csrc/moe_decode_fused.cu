@@ -170,9 +170,9 @@ __device__ __forceinline__ bool load_tagged(const unsigned long long* base, int 
 
 // 8 bytes at an even shared-memory address (three aligned words, funnel shift)
 __device__ __forceinline__ uint2 lds8_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = (uint32_t)(a & 3) * 8u;
+    const uint32_t off = smem_u32(p) & 3u;
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(p - off);   // stays a shared pointer
+    const uint32_t sh = off * 8u;
     const uint32_t w0 = b[0], w1 = b[1], w2 = b[2];
     return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
 }

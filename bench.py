@@ -336,12 +336,18 @@ def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index):
     if pg:
         pg.barrier()
     clocks = sampler.stop(t0, t1)
-    ms = e0.elapsed_time(e1)
-    if pg:
-        tt = torch.tensor([ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(torch, e0.elapsed_time(e1), pg, dev)
     return ms, clocks
+
+
+def max_over_ranks(torch, ms, pg, dev):
+    """The slowest rank's time: every rank gets the same value (weak scaling
+    divides the units all ranks processed by it)."""
+    if not pg:
+        return ms
+    tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+    pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+    return float(tt.item())
 
 
 def bench_layer(args, torch, q, dev, stream, ws, pg, local):

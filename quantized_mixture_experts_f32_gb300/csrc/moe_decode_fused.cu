@@ -41,10 +41,10 @@
 
 #ifdef QMOE_PHASE_TRACE
 // per-CTA phase timestamps (%globaltimer), compiled only into diagnostic builds
-__device__ unsigned long long g_qmoe_trace[1024 * 64];
+__device__ unsigned long long g_qmoe_trace[1024 * 128];
 #define QMOE_TRACE(slot)                                                            \
     do {                                                                            \
-        g_qmoe_trace[blockIdx.x * 64 + (slot)] = qmoe::globaltimer();               \
+        g_qmoe_trace[blockIdx.x * 128 + (slot)] = qmoe::globaltimer();              \
     } while (0)
 #else
 #define QMOE_TRACE(slot) \
@@ -76,6 +76,11 @@ struct SmemLayout {
 
 __host__ __device__ inline int al(int v, int a) { return (v + a - 1) / a * a; }
 
+// Staged act index with 4 floats of padding after every 128: the two
+// half-superblocks that the 8 lanes of a down row read at once then use
+// different banks.
+__host__ __device__ __forceinline__ int apad(int f) { return f + 4 * (f >> 7); }
+
 // nloc_max: pairs of the experts one CTA's down rows can touch
 __host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, int nloc_max,
                                                    int slot_bytes, int ns) {
@@ -83,7 +88,7 @@ __host__ __device__ inline SmemLayout fused_layout(int T, int H, int K, int F, i
     const int P = T * K;
     // after gate/up the x region holds act of this CTA's down experts and the
     // group sums of act (groups of 8 or 16; sized for 8)
-    const int act_bytes = al(nloc_max * F * 4, 16);
+    const int act_bytes = al(nloc_max * apad(F) * 4, 16);
     const int asum_bytes = al(nloc_max * (F / 8) * 4, 16);
     int o = 0;
     L.off_bar = o;      o += NSLOT * 8;
@@ -246,8 +251,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     constexpr int RBG = NSB_G * Q4K_BYTES;                        // gate/up row bytes
     constexpr int BBD = DQT == 1 ? Q4K_BYTES : Q6K_BYTES;
     constexpr int RBD = NSB_D * BBD;                              // down row bytes
-    constexpr int NTG = (8 * NSB_G + 31) / 32;                    // gate/up tasks per lane
+    constexpr int NTG = 2;                                        // 16-byte pieces per lane (one chunk)
+    static_assert(NSB_G <= 8, "one 32-byte chunk per lane covers at most 8 superblocks");
     constexpr int GS = DQT == 1 ? 16 : 8;                         // act group of one down scale
+    const int FPAD = apad(F);                                     // staged act row (padded)
+    constexpr int RPASS = 3;                                      // row passes of 4 per down chunk
 
     uint64_t* fullb = reinterpret_cast<uint64_t*>(sm + L.off_bar);
     int* misc = reinterpret_cast<int*>(sm + L.off_misc);
@@ -412,6 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     // CTA's share of the work, so that the weight copies start right after.
     float* lg_s = reinterpret_cast<float*>(ring);                 // ring is idle until phase C
     int32_t* sel = reinterpret_cast<int32_t*>(lg_s + T * E);      // [T][K]
+    int32_t* keys = sel + P;                                      // [T][E] order keys
     {
         constexpr int LPT = 2;                                     // logits per thread (T*E <= 1024)
         float v[LPT];
@@ -421,7 +430,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         }
 #pragma unroll
         for (int z = 0; z < LPT; ++z)
-            if (tid + z * NTHREADS < T * E) lg_s[tid + z * NTHREADS] = v[z];
+            if (tid + z * NTHREADS < T * E) {
+                lg_s[tid + z * NTHREADS] = v[z];
+                keys[tid + z * NTHREADS] = order_key(v[z]);
+            }
     }
     for (int i = tid; i < P; i += NTHREADS) sel[i] = 0;
     __syncthreads();
@@ -437,11 +449,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             const int i = tid / tpe, sub = tid - (tid / tpe) * tpe;
             const bool valid = i < nel;
             const int t = valid ? i / E : 0, e = valid ? i - t * E : 0;
-            const float* l = lg_s + t * E;
-            const int v = order_key(l[e]);
+            const int* l = keys + t * E;
+            const int v = l[e];
             int rank = 0;
+#pragma unroll 8
             for (int e2 = sub; e2 < E; e2 += tpe) {
-                const int w = order_key(l[e2]);
+                const int w = l[e2];
                 rank += (w > v) || (w == v && e2 < e);
             }
             for (int o = tpe >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
@@ -449,11 +462,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         } else {
             for (int i = tid; i < nel; i += NTHREADS) {
                 const int t = i / E, e = i - t * E;
-                const float* l = lg_s + t * E;
-                const int v = order_key(l[e]);
+                const int* l = keys + t * E;
+                const int v = l[e];
                 int rank = 0;
+#pragma unroll 8
                 for (int e2 = 0; e2 < E; ++e2) {
-                    const int w = order_key(l[e2]);
+                    const int w = l[e2];
                     rank += (w > v) || (w == v && e2 < e);
                 }
                 if (rank < K) sel[t * K + rank] = e;
@@ -531,7 +545,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         // rows in expert order, each weighted by 1 + the expert's pair count
         // (one row load, one dot product per pair); CTA c owns the rows whose
         // weighted position falls in [c*W/G, (c+1)*W/G): a few experts at most.
-        const int RPC = (SB - 32) / RBD;
+        const int RPC = min((SB - 32) / RBD, 4 * RPASS);
         {
             const long long W = (long long)H * (P + nu);
             const long long wlo = W * c / G, whi = W * (c + 1) / G;
@@ -605,7 +619,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     if (tid == 0) QMOE_TRACE(3);
     const int n_ch = misc[M_NCH], n_gu = misc[M_NGU];
     const int gu_lo = misc[M_GULO], nseg = misc[M_NSEG];
-    const int CPE = F / p.cf, RPC = (SB - 32) / RBD;
+    const int CPE = F / p.cf, RPC = min((SB - 32) / RBD, 4 * RPASS);
     // chunk k -> (is_gu, used index u, start row, row count)
     auto decode = [&](int k, int& u, int& start, int& cnt) -> bool {
         if (k < n_gu) {
@@ -680,12 +694,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                     const int t = pr / K;
                     if (t != xtok) {
                         xtok = t;
+                        // lane -> 32-byte chunk c of superblock sb (both its 16-byte
+                        // pieces, which share one scale/min pair)
 #pragma unroll
                         for (int jt = 0; jt < NTG; ++jt) {
-                            const int tsk = lane + 32 * jt;
-                            const int sb = tsk >> 3, pc = tsk & 7;
-                            if (tsk < 8 * NSB_G) {
-                                const int col = QK * sb + 64 * (pc >> 1) + 16 * (pc & 1);
+                            if (lane < 4 * NSB_G) {
+                                const int sb = lane >> 2, c = lane & 3;
+                                const int col = QK * sb + 64 * c + 16 * jt;
                                 const int ga = t * (H / 16) + col / 16, gb = ga + 2;
                                 const int4* pa = reinterpret_cast<const int4*>(xq + 12 * ga);
                                 const int4* pb = reinterpret_cast<const int4*>(xq + 12 * gb);
@@ -704,29 +719,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                     }
                     if (lane == 0 && warp == 0 && j == 0) QMOE_TRACE(10);
                     for (int i = 0; i < nf; ++i) {
-                        // gate row i and up row i, all of this lane's pieces at once
+                        // gate row i and up row i: this lane's chunk of each
                         float g = 0.f, v = 0.f;
-                        uint4 hd[2 * NTG], qd[2 * NTG];
+                        if (lane < 4 * NSB_G) {
+                            const int sb = lane >> 2, c = lane & 3;
+                            uint4 hd[2], qd[2][2];
 #pragma unroll
-                        for (int z = 0; z < 2 * NTG; ++z) {
-                            const int jt = z >> 1, tsk = lane + 32 * jt;
-                            if (tsk < 8 * NSB_G) {
-                                const int sb = tsk >> 3, pc = tsk & 7;
-                                const int row = (z & 1) ? nf + i : i;
-                                const uint8_t* b = slot + row * RBG + sb * Q4K_BYTES;
-                                hd[z] = *reinterpret_cast<const uint4*>(b);
-                                qd[z] = *reinterpret_cast<const uint4*>(b + 16 + 16 * pc);
+                            for (int gu = 0; gu < 2; ++gu) {
+                                const uint8_t* b = slot + (gu ? nf + i : i) * RBG + sb * Q4K_BYTES;
+                                hd[gu] = *reinterpret_cast<const uint4*>(b);
+                                qd[gu][0] = *reinterpret_cast<const uint4*>(b + 16 + 32 * c);
+                                qd[gu][1] = *reinterpret_cast<const uint4*>(b + 32 + 32 * c);
                             }
-                        }
 #pragma unroll
-                        for (int z = 0; z < 2 * NTG; ++z) {
-                            const int jt = z >> 1, tsk = lane + 32 * jt;
-                            if (tsk < 8 * NSB_G) {
-                                const int pc = tsk & 7;
-                                float QA, QB;
-                                q4_piece_dp4a(qd[z], xa[jt], xb[jt], SXA[jt], SXB[jt], QA, QB);
-                                const float c = q4_piece_finish_exact(hd[z], pc, QA, QB, XA[jt], XB[jt]);
-                                if (z & 1) v += c; else g += c;
+                            for (int gu = 0; gu < 2; ++gu) {
+                                float QA0, QB0, QA1, QB1;
+                                q4_piece_dp4a(qd[gu][0], xa[0], xb[0], SXA[0], SXB[0], QA0, QB0);
+                                q4_piece_dp4a(qd[gu][1], xa[1], xb[1], SXA[1], SXB[1], QA1, QB1);
+                                const float cc = q4_piece_finish_exact(hd[gu], 2 * c, QA0 + QA1, QB0 + QB1,
+                                                                       XA[0] + XA[1], XB[0] + XB[1]);
+                                if (gu) v += cc; else g += cc;
                             }
                         }
                         // lanes 0-15 end with the gate sum, lanes 16-31 with the up sum
@@ -769,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                 for (int z = 0; z < GS; ++z) s += v[z];
 #pragma unroll
                 for (int z = 0; z < GS; z += 4)
-                    *reinterpret_cast<float4*>(act_s + (size_t)lp * F + g * GS + z) =
+                    *reinterpret_cast<float4*>(act_s + (size_t)lp * FPAD + apad(g * GS + z)) =
                         make_float4(v[z], v[z + 1], v[z + 2], v[z + 3]);
                 asum[i] = s;
             }
@@ -787,6 +799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
             const int k = warp + NCW * j;
             const int s = warp + NCW * (j % NS);
             const bool ok = __all_sync(0xffffffffu, mbar_wait(&fullb[s], (uint32_t)(j / NS) & 1u));
+            if (lane == 0 && warp + NCW * j >= n_gu && warp + NCW * (j - 1) < n_gu) QMOE_TRACE(64 + warp);
             if (!ok) { if (lane == 0) { set_status(p.status, ST_TIMEOUT); misc[M_ABORT] = 1; } }
             if (__all_sync(0xffffffffu, ok && misc[M_ABORT] == 0)) {
                 int u, r0, nr;
@@ -797,26 +810,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                 const int q0 = used_first[u], q1 = used_first[u + 1];
                 for (int qi = q0; qi < q1; ++qi) {
                     const int pr = pairs[qi];
-                    const float* a = act_s + (size_t)(qi - qbase) * F;
+                    const float* a = act_s + (size_t)(qi - qbase) * FPAD;
                     const float* as = asum + (size_t)(qi - qbase) * (F / GS);
-                    for (int rb = 0; rb < nr; rb += 4) {
-                        const int r = rb + rr;
-                        float acc = 0.f;
-                        if (r < nr) {
-                            const uint8_t* row = slot + (size_t)r * RBD;
+                    if (DQT == 2) {
+                        // Q6_K: lane (kk) owns positions 8m..8m+7 of the 4 groups of
+                        // half n of every superblock; its act values are loaded once
+                        // per superblock and reused for every row pass (rows rr,
+                        // rr+4, rr+8 of the chunk)
+                        const int n = kk >> 2, m = kk & 3;
+                        float acc[RPASS];
 #pragma unroll
-                            for (int sb = 0; sb < NSB_D; ++sb) {
-                                if (DQT == 2) {
-                                    const int n = kk >> 2, m = kk & 3;
-                                    const uint8_t* blk = row + sb * Q6K_BYTES;
+                        for (int rb = 0; rb < RPASS; ++rb) acc[rb] = 0.f;
+#pragma unroll 1
+                        for (int sb = 0; sb < NSB_D; ++sb) {
+                            const float* ab = a + apad(QK * sb + 128 * n) + 8 * m;
+                            const float* asb = as + (QK * sb + 128 * n + 8 * m) / 8;
+                            float4 xv[4][2];
+                            float xs[4];
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                xv[g][0] = *reinterpret_cast<const float4*>(ab + 32 * g);
+                                xv[g][1] = *reinterpret_cast<const float4*>(ab + 32 * g + 4);
+                                xs[g] = asb[4 * g];
+                            }
+#pragma unroll
+                            for (int rb = 0; rb < RPASS; ++rb) {
+                                const int r = 4 * rb + rr;
+                                if (r < nr) {
+                                    const uint8_t* blk = slot + (size_t)r * RBD + sb * Q6K_BYTES;
                                     const uint2 qa = lds8_a2(blk + 64 * n + 8 * m);
                                     const uint2 qb = lds8_a2(blk + 64 * n + 32 + 8 * m);
                                     const uint2 qh = lds8_a2(blk + 128 + 32 * n + 8 * m);
                                     const uint2 scw = lds8_a2(blk + 192 + 8 * n);
                                     const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
                                     const int sb0 = (m >> 1) * 8;
-                                    const float* ab = a + QK * sb + 128 * n + 8 * m;
-                                    const float* asb = as + (QK * sb + 128 * n + 8 * m) / 8;
 #pragma unroll
                                     for (int g = 0; g < 4; ++g) {
                                         const int bo = sb0 + 16 * g;
@@ -832,39 +859,72 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                                             else if (g == 1) q6 = (B & 0x0F0F0F0Fu) | ((Hh << 2) & 0x30303030u);
                                             else if (g == 2) q6 = ((A >> 4) & 0x0F0F0F0Fu) | (Hh & 0x30303030u);
                                             else q6 = ((B >> 4) & 0x0F0F0F0Fu) | ((Hh >> 2) & 0x30303030u);
-                                            const float4 xv = *reinterpret_cast<const float4*>(ab + 32 * g + 4 * hf);
-                                            fma2(p0, p1, mag<0>(q6), mag<1>(q6), xv.x, xv.y);
-                                            fma2(p0, p1, mag<2>(q6), mag<3>(q6), xv.z, xv.w);
+                                            const float4 x4 = xv[g][hf];
+                                            fma2(p0, p1, mag<0>(q6), mag<1>(q6), x4.x, x4.y);
+                                            fma2(p0, p1, mag<2>(q6), mag<3>(q6), x4.z, x4.w);
                                         }
-                                        acc = fmaf(d * sc, fmaf(256.f, p0 + p1, -160.f * asb[4 * g]), acc);
+                                        acc[rb] = fmaf(d * sc, fmaf(256.f, p0 + p1, -160.f * xs[g]), acc[rb]);
                                     }
-                                } else {
-                                    const int pc = kk;
-                                    const uint8_t* blk = row + sb * Q4K_BYTES;
-                                    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-                                    const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 16 * pc);
-                                    const int col = QK * sb + 64 * (pc >> 1) + 16 * (pc & 1);
-                                    float4 va[4], vb[4];
-#pragma unroll
-                                    for (int z = 0; z < 4; ++z) {
-                                        va[z] = *reinterpret_cast<const float4*>(a + col + 4 * z);
-                                        vb[z] = *reinterpret_cast<const float4*>(a + col + 32 + 4 * z);
-                                    }
-                                    float PA, PB;
-                                    q4_piece_regs(q, va, vb, PA, PB);
-                                    acc += q4_piece_finish(hdr, pc, PA, PB, as[col / 16], as[col / 16 + 2]);
                                 }
                             }
                         }
-                        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-                        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                        if (r < nr && kk == 0)
-                            st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(acc, tag));
+#pragma unroll
+                        for (int rb = 0; rb < RPASS; ++rb) {
+                            float v = acc[rb];
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            v += __shfl_xor_sync(0xffffffffu, v, 2);
+                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                            const int r = 4 * rb + rr;
+                            if (r < nr && kk == 0)
+                                st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(v, tag));
+                        }
+                    } else {
+                        // Q4_K: lane (kk) owns 16-byte piece kk of every superblock;
+                        // its 32 act values are loaded once per superblock and reused
+                        // for every row pass
+                        const int pc = kk;
+                        float acc[RPASS];
+#pragma unroll
+                        for (int rb = 0; rb < RPASS; ++rb) acc[rb] = 0.f;
+#pragma unroll 1
+                        for (int sb = 0; sb < NSB_D; ++sb) {
+                            const int col = QK * sb + 64 * (pc >> 1) + 16 * (pc & 1);
+                            const float* ac = a + apad(col);
+                            float4 va[4], vb[4];
+#pragma unroll
+                            for (int z = 0; z < 4; ++z) {
+                                va[z] = *reinterpret_cast<const float4*>(ac + 4 * z);
+                                vb[z] = *reinterpret_cast<const float4*>(ac + 32 + 4 * z);
+                            }
+                            const float XA = as[col / 16], XB = as[col / 16 + 2];
+#pragma unroll
+                            for (int rb = 0; rb < RPASS; ++rb) {
+                                const int r = 4 * rb + rr;
+                                if (r < nr) {
+                                    const uint8_t* blk = slot + (size_t)r * RBD + sb * Q4K_BYTES;
+                                    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+                                    const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 16 * pc);
+                                    float PA, PB;
+                                    q4_piece_regs(q, va, vb, PA, PB);
+                                    acc[rb] += q4_piece_finish(hdr, pc, PA, PB, XA, XB);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int rb = 0; rb < RPASS; ++rb) {
+                            float v = acc[rb];
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            v += __shfl_xor_sync(0xffffffffu, v, 2);
+                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                            const int r = 4 * rb + rr;
+                            if (r < nr && kk == 0)
+                                st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(v, tag));
+                        }
                     }
                 }
             }
             __syncwarp();
+            if (lane == 0 && warp + NCW * j >= n_gu && warp + NCW * (j - 1) < n_gu) QMOE_TRACE(80 + warp);
             if (lane == 0 && warp == 0) QMOE_TRACE(15);
             if (lane == 0) issue(j + NS);
         }
@@ -900,6 +960,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         }
         if (!ok) set_status(p.status, ST_TIMEOUT);
     }
+    if (tid == 0) QMOE_TRACE(12);
     __syncthreads();
     if (tid == 0) QMOE_TRACE(8);
     if (tid == 0) {
@@ -976,7 +1037,7 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
     SmemLayout L = fused_layout(s.T, s.H, s.K, s.F, nloc_max, sb, ns);
     while (L.total > SMEM_MAX && ns > 2) L = fused_layout(s.T, s.H, s.K, s.F, nloc_max, sb, --ns);
     if (L.total > SMEM_MAX) return false;
-    if (s.T * s.E * 4 + P * 4 > NCW * ns * sb) return false;   // routing scratch in the ring
+    if (2 * s.T * s.E * 4 + P * 4 > NCW * ns * sb) return false;   // routing scratch in the ring
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
     // f rows per gate/up chunk: the largest power of two that fits the slot and

@@ -1041,9 +1041,10 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
     // f rows per gate/up chunk: the largest power of two that fits the slot and
-    // divides F
+    // divides F; one token keeps single-row chunks (a CTA's share of ~40 rows
+    // then spreads over its 16 warps at 2-3 rows each instead of 2-4)
     int cf = 1;
-    while (2 * (2 * cf) * rbg <= sb && s.F % (2 * cf) == 0) cf *= 2;
+    while (s.T > 1 && 2 * (2 * cf) * rbg <= sb && s.F % (2 * cf) == 0) cf *= 2;
     if (cf < 1 || (sb - 32) / rbd < 1) return false;
     plan->cf = cf;
     plan->ns = ns;

@@ -49,11 +49,17 @@ WORKLOADS = {
                     desc="qwen3moe-30b-a3b MoE layer prefill, T=512, biased router, Q6_K down"),
     "step48": dict(cfg=None, copies=1, e2e=10, steps=400, warmup=3,
                    desc="qwen3moe-30b-a3b 48-layer decode step, T=1, context 4096"),
+    # supplementary (not one of the five configurations): the prefill layer at
+    # T=4096, where the contraction is compute-bound and the tensor-pipe
+    # fraction is the meaningful one
+    "prefill4096": dict(cfg=4, T=4096, copies=2, e2e=5, steps=60, warmup=3,
+                        desc="qwen3moe-30b-a3b MoE layer prefill, T=4096, biased router, Q6_K "
+                             "down (supplementary)"),
 }
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_fused_decode_T1.md", "batch8": None, "prefill": None,
-               "step48": None}
+               "step48": None, "prefill4096": None}
 FUSED_SOURCES = ["moe_decode_fused.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -352,7 +358,7 @@ def max_over_ranks(torch, ms, pg, dev):
 
 def bench_layer(args, torch, q, dev, stream, ws, pg, local):
     w = WORKLOADS[args.workload]
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[w["cfg"]])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS[w["cfg"]], T=w.get("T"))
     T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
     gt, ut, dt = q.QTYPE[inp["gate_t"]], q.QTYPE[inp["up_t"]], q.QTYPE[inp["down_t"]]
     x = torch.from_numpy(inp["x"]).to(dev)

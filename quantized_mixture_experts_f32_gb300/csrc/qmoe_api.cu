@@ -430,6 +430,11 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
         cudaError_t e = qmoe::launch_rope_table(c->inv_freq, k.head_dim, pos, c->rope_cs, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
     }
+    // the hidden state alternates between `hidden` and the context's staging
+    // row: the fused MoE layer then never writes over its own input (no wait
+    // for every CTA to have staged x before the first output row)
+    float* cur = hidden;
+    float* other = c->hout;
     for (int l = 0; l < n_layers; ++l) {
         const qmoe_layer_weights& w = layers[l];
         qmoe::LayerAttn la{w.attn_norm,
@@ -442,8 +447,8 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
                            static_cast<__half*>(w.k_cache),
                            static_cast<__half*>(w.v_cache)};
         // B1-B7: h += Wo attn(...)
-        cudaError_t e = qmoe::launch_attention_block(a, la, hidden, c->xs, c->q, c->kv, c->att,
-                                                     c->attn_part, hidden, c->stream);
+        cudaError_t e = qmoe::launch_attention_block(a, la, cur, c->xs, c->q, c->kv, c->att,
+                                                     c->attn_part, cur, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
         // B8 + B9: h = h + MoE(RMSNorm(h) * ffn_norm); the fused decode kernel
         // normalises x itself, other paths take a separate normalisation
@@ -452,19 +457,27 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
         qmoe::FusedPlan plan;
         if (qmoe::fused_decode_plan(ms, QMOE_Q4_K, QMOE_Q4_K, w.down_t, c->num_sms, &plan)) {
             e = qmoe::launch_fused_decode(
-                ms, plan, hidden, hidden, nullptr, w.router_w,
+                ms, plan, cur, cur, nullptr, w.router_w,
                 static_cast<const uint8_t*>(w.gate_exps), static_cast<const uint8_t*>(w.up_exps),
-                static_cast<const uint8_t*>(w.down_exps), hidden, ids_l, nullptr, c->fb,
+                static_cast<const uint8_t*>(w.down_exps), other, ids_l, nullptr, c->fb,
                 w.ffn_norm, k.rms_eps, c->stream);
             if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
+            float* t = cur;
+            cur = other;
+            other = t;
         } else {
-            e = qmoe::launch_rmsnorm(hidden, w.ffn_norm, k.rms_eps, k.hidden, c->xs, c->stream);
+            e = qmoe::launch_rmsnorm(cur, w.ffn_norm, k.rms_eps, k.hidden, c->xs, c->stream);
             if (e != cudaSuccess) return cuda_fail(c, e, "ffn norm launch");
-            qmoe_status st = run_moe(c, c->xs, hidden, nullptr, w.router_w, w.gate_exps,
+            qmoe_status st = run_moe(c, c->xs, cur, nullptr, w.router_w, w.gate_exps,
                                      w.up_exps, w.down_exps, QMOE_Q4_K, QMOE_Q4_K, w.down_t, 1,
-                                     hidden, ids_l, nullptr);
+                                     cur, ids_l, nullptr);
             if (st != QMOE_OK) return st;
         }
+    }
+    if (cur != hidden) {
+        cudaError_t e = cudaMemcpyAsync(hidden, cur, sizeof(float) * k.hidden,
+                                        cudaMemcpyDeviceToDevice, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "hidden copy");
     }
     c->err[0] = 0;
     return QMOE_OK;

@@ -526,6 +526,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         int u = incl - cw;
         for (uint32_t w = word; w; w &= w - 1u) used_e[u++] = lane * 32 + __ffs(w) - 1;
         __syncwarp();
+        // Start the selected experts' bytes moving now: CTA c prefetches into L2
+        // its 1/G share of the concatenated (gate, up, down) slices of the used
+        // experts; the bulk copies issued after the split then find them there.
+        {
+            const long long gu_b = (long long)F * RBG, dn_b = (long long)H * RBD;
+            const long long per = 2 * gu_b + dn_b, tot = per * nu;
+            const long long lo = tot * c / G, hi = tot * (c + 1) / G;
+            for (int piece = lane; piece < 3 * nu; piece += 32) {
+                const int uu = piece / 3, part = piece - 3 * uu;
+                const long long p0 = per * uu + (part == 0 ? 0 : part == 1 ? gu_b : 2 * gu_b);
+                const long long p1 = p0 + (part == 2 ? dn_b : gu_b);
+                const long long a0 = lo > p0 ? lo : p0, a1 = hi < p1 ? hi : p1;
+                if (a1 > a0) {
+                    const int e = used_e[uu];
+                    const uint8_t* base = part == 0 ? p.gate + (size_t)e * gu_b
+                                        : part == 1 ? p.up + (size_t)e * gu_b
+                                                    : p.down + (size_t)e * dn_b;
+                    const long long o0 = (a0 - p0) & ~15ll, o1 = ((a1 - p0) + 15) & ~15ll;
+                    const long long len = (o1 < p1 - p0 ? o1 : p1 - p0) - o0;
+                    if (len > 0) bulk_prefetch_l2(base + o0, (uint32_t)(len & ~15ll));
+                }
+            }
+        }
         // first pair of used expert u = number of pairs with a smaller expert id
         for (int uu = lane; uu < nu; uu += 32) {
             const int e = used_e[uu];

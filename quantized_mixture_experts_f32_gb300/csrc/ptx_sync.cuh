@@ -108,6 +108,11 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// L2 prefetch of `bytes` (multiple of 16) at a 16-byte aligned global address
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Tagged values: a float and the tag of the launch that wrote it, in one
 // 64-bit word that is stored and loaded in one access.  A reader that sees its
 // own launch's tag has the value itself, so no fence or counter is needed to

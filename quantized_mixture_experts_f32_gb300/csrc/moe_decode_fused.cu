@@ -182,6 +182,16 @@ __device__ __forceinline__ uint2 lds8_a2(const uint8_t* p) {
     return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
 }
 
+// 16 bytes at an even shared-memory address (five aligned words, funnel shift)
+__device__ __forceinline__ uint4 lds16_a2(const uint8_t* p) {
+    const uint32_t off = smem_u32(p) & 3u;
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(p - off);   // stays a shared pointer
+    const uint32_t sh = off * 8u;
+    const uint32_t w0 = b[0], w1 = b[1], w2 = b[2], w3 = b[3], w4 = b[4];
+    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                      __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
 // one 16-byte Q4_K nibble piece against 32 x values held in registers
 __device__ __forceinline__ void q4_piece_regs(uint4 q, const float4 (&xa)[4], const float4 (&xb)[4],
                                               float& PA, float& PB) {
@@ -568,7 +578,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
         // rows in expert order, each weighted by 1 + the expert's pair count
         // (one row load, one dot product per pair); CTA c owns the rows whose
         // weighted position falls in [c*W/G, (c+1)*W/G): a few experts at most.
-        const int RPC = min((SB - 32) / RBD, 4 * RPASS);
+        const int RPC = min((SB - 32) / RBD, DQT == 2 ? 8 : 4 * RPASS);
         {
             const long long W = (long long)H * (P + nu);
             const long long wlo = W * c / G, whi = W * (c + 1) / G;
@@ -642,7 +652,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     if (tid == 0) QMOE_TRACE(3);
     const int n_ch = misc[M_NCH], n_gu = misc[M_NGU];
     const int gu_lo = misc[M_GULO], nseg = misc[M_NSEG];
-    const int CPE = F / p.cf, RPC = min((SB - 32) / RBD, 4 * RPASS);
+    const int CPE = F / p.cf, RPC = min((SB - 32) / RBD, DQT == 2 ? 8 : 4 * RPASS);
     // chunk k -> (is_gu, used index u, start row, row count)
     auto decode = [&](int k, int& u, int& start, int& cnt) -> bool {
         if (k < n_gu) {
@@ -836,71 +846,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
                     const float* a = act_s + (size_t)(qi - qbase) * FPAD;
                     const float* as = asum + (size_t)(qi - qbase) * (F / GS);
                     if (DQT == 2) {
-                        // Q6_K: lane (kk) owns positions 8m..8m+7 of the 4 groups of
-                        // half n of every superblock; its act values are loaded once
-                        // per superblock and reused for every row pass (rows rr,
-                        // rr+4, rr+8 of the chunk)
-                        const int n = kk >> 2, m = kk & 3;
-                        float acc[RPASS];
-#pragma unroll
-                        for (int rb = 0; rb < RPASS; ++rb) acc[rb] = 0.f;
+                        // Q6_K: four lanes per row (lane = 4 r + 2 n + qq): half n of
+                        // every superblock, positions l = 16 qq .. 16 qq + 15 of its four
+                        // groups; every row of the chunk in one pass, each lane reading
+                        // 16-byte runs of its row once; act broadcast across rows
+                        const int r = lane >> 2, n = (lane >> 1) & 1, qq = lane & 1;
+                        float acc = 0.f;
+                        if (r < nr) {
 #pragma unroll 1
-                        for (int sb = 0; sb < NSB_D; ++sb) {
-                            const float* ab = a + apad(QK * sb + 128 * n) + 8 * m;
-                            const float* asb = as + (QK * sb + 128 * n + 8 * m) / 8;
-                            float4 xv[4][2];
-                            float xs[4];
+                            for (int sb = 0; sb < NSB_D; ++sb) {
+                                const uint8_t* blk = slot + (size_t)r * RBD + sb * Q6K_BYTES;
+                                const uint4 qa = lds16_a2(blk + 64 * n + 16 * qq);
+                                const uint4 qb = lds16_a2(blk + 64 * n + 32 + 16 * qq);
+                                const uint4 qh = lds16_a2(blk + 128 + 32 * n + 16 * qq);
+                                const uint2 scw = lds8_a2(blk + 192 + 8 * n);
+                                const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                                const float* ab = a + apad(QK * sb + 128 * n) + 16 * qq;
+                                const float* asb = as + (QK * sb + 128 * n + 16 * qq) / 8;
+                                const uint32_t A4[4] = {qa.x, qa.y, qa.z, qa.w};
+                                const uint32_t B4[4] = {qb.x, qb.y, qb.z, qb.w};
+                                const uint32_t H4[4] = {qh.x, qh.y, qh.z, qh.w};
 #pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                xv[g][0] = *reinterpret_cast<const float4*>(ab + 32 * g);
-                                xv[g][1] = *reinterpret_cast<const float4*>(ab + 32 * g + 4);
-                                xs[g] = asb[4 * g];
-                            }
+                                for (int g = 0; g < 4; ++g) {
+                                    const int bo = 8 * (2 * g + qq);         // scale byte of (g, qq)
+                                    const uint32_t sw = bo < 32 ? (scw.x >> bo) : (scw.y >> (bo - 32));
+                                    const float sc = (float)(int8_t)(sw & 0xFF);
+                                    float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-                            for (int rb = 0; rb < RPASS; ++rb) {
-                                const int r = 4 * rb + rr;
-                                if (r < nr) {
-                                    const uint8_t* blk = slot + (size_t)r * RBD + sb * Q6K_BYTES;
-                                    const uint2 qa = lds8_a2(blk + 64 * n + 8 * m);
-                                    const uint2 qb = lds8_a2(blk + 64 * n + 32 + 8 * m);
-                                    const uint2 qh = lds8_a2(blk + 128 + 32 * n + 8 * m);
-                                    const uint2 scw = lds8_a2(blk + 192 + 8 * n);
-                                    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-                                    const int sb0 = (m >> 1) * 8;
-#pragma unroll
-                                    for (int g = 0; g < 4; ++g) {
-                                        const int bo = sb0 + 16 * g;
-                                        const uint32_t sw = bo < 32 ? (scw.x >> bo) : (scw.y >> (bo - 32));
-                                        const float sc = (float)(int8_t)(sw & 0xFF);
-                                        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-                                        for (int hf = 0; hf < 2; ++hf) {
-                                            const uint32_t A = hf ? qa.y : qa.x, B = hf ? qb.y : qb.x;
-                                            const uint32_t Hh = hf ? qh.y : qh.x;
-                                            uint32_t q6;
-                                            if (g == 0) q6 = (A & 0x0F0F0F0Fu) | ((Hh << 4) & 0x30303030u);
-                                            else if (g == 1) q6 = (B & 0x0F0F0F0Fu) | ((Hh << 2) & 0x30303030u);
-                                            else if (g == 2) q6 = ((A >> 4) & 0x0F0F0F0Fu) | (Hh & 0x30303030u);
-                                            else q6 = ((B >> 4) & 0x0F0F0F0Fu) | ((Hh >> 2) & 0x30303030u);
-                                            const float4 x4 = xv[g][hf];
-                                            fma2(p0, p1, mag<0>(q6), mag<1>(q6), x4.x, x4.y);
-                                            fma2(p0, p1, mag<2>(q6), mag<3>(q6), x4.z, x4.w);
-                                        }
-                                        acc[rb] = fmaf(d * sc, fmaf(256.f, p0 + p1, -160.f * xs[g]), acc[rb]);
+                                    for (int wq = 0; wq < 4; ++wq) {
+                                        const uint32_t Aw = A4[wq], Bw = B4[wq], Hh = H4[wq];
+                                        uint32_t q6;
+                                        if (g == 0) q6 = (Aw & 0x0F0F0F0Fu) | ((Hh << 4) & 0x30303030u);
+                                        else if (g == 1) q6 = (Bw & 0x0F0F0F0Fu) | ((Hh << 2) & 0x30303030u);
+                                        else if (g == 2) q6 = ((Aw >> 4) & 0x0F0F0F0Fu) | (Hh & 0x30303030u);
+                                        else q6 = ((Bw >> 4) & 0x0F0F0F0Fu) | ((Hh >> 2) & 0x30303030u);
+                                        const float4 x4 = *reinterpret_cast<const float4*>(ab + 32 * g + 4 * wq);
+                                        fma2(p0, p1, mag<0>(q6), mag<1>(q6), x4.x, x4.y);
+                                        fma2(p0, p1, mag<2>(q6), mag<3>(q6), x4.z, x4.w);
                                     }
+                                    const float xsg = asb[4 * g] + asb[4 * g + 1];
+                                    acc = fmaf(d * sc, fmaf(256.f, p0 + p1, -160.f * xsg), acc);
                                 }
                             }
                         }
-#pragma unroll
-                        for (int rb = 0; rb < RPASS; ++rb) {
-                            float v = acc[rb];
-                            v += __shfl_xor_sync(0xffffffffu, v, 4);
-                            v += __shfl_xor_sync(0xffffffffu, v, 2);
-                            v += __shfl_xor_sync(0xffffffffu, v, 1);
-                            const int r = 4 * rb + rr;
-                            if (r < nr && kk == 0)
-                                st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(v, tag));
-                        }
+                        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                        if (r < nr && (lane & 3) == 0)
+                            st_relaxed_u64(p.y + (size_t)pr * H + r0 + r, tag_pack(acc, tag));
                     } else {
                         // Q4_K: lane (kk) owns 16-byte piece kk of every superblock;
                         // its 32 act values are loaded once per superblock and reused

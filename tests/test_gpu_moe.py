@@ -258,3 +258,28 @@ def test_guard_band_untouched(q):
     G.check(inp, got, TOL_FP32)
     for n, buf in bufs.items():
         assert torch.all(buf[:pad] == 0xA5) and torch.all(buf[-pad:] == 0xA5)
+
+
+@pytest.mark.parametrize("T", [1, 8, 33])
+def test_nan_token_stays_local(q, T):
+    """A token whose activations are NaN gets NaN logits; ranking on order keys
+    still yields a valid expert selection, so no kernel waits on a value that
+    never comes (the status stays OK), and every other token is unaffected."""
+    inp = synth.moe_inputs(synth.MOE_CONFIGS[3], T=T)
+    bad = T // 2
+    inp["x"] = inp["x"].copy()
+    inp["x"][bad, 5] = np.nan
+    d = G.upload(inp)
+    ctx = G.make_ctx(q, inp)
+    try:
+        got = G.run(q, ctx, inp, d)          # asserts QMOE_OK
+    finally:
+        q.qmoe_destroy(ctx)
+    assert ((got["ids"] >= 0) & (got["ids"] < inp["E"])).all()
+    assert not np.isfinite(got["out"][bad]).all()
+    keep = [t for t in range(T) if t != bad]
+    if keep:
+        sub = dict(inp, T=len(keep), x=inp["x"][keep])
+        ref = oracle.moe_forward(sub)
+        tol = TOL_FP32 if T <= 8 else TOL_BF16
+        assert rel_err(got["out"][keep], ref["out"]) <= tol

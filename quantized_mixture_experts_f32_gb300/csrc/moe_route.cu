@@ -187,12 +187,19 @@ constexpr int RG_LD = RG_K + 4;                    // padded smem row (floats)
 __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restrict__ x,
                                                           const float* __restrict__ wr, int T,
                                                           int H, int E,
-                                                          float* __restrict__ part) {
+                                                          float* __restrict__ part,
+                                                          uint32_t* __restrict__ clear, int nclear) {
     extern __shared__ float4 rg_smem4[];
     float* xs = reinterpret_cast<float*>(rg_smem4);              // [RG_T][RG_LD]
     float* ws = xs + RG_T * RG_LD;                               // [RG_E][RG_LD]
     const int e0 = blockIdx.x * RG_E, t0 = blockIdx.y * RG_T, k0 = blockIdx.z * RG_K;
     const int tid = threadIdx.x;
+    // the token bitmap and counts that topk_rank fills start from zero
+    {
+        const int nb = gridDim.x * gridDim.y * gridDim.z;
+        const int b = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        for (int i = b * RG_THREADS + tid; i < nclear; i += nb * RG_THREADS) clear[i] = 0u;
+    }
     // 64 rows x 32 float4 per operand, 8 float4 per thread each, all in flight
     float4 vx[8], vw[8];
 #pragma unroll
@@ -245,19 +252,38 @@ __global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part,
                                                  const float* __restrict__ bias, int T, int E,
                                                  int K, int norm, float* __restrict__ logits,
                                                  int32_t* __restrict__ ids,
-                                                 float* __restrict__ wts) {
+                                                 float* __restrict__ wts,
+                                                 uint32_t* __restrict__ tokmap,
+                                                 int32_t* __restrict__ counts,
+                                                 uint8_t* __restrict__ jmap) {
     extern __shared__ float lsm[];                 // 8 warps x (E logits + 16 selection slots)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
     float* l = lsm + warp * (E + 16);
     int* sel = reinterpret_cast<int*>(l + E);
-    for (int e = lane; e < E; e += 32) {
-        float v = 0.f;
-        for (int z = 0; z < S; ++z) v += part[((size_t)z * T + t) * E + e];
-        v += bias ? bias[e] : 0.f;
-        l[e] = v;
-        logits[(size_t)t * E + e] = v;
+    // S split-k partials summed in slice order; four experts per lane at a
+    // time, so the loads of a slice are independent of the running sums
+    for (int e0 = 0; e0 < E; e0 += 128) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int z = 0; z < S; ++z) {
+            const float* pz = part + ((size_t)z * T + t) * E;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = e0 + lane + 32 * i;
+                if (e < E) v[i] += pz[e];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = e0 + lane + 32 * i;
+            if (e < E) {
+                const float w = v[i] + (bias ? bias[e] : 0.f);
+                l[e] = w;
+                logits[(size_t)t * E + e] = w;
+            }
+        }
     }
     if (lane < 16) reinterpret_cast<int*>(l + E)[lane] = 0;
     __syncwarp();
@@ -281,70 +307,103 @@ __global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part,
     if (lane < K) {
         ids[(size_t)t * K + lane] = id;
         wts[(size_t)t * K + lane] = norm ? pj / psel : pj;
+        // expert id's token bitmap (row of W = ceil(T/32) words) and pair count
+        atomicOr(&tokmap[(size_t)id * ((T + 31) >> 5) + (t >> 5)], 1u << (t & 31));
+        atomicAdd(&counts[id], 1);
+        jmap[(size_t)id * T + t] = (uint8_t)lane;
     }
 }
 
-// One CTA: pairs p = t*K + j sorted by (expert, p).  A token selects an expert
-// at most once, so the rank of pair (t, e) inside expert e's list is the number
-// of earlier tokens that selected e: a popcount prefix over a per-expert token
-// bitmap.  Also emits the used-expert list.
-__global__ void __launch_bounds__(1024) sort_pairs(const int32_t* __restrict__ ids, int T, int E,
-                                                   int K, int32_t* __restrict__ n_used,
-                                                   int32_t* __restrict__ used_expert,
-                                                   int32_t* __restrict__ used_first,
-                                                   int32_t* __restrict__ pair_list) {
-    extern __shared__ uint32_t bm[];               // E * W bitmap words, then counts, offsets
-    const int W = (T + 31) / 32;
-    int32_t* counts = reinterpret_cast<int32_t*>(bm + (size_t)E * W);
-    int32_t* offs = counts + E;
-    const int P = T * K;
-    for (int i = threadIdx.x; i < E * W; i += blockDim.x) bm[i] = 0u;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = 0;
-    __syncthreads();
-    for (int p = threadIdx.x; p < P; p += blockDim.x) {
-        const int e = ids[p], t = p / K;
-        atomicOr(&bm[(size_t)e * W + (t >> 5)], 1u << (t & 31));
-        atomicAdd(&counts[e], 1);
+constexpr int EL_THREADS = 256;
+
+// One CTA per expert e: the pairs of e in ascending p.  A token selects an
+// expert at most once, so ascending p is ascending token order, and the rank of
+// token t in e's list is the number of set bits before t in e's token bitmap:
+// the row is staged in shared memory with the running popcount before each
+// word (a block scan), then every thread places its tokens independently; the
+// slot j of the pair (t, e) comes from the byte map topk_rank wrote.  The list
+// starts at the sum of the counts of the experts below e; the used-expert list
+// comes from the same prefix over the nonzero counts.
+__global__ void __launch_bounds__(EL_THREADS) expert_lists(const uint8_t* __restrict__ jmap,
+                                                           const uint32_t* __restrict__ tokmap,
+                                                           const int32_t* __restrict__ counts, int T,
+                                                           int E, int K, int32_t* __restrict__ n_used,
+                                                           int32_t* __restrict__ used_expert,
+                                                           int32_t* __restrict__ used_first,
+                                                           int32_t* __restrict__ pair_list) {
+    extern __shared__ uint32_t el_sm[];             // W words, then W running popcounts
+    __shared__ int red[2][EL_THREADS / 32];
+    __shared__ int scan[EL_THREADS / 32];
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int off = 0, ub = 0;
+    for (int i = tid; i < e; i += EL_THREADS) {
+        const int c = counts[i];
+        off += c;
+        ub += c > 0;
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int run = 0, used = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int c = e < E ? counts[e] : 0;
-            int incl = c;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const uint32_t nz = __ballot_sync(0xffffffffu, c > 0);
-            if (e < E) offs[e] = run + incl - c;
-            if (c > 0) {
-                const int slot = used + __popc(nz & ((1u << lane) - 1u));
-                used_expert[slot] = e;
-                used_first[slot] = run + incl - c;
-            }
-            run += __shfl_sync(0xffffffffu, incl, 31);
-            used += __popc(nz);
-        }
-        if (lane == 0) { *n_used = used; used_first[used] = P; }
+    for (int o = 16; o > 0; o >>= 1) {
+        off += __shfl_xor_sync(0xffffffffu, off, o);
+        ub += __shfl_xor_sync(0xffffffffu, ub, o);
+    }
+    if (lane == 0) {
+        red[0][warp] = off;
+        red[1][warp] = ub;
     }
     __syncthreads();
-    for (int p = threadIdx.x; p < P; p += blockDim.x) {
-        const int e = ids[p], t = p / K;
-        const uint32_t* row = bm + (size_t)e * W;
-        int r = __popc(row[t >> 5] & ((1u << (t & 31)) - 1u));
-        for (int w = 0; w < (t >> 5); ++w) r += __popc(row[w]);
-        pair_list[offs[e] + r] = p;
+    off = 0;
+    ub = 0;
+#pragma unroll
+    for (int w = 0; w < EL_THREADS / 32; ++w) {
+        off += red[0][w];
+        ub += red[1][w];
     }
-}
-
-constexpr size_t kSortSmemMax = 200 * 1024;
-
-size_t sort_pairs_smem(int T, int E) {
-    return sizeof(uint32_t) * (size_t)E * ((T + 31) / 32) + sizeof(int32_t) * 2 * E;
+    const int cnt = counts[e];
+    if (tid == 0) {
+        if (cnt > 0) {
+            used_expert[ub] = e;
+            used_first[ub] = off;
+        }
+        if (e == E - 1) {
+            const int used = ub + (cnt > 0);
+            *n_used = used;
+            used_first[used] = T * K;
+        }
+    }
+    if (cnt == 0) return;
+    const int W = (T + 31) >> 5;
+    uint32_t* words = el_sm;
+    int* before = reinterpret_cast<int*>(el_sm + W);
+    const uint32_t* row = tokmap + (size_t)e * W;
+    const int per = (W + EL_THREADS - 1) / EL_THREADS;
+    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+    int mine = 0;
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t b = row[w];
+        words[w] = b;
+        mine += __popc(b);
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    int run = off + incl - mine;
+    for (int w = 0; w < warp; ++w) run += scan[w];
+    for (int w = w0; w < w1; ++w) {
+        before[w] = run;
+        run += __popc(words[w]);
+    }
+    __syncthreads();
+    const uint8_t* jrow = jmap + (size_t)e * T;
+    for (int t = tid; t < T; t += EL_THREADS) {
+        const uint32_t b = words[t >> 5];
+        const uint32_t bit = 1u << (t & 31);
+        if (b & bit) pair_list[before[t >> 5] + __popc(b & (bit - 1u))] = t * K + jrow[t];
+    }
 }
 
 }  // namespace
@@ -353,28 +412,33 @@ cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* ro
                               const float* bias, const Route& r, cudaStream_t st) {
     const size_t rg_smem = sizeof(float) * (RG_T + RG_E) * RG_LD;
     dim3 g1((s.E + RG_E - 1) / RG_E, (s.T + RG_T - 1) / RG_T, s.H / RG_K);
-    router_gemm<<<g1, RG_THREADS, rg_smem, st>>>(x, router_w, s.T, s.H, s.E, r.logits_part);
+    const int W = (s.T + 31) / 32;
+    uint32_t* counts = r.tokmap + (size_t)s.E * W;      // E counters after the bitmap
+    router_gemm<<<g1, RG_THREADS, rg_smem, st>>>(x, router_w, s.T, s.H, s.E, r.logits_part, r.tokmap,
+                                                 s.E * W + s.E);
     topk_rank<<<(s.T + 7) / 8, 256, sizeof(float) * 8 * (s.E + 16), st>>>(
-        r.logits_part, s.H / RG_K, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts);
-    sort_pairs<<<1, 1024, sort_pairs_smem(s.T, s.E), st>>>(r.ids, s.T, s.E, s.K, r.n_used, r.used_expert, r.used_first,
-                                    r.pair_list);
+        r.logits_part, s.H / RG_K, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.tokmap,
+        reinterpret_cast<int32_t*>(counts), r.jmap);
+    expert_lists<<<s.E, EL_THREADS, sizeof(uint32_t) * 2 * W, st>>>(
+        r.jmap, r.tokmap, reinterpret_cast<const int32_t*>(counts), s.T, s.E, s.K, r.n_used, r.used_expert,
+        r.used_first, r.pair_list);
     return cudaGetLastError();
 }
 
 size_t route_many_part_floats(int T, int H, int E) { return (size_t)(H / RG_K) * T * E; }
 
+size_t route_many_tokmap_words(int T, int E) { return (size_t)E * ((T + 31) / 32) + E; }
+
 bool route_many_supported(const MoeShape& s, const Route& r) {
-    return r.logits_part && s.H % RG_K == 0 && sort_pairs_smem(s.T, s.E) <= kSortSmemMax;
+    // expert_lists stages a bitmap row and its running counts (8 bytes per 32 tokens)
+    return r.logits_part && r.tokmap && r.jmap && s.H % RG_K == 0 && s.K <= 32 &&
+           sizeof(uint32_t) * 2 * ((s.T + 31) / 32) <= 48 * 1024;
 }
 
 // Raise the dynamic shared-memory limits once per device context.
 cudaError_t route_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(float) * (RG_T + RG_E) * RG_LD));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(sort_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSortSmemMax);
-    return e;
+    return cudaFuncSetAttribute(router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(float) * (RG_T + RG_E) * RG_LD));
 }
 
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,

@@ -10,8 +10,9 @@
 //   prefill_gateup  per (expert, 64-f tile, token tile): A = 64 gate rows + 64 up
 //                   rows of Q4_K superblocks, TMA-loaded raw (3 stages) and
 //                   converted to fp16 in shared memory (128B-swizzled K-major)
-//                   by 16 dequant warps, a quarter of them per k-block of each
-//                   superblock; B = the expert's gathered x rows via TMA; fp32
+//                   by 16 dequant warps, all of them on each k-block in turn
+//                   (4 A stages ahead of the MMA); B = the expert's gathered
+//                   x rows via TMA; fp32
 //                   accumulator in TMEM; epilogue silu(g)*u -> fp16 act rows
 //   prefill_down    per (expert, 128-row tile, token tile): A = 128 down rows
 //                   (Q6_K or Q4_K, one bulk copy of the whole K), B = act rows,
@@ -42,13 +43,20 @@ constexpr int W_BLOAD = NDQ + 1;               // activation (B) tiles
 constexpr int W_MMA = NDQ + 2;                 // tcgen05.mma issue
 constexpr int PF_THREADS = (NDQ + 3) * 32;
 constexpr uint32_t TMEM_COLS = 256;
-constexpr int NA = 4;                          // A (fp16 weight) stages of the down GEMM: one per
-static_assert(NA * KBLK == QK, "k-block of a superblock");
+constexpr int NA = 4;                          // A (fp16 weight) stages: the 4 k-blocks of a superblock
+static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
 constexpr int NQ = 3;                          // raw Q4_K stages of the gate/up kernel
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
 constexpr int NBMAX = 8;                       // B stages, at most
 constexpr int B_BYTES_GU = 96 * 1024;
 constexpr int B_BYTES_DN = 64 * 1024;
+// CTAs of one (expert, token tile) that share its B rows can run as a cluster:
+// each then TMA-loads 1/C of every B stage and multicasts it to the others.
+// Measured on the T = 512 layer: C = 2 / 4 / 8 took 6% / 10% / 17% longer than
+// C = 1 (B bytes are not the limiter, and a cluster ties its CTAs' pipelines
+// together), so both kernels run unclustered.
+constexpr int GU_CLUSTER = 1;                  // of the F/64 gate/up tiles
+constexpr int DN_CLUSTER = 1;                  // of the H/128 down tiles
 
 struct PfBars {
     uint64_t qfull[NQ], qempty[NQ], afull[NA], aempty[NA], bfull[NBMAX], bempty[NBMAX], acc;
@@ -86,81 +94,84 @@ __device__ __forceinline__ uint4 codes_to_half8(uint32_t w0, uint32_t w1, __half
     return r;
 }
 
-// one thread: k-block c (64 k) of one A row from a Q4_K superblock at q: the
-// 32-byte chunk c holds sub-block 2c in its low nibbles (k 0..31) and 2c+1 in
-// its high nibbles (k 32..63) -> fp16 SW128 tile
-__device__ __forceinline__ void dq_q4k_k64_regs(uint4 hdr, uint4 v0, uint4 v1, int c,
-                                                uint8_t* atile, int row);
+// Q4_K: scale and offset of the two sub-blocks (2c, 2c + 1) of k-block c, as
+// half2 bit patterns {d*s, -dmin*m} (w = d*s*q - dmin*m)
+struct Q4Half {
+    uint32_t sA, cA, sB, cB;
+};
 
-__device__ __forceinline__ void dq_q4k_k64(const uint8_t* q, int c, uint8_t* atile, int row) {
-    const uint4* src = reinterpret_cast<const uint4*>(q + 16 + 32 * c);
-    dq_q4k_k64_regs(*reinterpret_cast<const uint4*>(q), src[0], src[1], c, atile, row);
-}
-
-// the same from registers: header hdr, chunk c as v0 (bytes 0..15), v1 (16..31)
-__device__ __forceinline__ void dq_q4k_k64_regs(uint4 hdr, uint4 v0, uint4 v1, int c,
-                                                uint8_t* atile, int row) {
+__device__ __forceinline__ Q4Half q4_half_scales(uint4 hdr, int c) {
     int sA, mA, sB, mB;
     q4_scales(hdr.y, hdr.z, hdr.w, c, sA, mA, sB, mB);
     const float d = half_bits(hdr.x), dmin = half_bits(hdr.x >> 16);
-    // w = d*s*q - dmin*m
-    const __half2 sub = __float2half2_rn(1024.f);
-    const __half2 sA2 = __float2half2_rn(d * (float)sA), cA2 = __float2half2_rn(-dmin * (float)mA);
-    const __half2 sB2 = __float2half2_rn(d * (float)sB), cB2 = __float2half2_rn(-dmin * (float)mB);
-    uint8_t* rb = atile + row * 128;
-    const int sw = row & 7;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const uint4 v = half ? v1 : v0;
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const uint32_t a0 = w[2 * cc], a1 = w[2 * cc + 1];
-            const int k8 = 2 * half + cc;                   // 8-k group of the low nibbles
-            *reinterpret_cast<uint4*>(rb + ((k8 ^ sw) << 4)) =
-                codes_to_half8(a0 & 0x0F0F0F0Fu, a1 & 0x0F0F0F0Fu, sub, sA2, cA2);
-            *reinterpret_cast<uint4*>(rb + (((k8 + 4) ^ sw) << 4)) =
-                codes_to_half8((a0 >> 4) & 0x0F0F0F0Fu, (a1 >> 4) & 0x0F0F0F0Fu, sub, sB2, cB2);
-        }
-    }
+    return {h2_bits(__float2half2_rn(d * (float)sA)), h2_bits(__float2half2_rn(-dmin * (float)mA)),
+            h2_bits(__float2half2_rn(d * (float)sB)), h2_bits(__float2half2_rn(-dmin * (float)mB))};
 }
 
-// 8 bytes at an even shared-memory address
-__device__ __forceinline__ uint2 lds8(const uint8_t* p) {
+__device__ __forceinline__ Q4Half shfl_half(const Q4Half& v, int src) {
+    return {__shfl_sync(0xffffffffu, v.sA, src), __shfl_sync(0xffffffffu, v.cA, src),
+            __shfl_sync(0xffffffffu, v.sB, src), __shfl_sync(0xffffffffu, v.cB, src)};
+}
+
+// one 16-k quarter of a Q4_K k-block: 8 code bytes v hold 8 k of sub-block 2c
+// in their low nibbles and the same 8 k of sub-block 2c + 1 in their high
+// nibbles -> two 16-byte fp16 pieces of the row (offsets o_lo, o_hi in the
+// 128B-swizzled tile)
+__device__ __forceinline__ void q4_quarter(uint2 v, const Q4Half& s, uint8_t* rb, int o_lo, int o_hi) {
+    const __half2 sub = __float2half2_rn(1024.f);
+    *reinterpret_cast<uint4*>(rb + o_lo) =
+        codes_to_half8(v.x & 0x0F0F0F0Fu, v.y & 0x0F0F0F0Fu, sub, bits_h2(s.sA), bits_h2(s.cA));
+    *reinterpret_cast<uint4*>(rb + o_hi) = codes_to_half8((v.x >> 4) & 0x0F0F0F0Fu, (v.y >> 4) & 0x0F0F0F0Fu,
+                                                          sub, bits_h2(s.sB), bits_h2(s.cB));
+}
+
+// 16 bytes at an even shared-memory address (five aligned words, funnel shift)
+__device__ __forceinline__ uint4 lds16(const uint8_t* p) {
     const uint32_t off = smem_u32(p) & 3u;
     const uint32_t* b = reinterpret_cast<const uint32_t*>(p - off);   // stays a shared pointer
     const uint32_t sh = off * 8u;
-    const uint32_t w0 = b[0], w1 = b[1], w2 = b[2];
-    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
+    const uint32_t w0 = b[0], w1 = b[1], w2 = b[2], w3 = b[3], w4 = b[4];
+    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                      __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
 }
 
-// one thread: k-block qb (64 k) of one A row from a Q6_K superblock at blk
-// (2-byte aligned): groups g = 2(qb&1) and 2(qb&1)+1 of half n = qb>>1,
-// positions l = 0..31 each
-__device__ __forceinline__ void dq_q6k_k64(const uint8_t* blk, int qb, uint8_t* atile, int row) {
-    const int n = qb >> 1;
-    const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-    const uint8_t* qhp = blk + 128 + 32 * n;
+// one 16-k quarter of a Q6_K k-block: 16 ql bytes (nibble at shl) and 16 qh
+// bytes (2 bits at shh) -> 6-bit codes, w = ds*(q6 - 32) -> two 16-byte pieces
+__device__ __forceinline__ void q6_quarter(uint4 ql, uint4 qh, int shl, int shh, __half2 ds, uint8_t* rb,
+                                           int o0, int o1) {
     const __half2 sub = __float2half2_rn(1056.f), zero = __float2half2_rn(0.f);
-    uint8_t* rb = atile + row * 128;
-    const int sw = row & 7;
+    const uint32_t l[4] = {ql.x, ql.y, ql.z, ql.w}, hb[4] = {qh.x, qh.y, qh.z, qh.w};
+    uint32_t c[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int g = 2 * (qb & 1) + h;
-        const uint8_t* qlp = blk + 64 * n + 32 * (g & 1);
-        const __half2 ds0 = __float2half2_rn(d * (float)static_cast<int8_t>(blk[192 + 8 * n + 2 * g]));
-        const __half2 ds1 = __float2half2_rn(d * (float)static_cast<int8_t>(blk[192 + 8 * n + 2 * g + 1]));
-        const int shl = 4 * (g >> 1), shh = 2 * g;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {                     // 8 positions each
-            const uint2 ql = lds8(qlp + 8 * cc), qh = lds8(qhp + 8 * cc);
-            const uint32_t c0 = ((ql.x >> shl) & 0x0F0F0F0Fu) | (((qh.x >> shh) & 0x03030303u) << 4);
-            const uint32_t c1 = ((ql.y >> shl) & 0x0F0F0F0Fu) | (((qh.y >> shh) & 0x03030303u) << 4);
-            // w = d*sc*(q6 - 32)
-            *reinterpret_cast<uint4*>(rb + (((4 * h + cc) ^ sw) << 4)) =
-                codes_to_half8(c0, c1, sub, cc < 2 ? ds0 : ds1, zero);
-        }
+    for (int i = 0; i < 4; ++i)
+        c[i] = ((l[i] >> shl) & 0x0F0F0F0Fu) | (((hb[i] >> shh) & 0x03030303u) << 4);
+    *reinterpret_cast<uint4*>(rb + o0) = codes_to_half8(c[0], c[1], sub, ds, zero);
+    *reinterpret_cast<uint4*>(rb + o1) = codes_to_half8(c[2], c[3], sub, ds, zero);
+}
+
+// B stages of a token tile of nb rows, NB deep, for k-blocks 0..NKB-1 (one
+// thread).  In a cluster of csize CTAs each loads rows [crank*nb/csize, ..+nb/csize)
+// of every stage (tensor map box of nb/csize rows) and multicasts them; a stage
+// is refilled once every CTA's MMA has released it (bempty counts csize
+// commits).  Before returning, the thread waits until the last NB stages have
+// been released everywhere, so no commit of a peer is still on its way to this
+// CTA's barriers when it exits.
+__device__ __forceinline__ void load_b_stages(PfBars* bars, uint8_t* bst, int BSTAGE, int NB, int NKB,
+                                              const CUtensorMap* tm, int nb, int row0, uint32_t csize,
+                                              uint32_t crank, uint16_t cmask) {
+    const int rows = nb / (int)csize;
+    for (int kb = 0; kb < NKB; ++kb) {
+        const int st = kb % NB;
+        if (!mbar_wait(&bars->bempty[st], ((uint32_t)(kb / NB) & 1u) ^ 1u)) return;
+        mbar_arrive_expect_tx(&bars->bfull[st], (uint32_t)BSTAGE);
+        if (csize > 1)
+            tma_load_2d_mc(bst + st * BSTAGE + (int)crank * rows * 128, tm, kb * KBLK, row0 + (int)crank * rows,
+                           &bars->bfull[st], cmask);
+        else
+            tma_load_2d(bst + st * BSTAGE, tm, kb * KBLK, row0, &bars->bfull[st]);
     }
+    for (int kb = NKB > NB ? NKB : NB; kb < NKB + NB; ++kb)
+        if (!mbar_wait(&bars->bempty[kb % NB], ((uint32_t)(kb / NB) & 1u) ^ 1u)) return;
 }
 
 struct GuParams {
@@ -191,6 +202,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_x256;
     const int e = p.used_expert[u];
     const int f0 = blockIdx.x * 64;
+    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
+    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
     const int H = p.H, F = p.F;
     const int NKB = H / KBLK, NSB = H / QK;
 
@@ -208,12 +221,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             mbar_init(&bars->qempty[i], NDQ);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&bars->afull[i], NDQ / NA);
+            mbar_init(&bars->afull[i], NDQ);
             mbar_init(&bars->aempty[i], 1);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], 1);
+            mbar_init(&bars->bempty[i], csize);
         }
         mbar_init(&bars->acc, 1);
         fence_barrier_init();
@@ -221,6 +234,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (warp == 0) tmem_alloc(&bars->tmem, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    if (csize > 1) cluster_sync_all();     // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
 
@@ -239,14 +253,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
     } else if (warp == W_BLOAD) {
         // the expert's gathered x rows, NB k-blocks ahead of the MMA
-        if (lane == 0) {
-            for (int kb = 0; kb < NKB; ++kb) {
-                const int st = kb % NB;
-                if (!mbar_wait(&bars->bempty[st], ((uint32_t)(kb / NB) & 1u) ^ 1u)) break;
-                mbar_arrive_expect_tx(&bars->bfull[st], (uint32_t)BSTAGE);
-                tma_load_2d(bst + st * BSTAGE, tmx, kb * KBLK, first + n0, &bars->bfull[st]);
-            }
-        }
+        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmx, nb, first + n0, csize, crank, cmask);
     } else if (warp == W_MMA) {
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f16(TILE_M, N);
@@ -263,26 +270,51 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                              (kb | k) != 0);
                 umma_commit(&bars->aempty[sa]);
-                umma_commit(&bars->bempty[sb]);
+                if (csize > 1)
+                    umma_commit_mc(&bars->bempty[sb], cmask);   // the stage is free in every CTA
+                else
+                    umma_commit(&bars->bempty[sb]);
             }
             umma_commit(&bars->acc);
         }
     } else {
-        // dequant: thread -> A row (tid & 127) and k-block c = tid >> 7 of every
-        // superblock (A stage c): 64 weights per visit, one scale decode
-        const int row = tid & 127, c = tid >> 7;
+        // dequant: thread -> A row 8*warp + (lane & 7) and 16-k quarter
+        // qq = lane >> 3 of every k-block (each 8-lane phase of a 16-byte store
+        // then covers all 32 banks).  All 16 warps fill each A stage in turn, so
+        // the NA stages (the 4 k-blocks of a superblock) run ahead of the MMA.
+        // A raw superblock column is read into registers at once and its stage
+        // released; the scales of k-block c are decoded by the row's lane with
+        // qq == c and shuffled to the other three.
+        const int qq = lane >> 3, row = 8 * warp + (lane & 7);
         const int grp = row >> 5, w32 = row & 31;
         const int src = w32 < 16 ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16);
+        uint8_t* const arow = ast + row * 128;
+        const int o_lo = (qq ^ (row & 7)) << 4, o_hi = ((qq + 4) ^ (row & 7)) << 4;
+        int sq = 0;
+        uint32_t qpar = 0;
         for (int sb = 0; sb < NSB; ++sb) {
-            const int sq = sb % NQ;
-            mbar_wait(&bars->qfull[sq], (uint32_t)(sb / NQ) & 1u);
-            mbar_wait(&bars->aempty[c], ((uint32_t)sb & 1u) ^ 1u);
-            dq_q4k_k64(qst + sq * QSTAGE_GU + src * Q4K_BYTES, c, ast + c * A_STAGE, row);
-            fence_proxy_async();
+            const uint8_t* blk = qst + sq * QSTAGE_GU + src * Q4K_BYTES;
+            mbar_wait(&bars->qfull[sq], qpar);
+            const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+            uint2 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * qq);
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars->afull[c]);
-                mbar_arrive(&bars->qempty[sq]);
+            if (lane == 0) mbar_arrive(&bars->qempty[sq]);
+            if (++sq == NQ) {
+                sq = 0;
+                qpar ^= 1u;
+            }
+            const Q4Half own = q4_half_scales(hdr, qq);
+            const uint32_t apar = ((uint32_t)sb & 1u) ^ 1u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const Q4Half sc = shfl_half(own, (lane & 7) + 8 * c);
+                mbar_wait(&bars->aempty[c], apar);
+                q4_quarter(v[c], sc, arow + c * A_STAGE, o_lo, o_hi);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->afull[c]);
             }
         }
         // epilogue: TMEM lane quarter (warp % 4); column quarter (warp / 4)
@@ -299,13 +331,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const int col = c0 + j;
                 if (lane < 16 && col < n) {
                     const float g = v[j];
-                    p.act[(size_t)(first + n0 + col) * F + f] = __float2half_rn(g / (1.f + expf(-g)) * up);
+                    p.act[(size_t)(first + n0 + col) * F + f] =
+                        __float2half_rn(__fdividef(g, 1.f + __expf(-g)) * up);
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (csize > 1) cluster_sync_all();     // no peer still writes into this CTA
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -337,6 +371,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const CUtensorMap* tmb = nb == 64 ? &tm_a64 : nb == 128 ? &tm_a128 : &tm_a256;
     const int e = p.used_expert[u];
     const int h0 = blockIdx.x * TILE_M;
+    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
+    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
     const int H = p.H, F = p.F;
     const int NKB = F / KBLK;
     const int BB = p.down_t == 1 ? Q4K_BYTES : Q6K_BYTES;
@@ -354,12 +390,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (tid == 0) {
         mbar_init(&bars->qfull[0], 1);
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&bars->afull[i], NDQ / NA);
+            mbar_init(&bars->afull[i], NDQ);
             mbar_init(&bars->aempty[i], 1);
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], 1);
+            mbar_init(&bars->bempty[i], csize);
         }
         mbar_init(&bars->acc, 1);
         fence_barrier_init();
@@ -367,6 +403,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (warp == 0) tmem_alloc(&bars->tmem, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    if (csize > 1) cluster_sync_all();     // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
 
@@ -378,14 +415,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bulk_g2s(qbuf, src, qbytes, &bars->qfull[0]);
         }
     } else if (warp == W_BLOAD) {
-        if (lane == 0) {
-            for (int kb = 0; kb < NKB; ++kb) {
-                const int st = kb % NB;
-                if (!mbar_wait(&bars->bempty[st], ((uint32_t)(kb / NB) & 1u) ^ 1u)) break;
-                mbar_arrive_expect_tx(&bars->bfull[st], (uint32_t)BSTAGE);
-                tma_load_2d(bst + st * BSTAGE, tmb, kb * KBLK, first + n0, &bars->bfull[st]);
-            }
-        }
+        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmb, nb, first + n0, csize, crank, cmask);
     } else if (warp == W_MMA) {
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f16(TILE_M, N);
@@ -402,24 +432,66 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                              (kb | k) != 0);
                 umma_commit(&bars->aempty[sa]);
-                umma_commit(&bars->bempty[sb]);
+                if (csize > 1)
+                    umma_commit_mc(&bars->bempty[sb], cmask);   // the stage is free in every CTA
+                else
+                    umma_commit(&bars->bempty[sb]);
             }
             umma_commit(&bars->acc);
         }
     } else {
-        // thread -> A row (tid & 127) and k-block c = tid >> 7 of every superblock
-        const int row = tid & 127, c = tid >> 7;
+        // thread -> A row 8*warp + (lane & 7), 16-k quarter qq = lane >> 3 of
+        // every k-block; all warps fill each A stage in turn (NA = the 4
+        // k-blocks of a superblock)
+        const int qq = lane >> 3, row = 8 * warp + (lane & 7);
+        const int sw = row & 7;
+        uint8_t* const arow = ast + row * 128;
         mbar_wait(&bars->qfull[0], 0);
         const uint8_t* rowp = qbuf + (size_t)row * RB;
         for (int sb = 0; sb < NKB / NA; ++sb) {
-            mbar_wait(&bars->aempty[c], ((uint32_t)sb & 1u) ^ 1u);
-            if (p.down_t == 2)
-                dq_q6k_k64(rowp + sb * Q6K_BYTES, c, ast + c * A_STAGE, row);
-            else
-                dq_q4k_k64(rowp + sb * Q4K_BYTES, c, ast + c * A_STAGE, row);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->afull[c]);
+            const uint32_t apar = ((uint32_t)sb & 1u) ^ 1u;
+            if (p.down_t == 2) {
+                // k-block qb = 2n + par is half n, groups g = 2 par + h (h = qq >> 1),
+                // positions 16(qq & 1) .. + 15: the same ql / qh bytes serve par 0 and 1
+                const uint8_t* blk = rowp + sb * Q6K_BYTES;
+                const int h = qq >> 1, hq = qq & 1;
+                const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                const uint4 scw = lds16(blk + 192);
+                const uint32_t scv[4] = {scw.x, scw.y, scw.z, scw.w};
+                const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const uint4 ql = lds16(blk + 64 * n + 32 * h + 16 * hq);
+                    const uint4 qh = lds16(blk + 128 + 32 * n + 16 * hq);
+#pragma unroll
+                    for (int par = 0; par < 2; ++par) {
+                        const int qb = 2 * n + par;
+                        // scale byte 8n + 2g + hq = 8n + 4 par + qq: word 2n + par, byte qq
+                        const int sc = (int)(scv[2 * n + par] << (24 - 8 * qq)) >> 24;
+                        const __half2 ds = __float2half2_rn(d * (float)sc);
+                        mbar_wait(&bars->aempty[qb], apar);
+                        q6_quarter(ql, qh, 4 * par, 4 * par + 2 * h, ds, arow + qb * A_STAGE, o0, o1);
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->afull[qb]);
+                    }
+                }
+            } else {
+                const uint8_t* blk = rowp + sb * Q4K_BYTES;
+                const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+                const Q4Half own = q4_half_scales(hdr, qq);
+                const int o_lo = (qq ^ sw) << 4, o_hi = ((qq + 4) ^ sw) << 4;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * qq);
+                    const Q4Half sc = shfl_half(own, (lane & 7) + 8 * c);
+                    mbar_wait(&bars->aempty[c], apar);
+                    q4_quarter(v, sc, arow + c * A_STAGE, o_lo, o_hi);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[c]);
+                }
+            }
         }
         mbar_wait(&bars->acc, 0);
         tc_fence_after();
@@ -437,6 +509,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (csize > 1) cluster_sync_all();     // no peer still writes into this CTA
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -508,6 +581,31 @@ bool map_half(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// largest power of two <= cmax that divides the tile count along x
+int cluster_for(int tiles, int cmax) {
+    int c = cmax;
+    while (c > 1 && tiles % c) c >>= 1;
+    return c;
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_clustered(void (*kernel)(Params...), dim3 grid, int cx, size_t smem, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(PF_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cx;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr size_t GU_SMEM = 1024 + ((NQ * QSTAGE_GU + 1023) & ~1023) + NA * A_STAGE + B_BYTES_GU +
                            sizeof(PfBars) + 64;
 
@@ -538,11 +636,13 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
 
     CUtensorMap tg, tu, tx64, tx128, tx256, ta64, ta128, ta256;
     const uint64_t rbg = (uint64_t)(s.H / QK) * Q4K_BYTES;
+    const int cgu = cluster_for(s.F / 64, GU_CLUSTER), cdn = cluster_for(s.H / TILE_M, DN_CLUSTER);
+    // B maps: boxes of nb / C rows (each CTA of a cluster loads its share)
     if (!map_bytes(&tg, gate, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_bytes(&tu, up, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
-        !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
-        !map_half(&tx256, xp, s.H, P, 256) || !map_half(&ta64, actp, s.F, P, 64) ||
-        !map_half(&ta128, actp, s.F, P, 128) || !map_half(&ta256, actp, s.F, P, 256))
+        !map_half(&tx64, xp, s.H, P, 64 / cgu) || !map_half(&tx128, xp, s.H, P, 128 / cgu) ||
+        !map_half(&tx256, xp, s.H, P, 256 / cgu) || !map_half(&ta64, actp, s.F, P, 64 / cdn) ||
+        !map_half(&ta128, actp, s.F, P, 128 / cdn) || !map_half(&ta256, actp, s.F, P, 256 / cdn))
         return cudaErrorInvalidValue;
 
     static bool attr_set = false;
@@ -554,14 +654,12 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         attr_set = true;
     }
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles};
-    dim3 g1(s.F / 64, max_used * ntiles);
-    prefill_gateup<<<g1, PF_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128, tx256, gp);
-    e = cudaGetLastError();
+    e = launch_clustered(prefill_gateup, dim3(s.F / 64, max_used * ntiles), cgu, GU_SMEM, st, tg, tu, tx64,
+                         tx128, tx256, gp);
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, ntiles, down_t};
-    dim3 g2(s.H / TILE_M, max_used * ntiles);
-    prefill_down<<<g2, PF_THREADS, dn_smem(s.F, down_t), st>>>(ta64, ta128, ta256, dp);
-    e = cudaGetLastError();
+    e = launch_clustered(prefill_down, dim3(s.H / TILE_M, max_used * ntiles), cdn, dn_smem(s.F, down_t), st,
+                         ta64, ta128, ta256, dp);
     if (e != cudaSuccess) return e;
     dim3 g3((s.H + 255) / 256, s.T);
     combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);

@@ -68,7 +68,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, logits_part, ftag, xs, q, kv, att, attn_part, inv_freq,
+        status, bar, xp, actp, inv_pos, logits_part, tokmap, jmap, ftag, xs, q, kv, att, attn_part, inv_freq,
         rope_cs, total;
     int attn_splits;
 };
@@ -117,6 +117,8 @@ Layout layout(const qmoe_config* c) {
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
     L.logits_part = take(sizeof(float) * qmoe::route_many_part_floats((int)T, (int)H, (int)E));
+    L.tokmap = take(sizeof(uint32_t) * qmoe::route_many_tokmap_words((int)T, (int)E));
+    L.jmap = take(E * T);
     const int Tf = (int)(T < 8 ? T : 8);                 // the fused decode kernel serves T <= 8
     L.ftag = take(qmoe::fused_bufs_bytes(Tf, (int)H, (int)E, (int)K, (int)F, FUSED_GRID_MAX));
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
@@ -283,6 +285,8 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.used_first = reinterpret_cast<int32_t*>(b + L.used_first);
     c->route.pair_list = reinterpret_cast<int32_t*>(b + L.pair_list);
     c->route.logits_part = reinterpret_cast<float*>(b + L.logits_part);
+    c->route.tokmap = reinterpret_cast<uint32_t*>(b + L.tokmap);
+    c->route.jmap = reinterpret_cast<uint8_t*>(b + L.jmap);
     c->act = reinterpret_cast<float*>(b + L.act);
     c->y = reinterpret_cast<float*>(b + L.y);
     c->hin = reinterpret_cast<float*>(b + L.hin);

@@ -20,6 +20,9 @@ struct Route {
     int32_t* used_first;  // [E+1]
     int32_t* pair_list;   // [T*K]
     float* logits_part;   // [H/128][T][E] split-k router partials (many-token path), or null
+    uint32_t* tokmap;     // [E][ceil(T/32)] token bitmap per expert, then [E] pair counts
+                          // (many-token path), or null
+    uint8_t* jmap;        // [E][T] slot j of pair (t, e) where e's bitmap has t (many-token path)
 };
 
 struct MoeShape {
@@ -31,12 +34,13 @@ struct MoeShape {
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
                          const float* bias, const Route& r, cudaStream_t st);
 
-// The same for many tokens (tiled router GEMM, per-token rank top-k, bitmap
-// stable sort); requires route_many_supported().
+// The same for many tokens (tiled router GEMM, per-token rank top-k, per-expert
+// lists from token bitmaps); requires route_many_supported().
 cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* router_w,
                               const float* bias, const Route& r, cudaStream_t st);
 bool route_many_supported(const MoeShape& s, const Route& r);
 size_t route_many_part_floats(int T, int H, int E);
+size_t route_many_tokmap_words(int T, int E);
 cudaError_t route_prepare();
 
 // A4 + A5: act[p][f] = silu(Wg_e x_t)[f] * (Wu_e x_t)[f] for every pair p.

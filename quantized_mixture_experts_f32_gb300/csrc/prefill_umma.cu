@@ -38,14 +38,28 @@ constexpr int TILE_M = 128;
 constexpr int TILE_NMAX = 256;
 constexpr int A_STAGE = TILE_M * KBLK * 2;     // 16 KB fp16 A block
 constexpr int NDQ = 16;                        // dequant / epilogue warps (4 threads per A row)
+constexpr int RPT = 16 / NDQ;                  // A rows per dequant thread
+static_assert(NDQ * RPT == 16 && NDQ % 4 == 0, "128 A rows, 8 per warp per pass");
 constexpr int W_QLOAD = NDQ;                   // weight copies
 constexpr int W_BLOAD = NDQ + 1;               // activation (B) tiles
 constexpr int W_MMA = NDQ + 2;                 // tcgen05.mma issue
-constexpr int PF_THREADS = (NDQ + 3) * 32;
+// a whole number of 4-warp groups (one idle warp): warp i of a CTA then sits on
+// SM sub-partition i % 4 however many CTAs share the SM, which the TMEM lane
+// quarter of the epilogue (warp % 4) relies on
+constexpr int PF_THREADS = (NDQ + 4) * 32;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int NA = 4;                          // A (fp16 weight) stages: the 4 k-blocks of a superblock
 static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
-constexpr int NQ = 3;                          // raw Q4_K stages of the gate/up kernel
+constexpr int NQ = 3;                          // raw Q4_K stages, at most
+// gate/up kernel: token-tile rows, raw and A stages, CTAs per SM it is built
+// for (the stage rings and TMEM columns must fit that many CTAs), TMEM columns
+constexpr int GU_NMAX = 256;
+constexpr int GU_NQ = 3;
+constexpr int GU_NA = 4;
+constexpr int GU_MINB = 1;
+constexpr uint32_t GU_TMEM = 256;
+static_assert(GU_NQ <= NQ && GU_NA <= NA && (GU_NA == 2 || GU_NA == 4) && GU_NMAX <= (int)GU_TMEM,
+              "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
 constexpr int NBMAX = 8;                       // B stages, at most
 constexpr int B_BYTES_GU = 96 * 1024;
@@ -183,7 +197,7 @@ struct GuParams {
 };
 
 // grid (F/64, max_used * ntiles), PF_THREADS threads
-__global__ void __launch_bounds__(PF_THREADS, 1)
+__global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                    const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ CUtensorMap tm_x128,
                    const __grid_constant__ CUtensorMap tm_x256, const GuParams p) {
@@ -194,9 +208,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int u = blockIdx.y / p.ntiles, nt = blockIdx.y % p.ntiles;
     if (u >= *p.n_used) return;
     const int first = p.used_first[u], cnt = p.used_first[u + 1] - first;
-    const int n0 = nt * TILE_NMAX;
+    const int n0 = nt * GU_NMAX;
     if (n0 >= cnt) return;
-    const int n = min(TILE_NMAX, cnt - n0);
+    const int n = min(GU_NMAX, cnt - n0);
     const int N = (n + 15) & ~15;
     const int nb = box_rows(n);
     const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_x256;
@@ -207,20 +221,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int H = p.H, F = p.F;
     const int NKB = H / KBLK, NSB = H / QK;
 
-    uint8_t* qst = sm;                                   // NQ x QSTAGE_GU
-    uint8_t* ast = sm + ((NQ * QSTAGE_GU + 1023) & ~1023);  // NA x A_STAGE (1024-aligned)
-    uint8_t* bst = ast + NA * A_STAGE;                   // B_BYTES_GU
+    uint8_t* qst = sm;                                   // GU_NQ x QSTAGE_GU
+    uint8_t* ast = sm + ((GU_NQ * QSTAGE_GU + 1023) & ~1023);  // GU_NA x A_STAGE (1024-aligned)
+    uint8_t* bst = ast + GU_NA * A_STAGE;                // B_BYTES_GU
     PfBars* bars = reinterpret_cast<PfBars*>(bst + B_BYTES_GU);
     const int NB = b_stages(B_BYTES_GU, nb);
     const int BSTAGE = nb * KBLK * 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int i = 0; i < NQ; ++i) {
+        for (int i = 0; i < GU_NQ; ++i) {
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], NDQ);
         }
-        for (int i = 0; i < NA; ++i) {
+        for (int i = 0; i < GU_NA; ++i) {
             mbar_init(&bars->afull[i], NDQ);
             mbar_init(&bars->aempty[i], 1);
         }
@@ -231,7 +245,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         mbar_init(&bars->acc, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(&bars->tmem, TMEM_COLS);
+    if (warp == 0) tmem_alloc(&bars->tmem, GU_TMEM);
     tc_fence_before();
     __syncthreads();
     if (csize > 1) cluster_sync_all();     // peers' barriers exist before any multicast
@@ -243,8 +257,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (lane == 0) {
             const int ybase = e * F + f0;
             for (int sb = 0; sb < NSB; ++sb) {
-                const int st = sb % NQ;
-                if (!mbar_wait(&bars->qempty[st], ((uint32_t)(sb / NQ) & 1u) ^ 1u)) break;
+                const int st = sb % GU_NQ;
+                if (!mbar_wait(&bars->qempty[st], ((uint32_t)(sb / GU_NQ) & 1u) ^ 1u)) break;
                 uint8_t* dst = qst + st * QSTAGE_GU;
                 mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
                 tma_load_2d(dst, &tm_gate, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
@@ -258,8 +272,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f16(TILE_M, N);
             for (int kb = 0; kb < NKB; ++kb) {
-                const int sa = kb % NA, sb = kb % NB;
-                if (!mbar_wait(&bars->afull[sa], (uint32_t)(kb / NA) & 1u) ||
+                const int sa = kb % GU_NA, sb = kb % NB;
+                if (!mbar_wait(&bars->afull[sa], (uint32_t)(kb / GU_NA) & 1u) ||
                     !mbar_wait(&bars->bfull[sb], (uint32_t)(kb / NB) & 1u))
                     break;
                 tc_fence_after();
@@ -277,52 +291,69 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             umma_commit(&bars->acc);
         }
-    } else {
-        // dequant: thread -> A row 8*warp + (lane & 7) and 16-k quarter
-        // qq = lane >> 3 of every k-block (each 8-lane phase of a 16-byte store
-        // then covers all 32 banks).  All 16 warps fill each A stage in turn, so
-        // the NA stages (the 4 k-blocks of a superblock) run ahead of the MMA.
+    } else if (warp < NDQ) {
+        // dequant: thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r) and 16-k
+        // quarter qq = lane >> 3 of every k-block (each 8-lane phase of a 16-byte
+        // store then covers all 32 banks).  All NDQ warps fill each A stage in turn, so
+        // the GU_NA stages run ahead of the MMA.
         // A raw superblock column is read into registers at once and its stage
         // released; the scales of k-block c are decoded by the row's lane with
         // qq == c and shuffled to the other three.
-        const int qq = lane >> 3, row = 8 * warp + (lane & 7);
-        const int grp = row >> 5, w32 = row & 31;
-        const int src = w32 < 16 ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16);
-        uint8_t* const arow = ast + row * 128;
-        const int o_lo = (qq ^ (row & 7)) << 4, o_hi = ((qq + 4) ^ (row & 7)) << 4;
+        const int qq = lane >> 3;
+        int src[RPT], rowb[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int row = 8 * warp + (lane & 7) + 8 * NDQ * r;
+            const int grp = row >> 5, w32 = row & 31;
+            src[r] = (w32 < 16 ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16)) * Q4K_BYTES;
+            rowb[r] = row * 128;
+        }
+        const int o_lo = (qq ^ (lane & 7)) << 4, o_hi = ((qq + 4) ^ (lane & 7)) << 4;   // row % 8 == lane % 8
         int sq = 0;
         uint32_t qpar = 0;
         for (int sb = 0; sb < NSB; ++sb) {
-            const uint8_t* blk = qst + sq * QSTAGE_GU + src * Q4K_BYTES;
+            const uint8_t* stg = qst + sq * QSTAGE_GU;
             mbar_wait(&bars->qfull[sq], qpar);
-            const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-            uint2 v[4];
+            uint4 hdr[RPT];
+            uint2 v[RPT][4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * qq);
+            for (int r = 0; r < RPT; ++r) {
+                hdr[r] = *reinterpret_cast<const uint4*>(stg + src[r]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    v[r][c] = *reinterpret_cast<const uint2*>(stg + src[r] + 16 + 32 * c + 8 * qq);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->qempty[sq]);
-            if (++sq == NQ) {
+            if (++sq == GU_NQ) {
                 sq = 0;
                 qpar ^= 1u;
             }
-            const Q4Half own = q4_half_scales(hdr, qq);
-            const uint32_t apar = ((uint32_t)sb & 1u) ^ 1u;
+            Q4Half own[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) own[r] = q4_half_scales(hdr[r], qq);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const Q4Half sc = shfl_half(own, (lane & 7) + 8 * c);
-                mbar_wait(&bars->aempty[c], apar);
-                q4_quarter(v[c], sc, arow + c * A_STAGE, o_lo, o_hi);
+                // k-block 4 sb + c: stage c % GU_NA, its use number (4 sb + c) / GU_NA
+                const int sa = c % GU_NA;
+                const uint32_t apar = (((uint32_t)((4 / GU_NA) * sb + c / GU_NA)) & 1u) ^ 1u;
+                Q4Half sc[RPT];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
+                mbar_wait(&bars->aempty[sa], apar);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) q4_quarter(v[r][c], sc[r], ast + sa * A_STAGE + rowb[r], o_lo, o_hi);
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->afull[c]);
+                if (lane == 0) mbar_arrive(&bars->afull[sa]);
             }
         }
         // epilogue: TMEM lane quarter (warp % 4); column quarter (warp / 4)
         mbar_wait(&bars->acc, 0);
         tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2;
+        const int lq = warp & 3, ch = warp >> 2, cpw = 1024 / NDQ;   // columns per warp
         const int f = f0 + 16 * lq + (lane & 15);
-        for (int c0 = ch * 64; c0 < min(N, ch * 64 + 64); c0 += 16) {
+        for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -340,7 +371,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (csize > 1) cluster_sync_all();     // no peer still writes into this CTA
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, GU_TMEM);
 }
 
 struct DnParams {
@@ -439,54 +470,82 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             umma_commit(&bars->acc);
         }
-    } else {
-        // thread -> A row 8*warp + (lane & 7), 16-k quarter qq = lane >> 3 of
-        // every k-block; all warps fill each A stage in turn (NA = the 4
-        // k-blocks of a superblock)
-        const int qq = lane >> 3, row = 8 * warp + (lane & 7);
-        const int sw = row & 7;
-        uint8_t* const arow = ast + row * 128;
+    } else if (warp < NDQ) {
+        // thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r), 16-k quarter
+        // qq = lane >> 3 of every k-block; all warps fill each A stage in turn
+        // (NA = the 4 k-blocks of a superblock)
+        const int qq = lane >> 3, sw = lane & 7;                 // row % 8 == lane % 8
         mbar_wait(&bars->qfull[0], 0);
-        const uint8_t* rowp = qbuf + (size_t)row * RB;
+        const uint8_t* rowp[RPT];
+        int rowb[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int row = 8 * warp + (lane & 7) + 8 * NDQ * r;
+            rowp[r] = qbuf + (size_t)row * RB;
+            rowb[r] = row * 128;
+        }
         for (int sb = 0; sb < NKB / NA; ++sb) {
             const uint32_t apar = ((uint32_t)sb & 1u) ^ 1u;
             if (p.down_t == 2) {
                 // k-block qb = 2n + par is half n, groups g = 2 par + h (h = qq >> 1),
                 // positions 16(qq & 1) .. + 15: the same ql / qh bytes serve par 0 and 1
-                const uint8_t* blk = rowp + sb * Q6K_BYTES;
                 const int h = qq >> 1, hq = qq & 1;
-                const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-                const uint4 scw = lds16(blk + 192);
-                const uint32_t scv[4] = {scw.x, scw.y, scw.z, scw.w};
                 const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+                float d[RPT];
+                uint32_t scv[RPT][4];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const uint8_t* blk = rowp[r] + sb * Q6K_BYTES;
+                    d[r] = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                    const uint4 scw = lds16(blk + 192);
+                    scv[r][0] = scw.x;
+                    scv[r][1] = scw.y;
+                    scv[r][2] = scw.z;
+                    scv[r][3] = scw.w;
+                }
 #pragma unroll
                 for (int n = 0; n < 2; ++n) {
-                    const uint4 ql = lds16(blk + 64 * n + 32 * h + 16 * hq);
-                    const uint4 qh = lds16(blk + 128 + 32 * n + 16 * hq);
+                    uint4 ql[RPT], qh[RPT];
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) {
+                        const uint8_t* blk = rowp[r] + sb * Q6K_BYTES;
+                        ql[r] = lds16(blk + 64 * n + 32 * h + 16 * hq);
+                        qh[r] = lds16(blk + 128 + 32 * n + 16 * hq);
+                    }
 #pragma unroll
                     for (int par = 0; par < 2; ++par) {
                         const int qb = 2 * n + par;
-                        // scale byte 8n + 2g + hq = 8n + 4 par + qq: word 2n + par, byte qq
-                        const int sc = (int)(scv[2 * n + par] << (24 - 8 * qq)) >> 24;
-                        const __half2 ds = __float2half2_rn(d * (float)sc);
                         mbar_wait(&bars->aempty[qb], apar);
-                        q6_quarter(ql, qh, 4 * par, 4 * par + 2 * h, ds, arow + qb * A_STAGE, o0, o1);
+#pragma unroll
+                        for (int r = 0; r < RPT; ++r) {
+                            // scale byte 8n + 2g + hq = 8n + 4 par + qq: word 2n + par, byte qq
+                            const int sc = (int)(scv[r][2 * n + par] << (24 - 8 * qq)) >> 24;
+                            q6_quarter(ql[r], qh[r], 4 * par, 4 * par + 2 * h, __float2half2_rn(d[r] * (float)sc),
+                                       ast + qb * A_STAGE + rowb[r], o0, o1);
+                        }
                         fence_proxy_async();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars->afull[qb]);
                     }
                 }
             } else {
-                const uint8_t* blk = rowp + sb * Q4K_BYTES;
-                const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-                const Q4Half own = q4_half_scales(hdr, qq);
                 const int o_lo = (qq ^ sw) << 4, o_hi = ((qq + 4) ^ sw) << 4;
+                Q4Half own[RPT];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r)
+                    own[r] = q4_half_scales(*reinterpret_cast<const uint4*>(rowp[r] + sb * Q4K_BYTES), qq);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * qq);
-                    const Q4Half sc = shfl_half(own, (lane & 7) + 8 * c);
+                    uint2 v[RPT];
+                    Q4Half sc[RPT];
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) {
+                        v[r] = *reinterpret_cast<const uint2*>(rowp[r] + sb * Q4K_BYTES + 16 + 32 * c + 8 * qq);
+                        sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
+                    }
                     mbar_wait(&bars->aempty[c], apar);
-                    q4_quarter(v, sc, arow + c * A_STAGE, o_lo, o_hi);
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r) q4_quarter(v[r], sc[r], ast + c * A_STAGE + rowb[r], o_lo, o_hi);
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->afull[c]);
@@ -495,9 +554,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         mbar_wait(&bars->acc, 0);
         tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2;
+        const int lq = warp & 3, ch = warp >> 2, cpw = 1024 / NDQ;   // columns per warp
         const int hrow = h0 + 32 * lq + lane;
-        for (int c0 = ch * 64; c0 < min(N, ch * 64 + 64); c0 += 16) {
+        for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -606,7 +665,7 @@ cudaError_t launch_clustered(void (*kernel)(Params...), dim3 grid, int cx, size_
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-constexpr size_t GU_SMEM = 1024 + ((NQ * QSTAGE_GU + 1023) & ~1023) + NA * A_STAGE + B_BYTES_GU +
+constexpr size_t GU_SMEM = 1024 + ((GU_NQ * QSTAGE_GU + 1023) & ~1023) + GU_NA * A_STAGE + B_BYTES_GU +
                            sizeof(PfBars) + 64;
 
 size_t dn_smem(int F, int down_t) {
@@ -629,7 +688,8 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
                            float* out, cudaStream_t st) {
     const int P = s.T * s.K;
     const int max_used = P < s.E ? P : s.E;
-    const int ntiles = (s.T + TILE_NMAX - 1) / TILE_NMAX;   // an expert sees each token once at most
+    // an expert sees each token once at most
+    const int ntiles_gu = (s.T + GU_NMAX - 1) / GU_NMAX, ntiles = (s.T + TILE_NMAX - 1) / TILE_NMAX;
     gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -653,8 +713,8 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles};
-    e = launch_clustered(prefill_gateup, dim3(s.F / 64, max_used * ntiles), cgu, GU_SMEM, st, tg, tu, tx64,
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles_gu};
+    e = launch_clustered(prefill_gateup, dim3(s.F / 64, max_used * ntiles_gu), cgu, GU_SMEM, st, tg, tu, tx64,
                          tx128, tx256, gp);
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, ntiles, down_t};

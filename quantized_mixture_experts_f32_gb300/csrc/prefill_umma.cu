@@ -37,7 +37,7 @@ constexpr int KBLK = 64;                       // k per tensor-core block (128 B
 constexpr int TILE_M = 128;
 constexpr int TILE_NMAX = 256;
 constexpr int A_STAGE = TILE_M * KBLK * 2;     // 16 KB fp16 A block
-constexpr int NDQ = 8;                         // dequant / epilogue warps (4 threads per A row)
+constexpr int NDQ = 16;                        // dequant / epilogue warps (4 threads per A row)
 constexpr int RPT = 16 / NDQ;                  // A rows per dequant thread
 static_assert(NDQ * RPT == 16 && NDQ % 4 == 0, "128 A rows, 8 per warp per pass");
 constexpr int W_QLOAD = NDQ;                   // weight copies
@@ -53,16 +53,16 @@ static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
 constexpr int NQ = 3;                          // raw Q4_K stages, at most
 // gate/up kernel: token-tile rows, raw and A stages, CTAs per SM it is built
 // for (the stage rings and TMEM columns must fit that many CTAs), TMEM columns
-constexpr int GU_NMAX = 128;
-constexpr int GU_NQ = 2;
-constexpr int GU_NA = 2;
-constexpr int GU_MINB = 2;
-constexpr uint32_t GU_TMEM = 128;
+constexpr int GU_NMAX = 256;
+constexpr int GU_NQ = 3;
+constexpr int GU_NA = 4;
+constexpr int GU_MINB = 1;
+constexpr uint32_t GU_TMEM = 256;
 static_assert(GU_NQ <= NQ && GU_NA <= NA && (GU_NA == 2 || GU_NA == 4) && GU_NMAX <= (int)GU_TMEM,
               "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
 constexpr int NBMAX = 8;                       // B stages, at most
-constexpr int B_BYTES_GU = 40 * 1024;
+constexpr int B_BYTES_GU = 96 * 1024;
 constexpr int B_BYTES_DN = 64 * 1024;
 // CTAs of one (expert, token tile) that share its B rows can run as a cluster:
 // each then TMA-loads 1/C of every B stage and multicasts it to the others.
@@ -665,11 +665,8 @@ cudaError_t launch_clustered(void (*kernel)(Params...), dim3 grid, int cx, size_
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// a whole number of KB: with two CTAs on an SM the second one's shared memory
-// then starts on a 1024-byte boundary too, where the 128-byte swizzle the
-// dequant warps write by hand lines up with the one TMA and the MMA apply
-constexpr size_t GU_SMEM = (1024 + ((GU_NQ * QSTAGE_GU + 1023) & ~1023) + GU_NA * A_STAGE + B_BYTES_GU +
-                            sizeof(PfBars) + 64 + 1023) & ~size_t(1023);
+constexpr size_t GU_SMEM = 1024 + ((GU_NQ * QSTAGE_GU + 1023) & ~1023) + GU_NA * A_STAGE + B_BYTES_GU +
+                           sizeof(PfBars) + 64;
 
 size_t dn_smem(int F, int down_t) {
     const size_t rb = (size_t)(F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);

@@ -16,7 +16,10 @@ issue "Forward-pass divergence on Qwen3-Coder 30B-A3B" (closing comment).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test (closed
 forms, library routines, brute force, invariants); the 48-layer composition as a
-whole is pinned only through its pinned parts.
+whole is pinned only through its pinned parts.  The Q8_K-activation functions
+(``q8k_quantize``, ``q8k_dot``, ``moe_ffn_q8k``) follow a reading of a format the
+pages name without defining (the GGUF 8-bit activation block); they are pinned
+by invariants, exact cases and the independent numpy dequantiser.
 """
 from __future__ import annotations
 
@@ -79,6 +82,12 @@ def lib():
             L.qo_rmsnorm.argtypes = [C.c_long, dp, fp, C.c_double, dp]
             L.qo_rope_neox.argtypes = [C.c_int, dp, C.c_int, C.c_double]
             L.qo_attend.argtypes = [C.c_int, dp, u16, u16, C.c_int, dp]
+            i8p, i16p = C.POINTER(C.c_int8), C.POINTER(C.c_int16)
+            L.qo_q8k_quantize.argtypes = [C.c_long, fp, fp, i8p, i16p]
+            L.qo_dot_q8k.argtypes = [C.c_int, up8, C.c_long, fp, i8p, i16p]
+            L.qo_dot_q8k.restype = C.c_double
+            L.qo_moe_ffn_q8k.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, dp, ip,
+                                         dp, up8, C.c_int, up8, C.c_int, up8, C.c_int, dp, dp]
             L.qo_decode_layer.argtypes = (
                 [C.c_int] * 8 + [C.c_double, C.c_double, C.c_int, dp] + [fp] * 4 + [up8] * 4
                 + [fp, up8, up8, up8, C.c_int, u16, u16, ip, fp, ip, dp, dp, dp])
@@ -169,6 +178,49 @@ def moe_ffn(x, ids, w, gate, up, down, gate_t, up_t, down_t, F, E, res=None, wan
                           _p(act, C.c_double), None)
     if rc:
         raise ValueError(f"moe_ffn failed rc={rc}")
+    return (out, act) if want_act else out
+
+
+# ----------------------------------------------------------------------------- Q8_K activations
+
+def q8k_quantize(x):
+    """Q8_K blocks of a float vector (length a multiple of 256): d [n/256] (f32),
+    q [n] (int8), bsums [n/16] (int16).  See qo_q8k_quantize for the reading."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    n = x.size
+    d = np.empty(n // 256, dtype=np.float32)
+    q = np.empty(n, dtype=np.int8)
+    bs = np.empty(n // 16, dtype=np.int16)
+    if lib().qo_q8k_quantize(n, _p(x, C.c_float), _p(d, C.c_float), _p(q, C.c_int8), _p(bs, C.c_int16)):
+        raise ValueError("length must be a multiple of 256")
+    return d, q, bs
+
+
+def q8k_dot(qtype: str, row: np.ndarray, cols: int, q8) -> float:
+    """One weight row (cols/256 superblocks) against Q8_K blocks, integer form."""
+    d, q, bs = (np.ascontiguousarray(a) for a in q8)
+    row = _u8(row).reshape(-1)
+    return lib().qo_dot_q8k(QCODE[qtype], _p(row, C.c_uint8), cols, _p(d, C.c_float),
+                            _p(q, C.c_int8), _p(bs, C.c_int16))
+
+
+def moe_ffn_q8k(x, ids, w, gate, up, down, gate_t, up_t, down_t, F, E, res=None, want_act=False):
+    """moe_ffn with every expert GEMV on Q8_K activations (x for gate/up, act for down)."""
+    x = _f64(np.atleast_2d(x))
+    T, H = x.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    K = ids.shape[1]
+    w = _f64(w)
+    res = None if res is None else _f64(np.atleast_2d(res))
+    out = np.empty((T, H), dtype=np.float64)
+    act = np.empty((T, K, F), dtype=np.float64) if want_act else None
+    g8, u8, d8 = _u8(gate).reshape(-1), _u8(up).reshape(-1), _u8(down).reshape(-1)
+    rc = lib().qo_moe_ffn_q8k(T, H, F, E, K, _p(x, C.c_double), _p(res, C.c_double),
+                              _p(ids, C.c_int32), _p(w, C.c_double), _p(g8, C.c_uint8), QCODE[gate_t],
+                              _p(u8, C.c_uint8), QCODE[up_t], _p(d8, C.c_uint8), QCODE[down_t],
+                              _p(out, C.c_double), _p(act, C.c_double))
+    if rc:
+        raise ValueError(f"moe_ffn_q8k failed rc={rc}")
     return (out, act) if want_act else out
 
 

@@ -292,6 +292,163 @@ int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double*
     return 0;
 }
 
+/* ------------------------------------------------------------------ Q8_K activations */
+
+/* The int8-activation variant ([P2] "Gaps ... G8": the expert GEMVs run as
+ * DP4A kernels on 8-bit activations; "The Q8_K point": that path scored 0.8725
+ * where FP32 activations scored 1.0).  The pages name the activation format,
+ * Q8_K, without defining it; the reading taken is the GGUF 8-bit activation
+ * block: 256 values, one fp32 scale d, 256 int8 codes and 16 sums of 16 codes.
+ * The block's value of largest magnitude v (the first, on a tie) maps to code
+ * -128: s = -128/v, q_i = min(127, rint(s*x_i)), d = 1/s, all in fp32 (the
+ * codes are integers decided by floating point, so they are decided in the
+ * precision a kernel uses); an all-zero block has d = 0 and q = 0.
+ * n is a multiple of 256; x has n floats; d gets n/256, q n, bsums n/16. */
+int qo_q8k_quantize(long n, const float* x, float* d, int8_t* q, int16_t* bsums) {
+    if (n % QO_QK) return -1;
+    for (long b = 0; b < n / QO_QK; ++b) {
+        const float* xb = x + b * QO_QK;
+        float v = 0.0f, amax = 0.0f;
+        for (int i = 0; i < QO_QK; ++i)
+            if (fabsf(xb[i]) > amax) {
+                amax = fabsf(xb[i]);
+                v = xb[i];
+            }
+        if (amax == 0.0f) {
+            d[b] = 0.0f;
+            for (int i = 0; i < QO_QK; ++i) q[b * QO_QK + i] = 0;
+        } else {
+            volatile float s = -128.0f / v;   /* kept in fp32 */
+            for (int i = 0; i < QO_QK; ++i) {
+                volatile float t = s * xb[i];
+                int c = (int)rintf(t);
+                q[b * QO_QK + i] = (int8_t)(c > 127 ? 127 : c);
+            }
+            d[b] = 1.0f / s;
+        }
+        for (int g = 0; g < QO_QK / 16; ++g) {
+            int acc = 0;
+            for (int i = 0; i < 16; ++i) acc += q[b * QO_QK + 16 * g + i];
+            bsums[b * (QO_QK / 16) + g] = (int16_t)acc;
+        }
+    }
+    return 0;
+}
+
+/* Code (0..15) of element i of a Q4_K superblock and its sub-block j = i/32
+ * (layout as in qo_q4k_element). */
+static int q4k_code(const uint8_t* blk, int i) {
+    int j = i / 32, l = i % 32;
+    return (blk[16 + 32 * (j / 2) + l] >> (4 * (j % 2))) & 15;
+}
+
+/* Signed code q6 - 32 of element i of a Q6_K superblock and its int8 scale
+ * (layout as in qo_q6k_element). */
+static int q6k_code(const uint8_t* blk, int i, int* scale) {
+    int n = i / 128, g = (i % 128) / 32, l = i % 32;
+    int lo = (blk[64 * n + l + 32 * (g % 2)] >> (4 * (g / 2))) & 15;
+    int hi = (blk[128 + 32 * n + l] >> (2 * g)) & 3;
+    *scale = ((const int8_t*)(blk + 192))[8 * n + l / 16 + 2 * g];
+    return (lo | (hi << 4)) - 32;
+}
+
+/* Dot product of one weight row (cols/256 superblocks of qtype) with a Q8_K
+ * vector, in the integer form an int8 kernel evaluates, superblock by
+ * superblock in order:
+ *   Q4_K: dx * sum_j [ d*s_j * S_j - dmin*m_j * B_j ], with S_j the integer sum
+ *         of q4*q8 over sub-block j (32 values) and B_j the sum of its q8 codes
+ *         (the two 16-code sums bsums[2j], bsums[2j+1]);
+ *   Q6_K: dx * d * sum over the 16 groups of 16 values of sc_g * sum (q6-32)*q8.
+ * Integer sums are exact; the scaling is in double. */
+double qo_dot_q8k(int qtype, const uint8_t* row, long cols, const float* d8, const int8_t* q8,
+                  const int16_t* bs8) {
+    int bb = qo_block_bytes(qtype);
+    double acc = 0.0;
+    for (long b = 0; b < cols / QO_QK; ++b) {
+        const uint8_t* blk = row + b * bb;
+        const int8_t* qb = q8 + b * QO_QK;
+        const int16_t* sb = bs8 + b * (QO_QK / 16);
+        double part = 0.0;
+        if (qtype == QO_Q4_K) {
+            double d = half_at(blk), dmin = half_at(blk + 2);
+            for (int j = 0; j < 8; ++j) {
+                long S = 0;
+                for (int l = 0; l < 32; ++l) S += (long)q4k_code(blk, 32 * j + l) * qb[32 * j + l];
+                long B = (long)sb[2 * j] + sb[2 * j + 1];
+                int s, m;
+                q4k_scale_min(blk + 4, j, &s, &m);
+                part += d * s * (double)S - dmin * m * (double)B;
+            }
+        } else {
+            double d = half_at(blk + 208);
+            for (int g = 0; g < 16; ++g) {
+                long S = 0;
+                int sc = 0;
+                for (int l = 0; l < 16; ++l) S += (long)q6k_code(blk, 16 * g + l, &sc) * qb[16 * g + l];
+                part += d * sc * (double)S;
+            }
+        }
+        acc += (double)d8[b] * part;
+    }
+    return acc;
+}
+
+/* The MoE FFN of qo_moe_ffn with every expert GEMV on Q8_K activations: the
+ * token's x (as fp32) is quantised once for gate and up, the SwiGLU output a
+ * (as fp32) once for down; the router, SwiGLU and the weighted sum stay as in
+ * qo_moe_ffn.  act (nullable) receives a [T][K][F]. */
+int qo_moe_ffn_q8k(int T, int H, int F, int E, int K, const double* x, const double* res,
+                   const int32_t* ids, const double* w,
+                   const uint8_t* gate, int gate_t, const uint8_t* up, int up_t,
+                   const uint8_t* down, int down_t, double* out, double* act) {
+    long sg = qo_expert_stride(gate_t, F, H), su = qo_expert_stride(up_t, F, H);
+    long sd = qo_expert_stride(down_t, H, F);
+    if (sg < 0 || su < 0 || sd < 0 || H % QO_QK || F % QO_QK) return -1;
+    for (long p = 0; p < (long)T * K; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return -2;
+    long rbg = sg / F, rbu = su / F, rbd = sd / H;    /* bytes per weight row */
+    double* Y = (double*)malloc(sizeof(double) * (size_t)T * K * H);
+    if (!Y) return -3;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long p = 0; p < (long)T * K; ++p) {
+        long t = p / K;
+        int e = ids[p];
+        float* xf = (float*)malloc(sizeof(float) * (size_t)(H > F ? H : F));
+        int8_t* q8 = (int8_t*)malloc((size_t)(H > F ? H : F));
+        float* d8 = (float*)malloc(sizeof(float) * (size_t)(H > F ? H : F) / QO_QK);
+        int16_t* b8 = (int16_t*)malloc(sizeof(int16_t) * (size_t)(H > F ? H : F) / 16);
+        double* a = (double*)malloc(sizeof(double) * (size_t)F);
+        if (!xf || !q8 || !d8 || !b8 || !a) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+            for (long h = 0; h < H; ++h) xf[h] = (float)x[t * H + h];
+            qo_q8k_quantize(H, xf, d8, q8, b8);
+            for (long f = 0; f < F; ++f) {
+                double g = qo_dot_q8k(gate_t, gate + (long)e * sg + f * rbg, H, d8, q8, b8);
+                double u = qo_dot_q8k(up_t, up + (long)e * su + f * rbu, H, d8, q8, b8);
+                a[f] = silu(g) * u;
+            }
+            if (act) memcpy(act + p * F, a, sizeof(double) * (size_t)F);
+            for (long f = 0; f < F; ++f) xf[f] = (float)a[f];
+            qo_q8k_quantize(F, xf, d8, q8, b8);
+            for (long h = 0; h < H; ++h)
+                Y[p * H + h] = qo_dot_q8k(down_t, down + (long)e * sd + h * rbd, F, d8, q8, b8);
+        }
+        free(xf); free(q8); free(d8); free(b8); free(a);
+    }
+    if (err) { free(Y); return -3; }
+    for (long t = 0; t < T; ++t)
+        for (long h = 0; h < H; ++h) {
+            double acc = res ? res[t * H + h] : x[t * H + h];
+            for (long j = 0; j < K; ++j) acc += w[t * K + j] * Y[(t * K + j) * H + h];
+            out[t * H + h] = acc;
+        }
+    free(Y);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ decoder layer pieces */
 
 /* RMSNorm: x / sqrt(mean(x^2) + eps) * w. */

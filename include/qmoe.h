@@ -121,6 +121,23 @@ qmoe_status qmoe_forward_ex(qmoe_ctx* ctx, const float* ffn_in, const float* res
                             qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
                             int n_tokens, float* out, int32_t* ids_out, float* weights_out);
 
+/* The same layer with 8-bit activations in every expert GEMV: the int8 (DP4A)
+ * variant of the aprender issue "qwen3moe (Qwen3-30B-A3B, ...) has NO working
+ * CUDA path" ("Gaps ... G8"; its R1 receipt measures it against FP32
+ * activations).  hidden_out = hidden_in + MoE(hidden_in) where x (per token)
+ * and the SwiGLU output (per selected expert) are first quantised to Q8_K
+ * blocks of 256 values: fp32 scale d, int8 codes, the block's largest-magnitude
+ * value (first on a tie) on code -128 (s = -128/v, q = min(127, rint(s*x)),
+ * d = 1/s, fp32), and each weight row is dotted with the codes in integer form.
+ * The router stays F32.  Arguments as qmoe_forward; ids_out / weights_out as
+ * qmoe_forward_ex (nullable).  hidden_out may alias hidden_in.  Any n_tokens in
+ * 1..max_tokens; hidden and ffn multiples of 256 (as for every entry point).
+ * Argument errors are returned before any launch, as for qmoe_forward. */
+qmoe_status qmoe_forward_q8k(qmoe_ctx* ctx, const float* hidden_in, const float* router_w,
+                             const void* gate_exps, const void* up_exps, const void* down_exps,
+                             qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
+                             int n_tokens, float* hidden_out, int32_t* ids_out, float* weights_out);
+
 /* Same as qmoe_forward, but hidden_in / hidden_out are HOST pointers (pinned
  * memory gives asynchronous copies).  Copies the activations to the device
  * workspace, runs the layer, copies the result back and synchronises the

@@ -40,7 +40,7 @@ LAUNCHES_PER_DECODE_STEP = 1
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
-            "qmoe_fused_decode_available"]
+            "qmoe_fused_decode_available", "qmoe_forward_q8k"]
 
 
 class qmoe_config(C.Structure):
@@ -83,6 +83,8 @@ def _load():
     L.qmoe_forward_ex.argtypes = [vp, fp, fp, fp, fp, vp, vp, vp, i, i, i, i, fp, ip, fp]
     L.qmoe_forward_ex.restype = i
     L.qmoe_forward_host.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp]
+    L.qmoe_forward_q8k.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp, ip, fp]
+    L.qmoe_forward_q8k.restype = i
     L.qmoe_forward_host.restype = i
     L.qmoe_decode_step.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, fp, ip]
     L.qmoe_decode_step.restype = i
@@ -150,6 +152,13 @@ def qmoe_forward_ex(ctx, ffn_in, residual, router_bias, router_w, gate_exps, up_
                                     _ptr(router_w), _ptr(gate_exps), _ptr(up_exps),
                                     _ptr(down_exps), gate_t, up_t, down_t, n_tokens, _ptr(out),
                                     _ptr(ids_out), _ptr(weights_out)))
+
+
+def qmoe_forward_q8k(ctx, hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t, up_t, down_t,
+                     n_tokens, hidden_out, ids_out=None, weights_out=None):
+    _check(ctx, lib.qmoe_forward_q8k(ctx, _ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
+                                     _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t,
+                                     n_tokens, _ptr(hidden_out), _ptr(ids_out), _ptr(weights_out)))
 
 
 def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,

@@ -29,6 +29,7 @@ struct qmoe_ctx {
     __half* xp;       // [P][H] fp16 gathered x (prefill)
     __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
     int32_t* inv_pos; // [P] pair -> position in the expert-sorted list
+    qmoe::Q8Bufs q8;  // Q8_K codes of x and act (qmoe_forward_q8k)
     int num_sms;
     // decode-step scratch
     float* xs;        // [H] normed hidden
@@ -68,7 +69,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, logits_part, tokmap, jmap, ftag, xs, q, kv, att, attn_part, inv_freq,
+        status, bar, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
         rope_cs, total;
     int attn_splits;
 };
@@ -119,6 +120,7 @@ Layout layout(const qmoe_config* c) {
     L.logits_part = take(sizeof(float) * qmoe::route_many_part_floats((int)T, (int)H, (int)E));
     L.tokmap = take(sizeof(uint32_t) * qmoe::route_many_tokmap_words((int)T, (int)E));
     L.jmap = take(E * T);
+    L.q8 = take(qmoe::q8_bufs_bytes((int)T, (int)H, (int)K, (int)F));
     const int Tf = (int)(T < 8 ? T : 8);                 // the fused decode kernel serves T <= 8
     L.ftag = take(qmoe::fused_bufs_bytes(Tf, (int)H, (int)E, (int)K, (int)F, FUSED_GRID_MAX));
     const size_t qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim;
@@ -287,6 +289,8 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.logits_part = reinterpret_cast<float*>(b + L.logits_part);
     c->route.tokmap = reinterpret_cast<uint32_t*>(b + L.tokmap);
     c->route.jmap = reinterpret_cast<uint8_t*>(b + L.jmap);
+    c->q8 = qmoe::q8_bufs_carve(reinterpret_cast<unsigned char*>(b + L.q8), c->cfg.max_tokens, c->cfg.hidden,
+                                c->cfg.top_k, c->cfg.ffn);
     c->act = reinterpret_cast<float*>(b + L.act);
     c->y = reinterpret_cast<float*>(b + L.y);
     c->hin = reinterpret_cast<float*>(b + L.hin);
@@ -378,6 +382,30 @@ qmoe_status qmoe_forward_ex(qmoe_ctx* c, const float* ffn_in, const float* resid
         return fail(c, QMOE_ERR_INVALID_ARG, "out may alias residual only for n_tokens <= %d", DECODE_ALIAS_MAX);
     return run_moe(c, ffn_in, residual, router_bias, router_w, gate_exps, up_exps, down_exps,
                    gate_t, up_t, down_t, n_tokens, out, ids_out, weights_out);
+}
+
+qmoe_status qmoe_forward_q8k(qmoe_ctx* c, const float* hidden_in, const float* router_w,
+                             const void* gate_exps, const void* up_exps, const void* down_exps,
+                             qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t, int n_tokens,
+                             float* hidden_out, int32_t* ids_out, float* weights_out) {
+    qmoe_status s = check_forward(c, hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t,
+                                  up_t, down_t, n_tokens, hidden_out);
+    if (s != QMOE_OK) return s;
+    const qmoe_config& k = c->cfg;
+    qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    cudaError_t e = qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    e = qmoe::launch_moe_q8k(ms, hidden_in, hidden_in, static_cast<const uint8_t*>(gate_exps), gate_t,
+                             static_cast<const uint8_t*>(up_exps), up_t,
+                             static_cast<const uint8_t*>(down_exps), down_t, c->route, c->q8, c->act,
+                             c->y, hidden_out, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "Q8_K expert launch");
+    if (ids_out || weights_out) {
+        e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
 }
 
 qmoe_status qmoe_forward_host(qmoe_ctx* c, const float* hin, const float* router_w,

@@ -57,6 +57,25 @@ cudaError_t launch_combine(const MoeShape& s, const float* y, const Route& r, co
                            float* out, cudaStream_t st);
 
 // Copy the routing results out (ids int32, weights f32), async.
+// The MoE FFN with 8-bit (Q8_K) activations in every expert GEMV (moe_q8k.cu):
+// the codes, scales and 16-value code sums of x (per token) and of act (per pair).
+struct Q8Bufs {
+    int8_t* qx;
+    float* dx;
+    int16_t* bx;
+    int8_t* qa;
+    float* da;
+    int16_t* ba;
+};
+size_t q8_bufs_bytes(int T, int H, int K, int F);
+Q8Bufs q8_bufs_carve(unsigned char* base, int T, int H, int K, int F);
+// after launch_route: quantise x, gate/up + SwiGLU into act, quantise act, down
+// into y, combine into out (= res + sum_j w_j y_j)
+cudaError_t launch_moe_q8k(const MoeShape& s, const float* x, const float* res, const uint8_t* gate,
+                           int gate_t, const uint8_t* up, int up_t, const uint8_t* down, int down_t,
+                           const Route& r, const Q8Bufs& b, float* act, float* y, float* out,
+                           cudaStream_t st);
+
 cudaError_t copy_route_out(const MoeShape& s, const Route& r, int32_t* ids_out, float* w_out,
                            cudaStream_t st);
 

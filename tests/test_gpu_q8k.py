@@ -1,0 +1,103 @@
+"""Parity of the CUDA Q8_K-activation MoE FFN (qmoe_forward_q8k) with the
+oracle's Q8_K variant (oracle.moe_ffn_q8k), through the C ABI.
+
+The activation codes are integers decided in fp32 on both sides from the same
+fp32 x, so the gate/up inputs agree exactly; act is fp32 on the GPU and fp64
+rounded to fp32 in the oracle, so a code of act can differ by one at a rounding
+boundary, an effect far below the bound.  Bound: max relative error 2e-3 (the
+fp32 paths' bound).  The GPU result must also sit much closer to the Q8_K
+oracle than to the FP32-activation oracle, so the path is shown to quantise.
+Expert ids must match exactly up to F32 near-ties, weights within 1e-5.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.compare import TOL_FP32, TOL_W, ids_match, rel_err, tie_bound_f32
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_mixture_experts_f32_gb300 as q
+    return q
+
+
+from tests import gpu_util as G  # noqa: E402
+
+
+def _run(q, inp):
+    d = G.upload(inp)
+    T, H, K = inp["T"], inp["H"], inp["K"]
+    ctx = G.make_ctx(q, inp)
+    try:
+        out = torch.empty((T, H), dtype=torch.float32, device=G.dev())
+        ids = torch.full((T, K), -1, dtype=torch.int32, device=G.dev())
+        w = torch.full((T, K), -1.0, dtype=torch.float32, device=G.dev())
+        q.qmoe_forward_q8k(ctx, d["x"], d["router"], d["gate"], d["up"], d["down"],
+                           q.QTYPE[inp["gate_t"]], q.QTYPE[inp["up_t"]], q.QTYPE[inp["down_t"]], T,
+                           out, ids, w)
+        assert q.qmoe_get_status(ctx) == q.QMOE_OK, q.qmoe_last_error(ctx)
+        return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+    finally:
+        q.qmoe_destroy(ctx)
+
+
+CASES = [
+    (1, None, {}),                                                   # tiny, T=4
+    (1, 9, {"gate_t": "Q6_K", "up_t": "Q6_K", "down_t": "Q4_K"}),    # other formats, ragged T
+    (2, None, {}),                                                   # Qwen3-30B-A3B decode, T=1
+    (3, None, {}),                                                   # decode batch 8, Q4_K down
+]
+
+
+@pytest.mark.parametrize("cfg_id,T,over", CASES)
+def test_q8k_layer_matches_oracle(q, cfg_id, T, over):
+    cfg = dict(synth.MOE_CONFIGS[cfg_id], **over)
+    inp = synth.moe_inputs(cfg, T=T)
+    got, ids, w = _run(q, inp)
+    logits, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"])
+    bound = tie_bound_f32(inp["router"], inp["x"], None)
+    ok, ties = ids_match(ids, rids, logits, bound)
+    assert ok, f"expert ids differ beyond near-ties:\n{ids}\n{rids}"
+    if ties:
+        _, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"], force=ids)
+    assert np.abs(w - rw).max() <= TOL_W
+    args = (inp["x"], rids, rw, inp["gate"], inp["up"], inp["down"], inp["gate_t"], inp["up_t"],
+            inp["down_t"], inp["F"], inp["E"])
+    want = oracle.moe_ffn_q8k(*args)
+    err = rel_err(got, want)
+    assert err <= TOL_FP32, f"max relative error {err:.3e} > {TOL_FP32:.1e}"
+    fp = oracle.moe_ffn(*args)
+    err_fp = rel_err(got - inp["x"], fp - inp["x"])
+    err_q8 = rel_err(got - inp["x"], want - inp["x"])
+    assert err_q8 < 0.2 * err_fp, (err_q8, err_fp)
+    print(f"cfg {cfg_id} T={inp['T']}: vs Q8_K oracle {err:.2e}, MoE part vs Q8_K {err_q8:.2e}, "
+          f"vs FP32-activation oracle {err_fp:.2e}")
+
+
+def test_q8k_argument_errors_before_launch(q):
+    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    d = G.upload(inp)
+    ctx = G.make_ctx(q, inp)
+    try:
+        out = torch.empty((inp["T"], inp["H"]), dtype=torch.float32, device=G.dev())
+        with pytest.raises(q.QmoeError):
+            q.qmoe_forward_q8k(ctx, None, d["router"], d["gate"], d["up"], d["down"], 1, 1, 2,
+                               inp["T"], out)
+        with pytest.raises(q.QmoeError):
+            q.qmoe_forward_q8k(ctx, d["x"], d["router"], d["gate"], d["up"], d["down"], 1, 1, 2,
+                               inp["T"] + 1, out)
+        with pytest.raises(q.QmoeError):
+            q.qmoe_forward_q8k(ctx, d["x"], d["router"], d["gate"], d["up"], d["down"], 1, 1, 7,
+                               inp["T"], out)
+    finally:
+        q.qmoe_destroy(ctx)

@@ -13,6 +13,9 @@
  *     y_e = Wd_e a                                Q6_K or Q4_K down dequant-GEMV
  *   out = residual + sum_j w_j y_{S_j}            weighted sum into the residual
  *
+ * qmoe_forward_q8k runs the same layer with x and a quantised to 8-bit (Q8_K)
+ * activations before every expert GEMV (the int8 variant of "Gaps ... G8").
+ *
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer that the caller allocated and owns
  *    (except qmoe_forward_host, whose activations are host pointers).  The

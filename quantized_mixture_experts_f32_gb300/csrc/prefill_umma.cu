@@ -296,9 +296,9 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         // quarter qq = lane >> 3 of every k-block (each 8-lane phase of a 16-byte
         // store then covers all 32 banks).  All NDQ warps fill each A stage in turn, so
         // the GU_NA stages run ahead of the MMA.
-        // A raw superblock column is read into registers at once and its stage
-        // released; the scales of k-block c are decoded by the row's lane with
-        // qq == c and shuffled to the other three.
+        // A raw superblock column is read into registers at once (its stage is
+        // released after the superblock's k-blocks); the scales of k-block c are
+        // decoded by the row's lane with qq == c and shuffled to the other three.
         const int qq = lane >> 3;
         int src[RPT], rowb[RPT];
 #pragma unroll
@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         int sq = 0;
         uint32_t qpar = 0;
         for (int sb = 0; sb < NSB; ++sb) {
+            const int sq_this = sq;
             const uint8_t* stg = qst + sq * QSTAGE_GU;
             mbar_wait(&bars->qfull[sq], qpar);
             uint4 hdr[RPT];
@@ -323,8 +324,6 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
                 for (int c = 0; c < 4; ++c)
                     v[r][c] = *reinterpret_cast<const uint2*>(stg + src[r] + 16 + 32 * c + 8 * qq);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->qempty[sq]);
             if (++sq == GU_NQ) {
                 sq = 0;
                 qpar ^= 1u;
@@ -347,6 +346,11 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->afull[sa]);
             }
+            // the raw stage is handed back only now: every value loaded from it
+            // has fed a store above, so no load of this warp is still pending
+            // when the next TMA copy may overwrite it (releasing right after the
+            // loads were issued let a late load read the next superblock)
+            if (lane == 0) mbar_arrive(&bars->qempty[sq_this]);
         }
         // epilogue: TMEM lane quarter (warp % 4); column quarter (warp / 4)
         mbar_wait(&bars->acc, 0);

@@ -55,11 +55,15 @@ WORKLOADS = {
     "prefill4096": dict(cfg=4, T=4096, copies=2, e2e=5, steps=60, warmup=3,
                         desc="qwen3moe-30b-a3b MoE layer prefill, T=4096, biased router, Q6_K "
                              "down (supplementary)"),
+    # supplementary: the int8-activation variant (qmoe_forward_q8k) of the decode layer
+    "decode_q8k": dict(cfg=2, copies=32, e2e=2000, steps=20000, warmup=200, q8k=True,
+                       desc="qwen3moe-30b-a3b MoE layer decode, T=1, Q8_K activations (int8 "
+                            "variant), Q4_K gate/up, Q6_K down (supplementary)"),
 }
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_fused_decode_T1.md", "batch8": None, "prefill": None,
-               "step48": None, "prefill4096": None}
+               "step48": None, "prefill4096": None, "decode_q8k": None}
 FUSED_SOURCES = ["moe_decode_fused.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -186,10 +190,11 @@ def expert_bytes(H, F, gate_t, up_t, down_t):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_sample_layer(inp, seconds: float, max_tokens: int):
+def cpu_sample_layer(inp, seconds: float, max_tokens: int, q8k: bool = False):
     """The oracle on a bounded sample of the layer workload: tokens/s/layer."""
     import oracle
     oracle.build()
+    forward = oracle.moe_forward_q8k if q8k else oracle.moe_forward
     T = inp["T"]
     n = min(T, max_tokens)
     one = dict(inp)
@@ -197,7 +202,7 @@ def cpu_sample_layer(inp, seconds: float, max_tokens: int):
     one["T"] = n
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.moe_forward(one)
+        forward(one)
         done += 1
         el = time.perf_counter() - t0
         if el >= seconds and done >= 1:
@@ -244,7 +249,8 @@ def run_reference(args):
         one = dict(inp)
         one["x"] = inp["x"][:sample]
         one["T"] = sample
-        step = lambda: oracle.moe_forward(one)  # noqa: E731
+        forward = oracle.moe_forward_q8k if w.get("q8k") else oracle.moe_forward
+        step = lambda: forward(one)  # noqa: E731
         tokens_per_step = sample
         what = f"{sample} tokens of the {args.workload} layer workload per step"
     else:
@@ -369,15 +375,24 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
     copies = [base] + [{n: t.clone() for n, t in base.items()} for _ in range(R - 1)]
     out = torch.empty((T, H), dtype=torch.float32, device=dev)
     ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream))
+    q8k = w.get("q8k", False)
+    assert not (q8k and bias is not None), "the Q8_K entry point takes no router bias"
 
     def mk(c):
+        if q8k:
+            return lambda: q.qmoe_forward_q8k(ctx, x, c["router"], c["gate"], c["up"], c["down"],
+                                              gt, ut, dt, T, out)
         return lambda: q.qmoe_forward_ex(ctx, x, None, bias, c["router"], c["gate"], c["up"],
                                          c["down"], gt, ut, dt, T, out)
 
     ids = torch.empty((T, K), dtype=torch.int32, device=dev)
     with torch.cuda.stream(stream):
-        q.qmoe_forward_ex(ctx, x, None, bias, base["router"], base["gate"], base["up"],
-                          base["down"], gt, ut, dt, T, out, ids, None)
+        if q8k:
+            q.qmoe_forward_q8k(ctx, x, base["router"], base["gate"], base["up"], base["down"], gt,
+                               ut, dt, T, out, ids, None)
+        else:
+            q.qmoe_forward_ex(ctx, x, None, bias, base["router"], base["gate"], base["up"],
+                              base["down"], gt, ut, dt, T, out, ids, None)
     stream.synchronize()
     distinct = len(np.unique(ids.cpu().numpy()))
     ebytes = distinct * expert_bytes(H, F, inp["gate_t"], inp["up_t"], inp["down_t"])
@@ -386,20 +401,32 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
                               pg, dev, local)
     secs = ms / 1e3
     step_s = secs / args.steps
-    # e2e: host buffers through qmoe_forward_host (copies + sync inside every step)
+    # e2e: host buffers through qmoe_forward_host (copies + sync inside every step);
+    # the Q8_K entry point has no host form, so its step copies pinned x in, runs
+    # the layer and copies the result out on the context's stream, then syncs
     hin = torch.from_numpy(inp["x"].copy()).pin_memory()
     hout = torch.empty_like(hin).pin_memory()
+    xin = torch.empty_like(x)
+
+    def host_step(c):
+        if q8k:
+            with torch.cuda.stream(stream):
+                xin.copy_(hin, non_blocking=True)
+                q.qmoe_forward_q8k(ctx, xin, c["router"], c["gate"], c["up"], c["down"], gt, ut,
+                                   dt, T, out)
+                hout.copy_(out, non_blocking=True)
+            stream.synchronize()
+        else:
+            q.qmoe_forward_host(ctx, hin, c["router"], c["gate"], c["up"], c["down"], gt, ut, dt,
+                                T, hout)
+
     for i in range(3):
-        c = copies[i % R]
-        q.qmoe_forward_host(ctx, hin, c["router"], c["gate"], c["up"], c["down"], gt, ut, dt, T,
-                            hout)
+        host_step(copies[i % R])
     if pg:
         pg.barrier()
     te0 = time.perf_counter()
     for i in range(args.e2e_steps):
-        c = copies[i % R]
-        q.qmoe_forward_host(ctx, hin, c["router"], c["gate"], c["up"], c["down"], gt, ut, dt, T,
-                            hout)
+        host_step(copies[i % R])
     te = time.perf_counter() - te0
     if pg:
         tt = torch.tensor([te], device=dev)
@@ -412,19 +439,23 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
         value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
         ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
         e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
-        launches=(q.LAUNCHES_PER_DECODE_FORWARD if T <= 8 else q.LAUNCHES_PER_PREFILL_FORWARD),
+        launches=(q.LAUNCHES_PER_Q8K_FORWARD if q8k else
+                  q.LAUNCHES_PER_DECODE_FORWARD if T <= 8 else q.LAUNCHES_PER_PREFILL_FORWARD),
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB"},
-        kernel=("moe_decode_fused (the whole layer is one kernel)" if T <= 8
+        kernel=("whole Q8_K layer call (routing, quantise, gate/up, quantise, down, combine)"
+                if q8k else "moe_decode_fused (the whole layer is one kernel)" if T <= 8
                 else "whole layer call (routing, gather, grouped GEMMs, combine)"))
+    if q8k:
+        res["dtype"] = "int8 activations (Q8_K), f32 accumulate"
     if T > 8:
         flops = T * K * 2 * (2 * F * H + H * F)
         res["tensor_tflops"] = flops / step_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
-        val, sample = cpu_sample_layer(inp, args.cpu_seconds, 8 if T <= 8 else 16)
+        val, sample = cpu_sample_layer(inp, args.cpu_seconds, 8 if T <= 8 else 16, q8k)
         cpu = {"value": val, "unit": "tokens/s/layer", "cores": cores(), "kind": "oracle",
                "sample": sample}
     return res, cpu
@@ -552,6 +583,8 @@ def main():
         "gpu_launches": args.steps * res["launches"],
         "clocks": res["clocks"],
     }
+    if "dtype" in res:
+        line["dtype"] = res["dtype"]
     if "tensor_tflops" in res:
         line["dtype"] = "f16 tensor-core operands, f32 accumulate"
         line["tensor"] = {"achieved_tflops": res["tensor_tflops"], "peak_tflops": tf,

@@ -224,6 +224,15 @@ def moe_ffn_q8k(x, ids, w, gate, up, down, gate_t, up_t, down_t, F, E, res=None,
     return (out, act) if want_act else out
 
 
+def moe_forward_q8k(inp: dict, norm_topk=True, force=None):
+    """out = x + MoE(x) with Q8_K activations in every expert GEMV (F32 router)."""
+    logits, ids, w, probs = route(inp["x"], inp["router"], inp["K"], inp.get("bias"), norm_topk,
+                                  force)
+    out = moe_ffn_q8k(inp["x"], ids, w, inp["gate"], inp["up"], inp["down"], inp["gate_t"],
+                      inp["up_t"], inp["down_t"], inp["F"], inp["E"])
+    return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
+
+
 def moe_forward(inp: dict, norm_topk=True, force=None):
     """out = x + MoE(x) for one layer's synthetic inputs (see ``synth.moe_inputs``)."""
     logits, ids, w, probs = route(inp["x"], inp["router"], inp["K"], inp.get("bias"), norm_topk,

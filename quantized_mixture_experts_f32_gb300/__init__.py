@@ -27,9 +27,11 @@ QTYPE = {"Q4_K": QMOE_Q4_K, "Q6_K": QMOE_Q6_K}
 # kernels one qmoe_forward enqueues on the decode path (n_tokens <= 8): the
 # whole layer is one fused cooperative kernel
 LAUNCHES_PER_DECODE_FORWARD = 1
-# n_tokens > 8 (tensor-core path): router GEMM, top-k, pair sort, gather, gate/up
-# GEMM, down GEMM, combine
+# n_tokens > 8 (tensor-core path): router GEMM, top-k, per-expert lists, gather,
+# gate/up GEMM, down GEMM, combine
 LAUNCHES_PER_PREFILL_FORWARD = 7
+# qmoe_forward_q8k: router, top-k, quantise x, gate/up, quantise act, down, combine
+LAUNCHES_PER_Q8K_FORWARD = 7
 # one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
 # its RMSNorm)

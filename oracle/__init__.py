@@ -19,7 +19,8 @@ forms, library routines, brute force, invariants); the 48-layer composition as a
 whole is pinned only through its pinned parts.  The Q8_K-activation functions
 (``q8k_quantize``, ``q8k_dot``, ``moe_ffn_q8k``) follow a reading of a format the
 pages name without defining (the GGUF 8-bit activation block); they are pinned
-by invariants, exact cases and the independent numpy dequantiser.
+by invariants, exact cases and the independent numpy dequantiser.  ``prefill_layer``
+is pinned against a batched causal formulation written in the tests.
 """
 from __future__ import annotations
 
@@ -305,3 +306,32 @@ def decode_layer(geo: dict, small: dict, experts: dict, h, pos, force=None, debu
     if debug:
         out.update(q=q, att=att)
     return out
+
+
+def prefill_layer(geo: dict, small: dict, experts: dict, hs, pos0: int, force=None):
+    """One decoder layer on T tokens at positions pos0 .. pos0+T-1 (prefill).
+
+    Within one layer a token's K and V depend on its own input only, so causal
+    attention over the cache (positions < pos0, as stored) and the earlier
+    tokens of the batch is exactly the layer applied token by token, each
+    writing its K/V slot before the next reads it (the token-by-token prefill
+    of the aprender issue "qwen3moe ... has NO working CUDA path", later gap
+    list, which a batched prefill must reproduce).  hs: f64 [T][H].  force
+    (optional): [T][K] expert ids.  Returns dict(h [T][H], ids [T][K], w [T][K],
+    k_cache, v_cache) with the caches' slots pos0.. pos0+T-1 written (copies)."""
+    hs = np.atleast_2d(_f64(hs))
+    T = hs.shape[0]
+    if pos0 < 0 or pos0 + T > geo["ctx"]:
+        raise ValueError("prefill positions outside the context")
+    cur = dict(small)
+    outs, ids, ws = [], [], []
+    for i in range(T):
+        r = decode_layer(geo, cur, experts, hs[i], pos0 + i,
+                         force=None if force is None else np.asarray(force)[i])
+        cur = dict(cur, k_cache=r["k_cache"], v_cache=r["v_cache"])
+        outs.append(r["h"])
+        ids.append(r["ids"])
+        ws.append(r["w"])
+    return dict(h=np.stack(outs), ids=np.stack(ids), w=np.stack(ws), k_cache=cur["k_cache"],
+                v_cache=cur["v_cache"])
+

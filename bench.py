@@ -41,22 +41,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "qwen3moe MoE-FFN tokens/s/layer; expert-weight HBM GB/s vs GB300 peak"
 
 WORKLOADS = {
-    "decode": dict(cfg=2, copies=32, e2e=2000, steps=20000, warmup=200,
+    "decode": dict(cfg="decode", copies=32, e2e=2000, steps=20000, warmup=200,
                    desc="qwen3moe-30b-a3b MoE layer decode, T=1, Q4_K gate/up, Q6_K down"),
-    "batch8": dict(cfg=3, copies=6, e2e=500, steps=4000, warmup=40,
+    "batch8": dict(cfg="batch8", copies=6, e2e=500, steps=4000, warmup=40,
                    desc="qwen3moe-30b-a3b MoE layer decode batch, T=8, Q4_K gate/up, Q4_K down"),
-    "prefill": dict(cfg=4, copies=3, e2e=20, steps=300, warmup=6,
+    "prefill": dict(cfg="prefill", copies=3, e2e=20, steps=300, warmup=6,
                     desc="qwen3moe-30b-a3b MoE layer prefill, T=512, biased router, Q6_K down"),
     "step48": dict(cfg=None, copies=1, e2e=10, steps=400, warmup=3,
                    desc="qwen3moe-30b-a3b 48-layer decode step, T=1, context 4096"),
     # supplementary (not one of the five configurations): the prefill layer at
     # T=4096, where the contraction is compute-bound and the tensor-pipe
     # fraction is the meaningful one
-    "prefill4096": dict(cfg=4, T=4096, copies=2, e2e=5, steps=60, warmup=3,
+    "prefill4096": dict(cfg="prefill", T=4096, copies=2, e2e=5, steps=60, warmup=3,
                         desc="qwen3moe-30b-a3b MoE layer prefill, T=4096, biased router, Q6_K "
                              "down (supplementary)"),
     # supplementary: the int8-activation variant (qmoe_forward_q8k) of the decode layer
-    "decode_q8k": dict(cfg=2, copies=32, e2e=2000, steps=20000, warmup=200, q8k=True,
+    "decode_q8k": dict(cfg="decode", copies=32, e2e=2000, steps=20000, warmup=200, q8k=True,
                        desc="qwen3moe-30b-a3b MoE layer decode, T=1, Q8_K activations (int8 "
                             "variant), Q4_K gate/up, Q6_K down (supplementary)"),
 }

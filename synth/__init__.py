@@ -82,13 +82,13 @@ def expert_tensor(seed: int, which: str, n_experts: int, qtype: str, rows: int, 
 # --------------------------------------------------------------------------- MoE FFN workloads
 
 MOE_CONFIGS = {
-    1: dict(name="tiny", H=256, E=8, K=2, F=256, T=4, gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K",
+    "tiny": dict(name="tiny", H=256, E=8, K=2, F=256, T=4, gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K",
             seed=0, bias_std=None),
-    2: dict(name="qwen3moe-30b-a3b layer decode T=1", H=2048, E=128, K=8, F=768, T=1,
+    "decode": dict(name="qwen3moe-30b-a3b layer decode T=1", H=2048, E=128, K=8, F=768, T=1,
             gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K", seed=1, bias_std=None),
-    3: dict(name="qwen3moe-30b-a3b layer decode T=8, Q4_K down", H=2048, E=128, K=8, F=768, T=8,
+    "batch8": dict(name="qwen3moe-30b-a3b layer decode T=8, Q4_K down", H=2048, E=128, K=8, F=768, T=8,
             gate_t="Q4_K", up_t="Q4_K", down_t="Q4_K", seed=2, bias_std=None),
-    4: dict(name="qwen3moe-30b-a3b layer prefill T=512, biased router", H=2048, E=128, K=8, F=768,
+    "prefill": dict(name="qwen3moe-30b-a3b layer prefill T=512, biased router", H=2048, E=128, K=8, F=768,
             T=512, gate_t="Q4_K", up_t="Q4_K", down_t="Q6_K", seed=3, bias_std=1.5),
 }
 

@@ -48,7 +48,7 @@ def _case(q, cfg_id, T=None, **over):
     return inp, got
 
 
-@pytest.mark.parametrize("cfg_id", [1, 2, 3])
+@pytest.mark.parametrize("cfg_id", ["tiny", "decode", "batch8"])
 def test_decode_configs_match_oracle(q, cfg_id):
     inp, got = _case(q, cfg_id)
     err, ties, gap = G.check(inp, got, TOL_FP32)
@@ -58,7 +58,7 @@ def test_decode_configs_match_oracle(q, cfg_id):
 def test_decode_sizes_take_the_fused_kernel(q):
     """Decode-size layers (T = 1 and T = 8 at the qwen3moe shape, both down
     qtypes) run as the single fused kernel; the T = 512 prefill does not."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     ctx = G.make_ctx(q, inp, max_tokens=512)
     try:
         for T in (1, 2, 4, 8):
@@ -74,7 +74,7 @@ def test_decode_sizes_take_the_fused_kernel(q):
 
 
 def test_prefill_config_matches_oracle(q):
-    inp, got = _case(q, 4)
+    inp, got = _case(q, "prefill")
     err, ties, gap = G.check(inp, got, TOL_BF16)
     counts = np.bincount(got["ids"].reshape(-1), minlength=inp["E"])
     assert counts.max() > 100 and (counts == 0).any()   # the bias skews routing
@@ -83,7 +83,7 @@ def test_prefill_config_matches_oracle(q):
 
 @pytest.mark.parametrize("T", [2, 3, 7, 9, 33, 300])
 def test_ragged_token_counts(q, T):
-    inp, got = _case(q, 3, T=T)
+    inp, got = _case(q, "batch8", T=T)
     G.check(inp, got, tol_for(T))
 
 
@@ -91,26 +91,26 @@ def test_ragged_token_counts(q, T):
 def test_tensor_core_path_tiny_shapes(q, T, down_t):
     """n_tokens > 8 on the small geometry (one superblock per row): token tiles
     of 64/128/256 rows, ragged expert segments, both down formats."""
-    inp, got = _case(q, 1, T=T, down_t=down_t)
+    inp, got = _case(q, "tiny", T=T, down_t=down_t)
     G.check(inp, got, TOL_BF16)
 
 
 @pytest.mark.parametrize("gate_t,down_t", [("Q6_K", "Q4_K"), ("Q4_K", "Q4_K"), ("Q6_K", "Q6_K")])
 def test_quant_type_combinations_tiny(q, gate_t, down_t):
-    inp, got = _case(q, 1, gate_t=gate_t, up_t=gate_t, down_t=down_t)
+    inp, got = _case(q, "tiny", gate_t=gate_t, up_t=gate_t, down_t=down_t)
     G.check(inp, got, TOL_FP32)
 
 
 def test_top1_and_dense_topk(q):
     for K in (1, 8):
-        inp, got = _case(q, 1, K=K)
+        inp, got = _case(q, "tiny", K=K)
         G.check(inp, got, TOL_FP32)
         if K == 8:
             assert all(sorted(r) == list(range(8)) for r in got["ids"].tolist())
 
 
 def test_equal_logits_pick_lowest_indices(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     inp["router"] = np.zeros_like(inp["router"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
@@ -124,7 +124,7 @@ def test_equal_logits_pick_lowest_indices(q):
 
 
 def test_no_renorm_option(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp, norm=0)
     try:
@@ -135,7 +135,7 @@ def test_no_renorm_option(q):
 
 
 def test_residual_and_alias(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
     try:
@@ -151,7 +151,7 @@ def test_residual_and_alias(q):
 
 
 def test_deterministic_and_batch_independent(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
     try:
@@ -167,7 +167,7 @@ def test_deterministic_and_batch_independent(q):
 
 
 def test_graph_capture_replays(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[2])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["decode"])
     d = G.upload(inp)
     out = torch.empty((1, inp["H"]), dtype=torch.float32, device=G.dev())
     s = torch.cuda.Stream()
@@ -189,7 +189,7 @@ def test_graph_capture_replays(q):
 
 
 def test_host_buffer_entry_point(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
     try:
@@ -204,7 +204,7 @@ def test_host_buffer_entry_point(q):
 
 
 def test_argument_errors_are_reported_before_launch(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
     out = torch.empty((inp["T"], inp["H"]), dtype=torch.float32, device=G.dev())
@@ -223,7 +223,7 @@ def test_argument_errors_are_reported_before_launch(q):
                 q.qmoe_forward(ctx, d["x"], d["router"], args["gate"], d["up"], d["down"],
                                args["gt"], 1, 2, args["n"], out)
             assert ei.value.status == status, (over, ei.value)
-        big = synth.moe_inputs(synth.MOE_CONFIGS[3], T=9)
+        big = synth.moe_inputs(synth.MOE_CONFIGS["batch8"], T=9)
         bd = G.upload(big)
         c2 = G.make_ctx(q, big)
         try:
@@ -240,7 +240,7 @@ def test_argument_errors_are_reported_before_launch(q):
 def test_guard_band_untouched(q):
     """Expert tensors placed between canary bytes: the canaries survive and the
     result is unchanged (no read or write outside the tensors' bytes matters)."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     d = G.upload(inp)
     pad = 4096
     bufs = {}
@@ -265,7 +265,7 @@ def test_nan_token_stays_local(q, T):
     """A token whose activations are NaN gets NaN logits; ranking on order keys
     still yields a valid expert selection, so no kernel waits on a value that
     never comes (the status stays OK), and every other token is unaffected."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3], T=T)
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"], T=T)
     bad = T // 2
     inp["x"] = inp["x"].copy()
     inp["x"][bad, 5] = np.nan

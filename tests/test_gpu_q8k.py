@@ -52,10 +52,10 @@ def _run(q, inp):
 
 
 CASES = [
-    (1, None, {}),                                                   # tiny, T=4
-    (1, 9, {"gate_t": "Q6_K", "up_t": "Q6_K", "down_t": "Q4_K"}),    # other formats, ragged T
-    (2, None, {}),                                                   # Qwen3-30B-A3B decode, T=1
-    (3, None, {}),                                                   # decode batch 8, Q4_K down
+    ("tiny", None, {}),                                                   # tiny, T=4
+    ("tiny", 9, {"gate_t": "Q6_K", "up_t": "Q6_K", "down_t": "Q4_K"}),    # other formats, ragged T
+    ("decode", None, {}),                                                   # Qwen3-30B-A3B decode, T=1
+    ("batch8", None, {}),                                                   # decode batch 8, Q4_K down
 ]
 
 
@@ -85,7 +85,7 @@ def test_q8k_layer_matches_oracle(q, cfg_id, T, over):
 
 
 def test_q8k_argument_errors_before_launch(q):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     d = G.upload(inp)
     ctx = G.make_ctx(q, inp)
     try:

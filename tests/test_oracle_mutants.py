@@ -14,7 +14,7 @@ from tests.compare import TOL_FP32, TOL_W, ids_match, rel_err, tie_bound_f32
 
 @pytest.fixture(scope="module")
 def case(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     ref = oracle_lib.moe_forward(inp)
     bound = tie_bound_f32(inp["router"], inp["x"])
     return inp, ref, bound

@@ -174,7 +174,7 @@ def test_q6k_scale_per_16_and_sign(oracle_lib):
 
 
 def test_numpy_and_c_dequant_agree_bit_for_bit(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     H, F = inp["H"], inp["F"]
     for e in range(inp["E"]):
         for name, qt, rows, cols in (("gate", "Q4_K", F, H), ("up", "Q4_K", F, H),
@@ -186,7 +186,7 @@ def test_numpy_and_c_dequant_agree_bit_for_bit(oracle_lib):
 
 def test_subnormal_scales_occur_and_decode(oracle_lib):
     # d = fp16(|N|*1e-3) is subnormal below 6.1e-5: the generator produces some
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     d = inp["gate"].reshape(-1, 144)[:, 0:2].copy().view(np.float16).reshape(-1)
     assert np.any((d != 0) & (np.abs(d.astype(np.float64)) < 2 ** -14))
 
@@ -198,7 +198,7 @@ def _route(oracle_lib, x, router, K, bias=None, norm=True):
 
 
 def test_router_logits_are_f32_rounded_matmul(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], 8)
     ref = inp["x"].astype(np.float64) @ inp["router"].astype(np.float64).T
     # exact double dot rounded to f32 may differ from numpy's BLAS order by 1 ulp at most
@@ -206,7 +206,7 @@ def test_router_logits_are_f32_rounded_matmul(oracle_lib):
 
 
 def test_router_weights_sum_to_one_and_order(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], 8)
     assert np.all(np.abs(w.sum(axis=1) - 1.0) < 1e-12)
     for t in range(ids.shape[0]):
@@ -220,14 +220,14 @@ def test_router_weights_sum_to_one_and_order(oracle_lib):
 
 
 def test_router_k1_gives_weight_one(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[2])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["decode"])
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], 1)
     assert w[0, 0] == 1.0
     assert ids[0, 0] == int(np.argmax(logits[0]))
 
 
 def test_router_k_equals_e_is_dense_softmax(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     E = inp["E"]
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], E)
     for t in range(inp["T"]):
@@ -245,7 +245,7 @@ def test_router_equal_logits_pick_lowest_indices(oracle_lib):
 
 
 def test_router_without_renorm_gives_softmax_probs(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], 8, norm=False)
     for t in range(inp["T"]):
         p = scipy.special.softmax(logits[t].astype(np.float64))
@@ -253,7 +253,7 @@ def test_router_without_renorm_gives_softmax_probs(oracle_lib):
 
 
 def test_router_bias_shifts_selection(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     bias = np.zeros(inp["E"], dtype=np.float32)
     bias[5] = 100.0
     logits, ids, w, probs = _route(oracle_lib, inp["x"], inp["router"], 2, bias=bias)
@@ -265,7 +265,7 @@ def test_router_bias_shifts_selection(oracle_lib):
 def test_ffn_brute_force_dense_config1(oracle_lib):
     """Dense evaluation of every expert for every token, combined through a
     top-k mask, equals the sparse oracle (config 1)."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     H, F, E, K, T = inp["H"], inp["F"], inp["E"], inp["K"], inp["T"]
     r = oracle_lib.moe_forward(inp)
     x = inp["x"].astype(np.float64)
@@ -289,7 +289,7 @@ def test_ffn_brute_force_dense_config1(oracle_lib):
 
 
 def test_ffn_expert_permutation_invariance(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     r = oracle_lib.moe_forward(inp)
     perm = np.random.default_rng(5).permutation(inp["E"])
     inv = np.argsort(perm)
@@ -302,7 +302,7 @@ def test_ffn_expert_permutation_invariance(oracle_lib):
 
 
 def test_ffn_batch_independence(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
     r = oracle_lib.moe_forward(inp)
     for t in (0, 5):
         one = dict(inp)
@@ -314,7 +314,7 @@ def test_ffn_batch_independence(oracle_lib):
 
 
 def test_ffn_zero_experts_returns_residual(oracle_lib):
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     p = dict(inp)
     for n in ("gate", "up", "down"):
         p[n] = np.zeros_like(inp[n])

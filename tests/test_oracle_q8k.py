@@ -132,7 +132,7 @@ def test_q4k_min_term_uses_the_code_sums(oracle_lib):
 def test_layer_is_the_composition_of_pinned_parts(oracle_lib):
     """moe_ffn_q8k on the small geometry equals its steps done here with the
     pinned quantiser and the independent numpy dequantiser."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     H, F, E, K = inp["H"], inp["F"], inp["E"], inp["K"]
     _, ids, w, _ = oracle_lib.route(inp["x"], inp["router"], K)
     got = oracle_lib.moe_ffn_q8k(inp["x"], ids, w, inp["gate"], inp["up"], inp["down"],
@@ -158,7 +158,7 @@ def test_layer_is_the_composition_of_pinned_parts(oracle_lib):
 def test_int8_activations_move_the_layer_output_a_little(oracle_lib):
     """Against the fp64-activation layer the Q8_K variant differs (it quantises)
     but stays close (8-bit codes per 256 values)."""
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[1])
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["tiny"])
     F, E, K = inp["F"], inp["E"], inp["K"]
     _, ids, w, _ = oracle_lib.route(inp["x"], inp["router"], K)
     args = (inp["x"], ids, w, inp["gate"], inp["up"], inp["down"], inp["gate_t"], inp["up_t"],

@@ -28,7 +28,7 @@ def q():
     return q
 
 
-@pytest.mark.parametrize("cfg_id", [2, 3, 1])
+@pytest.mark.parametrize("cfg_id", ["decode", "batch8", "tiny"])
 def test_noalloc_matches_context_forward_twice(q, cfg_id):
     from tests import gpu_util as G
     inp = synth.moe_inputs(synth.MOE_CONFIGS[cfg_id])
@@ -54,7 +54,7 @@ def test_noalloc_matches_context_forward_twice(q, cfg_id):
 
 def test_noalloc_refuses_beyond_capacity(q):
     from tests import gpu_util as G
-    inp = synth.moe_inputs(synth.MOE_CONFIGS[3], T=9)
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"], T=9)
     d = G.upload(inp)
     out = torch.empty((9, inp["H"]), dtype=torch.float32, device=G.dev())
     st = q.qmoe_forward_noalloc(d["x"], d["router"], d["gate"], d["up"], d["down"], 1, 1, 1,

@@ -11,8 +11,11 @@ tensor-core path) and ``step48`` (a full 48-layer decode step at context 4096).
 Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and a device synchronise, timed with CUDA events on the
 launching stream.  Every step reads a different device copy of the weights and
-the copies together touch more than 4x the L2 size, so weight bytes come from
-HBM.  ``value`` is summed over ranks (each rank runs its own replica).
+the copies together touch more than 4x the L2 size; right before the timed
+region a buffer of twice the L2 size is written, so weight bytes come from HBM
+in every timed step.  SM clocks are sampled over a window of back-to-back
+replays of the same graphs around the timed region.  ``value`` is summed over
+ranks (each rank runs its own replica).
 
 ``--impl reference`` times the CPU oracle (the reference arm) on the same
 workload and unit.
@@ -156,13 +159,13 @@ class ClockSampler:
     def stop(self, t0, t1):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [l for (ts, l) in self.lines if t0 - 0.15 <= ts <= t1 + 0.15] or \
+        rows = [l for (ts, l) in self.lines if t0 <= ts <= t1] or \
             [l for (_, l) in self.lines]
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -303,9 +306,17 @@ def dist_init():
     return ws, rank, local, pg
 
 
-def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index):
+def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index, clock_s=1.0):
     """Capture one graph over the rotation of `calls`, replay for exactly
-    `steps` steps after `warmup`; returns (ms, clocks)."""
+    `steps` steps after `warmup`; returns (ms, clocks).
+
+    L2: right before the timed region a buffer of twice the L2 size is written,
+    so no timed step finds weights that the warm-up left in L2; inside the
+    region consecutive steps read different weight copies.
+    Clocks: nvidia-smi samples every 100 ms, longer than a short timed region,
+    so the same graphs are also replayed back to back for about `clock_s`
+    seconds before and after it; the clock figures are the samples of that
+    window (the timed region included)."""
     R = len(calls)
     with torch.cuda.stream(stream):
         for i in range(min(3, R)):
@@ -327,6 +338,14 @@ def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index):
         for c in calls[:warmup % R]:
             c()
         stream.synchronize()
+        # one full replay, timed, sizes the clock window
+        t = time.perf_counter()
+        g_full.replay()
+        stream.synchronize()
+        per_full = max(time.perf_counter() - t, 1e-6)
+    n_clock = max(1, int(clock_s / 2 / per_full))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -336,19 +355,30 @@ def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index):
     e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     with torch.cuda.stream(stream):
+        for _ in range(n_clock):
+            g_full.replay()
+        flush.zero_()
+        if pg:
+            stream.synchronize()
+            pg.barrier()
         e0.record(stream)
         for _ in range(steps // R):
             g_full.replay()
         if g_rem is not None:
             g_rem.replay()
         e1.record(stream)
+        for _ in range(n_clock):
+            g_full.replay()
     stream.synchronize()
     t1 = time.time()
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     clocks = sampler.stop(t0, t1)
+    clocks["window_s"] = round(t1 - t0, 3)
     ms = max_over_ranks(torch, e0.elapsed_time(e1), pg, dev)
+    if clocks.get("sm_mhz"):
+        clocks["ms_per_step_x_mhz"] = ms / steps * clocks["sm_mhz"]
     return ms, clocks
 
 
@@ -444,7 +474,8 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
-                      f"per rotation vs L2 {l2 / 1e6:.0f} MB"},
+                      f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
+                      "written right before the timed region"},
         kernel=("whole Q8_K layer call (routing, quantise, gate/up, quantise, down, combine)"
                 if q8k else "moe_decode_fused (the whole layer is one kernel)" if T <= 8
                 else "whole layer call (routing, gather, grouped GEMMs, combine)"))
@@ -534,7 +565,8 @@ def bench_step48(args, torch, q, dev, stream, ws, pg, local):
         config={"workload": WORKLOADS["step48"]["desc"], "hidden": H, "n_experts": E,
                 "top_k": K, "ffn": F, "layers": L, "context": geo["ctx"], "tokens": 1,
                 "l2": f"one step touches {(ebytes + attn_bytes + kv_bytes + rbytes) / 1e9:.2f} GB "
-                      "vs a 136 MB L2"},
+                      "vs a 136 MB L2; a buffer of twice the L2 is written right before the "
+                      "timed region"},
         kernel="whole 48-layer decode step",
         tokens_per_s=args.steps * ws / secs,
         bytes_split={"experts": ebytes, "attention_weights": attn_bytes, "kv_cache": kv_bytes,

@@ -189,24 +189,32 @@ qmoe_status qmoe_decode_step(qmoe_ctx* ctx, const qmoe_layer_weights* layers, in
  * pool (a host framework's allocator, a plugin inside such a process), or
  * latency-critical loops that must not run a cudaMalloc, with its implicit
  * device synchronisation, after start-up.  It needs no context and allocates
- * nothing: its scratch (router logits, SwiGLU activations, grid-barrier
- * counters, status word) is one fixed device array inside the library, about
- * 288 KiB, which every GPU that loads the library holds until the process exits.
+ * nothing: its scratch (the tagged router logits, SwiGLU activations and down
+ * outputs that the fused decode kernel passes between its CTAs, the "x staged"
+ * marks, two control words and a status word) is one fixed device array inside
+ * the library of 2 MiB + 256 B, which every GPU that loads the library holds
+ * until the process exits.
  *  - Computes the same as qmoe_forward (hidden_out = hidden_in + MoE(hidden_in))
  *    with the same argument meaning, layout and alignment rules, on `stream`
  *    (a cudaStream_t; NULL = legacy default stream).
- *  - Served shapes: those of the fused single-kernel decode path -- n_tokens
- *    <= 8, gate/up Q4_K, hidden in {256, 2048}, ffn in {256, 768} -- and within
- *    the scratch capacity n_tokens*n_experts <= 8192, n_tokens*top_k*ffn <=
- *    65536.  Anything else returns QMOE_ERR_SHAPE and enqueues nothing.
+ *  - Served shapes: those of the fused single-kernel decode path (n_tokens
+ *    <= 8, gate/up Q4_K, hidden in {256, 2048}, ffn in {256, 768}; see
+ *    qmoe_fused_decode_available) whose tagged buffers fit the array:
+ *    8 * (n_tokens*n_experts + n_tokens*top_k*(ffn + hidden) + number of SMs),
+ *    each of the four parts rounded up to 256 B, at most 2 MiB.  At the
+ *    Qwen3-30B-A3B shape that is every n_tokens <= 8 at top_k 8.  Anything
+ *    else returns QMOE_ERR_SHAPE and enqueues nothing.
  *  - The first call on a device looks up the scratch's device address
  *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
  *    first call before any stream capture.
  *  - All calls share the one scratch array and it keeps the last call's
- *    contents; each call clears the counters it needs.  Calls whose execution
- *    overlaps on the GPU (other streams, other host threads) race on it and
- *    give wrong results: order them.
- *  - Returns launch / argument errors only; device-side status is not reported. */
+ *    contents.  Its control words carry over from call to call (they count
+ *    launches, so values left by an earlier call are never mistaken for this
+ *    call's); the status word is cleared at the start of every call.  Calls
+ *    whose execution overlaps on the GPU (other streams, other host threads)
+ *    race on it and give wrong results: order them.
+ *  - Returns launch / argument errors only; the device-side status of the call
+ *    (a bounded wait that ran out) is read with qmoe_noalloc_status. */
 qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float* router_w,
                                  const void* gate_exps, const void* up_exps,
                                  const void* down_exps, qmoe_qtype gate_t, qmoe_qtype up_t,
@@ -214,14 +222,35 @@ qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float* router_w,
                                  int ffn, int norm_topk_prob, int n_tokens, float* hidden_out,
                                  void* stream);
 
+/* Device-side status of the last qmoe_forward_noalloc call on the current
+ * device: synchronises `stream` (the stream that call used), reads the status
+ * word of the shared scratch and clears it.  QMOE_OK, or QMOE_ERR_TIMEOUT /
+ * QMOE_ERR_DEVICE_CHECK as for qmoe_get_status; QMOE_ERR_CUDA if the device
+ * was never set up by a call. */
+qmoe_status qmoe_noalloc_status(void* stream);
+
 /* Synchronise the stream and read the device status word (bounded-wait
  * timeouts, device index checks).  A non-OK status is sticky until read:
  * reading it clears it. */
 qmoe_status qmoe_get_status(qmoe_ctx* ctx);
 
 /* One-line description of the last error on this context ("" if none).  The
- * string is owned by the context and valid until the next call on it. */
+ * string is owned by the context and valid until the next call on it.  With
+ * ctx = NULL: why the last qmoe_create on this thread failed (for
+ * QMOE_ERR_NO_MEMORY the bytes the workspace needs and the bytes free). */
 const char* qmoe_last_error(qmoe_ctx* ctx);
+
+/* Test hooks of the failure paths (no counterpart on the pages).
+ * qmoe_debug_stall_next: the next fused decode launch on this context (a
+ *   qmoe_forward / qmoe_forward_ex of n_tokens <= 8 at a fused shape) waits for
+ *   router logits carrying a launch tag that no CTA writes, gives up after
+ *   wait_ns, records QMOE_ERR_TIMEOUT in the status word and exits without
+ *   computing (its outputs are left unwritten).  Later launches are normal:
+ *   this is how a test shows that a timed-out launch leaves the context usable.
+ * qmoe_debug_fail_alloc: the next n workspace allocations of qmoe_create, in
+ *   any thread, fail as if the device were out of memory (QMOE_ERR_NO_MEMORY). */
+qmoe_status qmoe_debug_stall_next(qmoe_ctx* ctx, uint64_t wait_ns);
+void qmoe_debug_fail_alloc(int n);
 
 /* Bytes of workspace a context with this config allocates (0 on bad config). */
 size_t qmoe_workspace_bytes(const qmoe_config* cfg);

@@ -42,7 +42,8 @@ LAUNCHES_PER_DECODE_STEP = 1
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
-            "qmoe_fused_decode_available", "qmoe_forward_q8k"]
+            "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_noalloc_status",
+            "qmoe_debug_stall_next", "qmoe_debug_fail_alloc"]
 
 
 class qmoe_config(C.Structure):
@@ -102,6 +103,12 @@ def _load():
     L.qmoe_expert_stride.restype = C.c_size_t
     L.qmoe_forward_noalloc.argtypes = [fp, fp, vp, vp, vp, i, i, i, i, i, i, i, i, i, fp, vp]
     L.qmoe_forward_noalloc.restype = i
+    L.qmoe_noalloc_status.argtypes = [vp]
+    L.qmoe_noalloc_status.restype = i
+    L.qmoe_debug_stall_next.argtypes = [vp, C.c_uint64]
+    L.qmoe_debug_stall_next.restype = i
+    L.qmoe_debug_fail_alloc.argtypes = [i]
+    L.qmoe_debug_fail_alloc.restype = None
     return L
 
 
@@ -129,7 +136,7 @@ def qmoe_create(cfg: qmoe_config):
     h = C.c_void_p()
     st = lib.qmoe_create(C.byref(cfg), C.byref(h))
     if st != QMOE_OK:
-        raise QmoeError(st, "qmoe_create failed (details on stderr)")
+        raise QmoeError(st, lib.qmoe_last_error(None).decode())
     return h
 
 
@@ -182,6 +189,19 @@ def qmoe_forward_noalloc(hidden_in, router_w, gate_exps, up_exps, down_exps, gat
                                     _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t, hidden,
                                     n_experts, top_k, ffn, norm_topk_prob, n_tokens,
                                     _ptr(hidden_out), stream or None)
+
+
+def qmoe_noalloc_status(stream=0) -> int:
+    """Device status of the last qmoe_forward_noalloc call on this device (clears it)."""
+    return lib.qmoe_noalloc_status(stream or None)
+
+
+def qmoe_debug_stall_next(ctx, wait_ns: int):
+    _check(ctx, lib.qmoe_debug_stall_next(ctx, wait_ns))
+
+
+def qmoe_debug_fail_alloc(n: int):
+    lib.qmoe_debug_fail_alloc(n)
 
 
 def qmoe_get_status(ctx) -> int:

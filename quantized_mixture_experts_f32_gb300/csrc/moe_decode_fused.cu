@@ -131,6 +131,8 @@ struct FusedParams {
     int* status;
     const float* norm_w;        // nullable: x is RMS-normalised per token and scaled first
     float eps;
+    unsigned long long wait_ns; // limit of every cross-CTA wait
+    int stall;                  // test hook: the logits wait expects a tag no CTA writes
     int T, H, E, K, F, norm, x_alias;
     int cf;          // f rows per gate/up chunk (divides F)
     SmemLayout L;
@@ -145,7 +147,8 @@ __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(st
 // they do (bounded).  Missing values read as 0; false if the wait timed out.
 template <int N>
 __device__ __forceinline__ bool load_tagged(const unsigned long long* base, int n, int first,
-                                            int stride, unsigned tag, float (&v)[N]) {
+                                            int stride, unsigned tag, float (&v)[N],
+                                            unsigned long long limit_ns = WAIT_LIMIT_NS) {
     uint32_t pend = 0u;                                   // bit z: value z still to come
 #pragma unroll
     for (int z = 0; z < N; ++z) {
@@ -156,7 +159,7 @@ __device__ __forceinline__ bool load_tagged(const unsigned long long* base, int 
     for (int round = 0; pend; ++round) {
         if (round == 1) t0 = globaltimer();
         if (round > 1) {
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
             __nanosleep(32);
         }
         unsigned long long w[N];
@@ -434,7 +437,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     {
         constexpr int LPT = 2;                                     // logits per thread (T*E <= 1024)
         float v[LPT];
-        if (!load_tagged<LPT>(p.lg, T * E, tid, NTHREADS, tag, v)) {
+        // (the test hook waits for a tag that no CTA writes, so the wait runs out)
+        const unsigned want = p.stall ? (tag ^ 0x80000000u) : tag;
+        if (!load_tagged<LPT>(p.lg, T * E, tid, NTHREADS, want, v, p.wait_ns)) {
             set_status(p.status, ST_TIMEOUT);
             misc[M_ABORT] = 1;
         }
@@ -1096,10 +1101,13 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
                                 float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
-                                const float* norm_w, float eps, cudaStream_t st) {
+                                const float* norm_w, float eps, cudaStream_t st,
+                                const FusedDebug* dbg) {
     FusedParams p;
     p.norm_w = norm_w;
     p.eps = eps;
+    p.wait_ns = dbg ? dbg->wait_ns : WAIT_LIMIT_NS;
+    p.stall = dbg ? dbg->stall : 0;
     p.x = x; p.res = res; p.bias = bias; p.router = router;
     p.gate = gate; p.up = up; p.down = down;
     p.out = out; p.ids_out = ids_out; p.w_out = w_out;

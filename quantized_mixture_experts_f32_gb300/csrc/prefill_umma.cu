@@ -64,13 +64,6 @@ constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one su
 constexpr int NBMAX = 8;                       // B stages, at most
 constexpr int B_BYTES_GU = 96 * 1024;
 constexpr int B_BYTES_DN = 64 * 1024;
-// CTAs of one (expert, token tile) that share its B rows can run as a cluster:
-// each then TMA-loads 1/C of every B stage and multicasts it to the others.
-// Measured on the T = 512 layer: C = 2 / 4 / 8 took 6% / 10% / 17% longer than
-// C = 1 (B bytes are not the limiter, and a cluster ties its CTAs' pipelines
-// together), so both kernels run unclustered.
-constexpr int GU_CLUSTER = 1;                  // of the F/64 gate/up tiles
-constexpr int DN_CLUSTER = 1;                  // of the H/128 down tiles
 
 struct PfBars {
     uint64_t qfull[NQ], qempty[NQ], afull[NA], aempty[NA], bfull[NBMAX], bempty[NBMAX], acc;
@@ -164,28 +157,15 @@ __device__ __forceinline__ void q6_quarter(uint4 ql, uint4 qh, int shl, int shh,
 }
 
 // B stages of a token tile of nb rows, NB deep, for k-blocks 0..NKB-1 (one
-// thread).  In a cluster of csize CTAs each loads rows [crank*nb/csize, ..+nb/csize)
-// of every stage (tensor map box of nb/csize rows) and multicasts them; a stage
-// is refilled once every CTA's MMA has released it (bempty counts csize
-// commits).  Before returning, the thread waits until the last NB stages have
-// been released everywhere, so no commit of a peer is still on its way to this
-// CTA's barriers when it exits.
+// thread): stage kb % NB is refilled once the MMA has released it.
 __device__ __forceinline__ void load_b_stages(PfBars* bars, uint8_t* bst, int BSTAGE, int NB, int NKB,
-                                              const CUtensorMap* tm, int nb, int row0, uint32_t csize,
-                                              uint32_t crank, uint16_t cmask) {
-    const int rows = nb / (int)csize;
+                                              const CUtensorMap* tm, int row0) {
     for (int kb = 0; kb < NKB; ++kb) {
         const int st = kb % NB;
         if (!mbar_wait(&bars->bempty[st], ((uint32_t)(kb / NB) & 1u) ^ 1u)) return;
         mbar_arrive_expect_tx(&bars->bfull[st], (uint32_t)BSTAGE);
-        if (csize > 1)
-            tma_load_2d_mc(bst + st * BSTAGE + (int)crank * rows * 128, tm, kb * KBLK, row0 + (int)crank * rows,
-                           &bars->bfull[st], cmask);
-        else
-            tma_load_2d(bst + st * BSTAGE, tm, kb * KBLK, row0, &bars->bfull[st]);
+        tma_load_2d(bst + st * BSTAGE, tm, kb * KBLK, row0, &bars->bfull[st]);
     }
-    for (int kb = NKB > NB ? NKB : NB; kb < NKB + NB; ++kb)
-        if (!mbar_wait(&bars->bempty[kb % NB], ((uint32_t)(kb / NB) & 1u) ^ 1u)) return;
 }
 
 struct GuParams {
@@ -216,8 +196,6 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_x256;
     const int e = p.used_expert[u];
     const int f0 = blockIdx.x * 64;
-    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
-    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
     const int H = p.H, F = p.F;
     const int NKB = H / KBLK, NSB = H / QK;
 
@@ -240,7 +218,7 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], csize);
+            mbar_init(&bars->bempty[i], 1);
         }
         mbar_init(&bars->acc, 1);
         fence_barrier_init();
@@ -248,7 +226,6 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     if (warp == 0) tmem_alloc(&bars->tmem, GU_TMEM);
     tc_fence_before();
     __syncthreads();
-    if (csize > 1) cluster_sync_all();     // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
 
@@ -267,7 +244,7 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         }
     } else if (warp == W_BLOAD) {
         // the expert's gathered x rows, NB k-blocks ahead of the MMA
-        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmx, nb, first + n0, csize, crank, cmask);
+        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmx, first + n0);
     } else if (warp == W_MMA) {
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f16(TILE_M, N);
@@ -284,10 +261,7 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
                     umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                              (kb | k) != 0);
                 umma_commit(&bars->aempty[sa]);
-                if (csize > 1)
-                    umma_commit_mc(&bars->bempty[sb], cmask);   // the stage is free in every CTA
-                else
-                    umma_commit(&bars->bempty[sb]);
+                umma_commit(&bars->bempty[sb]);
             }
             umma_commit(&bars->acc);
         }
@@ -374,7 +348,6 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     }
     tc_fence_before();
     __syncthreads();
-    if (csize > 1) cluster_sync_all();     // no peer still writes into this CTA
     if (warp == 0) tmem_dealloc(tmem, GU_TMEM);
 }
 
@@ -406,8 +379,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const CUtensorMap* tmb = nb == 64 ? &tm_a64 : nb == 128 ? &tm_a128 : &tm_a256;
     const int e = p.used_expert[u];
     const int h0 = blockIdx.x * TILE_M;
-    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
-    const uint16_t cmask = (uint16_t)((1u << csize) - 1u);
     const int H = p.H, F = p.F;
     const int NKB = F / KBLK;
     const int BB = p.down_t == 1 ? Q4K_BYTES : Q6K_BYTES;
@@ -430,7 +401,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], csize);
+            mbar_init(&bars->bempty[i], 1);
         }
         mbar_init(&bars->acc, 1);
         fence_barrier_init();
@@ -438,7 +409,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (warp == 0) tmem_alloc(&bars->tmem, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
-    if (csize > 1) cluster_sync_all();     // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
 
@@ -450,7 +420,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bulk_g2s(qbuf, src, qbytes, &bars->qfull[0]);
         }
     } else if (warp == W_BLOAD) {
-        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmb, nb, first + n0, csize, crank, cmask);
+        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmb, first + n0);
     } else if (warp == W_MMA) {
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_f16(TILE_M, N);
@@ -467,10 +437,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
                              (kb | k) != 0);
                 umma_commit(&bars->aempty[sa]);
-                if (csize > 1)
-                    umma_commit_mc(&bars->bempty[sb], cmask);   // the stage is free in every CTA
-                else
-                    umma_commit(&bars->bempty[sb]);
+                umma_commit(&bars->bempty[sb]);
             }
             umma_commit(&bars->acc);
         }
@@ -572,7 +539,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (csize > 1) cluster_sync_all();     // no peer still writes into this CTA
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
@@ -644,30 +610,6 @@ bool map_half(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// largest power of two <= cmax that divides the tile count along x
-int cluster_for(int tiles, int cmax) {
-    int c = cmax;
-    while (c > 1 && tiles % c) c >>= 1;
-    return c;
-}
-
-template <typename... Params, typename... Args>
-cudaError_t launch_clustered(void (*kernel)(Params...), dim3 grid, int cx, size_t smem, cudaStream_t st,
-                             Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(PF_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cx;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
 
 constexpr size_t GU_SMEM = 1024 + ((GU_NQ * QSTAGE_GU + 1023) & ~1023) + GU_NA * A_STAGE + B_BYTES_GU +
                            sizeof(PfBars) + 64;
@@ -700,13 +642,12 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
 
     CUtensorMap tg, tu, tx64, tx128, tx256, ta64, ta128, ta256;
     const uint64_t rbg = (uint64_t)(s.H / QK) * Q4K_BYTES;
-    const int cgu = cluster_for(s.F / 64, GU_CLUSTER), cdn = cluster_for(s.H / TILE_M, DN_CLUSTER);
-    // B maps: boxes of nb / C rows (each CTA of a cluster loads its share)
+    // B maps: boxes of 64 / 128 / 256 token rows
     if (!map_bytes(&tg, gate, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_bytes(&tu, up, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
-        !map_half(&tx64, xp, s.H, P, 64 / cgu) || !map_half(&tx128, xp, s.H, P, 128 / cgu) ||
-        !map_half(&tx256, xp, s.H, P, 256 / cgu) || !map_half(&ta64, actp, s.F, P, 64 / cdn) ||
-        !map_half(&ta128, actp, s.F, P, 128 / cdn) || !map_half(&ta256, actp, s.F, P, 256 / cdn))
+        !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
+        !map_half(&tx256, xp, s.H, P, 256) || !map_half(&ta64, actp, s.F, P, 64) ||
+        !map_half(&ta128, actp, s.F, P, 128) || !map_half(&ta256, actp, s.F, P, 256))
         return cudaErrorInvalidValue;
 
     static bool attr_set = false;
@@ -718,12 +659,14 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         attr_set = true;
     }
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles_gu};
-    e = launch_clustered(prefill_gateup, dim3(s.F / 64, max_used * ntiles_gu), cgu, GU_SMEM, st, tg, tu, tx64,
-                         tx128, tx256, gp);
+    prefill_gateup<<<dim3(s.F / 64, max_used * ntiles_gu), PF_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128,
+                                                                                     tx256, gp);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, ntiles, down_t};
-    e = launch_clustered(prefill_down, dim3(s.H / TILE_M, max_used * ntiles), cdn, dn_smem(s.F, down_t), st,
-                         ta64, ta128, ta256, dp);
+    prefill_down<<<dim3(s.H / TILE_M, max_used * ntiles), PF_THREADS, dn_smem(s.F, down_t), st>>>(
+        ta64, ta128, ta256, dp);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g3((s.H + 255) / 256, s.T);
     combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);

@@ -40,9 +40,23 @@ struct qmoe_ctx {
     double* inv_freq; // [head_dim/2] RoPE frequencies
     float2* rope_cs;  // [head_dim/2] cos/sin at the current position
     int attn_splits;
+    unsigned long long stall_ns; // test hook: the next fused launch stalls for this long (0: off)
 };
 
 namespace {
+
+// message of the last failed qmoe_create on this thread (read via qmoe_last_error(NULL))
+thread_local char g_create_err[512] = "";
+// test hook: the next n workspace allocations of qmoe_create fail as if out of memory
+int g_fail_alloc = 0;
+
+void create_fail(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_create_err, sizeof(g_create_err), fmt, ap);
+    va_end(ap);
+    fprintf(stderr, "qmoe_create: %s\n", g_create_err);
+}
 
 constexpr int DECODE_ALIAS_MAX = 8;
 constexpr int FUSED_GRID_MAX = 1024;     // largest grid of the fused decode kernel
@@ -159,10 +173,12 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
     qmoe::FusedPlan plan;
     if (qmoe::fused_decode_plan(s, gt, ut, dt, c->num_sms, &plan)) {
         // decode: the whole layer is one cooperative kernel
+        qmoe::FusedDebug dbg{c->stall_ns, 1};
         cudaError_t e = qmoe::launch_fused_decode(
             s, plan, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
             static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out,
-            w_out, c->fb, nullptr, 0.f, c->stream);
+            w_out, c->fb, nullptr, 0.f, c->stream, c->stall_ns ? &dbg : nullptr);
+        c->stall_ns = 0;
         if (e != cudaSuccess) return cuda_fail(c, e, "fused decode launch");
         c->err[0] = 0;
         return QMOE_OK;
@@ -225,13 +241,19 @@ size_t qmoe_expert_stride(qmoe_qtype qtype, int rows, int cols) {
 }
 
 qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
-    if (!out) return QMOE_ERR_INVALID_ARG;
+    g_create_err[0] = 0;
+    if (!out) {
+        create_fail("out is NULL");
+        return QMOE_ERR_INVALID_ARG;
+    }
     *out = nullptr;
     qmoe_ctx* c = new (std::nothrow) qmoe_ctx();
-    if (!c) return QMOE_ERR_NO_MEMORY;
+    if (!c) {
+        create_fail("host allocation of the context failed");
+        return QMOE_ERR_NO_MEMORY;
+    }
     if (!config_ok(cfg, c->err, sizeof(c->err))) {
-        // keep the message readable through a throwaway context is impossible; print it
-        fprintf(stderr, "qmoe_create: %s\n", c->err);
+        create_fail("%s", c->err);
         delete c;
         return QMOE_ERR_INVALID_ARG;
     }
@@ -239,7 +261,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->stream = static_cast<cudaStream_t>(cfg->stream);
     cudaError_t e = cudaGetDevice(&c->device);
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: cudaGetDevice: %s\n", cudaGetErrorString(e));
+        create_fail("cudaGetDevice: %s", cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_CUDA;
     }
@@ -247,19 +269,19 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     size_t free_b = 0, total_b = 0;
     e = cudaMemGetInfo(&free_b, &total_b);
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: cudaMemGetInfo: %s\n", cudaGetErrorString(e));
+        create_fail("cudaMemGetInfo: %s", cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_CUDA;
     }
     if (L.total > free_b) {
-        fprintf(stderr, "qmoe_create: workspace needs %zu bytes (%.1f MiB) but only %zu bytes (%.1f MiB) of %zu are free\n",
-                L.total, L.total / 1048576.0, free_b, free_b / 1048576.0, total_b);
+        create_fail("workspace needs %zu bytes (%.1f MiB) but only %zu bytes (%.1f MiB) of %zu are free",
+                    L.total, L.total / 1048576.0, free_b, free_b / 1048576.0, total_b);
         delete c;
         return QMOE_ERR_NO_MEMORY;
     }
     e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: cudaDeviceGetAttribute: %s\n", cudaGetErrorString(e));
+        create_fail("cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_CUDA;
     }
@@ -267,13 +289,20 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     if (e == cudaSuccess) e = qmoe::route_prepare();
     if (e == cudaSuccess) e = qmoe::decode_step_prepare();
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: kernel set-up: %s\n", cudaGetErrorString(e));
+        create_fail("kernel set-up: %s", cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_CUDA;
     }
-    e = cudaMalloc(&c->ws, L.total);
+    if (g_fail_alloc > 0) {
+        --g_fail_alloc;
+        e = cudaErrorMemoryAllocation;
+    } else {
+        e = cudaMalloc(&c->ws, L.total);
+    }
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: cudaMalloc(%zu): %s\n", L.total, cudaGetErrorString(e));
+        cudaGetLastError();
+        create_fail("workspace allocation of %zu bytes (%.1f MiB) failed with %zu bytes (%.1f MiB) free: %s",
+                    L.total, L.total / 1048576.0, free_b, free_b / 1048576.0, cudaGetErrorString(e));
         delete c;
         return QMOE_ERR_NO_MEMORY;
     }
@@ -316,7 +345,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
-        fprintf(stderr, "qmoe_create: workspace clear: %s\n", cudaGetErrorString(e));
+        create_fail("workspace clear: %s", cudaGetErrorString(e));
         cudaFree(c->ws);
         delete c;
         return QMOE_ERR_CUDA;
@@ -329,7 +358,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
             f[j] = pow((double)c->cfg.rope_base, -2.0 * (double)j / (double)c->cfg.head_dim);
         e = cudaMemcpy(c->inv_freq, f, sizeof(double) * half, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) {
-            fprintf(stderr, "qmoe_create: RoPE table upload: %s\n", cudaGetErrorString(e));
+            create_fail("RoPE table upload: %s", cudaGetErrorString(e));
             cudaFree(c->ws);
             delete c;
             return QMOE_ERR_CUDA;
@@ -529,6 +558,14 @@ qmoe_status qmoe_get_status(qmoe_ctx* c) {
     return QMOE_OK;
 }
 
-const char* qmoe_last_error(qmoe_ctx* c) { return c ? c->err : "null context"; }
+const char* qmoe_last_error(qmoe_ctx* c) { return c ? c->err : g_create_err; }
+
+qmoe_status qmoe_debug_stall_next(qmoe_ctx* c, uint64_t wait_ns) {
+    if (!c || wait_ns == 0) return QMOE_ERR_INVALID_ARG;
+    c->stall_ns = wait_ns;
+    return QMOE_OK;
+}
+
+void qmoe_debug_fail_alloc(int n) { g_fail_alloc = n > 0 ? n : 0; }
 
 }  // extern "C"

@@ -109,11 +109,20 @@ FusedBufs fused_bufs_carve(unsigned char* base, int T, int H, int E, int K, int 
 bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int num_sms,
                        FusedPlan* plan);
 
+// Test hook of the bounded waits: a launch with stall = 1 waits for router
+// logits carrying a tag that no CTA writes, for wait_ns, then records
+// QMOE_ERR_TIMEOUT and exits without computing (null: the normal 200 ms limit).
+struct FusedDebug {
+    unsigned long long wait_ns;
+    int stall;
+};
+
 cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const float* x,
                                 const float* res, const float* bias, const float* router,
                                 const uint8_t* gate, const uint8_t* up, const uint8_t* down,
                                 float* out, int32_t* ids_out, float* w_out, const FusedBufs& b,
-                                const float* norm_w, float eps, cudaStream_t st);
+                                const float* norm_w, float eps, cudaStream_t st,
+                                const FusedDebug* dbg = nullptr);
 
 int fused_threads();
 cudaError_t fused_prepare();

@@ -107,3 +107,22 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
         nullptr, nullptr, fb, nullptr, 0.f, st);
     return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
+
+extern "C" qmoe_status qmoe_noalloc_status(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NA_MAX_DEVICES)
+        return QMOE_ERR_CUDA;
+    unsigned char* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        if (!g_setup[dev].ready) return QMOE_ERR_CUDA;
+        scratch = g_setup[dev].scratch;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QMOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, scratch + 128, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return QMOE_ERR_CUDA;
+    if (v != 0 && cudaMemset(scratch + 128, 0, sizeof(int)) != cudaSuccess) return QMOE_ERR_CUDA;
+    return static_cast<qmoe_status>(v);
+}

@@ -1,7 +1,6 @@
 // umma.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a, inline
 // PTX: TMEM allocation, shared-memory matrix descriptors, the MMA itself, its
-// commit to an mbarrier, TMEM -> register loads, 2-D TMA tile loads (also
-// multicast to a cluster) and the cluster barrier.
+// commit to an mbarrier, TMEM -> register loads and 2-D TMA tile loads.
 //
 // Operand layout used everywhere: K-major, 64 half-precision values (128 bytes)
 // per row, 8-row groups of 1024 bytes, 128-byte swizzle (16-byte chunk index
@@ -94,46 +93,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
-}
-
-// the same tile delivered to every CTA of the cluster named in ctamask: it
-// lands at dst's shared-memory offset in each of them and completes bytes on
-// the barrier at bar's offset in each
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t ctamask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(ctamask)
-        : "memory");
-}
-
-// arrive once on the barrier at bar's offset in every CTA of ctamask when every
-// MMA issued so far by this thread has completed
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t ctamask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-            "r"(smem_u32(bar)),
-        "h"(ctamask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-// every thread of every CTA of the cluster: earlier shared-memory writes (and
-// barrier initialisation) become visible cluster-wide before anyone passes
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace qmoe

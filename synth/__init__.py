@@ -16,7 +16,8 @@ Recipe (every array is drawn with numpy ``Generator(PCG64(seed))``):
 * router weights ~ N(0, 0.02) as float32 [E][H]
 * optional per-expert router bias ~ N(0, 1.5) as float32 [E] (prefill workload)
 * every k-quant tensor: uniform random bytes for the whole superblock, then the
-  fp16 super-scales are overwritten with fp16(|N(0,1)| * 1e-3)
+  fp16 super-scales are overwritten with fp16(|N(0,1)| * 1e-3) (the spread is
+  a parameter, 1e-3 unless a case says otherwise)
   (Q4_K: d and dmin; Q6_K: d).  Q6_K's int8 sub-block scales stay uniform bytes.
 * activations ~ N(0, 1) as float32.
 * decode-step extras: norm weights 1 + 0.1 N(0,1); KV cache entries fp16(N(0,1)).
@@ -47,12 +48,12 @@ def matrix_bytes(qtype: str, rows: int, cols: int) -> int:
     return rows * row_bytes(qtype, cols)
 
 
-def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int) -> np.ndarray:
+def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int, d_std: float = 1e-3) -> np.ndarray:
     bb = BLOCK_BYTES[qtype]
     raw = np.frombuffer(rng.bytes(nblocks * bb), dtype=np.uint8).reshape(nblocks, bb).copy()
-    d = (np.abs(rng.standard_normal(nblocks)) * 1e-3).astype(np.float16)
+    d = (np.abs(rng.standard_normal(nblocks)) * d_std).astype(np.float16)
     if qtype == "Q4_K":
-        dmin = (np.abs(rng.standard_normal(nblocks)) * 1e-3).astype(np.float16)
+        dmin = (np.abs(rng.standard_normal(nblocks)) * d_std).astype(np.float16)
         raw[:, 0:2] = d.view(np.uint8).reshape(nblocks, 2)
         raw[:, 2:4] = dmin.view(np.uint8).reshape(nblocks, 2)
     else:
@@ -60,22 +61,25 @@ def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int) -> np.ndarr
     return raw
 
 
-def kquant_matrix(seed: int, tag: int, index: int, qtype: str, rows: int, cols: int) -> np.ndarray:
+def kquant_matrix(seed: int, tag: int, index: int, qtype: str, rows: int, cols: int,
+                  d_std: float = 1e-3) -> np.ndarray:
     """One quantised matrix [rows][cols] as uint8 [rows][row_bytes]."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
     nblk = rows * (cols // QK_K)
-    return _fill_kquant(rng, qtype, nblk).reshape(rows, row_bytes(qtype, cols))
+    return _fill_kquant(rng, qtype, nblk, d_std).reshape(rows, row_bytes(qtype, cols))
 
 
-def expert_slice(seed: int, which: str, e: int, qtype: str, rows: int, cols: int) -> np.ndarray:
-    return kquant_matrix(seed, _TAG[which], e, qtype, rows, cols)
+def expert_slice(seed: int, which: str, e: int, qtype: str, rows: int, cols: int,
+                 d_std: float = 1e-3) -> np.ndarray:
+    return kquant_matrix(seed, _TAG[which], e, qtype, rows, cols, d_std)
 
 
-def expert_tensor(seed: int, which: str, n_experts: int, qtype: str, rows: int, cols: int) -> np.ndarray:
+def expert_tensor(seed: int, which: str, n_experts: int, qtype: str, rows: int, cols: int,
+                  d_std: float = 1e-3) -> np.ndarray:
     """3-D expert tensor: expert e's slice starts at e * rows * row_bytes (contiguous)."""
     out = np.empty((n_experts, rows, row_bytes(qtype, cols)), dtype=np.uint8)
     for e in range(n_experts):
-        out[e] = expert_slice(seed, which, e, qtype, rows, cols)
+        out[e] = expert_slice(seed, which, e, qtype, rows, cols, d_std)
     return out
 
 
@@ -97,7 +101,9 @@ def moe_inputs(cfg: dict, T: int | None = None) -> dict:
     """All inputs of one MoE-FFN layer call, drawn in a fixed order.
 
     Order: router, bias (if any), input activations from the main stream; expert
-    tensors from their own per-expert streams.
+    tensors from their own per-expert streams.  ``cfg["d_std"]`` (default 1e-3)
+    is the spread of the fp16 super-scales; a smaller one gives small expert
+    outputs, for cases where the residual must not be negligible.
     """
     H, E, F = cfg["H"], cfg["E"], cfg["F"]
     T = cfg["T"] if T is None else T
@@ -108,9 +114,10 @@ def moe_inputs(cfg: dict, T: int | None = None) -> dict:
     if cfg.get("bias_std"):
         bias = rng.normal(0.0, cfg["bias_std"], size=E).astype(np.float32)
     x = rng.normal(0.0, 1.0, size=(T, H)).astype(np.float32)
-    gate = expert_tensor(seed, "gate", E, cfg["gate_t"], F, H)
-    up = expert_tensor(seed, "up", E, cfg["up_t"], F, H)
-    down = expert_tensor(seed, "down", E, cfg["down_t"], H, F)
+    ds = cfg.get("d_std", 1e-3)
+    gate = expert_tensor(seed, "gate", E, cfg["gate_t"], F, H, ds)
+    up = expert_tensor(seed, "up", E, cfg["up_t"], F, H, ds)
+    down = expert_tensor(seed, "down", E, cfg["down_t"], H, F, ds)
     return dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=bias, x=x,
                 gate=gate, up=up, down=down,
                 gate_t=cfg["gate_t"], up_t=cfg["up_t"], down_t=cfg["down_t"])

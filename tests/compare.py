@@ -2,13 +2,18 @@
 
 Tolerances:
 * expert ids: exact, as ordered lists (descending logit, ties to the lower
-  index).  The one allowed exception is a swap between two experts whose
-  oracle F32 logits differ by no more than ``tie_bound``: there both choices
-  are correct results of an F32 router, and the caller re-evaluates the oracle
-  with the kernel's selection before comparing values.
+  index).  A swap between two experts is accepted only where their oracle F32
+  logits differ by no more than ``tie_bound`` = 1e-5 * max|logit| of the token,
+  about ten times the real error of an F32 router sum at these sizes (~1e-6);
+  there both choices are correct results of an F32 router, and the caller
+  re-evaluates the oracle on the kernel's selection before comparing values and
+  reports the tokens it did that for.  At the fixed seeds of the five workloads
+  every 8th/9th gap is far above the bound, so the tests there require that no
+  token needed it.
 * routing weights: max |w - w_ref| <= 1e-5.
 * outputs: max |out - ref| / max |ref| over the whole tensor
-  (2e-3 for the fp32-accumulating decode path, 5e-3 for the bf16 prefill path).
+  (2e-3 for the fp32-accumulating decode path, 5e-3 for the half-precision
+  tensor-core prefill path).
 """
 from __future__ import annotations
 
@@ -26,21 +31,13 @@ def rel_err(out, ref) -> float:
     return float(np.abs(out - ref).max() / den) if den > 0 else float(np.abs(out - ref).max())
 
 
-def tie_bound_f32(router, x, bias=None) -> np.ndarray:
-    """Per-token bound on |fp32 logit - exact logit| for any summation order.
+TIE_REL = 1e-5
 
-    gamma_n * sum_h |Wr[e][h] x[h]| with gamma_n = n u / (1 - n u), u = 2^-24,
-    maximised over experts, plus one rounding of the result and of the bias add.
-    """
-    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
-    W = np.abs(np.asarray(router, dtype=np.float64))
-    n = W.shape[1] + 2
-    u = 2.0 ** -24
-    g = n * u / (1 - n * u)
-    mag = np.abs(x) @ W.T
-    if bias is not None:
-        mag = mag + np.abs(np.asarray(bias, dtype=np.float64))[None, :]
-    return 2.0 * g * mag.max(axis=1)
+
+def tie_bound(logits_ref) -> np.ndarray:
+    """Per-token near-tie allowance: 1e-5 * max|logit| of the token."""
+    lg = np.atleast_2d(np.asarray(logits_ref, dtype=np.float64))
+    return TIE_REL * np.abs(lg).max(axis=1)
 
 
 def ids_match(ids, ids_ref, logits_ref, bound) -> tuple[bool, list]:

@@ -57,6 +57,7 @@ def test_create_rejects_bad_config_before_touching_cuda(q):
     with pytest.raises(q.QmoeError) as ei:
         q.qmoe_create(q.make_config(2048, 128, 17, 768, 1))
     assert ei.value.status == 1
+    assert "top_k=17" in q.qmoe_last_error(None) and "top_k=17" in str(ei.value)
 
 
 def test_product_path_does_not_import_the_oracle():

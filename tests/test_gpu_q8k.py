@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from tests.compare import TOL_FP32, TOL_W, ids_match, rel_err, tie_bound_f32
+from tests.compare import TOL_FP32, TOL_W, ids_match, rel_err, tie_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -65,10 +65,12 @@ def test_q8k_layer_matches_oracle(q, cfg_id, T, over):
     inp = synth.moe_inputs(cfg, T=T)
     got, ids, w = _run(q, inp)
     logits, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"])
-    bound = tie_bound_f32(inp["router"], inp["x"], None)
-    ok, ties = ids_match(ids, rids, logits, bound)
+    ok, ties = ids_match(ids, rids, logits, tie_bound(logits))
     assert ok, f"expert ids differ beyond near-ties:\n{ids}\n{rids}"
+    if T is None:
+        assert ties == [], f"fixed-seed workload needed the near-tie allowance: {ties}"
     if ties:
+        print(f"near-tie tokens re-evaluated on the kernel's selection: {ties}")
         _, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"], force=ids)
     assert np.abs(w - rw).max() <= TOL_W
     args = (inp["x"], rids, rw, inp["gate"], inp["up"], inp["down"], inp["gate_t"], inp["up_t"],
@@ -101,3 +103,30 @@ def test_q8k_argument_errors_before_launch(q):
                                inp["T"], out)
     finally:
         q.qmoe_destroy(ctx)
+
+
+def test_q8k_residual_is_not_negligible(q):
+    """Small expert scales (d_std 7e-5) make the MoE part about as large as the
+    input, so the residual (hidden_in) and the MoE part both move the output far
+    beyond the bound: dropping either one is caught."""
+    inp = synth.moe_inputs(dict(synth.MOE_CONFIGS["decode"], d_std=7e-5))
+    got, ids, w = _run(q, inp)
+    _, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"])
+    assert np.array_equal(ids, rids)
+    args = (inp["x"], rids, rw, inp["gate"], inp["up"], inp["down"], inp["gate_t"], inp["up_t"],
+            inp["down_t"], inp["F"], inp["E"])
+    want = oracle.moe_ffn_q8k(*args)
+    x = inp["x"].astype(np.float64)
+    assert rel_err(want - x, want) > 10 * TOL_FP32 and rel_err(x, want) > 10 * TOL_FP32
+    err = rel_err(got, want)
+    assert err <= TOL_FP32, f"max relative error {err:.3e}"
+
+
+def test_q8k_zero_experts_return_the_input_bit_for_bit(q):
+    inp = synth.moe_inputs(synth.MOE_CONFIGS["batch8"])
+    for n in ("gate", "up", "down"):
+        inp[n] = np.zeros_like(inp[n])
+    got, ids, w = _run(q, inp)
+    _, rids, rw, _ = oracle.route(inp["x"], inp["router"], inp["K"])
+    assert np.array_equal(ids, rids)
+    assert np.array_equal(got.view(np.uint32), inp["x"].view(np.uint32))

@@ -1,6 +1,6 @@
-"""Pin of the oracle's prefill layer (SURVEY's next row: batched prefill of the
-whole layer, aprender issue "qwen3moe ... has NO working CUDA path", later gap
-list): the token-by-token composition equals a batched formulation written
+"""Pin of the oracle's prefill layer (the batched prefill of a whole decoder
+layer that the aprender issue "qwen3moe ... has NO working CUDA path" names in
+its later gap list, "Prefill is token-by-token"): the token-by-token composition equals a batched formulation written
 here from the definition -- all tokens' Q/K/V first, fp16 cache slots, causal
 masked softmax attention over the cache and the earlier tokens, O projection,
 FFN RMSNorm, routing and the MoE -- using the numpy dequantiser and library

@@ -65,9 +65,9 @@ WORKLOADS = {
 }
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
-PROFILE_FOR = {"decode": "moe_decode_fused_decode_T1.md", "batch8": None, "prefill": None,
+PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
                "step48": None, "prefill4096": None, "decode_q8k": None}
-FUSED_SOURCES = ["moe_decode_fused.cu", "kquant.cuh", "ptx_sync.cuh"]
+FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
 def parse():
@@ -477,7 +477,8 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
                       "written right before the timed region"},
         kernel=("whole Q8_K layer call (routing, quantise, gate/up, quantise, down, combine)"
-                if q8k else "moe_decode_fused (the whole layer is one kernel)" if T <= 8
+                if q8k else "moe_decode_t1 (the whole layer is one kernel)" if T == 1
+                else "moe_decode_fused (the whole layer is one kernel)" if T <= 8
                 else "whole layer call (routing, gather, grouped GEMMs, combine)"))
     if q8k:
         res["dtype"] = "int8 activations (Q8_K), f32 accumulate"

@@ -199,9 +199,9 @@ qmoe_status qmoe_decode_step(qmoe_ctx* ctx, const qmoe_layer_weights* layers, in
  *    (a cudaStream_t; NULL = legacy default stream).
  *  - Served shapes: those of the fused single-kernel decode path (n_tokens
  *    <= 8, gate/up Q4_K, hidden in {256, 2048}, ffn in {256, 768}; see
- *    qmoe_fused_decode_available) whose tagged buffers fit the array:
- *    8 * (n_tokens*n_experts + n_tokens*top_k*(ffn + hidden) + number of SMs),
- *    each of the four parts rounded up to 256 B, at most 2 MiB.  At the
+ *    qmoe_fused_decode_available) whose buffers fit the array:
+ *    8 * (n_tokens*n_experts + n_tokens*top_k*(ffn + hidden) + number of SMs)
+ *    + 4 * top_k*ffn, each of the five parts rounded up to 256 B, at most 2 MiB.  At the
  *    Qwen3-30B-A3B shape that is every n_tokens <= 8 at top_k 8.  Anything
  *    else returns QMOE_ERR_SHAPE and enqueues nothing.
  *  - The first call on a device looks up the scratch's device address

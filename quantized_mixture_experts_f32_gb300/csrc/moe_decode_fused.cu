@@ -1079,7 +1079,8 @@ bool fused_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int 
 size_t fused_bufs_bytes(int T, int H, int E, int K, int F, int grid) {
     const size_t P = (size_t)T * K;
     auto a = [](size_t v) { return (v + 255) / 256 * 256; };
-    return a(8 * (size_t)T * E) + a(8 * P * F) + a(8 * P * H) + a(8 * (size_t)grid);
+    return a(8 * (size_t)T * E) + a(8 * P * F) + a(8 * P * H) + a(8 * (size_t)grid) +
+           a(4 * (size_t)K * F);
 }
 
 FusedBufs fused_bufs_carve(unsigned char* base, int T, int H, int E, int K, int F, int grid,
@@ -1087,11 +1088,16 @@ FusedBufs fused_bufs_carve(unsigned char* base, int T, int H, int E, int K, int 
     const size_t P = (size_t)T * K;
     auto a = [](size_t v) { return (v + 255) / 256 * 256; };
     FusedBufs b;
-    b.lg = reinterpret_cast<unsigned long long*>(base);
-    b.act = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E));
-    b.y = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E) + a(8 * P * F));
-    b.xflag = reinterpret_cast<unsigned long long*>(base + a(8 * (size_t)T * E) + a(8 * P * F) +
-                                                    a(8 * P * H));
+    size_t o = 0;
+    b.lg = reinterpret_cast<unsigned long long*>(base + o);
+    o += a(8 * (size_t)T * E);
+    b.act = reinterpret_cast<unsigned long long*>(base + o);
+    o += a(8 * P * F);
+    b.y = reinterpret_cast<unsigned long long*>(base + o);
+    o += a(8 * P * H);
+    b.xflag = reinterpret_cast<unsigned long long*>(base + o);
+    o += a(8 * (size_t)grid);
+    b.plain_act = reinterpret_cast<float*>(base + o);
     b.ctl = ctl;
     b.status = status;
     return b;

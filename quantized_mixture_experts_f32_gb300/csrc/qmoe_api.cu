@@ -24,7 +24,7 @@ struct qmoe_ctx {
     float* hin;       // [T][H] staging for qmoe_forward_host
     float* hout;      // [T][H]
     int* status;      // device status word
-    unsigned* bar;    // fused kernel control words (exit counter, launch tag)
+    unsigned* bar;    // decode kernels' control words (exit counter, launch tag, arrival words)
     qmoe::FusedBufs fb; // tagged values passed between the fused kernel's CTAs
     __half* xp;       // [P][H] fp16 gathered x (prefill)
     __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
@@ -127,7 +127,7 @@ Layout layout(const qmoe_config* c) {
     L.hin = take(sizeof(float) * T * H);
     L.hout = take(sizeof(float) * T * H);
     L.status = take(sizeof(int) * 16);
-    L.bar = take(sizeof(unsigned) * 16);
+    L.bar = take(sizeof(unsigned) * 64);
     L.xp = take(sizeof(__half) * P * H);
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
@@ -170,10 +170,22 @@ qmoe_status run_moe(qmoe_ctx* c, const float* x, const float* res, const float* 
                     int gt, int ut, int dt, int T, float* out, int32_t* ids_out, float* w_out) {
     const qmoe_config& k = c->cfg;
     qmoe::MoeShape s{T, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    qmoe::FusedDebug dbg{c->stall_ns, 1};
+    qmoe::T1Plan p1;
+    if (qmoe::t1_decode_plan(s, gt, ut, dt, c->num_sms, &p1)) {
+        // one token: the whole layer is one latency-oriented kernel
+        cudaError_t e = qmoe::launch_t1_decode(
+            s, p1, dt, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
+            static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out, w_out,
+            c->fb, nullptr, 0.f, c->stream, c->stall_ns ? &dbg : nullptr);
+        c->stall_ns = 0;
+        if (e != cudaSuccess) return cuda_fail(c, e, "batch-1 decode launch");
+        c->err[0] = 0;
+        return QMOE_OK;
+    }
     qmoe::FusedPlan plan;
     if (qmoe::fused_decode_plan(s, gt, ut, dt, c->num_sms, &plan)) {
         // decode: the whole layer is one cooperative kernel
-        qmoe::FusedDebug dbg{c->stall_ns, 1};
         cudaError_t e = qmoe::launch_fused_decode(
             s, plan, x, res, bias, router_w, static_cast<const uint8_t*>(gate),
             static_cast<const uint8_t*>(up), static_cast<const uint8_t*>(down), out, ids_out,
@@ -231,6 +243,8 @@ int qmoe_fused_decode_available(const qmoe_ctx* c, int n_tokens, qmoe_qtype gate
     if (!valid_qtype(gate_t) || !valid_qtype(up_t) || !valid_qtype(down_t)) return 0;
     const qmoe_config& k = c->cfg;
     qmoe::MoeShape s{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    qmoe::T1Plan p1;
+    if (qmoe::t1_decode_plan(s, gate_t, up_t, down_t, c->num_sms, &p1)) return 1;
     qmoe::FusedPlan plan;
     return qmoe::fused_decode_plan(s, gate_t, up_t, down_t, c->num_sms, &plan) ? 1 : 0;
 }
@@ -286,6 +300,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
         return QMOE_ERR_CUDA;
     }
     e = qmoe::fused_prepare();
+    if (e == cudaSuccess) e = qmoe::t1_prepare();
     if (e == cudaSuccess) e = qmoe::route_prepare();
     if (e == cudaSuccess) e = qmoe::decode_step_prepare();
     if (e != cudaSuccess) {
@@ -515,8 +530,19 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
         // normalises x itself, other paths take a separate normalisation
         int32_t* ids_l = ids_out ? ids_out + (size_t)l * k.top_k : nullptr;
         qmoe::MoeShape ms{1, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+        qmoe::T1Plan p1;
         qmoe::FusedPlan plan;
-        if (qmoe::fused_decode_plan(ms, QMOE_Q4_K, QMOE_Q4_K, w.down_t, c->num_sms, &plan)) {
+        if (qmoe::t1_decode_plan(ms, QMOE_Q4_K, QMOE_Q4_K, w.down_t, c->num_sms, &p1)) {
+            e = qmoe::launch_t1_decode(
+                ms, p1, w.down_t, cur, cur, nullptr, w.router_w,
+                static_cast<const uint8_t*>(w.gate_exps), static_cast<const uint8_t*>(w.up_exps),
+                static_cast<const uint8_t*>(w.down_exps), other, ids_l, nullptr, c->fb,
+                w.ffn_norm, k.rms_eps, c->stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "batch-1 decode launch");
+            float* t = cur;
+            cur = other;
+            other = t;
+        } else if (qmoe::fused_decode_plan(ms, QMOE_Q4_K, QMOE_Q4_K, w.down_t, c->num_sms, &plan)) {
             e = qmoe::launch_fused_decode(
                 ms, plan, cur, cur, nullptr, w.router_w,
                 static_cast<const uint8_t*>(w.gate_exps), static_cast<const uint8_t*>(w.up_exps),

@@ -99,7 +99,9 @@ struct FusedBufs {
     unsigned long long* act;    // [T*K][F] silu(gate)*up
     unsigned long long* y;      // [T*K][H] down outputs
     unsigned long long* xflag;  // [grid] "x staged" marks
-    unsigned* ctl;              // [0] exit counter, [1] tag of the last launch
+    float* plain_act;           // [K][F] batch-1 kernel's SwiGLU output (plain fp32)
+    unsigned* ctl;              // [0] exit counter, [1] tag of the last launch,
+                                // [3] batch-1 kernel's act arrival count
     int* status;
 };
 size_t fused_bufs_bytes(int T, int H, int E, int K, int F, int grid);
@@ -126,6 +128,23 @@ cudaError_t launch_fused_decode(const MoeShape& s, const FusedPlan& plan, const 
 
 int fused_threads();
 cudaError_t fused_prepare();
+
+// Batch-1 decode kernel (moe_decode_t1.cu): one token, every weight copy of a
+// CTA issued at once, output rows owned by CTAs (no partial sums cross CTAs),
+// launched as a programmatic dependent of the previous kernel.  Uses the lg
+// and act buffers and the control words of FusedBufs.
+struct T1Plan {
+    int grid;
+    int smem;
+    const void* fn;
+};
+bool t1_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int num_sms, T1Plan* plan);
+cudaError_t launch_t1_decode(const MoeShape& s, const T1Plan& plan, int down_t, const float* x,
+                             const float* res, const float* bias, const float* router,
+                             const uint8_t* gate, const uint8_t* up, const uint8_t* down, float* out,
+                             int32_t* ids_out, float* w_out, const FusedBufs& b, const float* norm_w,
+                             float eps, cudaStream_t st, const FusedDebug* dbg = nullptr);
+cudaError_t t1_prepare();
 
 // Attention half of a decoder layer at decode time (batch 1).
 struct AttnShape {

@@ -76,7 +76,8 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
             void* ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_qmoe_noalloc_scratch) != cudaSuccess)
                 return QMOE_ERR_CUDA;
-            if (qmoe::fused_prepare() != cudaSuccess) return QMOE_ERR_CUDA;
+            if (qmoe::fused_prepare() != cudaSuccess || qmoe::t1_prepare() != cudaSuccess)
+                return QMOE_ERR_CUDA;
             int sms = 0;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return QMOE_ERR_CUDA;
@@ -88,23 +89,33 @@ extern "C" qmoe_status qmoe_forward_noalloc(const float* hidden_in, const float*
 
     qmoe::MoeShape s{n_tokens, hidden, n_experts, top_k, ffn, norm_topk_prob ? 1 : 0};
     qmoe::FusedPlan plan;
-    if (!qmoe::fused_decode_plan(s, gate_t, up_t, down_t, su->num_sms, &plan))
-        return QMOE_ERR_SHAPE;                 // only the fused decode shapes are served
+    qmoe::T1Plan p1;
+    const bool t1 = qmoe::t1_decode_plan(s, gate_t, up_t, down_t, su->num_sms, &p1);
+    if (!t1 && !qmoe::fused_decode_plan(s, gate_t, up_t, down_t, su->num_sms, &plan))
+        return QMOE_ERR_SHAPE;                 // only the single-kernel decode shapes are served
+    const int grid = t1 ? p1.grid : plan.grid;
     // capacity of the shared scratch
-    if (qmoe::fused_bufs_bytes(n_tokens, hidden, n_experts, top_k, ffn, plan.grid) > NA_TAGGED)
+    if (qmoe::fused_bufs_bytes(n_tokens, hidden, n_experts, top_k, ffn, grid) > NA_TAGGED)
         return QMOE_ERR_SHAPE;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned* ctl = reinterpret_cast<unsigned*>(su->scratch);
     int* status = reinterpret_cast<int*>(su->scratch + 128);
     const qmoe::FusedBufs fb = qmoe::fused_bufs_carve(su->scratch + NA_HEAD, n_tokens, hidden,
-                                                      n_experts, top_k, ffn, plan.grid, ctl, status);
+                                                      n_experts, top_k, ffn, grid, ctl, status);
     // the status word reports this call only
     if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return QMOE_ERR_CUDA;
-    cudaError_t e = qmoe::launch_fused_decode(
-        s, plan, hidden_in, nullptr, nullptr, router_w, static_cast<const uint8_t*>(gate_exps),
-        static_cast<const uint8_t*>(up_exps), static_cast<const uint8_t*>(down_exps), hidden_out,
-        nullptr, nullptr, fb, nullptr, 0.f, st);
+    cudaError_t e =
+        t1 ? qmoe::launch_t1_decode(s, p1, down_t, hidden_in, nullptr, nullptr, router_w,
+                                    static_cast<const uint8_t*>(gate_exps),
+                                    static_cast<const uint8_t*>(up_exps),
+                                    static_cast<const uint8_t*>(down_exps), hidden_out, nullptr,
+                                    nullptr, fb, nullptr, 0.f, st)
+           : qmoe::launch_fused_decode(s, plan, hidden_in, nullptr, nullptr, router_w,
+                                       static_cast<const uint8_t*>(gate_exps),
+                                       static_cast<const uint8_t*>(up_exps),
+                                       static_cast<const uint8_t*>(down_exps), hidden_out, nullptr,
+                                       nullptr, fb, nullptr, 0.f, st);
     return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
 }
 

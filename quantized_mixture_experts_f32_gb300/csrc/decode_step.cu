@@ -62,6 +62,34 @@ struct GemvArgs {
 // once then fall in 8 different bank groups instead of 2.
 __device__ __forceinline__ int xpad(int c) { return c + 4 * (c >> 6); }
 
+// Programmatic dependent launch: every kernel of the decode step is launched so
+// that it may start while the previous kernel on the stream drains.  Before
+// griddep_wait() a kernel touches only data that no kernel of the current step
+// before it writes (weights, KV slots of earlier positions); after it, the
+// previous kernel has completed and its writes are visible.  Each kernel lets
+// the next one launch only once it has passed its own wait, so a kernel that
+// starts early never overlaps the kernel two places before it.
+__device__ __forceinline__ void griddep_wait_launch() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int RPW, int NT>
 __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
     extern __shared__ float sx[];
@@ -97,6 +125,9 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
             }
         }
     }
+    // x is the previous kernel's output: wait for it only now, with the weight
+    // loads already in flight
+    griddep_wait_launch();
     // x (and the norm weights) in flight at once: cols <= 4096, 4 float4 per thread
     constexpr int XLD = 4096 / 4 / (GV_WARPS * 32);
     float4 xv[XLD], wv[XLD];
@@ -176,7 +207,11 @@ cudaError_t launch_gemv(const GemvArgs& g, int total_rows, cudaStream_t st) {
     const int rpw_max = nt <= 2 ? 4 : 2;
     const int rpw = rpw_max >= 4 && blocks(4) >= 148 ? 4 : blocks(2) >= 148 ? 2 : 1;
     dim3 grid(blocks(rpw)), thr(GV_WARPS * 32);
-#define QMOE_GEMV(R, N) q4k_gemv<R, N><<<grid, thr, smem, st>>>(g)
+#define QMOE_GEMV(R, N)                                                   \
+    do {                                                                  \
+        cudaError_t e_ = launch_pdl(q4k_gemv<R, N>, grid, thr, smem, st, g); \
+        if (e_ != cudaSuccess) return e_;                                 \
+    } while (0)
     if (nt == 1) {
         if (rpw == 4) QMOE_GEMV(4, 1); else if (rpw == 2) QMOE_GEMV(2, 1); else QMOE_GEMV(1, 1);
     } else if (nt == 2) {
@@ -202,6 +237,7 @@ constexpr int ATT_DPL = 8;            // head dims per lane in the norm/RoPE pas
 __global__ void rope_table(const double* __restrict__ inv_freq, int half, int pos,
                            float2* __restrict__ cs) {
     constexpr double TWO_PI = 6.283185307179586476925286766559;
+    griddep_wait_launch();
     for (int j = threadIdx.x; j < half; j += blockDim.x) {
         const double th = (double)pos * inv_freq[j];
         const double red = fma(-rint(th * (1.0 / TWO_PI)), TWO_PI, th);
@@ -297,6 +333,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
             }
         }
     }
+    // q, k and v are the previous kernel's output (the tile above holds only
+    // slots of earlier positions, and the slot at pos is overwritten below)
+    griddep_wait_launch();
     // q heads of this kv head: RMSNorm + RoPE (warp per head)
     for (int g = warp; g < group; g += nw) {
         float o[ATT_DPL];
@@ -410,6 +449,7 @@ __global__ void __launch_bounds__(MRG_THREADS) attn_merge(const float* __restric
     extern __shared__ float wsh[];                     // nvalid weights, then slice sums
     __shared__ float tot_s[2];
     const int h = blockIdx.x, tid = threadIdx.x;
+    griddep_wait_launch();
     const float* ph = part + (size_t)h * nsplit * (hd + 2);
     float* acc_s = wsh + nvalid;
     if (tid < 32) {
@@ -475,14 +515,17 @@ cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const
     const int group = a.nq / a.nkv;
     dim3 ga(a.nkv, nvalid);
     const int hpt = (group * ATT_CHUNK + ATT_THREADS - 1) / ATT_THREADS;
-#define QMOE_ATT(N)                                                                        \
-    attn_partial<N><<<ga, ATT_THREADS, attn_smem(group, a.hd), st>>>(                      \
-        q, kv, kv + kvd, L.q_norm, L.k_norm, a.eps, a.rope_cs, L.k_cache, L.v_cache, a.pos, \
-        a.hd, a.nq, a.nkv, a.max_ctx, nsplit, part)
+#define QMOE_ATT(N)                                                                          \
+    e = launch_pdl(attn_partial<N>, ga, dim3(ATT_THREADS), attn_smem(group, a.hd), st, q,          \
+                   (const float*)kv, (const float*)(kv + kvd), L.q_norm, L.k_norm, a.eps,          \
+                   a.rope_cs, L.k_cache, L.v_cache, a.pos, a.hd, a.nq, a.nkv, a.max_ctx, nsplit,   \
+                   part)
     if (hpt <= 1) QMOE_ATT(1); else if (hpt <= 2) QMOE_ATT(2); else if (hpt <= 4) QMOE_ATT(4); else QMOE_ATT(8);
 #undef QMOE_ATT
-    attn_merge<<<a.nq, MRG_THREADS, sizeof(float) * (nvalid + MRG_THREADS), st>>>(
-        part, nsplit, nvalid, a.hd, att);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(attn_merge, dim3(a.nq), dim3(MRG_THREADS), sizeof(float) * (nvalid + MRG_THREADS), st,
+                   (const float*)part, nsplit, nvalid, a.hd, att);
+    if (e != cudaSuccess) return e;
     // B7: h_out = h + Wo att
     GemvArgs go{};
     go.seg[0] = GemvSeg{L.wo, h_out, h, a.H};
@@ -515,8 +558,7 @@ cudaError_t decode_step_prepare() {
 
 cudaError_t launch_rope_table(const double* inv_freq, int hd, int pos, float2* cs,
                               cudaStream_t st) {
-    rope_table<<<1, 128, 0, st>>>(inv_freq, hd / 2, pos, cs);
-    return cudaGetLastError();
+    return launch_pdl(rope_table, dim3(1), dim3(128), 0, st, inv_freq, hd / 2, pos, cs);
 }
 
 bool attention_supported(int nq, int nkv, int hd) {

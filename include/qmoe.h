@@ -183,6 +183,31 @@ typedef struct {
 qmoe_status qmoe_decode_step(qmoe_ctx* ctx, const qmoe_layer_weights* layers, int n_layers,
                              int pos, float* hidden, int32_t* ids_out);
 
+/* Batched prefill: n_tokens tokens at positions pos0 .. pos0+n_tokens-1 through
+ * n_layers qwen3moe decoder layers, in place on hidden (F32 [n_tokens][H],
+ * device, 16-byte aligned).  Per layer it computes, for every token t, what
+ * qmoe_decode_step computes for one token at position pos0 + t, with causal
+ * attention: token t attends to the cache positions 0 .. pos0-1 as stored and
+ * to the batch's tokens 0 .. t.  Within a layer a token's K and V depend only
+ * on its own input, so this equals n_tokens decode steps in order (the
+ * token-by-token prefill of the aprender issue "qwen3moe ... has NO working
+ * CUDA path", later gap list, "Prefill is token-by-token", which names the
+ * batched form as the fix).  Differences from the decode step: the Q/K/V and O
+ * projections run as tensor-core GEMMs on fp16 rows of the normalised input and
+ * of the attention output (fp32 accumulation), and for n_tokens > 8 the MoE is
+ * the tensor-core grouped-GEMM path of qmoe_forward_ex (fp16 operands).
+ *  layers   : n_layers qmoe_layer_weights, as for qmoe_decode_step; the cache
+ *             slots pos0 .. pos0+n_tokens-1 of every layer are written (fp16),
+ *             the other slots are only read.
+ *  ids_out  : nullable, int32 [n_layers][n_tokens][k] selected experts.
+ * Requires the attention geometry in the config with at most 8 q heads per kv
+ * head and n_heads*head_dim, n_kv_heads*head_dim multiples of 128; otherwise
+ * QMOE_ERR_SHAPE.  1 <= n_tokens <= max_tokens, 0 <= pos0, pos0 + n_tokens <=
+ * max_ctx (else QMOE_ERR_SHAPE).  The context holds a scratch of
+ * about 56 KiB per max_tokens token at the Qwen3-30B-A3B shape for this call. */
+qmoe_status qmoe_prefill(qmoe_ctx* ctx, const qmoe_layer_weights* layers, int n_layers,
+                         int n_tokens, int pos0, float* hidden, int32_t* ids_out);
+
 /* Allocation-free variant of qmoe_forward for decode-sized calls.  The pages
  * have no counterpart to this entry point; it exists for callers that cannot
  * allocate device memory: processes whose device memory is owned by their own

@@ -318,13 +318,13 @@ def prefill_layer(geo: dict, small: dict, experts: dict, hs, pos0: int, force=No
     of the aprender issue "qwen3moe ... has NO working CUDA path", later gap
     list, which a batched prefill must reproduce).  hs: f64 [T][H].  force
     (optional): [T][K] expert ids.  Returns dict(h [T][H], ids [T][K], w [T][K],
-    k_cache, v_cache) with the caches' slots pos0.. pos0+T-1 written (copies)."""
+    router logits f32 [T][E], k_cache, v_cache) with the caches' slots pos0.. pos0+T-1 written (copies)."""
     hs = np.atleast_2d(_f64(hs))
     T = hs.shape[0]
     if pos0 < 0 or pos0 + T > geo["ctx"]:
         raise ValueError("prefill positions outside the context")
     cur = dict(small)
-    outs, ids, ws = [], [], []
+    outs, ids, ws, lgs = [], [], [], []
     for i in range(T):
         r = decode_layer(geo, cur, experts, hs[i], pos0 + i,
                          force=None if force is None else np.asarray(force)[i])
@@ -332,6 +332,7 @@ def prefill_layer(geo: dict, small: dict, experts: dict, hs, pos0: int, force=No
         outs.append(r["h"])
         ids.append(r["ids"])
         ws.append(r["w"])
-    return dict(h=np.stack(outs), ids=np.stack(ids), w=np.stack(ws), k_cache=cur["k_cache"],
-                v_cache=cur["v_cache"])
+        lgs.append(r["logits"])
+    return dict(h=np.stack(outs), ids=np.stack(ids), w=np.stack(ws), logits=np.stack(lgs),
+                k_cache=cur["k_cache"], v_cache=cur["v_cache"])
 

@@ -38,9 +38,13 @@ LAUNCHES_PER_Q8K_FORWARD = 7
 LAUNCHES_PER_DECODE_LAYER = 5
 # plus, once per qmoe_decode_step: the RoPE cos/sin table at the step's position
 LAUNCHES_PER_DECODE_STEP = 1
+# one decoder layer of qmoe_prefill up to the MoE input: RMSNorm, Q/K/V GEMMs,
+# Q/K norm + RoPE + KV append, attention, O GEMM, FFN RMSNorm; the MoE adds
+# LAUNCHES_PER_PREFILL_FORWARD (n_tokens > 8) or one fused kernel
+LAUNCHES_PER_PREFILL_LAYER_ATTN = 8
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
-            "qmoe_forward_host", "qmoe_decode_step", "qmoe_get_status", "qmoe_last_error",
+            "qmoe_forward_host", "qmoe_decode_step", "qmoe_prefill", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
             "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_noalloc_status",
             "qmoe_debug_stall_next", "qmoe_debug_fail_alloc"]
@@ -91,6 +95,8 @@ def _load():
     L.qmoe_forward_host.restype = i
     L.qmoe_decode_step.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, fp, ip]
     L.qmoe_decode_step.restype = i
+    L.qmoe_prefill.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, i, fp, ip]
+    L.qmoe_prefill.restype = i
     L.qmoe_get_status.argtypes = [vp]
     L.qmoe_get_status.restype = i
     L.qmoe_last_error.argtypes = [vp]
@@ -179,6 +185,10 @@ def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_ex
 
 def qmoe_decode_step(ctx, layers, n_layers, pos, hidden, ids_out=None):
     _check(ctx, lib.qmoe_decode_step(ctx, layers, n_layers, pos, _ptr(hidden), _ptr(ids_out)))
+
+
+def qmoe_prefill(ctx, layers, n_layers, n_tokens, pos0, hidden, ids_out=None):
+    _check(ctx, lib.qmoe_prefill(ctx, layers, n_layers, n_tokens, pos0, _ptr(hidden), _ptr(ids_out)))
 
 
 def qmoe_forward_noalloc(hidden_in, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,

@@ -174,9 +174,18 @@ struct GuParams {
     const int32_t* used_first;
     __half* act;          // [P][F] fp16, rows in pair-list order
     int H, F, ntiles;     // ntiles: token tiles per expert slot in grid.y
+    // plain mode (a dense Q4_K GEMM): y[t][yoff + r] = sum_k W[r][k] x[t][k]
+    // (+ res[t][yoff + r]) for the dense_T tokens of x, W = the tm_gate map
+    float* y;
+    const float* res;
+    int dense_T, ldy, yoff;
 };
 
-// grid (F/64, max_used * ntiles), PF_THREADS threads
+// MODE 0: grid (F/64, max_used * ntiles); A = 64 gate + 64 up rows of one
+// expert, epilogue silu(g)*u -> fp16 act.  MODE 1: grid (rows/128, ntiles);
+// A = 128 consecutive rows of one Q4_K matrix [rows][H] (H = its K), B = the
+// dense_T token rows of x, epilogue fp32 y (+ res).  PF_THREADS threads.
+template <int MODE>
 __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                    const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ CUtensorMap tm_x128,
@@ -186,16 +195,17 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
     // would turn every access into a generic one)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int u = blockIdx.y / p.ntiles, nt = blockIdx.y % p.ntiles;
-    if (u >= *p.n_used) return;
-    const int first = p.used_first[u], cnt = p.used_first[u + 1] - first;
+    if (MODE == 0 && u >= *p.n_used) return;
+    const int first = MODE == 0 ? p.used_first[u] : 0;
+    const int cnt = MODE == 0 ? p.used_first[u + 1] - first : p.dense_T;
     const int n0 = nt * GU_NMAX;
     if (n0 >= cnt) return;
     const int n = min(GU_NMAX, cnt - n0);
     const int N = (n + 15) & ~15;
     const int nb = box_rows(n);
     const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_x256;
-    const int e = p.used_expert[u];
-    const int f0 = blockIdx.x * 64;
+    const int e = MODE == 0 ? p.used_expert[u] : 0;
+    const int f0 = blockIdx.x * (MODE == 0 ? 64 : 128);
     const int H = p.H, F = p.F;
     const int NKB = H / KBLK, NSB = H / QK;
 
@@ -239,7 +249,10 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
                 uint8_t* dst = qst + st * QSTAGE_GU;
                 mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
                 tma_load_2d(dst, &tm_gate, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
-                tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                if (MODE == 0)
+                    tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                else
+                    tma_load_2d(dst + 64 * Q4K_BYTES, &tm_gate, sb * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
             }
         }
     } else if (warp == W_BLOAD) {
@@ -279,7 +292,10 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         for (int r = 0; r < RPT; ++r) {
             const int row = 8 * warp + (lane & 7) + 8 * NDQ * r;
             const int grp = row >> 5, w32 = row & 31;
-            src[r] = (w32 < 16 ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16)) * Q4K_BYTES;
+            // gate/up: A rows 32 g .. 32 g + 15 are gate rows 16 g .., the next 16
+            // the matching up rows (so TMEM lanes l and l + 16 pair up in the
+            // epilogue); plain: A row = stage row
+            src[r] = (MODE == 1 ? row : w32 < 16 ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16)) * Q4K_BYTES;
             rowb[r] = row * 128;
         }
         const int o_lo = (qq ^ (lane & 7)) << 4, o_hi = ((qq + 4) ^ (lane & 7)) << 4;   // row % 8 == lane % 8
@@ -330,18 +346,34 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
         mbar_wait(&bars->acc, 0);
         tc_fence_after();
         const int lq = warp & 3, ch = warp >> 2, cpw = 1024 / NDQ;   // columns per warp
-        const int f = f0 + 16 * lq + (lane & 15);
-        for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
+        if (MODE == 0) {
+            const int f = f0 + 16 * lq + (lane & 15);
+            for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float up = __shfl_down_sync(0xffffffffu, v[j], 16);
-                const int col = c0 + j;
-                if (lane < 16 && col < n) {
-                    const float g = v[j];
-                    p.act[(size_t)(first + n0 + col) * F + f] =
-                        __float2half_rn(__fdividef(g, 1.f + __expf(-g)) * up);
+                for (int j = 0; j < 16; ++j) {
+                    const float up = __shfl_down_sync(0xffffffffu, v[j], 16);
+                    const int col = c0 + j;
+                    if (lane < 16 && col < n) {
+                        const float g = v[j];
+                        p.act[(size_t)(first + n0 + col) * F + f] =
+                            __float2half_rn(__fdividef(g, 1.f + __expf(-g)) * up);
+                    }
+                }
+            }
+        } else {
+            const int row = p.yoff + f0 + 32 * lq + lane;
+            for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c0 + j;
+                    if (col < n) {
+                        const size_t o = (size_t)(n0 + col) * p.ldy + row;
+                        p.y[o] = v[j] + (p.res ? p.res[o] : 0.f);
+                    }
                 }
             }
         }
@@ -652,14 +684,16 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
 
     static bool attr_set = false;
     if (!attr_set) {
-        e = cudaFuncSetAttribute(prefill_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(prefill_gateup<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_gateup<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(prefill_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles_gu};
-    prefill_gateup<<<dim3(s.F / 64, max_used * ntiles_gu), PF_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128,
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles_gu, nullptr, nullptr, 0, 0, 0};
+    prefill_gateup<0><<<dim3(s.F / 64, max_used * ntiles_gu), PF_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128,
                                                                                      tx256, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -670,6 +704,27 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     if (e != cudaSuccess) return e;
     dim3 g3((s.H + 255) / 256, s.T);
     combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
+                                  int ldy, int yoff, const float* res, cudaStream_t st) {
+    if (rows % TILE_M || K % QK || T < 1) return cudaErrorInvalidValue;
+    CUtensorMap tw, tx64, tx128, tx256;
+    const uint64_t rb = (uint64_t)(K / QK) * Q4K_BYTES;
+    if (!map_bytes(&tw, W, rb, (uint64_t)rows, Q4K_BYTES, 64) || !map_half(&tx64, x, K, T, 64) ||
+        !map_half(&tx128, x, K, T, 128) || !map_half(&tx256, x, K, T, 256))
+        return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_gateup<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int ntiles = (T + GU_NMAX - 1) / GU_NMAX;
+    GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, ntiles, y, res, T, ldy, yoff};
+    prefill_gateup<1><<<dim3(rows / TILE_M, ntiles), PF_THREADS, GU_SMEM, st>>>(tw, tw, tx64, tx128, tx256, gp);
     return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@ struct qmoe_ctx {
     double* inv_freq; // [head_dim/2] RoPE frequencies
     float2* rope_cs;  // [head_dim/2] cos/sin at the current position
     int attn_splits;
+    void* pl_scratch; // batched prefill layer scratch (null: shape not served)
     unsigned long long stall_ns; // test hook: the next fused launch stalls for this long (0: off)
 };
 
@@ -84,8 +85,9 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
         status, bar, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
-        rope_cs, total;
+        rope_cs, pl, total;
     int attn_splits;
+    bool pl_ok;
 };
 
 bool config_ok(const qmoe_config* c, char* why, size_t n) {
@@ -146,6 +148,11 @@ Layout layout(const qmoe_config* c) {
     L.attn_part = take(sizeof(float) * (size_t)c->n_heads * L.attn_splits * (c->head_dim + 2) + 4);
     L.inv_freq = take(sizeof(double) * (c->head_dim > 0 ? c->head_dim / 2 : 1));
     L.rope_cs = take(sizeof(float2) * (c->head_dim > 0 ? c->head_dim / 2 : 1));
+    L.pl_ok = c->n_heads > 0 &&
+              qmoe::prefill_layer_supported(c->hidden, c->n_heads, c->n_kv_heads, c->head_dim);
+    L.pl = take(L.pl_ok ? qmoe::prefill_layer_scratch_bytes(c->max_tokens, c->hidden, c->n_heads,
+                                                            c->n_kv_heads, c->head_dim)
+                        : 0);
     L.total = off;
     return L;
 }
@@ -162,6 +169,24 @@ qmoe_status check_forward(qmoe_ctx* c, const float* in, const float* router_w, c
         return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "qtypes gate=%d up=%d down=%d (allowed: 1=Q4_K, 2=Q6_K)", gt, ut, dt);
     if (!aligned16(in) || !aligned16(router_w) || !aligned16(g) || !aligned16(u) || !aligned16(d) || !aligned16(out))
         return fail(c, QMOE_ERR_MISALIGNED, "every tensor base pointer must be 16-byte aligned");
+    return QMOE_OK;
+}
+
+qmoe_status check_layers(qmoe_ctx* c, const qmoe_layer_weights* layers, int n_layers) {
+    for (int l = 0; l < n_layers; ++l) {
+        const qmoe_layer_weights& w = layers[l];
+        if (!w.attn_norm || !w.wq || !w.wk || !w.wv || !w.wo || !w.q_norm || !w.k_norm ||
+            !w.ffn_norm || !w.router_w || !w.gate_exps || !w.up_exps || !w.down_exps ||
+            !w.k_cache || !w.v_cache)
+            return fail(c, QMOE_ERR_INVALID_ARG, "layer %d: null pointer", l);
+        if (!aligned16(w.wq) || !aligned16(w.wk) || !aligned16(w.wv) || !aligned16(w.wo) ||
+            !aligned16(w.router_w) || !aligned16(w.gate_exps) || !aligned16(w.up_exps) ||
+            !aligned16(w.down_exps) || !aligned16(w.k_cache) || !aligned16(w.v_cache) ||
+            !aligned16(w.attn_norm) || !aligned16(w.ffn_norm))
+            return fail(c, QMOE_ERR_MISALIGNED, "layer %d: a base pointer is not 16-byte aligned", l);
+        if (!valid_qtype(w.down_t))
+            return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "layer %d: down qtype %d", l, (int)w.down_t);
+    }
     return QMOE_OK;
 }
 
@@ -303,6 +328,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     if (e == cudaSuccess) e = qmoe::t1_prepare();
     if (e == cudaSuccess) e = qmoe::route_prepare();
     if (e == cudaSuccess) e = qmoe::decode_step_prepare();
+    if (e == cudaSuccess && L.pl_ok) e = qmoe::prefill_layer_prepare();
     if (e != cudaSuccess) {
         create_fail("kernel set-up: %s", cudaGetErrorString(e));
         delete c;
@@ -357,6 +383,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->attn_splits = L.attn_splits;
     c->inv_freq = reinterpret_cast<double*>(b + L.inv_freq);
     c->rope_cs = reinterpret_cast<float2*>(b + L.rope_cs);
+    c->pl_scratch = L.pl_ok ? b + L.pl : nullptr;
     e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) {
@@ -485,19 +512,9 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
     if (pos < 0 || pos >= k.max_ctx)
         return fail(c, QMOE_ERR_SHAPE, "pos=%d outside 0..max_ctx-1=%d", pos, k.max_ctx - 1);
     if (!aligned16(hidden)) return fail(c, QMOE_ERR_MISALIGNED, "hidden must be 16-byte aligned");
-    for (int l = 0; l < n_layers; ++l) {
-        const qmoe_layer_weights& w = layers[l];
-        if (!w.attn_norm || !w.wq || !w.wk || !w.wv || !w.wo || !w.q_norm || !w.k_norm ||
-            !w.ffn_norm || !w.router_w || !w.gate_exps || !w.up_exps || !w.down_exps ||
-            !w.k_cache || !w.v_cache)
-            return fail(c, QMOE_ERR_INVALID_ARG, "layer %d: null pointer", l);
-        if (!aligned16(w.wq) || !aligned16(w.wk) || !aligned16(w.wv) || !aligned16(w.wo) ||
-            !aligned16(w.router_w) || !aligned16(w.gate_exps) || !aligned16(w.up_exps) ||
-            !aligned16(w.down_exps) || !aligned16(w.k_cache) || !aligned16(w.v_cache) ||
-            !aligned16(w.attn_norm) || !aligned16(w.ffn_norm))
-            return fail(c, QMOE_ERR_MISALIGNED, "layer %d: a base pointer is not 16-byte aligned", l);
-        if (!valid_qtype(w.down_t))
-            return fail(c, QMOE_ERR_UNSUPPORTED_QTYPE, "layer %d: down qtype %d", l, (int)w.down_t);
+    {
+        qmoe_status ls = check_layers(c, layers, n_layers);
+        if (ls != QMOE_OK) return ls;
     }
     qmoe::AttnShape a{k.hidden, k.n_heads, k.n_kv_heads, k.head_dim, k.max_ctx, pos, k.rms_eps,
                       k.rope_base, c->inv_freq, c->rope_cs};
@@ -565,6 +582,52 @@ qmoe_status qmoe_decode_step(qmoe_ctx* c, const qmoe_layer_weights* layers, int 
         cudaError_t e = cudaMemcpyAsync(hidden, cur, sizeof(float) * k.hidden,
                                         cudaMemcpyDeviceToDevice, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "hidden copy");
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_prefill(qmoe_ctx* c, const qmoe_layer_weights* layers, int n_layers, int n_tokens,
+                         int pos0, float* hidden, int32_t* ids_out) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    const qmoe_config& k = c->cfg;
+    if (k.n_heads < 1 || k.max_ctx < 1)
+        return fail(c, QMOE_ERR_INVALID_ARG, "context was created without attention geometry");
+    if (!c->pl_scratch)
+        return fail(c, QMOE_ERR_SHAPE, "batched prefill does not serve n_heads=%d n_kv_heads=%d head_dim=%d "
+                    "(needs at most 8 q heads per kv head and 128-row multiples)", k.n_heads, k.n_kv_heads, k.head_dim);
+    if (!layers || n_layers < 1 || !hidden)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null layers / hidden or n_layers < 1");
+    if (n_tokens < 1 || n_tokens > k.max_tokens)
+        return fail(c, QMOE_ERR_SHAPE, "n_tokens=%d outside 1..max_tokens=%d", n_tokens, k.max_tokens);
+    if (pos0 < 0 || pos0 > k.max_ctx - n_tokens)
+        return fail(c, QMOE_ERR_SHAPE, "positions %d..%d outside 0..max_ctx-1=%d", pos0, pos0 + n_tokens - 1,
+                    k.max_ctx - 1);
+    if (!aligned16(hidden)) return fail(c, QMOE_ERR_MISALIGNED, "hidden must be 16-byte aligned");
+    {
+        qmoe_status ls = check_layers(c, layers, n_layers);
+        if (ls != QMOE_OK) return ls;
+    }
+    float* x2 = qmoe::prefill_layer_x2(c->pl_scratch, n_tokens, k.hidden, k.n_heads, k.n_kv_heads, k.head_dim);
+    for (int l = 0; l < n_layers; ++l) {
+        const qmoe_layer_weights& w = layers[l];
+        qmoe::PrefillLayerArgs a{n_tokens, k.hidden, k.n_heads, k.n_kv_heads, k.head_dim, k.max_ctx, pos0,
+                                 k.rms_eps, c->inv_freq, w.attn_norm,
+                                 static_cast<const uint8_t*>(w.wq), static_cast<const uint8_t*>(w.wk),
+                                 static_cast<const uint8_t*>(w.wv), static_cast<const uint8_t*>(w.wo),
+                                 w.q_norm, w.k_norm, w.ffn_norm,
+                                 static_cast<__half*>(w.k_cache), static_cast<__half*>(w.v_cache),
+                                 hidden, c->pl_scratch};
+        // B1-B8: h += Wo attn(...), x2 = RMSNorm(h) * ffn_norm
+        cudaError_t e = qmoe::launch_prefill_layer_attn(a, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "prefill attention launch");
+        // B9: h = h + MoE(x2).  The residual is updated in place: every output
+        // element is formed from the same element of the residual by one thread
+        int32_t* ids_l = ids_out ? ids_out + (size_t)l * n_tokens * k.top_k : nullptr;
+        qmoe_status st = run_moe(c, x2, hidden, nullptr, w.router_w, w.gate_exps, w.up_exps,
+                                 w.down_exps, QMOE_Q4_K, QMOE_Q4_K, w.down_t, n_tokens, hidden, ids_l,
+                                 nullptr);
+        if (st != QMOE_OK) return st;
     }
     c->err[0] = 0;
     return QMOE_OK;

@@ -183,4 +183,38 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
                            const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
                            float* out, cudaStream_t st);
 
+// A dense Q4_K GEMM on the tensor cores (prefill_umma.cu):
+// y[t][yoff + r] = sum_k W[r][k] x[t][k] (+ res[t][yoff + r]) for t < T,
+// W [rows][K] Q4_K rows (rows % 128 == 0, K % 256 == 0), x fp16 [T][K], y / res
+// fp32 with row pitch ldy.  res may equal y (in place).
+cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
+                                  int ldy, int yoff, const float* res, cudaStream_t st);
+
+// Batched prefill of one decoder layer (prefill_layer.cu): everything up to
+// the MoE input.  hidden [T][H] fp32 is updated in place to h + Wo attn, the
+// KV cache slots pos0 .. pos0+T-1 are written, and the MoE input
+// x2 = RMSNorm(h) * ffn_norm is left in the scratch (prefill_layer_x2).
+struct PrefillLayerArgs {
+    int T, H, nq, nkv, hd, max_ctx, pos0;
+    float eps;
+    const double* inv_freq;
+    const float* attn_norm;
+    const uint8_t* wq;
+    const uint8_t* wk;
+    const uint8_t* wv;
+    const uint8_t* wo;
+    const float* q_norm;
+    const float* k_norm;
+    const float* ffn_norm;
+    __half* k_cache;
+    __half* v_cache;
+    float* hidden;
+    void* scratch;            // prefill_layer_scratch_bytes(T, ...)
+};
+size_t prefill_layer_scratch_bytes(int T, int H, int nq, int nkv, int hd);
+bool prefill_layer_supported(int H, int nq, int nkv, int hd);
+cudaError_t prefill_layer_prepare();
+cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st);
+float* prefill_layer_x2(void* scratch, int T, int H, int nq, int nkv, int hd);
+
 }  // namespace qmoe

@@ -48,12 +48,20 @@ def matrix_bytes(qtype: str, rows: int, cols: int) -> int:
     return rows * row_bytes(qtype, cols)
 
 
-def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int, d_std: float = 1e-3) -> np.ndarray:
+def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int, d_std: float = 1e-3,
+                 centered: bool = False) -> np.ndarray:
+    """Random superblocks: random bytes, then the fp16 super-scales d (and dmin)
+    drawn as |N(0, d_std)|.  centered (Q4_K only): dmin = 7.5 d instead, so that
+    the offset dmin * m cancels d * sc * q on average over the uniformly random
+    6-bit sc, m and 4-bit q: zero-mean weights, as in a trained model (Q6_K
+    weights d * sc * (q - 32) with a signed sc are zero-mean already)."""
     bb = BLOCK_BYTES[qtype]
     raw = np.frombuffer(rng.bytes(nblocks * bb), dtype=np.uint8).reshape(nblocks, bb).copy()
     d = (np.abs(rng.standard_normal(nblocks)) * d_std).astype(np.float16)
     if qtype == "Q4_K":
         dmin = (np.abs(rng.standard_normal(nblocks)) * d_std).astype(np.float16)
+        if centered:
+            dmin = (d.astype(np.float32) * 7.5).astype(np.float16)
         raw[:, 0:2] = d.view(np.uint8).reshape(nblocks, 2)
         raw[:, 2:4] = dmin.view(np.uint8).reshape(nblocks, 2)
     else:
@@ -62,24 +70,24 @@ def _fill_kquant(rng: np.random.Generator, qtype: str, nblocks: int, d_std: floa
 
 
 def kquant_matrix(seed: int, tag: int, index: int, qtype: str, rows: int, cols: int,
-                  d_std: float = 1e-3) -> np.ndarray:
+                  d_std: float = 1e-3, centered: bool = False) -> np.ndarray:
     """One quantised matrix [rows][cols] as uint8 [rows][row_bytes]."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
     nblk = rows * (cols // QK_K)
-    return _fill_kquant(rng, qtype, nblk, d_std).reshape(rows, row_bytes(qtype, cols))
+    return _fill_kquant(rng, qtype, nblk, d_std, centered).reshape(rows, row_bytes(qtype, cols))
 
 
 def expert_slice(seed: int, which: str, e: int, qtype: str, rows: int, cols: int,
-                 d_std: float = 1e-3) -> np.ndarray:
-    return kquant_matrix(seed, _TAG[which], e, qtype, rows, cols, d_std)
+                 d_std: float = 1e-3, centered: bool = False) -> np.ndarray:
+    return kquant_matrix(seed, _TAG[which], e, qtype, rows, cols, d_std, centered)
 
 
 def expert_tensor(seed: int, which: str, n_experts: int, qtype: str, rows: int, cols: int,
-                  d_std: float = 1e-3) -> np.ndarray:
+                  d_std: float = 1e-3, centered: bool = False) -> np.ndarray:
     """3-D expert tensor: expert e's slice starts at e * rows * row_bytes (contiguous)."""
     out = np.empty((n_experts, rows, row_bytes(qtype, cols)), dtype=np.uint8)
     for e in range(n_experts):
-        out[e] = expert_slice(seed, which, e, qtype, rows, cols, d_std)
+        out[e] = expert_slice(seed, which, e, qtype, rows, cols, d_std, centered)
     return out
 
 
@@ -147,33 +155,52 @@ def step_layer_small(geo: dict, layer: int) -> dict:
     router = rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32)
     k_cache = rng.standard_normal((nkv, ctx, hd)).astype(np.float16)
     v_cache = rng.standard_normal((nkv, ctx, hd)).astype(np.float16)
-    wq = kquant_matrix(seed, _TAG["wq"], 0, "Q4_K", nq * hd, H)
-    wk = kquant_matrix(seed, _TAG["wk"], 0, "Q4_K", nkv * hd, H)
-    wv = kquant_matrix(seed, _TAG["wv"], 0, "Q4_K", nkv * hd, H)
-    wo = kquant_matrix(seed, _TAG["wo"], 0, "Q4_K", H, nq * hd)
+    ads, cen = geo.get("attn_d_std", 1e-3), geo.get("q4_centered", False)
+    wq = kquant_matrix(seed, _TAG["wq"], 0, "Q4_K", nq * hd, H, ads, cen)
+    wk = kquant_matrix(seed, _TAG["wk"], 0, "Q4_K", nkv * hd, H, ads, cen)
+    wv = kquant_matrix(seed, _TAG["wv"], 0, "Q4_K", nkv * hd, H, ads, cen)
+    wo = kquant_matrix(seed, _TAG["wo"], 0, "Q4_K", H, nq * hd, ads, cen)
     return dict(attn_norm=attn_norm, q_norm=q_norm, k_norm=k_norm, ffn_norm=ffn_norm,
                 router=router, k_cache=k_cache, v_cache=v_cache, wq=wq, wk=wk, wv=wv, wo=wo,
                 down_t=step_down_qtype(layer))
+
+
+def _expert_d_std(geo: dict, qtype: str) -> float:
+    """Spread of the expert super-scales: geo["expert_d_std"] (default 1e-3),
+    times geo["q6_d_scale"] (default 1) for Q6_K.  A Q6_K weight is d * sc * q
+    with an 8-bit sc and a 6-bit q, about ten times a Q4_K weight at the same d;
+    q6_d_scale = 0.1 gives both types the same weight spread."""
+    ds = geo.get("expert_d_std", 1e-3)
+    return ds * geo.get("q6_d_scale", 1.0) if qtype == "Q6_K" else ds
 
 
 def step_layer_experts(geo: dict, layer: int) -> dict:
     H, E, F = geo["H"], geo["E"], geo["F"]
     seed = geo["seed0"] + layer
     dt = step_down_qtype(layer)
-    return dict(gate=expert_tensor(seed, "gate", E, "Q4_K", F, H),
-                up=expert_tensor(seed, "up", E, "Q4_K", F, H),
-                down=expert_tensor(seed, "down", E, dt, H, F))
+    cen = geo.get("q4_centered", False)
+    return dict(gate=expert_tensor(seed, "gate", E, "Q4_K", F, H, _expert_d_std(geo, "Q4_K"), cen),
+                up=expert_tensor(seed, "up", E, "Q4_K", F, H, _expert_d_std(geo, "Q4_K"), cen),
+                down=expert_tensor(seed, "down", E, dt, H, F, _expert_d_std(geo, dt), cen))
 
 
 def step_layer_expert(geo: dict, layer: int, which: str, e: int) -> np.ndarray:
     """Regenerate one expert slice of one layer (identical to the full tensor's slice)."""
     H, F = geo["H"], geo["F"]
     seed = geo["seed0"] + layer
+    cen = geo.get("q4_centered", False)
     if which == "down":
-        return expert_slice(seed, "down", e, step_down_qtype(layer), H, F)
-    return expert_slice(seed, which, e, "Q4_K", F, H)
+        dt = step_down_qtype(layer)
+        return expert_slice(seed, "down", e, dt, H, F, _expert_d_std(geo, dt), cen)
+    return expert_slice(seed, which, e, "Q4_K", F, H, _expert_d_std(geo, "Q4_K"), cen)
 
 
 def step_input(geo: dict) -> np.ndarray:
     rng = np.random.Generator(np.random.PCG64(geo["input_seed"]))
     return rng.standard_normal(geo["H"]).astype(np.float32)
+
+
+def prefill_input(geo: dict, T: int) -> np.ndarray:
+    """Hidden states of T prompt tokens, F32 [T][H], standard normal."""
+    rng = np.random.Generator(np.random.PCG64(geo["input_seed"] + 1))
+    return rng.standard_normal((T, geo["H"])).astype(np.float32)

@@ -6,7 +6,9 @@ gate/up, Q6_K down) on seeded synthetic weights.  A step is one full MoE-FFN
 layer call (router, top-k, per-expert pair lists, gate/up + SwiGLU, down,
 weighted combine into the residual) through the C ABI.  Other workloads:
 ``batch8`` (8 tokens, Q4_K down), ``prefill`` (512 tokens, biased router, the
-tensor-core path) and ``step48`` (a full 48-layer decode step at context 4096).
+tensor-core path), ``step48`` (a full 48-layer decode step at context 4096) and
+``prefill_layer`` (a batched prefill of 512 prompt tokens through one whole
+decoder layer: attention block and MoE).
 
 Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs,
 bracketed by a barrier and a device synchronise, timed with CUDA events on the
@@ -52,6 +54,9 @@ WORKLOADS = {
                     desc="qwen3moe-30b-a3b MoE layer prefill, T=512, biased router, Q6_K down"),
     "step48": dict(cfg=None, copies=1, e2e=10, steps=400, warmup=3,
                    desc="qwen3moe-30b-a3b 48-layer decode step, T=1, context 4096"),
+    "prefill_layer": dict(cfg=None, copies=3, e2e=10, steps=300, warmup=6,
+                          desc="qwen3moe-30b-a3b decoder layer batched prefill, T=512 prompt tokens "
+                               "at positions 0..511, context 4096, Q6_K down"),
     # supplementary (not one of the five configurations): the prefill layer at
     # T=4096, where the contraction is compute-bound and the tensor-pipe
     # fraction is the meaningful one
@@ -66,7 +71,7 @@ WORKLOADS = {
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
-               "step48": None, "prefill4096": None, "decode_q8k": None}
+               "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -193,26 +198,53 @@ def expert_bytes(H, F, gate_t, up_t, down_t):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
+def cpu_rate(call, units: int, seconds: float, threads: int):
+    """Units per second of `call` (which processes `units`) run back to back on
+    `threads` host threads for about `seconds`.  The oracle is plain C called
+    through ctypes, which releases the interpreter lock for the call, and it
+    keeps no global state, so the threads run it side by side.  Returns (rate,
+    calls, elapsed)."""
+    counts = [0] * threads
+    t0 = time.perf_counter()
+
+    def work(i):
+        while time.perf_counter() - t0 < seconds:
+            call()
+            counts[i] += 1
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    el = time.perf_counter() - t0
+    return sum(counts) * units / el, sum(counts), el
+
+
+def cpu_baseline(call, units: int, seconds: float, what: str):
+    """The oracle on one thread and on every core: the all-core rate is the
+    baseline value, the single-thread rate is kept beside it."""
+    call()
+    one, n1, e1 = cpu_rate(call, units, seconds / 2, 1)
+    th = cores()
+    allc, na, ea = cpu_rate(call, units, seconds / 2, th)
+    return {"value": allc, "unit": "tokens/s/layer", "cores": th, "kind": "oracle",
+            "single_thread_value": one,
+            "sample": f"{what}: {n1} calls on 1 thread in {e1:.1f} s, {na} calls on {th} "
+                      f"threads in {ea:.1f} s"}
+
+
 def cpu_sample_layer(inp, seconds: float, max_tokens: int, q8k: bool = False):
     """The oracle on a bounded sample of the layer workload: tokens/s/layer."""
     import oracle
     oracle.build()
     forward = oracle.moe_forward_q8k if q8k else oracle.moe_forward
-    T = inp["T"]
-    n = min(T, max_tokens)
+    n = min(inp["T"], max_tokens)
     one = dict(inp)
     one["x"] = inp["x"][:n]
     one["T"] = n
-    done, t0 = 0, time.perf_counter()
-    while True:
-        forward(one)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds and done >= 1:
-            break
-        if el >= 3 * seconds:
-            break
-    return done * n / el, f"{done} oracle calls of {n} tokens of this layer workload, {el:.1f} s"
+    return cpu_baseline(lambda: forward(one), n, seconds,
+                        f"oracle calls on the first {n} tokens of this layer workload")
 
 
 def cpu_sample_step(geo, seconds: float):
@@ -220,18 +252,21 @@ def cpu_sample_step(geo, seconds: float):
     oracle.build()
     h = synth.step_input(geo).astype(np.float64)
     pos = geo["ctx"] - 1
-    layers, t0 = 0, time.perf_counter()
-    while True:
-        small = synth.step_layer_small(geo, layers)
-        ex = synth.step_layer_experts(geo, layers)
-        tl = time.perf_counter()
-        r = oracle.decode_layer(geo, small, ex, h, pos)
-        h = r["h"]
-        layers += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or layers >= geo["n_layers"]:
-            break
-    return layers / el, f"{layers} oracle decoder layers of the 48-layer step (context 4096), {el:.1f} s"
+    small = synth.step_layer_small(geo, 0)
+    ex = synth.step_layer_experts(geo, 0)
+    return cpu_baseline(lambda: oracle.decode_layer(geo, small, ex, h, pos), 1, seconds,
+                        "oracle decoder layers (layer 0 of the 48-layer step, context 4096)")
+
+
+def cpu_sample_prefill_layer(geo, seconds: float):
+    import oracle
+    oracle.build()
+    small = synth.step_layer_small(geo, 0)
+    ex = synth.step_layer_experts(geo, 0)
+    n = 4
+    hs = synth.prefill_input(geo, geo["T"])[:n].astype(np.float64)
+    return cpu_baseline(lambda: oracle.prefill_layer(geo, small, ex, hs, geo["pos0"]), n, seconds,
+                        f"oracle layer calls on the first {n} prompt tokens (token by token)")
 
 
 def cores():
@@ -256,6 +291,15 @@ def run_reference(args):
         step = lambda: forward(one)  # noqa: E731
         tokens_per_step = sample
         what = f"{sample} tokens of the {args.workload} layer workload per step"
+    elif args.workload == "prefill_layer":
+        geo = dict(synth.PREFILL_LAYER_DEFAULT)
+        small = synth.step_layer_small(geo, 0)
+        ex = synth.step_layer_experts(geo, 0)
+        sample = 4
+        hs = synth.prefill_input(geo, geo["T"])[:sample].astype(np.float64)
+        step = lambda: oracle.prefill_layer(geo, small, ex, hs, geo["pos0"])  # noqa: E731
+        tokens_per_step = sample
+        what = f"the first {sample} prompt tokens of the prefill layer workload per step"
     else:
         geo = dict(synth.STEP_DEFAULT)
         small = synth.step_layer_small(geo, 0)
@@ -270,10 +314,28 @@ def run_reference(args):
     warm = min(args.warmup, 1)
     for _ in range(warm):
         step()
-    k = max(3, min(args.steps, int(budget / max(est, 1e-6))))
+    # the K steps run on every host core (threads taking the next step in turn;
+    # the oracle is plain C behind ctypes, which releases the interpreter lock)
+    th = cores()
+    k = max(3, min(args.steps, int(budget * th / max(est, 1e-6))))
+    th = min(th, k)
+    left = [k]
+    lock = threading.Lock()
+
+    def work():
+        while True:
+            with lock:
+                if left[0] == 0:
+                    return
+                left[0] -= 1
+            step()
+
+    ts = [threading.Thread(target=work) for _ in range(th)]
     t0 = time.perf_counter()
-    for _ in range(k):
-        step()
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
     el = time.perf_counter() - t0
     val = k * tokens_per_step / el
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s/layer",
@@ -281,9 +343,10 @@ def run_reference(args):
             "ms_per_step": 1000 * el / k, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w["desc"]},
-            "cpu_baseline": {"value": val, "unit": "tokens/s/layer", "cores": cores(),
+            "cpu_baseline": {"value": val, "unit": "tokens/s/layer", "cores": th,
                              "kind": "oracle",
-                             "sample": f"{k} steps of {what} (steps capped to ~{budget:.0f} s)"},
+                             "sample": f"{k} steps of {what} on {th} threads (steps capped to "
+                                       f"~{budget:.0f} s of single-thread work per thread)"},
             "e2e": {"value": val, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -362,8 +425,12 @@ def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index, cl
             stream.synchronize()
             pg.barrier()
         e0.record(stream)
+        marks = [e0]
         for _ in range(steps // R):
             g_full.replay()
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            marks.append(ev)
         if g_rem is not None:
             g_rem.replay()
         e1.record(stream)
@@ -379,6 +446,14 @@ def timed_graphs(torch, stream, calls, steps, warmup, pg, dev, sampler_index, cl
     ms = max_over_ranks(torch, e0.elapsed_time(e1), pg, dev)
     if clocks.get("sm_mhz"):
         clocks["ms_per_step_x_mhz"] = ms / steps * clocks["sm_mhz"]
+    # the timed region in segments of one rotation each (R steps): spread of the
+    # per-step time inside it
+    seg = [marks[i].elapsed_time(marks[i + 1]) / R for i in range(len(marks) - 1)]
+    if seg:
+        clocks["segments"] = {"n": len(seg), "steps_each": R,
+                              "median_ms_per_step": float(np.median(seg)),
+                              "min_ms_per_step": float(np.min(seg)),
+                              "max_ms_per_step": float(np.max(seg))}
     return ms, clocks
 
 
@@ -487,9 +562,7 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
         res["tensor_tflops"] = flops / step_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
-        val, sample = cpu_sample_layer(inp, args.cpu_seconds, 8 if T <= 8 else 16, q8k)
-        cpu = {"value": val, "unit": "tokens/s/layer", "cores": cores(), "kind": "oracle",
-               "sample": sample}
+        cpu = cpu_sample_layer(inp, args.cpu_seconds, 8 if T <= 8 else 16, q8k)
     return res, cpu
 
 
@@ -574,9 +647,117 @@ def bench_step48(args, torch, q, dev, stream, ws, pg, local):
                      "routers": rbytes})
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
-        val, sample = cpu_sample_step(geo, args.cpu_seconds)
-        cpu = {"value": val, "unit": "tokens/s/layer", "cores": cores(), "kind": "oracle",
-               "sample": sample}
+        cpu = cpu_sample_step(geo, args.cpu_seconds)
+    return res, cpu
+
+
+def bench_prefill_layer(args, torch, q, dev, stream, ws, pg, local):
+    """One whole decoder layer (attention block + MoE) over T prompt tokens
+    through qmoe_prefill, the layer's weights and KV cache rotating over
+    `copies` device copies."""
+    geo = dict(synth.PREFILL_LAYER_DEFAULT)
+    T, pos0 = geo["T"], geo["pos0"]
+    H, E, K, F = geo["H"], geo["E"], geo["K"], geo["F"]
+    nq, nkv, hd = geo["n_heads"], geo["n_kv"], geo["head_dim"]
+    small = synth.step_layer_small(geo, 0)
+    ex = synth.step_layer_experts(geo, 0)
+    base = {}
+    for n in ("attn_norm", "q_norm", "k_norm", "ffn_norm", "router", "wq", "wk", "wv", "wo"):
+        base[n] = torch.from_numpy(np.ascontiguousarray(small[n])).to(dev)
+    for n in ("k_cache", "v_cache"):
+        base[n] = torch.from_numpy(np.ascontiguousarray(small[n]).view(np.uint16)).to(dev)
+    for n in ("gate", "up", "down"):
+        base[n] = torch.from_numpy(ex[n]).to(dev)
+    R = args.copies
+    copies = [base] + [{n: t.clone() for n, t in base.items()} for _ in range(R - 1)]
+    dt = q.QTYPE[small["down_t"]]
+
+    def layer_arr(d):
+        return (q.qmoe_layer_weights * 1)(q.qmoe_layer_weights(
+            d["attn_norm"].data_ptr(), d["wq"].data_ptr(), d["wk"].data_ptr(), d["wv"].data_ptr(),
+            d["wo"].data_ptr(), d["q_norm"].data_ptr(), d["k_norm"].data_ptr(),
+            d["ffn_norm"].data_ptr(), d["router"].data_ptr(), d["gate"].data_ptr(),
+            d["up"].data_ptr(), d["down"].data_ptr(), dt, d["k_cache"].data_ptr(),
+            d["v_cache"].data_ptr()))
+
+    arrs = [layer_arr(c) for c in copies]
+    h0 = torch.from_numpy(synth.prefill_input(geo, T)).to(dev)
+    hidden = torch.empty_like(h0)
+    ids = torch.empty((1, T, K), dtype=torch.int32, device=dev)
+    ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream, n_heads=nq,
+                                      n_kv_heads=nkv, head_dim=hd, max_ctx=geo["ctx"],
+                                      rope_base=geo["rope_base"], rms_eps=geo["eps"]))
+    with torch.cuda.stream(stream):
+        hidden.copy_(h0)
+        q.qmoe_prefill(ctx, arrs[0], 1, T, pos0, hidden, ids)
+    stream.synchronize()
+    distinct = len(np.unique(ids.cpu().numpy()))
+    ebytes = distinct * expert_bytes(H, F, "Q4_K", "Q4_K", small["down_t"])
+    attn_bytes = sum(small[n].nbytes for n in ("wq", "wk", "wv", "wo"))
+    qd, kvd = nq * hd, nkv * hd
+    keys = sum(pos0 + t + 1 for t in range(T))
+    # KV: the batch's slots written once, every visible key row read once per kv head
+    kv_bytes = 2 * 2 * T * kvd + 2 * 2 * nkv * hd * (pos0 + T)
+    rbytes = small["router"].nbytes
+    flops = (T * K * 2 * (2 * F * H + H * F) + 2 * T * (qd + 2 * kvd) * H + 2 * T * H * qd
+             + 4 * nq * hd * keys)
+
+    def mk(a):
+        def step():
+            hidden.copy_(h0)
+            q.qmoe_prefill(ctx, a, 1, T, pos0, hidden)
+        return step
+
+    ms, clocks = timed_graphs(torch, stream, [mk(a) for a in arrs], args.steps, args.warmup,
+                              pg, dev, local)
+    secs = ms / 1e3
+    step_s = secs / args.steps
+    hin = torch.from_numpy(synth.prefill_input(geo, T)).pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    for i in range(2):
+        with torch.cuda.stream(stream):
+            hidden.copy_(hin, non_blocking=True)
+            q.qmoe_prefill(ctx, arrs[i % R], 1, T, pos0, hidden)
+            hout.copy_(hidden, non_blocking=True)
+        stream.synchronize()
+    if pg:
+        pg.barrier()
+    te0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        with torch.cuda.stream(stream):
+            hidden.copy_(hin, non_blocking=True)
+            q.qmoe_prefill(ctx, arrs[i % R], 1, T, pos0, hidden)
+            hout.copy_(hidden, non_blocking=True)
+        stream.synchronize()
+    te = time.perf_counter() - te0
+    if pg:
+        tt = torch.tensor([te], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        te = float(tt.item())
+    q.qmoe_destroy(ctx)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = (ebytes + attn_bytes + rbytes) * R
+    res = dict(
+        value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
+        ebytes=ebytes, other_bytes=attn_bytes + kv_bytes + rbytes, distinct=distinct, T=T,
+        e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
+        launches=q.LAUNCHES_PER_PREFILL_LAYER_ATTN + q.LAUNCHES_PER_PREFILL_FORWARD,
+        tensor_tflops=flops / step_s / 1e12,
+        config={"workload": WORKLOADS["prefill_layer"]["desc"], "hidden": H, "n_experts": E,
+                "top_k": K, "ffn": F, "n_heads": nq, "n_kv_heads": nkv, "head_dim": hd,
+                "tokens": T, "pos0": pos0, "context": geo["ctx"], "distinct_experts": distinct,
+                "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
+                      f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
+                      "written right before the timed region"},
+        kernel="whole layer call (attention block GEMMs and attention, routing, grouped GEMMs, "
+               "combine)",
+        tokens_per_s=T * args.steps * ws / secs,
+        bytes_split={"experts": ebytes, "attention_weights": attn_bytes, "kv_cache": kv_bytes,
+                     "routers": rbytes},
+        flops_per_step=flops)
+    cpu = None
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        cpu = cpu_sample_prefill_layer(geo, args.cpu_seconds)
     return res, cpu
 
 
@@ -592,6 +773,8 @@ def main():
     stream = torch.cuda.Stream(dev)
     if args.workload == "step48":
         res, cpu = bench_step48(args, torch, q, dev, stream, ws, pg, local)
+    elif args.workload == "prefill_layer":
+        res, cpu = bench_prefill_layer(args, torch, q, dev, stream, ws, pg, local)
     else:
         res, cpu = bench_layer(args, torch, q, dev, stream, ws, pg, local)
     hbm, tf, kind = peaks()
@@ -622,6 +805,8 @@ def main():
         line["dtype"] = "f16 tensor-core operands, f32 accumulate"
         line["tensor"] = {"achieved_tflops": res["tensor_tflops"], "peak_tflops": tf,
                           "frac": res["tensor_tflops"] / tf, "peak_kind": kind}
+        if "flops_per_step" in res:
+            line["tensor"]["flops_per_step"] = res["flops_per_step"]
     if "bytes_split" in res:
         line["tokens_per_s"] = res["tokens_per_s"]
         line["bytes_per_step"] = res["bytes_split"]

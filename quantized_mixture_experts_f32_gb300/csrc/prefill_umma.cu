@@ -52,21 +52,31 @@ constexpr int NA = 4;                          // A (fp16 weight) stages: the 4 
 static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
 constexpr int NQ = 3;                          // raw Q4_K stages, at most
 // gate/up kernel: token-tile rows, raw and A stages, CTAs per SM it is built
-// for (the stage rings and TMEM columns must fit that many CTAs), TMEM columns
-constexpr int GU_NMAX = 256;
+// for (the stage rings and TMEM columns must fit that many CTAs), TMEM columns.
+// The A (weight) and B (token) rings have the same depth and share one pair of
+// barriers per stage: the MMA thread waits once and commits once per k-block
+// (its loop is a chain of dependent barrier operations, and their latency, not
+// the tensor core, set the pace when A and B had a pair each).
+constexpr int GU_NMAX = 192;
 constexpr int GU_NQ = 3;
 constexpr int GU_NA = 4;
-constexpr int GU_MINB = 1;
-constexpr uint32_t GU_TMEM = 256;
-static_assert(GU_NQ <= NQ && GU_NA <= NA && (GU_NA == 2 || GU_NA == 4) && GU_NMAX <= (int)GU_TMEM,
+constexpr int GU_ACC_COLS = 256;               // TMEM columns per accumulator (two of them)
+constexpr uint32_t GU_TMEM = 2 * GU_ACC_COLS;
+constexpr int GU_NEPI = 4;                     // epilogue warps, one per TMEM lane quarter
+constexpr int W_EPI = NDQ + 4;                 // the first of them (a multiple of 4)
+constexpr int GU_THREADS = (NDQ + 4 + GU_NEPI) * 32;
+static_assert(GU_NQ <= NQ && GU_NA <= NA && (GU_NA == 2 || GU_NA == 4) && GU_NMAX <= GU_ACC_COLS &&
+                  W_EPI % 4 == 0,
               "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
 constexpr int NBMAX = 8;                       // B stages, at most
-constexpr int B_BYTES_GU = 96 * 1024;
+constexpr int GU_BSTAGE = GU_NMAX * KBLK * 2;  // B stage stride (an item loads nb <= GU_NMAX rows)
+constexpr int B_BYTES_GU = GU_NA * GU_BSTAGE;
 constexpr int B_BYTES_DN = 64 * 1024;
 
 struct PfBars {
     uint64_t qfull[NQ], qempty[NQ], afull[NA], aempty[NA], bfull[NBMAX], bempty[NBMAX], acc;
+    uint64_t accfull[2], accempty[2];
     uint32_t tmem;
 };
 
@@ -76,8 +86,10 @@ __host__ __device__ inline int b_stages(int b_bytes, int nb) {
     return n < NBMAX ? n : NBMAX;
 }
 
-// token-tile height and the matching B tensor map (64 / 128 / 256 rows)
+// token-tile height and the matching B tensor map (64 / 128 / 256 rows; the
+// gate/up kernel's largest map is GU_NMAX rows)
 __device__ __forceinline__ int box_rows(int n) { return n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+__device__ __forceinline__ int box_rows_gu(int n) { return n <= 64 ? 64 : n <= 128 ? 128 : GU_NMAX; }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
@@ -173,7 +185,7 @@ struct GuParams {
     const int32_t* used_expert;
     const int32_t* used_first;
     __half* act;          // [P][F] fp16, rows in pair-list order
-    int H, F, ntiles;     // ntiles: token tiles per expert slot in grid.y
+    int H, F;             // K of the GEMM; rows per expert (MODE 0) / of the matrix (MODE 1)
     // plain mode (a dense Q4_K GEMM): y[t][yoff + r] = sum_k W[r][k] x[t][k]
     // (+ res[t][yoff + r]) for the dense_T tokens of x, W = the tm_gate map
     float* y;
@@ -181,102 +193,184 @@ struct GuParams {
     int dense_T, ldy, yoff;
 };
 
-// MODE 0: grid (F/64, max_used * ntiles); A = 64 gate + 64 up rows of one
-// expert, epilogue silu(g)*u -> fp16 act.  MODE 1: grid (rows/128, ntiles);
-// A = 128 consecutive rows of one Q4_K matrix [rows][H] (H = its K), B = the
-// dense_T token rows of x, epilogue fp32 y (+ res).  PF_THREADS threads.
+// One work item of the gate/up kernel: weight rows f0 .. of expert e against
+// the token rows first + n0 .. first + n0 + n - 1.
+struct GuItem {
+    int e, first, n0, n, f0;
+};
+
+// Items in the order (token tile, weight-row tile), the row tile fastest, so
+// that CTAs working at the same time share the token rows in L2.  MODE 0: the
+// token tiles are those of every used expert in turn (tfirst: exclusive
+// prefix of the tiles per used expert); MODE 1: the dense_T tokens.
 template <int MODE>
-__global__ void __launch_bounds__(PF_THREADS, GU_MINB)
+__device__ __forceinline__ GuItem gu_item(const GuParams& p, const int* tfirst, int n_used, int it) {
+    GuItem w;
+    const int FT = MODE == 0 ? p.F / 64 : p.F / TILE_M;
+    const int tt = it / FT, ft = it - tt * FT;
+    if (MODE == 0) {
+        int lo = 0, hi = n_used - 1;                     // last u with tfirst[u] <= tt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tfirst[mid] <= tt) lo = mid;
+            else hi = mid - 1;
+        }
+        w.e = p.used_expert[lo];
+        w.first = p.used_first[lo];
+        w.n0 = (tt - tfirst[lo]) * GU_NMAX;
+        w.n = min(GU_NMAX, p.used_first[lo + 1] - w.first - w.n0);
+        w.f0 = ft * 64;
+    } else {
+        w.e = 0;
+        w.first = 0;
+        w.n0 = tt * GU_NMAX;
+        w.n = min(GU_NMAX, p.dense_T - w.n0);
+        w.f0 = ft * TILE_M;
+    }
+    return w;
+}
+
+// Persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x,
+// ...; every ring (raw superblocks, A + B k-blocks, two TMEM accumulators)
+// runs on across items, so one item's loads and dequantisation overlap the
+// previous item's last MMAs and its epilogue.  MODE 0: A = 64 gate + 64 up
+// rows of one expert, epilogue silu(g)*u -> fp16 act.  MODE 1: A = 128
+// consecutive rows of one Q4_K matrix [F][H], B = the dense_T token rows of x,
+// epilogue fp32 y (+ res).  Warps: NDQ dequant, Q load, B load, MMA, one idle,
+// GU_NEPI epilogue.
+template <int MODE>
+__global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                    const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ CUtensorMap tm_x128,
-                   const __grid_constant__ CUtensorMap tm_x256, const GuParams p) {
+                   const __grid_constant__ CUtensorMap tm_xg, const GuParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     // 1024-aligned base, kept a shared-space pointer (an integer round trip
     // would turn every access into a generic one)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
-    const int u = blockIdx.y / p.ntiles, nt = blockIdx.y % p.ntiles;
-    if (MODE == 0 && u >= *p.n_used) return;
-    const int first = MODE == 0 ? p.used_first[u] : 0;
-    const int cnt = MODE == 0 ? p.used_first[u + 1] - first : p.dense_T;
-    const int n0 = nt * GU_NMAX;
-    if (n0 >= cnt) return;
-    const int n = min(GU_NMAX, cnt - n0);
-    const int N = (n + 15) & ~15;
-    const int nb = box_rows(n);
-    const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_x256;
-    const int e = MODE == 0 ? p.used_expert[u] : 0;
-    const int f0 = blockIdx.x * (MODE == 0 ? 64 : 128);
     const int H = p.H, F = p.F;
     const int NKB = H / KBLK, NSB = H / QK;
+    const int FT = MODE == 0 ? F / 64 : F / TILE_M;
 
     uint8_t* qst = sm;                                   // GU_NQ x QSTAGE_GU
     uint8_t* ast = sm + ((GU_NQ * QSTAGE_GU + 1023) & ~1023);  // GU_NA x A_STAGE (1024-aligned)
-    uint8_t* bst = ast + GU_NA * A_STAGE;                // B_BYTES_GU
+    uint8_t* bst = ast + GU_NA * A_STAGE;                // GU_NA x GU_BSTAGE
     PfBars* bars = reinterpret_cast<PfBars*>(bst + B_BYTES_GU);
-    const int NB = b_stages(B_BYTES_GU, nb);
-    const int BSTAGE = nb * KBLK * 2;
+    int* tfirst = reinterpret_cast<int*>(bars + 1);      // [n_used + 1] (MODE 0)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    const int n_used = MODE == 0 ? *p.n_used : 0;
     if (tid == 0) {
         for (int i = 0; i < GU_NQ; ++i) {
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], NDQ);
         }
         for (int i = 0; i < GU_NA; ++i) {
-            mbar_init(&bars->afull[i], NDQ);
+            mbar_init(&bars->afull[i], NDQ + 1);         // dequant warps + the B copy
             mbar_init(&bars->aempty[i], 1);
         }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->accfull[i], 1);
+            mbar_init(&bars->accempty[i], GU_NEPI);
         }
-        mbar_init(&bars->acc, 1);
         fence_barrier_init();
+    }
+    if (MODE == 0 && warp == W_QLOAD) {
+        // token tiles per used expert, exclusive prefix (one warp)
+        int carry = 0;
+        for (int u0 = 0; u0 < n_used; u0 += 32) {
+            const int u = u0 + lane;
+            const int t = u < n_used ? (p.used_first[u + 1] - p.used_first[u] + GU_NMAX - 1) / GU_NMAX : 0;
+            int incl = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (u < n_used) tfirst[u] = carry + incl - t;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) tfirst[n_used] = carry;
     }
     if (warp == 0) tmem_alloc(&bars->tmem, GU_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
+    const int n_items = MODE == 0 ? FT * tfirst[n_used] : FT * ((p.dense_T + GU_NMAX - 1) / GU_NMAX);
 
     if (warp == W_QLOAD) {
-        // raw gate/up superblock columns, NQ ahead of the dequant warps
+        // raw superblock columns of each item's 128 weight rows, GU_NQ ahead
         if (lane == 0) {
-            const int ybase = e * F + f0;
-            for (int sb = 0; sb < NSB; ++sb) {
-                const int st = sb % GU_NQ;
-                if (!mbar_wait(&bars->qempty[st], ((uint32_t)(sb / GU_NQ) & 1u) ^ 1u)) break;
-                uint8_t* dst = qst + st * QSTAGE_GU;
-                mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
-                tma_load_2d(dst, &tm_gate, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
-                if (MODE == 0)
-                    tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
-                else
-                    tma_load_2d(dst + 64 * Q4K_BYTES, &tm_gate, sb * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
+            int gs = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
+                const int ybase = w.e * F + w.f0;
+                for (int sb = 0; sb < NSB; ++sb, ++gs) {
+                    const int st = gs % GU_NQ;
+                    if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / GU_NQ) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = qst + st * QSTAGE_GU;
+                    mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
+                    tma_load_2d(dst, &tm_gate, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                    if (MODE == 0)
+                        tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                    else
+                        tma_load_2d(dst + 64 * Q4K_BYTES, &tm_gate, sb * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
+                }
             }
         }
     } else if (warp == W_BLOAD) {
-        // the expert's gathered x rows, NB k-blocks ahead of the MMA
-        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmx, first + n0);
+        // each item's token rows, in step with the A stages (which share the
+        // stage barriers: full = the dequant warps' arrivals plus this copy)
+        if (lane == 0) {
+            int gk = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
+                const int nb = box_rows_gu(w.n);
+                const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_xg;
+                for (int kb = 0; kb < NKB; ++kb, ++gk) {
+                    const int st = gk % GU_NA;
+                    if (!mbar_wait(&bars->aempty[st], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->afull[st], (uint32_t)(nb * KBLK * 2));
+                    tma_load_2d(bst + st * GU_BSTAGE, tmx, kb * KBLK, w.first + w.n0, &bars->afull[st]);
+                }
+            }
+        }
     } else if (warp == W_MMA) {
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16(TILE_M, N);
-            for (int kb = 0; kb < NKB; ++kb) {
-                const int sa = kb % GU_NA, sb = kb % NB;
-                if (!mbar_wait(&bars->afull[sa], (uint32_t)(kb / GU_NA) & 1u) ||
-                    !mbar_wait(&bars->bfull[sb], (uint32_t)(kb / NB) & 1u))
-                    break;
+            int gk = 0, j = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++j) {
+                const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
+                const int buf = j & 1;
+                // the epilogue has drained this accumulator (item j - 2)
+                if (!mbar_wait(&bars->accempty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u)) break;
                 tc_fence_after();
-                const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
-                const uint64_t bd = umma_sdesc(smem_u32(bst + sb * BSTAGE));
+                const uint32_t d = tmem + (uint32_t)(buf * GU_ACC_COLS);
+                const uint32_t idesc = umma_idesc_f16(TILE_M, (w.n + 15) & ~15);
+                for (int kb = 0; kb < NKB; ++kb, ++gk) {
+                    const int sa = gk % GU_NA;
+                    if (!mbar_wait(&bars->afull[sa], (uint32_t)(gk / GU_NA) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
+                    const uint64_t bd = umma_sdesc(smem_u32(bst + sa * GU_BSTAGE));
 #pragma unroll
-                for (int k = 0; k < KBLK / 16; ++k)
-                    umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                             (kb | k) != 0);
-                umma_commit(&bars->aempty[sa]);
-                umma_commit(&bars->bempty[sb]);
+                    for (int k = 0; k < KBLK / 16; ++k)
+                        umma_f16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (kb | k) != 0);
+                    umma_commit(&bars->aempty[sa]);
+                }
+                if (ok) umma_commit(&bars->accfull[buf]);
             }
-            umma_commit(&bars->acc);
         }
     } else if (warp < NDQ) {
         // dequant: thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r) and 16-k
@@ -299,12 +393,12 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
             rowb[r] = row * 128;
         }
         const int o_lo = (qq ^ (lane & 7)) << 4, o_hi = ((qq + 4) ^ (lane & 7)) << 4;   // row % 8 == lane % 8
-        int sq = 0;
-        uint32_t qpar = 0;
-        for (int sb = 0; sb < NSB; ++sb) {
-            const int sq_this = sq;
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int gk = 0;
+        for (int gs = 0; gs < my_items * NSB; ++gs) {
+            const int sq = gs % GU_NQ;
             const uint8_t* stg = qst + sq * QSTAGE_GU;
-            mbar_wait(&bars->qfull[sq], qpar);
+            if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / GU_NQ) & 1u)) break;
             uint4 hdr[RPT];
             uint2 v[RPT][4];
 #pragma unroll
@@ -314,68 +408,78 @@ __global__ void __launch_bounds__(PF_THREADS, GU_MINB)
                 for (int c = 0; c < 4; ++c)
                     v[r][c] = *reinterpret_cast<const uint2*>(stg + src[r] + 16 + 32 * c + 8 * qq);
             }
-            if (++sq == GU_NQ) {
-                sq = 0;
-                qpar ^= 1u;
-            }
             Q4Half own[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) own[r] = q4_half_scales(hdr[r], qq);
+            bool ok = true;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                // k-block 4 sb + c: stage c % GU_NA, its use number (4 sb + c) / GU_NA
-                const int sa = c % GU_NA;
-                const uint32_t apar = (((uint32_t)((4 / GU_NA) * sb + c / GU_NA)) & 1u) ^ 1u;
+            for (int c = 0; c < 4; ++c, ++gk) {
+                const int sa = gk % GU_NA;
                 Q4Half sc[RPT];
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
-                mbar_wait(&bars->aempty[sa], apar);
+                if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) q4_quarter(v[r][c], sc[r], ast + sa * A_STAGE + rowb[r], o_lo, o_hi);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->afull[sa]);
             }
+            if (!ok) break;
             // the raw stage is handed back only now: every value loaded from it
             // has fed a store above, so no load of this warp is still pending
             // when the next TMA copy may overwrite it (releasing right after the
             // loads were issued let a late load read the next superblock)
-            if (lane == 0) mbar_arrive(&bars->qempty[sq_this]);
+            if (lane == 0) mbar_arrive(&bars->qempty[sq]);
         }
-        // epilogue: TMEM lane quarter (warp % 4); column quarter (warp / 4)
-        mbar_wait(&bars->acc, 0);
-        tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2, cpw = 1024 / NDQ;   // columns per warp
-        if (MODE == 0) {
-            const int f = f0 + 16 * lq + (lane & 15);
-            for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
+    } else if (warp >= W_EPI) {
+        // epilogue: TMEM lane quarter warp % 4, every column of the item
+        const int lq = warp & 3;
+        int j = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+            const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
+            const int buf = j & 1, N = (w.n + 15) & ~15;
+            if (!mbar_wait(&bars->accfull[buf], (uint32_t)(j >> 1) & 1u)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(buf * GU_ACC_COLS) + ((uint32_t)(32 * lq) << 16);
+            if (MODE == 0) {
+                const int f = w.f0 + 16 * lq + (lane & 15);
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(d + (uint32_t)c0, v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float up = __shfl_down_sync(0xffffffffu, v[j], 16);
-                    const int col = c0 + j;
-                    if (lane < 16 && col < n) {
-                        const float g = v[j];
-                        p.act[(size_t)(first + n0 + col) * F + f] =
-                            __float2half_rn(__fdividef(g, 1.f + __expf(-g)) * up);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float up = __shfl_down_sync(0xffffffffu, v[jj], 16);
+                        const int col = c0 + jj;
+                        if (lane < 16 && col < w.n) {
+                            const float g = v[jj];
+                            p.act[(size_t)(w.first + w.n0 + col) * F + f] =
+                                __float2half_rn(__fdividef(g, 1.f + __expf(-g)) * up);
+                        }
+                    }
+                }
+            } else {
+                const int row = p.yoff + w.f0 + 32 * lq + lane;
+                for (int c0 = 0; c0 < N; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(d + (uint32_t)c0, v);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int col = c0 + jj;
+                        if (col < w.n) {
+                            const size_t o = (size_t)(w.n0 + col) * p.ldy + row;
+                            p.y[o] = v[jj] + (p.res ? p.res[o] : 0.f);
+                        }
                     }
                 }
             }
-        } else {
-            const int row = p.yoff + f0 + 32 * lq + lane;
-            for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = c0 + j;
-                    if (col < n) {
-                        const size_t o = (size_t)(n0 + col) * p.ldy + row;
-                        p.y[o] = v[j] + (p.res ? p.res[o] : 0.f);
-                    }
-                }
-            }
+            // every value of this accumulator is in registers: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->accempty[buf]);
         }
     }
     tc_fence_before();
@@ -644,7 +748,19 @@ bool map_half(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 
 
 constexpr size_t GU_SMEM = 1024 + ((GU_NQ * QSTAGE_GU + 1023) & ~1023) + GU_NA * A_STAGE + B_BYTES_GU +
-                           sizeof(PfBars) + 64;
+                           sizeof(PfBars) + sizeof(int) * 1025 + 64;   // + tfirst[E + 1]
+
+// SMs of the current device: the persistent gate/up grid
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+    }
+    return n;
+}
 
 size_t dn_smem(int F, int down_t) {
     const size_t rb = (size_t)(F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
@@ -667,18 +783,18 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     const int P = s.T * s.K;
     const int max_used = P < s.E ? P : s.E;
     // an expert sees each token once at most
-    const int ntiles_gu = (s.T + GU_NMAX - 1) / GU_NMAX, ntiles = (s.T + TILE_NMAX - 1) / TILE_NMAX;
+    const int ntiles = (s.T + TILE_NMAX - 1) / TILE_NMAX;
     gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tg, tu, tx64, tx128, tx256, ta64, ta128, ta256;
+    CUtensorMap tg, tu, tx64, tx128, txg, ta64, ta128, ta256;
     const uint64_t rbg = (uint64_t)(s.H / QK) * Q4K_BYTES;
     // B maps: boxes of 64 / 128 / 256 token rows
     if (!map_bytes(&tg, gate, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_bytes(&tu, up, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
-        !map_half(&tx256, xp, s.H, P, 256) || !map_half(&ta64, actp, s.F, P, 64) ||
+        !map_half(&txg, xp, s.H, P, GU_NMAX) || !map_half(&ta64, actp, s.F, P, 64) ||
         !map_half(&ta128, actp, s.F, P, 128) || !map_half(&ta256, actp, s.F, P, 256))
         return cudaErrorInvalidValue;
 
@@ -692,9 +808,8 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, ntiles_gu, nullptr, nullptr, 0, 0, 0};
-    prefill_gateup<0><<<dim3(s.F / 64, max_used * ntiles_gu), PF_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128,
-                                                                                     tx256, gp);
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0, 0};
+    prefill_gateup<0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128, txg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, ntiles, down_t};
@@ -710,10 +825,10 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
 cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
                                   int ldy, int yoff, const float* res, cudaStream_t st) {
     if (rows % TILE_M || K % QK || T < 1) return cudaErrorInvalidValue;
-    CUtensorMap tw, tx64, tx128, tx256;
+    CUtensorMap tw, tx64, tx128, txg;
     const uint64_t rb = (uint64_t)(K / QK) * Q4K_BYTES;
     if (!map_bytes(&tw, W, rb, (uint64_t)rows, Q4K_BYTES, 64) || !map_half(&tx64, x, K, T, 64) ||
-        !map_half(&tx128, x, K, T, 128) || !map_half(&tx256, x, K, T, 256))
+        !map_half(&tx128, x, K, T, 128) || !map_half(&txg, x, K, T, GU_NMAX))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -722,9 +837,10 @@ cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __hal
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int ntiles = (T + GU_NMAX - 1) / GU_NMAX;
-    GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, ntiles, y, res, T, ldy, yoff};
-    prefill_gateup<1><<<dim3(rows / TILE_M, ntiles), PF_THREADS, GU_SMEM, st>>>(tw, tw, tx64, tx128, tx256, gp);
+    const int items = (rows / TILE_M) * ((T + GU_NMAX - 1) / GU_NMAX);
+    GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, y, res, T, ldy, yoff};
+    prefill_gateup<1><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(tw, tw, tx64, tx128,
+                                                                                          txg, gp);
     return cudaGetLastError();
 }
 

@@ -136,6 +136,12 @@ def moe_inputs(cfg: dict, T: int | None = None) -> dict:
 STEP_DEFAULT = dict(n_layers=48, H=2048, E=128, K=8, F=768, n_heads=32, n_kv=4, head_dim=128,
                     ctx=4096, rope_base=1.0e7, eps=1e-6, seed0=100, input_seed=5000)
 
+# one decoder layer of the Qwen3-30B-A3B shape for a batched prefill of 512
+# prompt tokens at positions 0..511 (context 4096), with the weight spreads
+# under which attention output, MoE output and residual are of one order
+PREFILL_LAYER_DEFAULT = dict(STEP_DEFAULT, n_layers=1, T=512, pos0=0, expert_d_std=3e-4,
+                             attn_d_std=3e-4, q6_d_scale=0.1, q4_centered=True)
+
 
 def step_down_qtype(layer: int) -> str:
     """Down-projection quant type of layer i: Q6_K on even layers, Q4_K on odd ones."""

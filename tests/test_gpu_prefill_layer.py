@@ -199,6 +199,92 @@ def test_prefill_qwen3_geometry(q):
     print(f"qwen3 prefill T=48: rel err {err:.2e}, near-tie tokens {swaps}")
 
 
+def _oracle_kv(geo, small, hs, pos0):
+    """K and V cache rows of every token (fp16), from the oracle's pieces: the
+    first steps of its decoder layer (RMSNorm, the K and V rows, per-head K
+    RMSNorm, NEOX RoPE at pos0 + t), which within a layer depend on the token's
+    own input only."""
+    H, hd, nkv = geo["H"], geo["head_dim"], geo["n_kv"]
+    Wk = oracle.dequant_matrix("Q4_K", small["wk"], nkv * hd, H)
+    Wv = oracle.dequant_matrix("Q4_K", small["wv"], nkv * hd, H)
+    T = hs.shape[0]
+    kr = np.zeros((nkv, T, hd), dtype=np.float16)
+    vr = np.zeros((nkv, T, hd), dtype=np.float16)
+    for t in range(T):
+        x = oracle.rmsnorm(hs[t], small["attn_norm"], geo["eps"])
+        k, v = Wk @ x, Wv @ x
+        for g in range(nkv):
+            kh = oracle.rmsnorm(k[g * hd:(g + 1) * hd], small["k_norm"], geo["eps"])
+            kr[g, t] = oracle.rope_neox(kh, pos0 + t, geo["rope_base"]).astype(np.float16)
+            vr[g, t] = v[g * hd:(g + 1) * hd].astype(np.float16)
+    return kr, vr
+
+
+def test_prefill_qwen3_512_tokens_sampled(q):
+    """The prefill-layer workload itself: 512 prompt tokens at positions
+    0..511, context 4096, in the launch configuration the benchmark times.
+    Every token's K/V slot is checked; the layer output and ids on a sample
+    of tokens (first, last, both sides of the 256-token GEMM tile edge), each
+    from the oracle's decoder layer at that position over oracle K/V rows for
+    all earlier tokens."""
+    geo = dict(synth.PREFILL_LAYER_DEFAULT)
+    T, pos0 = geo["T"], geo["pos0"]
+    dev = torch.device("cuda:0")
+    small, d = _upload(geo, 0, dev)
+    arr = (q.qmoe_layer_weights * 1)(_layer_struct(q, d, small["down_t"]))
+    h0 = synth.prefill_input(geo, T)
+    hidden = torch.from_numpy(h0.copy()).to(dev)
+    ids = torch.full((1, T, geo["K"]), -1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ctx = q.qmoe_create(q.make_config(geo["H"], geo["E"], geo["K"], geo["F"], T, 1,
+                                      stream.cuda_stream, n_heads=geo["n_heads"],
+                                      n_kv_heads=geo["n_kv"], head_dim=geo["head_dim"],
+                                      max_ctx=geo["ctx"], rope_base=geo["rope_base"],
+                                      rms_eps=geo["eps"]))
+    try:
+        q.qmoe_prefill(ctx, arr, 1, T, pos0, hidden, ids)
+        assert q.qmoe_get_status(ctx) == q.QMOE_OK, q.qmoe_last_error(ctx)
+    finally:
+        q.qmoe_destroy(ctx)
+    h_gpu = hidden.cpu().numpy()
+    ids = ids.cpu().numpy()[0]
+    kc = d["k_cache"].cpu().numpy().view(np.float16)
+    vc = d["v_cache"].cpu().numpy().view(np.float16)
+    hs = h0.astype(np.float64)
+    kr, vr = _oracle_kv(geo, small, hs, pos0)
+    for got, ref, name in ((kc, kr, "k_cache"), (vc, vr, "v_cache")):
+        g = got[:, pos0:pos0 + T].astype(np.float64)
+        o = ref.astype(np.float64)
+        assert np.abs(g - o).max() <= TOL_BF16 * max(1.0, np.abs(o).max()), name
+        others = np.ones(geo["ctx"], bool)
+        others[pos0:pos0 + T] = False
+        assert np.array_equal(got[:, others], small[name][:, others]), name
+    ex = synth.step_layer_experts(geo, 0)
+    sample = [0, 1, 2, 127, 255, 256, 400, T - 1]
+    got, want, swaps = [], [], 0
+    for t in sample:
+        cur = dict(small)
+        cur["k_cache"] = small["k_cache"].copy()
+        cur["v_cache"] = small["v_cache"].copy()
+        cur["k_cache"][:, pos0:pos0 + t] = kr[:, :t]
+        cur["v_cache"][:, pos0:pos0 + t] = vr[:, :t]
+        r = oracle.decode_layer(geo, cur, ex, hs[t], pos0 + t)
+        if not np.array_equal(r["ids"], ids[t]):
+            lg = r["logits"].astype(np.float64)
+            kth = lg[r["ids"]].min()
+            changed = set(r["ids"].tolist()) ^ set(ids[t].tolist())
+            assert all(abs(lg[e] - kth) <= ID_SLACK * np.abs(lg).max() for e in changed), \
+                (t, r["ids"], ids[t])
+            r = oracle.decode_layer(geo, cur, ex, hs[t], pos0 + t, force=ids[t])
+            swaps += 1
+        got.append(h_gpu[t])
+        want.append(r["h"])
+    assert swaps <= 1
+    err = rel_err(np.stack(got), np.stack(want))
+    assert err <= TOL_BF16, f"hidden rel err {err:.3e}"
+    print(f"qwen3 prefill T=512 (sampled tokens {sample}): rel err {err:.2e}, near-tie tokens {swaps}")
+
+
 def test_prefill_rejects_bad_arguments(q):
     dev = torch.device("cuda:0")
     ctx = q.qmoe_create(q.make_config(256, 8, 2, 256, 8, 1, 0, n_heads=4, n_kv_heads=2,

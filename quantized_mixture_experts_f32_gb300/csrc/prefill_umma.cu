@@ -53,19 +53,21 @@ static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
 constexpr int NQ = 3;                          // raw Q4_K stages, at most
 // gate/up kernel: token-tile rows, raw and A stages, CTAs per SM it is built
 // for (the stage rings and TMEM columns must fit that many CTAs), TMEM columns.
-// The A (weight) and B (token) rings have the same depth and share one pair of
-// barriers per stage: the MMA thread waits once and commits once per k-block
-// (its loop is a chain of dependent barrier operations, and their latency, not
-// the tensor core, set the pace when A and B had a pair each).
+// The A (weight) and B (token) rings have the same depth and share their
+// barriers, one full / empty pair per two consecutive stages: the MMA thread
+// waits once and commits once per two k-blocks.  Its loop is a chain of
+// dependent operations (barrier wait, tcgen05.mma issues, commit), and that
+// chain, not the tensor core, sets the pace for token tiles of a few dozen
+// rows; fewer barrier operations per MMA shorten it.
 constexpr int GU_NMAX = 192;
 constexpr int GU_NQ = 3;
 constexpr int GU_NA = 4;
 constexpr int GU_ACC_COLS = 256;               // TMEM columns per accumulator (two of them)
 constexpr uint32_t GU_TMEM = 2 * GU_ACC_COLS;
-constexpr int GU_NEPI = 4;                     // epilogue warps, one per TMEM lane quarter
+constexpr int GU_NEPI = 8;                     // epilogue warps, two per TMEM lane quarter
 constexpr int W_EPI = NDQ + 4;                 // the first of them (a multiple of 4)
 constexpr int GU_THREADS = (NDQ + 4 + GU_NEPI) * 32;
-static_assert(GU_NQ <= NQ && GU_NA <= NA && (GU_NA == 2 || GU_NA == 4) && GU_NMAX <= GU_ACC_COLS &&
+static_assert(GU_NQ <= NQ && GU_NA == 4 && GU_NMAX <= GU_ACC_COLS &&
                   W_EPI % 4 == 0,
               "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
@@ -264,8 +266,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], NDQ);
         }
-        for (int i = 0; i < GU_NA; ++i) {
-            mbar_init(&bars->afull[i], NDQ + 1);         // dequant warps + the B copy
+        for (int i = 0; i < GU_NA / 2; ++i) {
+            mbar_init(&bars->afull[i], 2 * (NDQ + 1));   // per k-block: dequant warps + the B copy
             mbar_init(&bars->aempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -333,19 +335,19 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 const int nb = box_rows_gu(w.n);
                 const CUtensorMap* tmx = nb == 64 ? &tm_x64 : nb == 128 ? &tm_x128 : &tm_xg;
                 for (int kb = 0; kb < NKB; ++kb, ++gk) {
-                    const int st = gk % GU_NA;
-                    if (!mbar_wait(&bars->aempty[st], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                    const int st = gk % GU_NA, pr = (gk >> 1) & 1;
+                    if (!mbar_wait(&bars->aempty[pr], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->afull[st], (uint32_t)(nb * KBLK * 2));
-                    tma_load_2d(bst + st * GU_BSTAGE, tmx, kb * KBLK, w.first + w.n0, &bars->afull[st]);
+                    mbar_arrive_expect_tx(&bars->afull[pr], (uint32_t)(nb * KBLK * 2));
+                    tma_load_2d(bst + st * GU_BSTAGE, tmx, kb * KBLK, w.first + w.n0, &bars->afull[pr]);
                 }
             }
         }
     } else if (warp == W_MMA) {
         if (lane == 0) {
-            int gk = 0, j = 0;
+            int gp = 0, j = 0;                           // k-block pairs, items
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++j) {
                 const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
@@ -355,19 +357,23 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * GU_ACC_COLS);
                 const uint32_t idesc = umma_idesc_f16(TILE_M, (w.n + 15) & ~15);
-                for (int kb = 0; kb < NKB; ++kb, ++gk) {
-                    const int sa = gk % GU_NA;
-                    if (!mbar_wait(&bars->afull[sa], (uint32_t)(gk / GU_NA) & 1u)) {
+                for (int kp = 0; kp < NKB / 2; ++kp, ++gp) {
+                    const int pr = gp & 1;
+                    if (!mbar_wait(&bars->afull[pr], (uint32_t)(gp >> 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
-                    const uint64_t bd = umma_sdesc(smem_u32(bst + sa * GU_BSTAGE));
 #pragma unroll
-                    for (int k = 0; k < KBLK / 16; ++k)
-                        umma_f16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (kb | k) != 0);
-                    umma_commit(&bars->aempty[sa]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int sa = 2 * pr + h, kb = 2 * kp + h;
+                        const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
+                        const uint64_t bd = umma_sdesc(smem_u32(bst + sa * GU_BSTAGE));
+#pragma unroll
+                        for (int k = 0; k < KBLK / 16; ++k)
+                            umma_f16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (kb | k) != 0);
+                    }
+                    umma_commit(&bars->aempty[pr]);
                 }
                 if (ok) umma_commit(&bars->accfull[buf]);
             }
@@ -414,11 +420,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             bool ok = true;
 #pragma unroll
             for (int c = 0; c < 4; ++c, ++gk) {
-                const int sa = gk % GU_NA;
+                const int sa = gk % GU_NA, pr = (gk >> 1) & 1;
                 Q4Half sc[RPT];
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
-                if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                if (!mbar_wait(&bars->aempty[pr], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 for (int r = 0; r < RPT; ++r) q4_quarter(v[r][c], sc[r], ast + sa * A_STAGE + rowb[r], o_lo, o_hi);
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->afull[sa]);
+                if (lane == 0) mbar_arrive(&bars->afull[pr]);
             }
             if (!ok) break;
             // the raw stage is handed back only now: every value loaded from it
@@ -436,8 +442,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             if (lane == 0) mbar_arrive(&bars->qempty[sq]);
         }
     } else if (warp >= W_EPI) {
-        // epilogue: TMEM lane quarter warp % 4, every column of the item
-        const int lq = warp & 3;
+        // epilogue: TMEM lane quarter warp % 4; the two warps of a quarter take
+        // alternate 16-column chunks
+        const int lq = warp & 3, half = (warp - W_EPI) >> 2;
         int j = 0;
         for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
             const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             const uint32_t d = tmem + (uint32_t)(buf * GU_ACC_COLS) + ((uint32_t)(32 * lq) << 16);
             if (MODE == 0) {
                 const int f = w.f0 + 16 * lq + (lane & 15);
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                for (int c0 = 16 * half; c0 < N; c0 += 32) {
                     float v[16];
                     tmem_ld16(d + (uint32_t)c0, v);
 #pragma unroll
@@ -463,7 +470,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 }
             } else {
                 const int row = p.yoff + w.f0 + 32 * lq + lane;
-                for (int c0 = 0; c0 < N; c0 += 16) {
+                for (int c0 = 16 * half; c0 < N; c0 += 32) {
                     float v[16];
                     tmem_ld16(d + (uint32_t)c0, v);
 #pragma unroll

@@ -35,7 +35,6 @@ namespace {
 
 constexpr int KBLK = 64;                       // k per tensor-core block (128 B of fp16)
 constexpr int TILE_M = 128;
-constexpr int TILE_NMAX = 256;
 constexpr int A_STAGE = TILE_M * KBLK * 2;     // 16 KB fp16 A block
 constexpr int NDQ = 16;                        // dequant / epilogue warps (4 threads per A row)
 constexpr int RPT = 16 / NDQ;                  // A rows per dequant thread
@@ -43,11 +42,6 @@ static_assert(NDQ * RPT == 16 && NDQ % 4 == 0, "128 A rows, 8 per warp per pass"
 constexpr int W_QLOAD = NDQ;                   // weight copies
 constexpr int W_BLOAD = NDQ + 1;               // activation (B) tiles
 constexpr int W_MMA = NDQ + 2;                 // tcgen05.mma issue
-// a whole number of 4-warp groups (one idle warp): warp i of a CTA then sits on
-// SM sub-partition i % 4 however many CTAs share the SM, which the TMEM lane
-// quarter of the epilogue (warp % 4) relies on
-constexpr int PF_THREADS = (NDQ + 4) * 32;
-constexpr uint32_t TMEM_COLS = 256;
 constexpr int NA = 4;                          // A (fp16 weight) stages: the 4 k-blocks of a superblock
 static_assert(NA * KBLK == QK, "one A stage per k-block of a superblock");
 constexpr int NQ = 3;                          // raw Q4_K stages, at most
@@ -71,26 +65,22 @@ static_assert(GU_NQ <= NQ && GU_NA == 4 && GU_NMAX <= GU_ACC_COLS &&
                   W_EPI % 4 == 0,
               "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
-constexpr int NBMAX = 8;                       // B stages, at most
+// down kernel: token-tile rows, A / B stages, TMEM columns (two accumulators)
+constexpr int DN_NMAX = 128;
+constexpr int DN_NA = 2;
+constexpr int DN_BSTAGE = DN_NMAX * KBLK * 2;
+constexpr uint32_t DN_TMEM = 2 * DN_NMAX;
 constexpr int GU_BSTAGE = GU_NMAX * KBLK * 2;  // B stage stride (an item loads nb <= GU_NMAX rows)
 constexpr int B_BYTES_GU = GU_NA * GU_BSTAGE;
-constexpr int B_BYTES_DN = 64 * 1024;
 
 struct PfBars {
-    uint64_t qfull[NQ], qempty[NQ], afull[NA], aempty[NA], bfull[NBMAX], bempty[NBMAX], acc;
+    uint64_t qfull[NQ], qempty[NQ], afull[NA], aempty[NA];
     uint64_t accfull[2], accempty[2];
     uint32_t tmem;
 };
 
-// B stages that fit the region for a token tile of nb rows
-__host__ __device__ inline int b_stages(int b_bytes, int nb) {
-    const int n = b_bytes / (nb * KBLK * 2);
-    return n < NBMAX ? n : NBMAX;
-}
-
-// token-tile height and the matching B tensor map (64 / 128 / 256 rows; the
-// gate/up kernel's largest map is GU_NMAX rows)
-__device__ __forceinline__ int box_rows(int n) { return n <= 64 ? 64 : n <= 128 ? 128 : 256; }
+// token-tile height of the gate/up kernel and the matching B tensor map (64 /
+// 128 / GU_NMAX rows)
 __device__ __forceinline__ int box_rows_gu(int n) { return n <= 64 ? 64 : n <= 128 ? 128 : GU_NMAX; }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -168,18 +158,6 @@ __device__ __forceinline__ void q6_quarter(uint4 ql, uint4 qh, int shl, int shh,
         c[i] = ((l[i] >> shl) & 0x0F0F0F0Fu) | (((hb[i] >> shh) & 0x03030303u) << 4);
     *reinterpret_cast<uint4*>(rb + o0) = codes_to_half8(c[0], c[1], sub, ds, zero);
     *reinterpret_cast<uint4*>(rb + o1) = codes_to_half8(c[2], c[3], sub, ds, zero);
-}
-
-// B stages of a token tile of nb rows, NB deep, for k-blocks 0..NKB-1 (one
-// thread): stage kb % NB is refilled once the MMA has released it.
-__device__ __forceinline__ void load_b_stages(PfBars* bars, uint8_t* bst, int BSTAGE, int NB, int NKB,
-                                              const CUtensorMap* tm, int row0) {
-    for (int kb = 0; kb < NKB; ++kb) {
-        const int st = kb % NB;
-        if (!mbar_wait(&bars->bempty[st], ((uint32_t)(kb / NB) & 1u) ^ 1u)) return;
-        mbar_arrive_expect_tx(&bars->bfull[st], (uint32_t)BSTAGE);
-        tma_load_2d(bst + st * BSTAGE, tm, kb * KBLK, row0, &bars->bfull[st]);
-    }
 }
 
 struct GuParams {
@@ -500,189 +478,277 @@ struct DnParams {
     const int32_t* used_first;
     const uint8_t* down;
     float* y;             // [P][H] fp32, rows in pair-list order
-    int H, F, ntiles, down_t;
+    int H, F, down_t;
 };
 
-// grid (H/128, max_used * ntiles)
-__global__ void __launch_bounds__(PF_THREADS, 1)
+// Persistent down GEMM: one CTA per SM walks the items (token tile of DN_NMAX
+// rows of a used expert, 128-row tile of H), the row tile fastest.  An item's
+// 128 down rows are contiguous in memory (Q6_K rows of F/256 superblocks of
+// 210 bytes have no 16-byte aligned superblock columns, so they cannot be
+// tiled by TMA): one bulk copy of the whole K per item into one of two raw
+// buffers, so the next item's copy runs while this one is dequantised.  A and
+// B k-block stages (DN_NA deep) share one full / empty barrier pair each; two
+// TMEM accumulators; DN epilogue warps write fp32 y rows.  Warps as in the
+// gate/up kernel.
+__global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_down(const __grid_constant__ CUtensorMap tm_a64, const __grid_constant__ CUtensorMap tm_a128,
-                 const __grid_constant__ CUtensorMap tm_a256, const DnParams p) {
+                 const DnParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
-    // 1024-aligned base, kept a shared-space pointer (an integer round trip
-    // would turn every access into a generic one)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
-    const int u = blockIdx.y / p.ntiles, nt = blockIdx.y % p.ntiles;
-    if (u >= *p.n_used) return;
-    const int first = p.used_first[u], cnt = p.used_first[u + 1] - first;
-    const int n0 = nt * TILE_NMAX;
-    if (n0 >= cnt) return;
-    const int n = min(TILE_NMAX, cnt - n0);
-    const int N = (n + 15) & ~15;
-    const int nb = box_rows(n);
-    const CUtensorMap* tmb = nb == 64 ? &tm_a64 : nb == 128 ? &tm_a128 : &tm_a256;
-    const int e = p.used_expert[u];
-    const int h0 = blockIdx.x * TILE_M;
     const int H = p.H, F = p.F;
-    const int NKB = F / KBLK;
+    const int NKB = F / KBLK, NSB = F / QK;
+    const int HT = H / TILE_M;
     const int BB = p.down_t == 1 ? Q4K_BYTES : Q6K_BYTES;
     const int RB = (F / QK) * BB;
     const uint32_t qbytes = (uint32_t)(TILE_M * RB);       // whole K of 128 rows
+    const uint32_t RQ = (qbytes + 1023u) & ~1023u;
 
-    uint8_t* ast = sm;                                    // NA x A_STAGE
-    uint8_t* bst = ast + NA * A_STAGE;                    // B_BYTES_DN
-    uint8_t* qbuf = bst + B_BYTES_DN;                     // qbytes (+ slack)
-    PfBars* bars = reinterpret_cast<PfBars*>(qbuf + ((qbytes + 1023) & ~1023u) + 1024);
-    const int NB = b_stages(B_BYTES_DN, nb);
-    const int BSTAGE = nb * KBLK * 2;
+    uint8_t* qbuf = sm;                                   // 2 x RQ raw buffers
+    uint8_t* ast = sm + 2 * RQ;                           // DN_NA x A_STAGE
+    uint8_t* bst = ast + DN_NA * A_STAGE;                 // DN_NA x DN_BSTAGE
+    PfBars* bars = reinterpret_cast<PfBars*>(bst + DN_NA * DN_BSTAGE);
+    int* tfirst = reinterpret_cast<int*>(bars + 1);       // [n_used + 1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    const int n_used = *p.n_used;
     if (tid == 0) {
-        mbar_init(&bars->qfull[0], 1);
-        for (int i = 0; i < NA; ++i) {
-            mbar_init(&bars->afull[i], NDQ);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->qfull[i], 1);
+            mbar_init(&bars->qempty[i], NDQ);
+            mbar_init(&bars->accfull[i], 1);
+            mbar_init(&bars->accempty[i], GU_NEPI);
+        }
+        for (int i = 0; i < DN_NA; ++i) {
+            mbar_init(&bars->afull[i], NDQ + 1);          // dequant warps + the B copy
             mbar_init(&bars->aempty[i], 1);
         }
-        for (int i = 0; i < NB; ++i) {
-            mbar_init(&bars->bfull[i], 1);
-            mbar_init(&bars->bempty[i], 1);
-        }
-        mbar_init(&bars->acc, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(&bars->tmem, TMEM_COLS);
+    if (warp == W_QLOAD) {
+        // token tiles per used expert, exclusive prefix (one warp)
+        int carry = 0;
+        for (int u0 = 0; u0 < n_used; u0 += 32) {
+            const int u = u0 + lane;
+            const int t = u < n_used ? (p.used_first[u + 1] - p.used_first[u] + DN_NMAX - 1) / DN_NMAX : 0;
+            int incl = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (u < n_used) tfirst[u] = carry + incl - t;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) tfirst[n_used] = carry;
+    }
+    if (warp == 0) tmem_alloc(&bars->tmem, DN_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
+    const int n_items = HT * tfirst[n_used];
+    // item -> (used expert u, token tile, row tile)
+    auto item = [&](int it, int& e, int& first, int& n0, int& n, int& h0) {
+        const int tt = it / HT;
+        h0 = (it - tt * HT) * TILE_M;
+        int lo = 0, hi = n_used - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tfirst[mid] <= tt) lo = mid;
+            else hi = mid - 1;
+        }
+        e = p.used_expert[lo];
+        first = p.used_first[lo];
+        n0 = (tt - tfirst[lo]) * DN_NMAX;
+        n = min(DN_NMAX, p.used_first[lo + 1] - first - n0);
+    };
 
     if (warp == W_QLOAD) {
-        // the whole K of this CTA's 128 down rows: one bulk copy
         if (lane == 0) {
-            const uint8_t* src = p.down + (size_t)e * H * RB + (size_t)h0 * RB;
-            mbar_arrive_expect_tx(&bars->qfull[0], qbytes);
-            bulk_g2s(qbuf, src, qbytes, &bars->qfull[0]);
+            int j = 0;
+            for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+                int e, first, n0, n, h0;
+                item(it, e, first, n0, n, h0);
+                const int rb = j & 1;
+                if (!mbar_wait(&bars->qempty[rb], ((uint32_t)(j >> 1) & 1u) ^ 1u)) break;
+                mbar_arrive_expect_tx(&bars->qfull[rb], qbytes);
+                bulk_g2s(qbuf + rb * RQ, p.down + (size_t)e * H * RB + (size_t)h0 * RB, qbytes, &bars->qfull[rb]);
+            }
         }
     } else if (warp == W_BLOAD) {
-        if (lane == 0) load_b_stages(bars, bst, BSTAGE, NB, NKB, tmb, first + n0);
+        if (lane == 0) {
+            int gk = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                int e, first, n0, n, h0;
+                item(it, e, first, n0, n, h0);
+                const int nb = n <= 64 ? 64 : 128;
+                const CUtensorMap* tmb = nb == 64 ? &tm_a64 : &tm_a128;
+                for (int kb = 0; kb < NKB; ++kb, ++gk) {
+                    const int st = gk % DN_NA;
+                    if (!mbar_wait(&bars->aempty[st], ((uint32_t)(gk / DN_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->afull[st], (uint32_t)(nb * KBLK * 2));
+                    tma_load_2d(bst + st * DN_BSTAGE, tmb, kb * KBLK, first + n0, &bars->afull[st]);
+                }
+            }
+        }
     } else if (warp == W_MMA) {
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16(TILE_M, N);
-            for (int kb = 0; kb < NKB; ++kb) {
-                const int sa = kb % NA, sb = kb % NB;
-                if (!mbar_wait(&bars->afull[sa], (uint32_t)(kb / NA) & 1u) ||
-                    !mbar_wait(&bars->bfull[sb], (uint32_t)(kb / NB) & 1u))
-                    break;
+            int gk = 0, j = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++j) {
+                int e, first, n0, n, h0;
+                item(it, e, first, n0, n, h0);
+                const int buf = j & 1;
+                if (!mbar_wait(&bars->accempty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u)) break;
                 tc_fence_after();
-                const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
-                const uint64_t bd = umma_sdesc(smem_u32(bst + sb * BSTAGE));
+                const uint32_t d = tmem + (uint32_t)(buf * DN_NMAX);
+                const uint32_t idesc = umma_idesc_f16(TILE_M, (n + 15) & ~15);
+                for (int kb = 0; kb < NKB; ++kb, ++gk) {
+                    const int sa = gk % DN_NA;
+                    if (!mbar_wait(&bars->afull[sa], (uint32_t)(gk / DN_NA) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = umma_sdesc(smem_u32(ast + sa * A_STAGE));
+                    const uint64_t bd = umma_sdesc(smem_u32(bst + sa * DN_BSTAGE));
 #pragma unroll
-                for (int k = 0; k < KBLK / 16; ++k)
-                    umma_f16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc,
-                             (kb | k) != 0);
-                umma_commit(&bars->aempty[sa]);
-                umma_commit(&bars->bempty[sb]);
+                    for (int k = 0; k < KBLK / 16; ++k)
+                        umma_f16(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (kb | k) != 0);
+                    umma_commit(&bars->aempty[sa]);
+                }
+                if (ok) umma_commit(&bars->accfull[buf]);
             }
-            umma_commit(&bars->acc);
         }
     } else if (warp < NDQ) {
         // thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r), 16-k quarter
         // qq = lane >> 3 of every k-block; all warps fill each A stage in turn
-        // (NA = the 4 k-blocks of a superblock)
         const int qq = lane >> 3, sw = lane & 7;                 // row % 8 == lane % 8
-        mbar_wait(&bars->qfull[0], 0);
-        const uint8_t* rowp[RPT];
-        int rowb[RPT];
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int rowo[RPT], rowb[RPT];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int row = 8 * warp + (lane & 7) + 8 * NDQ * r;
-            rowp[r] = qbuf + (size_t)row * RB;
+            rowo[r] = row * RB;
             rowb[r] = row * 128;
         }
-        for (int sb = 0; sb < NKB / NA; ++sb) {
-            const uint32_t apar = ((uint32_t)sb & 1u) ^ 1u;
-            if (p.down_t == 2) {
-                // k-block qb = 2n + par is half n, groups g = 2 par + h (h = qq >> 1),
-                // positions 16(qq & 1) .. + 15: the same ql / qh bytes serve par 0 and 1
-                const int h = qq >> 1, hq = qq & 1;
-                const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
-                float d[RPT];
-                uint32_t scv[RPT][4];
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    const uint8_t* blk = rowp[r] + sb * Q6K_BYTES;
-                    d[r] = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-                    const uint4 scw = lds16(blk + 192);
-                    scv[r][0] = scw.x;
-                    scv[r][1] = scw.y;
-                    scv[r][2] = scw.z;
-                    scv[r][3] = scw.w;
-                }
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    uint4 ql[RPT], qh[RPT];
+        int gk = 0;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            const int rb = j & 1;
+            if (!mbar_wait(&bars->qfull[rb], (uint32_t)(j >> 1) & 1u)) break;
+            const uint8_t* qb0 = qbuf + rb * RQ;
+            for (int sb = 0; ok && sb < NSB; ++sb) {
+                if (p.down_t == 2) {
+                    // k-block 2n + par of the superblock is half n, groups g = 2 par + h
+                    // (h = qq >> 1), positions 16(qq & 1) .. + 15: the same ql / qh
+                    // bytes serve par 0 and 1
+                    const int h = qq >> 1, hq = qq & 1;
+                    const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+                    float d[RPT];
+                    uint32_t scv[RPT][4];
 #pragma unroll
                     for (int r = 0; r < RPT; ++r) {
-                        const uint8_t* blk = rowp[r] + sb * Q6K_BYTES;
-                        ql[r] = lds16(blk + 64 * n + 32 * h + 16 * hq);
-                        qh[r] = lds16(blk + 128 + 32 * n + 16 * hq);
+                        const uint8_t* blk = qb0 + rowo[r] + sb * Q6K_BYTES;
+                        d[r] = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                        const uint4 scw = lds16(blk + 192);
+                        scv[r][0] = scw.x;
+                        scv[r][1] = scw.y;
+                        scv[r][2] = scw.z;
+                        scv[r][3] = scw.w;
                     }
 #pragma unroll
-                    for (int par = 0; par < 2; ++par) {
-                        const int qb = 2 * n + par;
-                        mbar_wait(&bars->aempty[qb], apar);
+                    for (int n = 0; n < 2; ++n) {
+                        uint4 ql[RPT], qh[RPT];
 #pragma unroll
                         for (int r = 0; r < RPT; ++r) {
-                            // scale byte 8n + 2g + hq = 8n + 4 par + qq: word 2n + par, byte qq
-                            const int sc = (int)(scv[r][2 * n + par] << (24 - 8 * qq)) >> 24;
-                            q6_quarter(ql[r], qh[r], 4 * par, 4 * par + 2 * h, __float2half2_rn(d[r] * (float)sc),
-                                       ast + qb * A_STAGE + rowb[r], o0, o1);
+                            const uint8_t* blk = qb0 + rowo[r] + sb * Q6K_BYTES;
+                            ql[r] = lds16(blk + 64 * n + 32 * h + 16 * hq);
+                            qh[r] = lds16(blk + 128 + 32 * n + 16 * hq);
                         }
+#pragma unroll
+                        for (int par = 0; par < 2; ++par, ++gk) {
+                            const int sa = gk % DN_NA;
+                            if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / DN_NA) & 1u) ^ 1u)) {
+                                ok = false;
+                                break;
+                            }
+#pragma unroll
+                            for (int r = 0; r < RPT; ++r) {
+                                // scale byte 8n + 2g + hq = 8n + 4 par + qq: word 2n + par, byte qq
+                                const int sc = (int)(scv[r][2 * n + par] << (24 - 8 * qq)) >> 24;
+                                q6_quarter(ql[r], qh[r], 4 * par, 4 * par + 2 * h,
+                                           __float2half2_rn(d[r] * (float)sc), ast + sa * A_STAGE + rowb[r], o0, o1);
+                            }
+                            fence_proxy_async();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&bars->afull[sa]);
+                        }
+                        if (!ok) break;
+                    }
+                } else {
+                    const int o_lo = (qq ^ sw) << 4, o_hi = ((qq + 4) ^ sw) << 4;
+                    Q4Half own[RPT];
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r)
+                        own[r] = q4_half_scales(*reinterpret_cast<const uint4*>(qb0 + rowo[r] + sb * Q4K_BYTES), qq);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c, ++gk) {
+                        const int sa = gk % DN_NA;
+                        uint2 v[RPT];
+                        Q4Half sc[RPT];
+#pragma unroll
+                        for (int r = 0; r < RPT; ++r) {
+                            v[r] = *reinterpret_cast<const uint2*>(qb0 + rowo[r] + sb * Q4K_BYTES + 16 + 32 * c + 8 * qq);
+                            sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
+                        }
+                        if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / DN_NA) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int r = 0; r < RPT; ++r) q4_quarter(v[r], sc[r], ast + sa * A_STAGE + rowb[r], o_lo, o_hi);
                         fence_proxy_async();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&bars->afull[qb]);
+                        if (lane == 0) mbar_arrive(&bars->afull[sa]);
                     }
-                }
-            } else {
-                const int o_lo = (qq ^ sw) << 4, o_hi = ((qq + 4) ^ sw) << 4;
-                Q4Half own[RPT];
-#pragma unroll
-                for (int r = 0; r < RPT; ++r)
-                    own[r] = q4_half_scales(*reinterpret_cast<const uint4*>(rowp[r] + sb * Q4K_BYTES), qq);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint2 v[RPT];
-                    Q4Half sc[RPT];
-#pragma unroll
-                    for (int r = 0; r < RPT; ++r) {
-                        v[r] = *reinterpret_cast<const uint2*>(rowp[r] + sb * Q4K_BYTES + 16 + 32 * c + 8 * qq);
-                        sc[r] = shfl_half(own[r], (lane & 7) + 8 * c);
-                    }
-                    mbar_wait(&bars->aempty[c], apar);
-#pragma unroll
-                    for (int r = 0; r < RPT; ++r) q4_quarter(v[r], sc[r], ast + c * A_STAGE + rowb[r], o_lo, o_hi);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->afull[c]);
                 }
             }
+            // every value read from this raw buffer has fed a store above
+            if (ok && lane == 0) mbar_arrive(&bars->qempty[rb]);
         }
-        mbar_wait(&bars->acc, 0);
-        tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2, cpw = 1024 / NDQ;   // columns per warp
-        const int hrow = h0 + 32 * lq + lane;
-        for (int c0 = ch * cpw; c0 < min(N, ch * cpw + cpw); c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * lq) << 16) + (uint32_t)c0, v);
+    } else if (warp >= W_EPI) {
+        const int lq = warp & 3, half = (warp - W_EPI) >> 2;
+        int j = 0;
+        for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+            int e, first, n0, n, h0;
+            item(it, e, first, n0, n, h0);
+            const int buf = j & 1, N = (n + 15) & ~15;
+            if (!mbar_wait(&bars->accfull[buf], (uint32_t)(j >> 1) & 1u)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(buf * DN_NMAX) + ((uint32_t)(32 * lq) << 16);
+            const int hrow = h0 + 32 * lq + lane;
+            for (int c0 = 16 * half; c0 < N; c0 += 32) {
+                float v[16];
+                tmem_ld16(d + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int col = c0 + j;
-                if (col < n) p.y[(size_t)(first + n0 + col) * H + hrow] = v[j];
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int col = c0 + jj;
+                    if (col < n) p.y[(size_t)(first + n0 + col) * H + hrow] = v[jj];
+                }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->accempty[buf]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 0) tmem_dealloc(tmem, DN_TMEM);
 }
 
 // x rows of every pair, in pair-list order, as fp16; inverse pair -> position map
@@ -769,10 +835,10 @@ int sm_count() {
     return n;
 }
 
-size_t dn_smem(int F, int down_t) {
+size_t dn_smem(int F, int down_t, int E) {
     const size_t rb = (size_t)(F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
     const size_t q = (TILE_M * rb + 1023) & ~size_t(1023);
-    return 1024 + NA * A_STAGE + B_BYTES_DN + q + 1024 + sizeof(PfBars) + 64;
+    return 1024 + 2 * q + DN_NA * A_STAGE + DN_NA * DN_BSTAGE + sizeof(PfBars) + sizeof(int) * (E + 1) + 64;
 }
 
 }  // namespace
@@ -780,7 +846,7 @@ size_t dn_smem(int F, int down_t) {
 bool prefill_supported(const MoeShape& s, int gate_t, int up_t, int down_t) {
     if (gate_t != 1 || up_t != 1) return false;
     if (s.H % QK || s.F % QK || s.H % TILE_M || s.F % 64) return false;
-    return dn_smem(s.F, down_t) <= 227 * 1024 && GU_SMEM <= 227 * 1024 && encode_fn() != nullptr;
+    return dn_smem(s.F, down_t, s.E) <= 227 * 1024 && GU_SMEM <= 227 * 1024 && encode_fn() != nullptr;
 }
 
 cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
@@ -788,21 +854,18 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
                            const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
                            float* out, cudaStream_t st) {
     const int P = s.T * s.K;
-    const int max_used = P < s.E ? P : s.E;
-    // an expert sees each token once at most
-    const int ntiles = (s.T + TILE_NMAX - 1) / TILE_NMAX;
     gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tg, tu, tx64, tx128, txg, ta64, ta128, ta256;
+    CUtensorMap tg, tu, tx64, tx128, txg, ta64, ta128;
     const uint64_t rbg = (uint64_t)(s.H / QK) * Q4K_BYTES;
     // B maps: boxes of 64 / 128 / 256 token rows
     if (!map_bytes(&tg, gate, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_bytes(&tu, up, rbg, (uint64_t)s.E * s.F, Q4K_BYTES, 64) ||
         !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
         !map_half(&txg, xp, s.H, P, GU_NMAX) || !map_half(&ta64, actp, s.F, P, 64) ||
-        !map_half(&ta128, actp, s.F, P, 128) || !map_half(&ta256, actp, s.F, P, 256))
+        !map_half(&ta128, actp, s.F, P, 128))
         return cudaErrorInvalidValue;
 
     static bool attr_set = false;
@@ -819,9 +882,8 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     prefill_gateup<0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128, txg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, ntiles, down_t};
-    prefill_down<<<dim3(s.H / TILE_M, max_used * ntiles), PF_THREADS, dn_smem(s.F, down_t), st>>>(
-        ta64, ta128, ta256, dp);
+    DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t};
+    prefill_down<<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g3((s.H + 255) / 256, s.T);

@@ -181,9 +181,10 @@ constexpr int RG_T = 64, RG_E = 64, RG_K = 128;    // router tile: tokens x expe
 constexpr int RG_THREADS = 256;                    // 4 tokens x 4 experts per thread
 constexpr int RG_LD = RG_K + 4;                    // padded smem row (floats)
 
-// Split-k router GEMM: part[z][t][e] = sum over k in slice z of X[t][k] Wr[e][k].
-// Slices are summed in a fixed order by topk_rank, so the result is deterministic.
-// Grid (ceil(E/64), ceil(T/64), H/128); H is a multiple of 128.
+// Split-k router GEMM: part[z][t][e] = sum over k in slice z of X[t][k] Wr[e][k],
+// a slice being KS = H / gridDim.z columns (a multiple of RG_K) walked in chunks
+// of RG_K.  Slices are summed in a fixed order by topk_rank, so the result is
+// deterministic.  Grid (ceil(E/64), ceil(T/64), S).
 __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restrict__ x,
                                                           const float* __restrict__ wr, int T,
                                                           int H, int E,
@@ -192,7 +193,8 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
     extern __shared__ float4 rg_smem4[];
     float* xs = reinterpret_cast<float*>(rg_smem4);              // [RG_T][RG_LD]
     float* ws = xs + RG_T * RG_LD;                               // [RG_E][RG_LD]
-    const int e0 = blockIdx.x * RG_E, t0 = blockIdx.y * RG_T, k0 = blockIdx.z * RG_K;
+    const int KS = H / gridDim.z;
+    const int e0 = blockIdx.x * RG_E, t0 = blockIdx.y * RG_T;
     const int tid = threadIdx.x;
     // the token bitmap and counts that topk_rank fills start from zero
     {
@@ -200,6 +202,9 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
         const int b = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
         for (int i = b * RG_THREADS + tid; i < nclear; i += nb * RG_THREADS) clear[i] = 0u;
     }
+    const int tx = tid & 15, ty = tid >> 4;      // experts tx + 16j, tokens ty + 16i
+    float acc[4][4] = {};
+    for (int k0 = blockIdx.z * KS; k0 < (blockIdx.z + 1) * KS; k0 += RG_K) {
     // 64 rows x 32 float4 per operand, 8 float4 per thread each, all in flight
     float4 vx[8], vw[8];
 #pragma unroll
@@ -210,6 +215,7 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
         vw[i] = e0 + r < E ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + r) * H + k0 + c))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    __syncthreads();                             // the previous chunk is consumed
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int f = tid + i * RG_THREADS, r = f >> 5, c = (f & 31) * 4;
@@ -217,8 +223,6 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
         *reinterpret_cast<float4*>(ws + r * RG_LD + c) = vw[i];
     }
     __syncthreads();
-    const int tx = tid & 15, ty = tid >> 4;      // experts tx + 16j, tokens ty + 16i
-    float acc[4][4] = {};
 #pragma unroll 4
     for (int k = 0; k < RG_K; k += 4) {
         float4 a[4], w[4];
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
                 acc[i][j] = fmaf(a[i].z, w[j].z, acc[i][j]);
                 acc[i][j] = fmaf(a[i].w, w[j].w, acc[i][j]);
             }
+    }
     }
     float* dst = part + (size_t)blockIdx.z * T * E;
 #pragma unroll
@@ -285,16 +290,24 @@ __global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part,
             }
         }
     }
-    if (lane < 16) reinterpret_cast<int*>(l + E)[lane] = 0;
     __syncwarp();
-    for (int e = lane; e < E; e += 32) {
-        const int v = order_key(l[e]);
-        int rank = 0;
-        for (int e2 = 0; e2 < E; ++e2) {
-            const int w = order_key(l[e2]);
-            rank += (w > v) || (w == v && e2 < e);
+    // K rounds of a warp arg-max over 64-bit keys (order key of the logit, then
+    // E - 1 - e): round r takes the largest key below round r - 1's, which is
+    // the r-th logit in descending order, ties to the lower index
+    long long prev = LLONG_MAX;
+    for (int r = 0; r < K; ++r) {
+        long long best = LLONG_MIN;
+        for (int e = lane; e < E; e += 32) {
+            const long long key = (long long)order_key(l[e]) * 4294967296LL + (long long)(E - 1 - e);
+            if (key < prev && key > best) best = key;
         }
-        if (rank < K) sel[rank] = e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            if (other > best) best = other;
+        }
+        if (lane == 0) sel[r] = E - 1 - (int)(best & 0xffffffffLL);
+        prev = best;
     }
     __syncwarp();
     const float vmax = l[sel[0]];
@@ -408,16 +421,26 @@ __global__ void __launch_bounds__(EL_THREADS) expert_lists(const uint8_t* __rest
 
 }  // namespace
 
+// k-slices of the router GEMM: as few as keep about 300 CTAs busy (fewer
+// partial sums to write and read back), each a whole number of RG_K chunks
+int route_many_slices(int T, int H, int E) {
+    const int tiles = ((E + RG_E - 1) / RG_E) * ((T + RG_T - 1) / RG_T);
+    int S = H / RG_K;
+    while (S % 2 == 0 && tiles * (S / 2) >= 300) S /= 2;
+    return S;
+}
+
 cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* router_w,
                               const float* bias, const Route& r, cudaStream_t st) {
     const size_t rg_smem = sizeof(float) * (RG_T + RG_E) * RG_LD;
-    dim3 g1((s.E + RG_E - 1) / RG_E, (s.T + RG_T - 1) / RG_T, s.H / RG_K);
+    const int S = route_many_slices(s.T, s.H, s.E);
+    dim3 g1((s.E + RG_E - 1) / RG_E, (s.T + RG_T - 1) / RG_T, S);
     const int W = (s.T + 31) / 32;
     uint32_t* counts = r.tokmap + (size_t)s.E * W;      // E counters after the bitmap
     router_gemm<<<g1, RG_THREADS, rg_smem, st>>>(x, router_w, s.T, s.H, s.E, r.logits_part, r.tokmap,
                                                  s.E * W + s.E);
     topk_rank<<<(s.T + 7) / 8, 256, sizeof(float) * 8 * (s.E + 16), st>>>(
-        r.logits_part, s.H / RG_K, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.tokmap,
+        r.logits_part, S, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.tokmap,
         reinterpret_cast<int32_t*>(counts), r.jmap);
     expert_lists<<<s.E, EL_THREADS, sizeof(uint32_t) * 2 * W, st>>>(
         r.jmap, r.tokmap, reinterpret_cast<const int32_t*>(counts), s.T, s.E, s.K, r.n_used, r.used_expert,
@@ -425,6 +448,8 @@ cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* ro
     return cudaGetLastError();
 }
 
+// workspace for the partial sums of any call with up to T tokens (a call with
+// fewer tokens may use more slices, never more than H / RG_K)
 size_t route_many_part_floats(int T, int H, int E) { return (size_t)(H / RG_K) * T * E; }
 
 size_t route_many_tokmap_words(int T, int E) { return (size_t)E * ((T + 31) / 32) + E; }

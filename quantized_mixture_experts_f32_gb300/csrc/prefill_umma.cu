@@ -767,16 +767,25 @@ __global__ void gather_x_f16(const float* __restrict__ x, const int32_t* __restr
 }
 
 // out[t][h] = res[t][h] + sum_j w[t][j] * y[pos(t,j)][h], slot order j = 0..K-1
+// (four consecutive h per thread; every element is read and written by the
+// same thread, so out may alias res)
 __global__ void combine_pairs(const float* __restrict__ y, const int32_t* __restrict__ inv_pos,
                               const float* __restrict__ wts, const float* res, int H, int K,
                               float* out) {
     const int t = blockIdx.y;
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= H) return;
-    float acc = res[(size_t)t * H + h];
-    for (int j = 0; j < K; ++j)
-        acc = fmaf(wts[t * K + j], y[(size_t)inv_pos[t * K + j] * H + h], acc);
-    out[(size_t)t * H + h] = acc;
+    const int h4 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (4 * h4 >= H) return;
+    const int H4 = H / 4;
+    float4 acc = reinterpret_cast<const float4*>(res)[(size_t)t * H4 + h4];
+    for (int j = 0; j < K; ++j) {
+        const float w = wts[t * K + j];
+        const float4 v = reinterpret_cast<const float4*>(y)[(size_t)inv_pos[t * K + j] * H4 + h4];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(out)[(size_t)t * H4 + h4] = acc;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -886,7 +895,7 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     prefill_down<<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    dim3 g3((s.H + 255) / 256, s.T);
+    dim3 g3((s.H / 4 + 255) / 256, s.T);
     combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
     return cudaGetLastError();
 }

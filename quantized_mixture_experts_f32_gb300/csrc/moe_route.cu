@@ -421,12 +421,13 @@ __global__ void __launch_bounds__(EL_THREADS) expert_lists(const uint8_t* __rest
 
 }  // namespace
 
-// k-slices of the router GEMM: as few as keep about 300 CTAs busy (fewer
-// partial sums to write and read back), each a whole number of RG_K chunks
+// k-slices of the router GEMM: as few as keep about eight CTAs per SM in
+// flight (each CTA loads its chunks and computes them in turn, so fewer, longer
+// CTAs expose the load latency), each a whole number of RG_K chunks
 int route_many_slices(int T, int H, int E) {
     const int tiles = ((E + RG_E - 1) / RG_E) * ((T + RG_T - 1) / RG_T);
     int S = H / RG_K;
-    while (S % 2 == 0 && tiles * (S / 2) >= 300) S /= 2;
+    while (S % 2 == 0 && tiles * (S / 2) >= 1200) S /= 2;
     return S;
 }
 

@@ -27,8 +27,12 @@
 
 #include "kquant.cuh"
 #include "qmoe_internal.h"
+#include "umma.cuh"
 
 namespace qmoe {
+
+// 2-D fp16 tensor map, box 64 columns x box_rows rows, 128B swizzle (prefill_umma.cu)
+bool tensor_map_half(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
 
 namespace {
 
@@ -63,6 +67,25 @@ __global__ void __launch_bounds__(NR_THREADS) rmsnorm_rows(const float* __restri
     }
 }
 
+// the O projection split over K in two planes: h = h + p0 + p1 (in place),
+// then out = RMSNorm(h) * w (fp32), one block per token row
+__global__ void __launch_bounds__(NR_THREADS) residual_rmsnorm_rows(float* __restrict__ h,
+                                                                    const float* __restrict__ p0,
+                                                                    const float* __restrict__ p1,
+                                                                    const float* __restrict__ w, float eps,
+                                                                    int H, float* __restrict__ out) {
+    __shared__ float red[NR_THREADS / 32];
+    const size_t base = (size_t)blockIdx.x * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < H; i += NR_THREADS) {
+        const float v = (h[base + i] + p0[base + i]) + p1[base + i];
+        h[base + i] = v;
+        ss = fmaf(v, v, ss);
+    }
+    const float r = rsqrtf(block_sum_256(ss, red) / (float)H + eps);
+    for (int i = threadIdx.x; i < H; i += NR_THREADS) out[base + i] = h[base + i] * r * w[i];
+}
+
 // cos/sin of the NEOX RoPE angle of pair j at position pos: the angle
 // pos * base^(-2j/hd) is formed and reduced to [-pi, pi] in double (inv_freq
 // from the host, double), cos and sin taken in float
@@ -82,8 +105,8 @@ __device__ __forceinline__ float2 rope_cs(const double* __restrict__ inv_freq, i
 __global__ void __launch_bounds__(128) qk_norm_rope_append(
     const float* __restrict__ qkv, int nq, int nkv, int hd, const float* __restrict__ q_norm,
     const float* __restrict__ k_norm, float eps, const double* __restrict__ inv_freq, int pos0,
-    int max_ctx, float* __restrict__ qr, __half* __restrict__ k_cache, __half* __restrict__ v_cache,
-    int T) {
+    int max_ctx, float* __restrict__ qr, __half* __restrict__ qh, __half* __restrict__ k_cache,
+    __half* __restrict__ v_cache, int T) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x, hh = blockIdx.y * 4 + warp;
     if (t >= T || hh >= nq + nkv) return;
@@ -116,7 +139,15 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append(
             o[i + n / 2] = b * cs.x + a * cs.y;
         }
     }
-    if (isq) {
+    if (isq && qh) {
+        // fp16 rows for the tensor-core attention: [kv group][token][head of
+        // the group][hd], so a block's (token, head) rows are contiguous
+        const int group = nq / nkv, gq = hh / group, hq = hh - gq * group;
+        __half* dq = qh + (((size_t)gq * T + t) * group + hq) * hd;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < n) dq[lane + 32 * i] = __float2half_rn(o[i]);
+    } else if (isq) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             if (i < n) qr[(size_t)t * qd + hh * hd + lane + 32 * i] = o[i];
@@ -252,6 +283,224 @@ __global__ void __launch_bounds__(PA_THREADS) prefill_attention(
     }
 }
 
+// Causal GQA attention on the tensor cores.  CTA = (kv head g, 128 / group
+// tokens): its 128 query rows (token, head of the group) against key chunks of
+// 128 positions, two passes over the chunks.  Pass 1: S = Q K^T (tcgen05, fp32
+// in TMEM), each thread holds one row (its TMEM lane) and keeps the running
+// maximum and sum of exponentials of its visible scores.  Pass 2: S again,
+// P = exp(s - max) / sum as fp16 into shared memory (128B-swizzled, K-major),
+// V^T of the chunk staged by the threads in the same layout, O += P V^T in
+// TMEM.  Two passes instead of rescaling O on every new maximum keep the
+// accumulator in TMEM untouched until the end.  Epilogue: O rows -> fp16 att.
+// Masking: key p is visible to the row of token t when p <= pos0 + t; keys past
+// the block's last visible key are not read (their V^T columns are zero).
+// One thread (tid 0) issues the TMA copies and MMAs; 128 threads.
+constexpr int PT_THREADS = 128;
+constexpr int PT_KC = 128;                                 // keys per chunk
+
+__device__ __forceinline__ uint32_t h2_pack(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __half* __restrict__ v_cache, int nq, int nkv, int hd, int pos0, int max_ctx, int T,
+    __half* __restrict__ att, int* __restrict__ status) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    const int group = nq / nkv, QB = 128 / group;          // tokens per CTA
+    const int g = blockIdx.x, t0 = blockIdx.y * QB;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int nkb = hd / 64;                               // 64-wide k-blocks of hd
+    uint8_t* sQ = sm;                                      // nkb x 16 KB (128 rows)
+    uint8_t* sK = sQ + nkb * 16384;                        // nkb x 16 KB (128 keys)
+    uint8_t* sP = sK + nkb * 16384;                        // 2 x 16 KB (128 rows x 128 keys)
+    uint8_t* sV = sP + 2 * 16384;                          // 2 x (hd x 128 B): V^T, keys = K
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * hd * 128);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    uint64_t* tma_bar = bars;
+    uint64_t* mma_bar = bars + 1;
+    uint64_t* q_bar = bars + 2;
+    const int t_last = min(t0 + QB, T) - 1;                // last token of the block
+    const int kend = pos0 + t_last + 1;                    // keys the block sees
+    const int nchunks = (kend + PT_KC - 1) / PT_KC;
+    // this thread's query row
+    const int tl = tid / group, t = t0 + tl;
+    const int kmax = pos0 + t;                             // last key of this row
+    const float sl2 = rsqrtf((float)hd) * 1.4426950408889634f;   // scale * log2(e)
+
+    if (tid == 0) {
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        mbar_init(q_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tO = tmem + 128;             // columns: S [0,128), O [128, 128 + hd)
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    uint32_t tpar = 0, mpar = 0;
+    bool ok = true;
+
+    // Q rows of the block, one TMA box per 64-wide k-block
+    if (tid == 0) {
+        mbar_arrive_expect_tx(q_bar, (uint32_t)(nkb * 16384));
+        for (int kb = 0; kb < nkb; ++kb)
+            tma_load_2d(sQ + kb * 16384, &tm_q, kb * 64, (g * T + t0) * group, q_bar);
+        if (!mbar_wait(q_bar, 0)) ok = false;
+    }
+    // No thread leaves an iteration early: a failed wait only clears ok, and
+    // every iteration starts with a block-wide vote, so all threads stop at the
+    // same point and every barrier is reached by all of them.
+    float m = -INFINITY, l = 0.f;
+    for (int pass = 0; pass < 2; ++pass) {
+        bool stop = false;
+        for (int c = 0; c < nchunks; ++c) {
+            if (!__syncthreads_and(ok)) {
+                ok = false;
+                stop = true;
+                break;
+            }
+            const int k0 = c * PT_KC;
+            if (tid == 0) {
+                // K chunk (the previous chunk's MMAs have completed: every thread
+                // waited for them before the vote that starts the iteration)
+                mbar_arrive_expect_tx(tma_bar, (uint32_t)(nkb * 16384));
+                for (int kb = 0; kb < nkb; ++kb)
+                    tma_load_2d(sK + kb * 16384, &tm_k, kb * 64, g * max_ctx + k0, tma_bar);
+                if (!mbar_wait(tma_bar, tpar)) ok = false;
+                tpar ^= 1u;
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t idesc = umma_idesc_f16(128, PT_KC);
+                    for (int ks = 0; ks < hd / 16; ++ks) {
+                        const uint64_t ad = umma_sdesc(smem_u32(sQ + (ks >> 2) * 16384)) + (uint64_t)(2 * (ks & 3));
+                        const uint64_t bd = umma_sdesc(smem_u32(sK + (ks >> 2) * 16384)) + (uint64_t)(2 * (ks & 3));
+                        umma_f16(tS, ad, bd, idesc, ks != 0);
+                    }
+                    umma_commit(mma_bar);
+                }
+            }
+            if (pass == 1) {
+                // V^T of the chunk: thread -> key pair (2 i, 2 i + 1), half of hd
+                const int i = tid & 63, dh = tid >> 6, kk = 2 * i;
+                const int half_d = hd / 2;
+                for (int d0 = dh * half_d; d0 < dh * half_d + half_d; d0 += 8) {
+                    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+                    if (k0 + kk < kend)
+                        a = *reinterpret_cast<const uint4*>(v_cache + ((size_t)g * max_ctx + k0 + kk) * hd + d0);
+                    if (k0 + kk + 1 < kend)
+                        b = *reinterpret_cast<const uint4*>(v_cache + ((size_t)g * max_ctx + k0 + kk + 1) * hd + d0);
+                    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+                    uint8_t* reg = sV + (kk >> 6) * (hd * 128);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        // halves d0 + 2q (low) and d0 + 2q + 1 (high) of keys kk, kk + 1
+                        const uint32_t lo = __byte_perm(aw[q], bw[q], 0x5410);
+                        const uint32_t hi = __byte_perm(aw[q], bw[q], 0x7632);
+                        *reinterpret_cast<uint32_t*>(reg + sw128_offset(d0 + 2 * q, kk & 63)) = lo;
+                        *reinterpret_cast<uint32_t*>(reg + sw128_offset(d0 + 2 * q + 1, kk & 63)) = hi;
+                    }
+                }
+            }
+            if (!mbar_wait(mma_bar, mpar)) ok = false;
+            mpar ^= 1u;
+            tc_fence_after();
+            // this row's 128 scores, 16 at a time
+            float cm = -INFINITY;
+            float sv[PT_KC];
+#pragma unroll
+            for (int j0 = 0; j0 < PT_KC; j0 += 16) {
+                float v16[16];
+                tmem_ld16(tS + lane_off + (uint32_t)j0, v16);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float s2 = k0 + j0 + j <= kmax ? v16[j] * sl2 : -INFINITY;
+                    sv[j0 + j] = s2;
+                    cm = fmaxf(cm, s2);
+                }
+            }
+            if (pass == 0) {
+                if (cm > -INFINITY) {
+                    const float mn = fmaxf(m, cm);
+                    float sum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < PT_KC; ++j) sum += exp2f(sv[j] - mn);
+                    l = l * exp2f(m - mn) + sum;
+                    m = mn;
+                }
+            } else {
+                // P row -> fp16, 128B-swizzled K-major, two 64-key k-blocks
+                const float inv = 1.f / l;
+                uint8_t* prow = sP;
+#pragma unroll
+                for (int j0 = 0; j0 < PT_KC; j0 += 8) {
+                    uint4 w;
+                    w.x = h2_pack(exp2f(sv[j0 + 0] - m) * inv, exp2f(sv[j0 + 1] - m) * inv);
+                    w.y = h2_pack(exp2f(sv[j0 + 2] - m) * inv, exp2f(sv[j0 + 3] - m) * inv);
+                    w.z = h2_pack(exp2f(sv[j0 + 4] - m) * inv, exp2f(sv[j0 + 5] - m) * inv);
+                    w.w = h2_pack(exp2f(sv[j0 + 6] - m) * inv, exp2f(sv[j0 + 7] - m) * inv);
+                    *reinterpret_cast<uint4*>(prow + (j0 >> 6) * 16384 + sw128_offset(tid, j0 & 63)) = w;
+                }
+                fence_proxy_async();
+            }
+            tc_fence_before();
+            __syncthreads();
+            if (pass == 1 && tid == 0 && ok) {
+                // O += P V^T over the chunk's 128 keys
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_f16(128, hd);
+                for (int ks = 0; ks < PT_KC / 16; ++ks) {
+                    const uint64_t ad = umma_sdesc(smem_u32(sP + (ks >> 2) * 16384)) + (uint64_t)(2 * (ks & 3));
+                    const uint64_t bd = umma_sdesc(smem_u32(sV + (ks >> 2) * (hd * 128))) + (uint64_t)(2 * (ks & 3));
+                    umma_f16(tO, ad, bd, idesc, (c | ks) != 0);
+                }
+                umma_commit(mma_bar);
+            }
+            if (pass == 1) {
+                // P and V^T are reused by the next chunk: wait for this chunk's MMAs
+                if (!mbar_wait(mma_bar, mpar)) ok = false;
+                mpar ^= 1u;
+            }
+        }
+        if (stop) break;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && tid == 0) atomicExch(status, ST_TIMEOUT);
+    if (ok) {
+        tc_fence_after();
+        // O row -> fp16 att[t][h * hd + d], h = g * group + (row % group)
+        const int h = g * group + (tid - tl * group);
+        for (int d0 = 0; d0 < hd; d0 += 16) {
+            float v16[16];
+            tmem_ld16(tO + lane_off + (uint32_t)d0, v16);
+            if (t <= t_last) {
+                uint4 w0, w1;
+                w0.x = h2_pack(v16[0], v16[1]);
+                w0.y = h2_pack(v16[2], v16[3]);
+                w0.z = h2_pack(v16[4], v16[5]);
+                w0.w = h2_pack(v16[6], v16[7]);
+                w1.x = h2_pack(v16[8], v16[9]);
+                w1.y = h2_pack(v16[10], v16[11]);
+                w1.z = h2_pack(v16[12], v16[13]);
+                w1.w = h2_pack(v16[14], v16[15]);
+                uint4* dst = reinterpret_cast<uint4*>(att + (size_t)t * nq * hd + (size_t)h * hd + d0);
+                dst[0] = w0;
+                dst[1] = w1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+size_t pt_smem(int hd) { return 1024 + (size_t)(hd / 64) * 2 * 16384 + 2 * 16384 + 2 * (size_t)hd * 128 + 64; }
+
 size_t pa_smem(int group, int hd) {
     const int kw = hd / 2 + 1;
     return sizeof(float) * (size_t)PA_QT * group * hd + 4 * (size_t)((PA_CHUNK * kw + 3) & ~3) +
@@ -264,7 +513,8 @@ size_t prefill_layer_scratch_bytes(int T, int H, int nq, int nkv, int hd) {
     const size_t qd = (size_t)nq * hd, kvd = (size_t)nkv * hd;
     auto a = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t xin = (size_t)T * (H > (int)qd ? H : qd);
-    return a(4 * T * (qd + 2 * kvd)) + a(4 * T * qd) + a(2 * xin) + a(2 * T * qd) + a(4 * (size_t)T * H);
+    return a(4 * T * (qd + 2 * kvd)) + a(4 * T * qd) + a(2 * xin) + a(2 * T * qd) + a(4 * (size_t)T * H) +
+           a(8 * (size_t)T * H);
 }
 
 bool prefill_layer_supported(int H, int nq, int nkv, int hd) {
@@ -274,8 +524,17 @@ bool prefill_layer_supported(int H, int nq, int nkv, int hd) {
     return pa_smem(nq / nkv, hd) <= 200 * 1024;
 }
 
+// the tensor-core attention serves query groups whose rows tile 128 evenly and
+// head sizes of one or two 64-wide k-blocks
+bool pt_supported(int group, int hd) {
+    return (group == 1 || group == 2 || group == 4 || group == 8) && (hd == 64 || hd == 128);
+}
+
 cudaError_t prefill_layer_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(prefill_attention<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(prefill_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pt_smem(128));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_attention<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(prefill_attention<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e == cudaSuccess)
@@ -301,36 +560,66 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
     rmsnorm_rows<1><<<T, NR_THREADS, 0, st>>>(a.hidden, a.attn_norm, a.eps, a.H, x16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // B2: q, k, v rows of every token, side by side in one [T][qd + 2 kvd] buffer
+    // B2: q, k, v rows of every token, side by side in one [T][qd + 2 kvd]
+    // buffer, the three projections in one launch
     const int ld = qd + 2 * kvd;
-    e = launch_dense_q4k_gemm(a.wq, qd, a.H, x16, T, qkv, ld, 0, nullptr, st);
-    if (e == cudaSuccess) e = launch_dense_q4k_gemm(a.wk, kvd, a.H, x16, T, qkv, ld, qd, nullptr, st);
-    if (e == cudaSuccess) e = launch_dense_q4k_gemm(a.wv, kvd, a.H, x16, T, qkv, ld, qd + kvd, nullptr, st);
-    if (e != cudaSuccess) return e;
-    // B3-B5: per-head Q/K RMSNorm, NEOX RoPE, fp16 KV append at pos0 + t
+    {
+        const DenseSeg segs[3] = {{a.wq, qd, 0}, {a.wk, kvd, qd}, {a.wv, kvd, qd + kvd}};
+        e = launch_dense_q4k_gemm_multi(segs, 3, a.H, x16, T, qkv, ld, nullptr, 1, 0, st);
+        if (e != cudaSuccess) return e;
+    }
+    // B3-B5: per-head Q/K RMSNorm, NEOX RoPE, fp16 KV append at pos0 + t (q as
+    // fp16 rows grouped by kv head for the tensor-core attention, else fp32)
+    const int group = a.nq / a.nkv;
+    const bool tc = pt_supported(group, a.hd);
+    __half* qh = tc ? reinterpret_cast<__half*>(qr) : nullptr;
     qk_norm_rope_append<<<dim3(T, (a.nq + a.nkv + 3) / 4), 128, 0, st>>>(
-        qkv, a.nq, a.nkv, a.hd, a.q_norm, a.k_norm, a.eps, a.inv_freq, a.pos0, a.max_ctx, qr, a.k_cache,
-        a.v_cache, T);
+        qkv, a.nq, a.nkv, a.hd, a.q_norm, a.k_norm, a.eps, a.inv_freq, a.pos0, a.max_ctx, qr, qh,
+        a.k_cache, a.v_cache, T);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // B6: causal GQA attention over cache + batch
-    const int group = a.nq / a.nkv;
-    const int mv = (PA_QT * group + PA_THREADS / 32 - 1) / (PA_THREADS / 32);   // vectors per warp
-    const dim3 ga(a.nkv, (T + PA_QT - 1) / PA_QT);
-    const size_t sm = pa_smem(group, a.hd);
-    if (mv <= 1)
-        prefill_attention<1><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16);
-    else if (mv <= 2)
-        prefill_attention<2><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16);
-    else
-        prefill_attention<4><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16);
+    if (tc) {
+        CUtensorMap tq, tk;
+        if (!tensor_map_half(&tq, qh, (uint64_t)a.hd, (uint64_t)a.nkv * T * group, 128) ||
+            !tensor_map_half(&tk, a.k_cache, (uint64_t)a.hd, (uint64_t)a.nkv * a.max_ctx, 128))
+            return cudaErrorInvalidValue;
+        const int QB = 128 / group;
+        prefill_attention_tc<<<dim3(a.nkv, (T + QB - 1) / QB), PT_THREADS, pt_smem(a.hd), st>>>(
+            tq, tk, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16, a.status);
+    } else {
+        // other shapes: the CUDA-core kernel
+        const int mv = (PA_QT * group + PA_THREADS / 32 - 1) / (PA_THREADS / 32);   // vectors per warp
+        const dim3 ga(a.nkv, (T + PA_QT - 1) / PA_QT);
+        const size_t sm = pa_smem(group, a.hd);
+        if (mv <= 1)
+            prefill_attention<1><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
+                                                             a.pos0, a.max_ctx, T, att16);
+        else if (mv <= 2)
+            prefill_attention<2><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
+                                                             a.pos0, a.max_ctx, T, att16);
+        else
+            prefill_attention<4><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
+                                                             a.pos0, a.max_ctx, T, att16);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // B7: h = h + Wo att, in place (every element read and written by one thread)
-    e = launch_dense_q4k_gemm(a.wo, a.H, qd, att16, T, a.hidden, a.H, 0, a.hidden, st);
-    if (e != cudaSuccess) return e;
-    // B8: x2 = RMSNorm(h) * ffn_norm (the MoE input; h stays the residual)
-    rmsnorm_rows<0><<<T, NR_THREADS, 0, st>>>(a.hidden, a.ffn_norm, a.eps, a.H, x2);
+    // B7 + B8: h = h + Wo att, x2 = RMSNorm(h) * ffn_norm (the MoE input; h
+    // stays the residual).  With too few row x token tiles to fill the GPU the
+    // O projection is split over K into two planes that the norm kernel adds.
+    const DenseSeg so{a.wo, a.H, 0};
+    if (2 * dense_q4k_items(a.H, T) <= device_sm_count() && (qd / QK) % 2 == 0) {
+        float* part = x2 + (size_t)T * a.H;                // two [T][H] planes after x2
+        e = launch_dense_q4k_gemm_multi(&so, 1, qd, att16, T, part, a.H, nullptr, 2, (size_t)T * a.H, st);
+        if (e != cudaSuccess) return e;
+        residual_rmsnorm_rows<<<T, NR_THREADS, 0, st>>>(a.hidden, part, part + (size_t)T * a.H, a.ffn_norm,
+                                                        a.eps, a.H, x2);
+    } else {
+        // in place: every element of h is read and written by one thread
+        e = launch_dense_q4k_gemm_multi(&so, 1, qd, att16, T, a.hidden, a.H, a.hidden, 1, 0, st);
+        if (e != cudaSuccess) return e;
+        rmsnorm_rows<0><<<T, NR_THREADS, 0, st>>>(a.hidden, a.ffn_norm, a.eps, a.H, x2);
+    }
     return cudaGetLastError();
 }
 

@@ -165,18 +165,25 @@ struct GuParams {
     const int32_t* used_expert;
     const int32_t* used_first;
     __half* act;          // [P][F] fp16, rows in pair-list order
-    int H, F;             // K of the GEMM; rows per expert (MODE 0) / of the matrix (MODE 1)
-    // plain mode (a dense Q4_K GEMM): y[t][yoff + r] = sum_k W[r][k] x[t][k]
-    // (+ res[t][yoff + r]) for the dense_T tokens of x, W = the tm_gate map
+    int H, F;             // K of the GEMM; rows per expert (MODE 0) / of all segments (MODE 1)
+    // plain mode (dense Q4_K GEMMs): up to three weight matrices ("segments",
+    // maps tm_gate, tm_up, tm_w2) over the same x, segment s writing
+    // y[t][seg_yoff[s] + r] = sum_k W_s[r][k] x[t][k] (+ res[t][...]); with
+    // ksplit = 2 each item takes half of K and writes its own plane
+    // y + kh * part_stride (no res), the caller adding the two
     float* y;
     const float* res;
-    int dense_T, ldy, yoff;
+    int dense_T, ldy;
+    int seg_rows[3], seg_yoff[3];
+    int ksplit;
+    size_t part_stride;
 };
 
-// One work item of the gate/up kernel: weight rows f0 .. of expert e against
-// the token rows first + n0 .. first + n0 + n - 1.
+// One work item of the gate/up kernel: weight rows f0 .. of expert e (MODE 1:
+// of segment e) against the token rows first + n0 .. first + n0 + n - 1, over
+// K half kh (MODE 1 with ksplit 2; else 0).
 struct GuItem {
-    int e, first, n0, n, f0;
+    int e, first, n0, n, f0, kh;
 };
 
 // Items in the order (token tile, weight-row tile), the row tile fastest, so
@@ -187,7 +194,10 @@ template <int MODE>
 __device__ __forceinline__ GuItem gu_item(const GuParams& p, const int* tfirst, int n_used, int it) {
     GuItem w;
     const int FT = MODE == 0 ? p.F / 64 : p.F / TILE_M;
-    const int tt = it / FT, ft = it - tt * FT;
+    const int KS = MODE == 0 ? 1 : p.ksplit;
+    const int tt = it / (FT * KS), rem = it - tt * FT * KS;
+    w.kh = rem / FT;
+    const int ft = rem - w.kh * FT;
     if (MODE == 0) {
         int lo = 0, hi = n_used - 1;                     // last u with tfirst[u] <= tt
         while (lo < hi) {
@@ -201,11 +211,20 @@ __device__ __forceinline__ GuItem gu_item(const GuParams& p, const int* tfirst, 
         w.n = min(GU_NMAX, p.used_first[lo + 1] - w.first - w.n0);
         w.f0 = ft * 64;
     } else {
-        w.e = 0;
+        int seg = 0, f = ft * TILE_M;
+        if (f >= p.seg_rows[0]) {
+            f -= p.seg_rows[0];
+            seg = 1;
+            if (f >= p.seg_rows[1]) {
+                f -= p.seg_rows[1];
+                seg = 2;
+            }
+        }
+        w.e = seg;
         w.first = 0;
         w.n0 = tt * GU_NMAX;
         w.n = min(GU_NMAX, p.dense_T - w.n0);
-        w.f0 = ft * TILE_M;
+        w.f0 = f;
     }
     return w;
 }
@@ -221,14 +240,16 @@ __device__ __forceinline__ GuItem gu_item(const GuParams& p, const int* tfirst, 
 template <int MODE>
 __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
-                   const __grid_constant__ CUtensorMap tm_x64, const __grid_constant__ CUtensorMap tm_x128,
-                   const __grid_constant__ CUtensorMap tm_xg, const GuParams p) {
+                   const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x64,
+                   const __grid_constant__ CUtensorMap tm_x128, const __grid_constant__ CUtensorMap tm_xg,
+                   const GuParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     // 1024-aligned base, kept a shared-space pointer (an integer round trip
     // would turn every access into a generic one)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
-    const int NKB = H / KBLK, NSB = H / QK;
+    const int KS = MODE == 0 ? 1 : p.ksplit;
+    const int NKB = H / KBLK / KS, NSB = H / QK / KS;     // per item
     const int FT = MODE == 0 ? F / 64 : F / TILE_M;
 
     uint8_t* qst = sm;                                   // GU_NQ x QSTAGE_GU
@@ -276,7 +297,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem;
-    const int n_items = MODE == 0 ? FT * tfirst[n_used] : FT * ((p.dense_T + GU_NMAX - 1) / GU_NMAX);
+    const int n_items = MODE == 0 ? FT * tfirst[n_used] : FT * KS * ((p.dense_T + GU_NMAX - 1) / GU_NMAX);
 
     if (warp == W_QLOAD) {
         // raw superblock columns of each item's 128 weight rows, GU_NQ ahead
@@ -285,7 +306,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const GuItem w = gu_item<MODE>(p, tfirst, n_used, it);
-                const int ybase = w.e * F + w.f0;
+                const int ybase = MODE == 0 ? w.e * F + w.f0 : w.f0;
+                const CUtensorMap* tw = MODE == 0 ? &tm_gate : w.e == 0 ? &tm_gate : w.e == 1 ? &tm_up : &tm_w2;
+                const int sb0 = w.kh * NSB;
                 for (int sb = 0; sb < NSB; ++sb, ++gs) {
                     const int st = gs % GU_NQ;
                     if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / GU_NQ) & 1u) ^ 1u)) {
@@ -294,11 +317,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                     }
                     uint8_t* dst = qst + st * QSTAGE_GU;
                     mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
-                    tma_load_2d(dst, &tm_gate, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                    tma_load_2d(dst, tw, (sb0 + sb) * Q4K_BYTES, ybase, &bars->qfull[st]);
                     if (MODE == 0)
                         tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
                     else
-                        tma_load_2d(dst + 64 * Q4K_BYTES, &tm_gate, sb * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
+                        tma_load_2d(dst + 64 * Q4K_BYTES, tw, (sb0 + sb) * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
                 }
             }
         }
@@ -319,7 +342,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&bars->afull[pr], (uint32_t)(nb * KBLK * 2));
-                    tma_load_2d(bst + st * GU_BSTAGE, tmx, kb * KBLK, w.first + w.n0, &bars->afull[pr]);
+                    tma_load_2d(bst + st * GU_BSTAGE, tmx, (w.kh * NKB + kb) * KBLK, w.first + w.n0,
+                                &bars->afull[pr]);
                 }
             }
         }
@@ -447,7 +471,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                     }
                 }
             } else {
-                const int row = p.yoff + w.f0 + 32 * lq + lane;
+                const int yoff = w.e == 0 ? p.seg_yoff[0] : w.e == 1 ? p.seg_yoff[1] : p.seg_yoff[2];
+                const int row = yoff + w.f0 + 32 * lq + lane;
+                float* yp = p.y + (size_t)w.kh * p.part_stride;
+                const float* rp = KS == 1 ? p.res : nullptr;
                 for (int c0 = 16 * half; c0 < N; c0 += 32) {
                     float v[16];
                     tmem_ld16(d + (uint32_t)c0, v);
@@ -456,7 +483,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                         const int col = c0 + jj;
                         if (col < w.n) {
                             const size_t o = (size_t)(w.n0 + col) * p.ldy + row;
-                            p.y[o] = v[jj] + (p.res ? p.res[o] : 0.f);
+                            yp[o] = v[jj] + (rp ? rp[o] : 0.f);
                         }
                     }
                 }
@@ -852,6 +879,10 @@ size_t dn_smem(int F, int down_t, int E) {
 
 }  // namespace
 
+bool tensor_map_half(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    return map_half(m, base, cols, rows, box_rows);
+}
+
 bool prefill_supported(const MoeShape& s, int gate_t, int up_t, int down_t) {
     if (gate_t != 1 || up_t != 1) return false;
     if (s.H % QK || s.F % QK || s.H % TILE_M || s.F % 64) return false;
@@ -887,8 +918,9 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0, 0};
-    prefill_gateup<0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tx64, tx128, txg, gp);
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
+                {0, 0, 0}, {0, 0, 0}, 1, 0};
+    prefill_gateup<0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t};
@@ -900,13 +932,21 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     return cudaGetLastError();
 }
 
-cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
-                                  int ldy, int yoff, const float* res, cudaStream_t st) {
-    if (rows % TILE_M || K % QK || T < 1) return cudaErrorInvalidValue;
-    CUtensorMap tw, tx64, tx128, txg;
+cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, const __half* x, int T,
+                                        float* y, int ldy, const float* res, int ksplit, size_t part_stride,
+                                        cudaStream_t st) {
+    if (nseg < 1 || nseg > 3 || K % QK || T < 1 || (ksplit != 1 && ksplit != 2) || (K / QK) % ksplit)
+        return cudaErrorInvalidValue;
+    CUtensorMap tw[3], tx64, tx128, txg;
     const uint64_t rb = (uint64_t)(K / QK) * Q4K_BYTES;
-    if (!map_bytes(&tw, W, rb, (uint64_t)rows, Q4K_BYTES, 64) || !map_half(&tx64, x, K, T, 64) ||
-        !map_half(&tx128, x, K, T, 128) || !map_half(&txg, x, K, T, GU_NMAX))
+    int rows = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (seg[i].rows % TILE_M || !map_bytes(&tw[i], seg[i].W, rb, (uint64_t)seg[i].rows, Q4K_BYTES, 64))
+            return cudaErrorInvalidValue;
+        rows += seg[i].rows;
+    }
+    for (int i = nseg; i < 3; ++i) tw[i] = tw[0];
+    if (!map_half(&tx64, x, K, T, 64) || !map_half(&tx128, x, K, T, 128) || !map_half(&txg, x, K, T, GU_NMAX))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -915,11 +955,24 @@ cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __hal
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int items = (rows / TILE_M) * ((T + GU_NMAX - 1) / GU_NMAX);
-    GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, y, res, T, ldy, yoff};
-    prefill_gateup<1><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(tw, tw, tx64, tx128,
-                                                                                          txg, gp);
+    GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, y, res, T, ldy,
+                {nseg > 0 ? seg[0].rows : 0, nseg > 1 ? seg[1].rows : 0, nseg > 2 ? seg[2].rows : 0},
+                {nseg > 0 ? seg[0].yoff : 0, nseg > 1 ? seg[1].yoff : 0, nseg > 2 ? seg[2].yoff : 0},
+                ksplit, part_stride};
+    const int items = (rows / TILE_M) * ksplit * ((T + GU_NMAX - 1) / GU_NMAX);
+    prefill_gateup<1><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(
+        tw[0], tw[1], tw[2], tx64, tx128, txg, gp);
     return cudaGetLastError();
 }
+
+cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
+                                  int ldy, int yoff, const float* res, cudaStream_t st) {
+    const DenseSeg seg{W, rows, yoff};
+    return launch_dense_q4k_gemm_multi(&seg, 1, K, x, T, y, ldy, res, 1, 0, st);
+}
+
+int dense_q4k_items(int rows, int T) { return (rows / TILE_M) * ((T + GU_NMAX - 1) / GU_NMAX); }
+
+int device_sm_count() { return sm_count(); }
 
 }  // namespace qmoe

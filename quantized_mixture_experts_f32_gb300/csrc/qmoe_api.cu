@@ -617,7 +617,7 @@ qmoe_status qmoe_prefill(qmoe_ctx* c, const qmoe_layer_weights* layers, int n_la
                                  static_cast<const uint8_t*>(w.wv), static_cast<const uint8_t*>(w.wo),
                                  w.q_norm, w.k_norm, w.ffn_norm,
                                  static_cast<__half*>(w.k_cache), static_cast<__half*>(w.v_cache),
-                                 hidden, c->pl_scratch};
+                                 hidden, c->pl_scratch, c->status};
         // B1-B8: h += Wo attn(...), x2 = RMSNorm(h) * ffn_norm
         cudaError_t e = qmoe::launch_prefill_layer_attn(a, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "prefill attention launch");

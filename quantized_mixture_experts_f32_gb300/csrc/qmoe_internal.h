@@ -189,6 +189,18 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
 // fp32 with row pitch ldy.  res may equal y (in place).
 cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,
                                   int ldy, int yoff, const float* res, cudaStream_t st);
+// Up to three such GEMMs over the same x in one launch (segment i: W, rows,
+// output column offset yoff).  ksplit 2: each half of K writes its own plane
+// y + kh * part_stride with no residual (the caller adds the two planes).
+struct DenseSeg {
+    const uint8_t* W;
+    int rows, yoff;
+};
+cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, const __half* x, int T,
+                                        float* y, int ldy, const float* res, int ksplit, size_t part_stride,
+                                        cudaStream_t st);
+int dense_q4k_items(int rows, int T);   // work items of one dense GEMM of `rows` rows
+int device_sm_count();
 
 // Batched prefill of one decoder layer (prefill_layer.cu): everything up to
 // the MoE input.  hidden [T][H] fp32 is updated in place to h + Wo attn, the
@@ -210,6 +222,7 @@ struct PrefillLayerArgs {
     __half* v_cache;
     float* hidden;
     void* scratch;            // prefill_layer_scratch_bytes(T, ...)
+    int* status;              // device status word (a bounded wait that ran out)
 };
 size_t prefill_layer_scratch_bytes(int T, int H, int nq, int nkv, int hd);
 bool prefill_layer_supported(int H, int nq, int nkv, int hd);

@@ -38,10 +38,11 @@ LAUNCHES_PER_Q8K_FORWARD = 7
 LAUNCHES_PER_DECODE_LAYER = 5
 # plus, once per qmoe_decode_step: the RoPE cos/sin table at the step's position
 LAUNCHES_PER_DECODE_STEP = 1
-# one decoder layer of qmoe_prefill up to the MoE input: RMSNorm, Q/K/V GEMMs,
-# Q/K norm + RoPE + KV append, attention, O GEMM, FFN RMSNorm; the MoE adds
+# one decoder layer of qmoe_prefill up to the MoE input: RMSNorm, one Q/K/V
+# GEMM, RoPE cos/sin table, Q/K norm + RoPE + KV append, attention, O GEMM, FFN
+# RMSNorm (with the O projection's residual); the MoE adds
 # LAUNCHES_PER_PREFILL_FORWARD (n_tokens > 8) or one fused kernel
-LAUNCHES_PER_PREFILL_LAYER_ATTN = 8
+LAUNCHES_PER_PREFILL_LAYER_ATTN = 7
 
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_prefill", "qmoe_get_status", "qmoe_last_error",

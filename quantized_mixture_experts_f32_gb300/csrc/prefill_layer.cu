@@ -98,13 +98,22 @@ __device__ __forceinline__ float2 rope_cs(const double* __restrict__ inv_freq, i
     return make_float2(c, sn);
 }
 
+// cos/sin of every (token, pair) of the batch: cs[t][j] for position pos0 + t
+__global__ void rope_table_rows(const double* __restrict__ inv_freq, int half, int pos0, int T,
+                                float2* __restrict__ cs) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= T * half) return;
+    const int t = i / half, j = i - t * half;
+    cs[i] = rope_cs(inv_freq, j, pos0 + t);
+}
+
 // one warp per (token, head): heads 0..nq-1 are q heads (RMSNorm q_norm, RoPE,
 // fp32 out), heads nq..nq+nkv-1 are kv heads (k: RMSNorm k_norm, RoPE, fp16 into
 // cache slot pos0 + t; v: fp16 into the same slot).  Lane owns dims lane + 32 i,
 // so the rotated pairs (d, d + hd/2) sit in the same lane.
 __global__ void __launch_bounds__(128) qk_norm_rope_append(
     const float* __restrict__ qkv, int nq, int nkv, int hd, const float* __restrict__ q_norm,
-    const float* __restrict__ k_norm, float eps, const double* __restrict__ inv_freq, int pos0,
+    const float* __restrict__ k_norm, float eps, const float2* __restrict__ rcs, int pos0,
     int max_ctx, float* __restrict__ qr, __half* __restrict__ qh, __half* __restrict__ k_cache,
     __half* __restrict__ v_cache, int T) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,7 +142,7 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append(
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (i < n / 2) {
-            const float2 cs = rope_cs(inv_freq, lane + 32 * i, pos);
+            const float2 cs = rcs[(size_t)t * (hd / 2) + lane + 32 * i];
             const float a = v[i], b = v[i + n / 2];
             o[i] = a * cs.x - b * cs.y;
             o[i + n / 2] = b * cs.x + a * cs.y;
@@ -514,7 +523,7 @@ size_t prefill_layer_scratch_bytes(int T, int H, int nq, int nkv, int hd) {
     auto a = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t xin = (size_t)T * (H > (int)qd ? H : qd);
     return a(4 * T * (qd + 2 * kvd)) + a(4 * T * qd) + a(2 * xin) + a(2 * T * qd) + a(4 * (size_t)T * H) +
-           a(8 * (size_t)T * H);
+           a(8 * (size_t)T * H) + a(sizeof(float2) * (size_t)T * (hd / 2));
 }
 
 bool prefill_layer_supported(int H, int nq, int nkv, int hd) {
@@ -573,8 +582,11 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
     const int group = a.nq / a.nkv;
     const bool tc = pt_supported(group, a.hd);
     __half* qh = tc ? reinterpret_cast<__half*>(qr) : nullptr;
+    float2* rcs = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(x2) + al(4 * (size_t)T * a.H) +
+                                            al(8 * (size_t)T * a.H));
+    rope_table_rows<<<(T * (a.hd / 2) + 255) / 256, 256, 0, st>>>(a.inv_freq, a.hd / 2, a.pos0, T, rcs);
     qk_norm_rope_append<<<dim3(T, (a.nq + a.nkv + 3) / 4), 128, 0, st>>>(
-        qkv, a.nq, a.nkv, a.hd, a.q_norm, a.k_norm, a.eps, a.inv_freq, a.pos0, a.max_ctx, qr, qh,
+        qkv, a.nq, a.nkv, a.hd, a.q_norm, a.k_norm, a.eps, rcs, a.pos0, a.max_ctx, qr, qh,
         a.k_cache, a.v_cache, T);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

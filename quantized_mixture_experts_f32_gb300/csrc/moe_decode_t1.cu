@@ -443,40 +443,35 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
     __syncthreads();
     if (tid == 0) T1_TRACE(3);
     const bool abort_b = misc[MS_ABORT] != 0;
-    if (!abort_b) {
-        // rank of every logit among the E (ties: lower index first); tpe
-        // consecutive threads share one logit, each comparing a contiguous run
-        // of R keys (16-byte loads; the key array is padded to a multiple of 128
-        // with keys that never outrank a real one)
-        const int EP = (E + 127) & ~127;
-        int tpe = TN / E;
-        tpe = tpe >= 32 ? 32 : tpe >= 16 ? 16 : tpe >= 8 ? 8 : tpe >= 4 ? 4 : tpe >= 2 ? 2 : 1;
-        const int R = EP / tpe;                                   // a multiple of 4
-        const int4* key4 = reinterpret_cast<const int4*>(key_s);
-        for (int base = 0; base < E * tpe; base += TN) {
-            const int i = (base + tid) / tpe, sub = (base + tid) % tpe;
-            const bool valid = i < E;
-            const int v = valid ? key_s[i] : 0;
-            int rank = 0;
-#pragma unroll 8
-            for (int k = 0; k < R; k += 4) {
-                const int e2 = sub * R + k;
-                const int4 w = key4[e2 >> 2];
-                rank += (int)(w.x > v) + (int)((w.x == v) & (e2 < i));
-                rank += (int)(w.y > v) + (int)((w.y == v) & (e2 + 1 < i));
-                rank += (int)(w.z > v) + (int)((w.z == v) & (e2 + 2 < i));
-                rank += (int)(w.w > v) + (int)((w.w == v) & (e2 + 3 < i));
+    if (!abort_b && warp == 0) {
+        // top-k in K rounds of a warp arg-max over 64-bit keys (order key of the
+        // logit, then E - 1 - e): round r takes the largest key below round
+        // r - 1's, i.e. the r-th logit in descending order, ties to the lower index
+        long long prev = LLONG_MAX;
+        for (int r = 0; r < K; ++r) {
+            long long best = LLONG_MIN;
+            for (int i = lane; i < E; i += 32) {
+                const long long key = (long long)key_s[i] * 4294967296LL + (long long)(E - 1 - i);
+                if (key < prev && key > best) best = key;
             }
-            for (int o = tpe >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-            if (valid && sub == 0 && rank < K) sel[rank] = i;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const long long other = __shfl_xor_sync(0xffffffffu, best, o);
+                if (other > best) best = other;
+            }
+            if (lane == 0) sel[r] = E - 1 - (int)(best & 0xffffffffLL);
+            prev = best;
         }
     }
     __syncthreads();
     if (tid == 0) T1_TRACE(10);
 
-    // ---------------- every weight copy of this CTA, at once: lane 0 of warp j
-    // issues slot j's gate rows, up rows (one barrier) and down rows (another),
-    // the down rows from the 16-byte boundary below their first byte.
+    // ---------------- the gate/up copies of this CTA, at once: lane 0 of warp j
+    // issues slot j's gate rows and up rows (one barrier).  The down rows
+    // (another barrier, from the 16-byte boundary below their first byte) are
+    // requested later, once the warp has its first gate/up rows: they are not
+    // needed before the act exchange, and requested together with the gate/up
+    // rows they took a third of the bandwidth the gate/up phase waits on.
     // (Measured on this GPU: with all of a CTA's ~160 KB requested at once,
     // bulk copies, 16-byte cp.async copies and plain 16-byte loads all take
     // ~6 us to bring 24.5 MB into the 152 SMs; bulk copies leave the other
@@ -490,12 +485,20 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
             bulk_g2s(gu_s + (size_t)(2 * j) * L.nrs_max * RBG, p.gate + off, gbytes, &gub[j]);
             bulk_g2s(gu_s + (size_t)(2 * j + 1) * L.nrs_max * RBG, p.up + off, gbytes, &gub[j]);
         }
-        const uintptr_t src = reinterpret_cast<uintptr_t>(p.down) + ((size_t)e * H + h0) * RBD;
-        const uintptr_t a0 = src & ~uintptr_t(15), a1 = (src + (size_t)nrd * RBD + 15) & ~uintptr_t(15);
-        mbar_arrive_expect_tx(&dnb[j], (uint32_t)(a1 - a0));
-        if (a1 > a0)
-            bulk_g2s(dn_s + (size_t)j * L.dn_seg, reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0), &dnb[j]);
     }
+    bool dn_issued = abort_b || warp >= K;
+    auto issue_down = [&]() {
+        if (lane == 0) {
+            const int j = warp, e = sel[j];
+            const uintptr_t src = reinterpret_cast<uintptr_t>(p.down) + ((size_t)e * H + h0) * RBD;
+            const uintptr_t a0 = src & ~uintptr_t(15), a1 = (src + (size_t)nrd * RBD + 15) & ~uintptr_t(15);
+            mbar_arrive_expect_tx(&dnb[j], (uint32_t)(a1 - a0));
+            if (a1 > a0)
+                bulk_g2s(dn_s + (size_t)j * L.dn_seg, reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0),
+                         &dnb[j]);
+        }
+        dn_issued = true;
+    };
     if (lane == 0) T1_TRACE(64 + warp);
     // routing weights (warp 0) while the copies are in flight
     if (!abort_b && warp == 0) {
@@ -566,6 +569,7 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
             }
             if (!ok) break;
             if (lane == 0 && t0 == 2 * warp) T1_TRACE(80 + warp);
+            if (!dn_issued) issue_down();
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 gsum[u] = usum[u] = 0.f;
@@ -601,6 +605,8 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
             t1_status(p.status, ST_TIMEOUT);
             misc[MS_ABORT] = 1;
         }
+        // a warp with no gate/up rows (or one that gave up) still owes its slot's down copy
+        if (!dn_issued) issue_down();
         if (lane == 0) T1_TRACE(16 + warp);
     }
     // This CTA's act values are stored: count it in.  Readiness of all act

@@ -295,24 +295,28 @@ __global__ void __launch_bounds__(PA_THREADS) prefill_attention(
 // Causal GQA attention on the tensor cores.  CTA = (kv head g, 128 / group
 // tokens): its 128 query rows (token, head of the group) against key chunks of
 // 128 positions, two passes over the chunks.  Pass 1: S = Q K^T (tcgen05, fp32
-// in TMEM), each thread holds one row (its TMEM lane) and keeps the running
-// maximum and sum of exponentials of its visible scores.  Pass 2: S again,
-// P = exp(s - max) / sum as fp16 into shared memory (128B-swizzled, K-major),
-// V^T of the chunk staged by the threads in the same layout, O += P V^T in
-// TMEM.  Two passes instead of rescaling O on every new maximum keep the
-// accumulator in TMEM untouched until the end.  Epilogue: O rows -> fp16 att.
-// Masking: key p is visible to the row of token t when p <= pos0 + t; keys past
-// the block's last visible key are not read (their V^T columns are zero).
-// One thread (tid 0) issues the TMA copies and MMAs; 128 threads.
-constexpr int PT_THREADS = 128;
+// in TMEM); row r's scores are read by two threads (columns 0-63 and 64-127,
+// TMEM lane r), each keeping the running maximum and sum of exponentials of its
+// visible scores; the two halves are merged once, after the pass.  Pass 2: S
+// again, P = exp(s - max) / sum as fp16 into shared memory (128B-swizzled,
+// K-major: each thread's half of a row is one 64-key k-block), V^T of the chunk
+// staged by the threads in the same layout, O += P V^T in TMEM.  Two passes
+// instead of rescaling O on every new maximum keep the accumulator in TMEM
+// untouched until the end.  P reuses the K buffer (the S MMA that read K has
+// completed before P is written), so two CTAs fit an SM.  Epilogue: O rows ->
+// fp16 att.  Masking: key p is visible to the row of token t when p <= pos0 + t;
+// keys past the block's last visible key are not read (their V^T columns are
+// zero).  One thread (tid 0) issues the TMA copies and MMAs.
+constexpr int PT_THREADS = 256;
 constexpr int PT_KC = 128;                                 // keys per chunk
+constexpr int PT_HC = PT_KC / 2;                           // keys per thread (one half of a row)
 
 __device__ __forceinline__ uint32_t h2_pack(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
+__global__ void __launch_bounds__(PT_THREADS, 2) prefill_attention_tc(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __half* __restrict__ v_cache, int nq, int nkv, int hd, int pos0, int max_ctx, int T,
     __half* __restrict__ att, int* __restrict__ status) {
@@ -323,19 +327,21 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
     const int tid = threadIdx.x, warp = tid >> 5;
     const int nkb = hd / 64;                               // 64-wide k-blocks of hd
     uint8_t* sQ = sm;                                      // nkb x 16 KB (128 rows)
-    uint8_t* sK = sQ + nkb * 16384;                        // nkb x 16 KB (128 keys)
-    uint8_t* sP = sK + nkb * 16384;                        // 2 x 16 KB (128 rows x 128 keys)
-    uint8_t* sV = sP + 2 * 16384;                          // 2 x (hd x 128 B): V^T, keys = K
+    uint8_t* sK = sQ + nkb * 16384;                        // max(nkb, 2) x 16 KB: K, then P
+    uint8_t* sP = sK;                                      // 2 x 16 KB (128 rows x 128 keys)
+    uint8_t* sV = sK + (nkb > 2 ? nkb : 2) * 16384;        // 2 x (hd x 128 B): V^T, keys = K
     uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * hd * 128);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    float* xch = reinterpret_cast<float*>(bars + 4);       // [2][128] half-row statistics
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(xch + 512);
     uint64_t* tma_bar = bars;
     uint64_t* mma_bar = bars + 1;
     uint64_t* q_bar = bars + 2;
     const int t_last = min(t0 + QB, T) - 1;                // last token of the block
     const int kend = pos0 + t_last + 1;                    // keys the block sees
     const int nchunks = (kend + PT_KC - 1) / PT_KC;
-    // this thread's query row
-    const int tl = tid / group, t = t0 + tl;
+    // this thread's query row and half of the chunk's columns
+    const int row = tid & 127, hf = tid >> 7;
+    const int tl = row / group, t = t0 + tl;
     const int kmax = pos0 + t;                             // last key of this row
     const float sl2 = rsqrtf((float)hd) * 1.4426950408889634f;   // scale * log2(e)
 
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tS = tmem, tO = tmem + 128;             // columns: S [0,128), O [128, 128 + hd)
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t tpar = 0, mpar = 0;
     bool ok = true;
 
@@ -368,6 +374,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
     float m = -INFINITY, l = 0.f;
     for (int pass = 0; pass < 2; ++pass) {
         bool stop = false;
+        if (pass == 1) {
+            // merge the two half-row statistics of each row
+            xch[hf * 128 + row] = m;
+            xch[256 + hf * 128 + row] = l;
+            __syncthreads();
+            const float mo = xch[(hf ^ 1) * 128 + row], lo = xch[256 + (hf ^ 1) * 128 + row];
+            const float mn = fmaxf(m, mo);
+            l = (m > -INFINITY ? l * exp2f(m - mn) : 0.f) + (mo > -INFINITY ? lo * exp2f(mo - mn) : 0.f);
+            m = mn;
+        }
         for (int c = 0; c < nchunks; ++c) {
             if (!__syncthreads_and(ok)) {
                 ok = false;
@@ -395,17 +411,17 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
                 }
             }
             if (pass == 1) {
-                // V^T of the chunk: thread -> key pair (2 i, 2 i + 1), half of hd
-                const int i = tid & 63, dh = tid >> 6, kk = 2 * i;
-                const int half_d = hd / 2;
-                for (int d0 = dh * half_d; d0 < dh * half_d + half_d; d0 += 8) {
+                // V^T of the chunk: thread -> key pair (2 i, 2 i + 1), a quarter of hd
+                const int i = tid & 63, dq = tid >> 6, kk = 2 * i;
+                const int qd4 = hd / 4;
+                uint8_t* reg = sV + (kk >> 6) * (hd * 128);
+                for (int d0 = dq * qd4; d0 < dq * qd4 + qd4; d0 += 8) {
                     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
                     if (k0 + kk < kend)
                         a = *reinterpret_cast<const uint4*>(v_cache + ((size_t)g * max_ctx + k0 + kk) * hd + d0);
                     if (k0 + kk + 1 < kend)
                         b = *reinterpret_cast<const uint4*>(v_cache + ((size_t)g * max_ctx + k0 + kk + 1) * hd + d0);
                     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-                    uint8_t* reg = sV + (kk >> 6) * (hd * 128);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         // halves d0 + 2q (low) and d0 + 2q + 1 (high) of keys kk, kk + 1
@@ -419,16 +435,17 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
             if (!mbar_wait(mma_bar, mpar)) ok = false;
             mpar ^= 1u;
             tc_fence_after();
-            // this row's 128 scores, 16 at a time
+            // this thread's 64 scores of its row, 16 at a time
+            const int kb0 = k0 + PT_HC * hf;
             float cm = -INFINITY;
-            float sv[PT_KC];
+            float sv[PT_HC];
 #pragma unroll
-            for (int j0 = 0; j0 < PT_KC; j0 += 16) {
+            for (int j0 = 0; j0 < PT_HC; j0 += 16) {
                 float v16[16];
-                tmem_ld16(tS + lane_off + (uint32_t)j0, v16);
+                tmem_ld16(tS + lane_off + (uint32_t)(PT_HC * hf + j0), v16);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float s2 = k0 + j0 + j <= kmax ? v16[j] * sl2 : -INFINITY;
+                    const float s2 = kb0 + j0 + j <= kmax ? v16[j] * sl2 : -INFINITY;
                     sv[j0 + j] = s2;
                     cm = fmaxf(cm, s2);
                 }
@@ -438,22 +455,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
                     const float mn = fmaxf(m, cm);
                     float sum = 0.f;
 #pragma unroll
-                    for (int j = 0; j < PT_KC; ++j) sum += exp2f(sv[j] - mn);
+                    for (int j = 0; j < PT_HC; ++j) sum += exp2f(sv[j] - mn);
                     l = l * exp2f(m - mn) + sum;
                     m = mn;
                 }
             } else {
-                // P row -> fp16, 128B-swizzled K-major, two 64-key k-blocks
+                // this half of the P row -> fp16, one 64-key k-block (128B-swizzled K-major)
                 const float inv = 1.f / l;
-                uint8_t* prow = sP;
+                uint8_t* preg = sP + hf * 16384;
 #pragma unroll
-                for (int j0 = 0; j0 < PT_KC; j0 += 8) {
+                for (int j0 = 0; j0 < PT_HC; j0 += 8) {
                     uint4 w;
                     w.x = h2_pack(exp2f(sv[j0 + 0] - m) * inv, exp2f(sv[j0 + 1] - m) * inv);
                     w.y = h2_pack(exp2f(sv[j0 + 2] - m) * inv, exp2f(sv[j0 + 3] - m) * inv);
                     w.z = h2_pack(exp2f(sv[j0 + 4] - m) * inv, exp2f(sv[j0 + 5] - m) * inv);
                     w.w = h2_pack(exp2f(sv[j0 + 6] - m) * inv, exp2f(sv[j0 + 7] - m) * inv);
-                    *reinterpret_cast<uint4*>(prow + (j0 >> 6) * 16384 + sw128_offset(tid, j0 & 63)) = w;
+                    *reinterpret_cast<uint4*>(preg + sw128_offset(row, j0)) = w;
                 }
                 fence_proxy_async();
             }
@@ -471,7 +488,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
                 umma_commit(mma_bar);
             }
             if (pass == 1) {
-                // P and V^T are reused by the next chunk: wait for this chunk's MMAs
+                // P (in the K buffer) and V^T are reused by the next chunk: wait for this chunk's MMAs
                 if (!mbar_wait(mma_bar, mpar)) ok = false;
                 mpar ^= 1u;
             }
@@ -482,9 +499,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
     if (!ok && tid == 0) atomicExch(status, ST_TIMEOUT);
     if (ok) {
         tc_fence_after();
-        // O row -> fp16 att[t][h * hd + d], h = g * group + (row % group)
-        const int h = g * group + (tid - tl * group);
-        for (int d0 = 0; d0 < hd; d0 += 16) {
+        // O row -> fp16 att[t][h * hd + d], h = g * group + (row % group); this
+        // thread writes its half of hd
+        const int h = g * group + (row - tl * group);
+        for (int d0 = hf * (hd / 2); d0 < hf * (hd / 2) + hd / 2; d0 += 16) {
             float v16[16];
             tmem_ld16(tO + lane_off + (uint32_t)d0, v16);
             if (t <= t_last) {
@@ -508,7 +526,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_attention_tc(
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-size_t pt_smem(int hd) { return 1024 + (size_t)(hd / 64) * 2 * 16384 + 2 * 16384 + 2 * (size_t)hd * 128 + 64; }
+size_t pt_smem(int hd) {
+    const int nkb = hd / 64;
+    return 1024 + (size_t)nkb * 16384 + (size_t)(nkb > 2 ? nkb : 2) * 16384 + 2 * (size_t)hd * 128 + 32 +
+           sizeof(float) * 512 + 16;
+}
 
 size_t pa_smem(int group, int hd) {
     const int kw = hd / 2 + 1;

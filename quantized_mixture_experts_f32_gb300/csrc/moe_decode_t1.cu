@@ -173,19 +173,6 @@ __device__ __forceinline__ bool t1_load_tagged(const unsigned long long* base, i
     return true;
 }
 
-// non-blocking test of an mbarrier phase
-__device__ __forceinline__ bool t1_mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // bounded mbarrier wait with a caller-given limit: the suspending try_wait,
 // during which the warp issues nothing (a spin on the non-blocking test was
 // measured to more than double the kernel's issued instructions and slow the
@@ -228,17 +215,6 @@ __device__ __forceinline__ float t1_piece_finish(uint4 hdr, int pc, float QA, fl
     float r = (d * (float)sA) * QA - (dmin * (float)mA) * XA;
     r = fmaf(d * (float)sB, QB, r) - (dmin * (float)mB) * XB;
     return r;
-}
-
-// one 16-byte asynchronous copy global -> shared (both 16-byte aligned), L2 only
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
-
-// arrive on bar once every cp.async this thread issued so far has landed (the
-// barrier's expected count covers this arrival)
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // 16 bytes at an even shared-memory address (five aligned words, funnel shift)
@@ -553,22 +529,38 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
                 SXB[jt] = xscale[gb];
             }
         }
+        // Jobs of a warp: first a pair of rows (2w, 2w + 1) while pairs last for
+        // every warp, then the remaining rows one at a time, spread over all
+        // warps (pairs all the way put twice the rows on some warps than on
+        // others when the CTA's row count is not a multiple of 2 * TW, and the
+        // last warp sets the time of the phase)
         const int nrows = K * nrs;
+        const int np = min(nrows / 2, TW);
         bool ok = !abort_b;
-        for (int t0 = 2 * warp; ok && t0 < nrows; t0 += 2 * TW) {
+        for (int q = 0; ok; ++q) {
+            int tr[2];
+            if (q == 0 && warp < np) {
+                tr[0] = 2 * warp;
+                tr[1] = 2 * warp + 1;
+            } else {
+                const int qs = warp < np ? q - 1 : q;
+                tr[0] = 2 * np + warp + qs * TW;
+                tr[1] = -1;
+            }
+            if (tr[0] >= nrows) break;
             float gsum[2], usum[2];
             int jj[2], ii[2];
             bool on[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int t = t0 + u;
-                on[u] = t < nrows;
+                const int t = tr[u];
+                on[u] = t >= 0 && t < nrows;
                 jj[u] = on[u] ? t / nrs : 0;
                 ii[u] = on[u] ? t - jj[u] * nrs : 0;
                 if (on[u]) ok = ok && __all_sync(0xffffffffu, t1_mbar_wait(&gub[jj[u]], 0, p.wait_ns));
             }
             if (!ok) break;
-            if (lane == 0 && t0 == 2 * warp) T1_TRACE(80 + warp);
+            if (lane == 0 && q == 0) T1_TRACE(80 + warp);
             if (!dn_issued) issue_down();
 #pragma unroll
             for (int u = 0; u < 2; ++u) {

@@ -419,10 +419,55 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
     __syncthreads();
     if (tid == 0) T1_TRACE(3);
     const bool abort_b = misc[MS_ABORT] != 0;
-    if (!abort_b && warp == 0) {
-        // top-k in K rounds of a warp arg-max over 64-bit keys (order key of the
-        // logit, then E - 1 - e): round r takes the largest key below round
-        // r - 1's, i.e. the r-th logit in descending order, ties to the lower index
+    if (!abort_b && warp == 0 && E <= 128) {
+        // top-k for up to 128 experts: lane l sorts the (order key, index) pairs
+        // of experts l, l + 32, l + 64, l + 96 (larger key first, ties to the
+        // lower index), then K tournament rounds over the 32 lane heads: the
+        // largest head key by one warp max-reduction, the lowest index holding it
+        // by one min-reduction, and the owning lane drops its head.  (A warp
+        // arg-max over all keys per round was measured 4x slower: a round is a
+        // chain of five dependent shuffle steps.)
+        int ks[4], is[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+            const int i = lane + 32 * z;
+            ks[z] = i < E ? key_s[i] : INT_MIN;
+            is[z] = i < E ? i : INT_MAX;
+        }
+        auto cswap = [&](int x, int y) {
+            if (ks[y] > ks[x] || (ks[y] == ks[x] && is[y] < is[x])) {
+                const int tk = ks[x], ti = is[x];
+                ks[x] = ks[y];
+                is[x] = is[y];
+                ks[y] = tk;
+                is[y] = ti;
+            }
+        };
+        cswap(0, 1);
+        cswap(2, 3);
+        cswap(0, 2);
+        cswap(1, 3);
+        cswap(1, 2);
+        for (int r = 0; r < K; ++r) {
+            const int mk = __reduce_max_sync(0xffffffffu, ks[0]);
+            const int wi = (int)__reduce_min_sync(0xffffffffu, ks[0] == mk ? (unsigned)is[0] : 0xffffffffu);
+            if (lane == 0) sel[r] = wi;
+            if ((wi & 31) == lane) {
+                ks[0] = ks[1];
+                ks[1] = ks[2];
+                ks[2] = ks[3];
+                ks[3] = INT_MIN;
+                is[0] = is[1];
+                is[1] = is[2];
+                is[2] = is[3];
+                is[3] = INT_MAX;
+            }
+        }
+    } else if (!abort_b && warp == 0) {
+        // more experts: K rounds of a warp arg-max over 64-bit keys (order key
+        // of the logit, then E - 1 - e): round r takes the largest key below
+        // round r - 1's, i.e. the r-th logit in descending order, ties to the
+        // lower index
         long long prev = LLONG_MAX;
         for (int r = 0; r < K; ++r) {
             long long best = LLONG_MIN;

@@ -454,7 +454,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) moe_decode_fused(const FusedParam
     __syncthreads();
     if (tid == 0) QMOE_TRACE(2);
     const bool abort_b = misc[M_ABORT] != 0;
-    if (!abort_b) {
+    if (!abort_b && E <= 128) {
+        // up to 128 experts: warp t selects token t's top-k.  Lane l sorts the
+        // (order key, index) pairs of experts l, l + 32, l + 64, l + 96 (larger
+        // key first, ties to the lower index); then K tournament rounds over the
+        // 32 lane heads: the largest head key by one warp max-reduction, the
+        // lowest index holding it by one min-reduction, the owner drops its head
+        if (warp < T) {
+            const int* l = keys + warp * E;
+            int ks[4], is[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                const int i = lane + 32 * z;
+                ks[z] = i < E ? l[i] : INT_MIN;
+                is[z] = i < E ? i : INT_MAX;
+            }
+            auto cswap = [&](int x, int y) {
+                if (ks[y] > ks[x] || (ks[y] == ks[x] && is[y] < is[x])) {
+                    const int tk = ks[x], ti = is[x];
+                    ks[x] = ks[y];
+                    is[x] = is[y];
+                    ks[y] = tk;
+                    is[y] = ti;
+                }
+            };
+            cswap(0, 1);
+            cswap(2, 3);
+            cswap(0, 2);
+            cswap(1, 3);
+            cswap(1, 2);
+            for (int r = 0; r < K; ++r) {
+                const int mk = __reduce_max_sync(0xffffffffu, ks[0]);
+                const int wi = (int)__reduce_min_sync(0xffffffffu, ks[0] == mk ? (unsigned)is[0] : 0xffffffffu);
+                if (lane == 0) sel[warp * K + r] = wi;
+                if ((wi & 31) == lane) {
+                    ks[0] = ks[1];
+                    ks[1] = ks[2];
+                    ks[2] = ks[3];
+                    ks[3] = INT_MIN;
+                    is[0] = is[1];
+                    is[1] = is[2];
+                    is[2] = is[3];
+                    is[3] = INT_MAX;
+                }
+            }
+        }
+    } else if (!abort_b) {
         // rank of every logit among its token's E (ties: lower index first);
         // tpe consecutive lanes share one logit's E comparisons
         const int nel = T * E;

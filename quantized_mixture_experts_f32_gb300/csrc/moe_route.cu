@@ -291,11 +291,54 @@ __global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part,
         }
     }
     __syncwarp();
-    // K rounds of a warp arg-max over 64-bit keys (order key of the logit, then
-    // E - 1 - e): round r takes the largest key below round r - 1's, which is
-    // the r-th logit in descending order, ties to the lower index
+    if (E <= 128) {
+        // lane l sorts the (order key, index) pairs of experts l, l + 32, l + 64,
+        // l + 96 (larger key first, ties to the lower index); then K tournament
+        // rounds over the 32 lane heads: the largest head key by one warp
+        // max-reduction, the lowest index holding it by one min-reduction, and
+        // the owning lane drops its head
+        int ks[4], is[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+            const int i = lane + 32 * z;
+            ks[z] = i < E ? order_key(l[i]) : INT_MIN;
+            is[z] = i < E ? i : INT_MAX;
+        }
+        auto cswap = [&](int x, int y) {
+            if (ks[y] > ks[x] || (ks[y] == ks[x] && is[y] < is[x])) {
+                const int tk = ks[x], ti = is[x];
+                ks[x] = ks[y];
+                is[x] = is[y];
+                ks[y] = tk;
+                is[y] = ti;
+            }
+        };
+        cswap(0, 1);
+        cswap(2, 3);
+        cswap(0, 2);
+        cswap(1, 3);
+        cswap(1, 2);
+        for (int r = 0; r < K; ++r) {
+            const int mk = __reduce_max_sync(0xffffffffu, ks[0]);
+            const int wi = (int)__reduce_min_sync(0xffffffffu, ks[0] == mk ? (unsigned)is[0] : 0xffffffffu);
+            if (lane == 0) sel[r] = wi;
+            if ((wi & 31) == lane) {
+                ks[0] = ks[1];
+                ks[1] = ks[2];
+                ks[2] = ks[3];
+                ks[3] = INT_MIN;
+                is[0] = is[1];
+                is[1] = is[2];
+                is[2] = is[3];
+                is[3] = INT_MAX;
+            }
+        }
+    }
+    // more experts: K rounds of a warp arg-max over 64-bit keys (order key of
+    // the logit, then E - 1 - e): round r takes the largest key below round
+    // r - 1's, which is the r-th logit in descending order, ties to the lower index
     long long prev = LLONG_MAX;
-    for (int r = 0; r < K; ++r) {
+    for (int r = 0; E > 128 && r < K; ++r) {
         long long best = LLONG_MIN;
         for (int e = lane; e < E; e += 32) {
             const long long key = (long long)order_key(l[e]) * 4294967296LL + (long long)(E - 1 - e);

@@ -18,10 +18,10 @@ namespace qmoe {
 namespace {
 
 constexpr int RT_TOK = 8;     // tokens per router CTA
-constexpr int RT_EXP = 8;     // experts per router CTA (one warp each)
+constexpr int RT_EXP = 2;     // experts per router CTA (one warp each): E / 2 CTAs keep many SMs loading
 
 // logits[t][e] = sum_h Wr[e][h] x[t][h] (+ bias[e]), fp32 accumulation.
-__global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ x,
+__global__ void __launch_bounds__(32 * RT_EXP) router_kernel(const float* __restrict__ x,
                                                      const float* __restrict__ wr,
                                                      const float* __restrict__ bias, int T,
                                                      int H, int E, float* __restrict__ logits) {
@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ x
 #pragma unroll
     for (int i = 0; i < RT_TOK; ++i) acc[i] = 0.f;
     const float* wrow = wr + (size_t)e * H;
+#pragma unroll 4
     for (int h = 4 * lane; h < H; h += 128) {
         const float4 w = __ldg(reinterpret_cast<const float4*>(wrow + h));
 #pragma unroll
@@ -572,7 +573,7 @@ cudaError_t route_prepare() {
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
                          const float* bias, const Route& r, cudaStream_t st) {
     dim3 g1((s.E + RT_EXP - 1) / RT_EXP, (s.T + RT_TOK - 1) / RT_TOK);
-    router_kernel<<<g1, 256, 0, st>>>(x, router_w, bias, s.T, s.H, s.E, r.logits);
+    router_kernel<<<g1, 32 * RT_EXP, 0, st>>>(x, router_w, bias, s.T, s.H, s.E, r.logits);
     const int threads = 32 * (s.T >= 32 ? 32 : (s.T > 4 ? s.T : 4));
     topk_kernel<<<1, threads, 2 * s.E * sizeof(int32_t), st>>>(
         r.logits, s.T, s.E, s.K, s.norm_topk, r.ids, r.wts, r.n_used, r.used_expert,

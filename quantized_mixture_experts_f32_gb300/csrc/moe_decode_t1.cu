@@ -674,23 +674,37 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
     // groups of one down sub-scale
     const bool run_d = !abort_b && misc[MS_ABORT] == 0;
     if (run_d) {
-        for (int g = tid; g < K * (F / GS); g += TN) {
-            const int j = g / (F / GS), gl = g - j * (F / GS);
-            const float4* src = reinterpret_cast<const float4*>(p.act + (size_t)j * F + gl * GS);
-            float v[GS];
+        // two groups per thread per round, both groups' loads issued before any
+        // store (one L2 round trip per round instead of one per group)
+        const int ng = K * (F / GS);
+        for (int g0 = tid; g0 < ng; g0 += 2 * TN) {
+            float v[2][GS];
 #pragma unroll
-            for (int z = 0; z < GS / 4; ++z) {
-                const float4 w = __ldcg(src + z);
-                v[4 * z] = w.x; v[4 * z + 1] = w.y; v[4 * z + 2] = w.z; v[4 * z + 3] = w.w;
+            for (int u = 0; u < 2; ++u) {
+                const int g = g0 + u * TN;
+                const int j = g / (F / GS), gl = g - j * (F / GS);
+                const float4* src = reinterpret_cast<const float4*>(p.act + (size_t)j * F + gl * GS);
+#pragma unroll
+                for (int z = 0; z < GS / 4; ++z) {
+                    const float4 w = g < ng ? __ldcg(src + z) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u][4 * z] = w.x; v[u][4 * z + 1] = w.y; v[u][4 * z + 2] = w.z; v[u][4 * z + 3] = w.w;
+                }
             }
-            float s = 0.f;
 #pragma unroll
-            for (int z = 0; z < GS; ++z) s += v[z];
-            float* ast = act_st + (size_t)j * L.act_pitch;
+            for (int u = 0; u < 2; ++u) {
+                const int g = g0 + u * TN;
+                if (g >= ng) continue;
+                const int j = g / (F / GS), gl = g - j * (F / GS);
+                float s = 0.f;
 #pragma unroll
-            for (int z = 0; z < GS; z += 4)
-                *reinterpret_cast<float4*>(ast + apad1(gl * GS + z)) = make_float4(v[z], v[z + 1], v[z + 2], v[z + 3]);
-            ast[FPAD + gl] = s;
+                for (int z = 0; z < GS; ++z) s += v[u][z];
+                float* ast = act_st + (size_t)j * L.act_pitch;
+#pragma unroll
+                for (int z = 0; z < GS; z += 4)
+                    *reinterpret_cast<float4*>(ast + apad1(gl * GS + z)) =
+                        make_float4(v[u][z], v[u][z + 1], v[u][z + 2], v[u][z + 3]);
+                ast[FPAD + gl] = s;
+            }
         }
     }
     __syncthreads();

@@ -67,11 +67,16 @@ WORKLOADS = {
     "decode_q8k": dict(cfg="decode", copies=32, e2e=2000, steps=20000, warmup=200, q8k=True,
                        desc="qwen3moe-30b-a3b MoE layer decode, T=1, Q8_K activations (int8 "
                             "variant), Q4_K gate/up, Q6_K down (supplementary)"),
+    # supplementary: FP8 block-scaled experts (qmoe_forward_fp8) with the F32 router
+    "decode_fp8": dict(cfg=None, fp8="decode_fp8", copies=8, e2e=2000, steps=20000, warmup=200,
+                       desc="qwen3moe-30b-a3b MoE layer decode, T=1, FP8 (E4M3) experts with one "
+                            "fp32 scale per 128x128 block, F32 router (supplementary)"),
 }
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
-               "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None}
+               "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None,
+               "decode_fp8": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -247,6 +252,18 @@ def cpu_sample_layer(inp, seconds: float, max_tokens: int, q8k: bool = False):
                         f"oracle calls on the first {n} tokens of this layer workload")
 
 
+def cpu_sample_fp8(inp, seconds: float, max_tokens: int):
+    """The FP8 oracle on a bounded sample of the layer workload: tokens/s/layer."""
+    import oracle
+    oracle.build()
+    n = min(inp["T"], max_tokens)
+    one = dict(inp)
+    one["x"] = inp["x"][:n]
+    one["T"] = n
+    return cpu_baseline(lambda: oracle.moe_forward_fp8(one), n, seconds,
+                        f"FP8 oracle calls on the first {n} tokens of this layer workload")
+
+
 def cpu_sample_step(geo, seconds: float):
     import oracle
     oracle.build()
@@ -281,7 +298,16 @@ def run_reference(args):
     oracle.build()
     w = WORKLOADS[args.workload]
     budget = 150.0
-    if w["cfg"] is not None:
+    if w.get("fp8"):
+        inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]])
+        sample = min(inp["T"], 8)
+        one = dict(inp)
+        one["x"] = inp["x"][:sample]
+        one["T"] = sample
+        step = lambda: oracle.moe_forward_fp8(one)  # noqa: E731
+        tokens_per_step = sample
+        what = f"{sample} tokens of the {args.workload} layer workload per step"
+    elif w["cfg"] is not None:
         inp = synth.moe_inputs(synth.MOE_CONFIGS[w["cfg"]])
         sample = min(inp["T"], 8)
         one = dict(inp)
@@ -566,6 +592,81 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
     return res, cpu
 
 
+def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
+    """The MoE layer over FP8 block-scaled experts (qmoe_forward_fp8)."""
+    w = WORKLOADS[args.workload]
+    inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T"))
+    T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
+    names = ("router", "gate", "gate_scale", "up", "up_scale", "down", "down_scale")
+    x = torch.from_numpy(inp["x"]).to(dev)
+    base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev) for n in names}
+    R = args.copies
+    copies = [base] + [{n: t.clone() for n, t in base.items()} for _ in range(R - 1)]
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream))
+
+    def fwd(c, xin, o, ids=None):
+        q.qmoe_forward_fp8(ctx, xin, c["router"], c["gate"], c["gate_scale"], c["up"],
+                           c["up_scale"], c["down"], c["down_scale"], T, o, ids, None)
+
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        fwd(base, x, out, ids)
+    stream.synchronize()
+    distinct = len(np.unique(ids.cpu().numpy()))
+    per_expert = 3 * F * H + 4 * (inp["gate_scale"][0].size + inp["up_scale"][0].size
+                                  + inp["down_scale"][0].size)
+    ebytes = distinct * per_expert
+    rbytes = E * H * 4
+    ms, clocks = timed_graphs(torch, stream, [(lambda c=c: fwd(c, x, out)) for c in copies],
+                              args.steps, args.warmup, pg, dev, local)
+    secs = ms / 1e3
+    step_s = secs / args.steps
+    # e2e: pinned host x copied in, the layer, the result copied out, then a sync
+    hin = torch.from_numpy(inp["x"].copy()).pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    xin = torch.empty_like(x)
+
+    def host_step(c):
+        with torch.cuda.stream(stream):
+            xin.copy_(hin, non_blocking=True)
+            fwd(c, xin, out)
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(3):
+        host_step(copies[i % R])
+    if pg:
+        pg.barrier()
+    te0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        host_step(copies[i % R])
+    te = time.perf_counter() - te0
+    if pg:
+        tt = torch.tensor([te], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        te = float(tt.item())
+    q.qmoe_destroy(ctx)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = (ebytes + rbytes) * R
+    res = dict(
+        value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
+        ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
+        e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
+        launches=q.LAUNCHES_PER_FP8_FORWARD if T < 16 else q.LAUNCHES_PER_FP8_FORWARD_MANY,
+        config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
+                "tokens": T, "distinct_experts": distinct, "expert_bytes": per_expert,
+                "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
+                      f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
+                      "written right before the timed region"},
+        kernel="whole FP8 layer call (router, top-k, gate/up, down, combine)",
+        dtype="e4m3 weights widened exactly, f32 activations and accumulate")
+    cpu = None
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        cpu = cpu_sample_fp8(inp, args.cpu_seconds, 8)
+    return res, cpu
+
+
 def bench_step48(args, torch, q, dev, stream, ws, pg, local):
     geo = dict(synth.STEP_DEFAULT)
     L, H, E, K, F = geo["n_layers"], geo["H"], geo["E"], geo["K"], geo["F"]
@@ -775,6 +876,8 @@ def main():
         res, cpu = bench_step48(args, torch, q, dev, stream, ws, pg, local)
     elif args.workload == "prefill_layer":
         res, cpu = bench_prefill_layer(args, torch, q, dev, stream, ws, pg, local)
+    elif WORKLOADS[args.workload].get("fp8"):
+        res, cpu = bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local)
     else:
         res, cpu = bench_layer(args, torch, q, dev, stream, ws, pg, local)
     hbm, tf, kind = peaks()

@@ -15,6 +15,7 @@
  *
  * qmoe_forward_q8k runs the same layer with x and a quantised to 8-bit (Q8_K)
  * activations before every expert GEMV (the int8 variant of "Gaps ... G8").
+ * qmoe_forward_fp8 runs it over FP8 block-scaled experts instead of k-quants.
  *
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer that the caller allocated and owns
@@ -140,6 +141,30 @@ qmoe_status qmoe_forward_q8k(qmoe_ctx* ctx, const float* hidden_in, const float*
                              const void* gate_exps, const void* up_exps, const void* down_exps,
                              qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t,
                              int n_tokens, float* hidden_out, int32_t* ids_out, float* weights_out);
+
+/* The MoE layer over FP8 block-scaled experts with the F32 router (atlasinference
+ * source page "spark_model/weight_loader/qwen3.rs", load_layers: experts kept as
+ * FP8 with one scale per 128 x 128 block, FP8 weights against wider
+ * activations, and the option of a full-precision router so that expert
+ * selection is not decided by quantised logits).
+ *   gate_exps / up_exps: E4M3 ("e4m3fn") codes [E][ffn][hidden], one byte each;
+ *   down_exps: codes [E][hidden][ffn];
+ *   gate_scale / up_scale: fp32 [E][ffn/128][hidden/128];
+ *   down_scale: fp32 [E][hidden/128][ffn/128];
+ *   weight (r, c) of expert e = e4m3(code) * scale[e][r/128][c/128].
+ * Codes 0x7F / 0xFF (NaN) are not valid weights.  x, the SwiGLU output and
+ * every sum are fp32.  hidden_out = hidden_in + MoE(hidden_in); it may alias
+ * hidden_in for any n_tokens.  ids_out / weights_out as qmoe_forward_ex
+ * (nullable).  Serves hidden/256 in {2, 4, 8, 16} and ffn/256 in 1..6
+ * (QMOE_ERR_SHAPE otherwise).  Code and activation pointers 16-byte aligned,
+ * scale pointers 4-byte aligned (QMOE_ERR_MISALIGNED).  Argument errors are
+ * returned before any launch. */
+qmoe_status qmoe_forward_fp8(qmoe_ctx* ctx, const float* hidden_in, const float* router_w,
+                             const void* gate_exps, const float* gate_scale,
+                             const void* up_exps, const float* up_scale,
+                             const void* down_exps, const float* down_scale,
+                             int n_tokens, float* hidden_out, int32_t* ids_out,
+                             float* weights_out);
 
 /* Same as qmoe_forward, but hidden_in / hidden_out are HOST pointers (pinned
  * memory gives asynchronous copies).  Copies the activations to the device

@@ -20,7 +20,11 @@ whole is pinned only through its pinned parts.  The Q8_K-activation functions
 (``q8k_quantize``, ``q8k_dot``, ``moe_ffn_q8k``) follow a reading of a format the
 pages name without defining (the GGUF 8-bit activation block); they are pinned
 by invariants, exact cases and the independent numpy dequantiser.  ``prefill_layer``
-is pinned against a batched causal formulation written in the tests.
+is pinned against a batched causal formulation written in the tests.  The FP8
+functions (``fp8_e4m3_to_double``, ``fp8_dequant_matrix``, ``moe_ffn_fp8``) are
+pinned against the E4M3 definition, torch's float8_e4m3fn conversion and a
+dense numpy brute force (atlasinference source page
+"spark_model/weight_loader/qwen3.rs", load_layers: FP8 block-128 weights).
 """
 from __future__ import annotations
 
@@ -89,6 +93,13 @@ def lib():
             L.qo_dot_q8k.restype = C.c_double
             L.qo_moe_ffn_q8k.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, dp, ip,
                                          dp, up8, C.c_int, up8, C.c_int, up8, C.c_int, dp, dp]
+            L.qo_fp8_e4m3_to_double.argtypes = [C.c_uint8]
+            L.qo_fp8_e4m3_to_double.restype = C.c_double
+            L.qo_fp8_dequant_matrix.argtypes = [up8, fp, C.c_long, C.c_long, dp]
+            L.qo_fp8_scale_count.argtypes = [C.c_long, C.c_long]
+            L.qo_fp8_scale_count.restype = C.c_long
+            L.qo_moe_ffn_fp8.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, dp, ip,
+                                         dp, up8, fp, up8, fp, up8, fp, dp, dp, dp]
             L.qo_decode_layer.argtypes = (
                 [C.c_int] * 8 + [C.c_double, C.c_double, C.c_int, dp] + [fp] * 4 + [up8] * 4
                 + [fp, up8, up8, up8, C.c_int, u16, u16, ip, fp, ip, dp, dp, dp])
@@ -240,6 +251,69 @@ def moe_forward(inp: dict, norm_topk=True, force=None):
                                   force)
     out = moe_ffn(inp["x"], ids, w, inp["gate"], inp["up"], inp["down"], inp["gate_t"],
                   inp["up_t"], inp["down_t"], inp["F"], inp["E"])
+    return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
+
+
+# ----------------------------------------------------------------------------- FP8 experts
+
+def fp8_e4m3_to_double(code: int) -> float:
+    """Value of one E4M3 ("e4m3fn") code; NaN for S.1111.111."""
+    return lib().qo_fp8_e4m3_to_double(int(code) & 0xFF)
+
+
+def fp8_scale_count(rows: int, cols: int) -> int:
+    """Number of fp32 block scales (one per 128 x 128 tile) of a [rows][cols] matrix."""
+    return lib().qo_fp8_scale_count(rows, cols)
+
+
+def fp8_dequant_matrix(codes: np.ndarray, scale: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """W[r][c] = e4m3(codes[r][c]) * scale[r // 128][c // 128], in double."""
+    codes = _u8(codes).reshape(-1)
+    scale = _f32(scale).reshape(-1)
+    if codes.size != rows * cols or scale.size != fp8_scale_count(rows, cols):
+        raise ValueError("fp8_dequant_matrix: size mismatch")
+    out = np.empty((rows, cols), dtype=np.float64)
+    lib().qo_fp8_dequant_matrix(_p(codes, C.c_uint8), _p(scale, C.c_float), rows, cols,
+                                _p(out, C.c_double))
+    return out
+
+
+def moe_ffn_fp8(x, ids, w, gate, gate_scale, up, up_scale, down, down_scale, F, E, res=None,
+                want_act=False):
+    """out [T][H] (f64) = res + sum_j w_j * Wd(silu(Wg x) * Wu x) over FP8 block-scaled
+    experts (gate/up [E][F][H] codes, down [E][H][F], fp32 scales per 128 x 128 tile)."""
+    x = _f64(np.atleast_2d(x))
+    T, H = x.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    K = ids.shape[1]
+    w = _f64(w)
+    res = None if res is None else _f64(np.atleast_2d(res))
+    if (_u8(gate).size != E * F * H or _u8(up).size != E * F * H or _u8(down).size != E * H * F
+            or _f32(gate_scale).size != E * fp8_scale_count(F, H)
+            or _f32(up_scale).size != E * fp8_scale_count(F, H)
+            or _f32(down_scale).size != E * fp8_scale_count(H, F)):
+        raise ValueError("moe_ffn_fp8: tensor sizes do not match E, F, H")
+    out = np.empty((T, H), dtype=np.float64)
+    act = np.empty((T, K, F), dtype=np.float64) if want_act else None
+    g8, u8, d8 = _u8(gate).reshape(-1), _u8(up).reshape(-1), _u8(down).reshape(-1)
+    gs, us, ds = (_f32(a).reshape(-1) for a in (gate_scale, up_scale, down_scale))
+    rc = lib().qo_moe_ffn_fp8(T, H, F, E, K, _p(x, C.c_double), _p(res, C.c_double),
+                              _p(ids, C.c_int32), _p(w, C.c_double), _p(g8, C.c_uint8),
+                              _p(gs, C.c_float), _p(u8, C.c_uint8), _p(us, C.c_float),
+                              _p(d8, C.c_uint8), _p(ds, C.c_float), _p(out, C.c_double),
+                              _p(act, C.c_double), None)
+    if rc:
+        raise ValueError(f"moe_ffn_fp8 failed rc={rc}")
+    return (out, act) if want_act else out
+
+
+def moe_forward_fp8(inp: dict, norm_topk=True, force=None):
+    """out = x + MoE(x) over FP8 block-scaled experts with the F32 router (the
+    full-precision router option of the atlasinference Qwen3 loader)."""
+    logits, ids, w, probs = route(inp["x"], inp["router"], inp["K"], inp.get("bias"), norm_topk,
+                                  force)
+    out = moe_ffn_fp8(inp["x"], ids, w, inp["gate"], inp["gate_scale"], inp["up"],
+                      inp["up_scale"], inp["down"], inp["down_scale"], inp["F"], inp["E"])
     return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
 
 

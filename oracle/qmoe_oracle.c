@@ -24,8 +24,15 @@
  *       "The fix" (Q/K norm after bias, before RoPE).
  *  [P5] SharpInference issue "Forward-pass divergence on Qwen3-Coder 30B-A3B",
  *       closing comment (NEOX RoPE: rotated pairs offset by head_dim/2).
+ *  [P3] atlasinference source page "spark_model/weight_loader/qwen3.rs",
+ *       function load_layers, branches "Native FP8 MoE" and "Native FP8
+ *       Attention" (FP8 block-scaled weights with block size 128, loaded for
+ *       FP8-weight / 16-bit-activation GEMMs, the "w8a16" remark) and the
+ *       router-precision option (router kept in full precision while the
+ *       experts stay FP8).
  *  The bit layout inside a Q4_K / Q6_K superblock is the public GGUF k-quant
- *  format; the pages fix only the superblock sizes and field order.
+ *  format; the pages fix only the superblock sizes and field order.  The FP8
+ *  code is the OCP E4M3 ("e4m3fn") format; the pages fix only the block size.
  */
 #include <math.h>
 #include <stdint.h>
@@ -229,22 +236,22 @@ static void matvec(const double* W, long rows, long cols, const double* x, doubl
     }
 }
 
-/* MoE FFN of T tokens ([P2] "Gaps ... G3"): for each token t and slot j with
- * expert e = ids[t][j]:
- *   g = Wg_e x_t, u = Wu_e x_t           (Q4_K gate/up, [F][H], dequantised)
+/* Loader of one used expert's three matrices as dense doubles: Wg, Wu [F][H]
+ * and Wd [H][F]. */
+typedef void (*qo_expert_loader)(const void* ctx, int e, long H, long F, double* Wg, double* Wu,
+                                 double* Wd);
+
+/* The MoE FFN of T tokens ([P2] "Gaps ... G3") once the experts are dense:
+ * for each token t and slot j with expert e = ids[t][j]:
+ *   g = Wg_e x_t, u = Wu_e x_t           (gate/up, [F][H])
  *   a = silu(g) * u                      (fused SwiGLU)
- *   y_tj = Wd_e a                        (Q6_K or Q4_K down, [H][F])
+ *   y_tj = Wd_e a                        (down, [H][F])
  *   out_t = res_t + sum_j w[t][j] y_tj   (weighted sum into the residual,
  *                                         summed in slot order j = 0..K-1)
- * Expert e of each 3-D tensor is read in place at base + e*stride.
  * act (nullable) receives a [T][K][F]; ys (nullable) receives y [T][K][H]. */
-int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double* res,
-               const int32_t* ids, const double* w,
-               const uint8_t* gate, int gate_t, const uint8_t* up, int up_t,
-               const uint8_t* down, int down_t, double* out, double* act, double* ys) {
-    long sg = qo_expert_stride(gate_t, F, H), su = qo_expert_stride(up_t, F, H);
-    long sd = qo_expert_stride(down_t, H, F);
-    if (sg < 0 || su < 0 || sd < 0) return -1;
+static int moe_ffn_dense(int T, int H, int F, int E, int K, const double* x, const double* res,
+                         const int32_t* ids, const double* w, qo_expert_loader load,
+                         const void* ctx, double* out, double* act, double* ys) {
     for (long p = 0; p < (long)T * K; ++p)
         if (ids[p] < 0 || ids[p] >= E) return -2;
     double* Y = (double*)malloc(sizeof(double) * (size_t)T * K * H);
@@ -265,9 +272,7 @@ int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double*
 #pragma omp atomic write
             err = 1;
         } else {
-            qo_dequant_matrix(gate_t, gate + (long)e * sg, F, H, Wg);
-            qo_dequant_matrix(up_t, up + (long)e * su, F, H, Wu);
-            qo_dequant_matrix(down_t, down + (long)e * sd, H, F, Wd);
+            load(ctx, e, H, F, Wg, Wu, Wd);
             for (long p = 0; p < (long)T * K; ++p) {
                 if (ids[p] != e) continue;
                 long t = p / K;
@@ -290,6 +295,90 @@ int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double*
     if (ys) memcpy(ys, Y, sizeof(double) * (size_t)T * K * H);
     free(Y);
     return 0;
+}
+
+typedef struct {
+    const uint8_t *gate, *up, *down;
+    int gate_t, up_t, down_t;
+    long sg, su, sd;
+} kquant_experts;
+
+/* Expert e of each 3-D k-quant tensor is read in place at base + e*stride
+ * ([P2] "File facts"). */
+static void load_kquant_expert(const void* ctx, int e, long H, long F, double* Wg, double* Wu,
+                               double* Wd) {
+    const kquant_experts* k = (const kquant_experts*)ctx;
+    qo_dequant_matrix(k->gate_t, k->gate + (long)e * k->sg, F, H, Wg);
+    qo_dequant_matrix(k->up_t, k->up + (long)e * k->su, F, H, Wu);
+    qo_dequant_matrix(k->down_t, k->down + (long)e * k->sd, H, F, Wd);
+}
+
+/* MoE FFN over k-quant experts: Q4_K gate/up [F][H], Q6_K or Q4_K down [H][F]. */
+int qo_moe_ffn(int T, int H, int F, int E, int K, const double* x, const double* res,
+               const int32_t* ids, const double* w,
+               const uint8_t* gate, int gate_t, const uint8_t* up, int up_t,
+               const uint8_t* down, int down_t, double* out, double* act, double* ys) {
+    kquant_experts k = {gate, up, down, gate_t, up_t, down_t,
+                        qo_expert_stride(gate_t, F, H), qo_expert_stride(up_t, F, H),
+                        qo_expert_stride(down_t, H, F)};
+    if (k.sg < 0 || k.su < 0 || k.sd < 0) return -1;
+    return moe_ffn_dense(T, H, F, E, K, x, res, ids, w, load_kquant_expert, &k, out, act, ys);
+}
+
+/* ------------------------------------------------------------------ FP8 block-scaled experts */
+
+/* One FP8 E4M3 code (the "fn" variant: sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; no infinities; S.1111.111 is NaN).  A zero exponent field
+ * is subnormal: m/8 * 2^-6.  Largest finite magnitude 1.75 * 2^8 = 448. */
+double qo_fp8_e4m3_to_double(uint8_t c) {
+    int s = c >> 7, ex = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (ex == 15 && m == 7) return NAN;
+    if (ex == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, ex - 7);
+    return s ? -v : v;
+}
+
+/* Block-scaled FP8 matrix ([P3]: FP8 weights with block size 128): codes
+ * [rows][cols] e4m3 and one fp32 scale per 128 x 128 tile, stored as
+ * scale[(r/128) * ceil(cols/128) + c/128]; W[r][c] = e4m3(code) * scale. */
+void qo_fp8_dequant_matrix(const uint8_t* codes, const float* scale, long rows, long cols,
+                           double* out) {
+    long nb = (cols + 127) / 128;
+    for (long r = 0; r < rows; ++r)
+        for (long c = 0; c < cols; ++c)
+            out[r * cols + c] = qo_fp8_e4m3_to_double(codes[r * cols + c]) *
+                                (double)scale[(r / 128) * nb + c / 128];
+}
+
+long qo_fp8_scale_count(long rows, long cols) { return ((rows + 127) / 128) * ((cols + 127) / 128); }
+
+typedef struct {
+    const uint8_t *gate, *up, *down;
+    const float *gs, *us, *ds;
+} fp8_experts;
+
+/* Expert e of each 3-D tensor at e * rows * cols codes and
+ * e * qo_fp8_scale_count(rows, cols) scales. */
+static void load_fp8_expert(const void* ctx, int e, long H, long F, double* Wg, double* Wu,
+                            double* Wd) {
+    const fp8_experts* k = (const fp8_experts*)ctx;
+    long nfh = qo_fp8_scale_count(F, H), nhf = qo_fp8_scale_count(H, F);
+    qo_fp8_dequant_matrix(k->gate + (long)e * F * H, k->gs + (long)e * nfh, F, H, Wg);
+    qo_fp8_dequant_matrix(k->up + (long)e * F * H, k->us + (long)e * nfh, F, H, Wu);
+    qo_fp8_dequant_matrix(k->down + (long)e * H * F, k->ds + (long)e * nhf, H, F, Wd);
+}
+
+/* MoE FFN over FP8 block-scaled experts: gate/up [E][F][H] codes with
+ * [E][ceil(F/128)][ceil(H/128)] scales, down [E][H][F] with
+ * [E][ceil(H/128)][ceil(F/128)]. */
+int qo_moe_ffn_fp8(int T, int H, int F, int E, int K, const double* x, const double* res,
+                   const int32_t* ids, const double* w, const uint8_t* gate, const float* gate_scale,
+                   const uint8_t* up, const float* up_scale, const uint8_t* down,
+                   const float* down_scale, double* out, double* act, double* ys) {
+    if (H <= 0 || F <= 0) return -1;
+    fp8_experts k = {gate, up, down, gate_scale, up_scale, down_scale};
+    return moe_ffn_dense(T, H, F, E, K, x, res, ids, w, load_fp8_expert, &k, out, act, ys);
 }
 
 /* ------------------------------------------------------------------ Q8_K activations */

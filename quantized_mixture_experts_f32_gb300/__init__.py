@@ -32,6 +32,11 @@ LAUNCHES_PER_DECODE_FORWARD = 1
 LAUNCHES_PER_PREFILL_FORWARD = 7
 # qmoe_forward_q8k: router, top-k, quantise x, gate/up, quantise act, down, combine
 LAUNCHES_PER_Q8K_FORWARD = 7
+# qmoe_forward_fp8 below 16 tokens: router, top-k (with the per-expert lists),
+# gate/up, down, combine; from 16 tokens: router GEMM, top-k, per-expert lists,
+# gate/up, down, combine
+LAUNCHES_PER_FP8_FORWARD = 5
+LAUNCHES_PER_FP8_FORWARD_MANY = 6
 # one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
 # its RMSNorm)
@@ -47,7 +52,7 @@ LAUNCHES_PER_PREFILL_LAYER_ATTN = 7
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_prefill", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
-            "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_noalloc_status",
+            "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_forward_fp8", "qmoe_noalloc_status",
             "qmoe_debug_stall_next", "qmoe_debug_fail_alloc"]
 
 
@@ -93,6 +98,8 @@ def _load():
     L.qmoe_forward_host.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp]
     L.qmoe_forward_q8k.argtypes = [vp, fp, fp, vp, vp, vp, i, i, i, i, fp, ip, fp]
     L.qmoe_forward_q8k.restype = i
+    L.qmoe_forward_fp8.argtypes = [vp, fp, fp, vp, fp, vp, fp, vp, fp, i, fp, ip, fp]
+    L.qmoe_forward_fp8.restype = i
     L.qmoe_forward_host.restype = i
     L.qmoe_decode_step.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, fp, ip]
     L.qmoe_decode_step.restype = i
@@ -175,6 +182,14 @@ def qmoe_forward_q8k(ctx, hidden_in, router_w, gate_exps, up_exps, down_exps, ga
     _check(ctx, lib.qmoe_forward_q8k(ctx, _ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
                                      _ptr(up_exps), _ptr(down_exps), gate_t, up_t, down_t,
                                      n_tokens, _ptr(hidden_out), _ptr(ids_out), _ptr(weights_out)))
+
+
+def qmoe_forward_fp8(ctx, hidden_in, router_w, gate_exps, gate_scale, up_exps, up_scale,
+                     down_exps, down_scale, n_tokens, hidden_out, ids_out=None, weights_out=None):
+    _check(ctx, lib.qmoe_forward_fp8(ctx, _ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
+                                     _ptr(gate_scale), _ptr(up_exps), _ptr(up_scale),
+                                     _ptr(down_exps), _ptr(down_scale), n_tokens,
+                                     _ptr(hidden_out), _ptr(ids_out), _ptr(weights_out)))
 
 
 def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,

@@ -1,0 +1,240 @@
+// moe_fp8.cu -- expert GEMVs of the MoE FFN over FP8 block-scaled experts.
+//
+// atlasinference source page "spark_model/weight_loader/qwen3.rs", load_layers:
+// experts stored as FP8 with one scale per 128 x 128 block ("Native FP8 MoE"),
+// consumed with FP8 weights and 16-bit-or-wider activations (the "w8a16"
+// remark), routed by a full-precision router.  Codes are OCP E4M3 ("e4m3fn");
+// W[r][c] = e4m3(code[r][c]) * scale[r / 128][c / 128].  Layout per 3-D tensor:
+// codes [E][rows][cols] bytes, scales [E][rows/128][cols/128] fp32.
+//
+// Each E4M3 pair is widened with the hardware e4m3x2 -> f16x2 conversion (exact:
+// every E4M3 value is an fp16 value), then to fp32; x, act and every sum are
+// fp32.  A 16-byte chunk of a row (16 weights) never straddles a 128-column
+// scale block, so a lane multiplies its chunk's partial dot by one scale.
+//
+// Work is expert-centric and grid-strided: a warp item is two rows (one per
+// half-warp) of gate and up, or four rows of down, of one used expert; the
+// lane's chunks of every row of the item are loaded before any is used, so a
+// warp keeps 16 to 24 16-byte loads in flight.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "qmoe_internal.h"
+
+namespace qmoe {
+
+namespace {
+
+constexpr int F8_THREADS = 256;
+
+__device__ __forceinline__ float2 e4m3x2_f2(uint32_t two) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    return __half22float2(__half2(r));
+}
+
+// dot of 16 E4M3 weights (one 16-byte chunk) with 16 consecutive fp32 values
+__device__ __forceinline__ float chunk_dot(uint4 w, const float* __restrict__ v) {
+    const float4* v4 = reinterpret_cast<const float4*>(v);
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 x = __ldg(v4 + i);
+        const float2 lo = e4m3x2_f2(q[i] & 0xffffu), hi = e4m3x2_f2(q[i] >> 16);
+        a0 = fmaf(lo.x, x.x, a0);
+        a1 = fmaf(lo.y, x.y, a1);
+        a0 = fmaf(hi.x, x.z, a0);
+        a1 = fmaf(hi.y, x.w, a1);
+    }
+    return a0 + a1;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// sum over the 16 lanes of a half-warp (every lane gets its half's sum)
+__device__ __forceinline__ float half_sum(float v) {
+#pragma unroll
+    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
+// and f0 + 1 (half-warp hw takes row f0 + hw of both gate and up).  Lane chunk k
+// of a row covers columns 16 ((lane & 15) + 16 k) .. +15, k < NC = H / 256.
+// act[p][f] = silu(g) * u for every pair p routed to the expert.
+template <int NC>
+__global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
+    const float* __restrict__ x, int H, int F, int K, const uint8_t* __restrict__ gate,
+    const float* __restrict__ gs, const uint8_t* __restrict__ up, const float* __restrict__ us,
+    const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
+    const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
+    float* __restrict__ act) {
+    const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
+    const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * F8_THREADS) >> 5;
+    const int per = F >> 1, nbh = H >> 7;
+    const int items = *n_used * per;
+    for (int i = gw; i < items; i += nw) {
+        const int u = i / per, f = 2 * (i - u * per) + hw;
+        const int e = used_expert[u];
+        const size_t row = (size_t)e * F + f;
+        const uint8_t* gr = gate + row * H + 16 * hl;
+        const uint8_t* ur = up + row * H + 16 * hl;
+        const size_t sb = ((size_t)e * (F >> 7) + (f >> 7)) * nbh;
+        uint4 wg[NC], wu[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            wg[k] = ld_stream(gr + 256 * k);
+            wu[k] = ld_stream(ur + 256 * k);
+        }
+        float sg[NC], su[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            sg[k] = __ldg(gs + sb + 2 * k + (hl >> 3));
+            su[k] = __ldg(us + sb + 2 * k + (hl >> 3));
+        }
+        const int p0 = used_first[u], p1 = used_first[u + 1];
+        for (int q = p0; q < p1; ++q) {
+            const int p = pair_list[q];
+            const float* xt = x + (size_t)(p / K) * H + 16 * hl;
+            float g = 0.f, v = 0.f;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                g = fmaf(sg[k], chunk_dot(wg[k], xt + 256 * k), g);
+                v = fmaf(su[k], chunk_dot(wu[k], xt + 256 * k), v);
+            }
+            g = half_sum(g);
+            v = half_sum(v);
+            if (hl == 0) act[(size_t)p * F + f] = g / (1.f + expf(-g)) * v;
+        }
+    }
+}
+
+// Down projection.  Item i -> used expert u = i / (H/4), rows h0 = 4 (i % (H/4)) ..
+// h0 + 3; half-warp hw takes rows h0 + hw and h0 + 2 + hw.  Lane chunk k of a row
+// covers columns 16 ((lane & 15) + 16 k) .. +15, k < NC = F / 256.
+// y[p][h] = (Wd_e act_p)[h] for every pair p routed to the expert.
+template <int NC>
+__global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
+    const float* __restrict__ act, int H, int F, const uint8_t* __restrict__ down,
+    const float* __restrict__ ds, const int32_t* __restrict__ n_used,
+    const int32_t* __restrict__ used_expert, const int32_t* __restrict__ used_first,
+    const int32_t* __restrict__ pair_list, float* __restrict__ y) {
+    const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
+    const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
+    const int nw = (gridDim.x * F8_THREADS) >> 5;
+    const int per = H >> 2, nbf = F >> 7;
+    const int items = *n_used * per;
+    for (int i = gw; i < items; i += nw) {
+        const int u = i / per, h = 4 * (i - u * per) + hw;
+        const int e = used_expert[u];
+        const size_t row = (size_t)e * H + h;
+        const uint8_t* r0 = down + row * F + 16 * hl;
+        const uint8_t* r1 = r0 + 2 * (size_t)F;
+        uint4 w0[NC], w1[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            w0[k] = ld_stream(r0 + 256 * k);
+            w1[k] = ld_stream(r1 + 256 * k);
+        }
+        // rows h and h + 2 lie in one 128-row block (h0 is a multiple of 4)
+        const size_t sb = ((size_t)e * (H >> 7) + (h >> 7)) * nbf;
+        float s[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) s[k] = __ldg(ds + sb + 2 * k + (hl >> 3));
+        const int p0 = used_first[u], p1 = used_first[u + 1];
+        for (int q = p0; q < p1; ++q) {
+            const int p = pair_list[q];
+            const float* ap = act + (size_t)p * F + 16 * hl;
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                a = fmaf(s[k], chunk_dot(w0[k], ap + 256 * k), a);
+                b = fmaf(s[k], chunk_dot(w1[k], ap + 256 * k), b);
+            }
+            a = half_sum(a);
+            b = half_sum(b);
+            if (hl == 0) {
+                y[(size_t)p * H + h] = a;
+                y[(size_t)p * H + h + 2] = b;
+            }
+        }
+    }
+}
+
+// CTAs of a launch: enough for every warp item, at most the CTAs that are
+// resident at once (the kernels stride over the items)
+template <typename Kern>
+int fp8_grid(Kern kern, int* resident, int items, int num_sms) {
+    if (!*resident) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, F8_THREADS, 0) != cudaSuccess || n < 1)
+            n = 1;
+        *resident = n;
+    }
+    const int warps = F8_THREADS / 32;
+    const int need = (items + warps - 1) / warps;
+    const int cap = num_sms * *resident;
+    return need < cap ? (need > 0 ? need : 1) : cap;
+}
+
+template <int NC>
+cudaError_t gateup_nc(const MoeShape& s, const float* x, const Fp8Experts& w, const Route& r,
+                      float* act, int items, int num_sms, cudaStream_t st) {
+    static int resident = 0;   // per instantiation
+    const int grid = fp8_grid(fp8_gateup_kernel<NC>, &resident, items, num_sms);
+    fp8_gateup_kernel<NC><<<grid, F8_THREADS, 0, st>>>(x, s.H, s.F, s.K, w.gate, w.gate_scale, w.up,
+                                                      w.up_scale, r.n_used, r.used_expert,
+                                                      r.used_first, r.pair_list, act);
+    return cudaGetLastError();
+}
+
+template <int NC>
+cudaError_t down_nc(const MoeShape& s, const float* act, const Fp8Experts& w, const Route& r,
+                    float* y, int items, int num_sms, cudaStream_t st) {
+    static int resident = 0;   // per instantiation
+    const int grid = fp8_grid(fp8_down_kernel<NC>, &resident, items, num_sms);
+    fp8_down_kernel<NC><<<grid, F8_THREADS, 0, st>>>(act, s.H, s.F, w.down, w.down_scale, r.n_used,
+                                                    r.used_expert, r.used_first, r.pair_list, y);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fp8_supported(int H, int F) {
+    const int nh = H / 256, nf = F / 256;
+    return H % 256 == 0 && F % 256 == 0 && (nh == 2 || nh == 4 || nh == 8 || nh == 16) &&
+           (nf >= 1 && nf <= 6);
+}
+
+cudaError_t launch_fp8_experts(const MoeShape& s, const float* x, const Fp8Experts& w,
+                               const Route& r, float* act, float* y, int num_sms, cudaStream_t st) {
+    if (!fp8_supported(s.H, s.F)) return cudaErrorInvalidValue;
+    const int maxu = s.T * s.K < s.E ? s.T * s.K : s.E;   // used experts, an upper bound
+    const int i1 = maxu * (s.F / 2), i2 = maxu * (s.H / 4);
+    cudaError_t e;
+    switch (s.H / 256) {
+        case 2: e = gateup_nc<2>(s, x, w, r, act, i1, num_sms, st); break;
+        case 4: e = gateup_nc<4>(s, x, w, r, act, i1, num_sms, st); break;
+        case 8: e = gateup_nc<8>(s, x, w, r, act, i1, num_sms, st); break;
+        default: e = gateup_nc<16>(s, x, w, r, act, i1, num_sms, st); break;
+    }
+    if (e != cudaSuccess) return e;
+    switch (s.F / 256) {
+        case 1: return down_nc<1>(s, act, w, r, y, i2, num_sms, st);
+        case 2: return down_nc<2>(s, act, w, r, y, i2, num_sms, st);
+        case 3: return down_nc<3>(s, act, w, r, y, i2, num_sms, st);
+        case 4: return down_nc<4>(s, act, w, r, y, i2, num_sms, st);
+        case 5: return down_nc<5>(s, act, w, r, y, i2, num_sms, st);
+        default: return down_nc<6>(s, act, w, r, y, i2, num_sms, st);
+    }
+}
+
+}  // namespace qmoe

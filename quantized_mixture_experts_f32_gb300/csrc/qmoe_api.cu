@@ -479,6 +479,46 @@ qmoe_status qmoe_forward_q8k(qmoe_ctx* c, const float* hidden_in, const float* r
     return QMOE_OK;
 }
 
+qmoe_status qmoe_forward_fp8(qmoe_ctx* c, const float* hidden_in, const float* router_w,
+                             const void* gate_exps, const float* gate_scale, const void* up_exps,
+                             const float* up_scale, const void* down_exps,
+                             const float* down_scale, int n_tokens, float* hidden_out,
+                             int32_t* ids_out, float* weights_out) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    if (!hidden_in || !router_w || !gate_exps || !gate_scale || !up_exps || !up_scale ||
+        !down_exps || !down_scale || !hidden_out)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null tensor pointer");
+    const qmoe_config& k = c->cfg;
+    if (n_tokens < 1 || n_tokens > k.max_tokens)
+        return fail(c, QMOE_ERR_SHAPE, "n_tokens=%d outside 1..max_tokens=%d", n_tokens, k.max_tokens);
+    if (!qmoe::fp8_supported(k.hidden, k.ffn))
+        return fail(c, QMOE_ERR_SHAPE, "FP8 experts serve hidden/256 in {2,4,8,16} and ffn/256 in 1..6 (hidden=%d ffn=%d)", k.hidden, k.ffn);
+    if (!aligned16(hidden_in) || !aligned16(router_w) || !aligned16(gate_exps) ||
+        !aligned16(up_exps) || !aligned16(down_exps) || !aligned16(hidden_out))
+        return fail(c, QMOE_ERR_MISALIGNED, "activation, router and code base pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(gate_scale) | reinterpret_cast<uintptr_t>(up_scale) |
+         reinterpret_cast<uintptr_t>(down_scale)) & 3u)
+        return fail(c, QMOE_ERR_MISALIGNED, "scale pointers must be 4-byte aligned");
+    qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    const bool many = n_tokens >= 16 && qmoe::route_many_supported(ms, c->route);
+    cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
+                         : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    const qmoe::Fp8Experts w{static_cast<const uint8_t*>(gate_exps), gate_scale,
+                             static_cast<const uint8_t*>(up_exps), up_scale,
+                             static_cast<const uint8_t*>(down_exps), down_scale};
+    e = qmoe::launch_fp8_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "FP8 expert launch");
+    e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    if (ids_out || weights_out) {
+        e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
+}
+
 qmoe_status qmoe_forward_host(qmoe_ctx* c, const float* hin, const float* router_w,
                               const void* gate_exps, const void* up_exps, const void* down_exps,
                               qmoe_qtype gate_t, qmoe_qtype up_t, qmoe_qtype down_t, int n_tokens,

@@ -79,6 +79,22 @@ cudaError_t launch_moe_q8k(const MoeShape& s, const float* x, const float* res, 
 cudaError_t copy_route_out(const MoeShape& s, const Route& r, int32_t* ids_out, float* w_out,
                            cudaStream_t st);
 
+// FP8 block-scaled experts (moe_fp8.cu): E4M3 codes [E][rows][cols] and one fp32
+// scale per 128 x 128 block [E][rows/128][cols/128]; gate/up [F][H], down [H][F].
+struct Fp8Experts {
+    const uint8_t* gate;
+    const float* gate_scale;
+    const uint8_t* up;
+    const float* up_scale;
+    const uint8_t* down;
+    const float* down_scale;
+};
+bool fp8_supported(int H, int F);
+// after launch_route / launch_route_many: gate/up + SwiGLU into act [P][F], down
+// into y [P][H] (launch_combine finishes the layer)
+cudaError_t launch_fp8_experts(const MoeShape& s, const float* x, const Fp8Experts& w,
+                               const Route& r, float* act, float* y, int num_sms, cudaStream_t st);
+
 size_t row_bytes(int qtype, int cols);
 
 // Fused single-kernel decode path (T <= 8): launch plan chosen once per shape.

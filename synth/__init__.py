@@ -21,6 +21,10 @@ Recipe (every array is drawn with numpy ``Generator(PCG64(seed))``):
   (Q4_K: d and dmin; Q6_K: d).  Q6_K's int8 sub-block scales stay uniform bytes.
 * activations ~ N(0, 1) as float32.
 * decode-step extras: norm weights 1 + 0.1 N(0,1); KV cache entries fp16(N(0,1)).
+* FP8 block-scaled experts (E4M3 codes, one fp32 scale per 128 x 128 block):
+  codes with a random sign, a uniform 3-bit mantissa and an exponent field
+  rint(N(10, 2.5)) clipped to 0..15 (never the NaN pattern); block scales
+  base * U(0.5, 1.5), base 3e-4 for gate/up and 1e-3 for down.
 
 Expert tensors are drawn expert by expert from a stream keyed by
 (seed, tensor tag, expert), so that one expert's bytes can be regenerated alone
@@ -129,6 +133,76 @@ def moe_inputs(cfg: dict, T: int | None = None) -> dict:
     return dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=bias, x=x,
                 gate=gate, up=up, down=down,
                 gate_t=cfg["gate_t"], up_t=cfg["up_t"], down_t=cfg["down_t"])
+
+
+# --------------------------------------------------------------------------- FP8 block-scaled experts
+
+FP8_BLOCK = 128
+_TAG_FP8 = {"gate": 21, "up": 22, "down": 23}
+
+
+def _fp8_codes(rng: np.random.Generator, n: int) -> np.ndarray:
+    """n random E4M3 codes: random sign, mantissa uniform in 0..7, exponent field
+    rint(N(10, 2.5)) clipped to 0..15 (magnitudes spread log-normally around 8,
+    up to 448); the NaN pattern S.1111.111 is replaced by S.1111.110."""
+    sign = rng.integers(0, 2, size=n, dtype=np.uint8)
+    expo = np.clip(np.rint(rng.normal(10.0, 2.5, size=n)), 0, 15).astype(np.uint8)
+    mant = rng.integers(0, 8, size=n, dtype=np.uint8)
+    mant[(expo == 15) & (mant == 7)] = 6
+    return (sign << 7) | (expo << 3) | mant
+
+
+def fp8_scale_shape(rows: int, cols: int) -> tuple:
+    return (-(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK))
+
+
+def fp8_matrix(seed: int, tag: int, index: int, rows: int, cols: int,
+               scale_base: float = 1e-3) -> tuple:
+    """One block-scaled FP8 matrix: codes uint8 [rows][cols] and fp32 scales
+    [ceil(rows/128)][ceil(cols/128)] = scale_base * U(0.5, 1.5)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
+    codes = _fp8_codes(rng, rows * cols).reshape(rows, cols)
+    scales = (scale_base * rng.uniform(0.5, 1.5, size=fp8_scale_shape(rows, cols))).astype(np.float32)
+    return codes, scales
+
+
+def fp8_expert_tensor(seed: int, which: str, n_experts: int, rows: int, cols: int,
+                      scale_base: float = 1e-3) -> tuple:
+    """3-D FP8 expert tensor: codes [E][rows][cols], scales [E][rows/128][cols/128]."""
+    rb, cb = fp8_scale_shape(rows, cols)
+    codes = np.empty((n_experts, rows, cols), dtype=np.uint8)
+    scales = np.empty((n_experts, rb, cb), dtype=np.float32)
+    for e in range(n_experts):
+        codes[e], scales[e] = fp8_matrix(seed, _TAG_FP8[which], e, rows, cols, scale_base)
+    return codes, scales
+
+
+FP8_CONFIGS = {
+    "tiny_fp8": dict(name="tiny, FP8 experts", H=512, E=8, K=2, F=256, T=5, seed=10,
+                     gu_scale=6e-4, down_scale=3e-3),
+    "decode_fp8": dict(name="qwen3moe-30b-a3b layer decode T=1, FP8 block-scaled experts", H=2048,
+                       E=128, K=8, F=768, T=1, seed=11),
+}
+
+
+def moe_inputs_fp8(cfg: dict, T: int | None = None) -> dict:
+    """One MoE-FFN layer call over FP8 block-scaled experts: router ~ N(0, 0.02)
+    F32 [E][H] and x ~ N(0, 1) from the main stream (as ``moe_inputs``), the
+    expert tensors from their own per-expert streams.  Scale bases: gate/up
+    ``cfg["gu_scale"]`` (3e-4), down ``cfg["down_scale"]`` (1e-3): gate and up outputs
+    of order 1, MoE output of the order of x."""
+    H, E, F = cfg["H"], cfg["E"], cfg["F"]
+    T = cfg["T"] if T is None else T
+    seed = cfg["seed"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    router = rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32)
+    x = rng.normal(0.0, 1.0, size=(T, H)).astype(np.float32)
+    gsb, dsb = cfg.get("gu_scale", 3e-4), cfg.get("down_scale", 1e-3)
+    gate, gate_scale = fp8_expert_tensor(seed, "gate", E, F, H, gsb)
+    up, up_scale = fp8_expert_tensor(seed, "up", E, F, H, gsb)
+    down, down_scale = fp8_expert_tensor(seed, "down", E, H, F, dsb)
+    return dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=None, x=x, gate=gate,
+                gate_scale=gate_scale, up=up, up_scale=up_scale, down=down, down_scale=down_scale)
 
 
 # --------------------------------------------------------------------------- 48-layer decode step

@@ -12,6 +12,7 @@
 #include <math.h>
 
 #include "kquant.cuh"
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -70,24 +71,8 @@ __device__ __forceinline__ int xpad(int c) { return c + 4 * (c >> 6); }
 // the next one launch only once it has passed its own wait, so a kernel that
 // starts early never overlaps the kernel two places before it.
 __device__ __forceinline__ void griddep_wait_launch() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    pdl_wait();
+    pdl_launch_dependents();
 }
 
 template <int RPW, int NT>

@@ -14,6 +14,7 @@
 #include <math.h>
 
 #include "kquant.cuh"
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(256) down_kernel(
 // out[t][h] = res[t][h] + sum_j w[t][j] * y[t*K+j][h]  (slot order j = 0..K-1)
 __global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ wts,
                                const float* res, int H, int K, float* out) {
+    pdl_wait();                 // y of this call (launched as a programmatic dependent)
     const int t = blockIdx.y;
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
@@ -158,8 +160,7 @@ cudaError_t launch_down(const MoeShape& s, const float* act, const uint8_t* down
 cudaError_t launch_combine(const MoeShape& s, const float* y, const Route& r, const float* res,
                            float* out, cudaStream_t st) {
     dim3 g((s.H + 255) / 256, s.T);
-    combine_kernel<<<g, 256, 0, st>>>(y, r.wts, res, s.H, s.K, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, g, dim3(256), 0, st, y, r.wts, res, s.H, s.K, out);
 }
 
 }  // namespace qmoe

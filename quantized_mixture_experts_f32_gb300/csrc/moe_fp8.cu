@@ -15,11 +15,14 @@
 // Work is expert-centric and grid-strided: a warp item is two rows (one per
 // half-warp) of gate and up, or four rows of down, of one used expert; the
 // lane's chunks of every row of the item are loaded before any is used, so a
-// warp keeps 16 to 24 16-byte loads in flight.
+// warp keeps 12 to 16 16-byte loads in flight.  Both kernels are programmatic
+// dependents of the kernel before them; the down kernel loads its first item's
+// weights while the gate/up kernel still runs.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -76,6 +79,8 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ act) {
+    pdl_wait();                 // the routing of this call
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
@@ -131,27 +136,36 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
     const int per = H >> 2, nbf = F >> 7;
-    const int items = *n_used * per;
-    for (int i = gw; i < items; i += nw) {
+    // The routing was written two kernels back: the gate/up kernel lets this one
+    // launch only after its own wait on the routing kernel, so the lists are
+    // complete here and are read through L2.  The first item's weights are
+    // loaded before the wait on the gate/up kernel (they are never written).
+    const int items = __ldcg(n_used) * per;
+    uint4 w0[NC], w1[NC];
+    auto load = [&](int i) {
         const int u = i / per, h = 4 * (i - u * per) + hw;
-        const int e = used_expert[u];
-        const size_t row = (size_t)e * H + h;
-        const uint8_t* r0 = down + row * F + 16 * hl;
-        const uint8_t* r1 = r0 + 2 * (size_t)F;
-        uint4 w0[NC], w1[NC];
+        const uint8_t* r0 = down + ((size_t)__ldcg(used_expert + u) * H + h) * F + 16 * hl;
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
             w0[k] = ld_stream(r0 + 256 * k);
-            w1[k] = ld_stream(r1 + 256 * k);
+            w1[k] = ld_stream(r0 + 2 * (size_t)F + 256 * k);
         }
+    };
+    if (gw < items) load(gw);
+    pdl_wait();                 // act of this call
+    pdl_launch_dependents();
+    for (int i = gw; i < items; i += nw) {
+        if (i != gw) load(i);
+        const int u = i / per, h = 4 * (i - u * per) + hw;
+        const int e = __ldcg(used_expert + u);
         // rows h and h + 2 lie in one 128-row block (h0 is a multiple of 4)
         const size_t sb = ((size_t)e * (H >> 7) + (h >> 7)) * nbf;
         float s[NC];
 #pragma unroll
         for (int k = 0; k < NC; ++k) s[k] = __ldg(ds + sb + 2 * k + (hl >> 3));
-        const int p0 = used_first[u], p1 = used_first[u + 1];
+        const int p0 = __ldcg(used_first + u), p1 = __ldcg(used_first + u + 1);
         for (int q = p0; q < p1; ++q) {
-            const int p = pair_list[q];
+            const int p = __ldcg(pair_list + q);
             const float* ap = act + (size_t)p * F + 16 * hl;
             float a = 0.f, b = 0.f;
 #pragma unroll
@@ -190,10 +204,9 @@ cudaError_t gateup_nc(const MoeShape& s, const float* x, const Fp8Experts& w, co
                       float* act, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
     const int grid = fp8_grid(fp8_gateup_kernel<NC>, &resident, items, num_sms);
-    fp8_gateup_kernel<NC><<<grid, F8_THREADS, 0, st>>>(x, s.H, s.F, s.K, w.gate, w.gate_scale, w.up,
-                                                      w.up_scale, r.n_used, r.used_expert,
-                                                      r.used_first, r.pair_list, act);
-    return cudaGetLastError();
+    return launch_pdl(fp8_gateup_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.H, s.F, s.K,
+                      w.gate, w.gate_scale, w.up, w.up_scale, r.n_used, r.used_expert,
+                      r.used_first, r.pair_list, act);
 }
 
 template <int NC>
@@ -201,9 +214,8 @@ cudaError_t down_nc(const MoeShape& s, const float* act, const Fp8Experts& w, co
                     float* y, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
     const int grid = fp8_grid(fp8_down_kernel<NC>, &resident, items, num_sms);
-    fp8_down_kernel<NC><<<grid, F8_THREADS, 0, st>>>(act, s.H, s.F, w.down, w.down_scale, r.n_used,
-                                                    r.used_expert, r.used_first, r.pair_list, y);
-    return cudaGetLastError();
+    return launch_pdl(fp8_down_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, act, s.H, s.F,
+                      w.down, w.down_scale, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
 }
 
 }  // namespace

@@ -11,6 +11,7 @@
 
 #include "kquant.cuh"
 
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 
 namespace qmoe {
@@ -66,14 +67,14 @@ constexpr int TK_MAXV = 32;   // logits per lane (E <= 1024)
 // Per token (one warp): top-K of the F32 logits (ties -> lower index), softmax
 // over all E, routing weights renormalised over the K selected.  Then one warp
 // builds the per-expert pair lists with a stable counting sort.
-__global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                    int K, int norm, int32_t* __restrict__ ids,
-                                                    float* __restrict__ wts,
-                                                    int32_t* __restrict__ n_used,
-                                                    int32_t* __restrict__ used_expert,
-                                                    int32_t* __restrict__ used_first,
-                                                    int32_t* __restrict__ pair_list) {
-    extern __shared__ int32_t sm[];               // counts[E], cursor[E]
+// The whole top-k / lists step for T tokens, run by one block of any size that
+// is a multiple of 32 (blockDim.x <= 1024).  Logits are read through L2 (they
+// may come from other CTAs of the same launch).  sm: 2 E ints of shared memory.
+__device__ void topk_lists(const float* __restrict__ logits, int T, int E, int K, int norm,
+                           int32_t* __restrict__ ids, float* __restrict__ wts,
+                           int32_t* __restrict__ n_used, int32_t* __restrict__ used_expert,
+                           int32_t* __restrict__ used_first, int32_t* __restrict__ pair_list,
+                           int32_t* sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const int nv = (E + 31) / 32;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
 #pragma unroll
         for (int z = 0; z < 4; ++z) {
             const int i = lane + 32 * z;
-            ks[z] = i < E ? order_key(lt[i]) : INT_MIN;
+            ks[z] = i < E ? order_key(__ldcg(lt + i)) : INT_MIN;
             is[z] = i < E ? i : INT_MAX;
         }
         auto cswap = [&](int x, int y) {
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
             }
         }
         float z = 0.f;
-        for (int i = lane; i < E; i += 32) z += expf(lt[i] - vmax);
+        for (int i = lane; i < E; i += 32) z += expf(__ldcg(lt + i) - vmax);
         z = warp_sum(z);
         const float pj = lane < K ? expf(my_v - vmax) / z : 0.f;
         const float psel = warp_sum(pj);
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
 #pragma unroll
         for (int i = 0; i < TK_MAXV; ++i) {
             const int e = lane + 32 * i;
-            v[i] = (i < nv && e < E) ? order_key(logits[(size_t)t * E + e]) : INT_MIN;
+            v[i] = (i < nv && e < E) ? order_key(__ldcg(logits + (size_t)t * E + e)) : INT_MIN;
         }
         uint32_t taken = 0u;                      // bit i: v[i] selected
         float vmax = 0.f, psel = 0.f;
@@ -233,6 +234,90 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ lo
             __syncwarp();
         }
     }
+}
+
+__global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int K, int norm, int32_t* __restrict__ ids,
+                                                    float* __restrict__ wts,
+                                                    int32_t* __restrict__ n_used,
+                                                    int32_t* __restrict__ used_expert,
+                                                    int32_t* __restrict__ used_first,
+                                                    int32_t* __restrict__ pair_list) {
+    extern __shared__ int32_t sm[];               // counts[E], cursor[E]
+    topk_lists(logits, T, E, K, norm, ids, wts, n_used, used_expert, used_first, pair_list, sm);
+}
+
+// Router GEMV and top-k in one launch for up to RS_TOK tokens.  CTA e computes
+// logits[t][e] for every token, its RS_THREADS threads splitting the row (one
+// round trip of loads), and the last CTA to finish (an arrival counter, which it
+// resets for the next launch) runs the top-k and the per-expert lists.  The
+// router row is loaded before the wait on the previous kernel (weights are
+// never written by a kernel), x after it.
+constexpr int RS_TOK = 8, RS_THREADS = 256, RS_EMAX = 1024;
+
+__global__ void __launch_bounds__(RS_THREADS) router_topk_small(
+    const float* __restrict__ x, const float* __restrict__ wr, const float* __restrict__ bias,
+    int T, int H, int E, int K, int norm, float* __restrict__ logits, int32_t* __restrict__ ids,
+    float* __restrict__ wts, int32_t* __restrict__ n_used, int32_t* __restrict__ used_expert,
+    int32_t* __restrict__ used_first, int32_t* __restrict__ pair_list, unsigned* arrive) {
+    __shared__ float red[RS_TOK][RS_THREADS / 32];
+    __shared__ int32_t sm[2 * RS_EMAX];
+    __shared__ int is_last;
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* wrow = wr + (size_t)e * H;
+    constexpr int NW = 4;                         // row float4s a thread keeps in registers
+    float4 w[NW];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+        const int h = 4 * (threadIdx.x + k * RS_THREADS);
+        w[k] = h < H ? __ldg(reinterpret_cast<const float4*>(wrow + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    float acc[RS_TOK];
+#pragma unroll
+    for (int i = 0; i < RS_TOK; ++i) acc[i] = 0.f;
+    for (int h0 = 0; h0 < H; h0 += 4 * NW * RS_THREADS) {
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const int h = h0 + 4 * (threadIdx.x + k * RS_THREADS);
+            if (h >= H) continue;
+            const float4 wk = h0 == 0 ? w[k] : __ldg(reinterpret_cast<const float4*>(wrow + h));
+#pragma unroll
+            for (int i = 0; i < RS_TOK; ++i) {
+                if (i < T) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(x + (size_t)i * H + h));
+                    acc[i] = fmaf(wk.x, v.x, acc[i]);
+                    acc[i] = fmaf(wk.y, v.y, acc[i]);
+                    acc[i] = fmaf(wk.z, v.z, acc[i]);
+                    acc[i] = fmaf(wk.w, v.w, acc[i]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RS_TOK; ++i) {
+        if (i < T) {
+            const float v = warp_sum(acc[i]);
+            if (lane == 0) red[i][warp] = v;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        float v = 0.f;
+#pragma unroll
+        for (int k = 0; k < RS_THREADS / 32; ++k) v += red[threadIdx.x][k];
+        logits[(size_t)threadIdx.x * E + e] = v + (bias ? bias[e] : 0.f);
+        __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(arrive, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    topk_lists(logits, T, E, K, norm, ids, wts, n_used, used_expert, used_first, pair_list, sm);
+    if (threadIdx.x == 0) *arrive = 0u;
 }
 
 // ---------------------------------------------------------------------------- many tokens
@@ -572,6 +657,10 @@ cudaError_t route_prepare() {
 
 cudaError_t launch_route(const MoeShape& s, const float* x, const float* router_w,
                          const float* bias, const Route& r, cudaStream_t st) {
+    if (r.arrive && s.T <= RS_TOK && s.E <= RS_EMAX)
+        return launch_pdl(router_topk_small, dim3(s.E), dim3(RS_THREADS), 0, st, x, router_w, bias,
+                          s.T, s.H, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.n_used,
+                          r.used_expert, r.used_first, r.pair_list, r.arrive);
     dim3 g1((s.E + RT_EXP - 1) / RT_EXP, (s.T + RT_TOK - 1) / RT_TOK);
     router_kernel<<<g1, 32 * RT_EXP, 0, st>>>(x, router_w, bias, s.T, s.H, s.E, r.logits);
     const int threads = 32 * (s.T >= 32 ? 32 : (s.T > 4 ? s.T : 4));

@@ -84,7 +84,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
+        status, bar, arrive, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
         rope_cs, pl, total;
     int attn_splits;
     bool pl_ok;
@@ -130,6 +130,7 @@ Layout layout(const qmoe_config* c) {
     L.hout = take(sizeof(float) * T * H);
     L.status = take(sizeof(int) * 16);
     L.bar = take(sizeof(unsigned) * 64);
+    L.arrive = take(sizeof(unsigned) * 4);
     L.xp = take(sizeof(__half) * P * H);
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
@@ -359,6 +360,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.logits_part = reinterpret_cast<float*>(b + L.logits_part);
     c->route.tokmap = reinterpret_cast<uint32_t*>(b + L.tokmap);
     c->route.jmap = reinterpret_cast<uint8_t*>(b + L.jmap);
+    c->route.arrive = reinterpret_cast<unsigned*>(b + L.arrive);
     c->q8 = qmoe::q8_bufs_carve(reinterpret_cast<unsigned char*>(b + L.q8), c->cfg.max_tokens, c->cfg.hidden,
                                 c->cfg.top_k, c->cfg.ffn);
     c->act = reinterpret_cast<float*>(b + L.act);

@@ -23,6 +23,7 @@ struct Route {
     uint32_t* tokmap;     // [E][ceil(T/32)] token bitmap per expert, then [E] pair counts
                           // (many-token path), or null
     uint8_t* jmap;        // [E][T] slot j of pair (t, e) where e's bitmap has t (many-token path)
+    unsigned* arrive;     // [1] arrival counter of the one-launch routing (zero between launches), or null
 };
 
 struct MoeShape {

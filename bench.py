@@ -71,12 +71,15 @@ WORKLOADS = {
     "decode_fp8": dict(cfg=None, fp8="decode_fp8", copies=8, e2e=2000, steps=20000, warmup=200,
                        desc="qwen3moe-30b-a3b MoE layer decode, T=1, FP8 (E4M3) experts with one "
                             "fp32 scale per 128x128 block, F32 router (supplementary)"),
+    "prefill_fp8": dict(cfg=None, fp8="decode_fp8", T=512, copies=2, e2e=20, steps=300, warmup=6,
+                        desc="qwen3moe-30b-a3b MoE layer prefill, T=512, FP8 (E4M3) experts with "
+                             "one fp32 scale per 128x128 block, F32 router (supplementary)"),
 }
 
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
                "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None,
-               "decode_fp8": None}
+               "decode_fp8": None, "prefill_fp8": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -653,14 +656,19 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
         ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
         e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
-        launches=q.LAUNCHES_PER_FP8_FORWARD if T < 16 else q.LAUNCHES_PER_FP8_FORWARD_MANY,
+        launches=(q.LAUNCHES_PER_FP8_FORWARD if T <= 8 else q.LAUNCHES_PER_FP8_FORWARD + 1
+                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_FP8_FORWARD_MANY),
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct, "expert_bytes": per_expert,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
                       "written right before the timed region"},
-        kernel="whole FP8 layer call (router, top-k, gate/up, down, combine)",
-        dtype="e4m3 weights widened exactly, f32 activations and accumulate")
+        kernel=("whole FP8 layer call (router, top-k, gate/up, down, combine)" if T <= q.FP8_GEMV_MAX
+                else "whole FP8 layer call (routing, gather, grouped tensor-core GEMMs, combine)"),
+        dtype=("e4m3 weights widened exactly, f32 activations and accumulate" if T <= q.FP8_GEMV_MAX
+               else "e4m3 weights widened to f16 tensor-core operands, f32 accumulate"))
+    if T > q.FP8_GEMV_MAX:
+        res["tensor_tflops"] = T * K * 2 * (2 * F * H + H * F) / step_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
         cpu = cpu_sample_fp8(inp, args.cpu_seconds, 8)

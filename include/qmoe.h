@@ -152,8 +152,11 @@ qmoe_status qmoe_forward_q8k(qmoe_ctx* ctx, const float* hidden_in, const float*
  *   gate_scale / up_scale: fp32 [E][ffn/128][hidden/128];
  *   down_scale: fp32 [E][hidden/128][ffn/128];
  *   weight (r, c) of expert e = e4m3(code) * scale[e][r/128][c/128].
- * Codes 0x7F / 0xFF (NaN) are not valid weights.  x, the SwiGLU output and
- * every sum are fp32.  hidden_out = hidden_in + MoE(hidden_in); it may alias
+ * Codes 0x7F / 0xFF (NaN) are not valid weights.  Up to 32 tokens the expert
+ * GEMVs run on the CUDA cores with x, the SwiGLU output and every sum in fp32;
+ * more tokens run as grouped GEMMs on the tensor cores (weights widened to fp16
+ * as e4m3 * scale rounded once, x and the SwiGLU output rounded to fp16, fp32
+ * accumulation), like the k-quant path of qmoe_forward.  hidden_out = hidden_in + MoE(hidden_in); it may alias
  * hidden_in for any n_tokens.  ids_out / weights_out as qmoe_forward_ex
  * (nullable).  Serves hidden/256 in {2, 4, 8, 16} and ffn/256 in 1..6
  * (QMOE_ERR_SHAPE otherwise).  Code and activation pointers 16-byte aligned,

@@ -32,11 +32,13 @@ LAUNCHES_PER_DECODE_FORWARD = 1
 LAUNCHES_PER_PREFILL_FORWARD = 7
 # qmoe_forward_q8k: router, top-k, quantise x, gate/up, quantise act, down, combine
 LAUNCHES_PER_Q8K_FORWARD = 7
-# qmoe_forward_fp8 below 16 tokens: router, top-k (with the per-expert lists),
-# gate/up, down, combine; from 16 tokens: router GEMM, top-k, per-expert lists,
-# gate/up, down, combine
-LAUNCHES_PER_FP8_FORWARD = 5
-LAUNCHES_PER_FP8_FORWARD_MANY = 6
+# qmoe_forward_fp8 up to 32 tokens: routing (one launch up to 8 tokens, router
+# + top-k beyond), gate/up GEMV, down GEMV, combine; more than 32 tokens (tensor
+# cores): router GEMM, top-k, per-expert lists, gather, gate/up GEMM, down GEMM,
+# combine
+FP8_GEMV_MAX = 32
+LAUNCHES_PER_FP8_FORWARD = 4           # up to 8 tokens (5 for 9..32)
+LAUNCHES_PER_FP8_FORWARD_MANY = 7
 # one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
 # its RMSNorm)

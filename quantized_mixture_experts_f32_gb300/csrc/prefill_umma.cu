@@ -22,6 +22,7 @@
 // tokens on average), so token tiles of 16..256 are the N side.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -65,6 +66,12 @@ static_assert(GU_NQ <= NQ && GU_NA == 4 && GU_NMAX <= GU_ACC_COLS &&
                   W_EPI % 4 == 0,
               "gate/up rings");
 constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one superblock column
+// FP8 experts: a raw stage is one 128-column scale block of the item's rows
+// (64 gate + 64 up rows for gate/up, 128 rows for down): two k-blocks
+constexpr int F8_COLS = 128;
+constexpr int QSTAGE_F8 = 128 * F8_COLS;
+constexpr int F8_NQ = 3;
+template <int QF> __host__ __device__ constexpr int gu_qbytes() { return QF ? F8_NQ * QSTAGE_F8 : GU_NQ * QSTAGE_GU; }
 // down kernel: token-tile rows, A / B stages, TMEM columns (two accumulators)
 constexpr int DN_NMAX = 128;
 constexpr int DN_NA = 2;
@@ -103,6 +110,26 @@ __device__ __forceinline__ uint4 codes_to_half8(uint32_t w0, uint32_t w1, __half
     r.z = h2_bits(__hfma2(__hsub2(bits_h2(__byte_perm(w1, 0x64646464u, 0x4140)), sub), s, c));
     r.w = h2_bits(__hfma2(__hsub2(bits_h2(__byte_perm(w1, 0x64646464u, 0x4342)), sub), s, c));
     return r;
+}
+
+// 16 E4M3 codes (k order) times the block scale -> two 16-byte runs of 8 fp16
+// weights, stored at the row's swizzled chunks o0 and o1 (the E4M3 -> fp16
+// widening is exact; the product is rounded once, to fp16)
+__device__ __forceinline__ void f8_quarter(uint4 q, float s, uint8_t* arow, int o0, int o1) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * hh)) & 0xffffu), __NV_E4M3);
+            const float2 f = __half22float2(__half2(r));
+            h[2 * i + hh] = pack_half2(f.x * s, f.y * s);
+        }
+    }
+    *reinterpret_cast<uint4*>(arow + o0) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(arow + o1) = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
 // Q4_K: scale and offset of the two sub-blocks (2c, 2c + 1) of k-block c, as
@@ -177,6 +204,9 @@ struct GuParams {
     int seg_rows[3], seg_yoff[3];
     int ksplit;
     size_t part_stride;
+    // FP8 experts (QF 1): fp32 scales per 128 x 128 block, [E][F/128][H/128]
+    const float* gscale;
+    const float* uscale;
 };
 
 // One work item of the gate/up kernel: weight rows f0 .. of expert e (MODE 1:
@@ -237,7 +267,7 @@ __device__ __forceinline__ GuItem gu_item(const GuParams& p, const int* tfirst, 
 // consecutive rows of one Q4_K matrix [F][H], B = the dense_T token rows of x,
 // epilogue fp32 y (+ res).  Warps: NDQ dequant, Q load, B load, MMA, one idle,
 // GU_NEPI epilogue.
-template <int MODE>
+template <int MODE, int QF>
 __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                    const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x64,
@@ -249,11 +279,16 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
     const int KS = MODE == 0 ? 1 : p.ksplit;
-    const int NKB = H / KBLK / KS, NSB = H / QK / KS;     // per item
+    static_assert(QF == 0 || MODE == 0, "FP8 weights in the MoE mode only");
+    constexpr int NQS = QF ? F8_NQ : GU_NQ;              // raw stages
+    constexpr int QSB = QF ? QSTAGE_F8 : QSTAGE_GU;      // raw stage bytes
+    constexpr int QCOL = QF ? F8_COLS : Q4K_BYTES;       // raw bytes per row per stage
+    constexpr int KPS = QF ? F8_COLS / KBLK : QK / KBLK; // k-blocks per raw stage
+    const int NKB = H / KBLK / KS, NSB = NKB / KPS;      // per item
     const int FT = MODE == 0 ? F / 64 : F / TILE_M;
 
-    uint8_t* qst = sm;                                   // GU_NQ x QSTAGE_GU
-    uint8_t* ast = sm + ((GU_NQ * QSTAGE_GU + 1023) & ~1023);  // GU_NA x A_STAGE (1024-aligned)
+    uint8_t* qst = sm;                                   // NQS x QSB
+    uint8_t* ast = sm + ((gu_qbytes<QF>() + 1023) & ~1023);  // GU_NA x A_STAGE (1024-aligned)
     uint8_t* bst = ast + GU_NA * A_STAGE;                // GU_NA x GU_BSTAGE
     PfBars* bars = reinterpret_cast<PfBars*>(bst + B_BYTES_GU);
     int* tfirst = reinterpret_cast<int*>(bars + 1);      // [n_used + 1] (MODE 0)
@@ -261,7 +296,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 
     const int n_used = MODE == 0 ? *p.n_used : 0;
     if (tid == 0) {
-        for (int i = 0; i < GU_NQ; ++i) {
+        for (int i = 0; i < NQS; ++i) {
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], NDQ);
         }
@@ -310,18 +345,18 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 const CUtensorMap* tw = MODE == 0 ? &tm_gate : w.e == 0 ? &tm_gate : w.e == 1 ? &tm_up : &tm_w2;
                 const int sb0 = w.kh * NSB;
                 for (int sb = 0; sb < NSB; ++sb, ++gs) {
-                    const int st = gs % GU_NQ;
-                    if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / GU_NQ) & 1u) ^ 1u)) {
+                    const int st = gs % NQS;
+                    if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / NQS) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* dst = qst + st * QSTAGE_GU;
-                    mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_GU);
-                    tma_load_2d(dst, tw, (sb0 + sb) * Q4K_BYTES, ybase, &bars->qfull[st]);
+                    uint8_t* dst = qst + st * QSB;
+                    mbar_arrive_expect_tx(&bars->qfull[st], QSB);
+                    tma_load_2d(dst, tw, (sb0 + sb) * QCOL, ybase, &bars->qfull[st]);
                     if (MODE == 0)
-                        tma_load_2d(dst + 64 * Q4K_BYTES, &tm_up, sb * Q4K_BYTES, ybase, &bars->qfull[st]);
+                        tma_load_2d(dst + 64 * QCOL, &tm_up, sb * QCOL, ybase, &bars->qfull[st]);
                     else
-                        tma_load_2d(dst + 64 * Q4K_BYTES, tw, (sb0 + sb) * Q4K_BYTES, ybase + 64, &bars->qfull[st]);
+                        tma_load_2d(dst + 64 * QCOL, tw, (sb0 + sb) * QCOL, ybase + 64, &bars->qfull[st]);
                 }
             }
         }
@@ -380,7 +415,55 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 if (ok) umma_commit(&bars->accfull[buf]);
             }
         }
-    } else if (warp < NDQ) {
+    } else if (QF == 1 && warp < NDQ) {
+        // FP8 dequant: thread -> A row 8*warp + (lane & 7) and 16-k quarter
+        // qq = lane >> 3 of each k-block; A rows 32 g .. 32 g + 15 are gate rows
+        // 16 g .., the next 16 the matching up rows (as for k-quants).  The
+        // row's scale is the item's (row block, column block) scale of gate or up.
+        const int qq = lane >> 3, sw = lane & 7;
+        const int row = 8 * warp + (lane & 7);
+        const int grp = row >> 5, w32 = row & 31;
+        const bool is_gate = w32 < 16;
+        const int srow = (is_gate ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16)) * F8_COLS;
+        const int rowb = row * 128;
+        const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+        const float* scale = is_gate ? p.gscale : p.uscale;
+        const int nbh = H / F8_COLS;
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int gk = 0, gs = 0;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            const GuItem w = gu_item<MODE>(p, tfirst, n_used, blockIdx.x + j * gridDim.x);
+            const float* srow_scale = scale + ((size_t)w.e * (F / F8_COLS) + w.f0 / F8_COLS) * nbh;
+            for (int sb = 0; sb < NSB; ++sb, ++gs) {
+                const int sq = gs % NQS;
+                const uint8_t* stg = qst + sq * QSB;
+                if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / NQS) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint4 v[KPS];
+#pragma unroll
+                for (int c = 0; c < KPS; ++c) v[c] = *reinterpret_cast<const uint4*>(stg + srow + KBLK * c + 16 * qq);
+                const float sc = __ldg(srow_scale + sb);
+#pragma unroll
+                for (int c = 0; c < KPS; ++c, ++gk) {
+                    const int sa = gk % GU_NA, pr = (gk >> 1) & 1;
+                    if (!mbar_wait(&bars->aempty[pr], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    f8_quarter(v[c], sc, ast + sa * A_STAGE + rowb, o0, o1);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[pr]);
+                }
+                if (!ok) break;
+                // every value loaded from the raw stage has fed a store above
+                if (lane == 0) mbar_arrive(&bars->qempty[sq]);
+            }
+        }
+    } else if (QF == 0 && warp < NDQ) {
         // dequant: thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r) and 16-k
         // quarter qq = lane >> 3 of every k-block (each 8-lane phase of a 16-byte
         // store then covers all 32 banks).  All NDQ warps fill each A stage in turn, so
@@ -404,9 +487,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
         int gk = 0;
         for (int gs = 0; gs < my_items * NSB; ++gs) {
-            const int sq = gs % GU_NQ;
-            const uint8_t* stg = qst + sq * QSTAGE_GU;
-            if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / GU_NQ) & 1u)) break;
+            const int sq = gs % NQS;
+            const uint8_t* stg = qst + sq * QSB;
+            if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / NQS) & 1u)) break;
             uint4 hdr[RPT];
             uint2 v[RPT][4];
 #pragma unroll
@@ -506,6 +589,7 @@ struct DnParams {
     const uint8_t* down;
     float* y;             // [P][H] fp32, rows in pair-list order
     int H, F, down_t;
+    const float* dscale;  // FP8 experts (QF 1): [E][H/128][F/128] block scales
 };
 
 // Persistent down GEMM: one CTA per SM walks the items (token tile of DN_NMAX
@@ -517,9 +601,10 @@ struct DnParams {
 // B k-block stages (DN_NA deep) share one full / empty barrier pair each; two
 // TMEM accumulators; DN epilogue warps write fp32 y rows.  Warps as in the
 // gate/up kernel.
+template <int QF>
 __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_down(const __grid_constant__ CUtensorMap tm_a64, const __grid_constant__ CUtensorMap tm_a128,
-                 const DnParams p) {
+                 const __grid_constant__ CUtensorMap tm_w, const DnParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
@@ -527,10 +612,13 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     const int HT = H / TILE_M;
     const int BB = p.down_t == 1 ? Q4K_BYTES : Q6K_BYTES;
     const int RB = (F / QK) * BB;
-    const uint32_t qbytes = (uint32_t)(TILE_M * RB);       // whole K of 128 rows
-    const uint32_t RQ = (qbytes + 1023u) & ~1023u;
+    // k-quants: one bulk copy of the whole K of 128 rows per item, two raw
+    // buffers; FP8 (QF 1): a ring of F8_NQ raw stages of one 128-column scale
+    // block each, loaded by TMA (tm_w: [E*H][F] bytes, box 128 x 128)
+    const uint32_t qbytes = QF ? 0u : (uint32_t)(TILE_M * RB);
+    const uint32_t RQ = QF ? (uint32_t)(F8_NQ * QSTAGE_F8) / 2u : (qbytes + 1023u) & ~1023u;
 
-    uint8_t* qbuf = sm;                                   // 2 x RQ raw buffers
+    uint8_t* qbuf = sm;                                   // 2 x RQ raw bytes
     uint8_t* ast = sm + 2 * RQ;                           // DN_NA x A_STAGE
     uint8_t* bst = ast + DN_NA * A_STAGE;                 // DN_NA x DN_BSTAGE
     PfBars* bars = reinterpret_cast<PfBars*>(bst + DN_NA * DN_BSTAGE);
@@ -539,9 +627,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 
     const int n_used = *p.n_used;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < (QF ? F8_NQ : 2); ++i) {
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], NDQ);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->accfull[i], 1);
             mbar_init(&bars->accempty[i], GU_NEPI);
         }
@@ -590,7 +680,25 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         n = min(DN_NMAX, p.used_first[lo + 1] - first - n0);
     };
 
-    if (warp == W_QLOAD) {
+    if (QF == 1 && warp == W_QLOAD) {
+        if (lane == 0) {
+            int gs = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                int e, first, n0, n, h0;
+                item(it, e, first, n0, n, h0);
+                for (int sb = 0; sb < F / F8_COLS; ++sb, ++gs) {
+                    const int st = gs % F8_NQ;
+                    if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / F8_NQ) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_F8);
+                    tma_load_2d(qbuf + st * QSTAGE_F8, &tm_w, sb * F8_COLS, e * H + h0, &bars->qfull[st]);
+                }
+            }
+        }
+    } else if (QF == 0 && warp == W_QLOAD) {
         if (lane == 0) {
             int j = 0;
             for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
@@ -651,7 +759,48 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                 if (ok) umma_commit(&bars->accfull[buf]);
             }
         }
-    } else if (warp < NDQ) {
+    } else if (QF == 1 && warp < NDQ) {
+        // FP8: thread -> A row 8*warp + (lane & 7), 16-k quarter qq = lane >> 3
+        const int qq = lane >> 3, sw = lane & 7;
+        const int row = 8 * warp + (lane & 7);
+        const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+        const int nbf = F / F8_COLS;
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int gk = 0, gs = 0;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            int e, first, n0, n, h0;
+            item(blockIdx.x + j * gridDim.x, e, first, n0, n, h0);
+            const float* srow_scale = p.dscale + ((size_t)e * (H / F8_COLS) + h0 / F8_COLS) * nbf;
+            for (int sb = 0; sb < nbf; ++sb, ++gs) {
+                const int sq = gs % F8_NQ;
+                const uint8_t* stg = qbuf + sq * QSTAGE_F8;
+                if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / F8_NQ) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint4 v[F8_COLS / KBLK];
+#pragma unroll
+                for (int c = 0; c < F8_COLS / KBLK; ++c)
+                    v[c] = *reinterpret_cast<const uint4*>(stg + row * F8_COLS + KBLK * c + 16 * qq);
+                const float sc = __ldg(srow_scale + sb);
+#pragma unroll
+                for (int c = 0; c < F8_COLS / KBLK; ++c, ++gk) {
+                    const int sa = gk % DN_NA;
+                    if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / DN_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    f8_quarter(v[c], sc, ast + sa * A_STAGE + row * 128, o0, o1);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[sa]);
+                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&bars->qempty[sq]);
+            }
+        }
+    } else if (QF == 0 && warp < NDQ) {
         // thread -> A rows 8*warp + (lane & 7) (+ 8*NDQ*r), 16-k quarter
         // qq = lane >> 3 of every k-block; all warps fill each A stage in turn
         const int qq = lane >> 3, sw = lane & 7;                 // row % 8 == lane % 8
@@ -873,8 +1022,26 @@ int sm_count() {
 
 size_t dn_smem(int F, int down_t, int E) {
     const size_t rb = (size_t)(F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    const size_t q = (TILE_M * rb + 1023) & ~size_t(1023);
+    const size_t q = down_t == 3 ? (size_t)F8_NQ * QSTAGE_F8 / 2 : (TILE_M * rb + 1023) & ~size_t(1023);
     return 1024 + 2 * q + DN_NA * A_STAGE + DN_NA * DN_BSTAGE + sizeof(PfBars) + sizeof(int) * (E + 1) + 64;
+}
+
+// the attribute raising the dynamic shared-memory limit of every prefill GEMM
+// instantiation, once per process
+cudaError_t prefill_attrs() {
+    static cudaError_t e = [] {
+        cudaError_t r = cudaFuncSetAttribute(prefill_gateup<0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_gateup<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_gateup<0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_down<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_down<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        return r;
+    }();
+    return e;
 }
 
 }  // namespace
@@ -908,23 +1075,51 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
         !map_half(&ta128, actp, s.F, P, 128))
         return cudaErrorInvalidValue;
 
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(prefill_gateup<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_gateup<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    e = prefill_attrs();
+    if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
-                {0, 0, 0}, {0, 0, 0}, 1, 0};
-    prefill_gateup<0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
+                {0, 0, 0}, {0, 0, 0}, 1, 0, nullptr, nullptr};
+    prefill_gateup<0, 0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t};
-    prefill_down<<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, dp);
+    DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t, nullptr};
+    prefill_down<0><<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, ta64, dp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g3((s.H / 4 + 255) / 256, s.T);
+    combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
+    return cudaGetLastError();
+}
+
+bool prefill_fp8_supported(const MoeShape& s) {
+    if (s.H % F8_COLS || s.F % F8_COLS || s.H % TILE_M || s.F % 64) return false;
+    return dn_smem(s.F, 3, s.E) <= 227 * 1024 && GU_SMEM <= 227 * 1024 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_fp8(const MoeShape& s, const float* x, const float* res, const Fp8Experts& w,
+                               const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
+                               float* out, cudaStream_t st) {
+    const int P = s.T * s.K;
+    gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tg, tu, td, tx64, tx128, txg, ta64, ta128;
+    if (!map_bytes(&tg, w.gate, (uint64_t)s.H, (uint64_t)s.E * s.F, F8_COLS, 64) ||
+        !map_bytes(&tu, w.up, (uint64_t)s.H, (uint64_t)s.E * s.F, F8_COLS, 64) ||
+        !map_bytes(&td, w.down, (uint64_t)s.F, (uint64_t)s.E * s.H, F8_COLS, TILE_M) ||
+        !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
+        !map_half(&txg, xp, s.H, P, GU_NMAX) || !map_half(&ta64, actp, s.F, P, 64) ||
+        !map_half(&ta128, actp, s.F, P, 128))
+        return cudaErrorInvalidValue;
+    e = prefill_attrs();
+    if (e != cudaSuccess) return e;
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
+                {0, 0, 0}, {0, 0, 0}, 1, 0, w.gate_scale, w.up_scale};
+    prefill_gateup<0, 1><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    DnParams dp{r.n_used, r.used_expert, r.used_first, w.down, y, s.H, s.F, 3, w.down_scale};
+    prefill_down<1><<<sm_count(), GU_THREADS, dn_smem(s.F, 3, s.E), st>>>(ta64, ta128, td, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
@@ -948,19 +1143,16 @@ cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, co
     for (int i = nseg; i < 3; ++i) tw[i] = tw[0];
     if (!map_half(&tx64, x, K, T, 64) || !map_half(&tx128, x, K, T, 128) || !map_half(&txg, x, K, T, GU_NMAX))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_gateup<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+    {
+        const cudaError_t e = prefill_attrs();
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     GuParams gp{nullptr, nullptr, nullptr, nullptr, K, rows, y, res, T, ldy,
                 {nseg > 0 ? seg[0].rows : 0, nseg > 1 ? seg[1].rows : 0, nseg > 2 ? seg[2].rows : 0},
                 {nseg > 0 ? seg[0].yoff : 0, nseg > 1 ? seg[1].yoff : 0, nseg > 2 ? seg[2].yoff : 0},
-                ksplit, part_stride};
+                ksplit, part_stride, nullptr, nullptr};
     const int items = (rows / TILE_M) * ksplit * ((T + GU_NMAX - 1) / GU_NMAX);
-    prefill_gateup<1><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(
+    prefill_gateup<1, 0><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(
         tw[0], tw[1], tw[2], tx64, tx128, txg, gp);
     return cudaGetLastError();
 }

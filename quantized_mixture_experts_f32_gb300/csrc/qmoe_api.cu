@@ -60,6 +60,7 @@ void create_fail(const char* fmt, ...) {
 }
 
 constexpr int DECODE_ALIAS_MAX = 8;
+constexpr int FP8_GEMV_MAX = 32;         // qmoe_forward_fp8: largest call on the expert GEMVs
 constexpr int FUSED_GRID_MAX = 1024;     // largest grid of the fused decode kernel
 
 qmoe_status fail(qmoe_ctx* c, qmoe_status s, const char* fmt, ...) {
@@ -502,17 +503,26 @@ qmoe_status qmoe_forward_fp8(qmoe_ctx* c, const float* hidden_in, const float* r
          reinterpret_cast<uintptr_t>(down_scale)) & 3u)
         return fail(c, QMOE_ERR_MISALIGNED, "scale pointers must be 4-byte aligned");
     qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
-    const bool many = n_tokens >= 16 && qmoe::route_many_supported(ms, c->route);
-    cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
-                         : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
     const qmoe::Fp8Experts w{static_cast<const uint8_t*>(gate_exps), gate_scale,
                              static_cast<const uint8_t*>(up_exps), up_scale,
                              static_cast<const uint8_t*>(down_exps), down_scale};
-    e = qmoe::launch_fp8_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "FP8 expert launch");
-    e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    // up to FP8_GEMV_MAX tokens: expert GEMVs on the CUDA cores; more: grouped
+    // GEMMs on the tensor cores
+    const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route) &&
+                      qmoe::prefill_fp8_supported(ms);
+    cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
+                         : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    if (many) {
+        e = qmoe::launch_prefill_fp8(ms, hidden_in, hidden_in, w, c->route, c->xp, c->actp, c->y,
+                                     c->inv_pos, hidden_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "FP8 tensor-core expert launch");
+    } else {
+        e = qmoe::launch_fp8_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "FP8 expert launch");
+        e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    }
     if (ids_out || weights_out) {
         e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");

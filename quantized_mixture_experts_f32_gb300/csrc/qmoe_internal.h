@@ -95,6 +95,13 @@ bool fp8_supported(int H, int F);
 // into y [P][H] (launch_combine finishes the layer)
 cudaError_t launch_fp8_experts(const MoeShape& s, const float* x, const Fp8Experts& w,
                                const Route& r, float* act, float* y, int num_sms, cudaStream_t st);
+// many tokens (after launch_route_many): gather x as fp16, grouped gate/up and
+// down GEMMs on the tensor cores with the FP8 weights widened to fp16 in shared
+// memory, combine into out (prefill_umma.cu)
+bool prefill_fp8_supported(const MoeShape& s);
+cudaError_t launch_prefill_fp8(const MoeShape& s, const float* x, const float* res, const Fp8Experts& w,
+                               const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
+                               float* out, cudaStream_t st);
 
 size_t row_bytes(int qtype, int cols);
 

@@ -24,7 +24,11 @@ is pinned against a batched causal formulation written in the tests.  The FP8
 functions (``fp8_e4m3_to_double``, ``fp8_dequant_matrix``, ``moe_ffn_fp8``) are
 pinned against the E4M3 definition, torch's float8_e4m3fn conversion and a
 dense numpy brute force (atlasinference source page
-"spark_model/weight_loader/qwen3.rs", load_layers: FP8 block-128 weights).
+"spark_model/weight_loader/qwen3.rs", load_layers: FP8 block-128 weights).  The
+NVFP4 functions (``e2m1_to_double``, ``nvfp4_dequant_matrix``, ``moe_ffn_nvfp4``,
+``nvfp4_quantize``) are pinned against the E2M1 value table, torch's E4M3
+conversion, a numpy brute force, and brute-force optimality of every rounding
+decision of the quantiser (same page: BF16 -> NVFP4 runtime quantisation).
 """
 from __future__ import annotations
 
@@ -100,6 +104,12 @@ def lib():
             L.qo_fp8_scale_count.restype = C.c_long
             L.qo_moe_ffn_fp8.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, dp, dp, ip,
                                          dp, up8, fp, up8, fp, up8, fp, dp, dp, dp]
+            L.qo_e2m1_to_double.argtypes = [C.c_uint8]
+            L.qo_e2m1_to_double.restype = C.c_double
+            L.qo_nvfp4_dequant_matrix.argtypes = [up8, up8, C.c_float, C.c_long, C.c_long, dp]
+            L.qo_moe_ffn_nvfp4.argtypes = ([C.c_int] * 5 + [dp, dp, ip, dp] + [up8, up8, fp] * 3
+                                           + [dp, dp, dp])
+            L.qo_nvfp4_quantize.argtypes = [C.c_long, C.c_long, u16, up8, up8, fp]
             L.qo_decode_layer.argtypes = (
                 [C.c_int] * 8 + [C.c_double, C.c_double, C.c_int, dp] + [fp] * 4 + [up8] * 4
                 + [fp, up8, up8, up8, C.c_int, u16, u16, ip, fp, ip, dp, dp, dp])
@@ -314,6 +324,81 @@ def moe_forward_fp8(inp: dict, norm_topk=True, force=None):
                                   force)
     out = moe_ffn_fp8(inp["x"], ids, w, inp["gate"], inp["gate_scale"], inp["up"],
                       inp["up_scale"], inp["down"], inp["down_scale"], inp["F"], inp["E"])
+    return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
+
+
+# ----------------------------------------------------------------------------- NVFP4 experts
+
+def e2m1_to_double(code: int) -> float:
+    """Value of one FP4 E2M1 code (low 4 bits)."""
+    return lib().qo_e2m1_to_double(int(code) & 0x0F)
+
+
+def nvfp4_dequant_matrix(codes, bscale, global_scale: float, rows: int, cols: int) -> np.ndarray:
+    """W[r][c] = e2m1(code) * e4m3(bscale[r][c // 16]) * global, in double; codes
+    [rows][cols/2] bytes with the even element in the low nibble."""
+    codes = _u8(codes).reshape(-1)
+    bscale = _u8(bscale).reshape(-1)
+    if codes.size != rows * cols // 2 or bscale.size != rows * cols // 16 or cols % 16:
+        raise ValueError("nvfp4_dequant_matrix: size mismatch")
+    out = np.empty((rows, cols), dtype=np.float64)
+    lib().qo_nvfp4_dequant_matrix(_p(codes, C.c_uint8), _p(bscale, C.c_uint8), float(global_scale),
+                                  rows, cols, _p(out, C.c_double))
+    return out
+
+
+def nvfp4_quantize(x_bf16_bits: np.ndarray):
+    """BF16 matrix (uint16 bit patterns [rows][cols]) -> (codes [rows][cols/2],
+    bscale [rows][cols/16] E4M3 bytes, global fp32); see qo_nvfp4_quantize."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols // 2), dtype=np.uint8)
+    bs = np.empty((rows, cols // 16), dtype=np.uint8)
+    g = np.empty(1, dtype=np.float32)
+    if lib().qo_nvfp4_quantize(rows, cols, _p(x, C.c_uint16), _p(codes, C.c_uint8),
+                               _p(bs, C.c_uint8), _p(g, C.c_float)):
+        raise ValueError("nvfp4_quantize: cols must be a multiple of 16")
+    return codes, bs, float(g[0])
+
+
+_NV_NAMES = ("gate", "gate_bs", "gate_gs", "up", "up_bs", "up_gs", "down", "down_bs", "down_gs")
+
+
+def moe_ffn_nvfp4(x, ids, w, ex: dict, F, E, res=None, want_act=False):
+    """out [T][H] (f64) = res + sum_j w_j * Wd(silu(Wg x) * Wu x) over NVFP4 experts
+    (ex: gate/up codes [E][F][H/2], *_bs [E][F][H/16], *_gs [E]; down [E][H][F/2],
+    [E][H][F/16], [E])."""
+    x = _f64(np.atleast_2d(x))
+    T, H = x.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    K = ids.shape[1]
+    w = _f64(w)
+    res = None if res is None else _f64(np.atleast_2d(res))
+    want = {"gate": E * F * H // 2, "gate_bs": E * F * H // 16, "gate_gs": E,
+            "up": E * F * H // 2, "up_bs": E * F * H // 16, "up_gs": E,
+            "down": E * H * F // 2, "down_bs": E * H * F // 16, "down_gs": E}
+    arrs = []
+    for n in _NV_NAMES:
+        a = _f32(ex[n]).reshape(-1) if n.endswith("_gs") else _u8(ex[n]).reshape(-1)
+        if a.size != want[n]:
+            raise ValueError(f"moe_ffn_nvfp4: {n} has {a.size} elements, expected {want[n]}")
+        arrs.append(a)
+    out = np.empty((T, H), dtype=np.float64)
+    act = np.empty((T, K, F), dtype=np.float64) if want_act else None
+    ptrs = [_p(a, C.c_float if n.endswith("_gs") else C.c_uint8) for n, a in zip(_NV_NAMES, arrs)]
+    rc = lib().qo_moe_ffn_nvfp4(T, H, F, E, K, _p(x, C.c_double), _p(res, C.c_double),
+                                _p(ids, C.c_int32), _p(w, C.c_double), *ptrs,
+                                _p(out, C.c_double), _p(act, C.c_double), None)
+    if rc:
+        raise ValueError(f"moe_ffn_nvfp4 failed rc={rc}")
+    return (out, act) if want_act else out
+
+
+def moe_forward_nvfp4(inp: dict, norm_topk=True, force=None):
+    """out = x + MoE(x) over NVFP4 experts with the F32 router."""
+    logits, ids, w, probs = route(inp["x"], inp["router"], inp["K"], inp.get("bias"), norm_topk,
+                                  force)
+    out = moe_ffn_nvfp4(inp["x"], ids, w, inp, inp["F"], inp["E"])
     return dict(out=out, ids=ids, w=w, logits=logits, probs=probs)
 
 

@@ -381,6 +381,152 @@ int qo_moe_ffn_fp8(int T, int H, int F, int E, int K, const double* x, const dou
     return moe_ffn_dense(T, H, F, E, K, x, res, ids, w, load_fp8_expert, &k, out, act, ys);
 }
 
+/* ------------------------------------------------------------------ NVFP4 experts */
+
+/* One FP4 E2M1 code (low 4 bits): sign, 2 exponent bits with bias 1, 1 mantissa
+ * bit; a zero exponent field is subnormal (m/2).  Magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6; no infinities or NaN. */
+double qo_e2m1_to_double(uint8_t c) {
+    int s = (c >> 3) & 1, ex = (c >> 1) & 3, m = c & 1;
+    double v = ex == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, ex - 1);
+    return s ? -v : v;
+}
+
+/* NVFP4 matrix ([P3]: dense weights quantised from BF16 to NVFP4 at load, the
+ * "nvfp4_global_absmax" / "quantize_bf16_to_nvfp4" kernels): codes [rows][cols/2]
+ * bytes, element c in byte c/2, low nibble for even c; one E4M3 scale per 16
+ * consecutive elements of a row, bscale[rows][cols/16]; one fp32 global scale.
+ * W[r][c] = e2m1(code) * e4m3(bscale[r][c/16]) * global.  cols % 16 == 0. */
+void qo_nvfp4_dequant_matrix(const uint8_t* codes, const uint8_t* bscale, float global, long rows,
+                             long cols, double* out) {
+    for (long r = 0; r < rows; ++r)
+        for (long c = 0; c < cols; ++c) {
+            uint8_t b = codes[r * (cols / 2) + c / 2];
+            uint8_t q = (c & 1) ? (b >> 4) : (b & 15);
+            out[r * cols + c] = qo_e2m1_to_double(q) *
+                                qo_fp8_e4m3_to_double(bscale[r * (cols / 16) + c / 16]) *
+                                (double)global;
+        }
+}
+
+typedef struct {
+    const uint8_t *gate, *up, *down;          /* codes */
+    const uint8_t *gbs, *ubs, *dbs;           /* block scales */
+    const float *ggs, *ugs, *dgs;             /* global scales, one per expert */
+} nvfp4_experts;
+
+static void load_nvfp4_expert(const void* ctx, int e, long H, long F, double* Wg, double* Wu,
+                              double* Wd) {
+    const nvfp4_experts* k = (const nvfp4_experts*)ctx;
+    qo_nvfp4_dequant_matrix(k->gate + (long)e * F * (H / 2), k->gbs + (long)e * F * (H / 16),
+                            k->ggs[e], F, H, Wg);
+    qo_nvfp4_dequant_matrix(k->up + (long)e * F * (H / 2), k->ubs + (long)e * F * (H / 16),
+                            k->ugs[e], F, H, Wu);
+    qo_nvfp4_dequant_matrix(k->down + (long)e * H * (F / 2), k->dbs + (long)e * H * (F / 16),
+                            k->dgs[e], H, F, Wd);
+}
+
+/* MoE FFN over NVFP4 experts: gate/up codes [E][F][H/2], block scales
+ * [E][F][H/16], globals [E]; down codes [E][H][F/2], scales [E][H][F/16],
+ * globals [E]. */
+int qo_moe_ffn_nvfp4(int T, int H, int F, int E, int K, const double* x, const double* res,
+                     const int32_t* ids, const double* w, const uint8_t* gate, const uint8_t* gate_bs,
+                     const float* gate_gs, const uint8_t* up, const uint8_t* up_bs,
+                     const float* up_gs, const uint8_t* down, const uint8_t* down_bs,
+                     const float* down_gs, double* out, double* act, double* ys) {
+    if (H <= 0 || F <= 0 || H % 16 || F % 16) return -1;
+    nvfp4_experts k = {gate, up, down, gate_bs, up_bs, down_bs, gate_gs, up_gs, down_gs};
+    return moe_ffn_dense(T, H, F, E, K, x, res, ids, w, load_nvfp4_expert, &k, out, act, ys);
+}
+
+/* Round a non-negative float to the nearest E4M3 code (ties to the even code),
+ * saturating at 448 (code 0x7E): a scan over the 127 finite non-negative codes
+ * in increasing order. */
+static uint8_t e4m3_encode_rne(float t) {
+    if (!(t > 0.0f)) return 0;
+    if (t >= 448.0f) return 0x7E;
+    uint8_t best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double lo = qo_fp8_e4m3_to_double((uint8_t)(c - 1)), hi = qo_fp8_e4m3_to_double((uint8_t)c);
+        if ((double)t >= hi) { best = (uint8_t)c; continue; }
+        /* lo <= t < hi */
+        double dl = (double)t - lo, dh = hi - (double)t;
+        if (dh < dl || (dh == dl && (c & 1) == 0)) best = (uint8_t)c;
+        else best = (uint8_t)(c - 1);
+        break;
+    }
+    return best;
+}
+
+/* Round v to the nearest E2M1 code (ties to the even code), saturating at 6;
+ * the sign bit is v's (so -0 and small negatives give the code 8, minus zero). */
+static uint8_t e2m1_encode_rne(float v) {
+    float a = fabsf(v);
+    uint8_t m;
+    if (a <= 0.25f) m = 0;
+    else if (a < 0.75f) m = 1;
+    else if (a <= 1.25f) m = 2;
+    else if (a < 1.75f) m = 3;
+    else if (a <= 2.5f) m = 4;
+    else if (a < 3.5f) m = 5;
+    else if (a <= 5.0f) m = 6;
+    else m = 7;
+    return (uint8_t)(m | (signbit(v) ? 8 : 0));
+}
+
+static float bf16_to_float(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Runtime quantisation of a BF16 matrix [rows][cols] to NVFP4 ([P3]: a global
+ * absmax pass, then the per-block quantisation).  Every decision is taken in
+ * fp32, in this order:
+ *   amax = max |x|;  global = amax / 2688   (2688 = 448 * 6: the largest block
+ *                                            scale times the largest E2M1 value)
+ *   per 16-element block: s = e4m3_rne(bmax / (6 * global)), d = e4m3(s) * global,
+ *   q = e2m1_rne(x / d) (0 where d = 0).
+ * An all-zero matrix has global = 0, zero scales and zero codes.  codes gets
+ * rows*cols/2 bytes, bscale rows*cols/16, *global one float. */
+int qo_nvfp4_quantize(long rows, long cols, const uint16_t* x, uint8_t* codes, uint8_t* bscale,
+                      float* global) {
+    if (rows <= 0 || cols <= 0 || cols % 16) return -1;
+    float amax = 0.0f;
+    for (long i = 0; i < rows * cols; ++i) {
+        float a = fabsf(bf16_to_float(x[i]));
+        if (a > amax) amax = a;
+    }
+    float g = amax / 2688.0f;
+    *global = g;
+    for (long r = 0; r < rows; ++r)
+        for (long b = 0; b < cols / 16; ++b) {
+            const uint16_t* xb = x + r * cols + 16 * b;
+            float bmax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float a = fabsf(bf16_to_float(xb[i]));
+                if (a > bmax) bmax = a;
+            }
+            uint8_t s = 0;
+            if (g > 0.0f) {
+                float den = 6.0f * g;
+                s = e4m3_encode_rne(bmax / den);
+            }
+            bscale[r * (cols / 16) + b] = s;
+            float d = (float)qo_fp8_e4m3_to_double(s) * g;
+            for (int i = 0; i < 16; i += 2) {
+                uint8_t lo = 0, hi = 0;
+                if (d > 0.0f) {
+                    lo = e2m1_encode_rne(bf16_to_float(xb[i]) / d);
+                    hi = e2m1_encode_rne(bf16_to_float(xb[i + 1]) / d);
+                }
+                codes[r * (cols / 2) + (16 * b + i) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ Q8_K activations */
 
 /* The int8-activation variant ([P2] "Gaps ... G8": the expert GEMVs run as

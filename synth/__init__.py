@@ -21,6 +21,10 @@ Recipe (every array is drawn with numpy ``Generator(PCG64(seed))``):
   (Q4_K: d and dmin; Q6_K: d).  Q6_K's int8 sub-block scales stay uniform bytes.
 * activations ~ N(0, 1) as float32.
 * decode-step extras: norm weights 1 + 0.1 N(0,1); KV cache entries fp16(N(0,1)).
+* NVFP4 experts (E2M1 codes two per byte, an E4M3 scale per 16 elements, an
+  fp32 global scale per expert matrix): uniform random code bytes, block scales
+  with exponent field uniform in 5..8 and a uniform mantissa, globals
+  base * U(0.5, 1.5); BF16 matrices for the quantiser ~ N(0, 0.02) truncated.
 * FP8 block-scaled experts (E4M3 codes, one fp32 scale per 128 x 128 block):
   codes with a random sign, a uniform 3-bit mantissa and an exponent field
   rint(N(10, 2.5)) clipped to 0..15 (never the NaN pattern); block scales
@@ -203,6 +207,72 @@ def moe_inputs_fp8(cfg: dict, T: int | None = None) -> dict:
     down, down_scale = fp8_expert_tensor(seed, "down", E, H, F, dsb)
     return dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=None, x=x, gate=gate,
                 gate_scale=gate_scale, up=up, up_scale=up_scale, down=down, down_scale=down_scale)
+
+
+# --------------------------------------------------------------------------- NVFP4 experts
+
+_TAG_NV = {"gate": 31, "up": 32, "down": 33}
+
+
+def nvfp4_matrix(seed: int, tag: int, index: int, rows: int, cols: int,
+                 global_base: float = 5e-3) -> tuple:
+    """One NVFP4 matrix: codes uint8 [rows][cols/2] (uniform random nibbles, every
+    E2M1 code equally likely), E4M3 block scales uint8 [rows][cols/16] (positive,
+    exponent field uniform in 5..8, mantissa uniform: 0.25 .. 3.75) and a float32
+    global scale global_base * U(0.5, 1.5)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
+    codes = np.frombuffer(rng.bytes(rows * cols // 2), dtype=np.uint8).reshape(rows, cols // 2).copy()
+    expo = rng.integers(5, 9, size=(rows, cols // 16), dtype=np.uint8)
+    mant = rng.integers(0, 8, size=(rows, cols // 16), dtype=np.uint8)
+    bscale = (expo << 3) | mant
+    g = np.float32(global_base * rng.uniform(0.5, 1.5))
+    return codes, bscale, g
+
+
+def nvfp4_expert_tensor(seed: int, which: str, n_experts: int, rows: int, cols: int,
+                        global_base: float = 5e-3) -> tuple:
+    """3-D NVFP4 expert tensor: codes [E][rows][cols/2], block scales
+    [E][rows][cols/16], global scales [E]."""
+    codes = np.empty((n_experts, rows, cols // 2), dtype=np.uint8)
+    bs = np.empty((n_experts, rows, cols // 16), dtype=np.uint8)
+    gs = np.empty(n_experts, dtype=np.float32)
+    for e in range(n_experts):
+        codes[e], bs[e], gs[e] = nvfp4_matrix(seed, _TAG_NV[which], e, rows, cols, global_base)
+    return codes, bs, gs
+
+
+NVFP4_CONFIGS = {
+    "tiny_nvfp4": dict(name="tiny, NVFP4 experts", H=512, E=8, K=2, F=256, T=5, seed=20,
+                       gu_global=1e-2, down_global=2e-2),
+    "decode_nvfp4": dict(name="qwen3moe-30b-a3b layer decode T=1, NVFP4 experts", H=2048, E=128,
+                         K=8, F=768, T=1, seed=21),
+}
+
+
+def moe_inputs_nvfp4(cfg: dict, T: int | None = None) -> dict:
+    """One MoE-FFN layer call over NVFP4 experts: router and x as ``moe_inputs``,
+    expert tensors from their own per-expert streams.  Global-scale bases:
+    gate/up ``cfg["gu_global"]`` (5e-3), down ``cfg["down_global"]`` (1e-2)."""
+    H, E, F = cfg["H"], cfg["E"], cfg["F"]
+    T = cfg["T"] if T is None else T
+    seed = cfg["seed"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    router = rng.normal(0.0, 0.02, size=(E, H)).astype(np.float32)
+    x = rng.normal(0.0, 1.0, size=(T, H)).astype(np.float32)
+    gb, db = cfg.get("gu_global", 5e-3), cfg.get("down_global", 1e-2)
+    d = dict(H=H, E=E, K=cfg["K"], F=F, T=T, router=router, bias=None, x=x)
+    for which, rows, cols, base in (("gate", F, H, gb), ("up", F, H, gb), ("down", H, F, db)):
+        d[which], d[which + "_bs"], d[which + "_gs"] = nvfp4_expert_tensor(seed, which, E, rows,
+                                                                            cols, base)
+    return d
+
+
+def bf16_matrix(seed: int, rows: int, cols: int, std: float = 0.02) -> np.ndarray:
+    """A BF16 weight matrix ~ N(0, std) as uint16 bit patterns (float32 values
+    truncated to their upper 16 bits), the input of the NVFP4 runtime quantiser."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 77])))
+    v = rng.normal(0.0, std, size=(rows, cols)).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
 
 
 # --------------------------------------------------------------------------- 48-layer decode step

@@ -71,6 +71,10 @@ WORKLOADS = {
     "decode_fp8": dict(cfg=None, fp8="decode_fp8", copies=8, e2e=2000, steps=20000, warmup=200,
                        desc="qwen3moe-30b-a3b MoE layer decode, T=1, FP8 (E4M3) experts with one "
                             "fp32 scale per 128x128 block, F32 router (supplementary)"),
+    "decode_nvfp4": dict(cfg=None, nvfp4="decode_nvfp4", copies=16, e2e=2000, steps=20000,
+                         warmup=200,
+                         desc="qwen3moe-30b-a3b MoE layer decode, T=1, NVFP4 experts (E2M1, E4M3 "
+                              "scale per 16, fp32 global per matrix), F32 router (supplementary)"),
     "prefill_fp8": dict(cfg=None, fp8="decode_fp8", T=512, copies=2, e2e=20, steps=300, warmup=6,
                         desc="qwen3moe-30b-a3b MoE layer prefill, T=512, FP8 (E4M3) experts with "
                              "one fp32 scale per 128x128 block, F32 router (supplementary)"),
@@ -79,7 +83,7 @@ WORKLOADS = {
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
                "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None,
-               "decode_fp8": None, "prefill_fp8": None}
+               "decode_fp8": None, "prefill_fp8": None, "decode_nvfp4": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -255,16 +259,18 @@ def cpu_sample_layer(inp, seconds: float, max_tokens: int, q8k: bool = False):
                         f"oracle calls on the first {n} tokens of this layer workload")
 
 
-def cpu_sample_fp8(inp, seconds: float, max_tokens: int):
-    """The FP8 oracle on a bounded sample of the layer workload: tokens/s/layer."""
+def cpu_sample_fp8(inp, seconds: float, max_tokens: int, nv: bool = False):
+    """The FP8 / NVFP4 oracle on a bounded sample of the layer workload: tokens/s/layer."""
     import oracle
     oracle.build()
     n = min(inp["T"], max_tokens)
     one = dict(inp)
     one["x"] = inp["x"][:n]
     one["T"] = n
-    return cpu_baseline(lambda: oracle.moe_forward_fp8(one), n, seconds,
-                        f"FP8 oracle calls on the first {n} tokens of this layer workload")
+    forward = oracle.moe_forward_nvfp4 if nv else oracle.moe_forward_fp8
+    return cpu_baseline(lambda: forward(one), n, seconds,
+                        f"{'NVFP4' if nv else 'FP8'} oracle calls on the first {n} tokens of this "
+                        "layer workload")
 
 
 def cpu_sample_step(geo, seconds: float):
@@ -301,13 +307,16 @@ def run_reference(args):
     oracle.build()
     w = WORKLOADS[args.workload]
     budget = 150.0
-    if w.get("fp8"):
-        inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]])
+    if w.get("fp8") or w.get("nvfp4"):
+        nv = bool(w.get("nvfp4"))
+        inp = (synth.moe_inputs_nvfp4(synth.NVFP4_CONFIGS[w["nvfp4"]]) if nv
+               else synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T")))
         sample = min(inp["T"], 8)
         one = dict(inp)
         one["x"] = inp["x"][:sample]
         one["T"] = sample
-        step = lambda: oracle.moe_forward_fp8(one)  # noqa: E731
+        forward = oracle.moe_forward_nvfp4 if nv else oracle.moe_forward_fp8
+        step = lambda: forward(one)  # noqa: E731
         tokens_per_step = sample
         what = f"{sample} tokens of the {args.workload} layer workload per step"
     elif w["cfg"] is not None:
@@ -596,11 +605,18 @@ def bench_layer(args, torch, q, dev, stream, ws, pg, local):
 
 
 def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
-    """The MoE layer over FP8 block-scaled experts (qmoe_forward_fp8)."""
+    """The MoE layer over FP8 block-scaled experts (qmoe_forward_fp8) or NVFP4
+    experts (qmoe_forward_nvfp4)."""
     w = WORKLOADS[args.workload]
-    inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T"))
+    nv = bool(w.get("nvfp4"))
+    if nv:
+        inp = synth.moe_inputs_nvfp4(synth.NVFP4_CONFIGS[w["nvfp4"]], T=w.get("T"))
+        names = ("router", "gate", "gate_bs", "gate_gs", "up", "up_bs", "up_gs", "down", "down_bs",
+                 "down_gs")
+    else:
+        inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T"))
+        names = ("router", "gate", "gate_scale", "up", "up_scale", "down", "down_scale")
     T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
-    names = ("router", "gate", "gate_scale", "up", "up_scale", "down", "down_scale")
     x = torch.from_numpy(inp["x"]).to(dev)
     base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev) for n in names}
     R = args.copies
@@ -609,16 +625,22 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
     ctx = q.qmoe_create(q.make_config(H, E, K, F, T, 1, stream.cuda_stream))
 
     def fwd(c, xin, o, ids=None):
-        q.qmoe_forward_fp8(ctx, xin, c["router"], c["gate"], c["gate_scale"], c["up"],
-                           c["up_scale"], c["down"], c["down_scale"], T, o, ids, None)
+        if nv:
+            q.qmoe_forward_nvfp4(ctx, xin, *[c[n] for n in names], T, o, ids, None)
+        else:
+            q.qmoe_forward_fp8(ctx, xin, c["router"], c["gate"], c["gate_scale"], c["up"],
+                               c["up_scale"], c["down"], c["down_scale"], T, o, ids, None)
 
     ids = torch.empty((T, K), dtype=torch.int32, device=dev)
     with torch.cuda.stream(stream):
         fwd(base, x, out, ids)
     stream.synchronize()
     distinct = len(np.unique(ids.cpu().numpy()))
-    per_expert = 3 * F * H + 4 * (inp["gate_scale"][0].size + inp["up_scale"][0].size
-                                  + inp["down_scale"][0].size)
+    if nv:   # codes, E4M3 block scales and the fp32 global of each matrix
+        per_expert = 3 * (F * H // 2 + F * H // 16 + 4)
+    else:    # codes and the fp32 block scales
+        per_expert = 3 * F * H + 4 * (inp["gate_scale"][0].size + inp["up_scale"][0].size
+                                      + inp["down_scale"][0].size)
     ebytes = distinct * per_expert
     rbytes = E * H * 4
     ms, clocks = timed_graphs(torch, stream, [(lambda c=c: fwd(c, x, out)) for c in copies],
@@ -657,21 +679,25 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
         e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
         launches=(q.LAUNCHES_PER_FP8_FORWARD if T <= 8 else q.LAUNCHES_PER_FP8_FORWARD + 1
-                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_FP8_FORWARD_MANY),
+                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_NVFP4_FORWARD + 2 if nv
+                  else q.LAUNCHES_PER_FP8_FORWARD_MANY),
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct, "expert_bytes": per_expert,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
                       "written right before the timed region"},
-        kernel=("whole FP8 layer call (router, top-k, gate/up, down, combine)" if T <= q.FP8_GEMV_MAX
+        kernel=(f"whole {'NVFP4' if nv else 'FP8'} layer call (router, top-k, gate/up, down, combine)"
+                if T <= q.FP8_GEMV_MAX or nv
                 else "whole FP8 layer call (routing, gather, grouped tensor-core GEMMs, combine)"),
-        dtype=("e4m3 weights widened exactly, f32 activations and accumulate" if T <= q.FP8_GEMV_MAX
+        dtype=("e2m1 weights and e4m3 scales widened exactly, f32 activations and accumulate" if nv
+               else "e4m3 weights widened exactly, f32 activations and accumulate"
+               if T <= q.FP8_GEMV_MAX
                else "e4m3 weights widened to f16 tensor-core operands, f32 accumulate"))
-    if T > q.FP8_GEMV_MAX:
+    if T > q.FP8_GEMV_MAX and not nv:
         res["tensor_tflops"] = T * K * 2 * (2 * F * H + H * F) / step_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
-        cpu = cpu_sample_fp8(inp, args.cpu_seconds, 8)
+        cpu = cpu_sample_fp8(inp, args.cpu_seconds, 8, nv)
     return res, cpu
 
 
@@ -884,7 +910,7 @@ def main():
         res, cpu = bench_step48(args, torch, q, dev, stream, ws, pg, local)
     elif args.workload == "prefill_layer":
         res, cpu = bench_prefill_layer(args, torch, q, dev, stream, ws, pg, local)
-    elif WORKLOADS[args.workload].get("fp8"):
+    elif WORKLOADS[args.workload].get("fp8") or WORKLOADS[args.workload].get("nvfp4"):
         res, cpu = bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local)
     else:
         res, cpu = bench_layer(args, torch, q, dev, stream, ws, pg, local)

@@ -15,7 +15,9 @@
  *
  * qmoe_forward_q8k runs the same layer with x and a quantised to 8-bit (Q8_K)
  * activations before every expert GEMV (the int8 variant of "Gaps ... G8").
- * qmoe_forward_fp8 runs it over FP8 block-scaled experts instead of k-quants.
+ * qmoe_forward_fp8 and qmoe_forward_nvfp4 run it over FP8 block-scaled and
+ * NVFP4 experts instead of k-quants (qmoe_nvfp4_quantize makes NVFP4 weights
+ * from BF16 ones).
  *
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer that the caller allocated and owns
@@ -168,6 +170,44 @@ qmoe_status qmoe_forward_fp8(qmoe_ctx* ctx, const float* hidden_in, const float*
                              const void* down_exps, const float* down_scale,
                              int n_tokens, float* hidden_out, int32_t* ids_out,
                              float* weights_out);
+
+/* The MoE layer over NVFP4 experts with the F32 router (atlasinference source
+ * page "spark_model/weight_loader/qwen3.rs", load_layers: weights quantised
+ * from BF16 to NVFP4 at load).  NVFP4 (the public format): FP4 E2M1 elements,
+ * two per byte with the even element in the low nibble, one E4M3 scale per 16
+ * consecutive elements of a row, one fp32 scale per matrix:
+ *   weight (r, c) of expert e = e2m1(code) * e4m3(bscale[e][r][c/16]) * global[e].
+ *   gate_exps / up_exps: codes [E][ffn][hidden/2]; *_bscale [E][ffn][hidden/16];
+ *   down_exps: codes [E][hidden][ffn/2]; down_bscale [E][hidden][ffn/16];
+ *   *_global: fp32 [E].
+ * x, the SwiGLU output and every sum are fp32 (expert GEMVs on the CUDA cores
+ * for every n_tokens).  hidden_out = hidden_in + MoE(hidden_in) and may alias
+ * hidden_in.  ids_out / weights_out as qmoe_forward_ex (nullable).  Serves
+ * hidden/512 in {1, 2, 4, 8} and ffn/256 in 1..6 (QMOE_ERR_SHAPE otherwise).
+ * Code and activation pointers 16-byte aligned, block scales 2-byte, globals
+ * 4-byte (QMOE_ERR_MISALIGNED).  Argument errors are returned before any launch. */
+qmoe_status qmoe_forward_nvfp4(qmoe_ctx* ctx, const float* hidden_in, const float* router_w,
+                               const void* gate_exps, const void* gate_bscale,
+                               const float* gate_global, const void* up_exps,
+                               const void* up_bscale, const float* up_global,
+                               const void* down_exps, const void* down_bscale,
+                               const float* down_global, int n_tokens, float* hidden_out,
+                               int32_t* ids_out, float* weights_out);
+
+/* Runtime quantisation of n_mats consecutive BF16 matrices [rows][cols] (device
+ * memory, bit patterns) to NVFP4 (same page: a global-absmax pass, then the
+ * per-block quantisation).  Per matrix, every decision in fp32:
+ *   amax = max |x|; global = amax / 2688 (448 * 6);
+ *   per 16 elements: s = E4M3 nearest to bmax / (6 * global) (ties to even,
+ *   saturating at 448); d = e4m3(s) * global; code = E2M1 nearest to x / d
+ *   (ties to even, saturating at 6; 0 where d = 0).
+ * Outputs (device, caller-owned): codes [n_mats][rows][cols/2] (8-byte
+ * aligned), bscale [n_mats][rows][cols/16], global [n_mats] (4-byte aligned).
+ * x 16-byte aligned; cols a positive multiple of 16; n_mats in 1..1024.
+ * Enqueued on the context's stream; uses a few bytes of its workspace, so it is
+ * ordered with the context's other calls. */
+qmoe_status qmoe_nvfp4_quantize(qmoe_ctx* ctx, const void* x_bf16, int n_mats, int rows, int cols,
+                                void* codes, void* bscale, float* global);
 
 /* Same as qmoe_forward, but hidden_in / hidden_out are HOST pointers (pinned
  * memory gives asynchronous copies).  Copies the activations to the device

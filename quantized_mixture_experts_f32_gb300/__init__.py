@@ -39,6 +39,9 @@ LAUNCHES_PER_Q8K_FORWARD = 7
 FP8_GEMV_MAX = 32
 LAUNCHES_PER_FP8_FORWARD = 4           # up to 8 tokens (5 for 9..32)
 LAUNCHES_PER_FP8_FORWARD_MANY = 7
+# qmoe_forward_nvfp4: as the FP8 GEMV path at every token count (4 launches up
+# to 8 tokens, 5 for 9..32, 6 beyond with the many-token routing)
+LAUNCHES_PER_NVFP4_FORWARD = 4
 # one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with
 # its RMSNorm)
@@ -54,7 +57,8 @@ LAUNCHES_PER_PREFILL_LAYER_ATTN = 7
 EXPORTED = ["qmoe_create", "qmoe_destroy", "qmoe_set_stream", "qmoe_forward", "qmoe_forward_ex",
             "qmoe_forward_host", "qmoe_decode_step", "qmoe_prefill", "qmoe_get_status", "qmoe_last_error",
             "qmoe_workspace_bytes", "qmoe_expert_stride", "qmoe_forward_noalloc",
-            "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_forward_fp8", "qmoe_noalloc_status",
+            "qmoe_fused_decode_available", "qmoe_forward_q8k", "qmoe_forward_fp8", "qmoe_forward_nvfp4",
+            "qmoe_nvfp4_quantize", "qmoe_noalloc_status",
             "qmoe_debug_stall_next", "qmoe_debug_fail_alloc"]
 
 
@@ -102,6 +106,10 @@ def _load():
     L.qmoe_forward_q8k.restype = i
     L.qmoe_forward_fp8.argtypes = [vp, fp, fp, vp, fp, vp, fp, vp, fp, i, fp, ip, fp]
     L.qmoe_forward_fp8.restype = i
+    L.qmoe_forward_nvfp4.argtypes = [vp, fp, fp] + [vp, vp, fp] * 3 + [i, fp, ip, fp]
+    L.qmoe_forward_nvfp4.restype = i
+    L.qmoe_nvfp4_quantize.argtypes = [vp, vp, i, i, i, vp, vp, fp]
+    L.qmoe_nvfp4_quantize.restype = i
     L.qmoe_forward_host.restype = i
     L.qmoe_decode_step.argtypes = [vp, C.POINTER(qmoe_layer_weights), i, i, fp, ip]
     L.qmoe_decode_step.restype = i
@@ -192,6 +200,21 @@ def qmoe_forward_fp8(ctx, hidden_in, router_w, gate_exps, gate_scale, up_exps, u
                                      _ptr(gate_scale), _ptr(up_exps), _ptr(up_scale),
                                      _ptr(down_exps), _ptr(down_scale), n_tokens,
                                      _ptr(hidden_out), _ptr(ids_out), _ptr(weights_out)))
+
+
+def qmoe_forward_nvfp4(ctx, hidden_in, router_w, gate_exps, gate_bscale, gate_global, up_exps,
+                       up_bscale, up_global, down_exps, down_bscale, down_global, n_tokens,
+                       hidden_out, ids_out=None, weights_out=None):
+    _check(ctx, lib.qmoe_forward_nvfp4(ctx, _ptr(hidden_in), _ptr(router_w), _ptr(gate_exps),
+                                       _ptr(gate_bscale), _ptr(gate_global), _ptr(up_exps),
+                                       _ptr(up_bscale), _ptr(up_global), _ptr(down_exps),
+                                       _ptr(down_bscale), _ptr(down_global), n_tokens,
+                                       _ptr(hidden_out), _ptr(ids_out), _ptr(weights_out)))
+
+
+def qmoe_nvfp4_quantize(ctx, x_bf16, n_mats, rows, cols, codes, bscale, global_scale):
+    _check(ctx, lib.qmoe_nvfp4_quantize(ctx, _ptr(x_bf16), n_mats, rows, cols, _ptr(codes),
+                                        _ptr(bscale), _ptr(global_scale)))
 
 
 def qmoe_forward_host(ctx, hidden_in_host, router_w, gate_exps, up_exps, down_exps, gate_t, up_t,

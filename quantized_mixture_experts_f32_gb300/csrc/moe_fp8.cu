@@ -18,10 +18,9 @@
 // warp keeps 12 to 16 16-byte loads in flight.  Both kernels are programmatic
 // dependents of the kernel before them; the down kernel loads its first item's
 // weights while the gate/up kernel still runs.
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <math.h>
 
+#include "lowbit.cuh"
 #include "pdl.cuh"
 #include "qmoe_internal.h"
 
@@ -30,11 +29,6 @@ namespace qmoe {
 namespace {
 
 constexpr int F8_THREADS = 256;
-
-__device__ __forceinline__ float2 e4m3x2_f2(uint32_t two) {
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-    return __half22float2(__half2(r));
-}
 
 // dot of 16 E4M3 weights (one 16-byte chunk) with 16 consecutive fp32 values
 __device__ __forceinline__ float chunk_dot(uint4 w, const float* __restrict__ v) {
@@ -51,21 +45,6 @@ __device__ __forceinline__ float chunk_dot(uint4 w, const float* __restrict__ v)
         a1 = fmaf(hi.y, x.w, a1);
     }
     return a0 + a1;
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// sum over the 16 lanes of a half-warp (every lane gets its half's sum)
-__device__ __forceinline__ float half_sum(float v) {
-#pragma unroll
-    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
 }
 
 // Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
@@ -109,14 +88,19 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
         for (int q = p0; q < p1; ++q) {
             const int p = pair_list[q];
             const float* xt = x + (size_t)(p / K) * H + 16 * hl;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                opaque(wg[k]);
+                opaque(wu[k]);
+            }
             float g = 0.f, v = 0.f;
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 g = fmaf(sg[k], chunk_dot(wg[k], xt + 256 * k), g);
                 v = fmaf(su[k], chunk_dot(wu[k], xt + 256 * k), v);
             }
-            g = half_sum(g);
-            v = half_sum(v);
+            g = group_sum<16>(g);
+            v = group_sum<16>(v);
             if (hl == 0) act[(size_t)p * F + f] = g / (1.f + expf(-g)) * v;
         }
     }
@@ -167,14 +151,19 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
         for (int q = p0; q < p1; ++q) {
             const int p = __ldcg(pair_list + q);
             const float* ap = act + (size_t)p * F + 16 * hl;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                opaque(w0[k]);
+                opaque(w1[k]);
+            }
             float a = 0.f, b = 0.f;
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 a = fmaf(s[k], chunk_dot(w0[k], ap + 256 * k), a);
                 b = fmaf(s[k], chunk_dot(w1[k], ap + 256 * k), b);
             }
-            a = half_sum(a);
-            b = half_sum(b);
+            a = group_sum<16>(a);
+            b = group_sum<16>(b);
             if (hl == 0) {
                 y[(size_t)p * H + h] = a;
                 y[(size_t)p * H + h + 2] = b;
@@ -183,27 +172,11 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
     }
 }
 
-// CTAs of a launch: enough for every warp item, at most the CTAs that are
-// resident at once (the kernels stride over the items)
-template <typename Kern>
-int fp8_grid(Kern kern, int* resident, int items, int num_sms) {
-    if (!*resident) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, F8_THREADS, 0) != cudaSuccess || n < 1)
-            n = 1;
-        *resident = n;
-    }
-    const int warps = F8_THREADS / 32;
-    const int need = (items + warps - 1) / warps;
-    const int cap = num_sms * *resident;
-    return need < cap ? (need > 0 ? need : 1) : cap;
-}
-
 template <int NC>
 cudaError_t gateup_nc(const MoeShape& s, const float* x, const Fp8Experts& w, const Route& r,
                       float* act, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
-    const int grid = fp8_grid(fp8_gateup_kernel<NC>, &resident, items, num_sms);
+    const int grid = strided_grid(fp8_gateup_kernel<NC>, F8_THREADS, &resident, items, num_sms);
     return launch_pdl(fp8_gateup_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.H, s.F, s.K,
                       w.gate, w.gate_scale, w.up, w.up_scale, r.n_used, r.used_expert,
                       r.used_first, r.pair_list, act);
@@ -213,7 +186,7 @@ template <int NC>
 cudaError_t down_nc(const MoeShape& s, const float* act, const Fp8Experts& w, const Route& r,
                     float* y, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
-    const int grid = fp8_grid(fp8_down_kernel<NC>, &resident, items, num_sms);
+    const int grid = strided_grid(fp8_down_kernel<NC>, F8_THREADS, &resident, items, num_sms);
     return launch_pdl(fp8_down_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, act, s.H, s.F,
                       w.down, w.down_scale, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
 }

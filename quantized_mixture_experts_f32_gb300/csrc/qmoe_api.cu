@@ -25,6 +25,7 @@ struct qmoe_ctx {
     float* hout;      // [T][H]
     int* status;      // device status word
     unsigned* bar;    // decode kernels' control words (exit counter, launch tag, arrival words)
+    unsigned* nvq;    // per-matrix amax words of qmoe_nvfp4_quantize
     qmoe::FusedBufs fb; // tagged values passed between the fused kernel's CTAs
     __half* xp;       // [P][H] fp16 gathered x (prefill)
     __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
@@ -61,6 +62,7 @@ void create_fail(const char* fmt, ...) {
 
 constexpr int DECODE_ALIAS_MAX = 8;
 constexpr int FP8_GEMV_MAX = 32;         // qmoe_forward_fp8: largest call on the expert GEMVs
+constexpr int NVFP4_QUANT_MATS_MAX = 1024;   // matrices per qmoe_nvfp4_quantize call
 constexpr int FUSED_GRID_MAX = 1024;     // largest grid of the fused decode kernel
 
 qmoe_status fail(qmoe_ctx* c, qmoe_status s, const char* fmt, ...) {
@@ -85,7 +87,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, arrive, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
+        status, bar, arrive, nvq, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
         rope_cs, pl, total;
     int attn_splits;
     bool pl_ok;
@@ -132,6 +134,7 @@ Layout layout(const qmoe_config* c) {
     L.status = take(sizeof(int) * 16);
     L.bar = take(sizeof(unsigned) * 64);
     L.arrive = take(sizeof(unsigned) * 4);
+    L.nvq = take(sizeof(unsigned) * NVFP4_QUANT_MATS_MAX);
     L.xp = take(sizeof(__half) * P * H);
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
@@ -362,6 +365,7 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.tokmap = reinterpret_cast<uint32_t*>(b + L.tokmap);
     c->route.jmap = reinterpret_cast<uint8_t*>(b + L.jmap);
     c->route.arrive = reinterpret_cast<unsigned*>(b + L.arrive);
+    c->nvq = reinterpret_cast<unsigned*>(b + L.nvq);
     c->q8 = qmoe::q8_bufs_carve(reinterpret_cast<unsigned char*>(b + L.q8), c->cfg.max_tokens, c->cfg.hidden,
                                 c->cfg.top_k, c->cfg.ffn);
     c->act = reinterpret_cast<float*>(b + L.act);
@@ -527,6 +531,71 @@ qmoe_status qmoe_forward_fp8(qmoe_ctx* c, const float* hidden_in, const float* r
         e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
     }
+    c->err[0] = 0;
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float* router_w,
+                               const void* gate_exps, const void* gate_bscale, const float* gate_global,
+                               const void* up_exps, const void* up_bscale, const float* up_global,
+                               const void* down_exps, const void* down_bscale,
+                               const float* down_global, int n_tokens, float* hidden_out,
+                               int32_t* ids_out, float* weights_out) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    if (!hidden_in || !router_w || !gate_exps || !gate_bscale || !gate_global || !up_exps ||
+        !up_bscale || !up_global || !down_exps || !down_bscale || !down_global || !hidden_out)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null tensor pointer");
+    const qmoe_config& k = c->cfg;
+    if (n_tokens < 1 || n_tokens > k.max_tokens)
+        return fail(c, QMOE_ERR_SHAPE, "n_tokens=%d outside 1..max_tokens=%d", n_tokens, k.max_tokens);
+    if (!qmoe::nvfp4_supported(k.hidden, k.ffn))
+        return fail(c, QMOE_ERR_SHAPE, "NVFP4 experts serve hidden/512 in {1,2,4,8} and ffn/256 in 1..6 (hidden=%d ffn=%d)", k.hidden, k.ffn);
+    if (!aligned16(hidden_in) || !aligned16(router_w) || !aligned16(gate_exps) ||
+        !aligned16(up_exps) || !aligned16(down_exps) || !aligned16(hidden_out))
+        return fail(c, QMOE_ERR_MISALIGNED, "activation, router and code base pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(gate_bscale) | reinterpret_cast<uintptr_t>(up_bscale) |
+         reinterpret_cast<uintptr_t>(down_bscale)) & 1u)
+        return fail(c, QMOE_ERR_MISALIGNED, "block-scale pointers must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(gate_global) | reinterpret_cast<uintptr_t>(up_global) |
+         reinterpret_cast<uintptr_t>(down_global)) & 3u)
+        return fail(c, QMOE_ERR_MISALIGNED, "global-scale pointers must be 4-byte aligned");
+    qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route);
+    cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
+                         : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
+    const qmoe::NvExperts w{static_cast<const uint8_t*>(gate_exps), static_cast<const uint8_t*>(gate_bscale),
+                            gate_global, static_cast<const uint8_t*>(up_exps),
+                            static_cast<const uint8_t*>(up_bscale), up_global,
+                            static_cast<const uint8_t*>(down_exps), static_cast<const uint8_t*>(down_bscale),
+                            down_global};
+    e = qmoe::launch_nvfp4_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 expert launch");
+    e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    if (ids_out || weights_out) {
+        e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");
+    }
+    c->err[0] = 0;
+    return QMOE_OK;
+}
+
+qmoe_status qmoe_nvfp4_quantize(qmoe_ctx* c, const void* x_bf16, int n_mats, int rows, int cols,
+                                void* codes, void* bscale, float* global) {
+    if (!c) return QMOE_ERR_INVALID_ARG;
+    if (!x_bf16 || !codes || !bscale || !global)
+        return fail(c, QMOE_ERR_INVALID_ARG, "null tensor pointer");
+    if (n_mats < 1 || n_mats > NVFP4_QUANT_MATS_MAX || rows < 1 || cols < 16 || cols % 16)
+        return fail(c, QMOE_ERR_SHAPE, "n_mats=%d (1..%d), rows=%d, cols=%d (a positive multiple of 16)",
+                    n_mats, NVFP4_QUANT_MATS_MAX, rows, cols);
+    if (!aligned16(x_bf16) || (reinterpret_cast<uintptr_t>(codes) & 7u) ||
+        (reinterpret_cast<uintptr_t>(global) & 3u))
+        return fail(c, QMOE_ERR_MISALIGNED, "x 16-byte, codes 8-byte and global 4-byte aligned");
+    const cudaError_t e = qmoe::launch_nvfp4_quantize(
+        static_cast<const uint16_t*>(x_bf16), n_mats, rows, cols, static_cast<uint8_t*>(codes),
+        static_cast<uint8_t*>(bscale), global, c->nvq, c->num_sms, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 quantise launch");
     c->err[0] = 0;
     return QMOE_OK;
 }

@@ -95,6 +95,27 @@ bool fp8_supported(int H, int F);
 // into y [P][H] (launch_combine finishes the layer)
 cudaError_t launch_fp8_experts(const MoeShape& s, const float* x, const Fp8Experts& w,
                                const Route& r, float* act, float* y, int num_sms, cudaStream_t st);
+// NVFP4 experts (moe_nvfp4.cu): E2M1 codes [E][rows][cols/2] (even element in
+// the low nibble), E4M3 block scales [E][rows][cols/16], fp32 globals [E].
+struct NvExperts {
+    const uint8_t* gate;
+    const uint8_t* gate_bs;
+    const float* gate_gs;
+    const uint8_t* up;
+    const uint8_t* up_bs;
+    const float* up_gs;
+    const uint8_t* down;
+    const uint8_t* down_bs;
+    const float* down_gs;
+};
+bool nvfp4_supported(int H, int F);
+cudaError_t launch_nvfp4_experts(const MoeShape& s, const float* x, const NvExperts& w,
+                                 const Route& r, float* act, float* y, int num_sms, cudaStream_t st);
+// BF16 -> NVFP4 of n_mats matrices [rows][cols] (consecutive); amax_bits: n_mats
+// words of scratch
+cudaError_t launch_nvfp4_quantize(const uint16_t* x, int n_mats, int rows, int cols, uint8_t* codes,
+                                  uint8_t* bscale, float* global, unsigned* amax_bits, int num_sms,
+                                  cudaStream_t st);
 // many tokens (after launch_route_many): gather x as fp16, grouped gate/up and
 // down GEMMs on the tensor cores with the FP8 weights widened to fp16 in shared
 // memory, combine into out (prefill_umma.cu)

@@ -75,6 +75,10 @@ WORKLOADS = {
                          warmup=200,
                          desc="qwen3moe-30b-a3b MoE layer decode, T=1, NVFP4 experts (E2M1, E4M3 "
                               "scale per 16, fp32 global per matrix), F32 router (supplementary)"),
+    "prefill_nvfp4": dict(cfg=None, nvfp4="decode_nvfp4", T=512, copies=3, e2e=20, steps=300,
+                          warmup=6,
+                          desc="qwen3moe-30b-a3b MoE layer prefill, T=512, NVFP4 experts, F32 "
+                               "router (supplementary)"),
     "prefill_fp8": dict(cfg=None, fp8="decode_fp8", T=512, copies=2, e2e=20, steps=300, warmup=6,
                         desc="qwen3moe-30b-a3b MoE layer prefill, T=512, FP8 (E4M3) experts with "
                              "one fp32 scale per 128x128 block, F32 router (supplementary)"),
@@ -83,7 +87,8 @@ WORKLOADS = {
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
                "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None,
-               "decode_fp8": None, "prefill_fp8": None, "decode_nvfp4": None}
+               "decode_fp8": None, "prefill_fp8": None, "decode_nvfp4": None,
+               "prefill_nvfp4": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
 
 
@@ -309,7 +314,7 @@ def run_reference(args):
     budget = 150.0
     if w.get("fp8") or w.get("nvfp4"):
         nv = bool(w.get("nvfp4"))
-        inp = (synth.moe_inputs_nvfp4(synth.NVFP4_CONFIGS[w["nvfp4"]]) if nv
+        inp = (synth.moe_inputs_nvfp4(synth.NVFP4_CONFIGS[w["nvfp4"]], T=w.get("T")) if nv
                else synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T")))
         sample = min(inp["T"], 8)
         one = dict(inp)
@@ -617,6 +622,7 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[w["fp8"]], T=w.get("T"))
         names = ("router", "gate", "gate_scale", "up", "up_scale", "down", "down_scale")
     T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
+    fmt = "NVFP4" if nv else "FP8"
     x = torch.from_numpy(inp["x"]).to(dev)
     base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev) for n in names}
     R = args.copies
@@ -679,21 +685,20 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
         e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
         launches=(q.LAUNCHES_PER_FP8_FORWARD if T <= 8 else q.LAUNCHES_PER_FP8_FORWARD + 1
-                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_NVFP4_FORWARD + 2 if nv
-                  else q.LAUNCHES_PER_FP8_FORWARD_MANY),
+                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_FP8_FORWARD_MANY),
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct, "expert_bytes": per_expert,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
                       "written right before the timed region"},
-        kernel=(f"whole {'NVFP4' if nv else 'FP8'} layer call (router, top-k, gate/up, down, combine)"
-                if T <= q.FP8_GEMV_MAX or nv
-                else "whole FP8 layer call (routing, gather, grouped tensor-core GEMMs, combine)"),
-        dtype=("e2m1 weights and e4m3 scales widened exactly, f32 activations and accumulate" if nv
-               else "e4m3 weights widened exactly, f32 activations and accumulate"
-               if T <= q.FP8_GEMV_MAX
-               else "e4m3 weights widened to f16 tensor-core operands, f32 accumulate"))
-    if T > q.FP8_GEMV_MAX and not nv:
+        kernel=(f"whole {fmt} layer call (router, top-k, gate/up, down, combine)"
+                if T <= q.FP8_GEMV_MAX
+                else f"whole {fmt} layer call (routing, gather, grouped tensor-core GEMMs, combine)"),
+        dtype=(f"{'e2m1 weights and e4m3 scales' if nv else 'e4m3 weights'} widened exactly, f32 "
+               "activations and accumulate" if T <= q.FP8_GEMV_MAX
+               else f"{'e2m1' if nv else 'e4m3'} weights widened to f16 tensor-core operands, f32 "
+                    "accumulate"))
+    if T > q.FP8_GEMV_MAX:
         res["tensor_tflops"] = T * K * 2 * (2 * F * H + H * F) / step_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:

@@ -180,8 +180,11 @@ qmoe_status qmoe_forward_fp8(qmoe_ctx* ctx, const float* hidden_in, const float*
  *   gate_exps / up_exps: codes [E][ffn][hidden/2]; *_bscale [E][ffn][hidden/16];
  *   down_exps: codes [E][hidden][ffn/2]; down_bscale [E][hidden][ffn/16];
  *   *_global: fp32 [E].
- * x, the SwiGLU output and every sum are fp32 (expert GEMVs on the CUDA cores
- * for every n_tokens).  hidden_out = hidden_in + MoE(hidden_in) and may alias
+ * Up to 32 tokens (and whenever a block-scale pointer is not 16-byte aligned)
+ * the expert GEMVs run on the CUDA cores with x, the SwiGLU output and every
+ * sum in fp32; more tokens run as grouped GEMMs on the tensor cores (weights
+ * widened to fp16 as e2m1 * e4m3 * global rounded once, x and the SwiGLU
+ * output rounded to fp16, fp32 accumulation).  hidden_out = hidden_in + MoE(hidden_in) and may alias
  * hidden_in.  ids_out / weights_out as qmoe_forward_ex (nullable).  Serves
  * hidden/512 in {1, 2, 4, 8} and ffn/256 in 1..6 (QMOE_ERR_SHAPE otherwise).
  * Code and activation pointers 16-byte aligned, block scales 2-byte, globals

@@ -39,8 +39,8 @@ LAUNCHES_PER_Q8K_FORWARD = 7
 FP8_GEMV_MAX = 32
 LAUNCHES_PER_FP8_FORWARD = 4           # up to 8 tokens (5 for 9..32)
 LAUNCHES_PER_FP8_FORWARD_MANY = 7
-# qmoe_forward_nvfp4: as the FP8 GEMV path at every token count (4 launches up
-# to 8 tokens, 5 for 9..32, 6 beyond with the many-token routing)
+# qmoe_forward_nvfp4: as qmoe_forward_fp8 (4 launches up to 8 tokens, 5 for
+# 9..32, 7 on the tensor cores beyond)
 LAUNCHES_PER_NVFP4_FORWARD = 4
 # one decoder layer of qmoe_decode_step: RMSNorm + Q/K/V GEMV, attention (with
 # Q/K norm, RoPE and the KV append), split merge, O GEMV, fused MoE layer (with

@@ -22,6 +22,7 @@
 // tokens on average), so token tiles of 16..256 are the N side.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -71,7 +72,19 @@ constexpr int QSTAGE_GU = 2 * 64 * Q4K_BYTES;  // 64 gate + 64 up rows of one su
 constexpr int F8_COLS = 128;
 constexpr int QSTAGE_F8 = 128 * F8_COLS;
 constexpr int F8_NQ = 3;
-template <int QF> __host__ __device__ constexpr int gu_qbytes() { return QF ? F8_NQ * QSTAGE_F8 : GU_NQ * QSTAGE_GU; }
+// NVFP4 experts (QF 2): a raw stage is one 256-column slice of the item's rows,
+// E2M1 codes (128 bytes a row) then their E4M3 block scales (16 bytes a row)
+constexpr int NV_COLS = 256;
+constexpr int NV_CB = NV_COLS / 2, NV_SB = NV_COLS / 16;      // code / scale bytes per row
+constexpr int QSTAGE_NV = 128 * (NV_CB + NV_SB);
+template <int QF> __host__ __device__ constexpr int gu_qbytes() {
+    return QF == 1 ? F8_NQ * QSTAGE_F8 : QF == 2 ? F8_NQ * QSTAGE_NV : GU_NQ * QSTAGE_GU;
+}
+// raw bytes of the down kernel's ring (two halves, 2 KB-aligned so that the A
+// stages after it stay 1 KB-aligned)
+template <int QF> __host__ __device__ constexpr int dn_qring() {
+    return QF == 1 ? F8_NQ * QSTAGE_F8 : QF == 2 ? ((F8_NQ * QSTAGE_NV + 2047) & ~2047) : 0;
+}
 // down kernel: token-tile rows, A / B stages, TMEM columns (two accumulators)
 constexpr int DN_NMAX = 128;
 constexpr int DN_NA = 2;
@@ -130,6 +143,30 @@ __device__ __forceinline__ void f8_quarter(uint4 q, float s, uint8_t* arow, int 
     }
     *reinterpret_cast<uint4*>(arow + o0) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(arow + o1) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// 16 E2M1 codes (8 bytes, the even element in each low nibble) times the block
+// scale -> two 16-byte runs of 8 fp16 weights at the row's swizzled chunks
+__device__ __forceinline__ void nv_quarter(uint2 q, float s, uint8_t* arow, int o0, int o1) {
+    const uint32_t w[2] = {q.x, q.y};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const __half2_raw r = __nv_cvt_fp4x2_to_halfraw2(
+                static_cast<__nv_fp4x2_storage_t>((w[i] >> (8 * b)) & 0xffu), __NV_E2M1);
+            const float2 f = __half22float2(__half2(r));
+            h[4 * i + b] = pack_half2(f.x * s, f.y * s);
+        }
+    }
+    *reinterpret_cast<uint4*>(arow + o0) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(arow + o1) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+__device__ __forceinline__ float e4m3_float(uint32_t byte) {
+    const __half_raw r = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte & 0xffu), __NV_E4M3);
+    return __half2float(__half(r));
 }
 
 // Q4_K: scale and offset of the two sub-blocks (2c, 2c + 1) of k-block c, as
@@ -204,7 +241,8 @@ struct GuParams {
     int seg_rows[3], seg_yoff[3];
     int ksplit;
     size_t part_stride;
-    // FP8 experts (QF 1): fp32 scales per 128 x 128 block, [E][F/128][H/128]
+    // FP8 experts (QF 1): fp32 scales per 128 x 128 block, [E][F/128][H/128];
+    // NVFP4 experts (QF 2): fp32 global scales [E] (block scales come by TMA)
     const float* gscale;
     const float* uscale;
 };
@@ -272,6 +310,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_gateup(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                    const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x64,
                    const __grid_constant__ CUtensorMap tm_x128, const __grid_constant__ CUtensorMap tm_xg,
+                   const __grid_constant__ CUtensorMap tm_gsc, const __grid_constant__ CUtensorMap tm_usc,
                    const GuParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     // 1024-aligned base, kept a shared-space pointer (an integer round trip
@@ -279,11 +318,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
     const int KS = MODE == 0 ? 1 : p.ksplit;
-    static_assert(QF == 0 || MODE == 0, "FP8 weights in the MoE mode only");
+    static_assert(QF == 0 || MODE == 0, "FP8 / NVFP4 weights in the MoE mode only");
     constexpr int NQS = QF ? F8_NQ : GU_NQ;              // raw stages
-    constexpr int QSB = QF ? QSTAGE_F8 : QSTAGE_GU;      // raw stage bytes
-    constexpr int QCOL = QF ? F8_COLS : Q4K_BYTES;       // raw bytes per row per stage
-    constexpr int KPS = QF ? F8_COLS / KBLK : QK / KBLK; // k-blocks per raw stage
+    constexpr int QSB = QF == 1 ? QSTAGE_F8 : QF == 2 ? QSTAGE_NV : QSTAGE_GU;   // raw stage bytes
+    constexpr int QCOL = QF == 1 ? F8_COLS : QF == 2 ? NV_CB : Q4K_BYTES;   // code bytes per row per stage
+    constexpr int KPS = QF == 1 ? F8_COLS / KBLK : QK / KBLK;   // k-blocks per raw stage
     const int NKB = H / KBLK / KS, NSB = NKB / KPS;      // per item
     const int FT = MODE == 0 ? F / 64 : F / TILE_M;
 
@@ -357,6 +396,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                         tma_load_2d(dst + 64 * QCOL, &tm_up, sb * QCOL, ybase, &bars->qfull[st]);
                     else
                         tma_load_2d(dst + 64 * QCOL, tw, (sb0 + sb) * QCOL, ybase + 64, &bars->qfull[st]);
+                    if (QF == 2) {
+                        tma_load_2d(dst + 128 * NV_CB, &tm_gsc, sb * NV_SB, ybase, &bars->qfull[st]);
+                        tma_load_2d(dst + 128 * NV_CB + 64 * NV_SB, &tm_usc, sb * NV_SB, ybase, &bars->qfull[st]);
+                    }
                 }
             }
         }
@@ -413,6 +456,54 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                     umma_commit(&bars->aempty[pr]);
                 }
                 if (ok) umma_commit(&bars->accfull[buf]);
+            }
+        }
+    } else if (QF == 2 && warp < NDQ) {
+        // NVFP4 dequant: thread -> A row 8*warp + (lane & 7) and 16-k quarter
+        // qq = lane >> 3 of each k-block (one 16-element scale block: 8 code
+        // bytes and one scale byte); A rows paired gate / up as for k-quants
+        const int qq = lane >> 3, sw = lane & 7;
+        const int row = 8 * warp + (lane & 7);
+        const int grp = row >> 5, w32 = row & 31;
+        const bool is_gate = w32 < 16;
+        const int srow = is_gate ? 16 * grp + w32 : 64 + 16 * grp + (w32 - 16);
+        const int rowb = row * 128;
+        const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+        const float* glob = is_gate ? p.gscale : p.uscale;
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int gk = 0, gs = 0;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            const GuItem w = gu_item<MODE>(p, tfirst, n_used, blockIdx.x + j * gridDim.x);
+            const float gsc = __ldg(glob + w.e);
+            for (int sb = 0; sb < NSB; ++sb, ++gs) {
+                const int sq = gs % NQS;
+                const uint8_t* stg = qst + sq * QSB;
+                if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / NQS) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint2 v[KPS];
+#pragma unroll
+                for (int c = 0; c < KPS; ++c)
+                    v[c] = *reinterpret_cast<const uint2*>(stg + srow * NV_CB + 32 * c + 8 * qq);
+                const uint4 scw = *reinterpret_cast<const uint4*>(stg + 128 * NV_CB + srow * NV_SB);
+                const uint32_t sc4[4] = {scw.x, scw.y, scw.z, scw.w};   // byte 4 c + qq: word c, byte qq
+#pragma unroll
+                for (int c = 0; c < KPS; ++c, ++gk) {
+                    const int sa = gk % GU_NA, pr = (gk >> 1) & 1;
+                    const float sc = e4m3_float(sc4[c] >> (8 * qq)) * gsc;
+                    if (!mbar_wait(&bars->aempty[pr], ((uint32_t)(gk / GU_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    nv_quarter(v[c], sc, ast + sa * A_STAGE + rowb, o0, o1);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[pr]);
+                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&bars->qempty[sq]);
             }
         }
     } else if (QF == 1 && warp < NDQ) {
@@ -589,7 +680,7 @@ struct DnParams {
     const uint8_t* down;
     float* y;             // [P][H] fp32, rows in pair-list order
     int H, F, down_t;
-    const float* dscale;  // FP8 experts (QF 1): [E][H/128][F/128] block scales
+    const float* dscale;  // FP8 (QF 1): [E][H/128][F/128] block scales; NVFP4 (QF 2): globals [E]
 };
 
 // Persistent down GEMM: one CTA per SM walks the items (token tile of DN_NMAX
@@ -604,7 +695,8 @@ struct DnParams {
 template <int QF>
 __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_down(const __grid_constant__ CUtensorMap tm_a64, const __grid_constant__ CUtensorMap tm_a128,
-                 const __grid_constant__ CUtensorMap tm_w, const DnParams p) {
+                 const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
+                 const DnParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
@@ -616,7 +708,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     // buffers; FP8 (QF 1): a ring of F8_NQ raw stages of one 128-column scale
     // block each, loaded by TMA (tm_w: [E*H][F] bytes, box 128 x 128)
     const uint32_t qbytes = QF ? 0u : (uint32_t)(TILE_M * RB);
-    const uint32_t RQ = QF ? (uint32_t)(F8_NQ * QSTAGE_F8) / 2u : (qbytes + 1023u) & ~1023u;
+    const uint32_t RQ = QF ? (uint32_t)dn_qring<QF>() / 2u : (qbytes + 1023u) & ~1023u;
+    constexpr int DQS = QF == 2 ? QSTAGE_NV : QSTAGE_F8;   // raw stage bytes (QF 1, 2)
+    constexpr int DCOLS = QF == 2 ? NV_COLS : F8_COLS;    // columns per raw stage
 
     uint8_t* qbuf = sm;                                   // 2 x RQ raw bytes
     uint8_t* ast = sm + 2 * RQ;                           // DN_NA x A_STAGE
@@ -680,21 +774,27 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         n = min(DN_NMAX, p.used_first[lo + 1] - first - n0);
     };
 
-    if (QF == 1 && warp == W_QLOAD) {
+    if (QF != 0 && warp == W_QLOAD) {
         if (lane == 0) {
             int gs = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 int e, first, n0, n, h0;
                 item(it, e, first, n0, n, h0);
-                for (int sb = 0; sb < F / F8_COLS; ++sb, ++gs) {
+                for (int sb = 0; sb < F / DCOLS; ++sb, ++gs) {
                     const int st = gs % F8_NQ;
                     if (!mbar_wait(&bars->qempty[st], ((uint32_t)(gs / F8_NQ) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&bars->qfull[st], QSTAGE_F8);
-                    tma_load_2d(qbuf + st * QSTAGE_F8, &tm_w, sb * F8_COLS, e * H + h0, &bars->qfull[st]);
+                    uint8_t* dst = qbuf + st * DQS;
+                    mbar_arrive_expect_tx(&bars->qfull[st], DQS);
+                    if (QF == 1) {
+                        tma_load_2d(dst, &tm_w, sb * F8_COLS, e * H + h0, &bars->qfull[st]);
+                    } else {
+                        tma_load_2d(dst, &tm_w, sb * NV_CB, e * H + h0, &bars->qfull[st]);
+                        tma_load_2d(dst + TILE_M * NV_CB, &tm_ws, sb * NV_SB, e * H + h0, &bars->qfull[st]);
+                    }
                 }
             }
         }
@@ -757,6 +857,49 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                     umma_commit(&bars->aempty[sa]);
                 }
                 if (ok) umma_commit(&bars->accfull[buf]);
+            }
+        }
+    } else if (QF == 2 && warp < NDQ) {
+        // NVFP4: thread -> A row 8*warp + (lane & 7), 16-k quarter qq = lane >> 3
+        // (8 code bytes and one scale byte of each k-block)
+        const int qq = lane >> 3, sw = lane & 7;
+        const int row = 8 * warp + (lane & 7);
+        const int o0 = ((2 * qq) ^ sw) << 4, o1 = ((2 * qq + 1) ^ sw) << 4;
+        const int my_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        int gk = 0, gs = 0;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            int e, first, n0, n, h0;
+            item(blockIdx.x + j * gridDim.x, e, first, n0, n, h0);
+            const float gsc = __ldg(p.dscale + e);
+            for (int sb = 0; sb < F / NV_COLS; ++sb, ++gs) {
+                const int sq = gs % F8_NQ;
+                const uint8_t* stg = qbuf + sq * QSTAGE_NV;
+                if (!mbar_wait(&bars->qfull[sq], (uint32_t)(gs / F8_NQ) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint2 v[NV_COLS / KBLK];
+#pragma unroll
+                for (int c = 0; c < NV_COLS / KBLK; ++c)
+                    v[c] = *reinterpret_cast<const uint2*>(stg + row * NV_CB + 32 * c + 8 * qq);
+                const uint4 scw = *reinterpret_cast<const uint4*>(stg + TILE_M * NV_CB + row * NV_SB);
+                const uint32_t sc4[4] = {scw.x, scw.y, scw.z, scw.w};
+#pragma unroll
+                for (int c = 0; c < NV_COLS / KBLK; ++c, ++gk) {
+                    const int sa = gk % DN_NA;
+                    const float sc = e4m3_float(sc4[c] >> (8 * qq)) * gsc;
+                    if (!mbar_wait(&bars->aempty[sa], ((uint32_t)(gk / DN_NA) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    nv_quarter(v[c], sc, ast + sa * A_STAGE + row * 128, o0, o1);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[sa]);
+                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(&bars->qempty[sq]);
             }
         }
     } else if (QF == 1 && warp < NDQ) {
@@ -1022,7 +1165,9 @@ int sm_count() {
 
 size_t dn_smem(int F, int down_t, int E) {
     const size_t rb = (size_t)(F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    const size_t q = down_t == 3 ? (size_t)F8_NQ * QSTAGE_F8 / 2 : (TILE_M * rb + 1023) & ~size_t(1023);
+    const size_t q = down_t == 3   ? (size_t)dn_qring<1>() / 2
+                     : down_t == 4 ? (size_t)dn_qring<2>() / 2
+                                   : (TILE_M * rb + 1023) & ~size_t(1023);
     return 1024 + 2 * q + DN_NA * A_STAGE + DN_NA * DN_BSTAGE + sizeof(PfBars) + sizeof(int) * (E + 1) + 64;
 }
 
@@ -1038,7 +1183,11 @@ cudaError_t prefill_attrs() {
         if (r == cudaSuccess)
             r = cudaFuncSetAttribute(prefill_down<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_gateup<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
             r = cudaFuncSetAttribute(prefill_down<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_down<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         return r;
     }();
     return e;
@@ -1079,11 +1228,11 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
                 {0, 0, 0}, {0, 0, 0}, 1, 0, nullptr, nullptr};
-    prefill_gateup<0, 0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
+    prefill_gateup<0, 0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tg, tg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t, nullptr};
-    prefill_down<0><<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, ta64, dp);
+    prefill_down<0><<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, ta64, ta64, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
@@ -1115,11 +1264,51 @@ cudaError_t launch_prefill_fp8(const MoeShape& s, const float* x, const float* r
     if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
                 {0, 0, 0}, {0, 0, 0}, 1, 0, w.gate_scale, w.up_scale};
-    prefill_gateup<0, 1><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, gp);
+    prefill_gateup<0, 1><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tg, tg, gp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, w.down, y, s.H, s.F, 3, w.down_scale};
-    prefill_down<1><<<sm_count(), GU_THREADS, dn_smem(s.F, 3, s.E), st>>>(ta64, ta128, td, dp);
+    prefill_down<1><<<sm_count(), GU_THREADS, dn_smem(s.F, 3, s.E), st>>>(ta64, ta128, td, td, dp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g3((s.H / 4 + 255) / 256, s.T);
+    combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
+    return cudaGetLastError();
+}
+
+bool prefill_nvfp4_supported(const MoeShape& s) {
+    if (s.H % NV_COLS || s.F % NV_COLS || s.H % TILE_M || s.F % 64) return false;
+    return dn_smem(s.F, 4, s.E) <= 227 * 1024 && GU_SMEM <= 227 * 1024 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_nvfp4(const MoeShape& s, const float* x, const float* res, const NvExperts& w,
+                                 const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
+                                 float* out, cudaStream_t st) {
+    const int P = s.T * s.K;
+    gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tg, tu, tgs, tus, td, tds, tx64, tx128, txg, ta64, ta128;
+    const uint64_t gu_rows = (uint64_t)s.E * s.F, dn_rows = (uint64_t)s.E * s.H;
+    if (!map_bytes(&tg, w.gate, (uint64_t)s.H / 2, gu_rows, NV_CB, 64) ||
+        !map_bytes(&tu, w.up, (uint64_t)s.H / 2, gu_rows, NV_CB, 64) ||
+        !map_bytes(&tgs, w.gate_bs, (uint64_t)s.H / 16, gu_rows, NV_SB, 64) ||
+        !map_bytes(&tus, w.up_bs, (uint64_t)s.H / 16, gu_rows, NV_SB, 64) ||
+        !map_bytes(&td, w.down, (uint64_t)s.F / 2, dn_rows, NV_CB, TILE_M) ||
+        !map_bytes(&tds, w.down_bs, (uint64_t)s.F / 16, dn_rows, NV_SB, TILE_M) ||
+        !map_half(&tx64, xp, s.H, P, 64) || !map_half(&tx128, xp, s.H, P, 128) ||
+        !map_half(&txg, xp, s.H, P, GU_NMAX) || !map_half(&ta64, actp, s.F, P, 64) ||
+        !map_half(&ta128, actp, s.F, P, 128))
+        return cudaErrorInvalidValue;
+    e = prefill_attrs();
+    if (e != cudaSuccess) return e;
+    GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
+                {0, 0, 0}, {0, 0, 0}, 1, 0, w.gate_gs, w.up_gs};
+    prefill_gateup<0, 2><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tgs, tus, gp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    DnParams dp{r.n_used, r.used_expert, r.used_first, w.down, y, s.H, s.F, 4, w.down_gs};
+    prefill_down<2><<<sm_count(), GU_THREADS, dn_smem(s.F, 4, s.E), st>>>(ta64, ta128, td, tds, dp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
@@ -1153,7 +1342,7 @@ cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, co
                 ksplit, part_stride, nullptr, nullptr};
     const int items = (rows / TILE_M) * ksplit * ((T + GU_NMAX - 1) / GU_NMAX);
     prefill_gateup<1, 0><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(
-        tw[0], tw[1], tw[2], tx64, tx128, txg, gp);
+        tw[0], tw[1], tw[2], tx64, tx128, txg, tw[0], tw[0], gp);
     return cudaGetLastError();
 }
 

@@ -561,6 +561,9 @@ qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float*
         return fail(c, QMOE_ERR_MISALIGNED, "global-scale pointers must be 4-byte aligned");
     qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
     const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route);
+    // the tensor-core path copies the block scales by TMA (16-byte aligned rows)
+    const bool tc = many && qmoe::prefill_nvfp4_supported(ms) && aligned16(gate_bscale) &&
+                    aligned16(up_bscale) && aligned16(down_bscale);
     cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
                          : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
@@ -569,10 +572,16 @@ qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float*
                             static_cast<const uint8_t*>(up_bscale), up_global,
                             static_cast<const uint8_t*>(down_exps), static_cast<const uint8_t*>(down_bscale),
                             down_global};
-    e = qmoe::launch_nvfp4_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 expert launch");
-    e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
-    if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    if (tc) {
+        e = qmoe::launch_prefill_nvfp4(ms, hidden_in, hidden_in, w, c->route, c->xp, c->actp, c->y,
+                                       c->inv_pos, hidden_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 tensor-core expert launch");
+    } else {
+        e = qmoe::launch_nvfp4_experts(ms, hidden_in, w, c->route, c->act, c->y, c->num_sms, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 expert launch");
+        e = qmoe::launch_combine(ms, c->y, c->route, hidden_in, hidden_out, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    }
     if (ids_out || weights_out) {
         e = qmoe::copy_route_out(ms, c->route, ids_out, weights_out, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "routing copy");

@@ -116,6 +116,12 @@ cudaError_t launch_nvfp4_experts(const MoeShape& s, const float* x, const NvExpe
 cudaError_t launch_nvfp4_quantize(const uint16_t* x, int n_mats, int rows, int cols, uint8_t* codes,
                                   uint8_t* bscale, float* global, unsigned* amax_bits, int num_sms,
                                   cudaStream_t st);
+// many tokens over NVFP4 experts: as launch_prefill_fp8 (E2M1 widened and
+// scaled by block and global scale to fp16 in shared memory)
+bool prefill_nvfp4_supported(const MoeShape& s);
+cudaError_t launch_prefill_nvfp4(const MoeShape& s, const float* x, const float* res, const NvExperts& w,
+                                 const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
+                                 float* out, cudaStream_t st);
 // many tokens (after launch_route_many): gather x as fp16, grouped gate/up and
 // down GEMMs on the tensor cores with the FP8 weights widened to fp16 in shared
 // memory, combine into out (prefill_umma.cu)

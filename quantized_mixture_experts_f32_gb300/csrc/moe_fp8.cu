@@ -20,7 +20,7 @@
 // weights while the gate/up kernel still runs.
 #include <math.h>
 
-#include "lowbit.cuh"
+#include "lowbit_items.cuh"
 #include "pdl.cuh"
 #include "qmoe_internal.h"
 
@@ -30,31 +30,11 @@ namespace {
 
 constexpr int F8_THREADS = 256;
 
-// dot of 16 E4M3 weights (one 16-byte chunk) with 16 consecutive fp32 values
-__device__ __forceinline__ float chunk_dot(uint4 w, const float* __restrict__ v) {
-    const float4* v4 = reinterpret_cast<const float4*>(v);
-    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 x = __ldg(v4 + i);
-        const float2 lo = e4m3x2_f2(q[i] & 0xffffu), hi = e4m3x2_f2(q[i] >> 16);
-        a0 = fmaf(lo.x, x.x, a0);
-        a1 = fmaf(lo.y, x.y, a1);
-        a0 = fmaf(hi.x, x.z, a0);
-        a1 = fmaf(hi.y, x.w, a1);
-    }
-    return a0 + a1;
-}
-
 // Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
-// and f0 + 1 (half-warp hw takes row f0 + hw of both gate and up).  Lane chunk k
-// of a row covers columns 16 ((lane & 15) + 16 k) .. +15, k < NC = H / 256.
-// act[p][f] = silu(g) * u for every pair p routed to the expert.
+// and f0 + 1 (half-warp hw takes row f0 + hw of both gate and up); NC = H / 256.
 template <int NC>
 __global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
-    const float* __restrict__ x, int H, int F, int K, const uint8_t* __restrict__ gate,
-    const float* __restrict__ gs, const uint8_t* __restrict__ up, const float* __restrict__ us,
+    const float* __restrict__ x, int H, int F, int K, const Fp8Experts w,
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ act) {
@@ -63,112 +43,45 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
-    const int per = F >> 1, nbh = H >> 7;
+    const int per = F >> 1;
     const int items = *n_used * per;
     for (int i = gw; i < items; i += nw) {
-        const int u = i / per, f = 2 * (i - u * per) + hw;
-        const int e = used_expert[u];
-        const size_t row = (size_t)e * F + f;
-        const uint8_t* gr = gate + row * H + 16 * hl;
-        const uint8_t* ur = up + row * H + 16 * hl;
-        const size_t sb = ((size_t)e * (F >> 7) + (f >> 7)) * nbh;
-        uint4 wg[NC], wu[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            wg[k] = ld_stream(gr + 256 * k);
-            wu[k] = ld_stream(ur + 256 * k);
-        }
-        float sg[NC], su[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            sg[k] = __ldg(gs + sb + 2 * k + (hl >> 3));
-            su[k] = __ldg(us + sb + 2 * k + (hl >> 3));
-        }
-        const int p0 = used_first[u], p1 = used_first[u + 1];
-        for (int q = p0; q < p1; ++q) {
-            const int p = pair_list[q];
-            const float* xt = x + (size_t)(p / K) * H + 16 * hl;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                opaque(wg[k]);
-                opaque(wu[k]);
-            }
-            float g = 0.f, v = 0.f;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                g = fmaf(sg[k], chunk_dot(wg[k], xt + 256 * k), g);
-                v = fmaf(su[k], chunk_dot(wu[k], xt + 256 * k), v);
-            }
-            g = group_sum<16>(g);
-            v = group_sum<16>(v);
-            if (hl == 0) act[(size_t)p * F + f] = g / (1.f + expf(-g)) * v;
-        }
+        const int u = i / per;
+        lowbit::f8_gateup_rows<NC>(x, H, F, K, w, used_expert[u], 2 * (i - u * per) + hw, hl,
+                                   pair_list, used_first[u], used_first[u + 1], act);
     }
 }
 
 // Down projection.  Item i -> used expert u = i / (H/4), rows h0 = 4 (i % (H/4)) ..
-// h0 + 3; half-warp hw takes rows h0 + hw and h0 + 2 + hw.  Lane chunk k of a row
-// covers columns 16 ((lane & 15) + 16 k) .. +15, k < NC = F / 256.
-// y[p][h] = (Wd_e act_p)[h] for every pair p routed to the expert.
+// h0 + 3; half-warp hw takes rows h0 + hw and h0 + 2 + hw; NC = F / 256.
 template <int NC>
 __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
-    const float* __restrict__ act, int H, int F, const uint8_t* __restrict__ down,
-    const float* __restrict__ ds, const int32_t* __restrict__ n_used,
-    const int32_t* __restrict__ used_expert, const int32_t* __restrict__ used_first,
-    const int32_t* __restrict__ pair_list, float* __restrict__ y) {
+    const float* __restrict__ act, int H, int F, const Fp8Experts w,
+    const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
+    const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
+    float* __restrict__ y) {
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
-    const int per = H >> 2, nbf = F >> 7;
+    const int per = H >> 2;
     // The routing was written two kernels back: the gate/up kernel lets this one
     // launch only after its own wait on the routing kernel, so the lists are
     // complete here and are read through L2.  The first item's weights are
     // loaded before the wait on the gate/up kernel (they are never written).
     const int items = __ldcg(n_used) * per;
-    uint4 w0[NC], w1[NC];
-    auto load = [&](int i) {
-        const int u = i / per, h = 4 * (i - u * per) + hw;
-        const uint8_t* r0 = down + ((size_t)__ldcg(used_expert + u) * H + h) * F + 16 * hl;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            w0[k] = ld_stream(r0 + 256 * k);
-            w1[k] = ld_stream(r0 + 2 * (size_t)F + 256 * k);
-        }
-    };
-    if (gw < items) load(gw);
+    lowbit::F8Down<NC> d;
+    if (gw < items) {
+        const int u = gw / per;
+        lowbit::f8_down_load<NC>(d, w, __ldcg(used_expert + u), 4 * (gw - u * per) + hw, H, F, hl);
+    }
     pdl_wait();                 // act of this call
     pdl_launch_dependents();
     for (int i = gw; i < items; i += nw) {
-        if (i != gw) load(i);
         const int u = i / per, h = 4 * (i - u * per) + hw;
-        const int e = __ldcg(used_expert + u);
-        // rows h and h + 2 lie in one 128-row block (h0 is a multiple of 4)
-        const size_t sb = ((size_t)e * (H >> 7) + (h >> 7)) * nbf;
-        float s[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) s[k] = __ldg(ds + sb + 2 * k + (hl >> 3));
-        const int p0 = __ldcg(used_first + u), p1 = __ldcg(used_first + u + 1);
-        for (int q = p0; q < p1; ++q) {
-            const int p = __ldcg(pair_list + q);
-            const float* ap = act + (size_t)p * F + 16 * hl;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                opaque(w0[k]);
-                opaque(w1[k]);
-            }
-            float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                a = fmaf(s[k], chunk_dot(w0[k], ap + 256 * k), a);
-                b = fmaf(s[k], chunk_dot(w1[k], ap + 256 * k), b);
-            }
-            a = group_sum<16>(a);
-            b = group_sum<16>(b);
-            if (hl == 0) {
-                y[(size_t)p * H + h] = a;
-                y[(size_t)p * H + h + 2] = b;
-            }
-        }
+        const int e = used_expert[u];
+        if (i != gw) lowbit::f8_down_load<NC>(d, w, e, h, H, F, hl);
+        lowbit::f8_down_rows<NC, false>(d, w, e, h, H, F, hl, pair_list, used_first[u],
+                                        used_first[u + 1], act, y);
     }
 }
 
@@ -177,9 +90,8 @@ cudaError_t gateup_nc(const MoeShape& s, const float* x, const Fp8Experts& w, co
                       float* act, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
     const int grid = strided_grid(fp8_gateup_kernel<NC>, F8_THREADS, &resident, items, num_sms);
-    return launch_pdl(fp8_gateup_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.H, s.F, s.K,
-                      w.gate, w.gate_scale, w.up, w.up_scale, r.n_used, r.used_expert,
-                      r.used_first, r.pair_list, act);
+    return launch_pdl(fp8_gateup_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.H, s.F, s.K, w,
+                      r.n_used, r.used_expert, r.used_first, r.pair_list, act);
 }
 
 template <int NC>
@@ -187,8 +99,8 @@ cudaError_t down_nc(const MoeShape& s, const float* act, const Fp8Experts& w, co
                     float* y, int items, int num_sms, cudaStream_t st) {
     static int resident = 0;   // per instantiation
     const int grid = strided_grid(fp8_down_kernel<NC>, F8_THREADS, &resident, items, num_sms);
-    return launch_pdl(fp8_down_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, act, s.H, s.F,
-                      w.down, w.down_scale, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
+    return launch_pdl(fp8_down_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, act, s.H, s.F, w,
+                      r.n_used, r.used_expert, r.used_first, r.pair_list, y);
 }
 
 }  // namespace

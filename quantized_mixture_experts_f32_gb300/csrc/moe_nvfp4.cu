@@ -20,7 +20,7 @@
 // scaled by their block scales; the matrix's global scale multiplies the row sum.
 #include <math.h>
 
-#include "lowbit.cuh"
+#include "lowbit_items.cuh"
 #include "pdl.cuh"
 #include "qmoe_internal.h"
 
@@ -107,75 +107,8 @@ __global__ void nvfp4_global(const unsigned* __restrict__ amax_bits, int n_mats,
 
 // --------------------------------------------------------------------------- expert GEMVs
 
-// sum of 32 weights (one 16-byte chunk; bytes 0..7 = elements 0..15 with block
-// scale sa, bytes 8..15 = elements 16..31 with scale sb) times 32 fp32 values
-__device__ __forceinline__ float nv_chunk(uint4 w, const float* __restrict__ v, float sa, float sb) {
-    const float4* v4 = reinterpret_cast<const float4*>(v);
-    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-    float h[2];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const uint32_t word = q[2 * half + i];
-#pragma unroll
-            for (int by = 0; by < 4; by += 2) {
-                const float4 x = __ldg(v4 + 4 * half + 2 * i + by / 2);
-                const float2 p0 = e2m1x2_f2(word >> (8 * by)), p1 = e2m1x2_f2(word >> (8 * by + 8));
-                a0 = fmaf(p0.x, x.x, a0);
-                a1 = fmaf(p0.y, x.y, a1);
-                a0 = fmaf(p1.x, x.z, a0);
-                a1 = fmaf(p1.y, x.w, a1);
-            }
-        }
-        h[half] = a0 + a1;
-    }
-    return fmaf(sa, h[0], sb * h[1]);
-}
-
-// the same for two weight chunks (gate and up) against the same 32 values,
-// each value loaded once
-__device__ __forceinline__ void nv_chunk2(uint4 wa, uint4 wb, const float* __restrict__ v, float2 sa,
-                                          float2 sb, float& ra, float& rb) {
-    const float4* v4 = reinterpret_cast<const float4*>(v);
-    const uint32_t qa[4] = {wa.x, wa.y, wa.z, wa.w}, qb[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        float a = 0.f, b = 0.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-#pragma unroll
-            for (int by = 0; by < 4; by += 2) {
-                const float4 x = __ldg(v4 + 4 * half + 2 * i + by / 2);
-                const uint32_t wa_ = qa[2 * half + i] >> (8 * by), wb_ = qb[2 * half + i] >> (8 * by);
-                const float2 a0 = e2m1x2_f2(wa_), a1 = e2m1x2_f2(wa_ >> 8);
-                const float2 b0 = e2m1x2_f2(wb_), b1 = e2m1x2_f2(wb_ >> 8);
-                a = fmaf(a0.x, x.x, a);
-                b = fmaf(b0.x, x.x, b);
-                a = fmaf(a0.y, x.y, a);
-                b = fmaf(b0.y, x.y, b);
-                a = fmaf(a1.x, x.z, a);
-                b = fmaf(b1.x, x.z, b);
-                a = fmaf(a1.y, x.w, a);
-                b = fmaf(b1.y, x.w, b);
-            }
-        }
-        ra = fmaf(half ? sa.y : sa.x, a, ra);
-        rb = fmaf(half ? sb.y : sb.x, b, rb);
-    }
-}
-
-// the two E4M3 block scales of chunk k of a lane: bytes 2 (ql + 8 k) and +1
-__device__ __forceinline__ float2 nv_scales(const uint8_t* __restrict__ row_bs, int idx) {
-    const uint32_t two = __ldg(reinterpret_cast<const unsigned short*>(row_bs + idx));
-    return e4m3x2_f2(two);
-}
-
 // Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
-// and f0 + 1 (half-warp hw takes row f0 + hw of gate and up).  Lane chunk k of
-// a row: bytes 16 ((lane & 15) + 16 k) .. +15, columns 32 ((lane & 15) + 16 k)
-// .. +31, k < NC = H / 512.
+// and f0 + 1 (half-warp hw takes row f0 + hw of gate and up); NC = H / 512.
 template <int NC>
 __global__ void __launch_bounds__(NV_THREADS) nvfp4_gateup_kernel(
     const float* __restrict__ x, int H, int F, int K, const NvExperts w,
@@ -190,47 +123,14 @@ __global__ void __launch_bounds__(NV_THREADS) nvfp4_gateup_kernel(
     const int per = F >> 1;
     const int items = *n_used * per;
     for (int i = gw; i < items; i += nw) {
-        const int u = i / per, f = 2 * (i - u * per) + hw;
-        const int e = used_expert[u];
-        const size_t row = (size_t)e * F + f;
-        const uint8_t* gr = w.gate + row * (H / 2) + 16 * hl;
-        const uint8_t* ur = w.up + row * (H / 2) + 16 * hl;
-        uint4 wg[NC], wu[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            wg[k] = ld_stream(gr + 256 * k);
-            wu[k] = ld_stream(ur + 256 * k);
-        }
-        const uint8_t* gbs = w.gate_bs + row * (H / 16);
-        const uint8_t* ubs = w.up_bs + row * (H / 16);
-        float2 sg[NC], su[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            sg[k] = nv_scales(gbs, 2 * (hl + 16 * k));
-            su[k] = nv_scales(ubs, 2 * (hl + 16 * k));
-        }
-        const float gg = __ldg(w.gate_gs + e), ug = __ldg(w.up_gs + e);
-        const int p0 = used_first[u], p1 = used_first[u + 1];
-        for (int pq = p0; pq < p1; ++pq) {
-            const int p = pair_list[pq];
-            const float* xt = x + (size_t)(p / K) * H + 32 * hl;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                opaque(wg[k]);
-                opaque(wu[k]);
-            }
-            float g = 0.f, v = 0.f;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) nv_chunk2(wg[k], wu[k], xt + 512 * k, sg[k], su[k], g, v);
-            g = group_sum<16>(g) * gg;
-            v = group_sum<16>(v) * ug;
-            if (hl == 0) act[(size_t)p * F + f] = g / (1.f + expf(-g)) * v;
-        }
+        const int u = i / per;
+        lowbit::nv_gateup_rows<NC>(x, H, F, K, w, used_expert[u], 2 * (i - u * per) + hw, hl,
+                                   pair_list, used_first[u], used_first[u + 1], act);
     }
 }
 
 // Down projection.  Item i -> used expert u = i / (H/4), rows h0 = 4 (i % (H/4))
-// .. h0 + 3 (quarter-warp q takes row h0 + q); chunk k < NC = F / 256 as above.
+// .. h0 + 3 (quarter-warp q takes row h0 + q); NC = F / 256.
 template <int NC>
 __global__ void __launch_bounds__(NV_THREADS) nvfp4_down_kernel(
     const float* __restrict__ act, int H, int F, const NvExperts w,
@@ -244,37 +144,19 @@ __global__ void __launch_bounds__(NV_THREADS) nvfp4_down_kernel(
     // the routing is complete here (see the FP8 down kernel); the first item's
     // weights are loaded before the wait on the gate/up kernel
     const int items = __ldcg(n_used) * per;
-    uint4 wd[NC];
-    auto load = [&](int i) {
-        const int u = i / per, h = 4 * (i - u * per) + q;
-        const uint8_t* r = w.down + ((size_t)__ldcg(used_expert + u) * H + h) * (F / 2) + 16 * ql;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) wd[k] = ld_stream(r + 128 * k);
-    };
-    if (gw < items) load(gw);
+    lowbit::NvDown<NC> d;
+    if (gw < items) {
+        const int u = gw / per;
+        lowbit::nv_down_load<NC>(d, w, __ldcg(used_expert + u), 4 * (gw - u * per) + q, H, F, ql);
+    }
     pdl_wait();
     pdl_launch_dependents();
     for (int i = gw; i < items; i += nw) {
-        if (i != gw) load(i);
         const int u = i / per, h = 4 * (i - u * per) + q;
-        const int e = __ldcg(used_expert + u);
-        const uint8_t* dbs = w.down_bs + ((size_t)e * H + h) * (F / 16);
-        float2 s[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) s[k] = nv_scales(dbs, 2 * (ql + 8 * k));
-        const float dg = __ldg(w.down_gs + e);
-        const int p0 = __ldcg(used_first + u), p1 = __ldcg(used_first + u + 1);
-        for (int pq = p0; pq < p1; ++pq) {
-            const int p = __ldcg(pair_list + pq);
-            const float* ap = act + (size_t)p * F + 32 * ql;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) opaque(wd[k]);
-            float a = 0.f;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) a += nv_chunk(wd[k], ap + 256 * k, s[k].x, s[k].y);
-            a = group_sum<8>(a) * dg;
-            if (ql == 0) y[(size_t)p * H + h] = a;
-        }
+        const int e = used_expert[u];
+        if (i != gw) lowbit::nv_down_load<NC>(d, w, e, h, H, F, ql);
+        lowbit::nv_down_rows<NC, false>(d, w, e, h, H, F, ql, pair_list, used_first[u],
+                                        used_first[u + 1], act, y);
     }
 }
 

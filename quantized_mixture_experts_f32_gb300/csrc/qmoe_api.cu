@@ -560,6 +560,11 @@ qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float*
          reinterpret_cast<uintptr_t>(down_global)) & 3u)
         return fail(c, QMOE_ERR_MISALIGNED, "global-scale pointers must be 4-byte aligned");
     qmoe::MoeShape ms{n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, k.norm_topk_prob ? 1 : 0};
+    const qmoe::NvExperts w{static_cast<const uint8_t*>(gate_exps), static_cast<const uint8_t*>(gate_bscale),
+                            gate_global, static_cast<const uint8_t*>(up_exps),
+                            static_cast<const uint8_t*>(up_bscale), up_global,
+                            static_cast<const uint8_t*>(down_exps), static_cast<const uint8_t*>(down_bscale),
+                            down_global};
     const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route);
     // the tensor-core path copies the block scales by TMA (16-byte aligned rows)
     const bool tc = many && qmoe::prefill_nvfp4_supported(ms) && aligned16(gate_bscale) &&
@@ -567,11 +572,6 @@ qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float*
     cudaError_t e = many ? qmoe::launch_route_many(ms, hidden_in, router_w, nullptr, c->route, c->stream)
                          : qmoe::launch_route(ms, hidden_in, router_w, nullptr, c->route, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "route launch");
-    const qmoe::NvExperts w{static_cast<const uint8_t*>(gate_exps), static_cast<const uint8_t*>(gate_bscale),
-                            gate_global, static_cast<const uint8_t*>(up_exps),
-                            static_cast<const uint8_t*>(up_bscale), up_global,
-                            static_cast<const uint8_t*>(down_exps), static_cast<const uint8_t*>(down_bscale),
-                            down_global};
     if (tc) {
         e = qmoe::launch_prefill_nvfp4(ms, hidden_in, hidden_in, w, c->route, c->xp, c->actp, c->y,
                                        c->inv_pos, hidden_out, c->stream);

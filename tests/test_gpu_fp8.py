@@ -73,7 +73,8 @@ def _check(inp, got, ids, w, exact_ids):
 GEMV_MAX = 32   # calls with more tokens run on the tensor cores (fp16 operands)
 
 # (config, T, overrides): the tiny case spans several items per warp and a
-# ragged token count; decode is the Qwen3-30B-A3B layer at T=1 and T=8; T=32
+# ragged token count; decode is the Qwen3-30B-A3B layer at T=1 and T=8 (the
+# one-launch kernel) and T=16 (the multi-kernel GEMVs at that shape); T=32
 # is the largest call on the CUDA-core GEMVs (two-launch routing), T=33 and
 # T=40 the smallest on the tensor cores (token tiles shorter than 16 rows); the
 # H=1024 / F=512 cases other unrolls and tile counts; T=512 the Qwen3-30B-A3B
@@ -88,6 +89,7 @@ CASES = [
     ("tiny_fp8", 200, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 12}),
     ("decode_fp8", None, {}),
     ("decode_fp8", 8, {}),
+    ("decode_fp8", 16, {}),
     ("decode_fp8", 512, {}),
 ]
 

@@ -77,7 +77,8 @@ GEMV_MAX = 32   # calls with more tokens run on the tensor cores (fp16 operands)
 
 # tiny: several items per warp, ragged T; T=32 the largest GEMV call, T=33 and
 # T=40 the smallest on the tensor cores; H=1024 / F=512 other unrolls and tile
-# counts; decode: the Qwen3-30B-A3B layer at T=1 and 8; T=512 its prefill shape
+# counts; decode: the Qwen3-30B-A3B layer at T=1 and 8 (the one-launch kernel),
+# T=16 (the multi-kernel GEMVs at that shape); T=512 its prefill shape
 CASES = [
     ("tiny_nvfp4", None, {}),
     ("tiny_nvfp4", 1, {}),
@@ -88,6 +89,7 @@ CASES = [
     ("tiny_nvfp4", 200, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 22}),
     ("decode_nvfp4", None, {}),
     ("decode_nvfp4", 8, {}),
+    ("decode_nvfp4", 16, {}),
     ("decode_nvfp4", 512, {}),
 ]
 

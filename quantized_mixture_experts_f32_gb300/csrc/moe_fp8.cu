@@ -15,7 +15,7 @@
 // Work is expert-centric and grid-strided: a warp item is two rows (one per
 // half-warp) of gate and up, or four rows of down, of one used expert; the
 // lane's chunks of every row of the item are loaded before any is used, so a
-// warp keeps 12 to 16 16-byte loads in flight.  Both kernels are programmatic
+// lane keeps 16 (gate/up) or 6 (down) 16-byte loads in flight.  Both kernels are programmatic
 // dependents of the kernel before them; the down kernel loads its first item's
 // weights while the gate/up kernel still runs.
 #include <math.h>

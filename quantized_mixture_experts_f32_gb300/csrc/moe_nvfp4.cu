@@ -16,8 +16,9 @@
 // Expert GEMVs: as the FP8 ones (moe_fp8.cu); a 16-byte chunk is 32 weights, so
 // a gate/up row of H = 2048 (1 KB) is 4 chunks per lane of a half-warp (items:
 // two rows of gate and up) and a down row of F = 768 (384 B) 3 chunks per lane
-// of a quarter-warp (items: four rows).  Each chunk's two 16-element halves are summed apart and
-// scaled by their block scales; the matrix's global scale multiplies the row sum.
+// of a quarter-warp (items: four rows).  Each chunk's two 16-element halves are
+// summed apart and scaled by their block scales; the matrix's global scale
+// multiplies the row sum.
 #include <math.h>
 
 #include "lowbit_items.cuh"

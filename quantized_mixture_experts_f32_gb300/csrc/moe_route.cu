@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(RG_THREADS) router_gemm(const float* __restric
                                                           int H, int E,
                                                           float* __restrict__ part,
                                                           uint32_t* __restrict__ clear, int nclear) {
+    pdl_wait();
     extern __shared__ float4 rg_smem4[];
     float* xs = reinterpret_cast<float*>(rg_smem4);              // [RG_T][RG_LD]
     float* ws = xs + RG_T * RG_LD;                               // [RG_E][RG_LD]
@@ -230,6 +231,7 @@ __global__ void __launch_bounds__(256) topk_rank(const float* __restrict__ part,
                                                  uint32_t* __restrict__ tokmap,
                                                  int32_t* __restrict__ counts,
                                                  uint8_t* __restrict__ jmap) {
+    pdl_wait();
     extern __shared__ float lsm[];                 // 8 warps x (E logits + 16 selection slots)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(EL_THREADS) expert_lists(const uint8_t* __rest
                                                            int32_t* __restrict__ used_expert,
                                                            int32_t* __restrict__ used_first,
                                                            int32_t* __restrict__ pair_list) {
+    pdl_wait();
     extern __shared__ uint32_t el_sm[];             // W words, then W running popcounts
     __shared__ int red[2][EL_THREADS / 32];
     __shared__ int scan[EL_THREADS / 32];
@@ -450,15 +453,16 @@ cudaError_t launch_route_many(const MoeShape& s, const float* x, const float* ro
     dim3 g1((s.E + RG_E - 1) / RG_E, (s.T + RG_T - 1) / RG_T, S);
     const int W = (s.T + 31) / 32;
     uint32_t* counts = r.tokmap + (size_t)s.E * W;      // E counters after the bitmap
-    router_gemm<<<g1, RG_THREADS, rg_smem, st>>>(x, router_w, s.T, s.H, s.E, r.logits_part, r.tokmap,
-                                                 s.E * W + s.E);
-    topk_rank<<<(s.T + 7) / 8, 256, sizeof(float) * 8 * (s.E + 16), st>>>(
-        r.logits_part, S, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.tokmap,
-        reinterpret_cast<int32_t*>(counts), r.jmap);
-    expert_lists<<<s.E, EL_THREADS, sizeof(uint32_t) * 2 * W, st>>>(
-        r.jmap, r.tokmap, reinterpret_cast<const int32_t*>(counts), s.T, s.E, s.K, r.n_used, r.used_expert,
-        r.used_first, r.pair_list);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(router_gemm, g1, dim3(RG_THREADS), rg_smem, st, x, router_w, s.T, s.H,
+                               s.E, r.logits_part, r.tokmap, s.E * W + s.E);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_rank, dim3((s.T + 7) / 8), dim3(256), sizeof(float) * 8 * (s.E + 16), st,
+                   r.logits_part, S, bias, s.T, s.E, s.K, s.norm_topk, r.logits, r.ids, r.wts, r.tokmap,
+                   reinterpret_cast<int32_t*>(counts), r.jmap);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(expert_lists, dim3(s.E), dim3(EL_THREADS), sizeof(uint32_t) * 2 * W, st, r.jmap,
+                      r.tokmap, reinterpret_cast<const int32_t*>(counts), s.T, s.E, s.K, r.n_used,
+                      r.used_expert, r.used_first, r.pair_list);
 }
 
 // workspace for the partial sums of any call with up to T tokens (a call with

@@ -26,6 +26,7 @@
 #include <math.h>
 
 #include "kquant.cuh"
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 #include "umma.cuh"
 
@@ -55,6 +56,7 @@ template <int F16>
 __global__ void __launch_bounds__(NR_THREADS) rmsnorm_rows(const float* __restrict__ h,
                                                            const float* __restrict__ w, float eps,
                                                            int H, void* __restrict__ out) {
+    pdl_wait();
     __shared__ float red[NR_THREADS / 32];
     const float* row = h + (size_t)blockIdx.x * H;
     float ss = 0.f;
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(NR_THREADS) residual_rmsnorm_rows(float* __res
                                                                     const float* __restrict__ p1,
                                                                     const float* __restrict__ w, float eps,
                                                                     int H, float* __restrict__ out) {
+    pdl_wait();
     __shared__ float red[NR_THREADS / 32];
     const size_t base = (size_t)blockIdx.x * H;
     float ss = 0.f;
@@ -101,6 +104,7 @@ __device__ __forceinline__ float2 rope_cs(const double* __restrict__ inv_freq, i
 // cos/sin of every (token, pair) of the batch: cs[t][j] for position pos0 + t
 __global__ void rope_table_rows(const double* __restrict__ inv_freq, int half, int pos0, int T,
                                 float2* __restrict__ cs) {
+    pdl_wait();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= T * half) return;
     const int t = i / half, j = i - t * half;
@@ -116,6 +120,7 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append(
     const float* __restrict__ k_norm, float eps, const float2* __restrict__ rcs, int pos0,
     int max_ctx, float* __restrict__ qr, __half* __restrict__ qh, __half* __restrict__ k_cache,
     __half* __restrict__ v_cache, int T) {
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x, hh = blockIdx.y * 4 + warp;
     if (t >= T || hh >= nq + nkv) return;
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(PA_THREADS) prefill_attention(
     const float* __restrict__ qr, const __half* __restrict__ k_cache,
     const __half* __restrict__ v_cache, int nq, int nkv, int hd, int pos0, int max_ctx, int T,
     __half* __restrict__ att) {
+    pdl_wait();
     extern __shared__ __align__(16) float sm[];
     const int g = blockIdx.x, t0 = blockIdx.y * PA_QT;
     const int group = nq / nkv, nvec = PA_QT * group;         // query vectors of the block
@@ -320,6 +326,8 @@ __global__ void __launch_bounds__(PT_THREADS, 2) prefill_attention_tc(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __half* __restrict__ v_cache, int nq, int nkv, int hd, int pos0, int max_ctx, int T,
     __half* __restrict__ att, int* __restrict__ status) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int group = nq / nkv, QB = 128 / group;          // tokens per CTA
@@ -588,8 +596,8 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
     b += al(2 * (size_t)T * qd);
     float* x2 = reinterpret_cast<float*>(b);
     // B1: x = RMSNorm(h) * attn_norm, fp16 rows
-    rmsnorm_rows<1><<<T, NR_THREADS, 0, st>>>(a.hidden, a.attn_norm, a.eps, a.H, x16);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(rmsnorm_rows<1>, dim3(T), dim3(NR_THREADS), 0, st, a.hidden, a.attn_norm,
+                               a.eps, a.H, x16);
     if (e != cudaSuccess) return e;
     // B2: q, k, v rows of every token, side by side in one [T][qd + 2 kvd]
     // buffer, the three projections in one launch
@@ -606,11 +614,11 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
     __half* qh = tc ? reinterpret_cast<__half*>(qr) : nullptr;
     float2* rcs = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(x2) + al(4 * (size_t)T * a.H) +
                                             al(8 * (size_t)T * a.H));
-    rope_table_rows<<<(T * (a.hd / 2) + 255) / 256, 256, 0, st>>>(a.inv_freq, a.hd / 2, a.pos0, T, rcs);
-    qk_norm_rope_append<<<dim3(T, (a.nq + a.nkv + 3) / 4), 128, 0, st>>>(
-        qkv, a.nq, a.nkv, a.hd, a.q_norm, a.k_norm, a.eps, rcs, a.pos0, a.max_ctx, qr, qh,
-        a.k_cache, a.v_cache, T);
-    e = cudaGetLastError();
+    e = launch_pdl(rope_table_rows, dim3((T * (a.hd / 2) + 255) / 256), dim3(256), 0, st, a.inv_freq,
+                   a.hd / 2, a.pos0, T, rcs);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(qk_norm_rope_append, dim3(T, (a.nq + a.nkv + 3) / 4), dim3(128), 0, st, qkv, a.nq, a.nkv,
+                   a.hd, a.q_norm, a.k_norm, a.eps, rcs, a.pos0, a.max_ctx, qr, qh, a.k_cache, a.v_cache, T);
     if (e != cudaSuccess) return e;
     // B6: causal GQA attention over cache + batch
     if (tc) {
@@ -619,24 +627,17 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
             !tensor_map_half(&tk, a.k_cache, (uint64_t)a.hd, (uint64_t)a.nkv * a.max_ctx, 128))
             return cudaErrorInvalidValue;
         const int QB = 128 / group;
-        prefill_attention_tc<<<dim3(a.nkv, (T + QB - 1) / QB), PT_THREADS, pt_smem(a.hd), st>>>(
-            tq, tk, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16, a.status);
+        e = launch_pdl(prefill_attention_tc, dim3(a.nkv, (T + QB - 1) / QB), dim3(PT_THREADS), pt_smem(a.hd),
+                       st, tq, tk, a.v_cache, a.nq, a.nkv, a.hd, a.pos0, a.max_ctx, T, att16, a.status);
     } else {
         // other shapes: the CUDA-core kernel
         const int mv = (PA_QT * group + PA_THREADS / 32 - 1) / (PA_THREADS / 32);   // vectors per warp
         const dim3 ga(a.nkv, (T + PA_QT - 1) / PA_QT);
         const size_t sm = pa_smem(group, a.hd);
-        if (mv <= 1)
-            prefill_attention<1><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
-                                                             a.pos0, a.max_ctx, T, att16);
-        else if (mv <= 2)
-            prefill_attention<2><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
-                                                             a.pos0, a.max_ctx, T, att16);
-        else
-            prefill_attention<4><<<ga, PA_THREADS, sm, st>>>(qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
-                                                             a.pos0, a.max_ctx, T, att16);
+        auto kern = mv <= 1 ? prefill_attention<1> : mv <= 2 ? prefill_attention<2> : prefill_attention<4>;
+        e = launch_pdl(kern, ga, dim3(PA_THREADS), sm, st, qr, a.k_cache, a.v_cache, a.nq, a.nkv, a.hd,
+                       a.pos0, a.max_ctx, T, att16);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // B7 + B8: h = h + Wo att, x2 = RMSNorm(h) * ffn_norm (the MoE input; h
     // stays the residual).  With too few row x token tiles to fill the GPU the
@@ -646,15 +647,15 @@ cudaError_t launch_prefill_layer_attn(const PrefillLayerArgs& a, cudaStream_t st
         float* part = x2 + (size_t)T * a.H;                // two [T][H] planes after x2
         e = launch_dense_q4k_gemm_multi(&so, 1, qd, att16, T, part, a.H, nullptr, 2, (size_t)T * a.H, st);
         if (e != cudaSuccess) return e;
-        residual_rmsnorm_rows<<<T, NR_THREADS, 0, st>>>(a.hidden, part, part + (size_t)T * a.H, a.ffn_norm,
-                                                        a.eps, a.H, x2);
+        return launch_pdl(residual_rmsnorm_rows, dim3(T), dim3(NR_THREADS), 0, st, a.hidden, part,
+                          part + (size_t)T * a.H, a.ffn_norm, a.eps, a.H, x2);
     } else {
         // in place: every element of h is read and written by one thread
         e = launch_dense_q4k_gemm_multi(&so, 1, qd, att16, T, a.hidden, a.H, a.hidden, 1, 0, st);
         if (e != cudaSuccess) return e;
-        rmsnorm_rows<0><<<T, NR_THREADS, 0, st>>>(a.hidden, a.ffn_norm, a.eps, a.H, x2);
+        return launch_pdl(rmsnorm_rows<0>, dim3(T), dim3(NR_THREADS), 0, st, a.hidden, a.ffn_norm, a.eps, a.H,
+                          x2);
     }
-    return cudaGetLastError();
 }
 
 float* prefill_layer_x2(void* scratch, int T, int H, int nq, int nkv, int hd) {

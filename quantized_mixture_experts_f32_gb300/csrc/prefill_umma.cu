@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "kquant.cuh"
+#include "pdl.cuh"
 #include "qmoe_internal.h"
 #include "umma.cuh"
 
@@ -312,6 +313,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_x128, const __grid_constant__ CUtensorMap tm_xg,
                    const __grid_constant__ CUtensorMap tm_gsc, const __grid_constant__ CUtensorMap tm_usc,
                    const GuParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(1024) uint8_t smraw[];
     // 1024-aligned base, kept a shared-space pointer (an integer round trip
     // would turn every access into a generic one)
@@ -697,6 +700,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     prefill_down(const __grid_constant__ CUtensorMap tm_a64, const __grid_constant__ CUtensorMap tm_a128,
                  const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
                  const DnParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int H = p.H, F = p.F;
@@ -1073,6 +1078,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 // x rows of every pair, in pair-list order, as fp16; inverse pair -> position map
 __global__ void gather_x_f16(const float* __restrict__ x, const int32_t* __restrict__ pair_list,
                              int K, int H, __half* __restrict__ xp, int32_t* __restrict__ inv_pos) {
+    pdl_wait();
     const int pos = blockIdx.x;
     const int pr = pair_list[pos];
     const int t = pr / K;
@@ -1091,6 +1097,7 @@ __global__ void gather_x_f16(const float* __restrict__ x, const int32_t* __restr
 __global__ void combine_pairs(const float* __restrict__ y, const int32_t* __restrict__ inv_pos,
                               const float* __restrict__ wts, const float* res, int H, int K,
                               float* out) {
+    pdl_wait();
     const int t = blockIdx.y;
     const int h4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (4 * h4 >= H) return;
@@ -1210,8 +1217,7 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
                            const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
                            float* out, cudaStream_t st) {
     const int P = s.T * s.K;
-    gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(gather_x_f16, dim3(P), dim3(128), 0, st, x, r.pair_list, s.K, s.H, xp, inv_pos);
     if (e != cudaSuccess) return e;
 
     CUtensorMap tg, tu, tx64, tx128, txg, ta64, ta128;
@@ -1228,16 +1234,15 @@ cudaError_t launch_prefill(const MoeShape& s, const float* x, const float* res,
     if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
                 {0, 0, 0}, {0, 0, 0}, 1, 0, nullptr, nullptr};
-    prefill_gateup<0, 0><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tg, tg, gp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_gateup<0, 0>, dim3(sm_count()), dim3(GU_THREADS), GU_SMEM, st, tg, tu, tu, tx64,
+                   tx128, txg, tg, tg, gp);
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, down, y, s.H, s.F, down_t, nullptr};
-    prefill_down<0><<<sm_count(), GU_THREADS, dn_smem(s.F, down_t, s.E), st>>>(ta64, ta128, ta64, ta64, dp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_down<0>, dim3(sm_count()), dim3(GU_THREADS), dn_smem(s.F, down_t, s.E), st, ta64,
+                   ta128, ta64, ta64, dp);
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
-    combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_pairs, g3, dim3(256), 0, st, y, inv_pos, r.wts, res, s.H, s.K, out);
 }
 
 bool prefill_fp8_supported(const MoeShape& s) {
@@ -1249,8 +1254,7 @@ cudaError_t launch_prefill_fp8(const MoeShape& s, const float* x, const float* r
                                const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
                                float* out, cudaStream_t st) {
     const int P = s.T * s.K;
-    gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(gather_x_f16, dim3(P), dim3(128), 0, st, x, r.pair_list, s.K, s.H, xp, inv_pos);
     if (e != cudaSuccess) return e;
     CUtensorMap tg, tu, td, tx64, tx128, txg, ta64, ta128;
     if (!map_bytes(&tg, w.gate, (uint64_t)s.H, (uint64_t)s.E * s.F, F8_COLS, 64) ||
@@ -1264,16 +1268,15 @@ cudaError_t launch_prefill_fp8(const MoeShape& s, const float* x, const float* r
     if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
                 {0, 0, 0}, {0, 0, 0}, 1, 0, w.gate_scale, w.up_scale};
-    prefill_gateup<0, 1><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tg, tg, gp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_gateup<0, 1>, dim3(sm_count()), dim3(GU_THREADS), GU_SMEM, st, tg, tu, tu, tx64,
+                   tx128, txg, tg, tg, gp);
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, w.down, y, s.H, s.F, 3, w.down_scale};
-    prefill_down<1><<<sm_count(), GU_THREADS, dn_smem(s.F, 3, s.E), st>>>(ta64, ta128, td, td, dp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_down<1>, dim3(sm_count()), dim3(GU_THREADS), dn_smem(s.F, 3, s.E), st, ta64, ta128,
+                   td, td, dp);
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
-    combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_pairs, g3, dim3(256), 0, st, y, inv_pos, r.wts, res, s.H, s.K, out);
 }
 
 bool prefill_nvfp4_supported(const MoeShape& s) {
@@ -1285,8 +1288,7 @@ cudaError_t launch_prefill_nvfp4(const MoeShape& s, const float* x, const float*
                                  const Route& r, __half* xp, __half* actp, float* y, int32_t* inv_pos,
                                  float* out, cudaStream_t st) {
     const int P = s.T * s.K;
-    gather_x_f16<<<P, 128, 0, st>>>(x, r.pair_list, s.K, s.H, xp, inv_pos);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(gather_x_f16, dim3(P), dim3(128), 0, st, x, r.pair_list, s.K, s.H, xp, inv_pos);
     if (e != cudaSuccess) return e;
     CUtensorMap tg, tu, tgs, tus, td, tds, tx64, tx128, txg, ta64, ta128;
     const uint64_t gu_rows = (uint64_t)s.E * s.F, dn_rows = (uint64_t)s.E * s.H;
@@ -1304,16 +1306,15 @@ cudaError_t launch_prefill_nvfp4(const MoeShape& s, const float* x, const float*
     if (e != cudaSuccess) return e;
     GuParams gp{r.n_used, r.used_expert, r.used_first, actp, s.H, s.F, nullptr, nullptr, 0, 0,
                 {0, 0, 0}, {0, 0, 0}, 1, 0, w.gate_gs, w.up_gs};
-    prefill_gateup<0, 2><<<sm_count(), GU_THREADS, GU_SMEM, st>>>(tg, tu, tu, tx64, tx128, txg, tgs, tus, gp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_gateup<0, 2>, dim3(sm_count()), dim3(GU_THREADS), GU_SMEM, st, tg, tu, tu, tx64,
+                   tx128, txg, tgs, tus, gp);
     if (e != cudaSuccess) return e;
     DnParams dp{r.n_used, r.used_expert, r.used_first, w.down, y, s.H, s.F, 4, w.down_gs};
-    prefill_down<2><<<sm_count(), GU_THREADS, dn_smem(s.F, 4, s.E), st>>>(ta64, ta128, td, tds, dp);
-    e = cudaGetLastError();
+    e = launch_pdl(prefill_down<2>, dim3(sm_count()), dim3(GU_THREADS), dn_smem(s.F, 4, s.E), st, ta64, ta128,
+                   td, tds, dp);
     if (e != cudaSuccess) return e;
     dim3 g3((s.H / 4 + 255) / 256, s.T);
-    combine_pairs<<<g3, 256, 0, st>>>(y, inv_pos, r.wts, res, s.H, s.K, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_pairs, g3, dim3(256), 0, st, y, inv_pos, r.wts, res, s.H, s.K, out);
 }
 
 cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, const __half* x, int T,
@@ -1341,9 +1342,9 @@ cudaError_t launch_dense_q4k_gemm_multi(const DenseSeg* seg, int nseg, int K, co
                 {nseg > 0 ? seg[0].yoff : 0, nseg > 1 ? seg[1].yoff : 0, nseg > 2 ? seg[2].yoff : 0},
                 ksplit, part_stride, nullptr, nullptr};
     const int items = (rows / TILE_M) * ksplit * ((T + GU_NMAX - 1) / GU_NMAX);
-    prefill_gateup<1, 0><<<items < sm_count() ? items : sm_count(), GU_THREADS, GU_SMEM, st>>>(
-        tw[0], tw[1], tw[2], tx64, tx128, txg, tw[0], tw[0], gp);
-    return cudaGetLastError();
+    const int grid = items < sm_count() ? items : sm_count();
+    return launch_pdl(prefill_gateup<1, 0>, dim3(grid), dim3(GU_THREADS), GU_SMEM, st, tw[0], tw[1], tw[2],
+                      tx64, tx128, txg, tw[0], tw[0], gp);
 }
 
 cudaError_t launch_dense_q4k_gemm(const uint8_t* W, int rows, int K, const __half* x, int T, float* y,

@@ -87,6 +87,9 @@ CASES = [
     ("tiny_fp8", 40, {}),
     ("tiny_fp8", 7, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 12}),
     ("tiny_fp8", 200, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 12}),
+    ("tiny_fp8", 3, {"E": 256, "K": 8, "seed": 30}),      # more than 128 experts: the generic top-k
+    ("tiny_fp8", 40, {"E": 256, "K": 8, "seed": 30}),
+    ("tiny_fp8", 4, {"E": 8, "K": 1, "seed": 31}),        # top-1
     ("decode_fp8", None, {}),
     ("decode_fp8", 8, {}),
     ("decode_fp8", 16, {}),

@@ -87,6 +87,9 @@ CASES = [
     ("tiny_nvfp4", 40, {}),
     ("tiny_nvfp4", 7, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 22}),
     ("tiny_nvfp4", 200, {"H": 1024, "F": 512, "E": 16, "K": 4, "seed": 22}),
+    ("tiny_nvfp4", 3, {"E": 256, "K": 8, "seed": 30}),      # more than 128 experts: the generic top-k
+    ("tiny_nvfp4", 40, {"E": 256, "K": 8, "seed": 30}),
+    ("tiny_nvfp4", 4, {"E": 8, "K": 1, "seed": 31}),        # top-1
     ("decode_nvfp4", None, {}),
     ("decode_nvfp4", 8, {}),
     ("decode_nvfp4", 16, {}),

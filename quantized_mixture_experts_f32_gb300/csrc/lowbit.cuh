@@ -54,10 +54,13 @@ __device__ __forceinline__ float group_sum(float v) {
 // CTAs of a grid-strided launch: enough for every warp item, at most the CTAs
 // resident at once (resident: per-kernel cache, filled on first use)
 template <typename Kern>
-int strided_grid(Kern kern, int threads, int* resident, int items, int num_sms) {
+int strided_grid(Kern kern, int threads, int* resident, int items, int num_sms, size_t smem = 0) {
     if (!*resident) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess || n < 1)
+        if (smem && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                        cudaSuccess)
+            cudaGetLastError();
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1)
             n = 1;
         *resident = n;
     }

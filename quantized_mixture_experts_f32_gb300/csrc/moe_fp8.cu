@@ -32,34 +32,47 @@ constexpr int F8_THREADS = 256;
 
 // Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
 // and f0 + 1 (half-warp hw takes row f0 + hw of both gate and up); NC = H / 256.
-template <int NC>
+// STAGE: the T x rows are first staged in shared memory (padded; few tokens).
+template <int NC, bool STAGE>
 __global__ void __launch_bounds__(F8_THREADS) fp8_gateup_kernel(
-    const float* __restrict__ x, int H, int F, int K, const Fp8Experts w,
+    const float* __restrict__ x, int T, int H, int F, int K, const Fp8Experts w,
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ act) {
+    extern __shared__ __align__(16) float xs[];
     pdl_wait();                 // the routing of this call
     pdl_launch_dependents();
+    if (STAGE) {
+        lowbit::vstage(xs, x, T, H);
+        __syncthreads();
+    }
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
     const int per = F >> 1;
     const int items = *n_used * per;
     for (int i = gw; i < items; i += nw) {
-        const int u = i / per;
-        lowbit::f8_gateup_rows<NC>(x, H, F, K, w, used_expert[u], 2 * (i - u * per) + hw, hl,
-                                   pair_list, used_first[u], used_first[u + 1], act);
+        const int u = i / per, f = 2 * (i - u * per) + hw;
+        if (STAGE)
+            lowbit::f8_gateup_rows<NC, lowbit::SRC_SMEM>(xs, lowbit::vpad_ld(H), H, F, K, w, used_expert[u],
+                                                         f, hl, pair_list, used_first[u], used_first[u + 1],
+                                                         act);
+        else
+            lowbit::f8_gateup_rows<NC, lowbit::SRC_NC>(x, H, H, F, K, w, used_expert[u], f, hl, pair_list,
+                                                       used_first[u], used_first[u + 1], act);
     }
 }
 
 // Down projection.  Item i -> used expert u = i / (H/4), rows h0 = 4 (i % (H/4)) ..
 // h0 + 3; half-warp hw takes rows h0 + hw and h0 + 2 + hw; NC = F / 256.
-template <int NC>
+// STAGE: the P act rows are first staged in shared memory (padded).
+template <int NC, bool STAGE>
 __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
-    const float* __restrict__ act, int H, int F, const Fp8Experts w,
+    const float* __restrict__ act, int P, int H, int F, const Fp8Experts w,
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ y) {
+    extern __shared__ __align__(16) float as[];
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * F8_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * F8_THREADS) >> 5;
@@ -76,30 +89,58 @@ __global__ void __launch_bounds__(F8_THREADS) fp8_down_kernel(
     }
     pdl_wait();                 // act of this call
     pdl_launch_dependents();
+    if (STAGE) {
+        lowbit::vstage(as, act, P, F);
+        __syncthreads();
+    }
     for (int i = gw; i < items; i += nw) {
         const int u = i / per, h = 4 * (i - u * per) + hw;
         const int e = used_expert[u];
         if (i != gw) lowbit::f8_down_load<NC>(d, w, e, h, H, F, hl);
-        lowbit::f8_down_rows<NC, false>(d, w, e, h, H, F, hl, pair_list, used_first[u],
-                                        used_first[u + 1], act, y);
+        if (STAGE)
+            lowbit::f8_down_rows<NC, lowbit::SRC_SMEM>(d, w, e, h, H, F, hl, pair_list, used_first[u],
+                                                       used_first[u + 1], as, lowbit::vpad_ld(F), y);
+        else
+            lowbit::f8_down_rows<NC, lowbit::SRC_NC>(d, w, e, h, H, F, hl, pair_list, used_first[u],
+                                                     used_first[u + 1], act, F, y);
     }
 }
+
+// x / act rows are staged in shared memory when they fit in this much
+constexpr size_t LB_STAGE_MAX = 72 * 1024;
 
 template <int NC>
 cudaError_t gateup_nc(const MoeShape& s, const float* x, const Fp8Experts& w, const Route& r,
                       float* act, int items, int num_sms, cudaStream_t st) {
-    static int resident = 0;   // per instantiation
-    const int grid = strided_grid(fp8_gateup_kernel<NC>, F8_THREADS, &resident, items, num_sms);
-    return launch_pdl(fp8_gateup_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.H, s.F, s.K, w,
-                      r.n_used, r.used_expert, r.used_first, r.pair_list, act);
+    const size_t smem = sizeof(float) * (size_t)s.T * lowbit::vpad_ld(s.H);
+    if (smem <= LB_STAGE_MAX) {
+        static int resident = 0;   // per instantiation, at the largest staging
+        const int grid = strided_grid(fp8_gateup_kernel<NC, true>, F8_THREADS, &resident, items, num_sms,
+                                      LB_STAGE_MAX);
+        return launch_pdl(fp8_gateup_kernel<NC, true>, dim3(grid), dim3(F8_THREADS), smem, st, x, s.T, s.H,
+                          s.F, s.K, w, r.n_used, r.used_expert, r.used_first, r.pair_list, act);
+    }
+    static int resident = 0;
+    const int grid = strided_grid(fp8_gateup_kernel<NC, false>, F8_THREADS, &resident, items, num_sms, 0);
+    return launch_pdl(fp8_gateup_kernel<NC, false>, dim3(grid), dim3(F8_THREADS), 0, st, x, s.T, s.H, s.F,
+                      s.K, w, r.n_used, r.used_expert, r.used_first, r.pair_list, act);
 }
 
 template <int NC>
 cudaError_t down_nc(const MoeShape& s, const float* act, const Fp8Experts& w, const Route& r,
                     float* y, int items, int num_sms, cudaStream_t st) {
-    static int resident = 0;   // per instantiation
-    const int grid = strided_grid(fp8_down_kernel<NC>, F8_THREADS, &resident, items, num_sms);
-    return launch_pdl(fp8_down_kernel<NC>, dim3(grid), dim3(F8_THREADS), 0, st, act, s.H, s.F, w,
+    const int P = s.T * s.K;
+    const size_t smem = sizeof(float) * (size_t)P * lowbit::vpad_ld(s.F);
+    if (smem <= LB_STAGE_MAX) {
+        static int resident = 0;
+        const int grid = strided_grid(fp8_down_kernel<NC, true>, F8_THREADS, &resident, items, num_sms,
+                                      LB_STAGE_MAX);
+        return launch_pdl(fp8_down_kernel<NC, true>, dim3(grid), dim3(F8_THREADS), smem, st, act, P, s.H,
+                          s.F, w, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
+    }
+    static int resident = 0;
+    const int grid = strided_grid(fp8_down_kernel<NC, false>, F8_THREADS, &resident, items, num_sms, 0);
+    return launch_pdl(fp8_down_kernel<NC, false>, dim3(grid), dim3(F8_THREADS), 0, st, act, P, s.H, s.F, w,
                       r.n_used, r.used_expert, r.used_first, r.pair_list, y);
 }
 

@@ -110,34 +110,47 @@ __global__ void nvfp4_global(const unsigned* __restrict__ amax_bits, int n_mats,
 
 // Gate/up + SwiGLU.  Item i -> used expert u = i / (F/2), rows f0 = 2 (i % (F/2))
 // and f0 + 1 (half-warp hw takes row f0 + hw of gate and up); NC = H / 512.
-template <int NC>
+// STAGE: the T x rows are first staged in shared memory (padded; few tokens).
+template <int NC, bool STAGE>
 __global__ void __launch_bounds__(NV_THREADS) nvfp4_gateup_kernel(
-    const float* __restrict__ x, int H, int F, int K, const NvExperts w,
+    const float* __restrict__ x, int T, int H, int F, int K, const NvExperts w,
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ act) {
+    extern __shared__ __align__(16) float xs[];
     pdl_wait();
     pdl_launch_dependents();
+    if (STAGE) {
+        lowbit::vstage(xs, x, T, H);
+        __syncthreads();
+    }
     const int lane = threadIdx.x & 31, hw = lane >> 4, hl = lane & 15;
     const int gw = (blockIdx.x * NV_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * NV_THREADS) >> 5;
     const int per = F >> 1;
     const int items = *n_used * per;
     for (int i = gw; i < items; i += nw) {
-        const int u = i / per;
-        lowbit::nv_gateup_rows<NC>(x, H, F, K, w, used_expert[u], 2 * (i - u * per) + hw, hl,
-                                   pair_list, used_first[u], used_first[u + 1], act);
+        const int u = i / per, f = 2 * (i - u * per) + hw;
+        if (STAGE)
+            lowbit::nv_gateup_rows<NC, lowbit::SRC_SMEM>(xs, lowbit::vpad_ld(H), H, F, K, w, used_expert[u],
+                                                         f, hl, pair_list, used_first[u], used_first[u + 1],
+                                                         act);
+        else
+            lowbit::nv_gateup_rows<NC, lowbit::SRC_NC>(x, H, H, F, K, w, used_expert[u], f, hl, pair_list,
+                                                       used_first[u], used_first[u + 1], act);
     }
 }
 
 // Down projection.  Item i -> used expert u = i / (H/4), rows h0 = 4 (i % (H/4))
-// .. h0 + 3 (quarter-warp q takes row h0 + q); NC = F / 256.
-template <int NC>
+// .. h0 + 3 (quarter-warp q takes row h0 + q); NC = F / 256.  STAGE: the P act
+// rows are first staged in shared memory (padded).
+template <int NC, bool STAGE>
 __global__ void __launch_bounds__(NV_THREADS) nvfp4_down_kernel(
-    const float* __restrict__ act, int H, int F, const NvExperts w,
+    const float* __restrict__ act, int P, int H, int F, const NvExperts w,
     const int32_t* __restrict__ n_used, const int32_t* __restrict__ used_expert,
     const int32_t* __restrict__ used_first, const int32_t* __restrict__ pair_list,
     float* __restrict__ y) {
+    extern __shared__ __align__(16) float as[];
     const int lane = threadIdx.x & 31, q = lane >> 3, ql = lane & 7;
     const int gw = (blockIdx.x * NV_THREADS + threadIdx.x) >> 5;
     const int nw = (gridDim.x * NV_THREADS) >> 5;
@@ -152,31 +165,59 @@ __global__ void __launch_bounds__(NV_THREADS) nvfp4_down_kernel(
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (STAGE) {
+        lowbit::vstage(as, act, P, F);
+        __syncthreads();
+    }
     for (int i = gw; i < items; i += nw) {
         const int u = i / per, h = 4 * (i - u * per) + q;
         const int e = used_expert[u];
         if (i != gw) lowbit::nv_down_load<NC>(d, w, e, h, H, F, ql);
-        lowbit::nv_down_rows<NC, false>(d, w, e, h, H, F, ql, pair_list, used_first[u],
-                                        used_first[u + 1], act, y);
+        if (STAGE)
+            lowbit::nv_down_rows<NC, lowbit::SRC_SMEM>(d, w, e, h, H, F, ql, pair_list, used_first[u],
+                                                       used_first[u + 1], as, lowbit::vpad_ld(F), y);
+        else
+            lowbit::nv_down_rows<NC, lowbit::SRC_NC>(d, w, e, h, H, F, ql, pair_list, used_first[u],
+                                                     used_first[u + 1], act, F, y);
     }
 }
+
+// x / act rows are staged in shared memory when they fit in this much
+constexpr size_t NV_STAGE_MAX = 72 * 1024;
 
 template <int NC>
 cudaError_t nv_gateup(const MoeShape& s, const float* x, const NvExperts& w, const Route& r,
                       float* act, int items, int num_sms, cudaStream_t st) {
-    static int resident = 0;   // per instantiation
-    const int grid = strided_grid(nvfp4_gateup_kernel<NC>, NV_THREADS, &resident, items, num_sms);
-    return launch_pdl(nvfp4_gateup_kernel<NC>, dim3(grid), dim3(NV_THREADS), 0, st, x, s.H, s.F, s.K,
-                      w, r.n_used, r.used_expert, r.used_first, r.pair_list, act);
+    const size_t smem = sizeof(float) * (size_t)s.T * lowbit::vpad_ld(s.H);
+    if (smem <= NV_STAGE_MAX) {
+        static int resident = 0;   // per instantiation, at the largest staging
+        const int grid = strided_grid(nvfp4_gateup_kernel<NC, true>, NV_THREADS, &resident, items, num_sms,
+                                      NV_STAGE_MAX);
+        return launch_pdl(nvfp4_gateup_kernel<NC, true>, dim3(grid), dim3(NV_THREADS), smem, st, x, s.T,
+                          s.H, s.F, s.K, w, r.n_used, r.used_expert, r.used_first, r.pair_list, act);
+    }
+    static int resident = 0;
+    const int grid = strided_grid(nvfp4_gateup_kernel<NC, false>, NV_THREADS, &resident, items, num_sms, 0);
+    return launch_pdl(nvfp4_gateup_kernel<NC, false>, dim3(grid), dim3(NV_THREADS), 0, st, x, s.T, s.H,
+                      s.F, s.K, w, r.n_used, r.used_expert, r.used_first, r.pair_list, act);
 }
 
 template <int NC>
 cudaError_t nv_down(const MoeShape& s, const float* act, const NvExperts& w, const Route& r,
                     float* y, int items, int num_sms, cudaStream_t st) {
-    static int resident = 0;   // per instantiation
-    const int grid = strided_grid(nvfp4_down_kernel<NC>, NV_THREADS, &resident, items, num_sms);
-    return launch_pdl(nvfp4_down_kernel<NC>, dim3(grid), dim3(NV_THREADS), 0, st, act, s.H, s.F, w,
-                      r.n_used, r.used_expert, r.used_first, r.pair_list, y);
+    const int P = s.T * s.K;
+    const size_t smem = sizeof(float) * (size_t)P * lowbit::vpad_ld(s.F);
+    if (smem <= NV_STAGE_MAX) {
+        static int resident = 0;
+        const int grid = strided_grid(nvfp4_down_kernel<NC, true>, NV_THREADS, &resident, items, num_sms,
+                                      NV_STAGE_MAX);
+        return launch_pdl(nvfp4_down_kernel<NC, true>, dim3(grid), dim3(NV_THREADS), smem, st, act, P, s.H,
+                          s.F, w, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
+    }
+    static int resident = 0;
+    const int grid = strided_grid(nvfp4_down_kernel<NC, false>, NV_THREADS, &resident, items, num_sms, 0);
+    return launch_pdl(nvfp4_down_kernel<NC, false>, dim3(grid), dim3(NV_THREADS), 0, st, act, P, s.H, s.F,
+                      w, r.n_used, r.used_expert, r.used_first, r.pair_list, y);
 }
 
 }  // namespace

@@ -623,6 +623,7 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         names = ("router", "gate", "gate_scale", "up", "up_scale", "down", "down_scale")
     T, H, E, K, F = inp["T"], inp["H"], inp["E"], inp["K"], inp["F"]
     fmt = "NVFP4" if nv else "FP8"
+    one = T == 1 and (H, F) == (2048, 768) and E <= 128   # the one-kernel decode
     x = torch.from_numpy(inp["x"]).to(dev)
     base = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev) for n in names}
     R = args.copies
@@ -684,14 +685,16 @@ def bench_layer_fp8(args, torch, q, dev, stream, ws, pg, local):
         value=T * args.steps * ws / secs, ms=ms, step_s=step_s, clocks=clocks,
         ebytes=ebytes, other_bytes=rbytes, distinct=distinct, T=T,
         e2e=T * args.e2e_steps * ws / te, h2d=T * H * 4, d2h=T * H * 4,
-        launches=(q.LAUNCHES_PER_FP8_FORWARD if T <= 8 else q.LAUNCHES_PER_FP8_FORWARD + 1
-                  if T <= q.FP8_GEMV_MAX else q.LAUNCHES_PER_FP8_FORWARD_MANY),
+        launches=(q.LAUNCHES_PER_LOWBIT_T1 if one else q.LAUNCHES_PER_FP8_FORWARD if T <= 8
+                  else q.LAUNCHES_PER_FP8_FORWARD + 1 if T <= q.FP8_GEMV_MAX
+                  else q.LAUNCHES_PER_FP8_FORWARD_MANY),
         config={"workload": w["desc"], "hidden": H, "n_experts": E, "top_k": K, "ffn": F,
                 "tokens": T, "distinct_experts": distinct, "expert_bytes": per_expert,
                 "l2": f"weights rotate over {R} device copies, {touched / 1e6:.0f} MB touched "
                       f"per rotation vs L2 {l2 / 1e6:.0f} MB; a {2 * l2 / 1e6:.0f} MB buffer is "
                       "written right before the timed region"},
-        kernel=(f"whole {fmt} layer call (router, top-k, gate/up, down, combine)"
+        kernel=(f"lowbit_t1<{fmt}> (the whole layer is one kernel)" if one
+                else f"whole {fmt} layer call (router, top-k, gate/up, down, combine)"
                 if T <= q.FP8_GEMV_MAX
                 else f"whole {fmt} layer call (routing, gather, grouped tensor-core GEMMs, combine)"),
         dtype=(f"{'e2m1 weights and e4m3 scales' if nv else 'e4m3 weights'} widened exactly, f32 "

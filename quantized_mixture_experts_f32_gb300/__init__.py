@@ -37,7 +37,10 @@ LAUNCHES_PER_Q8K_FORWARD = 7
 # cores): router GEMM, top-k, per-expert lists, gather, gate/up GEMM, down GEMM,
 # combine
 FP8_GEMV_MAX = 32
-LAUNCHES_PER_FP8_FORWARD = 4           # up to 8 tokens (5 for 9..32)
+# one token at hidden 2048 / ffn 768 (up to 128 experts): the whole FP8 or NVFP4
+# layer is one cooperative kernel
+LAUNCHES_PER_LOWBIT_T1 = 1
+LAUNCHES_PER_FP8_FORWARD = 4           # otherwise up to 8 tokens (5 for 9..32)
 LAUNCHES_PER_FP8_FORWARD_MANY = 7
 # qmoe_forward_nvfp4: as qmoe_forward_fp8 (4 launches up to 8 tokens, 5 for
 # 9..32, 7 on the tensor cores beyond)

@@ -26,6 +26,8 @@ struct qmoe_ctx {
     int* status;      // device status word
     unsigned* bar;    // decode kernels' control words (exit counter, launch tag, arrival words)
     unsigned* nvq;    // per-matrix amax words of qmoe_nvfp4_quantize
+    unsigned* ltctl;  // counters and launch tag of the one-launch FP8 / NVFP4 decode kernel
+    unsigned long long* ltlg; // its tagged router logits [E]
     qmoe::FusedBufs fb; // tagged values passed between the fused kernel's CTAs
     __half* xp;       // [P][H] fp16 gathered x (prefill)
     __half* actp;     // [P][F] fp16 SwiGLU output (prefill)
@@ -87,7 +89,7 @@ bool valid_qtype(int q) { return q == QMOE_Q4_K || q == QMOE_Q6_K; }
 
 struct Layout {
     size_t logits, ids, wts, n_used, used_expert, used_first, pair_list, act, y, hin, hout,
-        status, bar, arrive, nvq, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
+        status, bar, arrive, nvq, ltctl, ltlg, xp, actp, inv_pos, logits_part, tokmap, jmap, q8, ftag, xs, q, kv, att, attn_part, inv_freq,
         rope_cs, pl, total;
     int attn_splits;
     bool pl_ok;
@@ -135,6 +137,8 @@ Layout layout(const qmoe_config* c) {
     L.bar = take(sizeof(unsigned) * 64);
     L.arrive = take(sizeof(unsigned) * 4);
     L.nvq = take(sizeof(unsigned) * NVFP4_QUANT_MATS_MAX);
+    L.ltctl = take(sizeof(unsigned) * 4);
+    L.ltlg = take(sizeof(unsigned long long) * E);
     L.xp = take(sizeof(__half) * P * H);
     L.actp = take(sizeof(__half) * P * F);
     L.inv_pos = take(sizeof(int32_t) * P);
@@ -366,6 +370,8 @@ qmoe_status qmoe_create(const qmoe_config* cfg, qmoe_ctx** out) {
     c->route.jmap = reinterpret_cast<uint8_t*>(b + L.jmap);
     c->route.arrive = reinterpret_cast<unsigned*>(b + L.arrive);
     c->nvq = reinterpret_cast<unsigned*>(b + L.nvq);
+    c->ltctl = reinterpret_cast<unsigned*>(b + L.ltctl);
+    c->ltlg = reinterpret_cast<unsigned long long*>(b + L.ltlg);
     c->q8 = qmoe::q8_bufs_carve(reinterpret_cast<unsigned char*>(b + L.q8), c->cfg.max_tokens, c->cfg.hidden,
                                 c->cfg.top_k, c->cfg.ffn);
     c->act = reinterpret_cast<float*>(b + L.act);
@@ -510,6 +516,15 @@ qmoe_status qmoe_forward_fp8(qmoe_ctx* c, const float* hidden_in, const float* r
     const qmoe::Fp8Experts w{static_cast<const uint8_t*>(gate_exps), gate_scale,
                              static_cast<const uint8_t*>(up_exps), up_scale,
                              static_cast<const uint8_t*>(down_exps), down_scale};
+    if (qmoe::lowbit_t1_supported(1, n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, c->num_sms)) {
+        // one token: the whole layer is one kernel
+        cudaError_t e = qmoe::launch_lowbit_t1(1, ms, hidden_in, router_w, &w, nullptr, c->act, hidden_out,
+                                               ids_out, weights_out, c->ltlg, c->ltctl, c->status,
+                                               c->num_sms, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "FP8 decode launch");
+        c->err[0] = 0;
+        return QMOE_OK;
+    }
     // up to FP8_GEMV_MAX tokens: expert GEMVs on the CUDA cores; more: grouped
     // GEMMs on the tensor cores
     const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route) &&
@@ -565,6 +580,15 @@ qmoe_status qmoe_forward_nvfp4(qmoe_ctx* c, const float* hidden_in, const float*
                             static_cast<const uint8_t*>(up_bscale), up_global,
                             static_cast<const uint8_t*>(down_exps), static_cast<const uint8_t*>(down_bscale),
                             down_global};
+    if (qmoe::lowbit_t1_supported(2, n_tokens, k.hidden, k.n_experts, k.top_k, k.ffn, c->num_sms)) {
+        // one token: the whole layer is one kernel
+        cudaError_t e = qmoe::launch_lowbit_t1(2, ms, hidden_in, router_w, nullptr, &w, c->act, hidden_out,
+                                               ids_out, weights_out, c->ltlg, c->ltctl, c->status,
+                                               c->num_sms, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "NVFP4 decode launch");
+        c->err[0] = 0;
+        return QMOE_OK;
+    }
     const bool many = n_tokens > FP8_GEMV_MAX && qmoe::route_many_supported(ms, c->route);
     // the tensor-core path copies the block scales by TMA (16-byte aligned rows)
     const bool tc = many && qmoe::prefill_nvfp4_supported(ms) && aligned16(gate_bscale) &&

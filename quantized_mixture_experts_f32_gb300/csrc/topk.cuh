@@ -17,6 +17,69 @@ __device__ __forceinline__ float key_value(int k) { return __int_as_float(k ^ ((
 
 constexpr int TK_MAXV = 32;   // logits per lane (E <= 1024)
 
+// One token's top-K of up to 128 F32 logits by one warp (ties to the lower
+// index), softmax over all E and the weights renormalised over the K selected
+// (norm), lane j < K ending with selection j (id and weight).  Lane l sorts the
+// (order key, index) pairs of experts l, l + 32, l + 64, l + 96 (larger key
+// first), then K tournament rounds over the 32 lane heads: the largest head key
+// by one warp max-reduction, the lowest index holding it by one min-reduction,
+// the owner drops its head.  SMEM: logits in shared memory (else global memory,
+// read through L2: they may come from other CTAs of the same launch).
+template <bool SMEM>
+__device__ __forceinline__ void topk_warp128(const float* lt, int E, int K, int norm, int& my_id,
+                                             float& my_w) {
+    const int lane = threadIdx.x & 31;
+    auto ld = [&](int i) { return SMEM ? lt[i] : __ldcg(lt + i); };
+    int ks[4], is[4];
+#pragma unroll
+    for (int z = 0; z < 4; ++z) {
+        const int i = lane + 32 * z;
+        ks[z] = i < E ? order_key(ld(i)) : INT_MIN;
+        is[z] = i < E ? i : INT_MAX;
+    }
+    auto cswap = [&](int x, int y) {
+        if (ks[y] > ks[x] || (ks[y] == ks[x] && is[y] < is[x])) {
+            const int tk = ks[x], ti = is[x];
+            ks[x] = ks[y];
+            is[x] = is[y];
+            ks[y] = tk;
+            is[y] = ti;
+        }
+    };
+    cswap(0, 1);
+    cswap(2, 3);
+    cswap(0, 2);
+    cswap(1, 3);
+    cswap(1, 2);
+    my_id = 0;
+    float my_v = 0.f, vmax = 0.f;
+    for (int r = 0; r < K; ++r) {
+        const int mk = __reduce_max_sync(0xffffffffu, ks[0]);
+        const int wi = (int)__reduce_min_sync(0xffffffffu, ks[0] == mk ? (unsigned)is[0] : 0xffffffffu);
+        if (r == 0) vmax = key_value(mk);
+        if (lane == r) {
+            my_id = wi;
+            my_v = key_value(mk);
+        }
+        if ((wi & 31) == lane) {
+            ks[0] = ks[1];
+            ks[1] = ks[2];
+            ks[2] = ks[3];
+            ks[3] = INT_MIN;
+            is[0] = is[1];
+            is[1] = is[2];
+            is[2] = is[3];
+            is[3] = INT_MAX;
+        }
+    }
+    float z = 0.f;
+    for (int i = lane; i < E; i += 32) z += expf(ld(i) - vmax);
+    z = warp_sum(z);
+    const float pj = lane < K ? expf(my_v - vmax) / z : 0.f;
+    const float psel = warp_sum(pj);
+    my_w = norm ? pj / psel : pj;
+}
+
 // Per token (one warp): top-K of the F32 logits (ties -> lower index), softmax
 // over all E, routing weights renormalised over the K selected.  Then one warp
 // builds the per-expert pair lists with a stable counting sort.
@@ -32,62 +95,12 @@ __device__ __noinline__ void topk_lists(const float* __restrict__ logits, int T,
     const int nwarps = blockDim.x >> 5;
     const int nv = (E + 31) / 32;
     for (int t = warp; E <= 128 && t < T; t += nwarps) {
-        // up to 128 experts: lane l sorts the (order key, index) pairs of experts
-        // l, l + 32, l + 64, l + 96 (larger key first, ties to the lower index),
-        // then K tournament rounds over the 32 lane heads (the largest head key
-        // by one warp max-reduction, the lowest index holding it by one
-        // min-reduction, the owner drops its head); lane j keeps selection j
-        const float* lt = logits + (size_t)t * E;
-        int ks[4], is[4];
-#pragma unroll
-        for (int z = 0; z < 4; ++z) {
-            const int i = lane + 32 * z;
-            ks[z] = i < E ? order_key(__ldcg(lt + i)) : INT_MIN;
-            is[z] = i < E ? i : INT_MAX;
-        }
-        auto cswap = [&](int x, int y) {
-            if (ks[y] > ks[x] || (ks[y] == ks[x] && is[y] < is[x])) {
-                const int tk = ks[x], ti = is[x];
-                ks[x] = ks[y];
-                is[x] = is[y];
-                ks[y] = tk;
-                is[y] = ti;
-            }
-        };
-        cswap(0, 1);
-        cswap(2, 3);
-        cswap(0, 2);
-        cswap(1, 3);
-        cswap(1, 2);
-        int my_id = 0;
-        float my_v = 0.f, vmax = 0.f;
-        for (int r = 0; r < K; ++r) {
-            const int mk = __reduce_max_sync(0xffffffffu, ks[0]);
-            const int wi = (int)__reduce_min_sync(0xffffffffu, ks[0] == mk ? (unsigned)is[0] : 0xffffffffu);
-            if (r == 0) vmax = key_value(mk);
-            if (lane == r) {
-                my_id = wi;
-                my_v = key_value(mk);
-            }
-            if ((wi & 31) == lane) {
-                ks[0] = ks[1];
-                ks[1] = ks[2];
-                ks[2] = ks[3];
-                ks[3] = INT_MIN;
-                is[0] = is[1];
-                is[1] = is[2];
-                is[2] = is[3];
-                is[3] = INT_MAX;
-            }
-        }
-        float z = 0.f;
-        for (int i = lane; i < E; i += 32) z += expf(__ldcg(lt + i) - vmax);
-        z = warp_sum(z);
-        const float pj = lane < K ? expf(my_v - vmax) / z : 0.f;
-        const float psel = warp_sum(pj);
+        int my_id;
+        float my_w;
+        topk_warp128<false>(logits + (size_t)t * E, E, K, norm, my_id, my_w);
         if (lane < K) {
             ids[(size_t)t * K + lane] = my_id;
-            wts[(size_t)t * K + lane] = norm ? pj / psel : pj;
+            wts[(size_t)t * K + lane] = my_w;
         }
     }
     for (int t = warp; E > 128 && t < T; t += nwarps) {

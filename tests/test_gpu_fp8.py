@@ -111,15 +111,17 @@ def test_fp8_layer_matches_oracle(q, cfg_id, T, over):
     print(f"{cfg_id} T={inp['T']}: max relative error {err:.2e}")
 
 
-def test_fp8_in_place_and_repeatable(q):
-    inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS["tiny_fp8"], T=6)
+# the GEMV path (tiny, T=6) and the one-kernel decode path (Qwen3 shape, T=1)
+@pytest.mark.parametrize("cfg_id,T", [("tiny_fp8", 6), ("decode_fp8", 1)])
+def test_fp8_in_place_and_repeatable(q, cfg_id, T):
+    inp = synth.moe_inputs_fp8(synth.FP8_CONFIGS[cfg_id], T=T)
     d = _upload(inp)
     ctx = G.make_ctx(q, inp)
     try:
-        first, ids, w = _call(q, ctx, d, 6, inp["K"])
-        again, _, _ = _call(q, ctx, d, 6, inp["K"])
+        first, ids, w = _call(q, ctx, d, T, inp["K"])
+        again, _, _ = _call(q, ctx, d, T, inp["K"])
         buf = d["x"].clone()
-        inplace, _, _ = _call(q, ctx, d, 6, inp["K"], out=buf, x=buf)
+        inplace, _, _ = _call(q, ctx, d, T, inp["K"], out=buf, x=buf)
     finally:
         q.qmoe_destroy(ctx)
     assert np.array_equal(first, again), "two calls on the same inputs differ"

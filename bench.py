@@ -87,9 +87,14 @@ WORKLOADS = {
 # kernels whose summary under profiles/ carries a DRAM traffic figure
 PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill": None,
                "step48": None, "prefill4096": None, "decode_q8k": None, "prefill_layer": None,
-               "decode_fp8": None, "prefill_fp8": None, "decode_nvfp4": None,
-               "prefill_nvfp4": None}
+               "decode_fp8": "moe_fp8_decode_T1.md", "prefill_fp8": None,
+               "decode_nvfp4": "moe_nvfp4_decode_T1.md", "prefill_nvfp4": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
+LOWBIT_T1_SOURCES = ["moe_lowbit_t1.cu", "lowbit_items.cuh", "lowbit.cuh", "topk.cuh", "kquant.cuh",
+                     "ptx_sync.cuh"]
+# the sources a profile's DRAM figure was taken on, per workload
+PROFILE_SOURCES = {"decode": FUSED_SOURCES, "decode_fp8": LOWBIT_T1_SOURCES,
+                   "decode_nvfp4": LOWBIT_T1_SOURCES}
 
 
 def parse():
@@ -126,9 +131,9 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def fused_source_hash() -> str:
+def fused_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in FUSED_SOURCES:
+    for f in sources or FUSED_SOURCES:
         h.update(open(os.path.join(ROOT, "quantized_mixture_experts_f32_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -145,7 +150,7 @@ def profiled_traffic(workload: str):
     txt = open(p).read()
     m_src = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
-    if not m_src or not m_tr or m_src.group(1) != fused_source_hash():
+    if not m_src or not m_tr or m_src.group(1) != fused_source_hash(PROFILE_SOURCES.get(workload)):
         return None
     return int(m_tr.group(1))
 

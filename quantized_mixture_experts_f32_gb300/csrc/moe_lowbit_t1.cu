@@ -119,10 +119,31 @@ __global__ void __launch_bounds__(LT_THREADS, 1) lowbit_t1(const LtParams p) {
     }
     __syncthreads();
 
-    // ---- C: gate/up items, every warp of the grid
+    // ---- C: gate/up items, every warp of the grid.  Warps are numbered warp-major
+    // over the CTAs, so the items beyond one per warp fall on a few warps of every
+    // CTA rather than on every warp of the first CTAs.
+    const int nq = H >> 2;
+    const int q0 = (int)((long)nq * blockIdx.x / G), q1 = (int)((long)nq * (blockIdx.x + 1) / G);
     if (ok) {
-        const int gw = blockIdx.x * LT_WARPS + warp, nw = G * LT_WARPS;
+        const int gw = warp * G + blockIdx.x, nw = G * LT_WARPS;
         const int hw = lane >> 4, hl = lane & 15, per = F >> 1;
+        if (lane == 0) {
+            // the rows of this warp's later items start towards L2 now, while its
+            // first item computes
+            for (int i = gw + nw; i < K * per; i += nw) {
+                const int j = i / per;
+                const size_t row = (size_t)s_sel[j] * F + 2 * (i - j * per);
+                if (FMT == 1) {
+                    bulk_prefetch_l2(p.f8.gate + row * H, (uint32_t)(2 * H));
+                    bulk_prefetch_l2(p.f8.up + row * H, (uint32_t)(2 * H));
+                } else {
+                    bulk_prefetch_l2(p.nv.gate + row * (H / 2), (uint32_t)H);
+                    bulk_prefetch_l2(p.nv.up + row * (H / 2), (uint32_t)H);
+                    bulk_prefetch_l2(p.nv.gate_bs + row * (H / 16), (uint32_t)(H / 8));
+                    bulk_prefetch_l2(p.nv.up_bs + row * (H / 16), (uint32_t)(H / 8));
+                }
+            }
+        }
         for (int i = gw; i < K * per; i += nw) {
             const int j = i / per, f = 2 * (i - j * per) + hw;
             if (FMT == 1)
@@ -131,6 +152,19 @@ __global__ void __launch_bounds__(LT_THREADS, 1) lowbit_t1(const LtParams p) {
             else
                 lowbit::nv_gateup_rows<NCG, lowbit::SRC_SMEM>(xs, xld, H, F, K, p.nv, s_sel[j], f, hl, s_slot,
                                                               j, j + 1, p.act);
+        }
+        if (lane == 0 && warp < K) {
+            // slot `warp`'s down rows of this CTA start towards L2 once the warp's
+            // gate/up bytes are in (they stream while the grid gathers at the
+            // act counter)
+            const size_t r0 = (size_t)s_sel[warp] * H + 4 * q0;
+            const uint32_t nr = (uint32_t)(4 * (q1 - q0));
+            if (FMT == 1) {
+                bulk_prefetch_l2(p.f8.down + r0 * F, nr * (uint32_t)F);
+            } else {
+                bulk_prefetch_l2(p.nv.down + r0 * (F / 2), nr * (uint32_t)(F / 2));
+                bulk_prefetch_l2(p.nv.down_bs + r0 * (F / 16), nr * (uint32_t)(F / 16));
+            }
         }
     }
     __syncthreads();
@@ -142,8 +176,6 @@ __global__ void __launch_bounds__(LT_THREADS, 1) lowbit_t1(const LtParams p) {
     ok = ok && s_ok != 0;
 
     // ---- D: this CTA's output rows, every slot, then the combine
-    const int nq = H >> 2;
-    const int q0 = (int)((long)nq * blockIdx.x / G), q1 = (int)((long)nq * (blockIdx.x + 1) / G);
     if (ok) {
         lowbit::vstage(as, p.act, K, F);
         __syncthreads();

@@ -27,7 +27,9 @@
 //    stores SiLU(g)*u; the CTA then counts itself in on one arrival word;
 //  * D: once every CTA has counted in (one thread polls that word), every CTA
 //    loads the k*F act values and computes y_j[h] for its own output rows and
-//    every slot from the down rows already in shared memory;
+//    every slot from the down rows already in shared memory (Q6_K rows are
+//    first unpacked to one code per byte in column order, while the CTA waits
+//    for the others, so that every lane of the dot products does useful work);
 //  * finally out[h] = res[h] + sum_j w_j y_j[h] in slot order: a CTA owns whole
 //    output rows, so no partial sums cross CTAs and no atomics touch values.
 // Every cross-CTA wait is bounded (%globaltimer); on expiry the kernel records
@@ -77,16 +79,24 @@ __host__ __device__ __forceinline__ int apad1(int f) { return f + 4 * (f >> 7); 
 struct T1Layout {
     int off_bar, off_misc, off_red, off_lg, off_key, off_sel, off_wts, off_x, off_xq, off_xsum,
         off_xscale, off_ys, off_gu, off_dn, total;
-    int nrs_max, nrd_max, dn_seg, act_pitch;
+    int nrs_max, nrd_max, dn_seg, act_pitch, uq_row;
 };
 
-// x (fp32, phase A) and, later, the staged act values share one region
-__host__ __device__ inline T1Layout t1_layout(int H, int E, int K, int F, int G, int rbg, int rbd) {
+// x (fp32, phase A) and, later, the staged act values share one region; so do
+// the gate/up rows and, once they are consumed, the unpacked Q6_K down rows
+// (uq_row bytes each: F six-bit codes, one per byte in column order, then F/16
+// floats d * scale; 0 when the down matrix is Q4_K)
+__host__ __device__ inline T1Layout t1_layout(int H, int E, int K, int F, int G, int rbg, int rbd,
+                                              int uq_row) {
     T1Layout L;
     L.nrs_max = (F + G - 1) / G;                 // gate/up rows per slot and CTA
     L.nrd_max = (H + G - 1) / G;                 // output rows per CTA
     L.dn_seg = al1(L.nrd_max * rbd + 32, 128);
-    L.act_pitch = al1(apad1(F) + F / 8, 4);      // one staged act row + its group sums
+    L.uq_row = uq_row;
+    // one staged act row: Q4_K down -- padded as apad1 plus its group sums;
+    // Q6_K down -- 16 lanes' column ranges, 4 floats of padding after each
+    const int ap4 = apad1(F) + F / 8, ap6 = F + 64;
+    L.act_pitch = al1(uq_row ? ap6 : ap4, 4);
     int o = 0;
     L.off_bar = o;    o += 2 * MAXK * 8;
     L.off_misc = o;   o += MS_COUNT * 4;
@@ -102,7 +112,8 @@ __host__ __device__ inline T1Layout t1_layout(int H, int E, int K, int F, int G,
     L.off_xscale = o; o += (H / 16) * 4;
     L.off_ys = o;     o += al1(K * L.nrd_max * 4, 16);
     o = al1(o, 128);
-    L.off_gu = o;     o += 2 * K * L.nrs_max * rbg;
+    L.off_gu = o;
+    o += 2 * K * L.nrs_max * rbg > K * L.nrd_max * uq_row ? 2 * K * L.nrs_max * rbg : K * L.nrd_max * uq_row;
     o = al1(o, 128);
     L.off_dn = o;     o += K * L.dn_seg;
     L.total = o;
@@ -225,15 +236,6 @@ __device__ __forceinline__ uint4 t1_lds16(const uint8_t* p) {
     const uint32_t w0 = b[0], w1 = b[1], w2 = b[2], w3 = b[3], w4 = b[4];
     return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
                       __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
-}
-
-// 8 bytes at an even shared-memory address
-__device__ __forceinline__ uint2 t1_lds8(const uint8_t* p) {
-    const uint32_t off = smem_u32(p) & 3u;
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(p - off);
-    const uint32_t sh = off * 8u;
-    const uint32_t w0 = b[0], w1 = b[1], w2 = b[2];
-    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
 }
 
 template <int NSB_G, int NSB_D, int DQT>
@@ -655,66 +657,255 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
         __threadfence();
         atomicAdd(p.ctl + ACT_WORD, 1u);
         T1_TRACE(4);
-        if (!abort_b && misc[MS_ABORT] == 0) {
-            const unsigned long long t0 = globaltimer();
-            for (int it = 1; ld_acquire_gpu(p.ctl + ACT_WORD) < (unsigned)G; ++it) {
-                __nanosleep(32);
-                if ((it & 15) == 0 && globaltimer() - t0 > p.wait_ns) {
+    }
+    // ---------------- D prologue: the k x F act values staged in shared memory
+    // once every CTA has counted in (and, for a Q6_K down matrix, the down rows
+    // unpacked meanwhile)
+    const bool run_pre = !abort_b && misc[MS_ABORT] == 0;
+    if constexpr (DQT == 2) {
+        // Warp 0: one lane polls the act counter, then the warp copies every act
+        // value (cp.async through L2) into the staging layout: lane q of a
+        // half-warp later reads columns [LQ q, LQ q + LQ) of a slot, so each such
+        // range is followed by 4 floats of padding (the 8 lanes of one 16-byte
+        // shared load then hit distinct banks).  The act values' L2 round trip
+        // thus overlaps the unpacking below.
+        if (warp == 0) {
+            int okp = 0;
+            if (lane == 0 && run_pre) {
+                okp = 1;
+                const unsigned long long t0 = globaltimer();
+                for (int it = 1; ld_acquire_gpu(p.ctl + ACT_WORD) < (unsigned)G; ++it) {
+                    __nanosleep(32);
+                    if ((it & 15) == 0 && globaltimer() - t0 > p.wait_ns) {
+                        t1_status(p.status, ST_TIMEOUT);
+                        misc[MS_ABORT] = 1;
+                        okp = 0;
+                        break;
+                    }
+                }
+                T1_TRACE(5);
+            }
+            okp = __shfl_sync(0xffffffffu, okp, 0);
+            if (okp) {
+                constexpr int LQ = 16 * NSB_D, F4 = NSB_D * QK / 4;   // F / 4
+                const int n4 = K * F4;
+                for (int i = lane; i < n4; i += 32) {
+                    const int j = i / F4, c = 4 * (i - j * F4);
+                    const int ql = c / LQ;
+                    cp_async_cg16(act_st + (size_t)j * L.act_pitch + ql * (LQ + 4) + (c - ql * LQ),
+                                  reinterpret_cast<const float4*>(p.act) + i);
+                }
+                cp_async_wait_all();
+            }
+        } else {
+            // While the other CTAs finish: this CTA's Q6_K down rows, unpacked from
+            // their copies into the (consumed) gate/up region as one six-bit code per
+            // byte in column order and the float d * scale of each 16 columns.  A unit
+            // is (slot, row, superblock s, half n, low-bit pair g01, 16 positions qq):
+            // one 16-byte run of low-bit codes, one of high bits, and from them the
+            // 16 codes of group g01 (low nibbles) and of group g01 + 2 (high
+            // nibbles).  Consecutive threads take consecutive units, so the 8 lanes
+            // of one 16-byte store write 8 different 16-byte slots of 128 bytes
+            // except for the half bit (two ways, not eight).
+            // (warps 1.. only)
+            if (!abort_b && misc[MS_ABORT] == 0) {
+                bool okd = true;
+                for (int j = 0; j < K; ++j) okd = okd && t1_mbar_wait(&dnb[j], 0, p.wait_ns);
+                if (tid == 32) T1_TRACE(11);
+                if (!okd) {
                     t1_status(p.status, ST_TIMEOUT);
                     misc[MS_ABORT] = 1;
-                    break;
+                } else {
+                    constexpr int UPR = 8 * NSB_D;
+                    uint8_t* uq = gu_s;
+                    const int nu = K * nrd * UPR;
+                    // rr / nrd as a multiply-high by ceil(2^32 / nrd): exact for rr,
+                    // nrd < 2^16 (nrd = 1 needs 2^32 itself and is taken apart)
+                    const unsigned magic = nrd > 1 ? (unsigned)((0x100000000ull + nrd - 1) / nrd) : 0u;
+                    // UB units per thread per pass, every unit's shared loads issued
+                    // before any of its stores (independent work for the scheduler)
+                    constexpr int UB = 3;
+                    for (int u0 = tid - 32; u0 < nu; u0 += UB * (TN - 32)) {
+                        uint4 ql[UB], qh[UB];
+                        int sc_lo[UB], sc_hi[UB], sh[UB];
+                        float d[UB];
+                        uint8_t* run[UB];
+                        float* dsc[UB];
+#pragma unroll
+                        for (int b = 0; b < UB; ++b) {
+                            const int u = min(u0 + b * (TN - 32), nu - 1);  // a repeated unit stores the same bytes
+                            const int rr = u / UPR, w = u - rr * UPR;
+                            const int j = nrd == 1 ? rr : (int)__umulhi((unsigned)rr, magic), r = rr - j * nrd;
+                            const int qq = w & 1, g01 = (w >> 1) & 1, n = (w >> 2) & 1, s = w >> 3;
+                            const uintptr_t src = reinterpret_cast<uintptr_t>(p.down) + ((size_t)sel[j] * H + h0) * RBD;
+                            const uint8_t* blk = dn_s + (size_t)j * L.dn_seg + (src & 15) + (size_t)r * RBD + s * Q6K_BYTES;
+                            ql[b] = t1_lds16(blk + 64 * n + 32 * g01 + 16 * qq);
+                            qh[b] = t1_lds16(blk + 128 + 32 * n + 16 * qq);
+                            sc_lo[b] = (int)*reinterpret_cast<const int8_t*>(blk + 192 + 8 * n + 2 * g01 + qq);
+                            sc_hi[b] = (int)*reinterpret_cast<const int8_t*>(blk + 192 + 8 * n + 2 * g01 + qq + 4);
+                            d[b] = __half2float(*reinterpret_cast<const __half*>(blk + 208));
+                            sh[b] = 2 * g01;                         // high bits of group g at bit 2g
+                            uint8_t* dst = uq + (size_t)(j * L.nrd_max + r) * L.uq_row;
+                            run[b] = dst + QK * s + 128 * n + 32 * g01 + 16 * qq;
+                            dsc[b] = reinterpret_cast<float*>(dst + F) + 16 * s + 8 * n + 2 * g01 + qq;
+                        }
+#pragma unroll
+                        for (int b = 0; b < UB; ++b) {
+                            const uint32_t L4[4] = {ql[b].x, ql[b].y, ql[b].z, ql[b].w};
+                            const uint32_t H4[4] = {qh[b].x, qh[b].y, qh[b].z, qh[b].w};
+                            uint32_t lo[4], hi[4];
+#pragma unroll
+                            for (int wq = 0; wq < 4; ++wq) {
+                                const uint32_t hb = H4[wq] >> sh[b];
+                                lo[wq] = (L4[wq] & 0x0F0F0F0Fu) | ((hb << 4) & 0x30303030u);
+                                hi[wq] = ((L4[wq] >> 4) & 0x0F0F0F0Fu) | (hb & 0x30303030u);
+                            }
+                            *reinterpret_cast<uint4*>(run[b]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            *reinterpret_cast<uint4*>(run[b] + 64) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            dsc[b][0] = d[b] * (float)sc_lo[b];
+                            dsc[b][4] = d[b] * (float)sc_hi[b];
+                        }
+                    }
+                    if (tid == 32) T1_TRACE(13);
                 }
             }
         }
-        T1_TRACE(5);
+        __syncthreads();
+    } else {
+        if (tid == 0) {
+            if (!abort_b && misc[MS_ABORT] == 0) {
+                const unsigned long long t0 = globaltimer();
+                for (int it = 1; ld_acquire_gpu(p.ctl + ACT_WORD) < (unsigned)G; ++it) {
+                    __nanosleep(32);
+                    if ((it & 15) == 0 && globaltimer() - t0 > p.wait_ns) {
+                        t1_status(p.status, ST_TIMEOUT);
+                        misc[MS_ABORT] = 1;
+                        break;
+                    }
+                }
+            }
+            T1_TRACE(5);
+        }
+        __syncthreads();
+        if (run_pre && misc[MS_ABORT] == 0) {
+            // two groups per thread per round, both groups' loads issued before any
+            // store (one L2 round trip per round instead of one per group)
+            const int ng = K * (F / GS);
+            for (int g0 = tid; g0 < ng; g0 += 2 * TN) {
+                float v[2][GS];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int g = g0 + u * TN;
+                    const int j = g / (F / GS), gl = g - j * (F / GS);
+                    const float4* src = reinterpret_cast<const float4*>(p.act + (size_t)j * F + gl * GS);
+#pragma unroll
+                    for (int z = 0; z < GS / 4; ++z) {
+                        const float4 w = g < ng ? __ldcg(src + z) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[u][4 * z] = w.x; v[u][4 * z + 1] = w.y; v[u][4 * z + 2] = w.z; v[u][4 * z + 3] = w.w;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int g = g0 + u * TN;
+                    if (g >= ng) continue;
+                    const int j = g / (F / GS), gl = g - j * (F / GS);
+                    float s = 0.f;
+#pragma unroll
+                    for (int z = 0; z < GS; ++z) s += v[u][z];
+                    float* ast = act_st + (size_t)j * L.act_pitch;
+#pragma unroll
+                    for (int z = 0; z < GS; z += 4)
+                        *reinterpret_cast<float4*>(ast + apad1(gl * GS + z)) =
+                            make_float4(v[u][z], v[u][z + 1], v[u][z + 2], v[u][z + 3]);
+                    ast[FPAD + gl] = s;
+                }
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    // ---------------- D prologue: all k x F act values (plain loads from L2,
-    // ordered after the count's acquire by the barrier) and their sums over the
-    // groups of one down sub-scale
     const bool run_d = !abort_b && misc[MS_ABORT] == 0;
-    if (run_d) {
-        // two groups per thread per round, both groups' loads issued before any
-        // store (one L2 round trip per round instead of one per group)
-        const int ng = K * (F / GS);
-        for (int g0 = tid; g0 < ng; g0 += 2 * TN) {
-            float v[2][GS];
+    if (tid == 0) T1_TRACE(12);
+    // ---------------- D: y_j[h] for this CTA's rows and every slot.
+    if constexpr (DQT == 2) {
+        // Q6_K down from the unpacked rows.  Half-warp hw (of 32) serves slot
+        // hw / hps (hps = 32 / K half-warps per slot) and rows sub, sub + hps, ...
+        // of it; lane q owns columns [LQ q, LQ q + LQ) -- NSB_D groups of 16 --
+        // holds their act values and group sums, and for each row takes the dot
+        // with the six-bit codes (as 0.5 + code / 256, two fp32x2 FMA chains) and
+        // sum_g d s_g (256 P_g - 160 A_g) = sum (code - 32) a; the 16 lanes' parts
+        // are summed by a fixed butterfly.
+        if (run_d) {
+            constexpr int LQ = 16 * NSB_D;
+            const int hps = 32 / K;
+            const int hw = 2 * warp + (lane >> 4), q = lane & 15;
+            const int j = hw / hps, sub = hw - j * hps;
+            const unsigned hmask = 0xFFFFu << (lane & 16);
+            const uint8_t* uq = gu_s;
+            if (j < K) {
+                const float* ast = act_st + (size_t)j * L.act_pitch + q * (LQ + 4);
+                float4 av[NSB_D][4];
+                float A[NSB_D];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int g = g0 + u * TN;
-                const int j = g / (F / GS), gl = g - j * (F / GS);
-                const float4* src = reinterpret_cast<const float4*>(p.act + (size_t)j * F + gl * GS);
+                for (int t = 0; t < NSB_D; ++t) {
 #pragma unroll
-                for (int z = 0; z < GS / 4; ++z) {
-                    const float4 w = g < ng ? __ldcg(src + z) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[u][4 * z] = w.x; v[u][4 * z + 1] = w.y; v[u][4 * z + 2] = w.z; v[u][4 * z + 3] = w.w;
+                    for (int k = 0; k < 4; ++k) av[t][k] = *reinterpret_cast<const float4*>(ast + 16 * t + 4 * k);
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        a0 += av[t][k].x + av[t][k].y;
+                        a1 += av[t][k].z + av[t][k].w;
+                    }
+                    A[t] = a0 + a1;
+                }
+                // two rows per pass (rows r and r + hps): twice the independent
+                // work between the shared loads and the butterfly
+                auto row_dot = [&](int r) {
+                    const uint8_t* row = uq + (size_t)(j * L.nrd_max + r) * L.uq_row;
+                    const float* dsc = reinterpret_cast<const float*>(row + F) + q * NSB_D;
+                    uint4 w[NSB_D];
+                    float ds[NSB_D];
+#pragma unroll
+                    for (int t = 0; t < NSB_D; ++t) {
+                        w[t] = *reinterpret_cast<const uint4*>(row + LQ * q + 16 * t);
+                        ds[t] = dsc[t];
+                    }
+                    float part = 0.f;
+#pragma unroll
+                    for (int t = 0; t < NSB_D; ++t) {
+                        const uint32_t W[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+                        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            fma2(p0, p1, mag<0>(W[k]), mag<1>(W[k]), av[t][k].x, av[t][k].y);
+                            fma2(p0, p1, mag<2>(W[k]), mag<3>(W[k]), av[t][k].z, av[t][k].w);
+                        }
+                        part = fmaf(ds[t], fmaf(256.f, p0 + p1, -160.f * A[t]), part);
+                    }
+                    return part;
+                };
+                for (int r = sub; r < nrd; r += 2 * hps) {
+                    const int r2 = r + hps;
+                    const bool two = r2 < nrd;
+                    float pa = row_dot(r);
+                    float pb = row_dot(two ? r2 : r);
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) {
+                        pa += __shfl_xor_sync(hmask, pa, o);
+                        pb += __shfl_xor_sync(hmask, pb, o);
+                    }
+                    if (q == 0) {
+                        ys[j * L.nrd_max + r] = pa;
+                        if (two) ys[j * L.nrd_max + r2] = pb;
+                    }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int g = g0 + u * TN;
-                if (g >= ng) continue;
-                const int j = g / (F / GS), gl = g - j * (F / GS);
-                float s = 0.f;
-#pragma unroll
-                for (int z = 0; z < GS; ++z) s += v[u][z];
-                float* ast = act_st + (size_t)j * L.act_pitch;
-#pragma unroll
-                for (int z = 0; z < GS; z += 4)
-                    *reinterpret_cast<float4*>(ast + apad1(gl * GS + z)) =
-                        make_float4(v[u][z], v[u][z + 1], v[u][z + 2], v[u][z + 3]);
-                ast[FPAD + gl] = s;
-            }
+            if (lane == 0) T1_TRACE(48 + warp);
         }
-    }
-    __syncthreads();
-    if (tid == 0) T1_TRACE(12);
-    // ---------------- D: y_j[h] for this CTA's rows and every slot.  Warp task
-    // (slot j, block of 8 rows); a lane owns one fixed part of a row -- a
-    // quarter of a Q6_K superblock or a 16-byte piece of a Q4_K superblock --
-    // for several rows of the block, and the parts of a row are summed across
-    // lanes by a fixed butterfly.
-    if (run_d) {
+    } else if (run_d) {
+        // Q4_K down from the raw rows.  Warp task (slot j, block of 8 rows); a
+        // lane owns one 16-byte piece of a superblock for the 8 rows of the
+        // block, and the parts of a row are summed across lanes by a fixed
+        // butterfly.
         const int nrb = (nrd + 7) / 8;
         for (int t = warp; t < K * nrb; t += TW) {
             const int j = t / nrb, rb = t - j * nrb;
@@ -726,75 +917,7 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
             const float* asm_ = ast + FPAD;
             const uintptr_t src = reinterpret_cast<uintptr_t>(p.down) + ((size_t)sel[j] * H + h0) * RBD;
             const uint8_t* seg = dn_s + (size_t)j * L.dn_seg + (src & 15);
-            if (DQT == 2) {
-                // Q6_K: lane = 16 h + q; q < 4*NSB_D is (superblock s, half n,
-                // positions 16 qq .. 16 qq + 15 of its four groups); rows
-                // 8 rb + 2 k + h, k < 4
-                const int h = lane >> 4, q = lane & 15;
-                const bool qon = q < 4 * NSB_D;
-                const int s = q >> 2, n = (q >> 1) & 1, qq = q & 1;
-                const float* ab = ast + apad1(QK * s + 128 * n) + 16 * qq;
-                const float* asb = asm_ + (QK * s + 128 * n + 16 * qq) / 8;
-                // this lane's 64 act values, read once and kept for its 4 rows
-                float4 av[16];
-                float xg[4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-#pragma unroll
-                    for (int wq = 0; wq < 4; ++wq)
-                        av[4 * g + wq] = qon ? *reinterpret_cast<const float4*>(ab + 32 * g + 4 * wq)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                    xg[g] = qon ? asb[4 * g] + asb[4 * g + 1] : 0.f;
-                }
-                float part[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = 8 * rb + 2 * k + h;
-                    part[k] = 0.f;
-                    if (qon && r < nrd) {
-                        const uint8_t* blk = seg + (size_t)r * RBD + s * Q6K_BYTES;
-                        const uint4 qa = t1_lds16(blk + 64 * n + 16 * qq);
-                        const uint4 qb = t1_lds16(blk + 64 * n + 32 + 16 * qq);
-                        const uint4 qh = t1_lds16(blk + 128 + 32 * n + 16 * qq);
-                        const uint2 scw = t1_lds8(blk + 192 + 8 * n);
-                        const float d = __half2float(*reinterpret_cast<const __half*>(blk + 208));
-                        const uint32_t A4[4] = {qa.x, qa.y, qa.z, qa.w};
-                        const uint32_t B4[4] = {qb.x, qb.y, qb.z, qb.w};
-                        const uint32_t H4[4] = {qh.x, qh.y, qh.z, qh.w};
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int bo = 8 * (2 * g + qq);          // scale byte of (g, qq)
-                            const uint32_t sw = bo < 32 ? (scw.x >> bo) : (scw.y >> (bo - 32));
-                            const float sc = (float)(int8_t)(sw & 0xFF);
-                            float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-                            for (int wq = 0; wq < 4; ++wq) {
-                                const uint32_t Aw = A4[wq], Bw = B4[wq], Hh = H4[wq];
-                                uint32_t q6;
-                                if (g == 0) q6 = (Aw & 0x0F0F0F0Fu) | ((Hh << 4) & 0x30303030u);
-                                else if (g == 1) q6 = (Bw & 0x0F0F0F0Fu) | ((Hh << 2) & 0x30303030u);
-                                else if (g == 2) q6 = ((Aw >> 4) & 0x0F0F0F0Fu) | (Hh & 0x30303030u);
-                                else q6 = ((Bw >> 4) & 0x0F0F0F0Fu) | ((Hh >> 2) & 0x30303030u);
-                                const float4 x4 = av[4 * g + wq];
-                                fma2(p0, p1, mag<0>(q6), mag<1>(q6), x4.x, x4.y);
-                                fma2(p0, p1, mag<2>(q6), mag<3>(q6), x4.z, x4.w);
-                            }
-                            // sum (q6 - 32) a = 256 P - 128 A - 32 A
-                            part[k] = fmaf(d * sc, fmaf(256.f, p0 + p1, -160.f * xg[g]), part[k]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float v = part[k];
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    const int r = 8 * rb + 2 * k + h;
-                    if (q == 0 && r < nrd) ys[j * L.nrd_max + r] = v;
-                }
-            } else {
+            {
                 // Q4_K: lane < 8*NSB_D is (superblock s, 16-byte piece pc); rows
                 // 8 rb + k, k < 8
                 const bool on = lane < 8 * NSB_D;
@@ -907,7 +1030,7 @@ bool t1_decode_plan(const MoeShape& s, int gate_t, int up_t, int down_t, int num
     if (s.K > TW) return false;
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    const T1Layout L = t1_layout(s.H, s.E, s.K, s.F, G, rbg, rbd);
+    const T1Layout L = t1_layout(s.H, s.E, s.K, s.F, G, rbg, rbd, down_t == 2 ? s.F + s.F / 4 : 0);
     if (L.total > 227 * 1024) return false;
     plan->grid = G;
     plan->smem = L.total;
@@ -931,7 +1054,7 @@ cudaError_t launch_t1_decode(const MoeShape& s, const T1Plan& plan, int down_t, 
     p.H = s.H; p.E = s.E; p.K = s.K; p.F = s.F; p.norm = s.norm_topk;
     const int rbg = (s.H / QK) * Q4K_BYTES;
     const int rbd = (s.F / QK) * (down_t == 1 ? Q4K_BYTES : Q6K_BYTES);
-    p.L = t1_layout(s.H, s.E, s.K, s.F, plan.grid, rbg, rbd);
+    p.L = t1_layout(s.H, s.E, s.K, s.F, plan.grid, rbg, rbd, down_t == 2 ? s.F + s.F / 4 : 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(TN);

@@ -121,6 +121,14 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// 16 bytes global -> shared through L2 only (no L1 line is filled, so values
+// other SMs stored in this launch are seen once their publication was acquired);
+// cp_async_wait_all waits for every such copy this thread issued
+__device__ __forceinline__ void cp_async_cg16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // L2 prefetch of `bytes` (multiple of 16) at a 16-byte aligned global address
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

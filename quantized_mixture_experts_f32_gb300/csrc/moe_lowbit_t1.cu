@@ -1,5 +1,6 @@
 // moe_lowbit_t1.cu -- the whole MoE layer for one token over FP8 or NVFP4
-// experts in one cooperative launch, one CTA per SM.
+// experts in one launch of one CTA per SM, a programmatic dependent of the
+// previous kernel (its router rows prefetched into L2 before the wait).
 //
 // The layer's steps (aprender issue "qwen3moe (Qwen3-30B-A3B, ...) has NO working
 // CUDA path", "Gaps ... G3") over the formats of the atlasinference source page
@@ -23,6 +24,7 @@
 #include <math.h>
 
 #include "lowbit_items.cuh"
+#include "pdl.cuh"
 #include "ptx_sync.cuh"
 #include "qmoe_internal.h"
 #include "topk.cuh"
@@ -64,6 +66,12 @@ __global__ void __launch_bounds__(LT_THREADS, 1) lowbit_t1(const LtParams p) {
     __shared__ float s_w[LT_KMAX];
     __shared__ unsigned s_tag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // before the previous kernel on the stream has finished: weights only (this
+    // CTA's router rows towards L2); x, the control words and the logits after
+    if (tid == 0)
+        for (int e = blockIdx.x; e < E; e += G) bulk_prefetch_l2(p.router + (size_t)e * H, (uint32_t)(H * 4));
+    pdl_wait();
+    pdl_launch_dependents();
     if (tid == 0) {
         s_tag = ld_acquire_gpu(p.ctl + 1) + 1u;
         s_ok = 1;
@@ -226,17 +234,10 @@ cudaError_t lt_launch(const LtParams& p, int num_sms, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(LT_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr_[1];
-    attr_[0].id = cudaLaunchAttributeCooperative;
-    attr_[0].val.cooperative = 1;
-    cfg.attrs = attr_;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, lowbit_t1<FMT, NCG, NCD>, p);
+    // one CTA per SM (the register file holds one 512-thread CTA at 128 registers),
+    // grid = SM count: every CTA is resident once the previous kernel's CTAs have
+    // left, and those never wait on this grid
+    return launch_pdl(lowbit_t1<FMT, NCG, NCD>, dim3(num_sms), dim3(LT_THREADS), smem, st, p);
 }
 
 }  // namespace

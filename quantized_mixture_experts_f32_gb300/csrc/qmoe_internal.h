@@ -112,8 +112,9 @@ bool nvfp4_supported(int H, int F);
 cudaError_t launch_nvfp4_experts(const MoeShape& s, const float* x, const NvExperts& w,
                                  const Route& r, float* act, float* y, int num_sms, cudaStream_t st);
 // One token over FP8 (fmt 1) or NVFP4 (fmt 2) experts: the whole layer in one
-// cooperative launch (moe_lowbit_t1.cu); lg: E tagged words, ctl: 4 words, both
-// zero at creation and owned by this kernel
+// launch of one CTA per SM, a programmatic dependent of the previous kernel
+// (moe_lowbit_t1.cu); lg: E tagged words, ctl: 4 words, both zero at creation
+// and owned by this kernel
 bool lowbit_t1_supported(int fmt, int T, int H, int E, int K, int F, int num_sms);
 cudaError_t launch_lowbit_t1(int fmt, const MoeShape& s, const float* x, const float* router_w,
                              const Fp8Experts* f8, const NvExperts* nv, float* act, float* out,

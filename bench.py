@@ -90,7 +90,7 @@ PROFILE_FOR = {"decode": "moe_decode_t1_decode_T1.md", "batch8": None, "prefill"
                "decode_fp8": "moe_fp8_decode_T1.md", "prefill_fp8": None,
                "decode_nvfp4": "moe_nvfp4_decode_T1.md", "prefill_nvfp4": None}
 FUSED_SOURCES = ["moe_decode_t1.cu", "kquant.cuh", "ptx_sync.cuh"]
-LOWBIT_T1_SOURCES = ["moe_lowbit_t1.cu", "lowbit_items.cuh", "lowbit.cuh", "topk.cuh", "kquant.cuh",
+LOWBIT_T1_SOURCES = ["moe_lowbit_t1.cu", "lowbit_items.cuh", "lowbit.cuh", "topk.cuh", "kquant.cuh", "pdl.cuh",
                      "ptx_sync.cuh"]
 # the sources a profile's DRAM figure was taken on, per workload
 PROFILE_SOURCES = {"decode": FUSED_SOURCES, "decode_fp8": LOWBIT_T1_SOURCES,

@@ -25,20 +25,22 @@ QMOE_Q4_K, QMOE_Q6_K = 1, 2
 QTYPE = {"Q4_K": QMOE_Q4_K, "Q6_K": QMOE_Q6_K}
 
 # kernels one qmoe_forward enqueues on the decode path (n_tokens <= 8): the
-# whole layer is one fused cooperative kernel
+# whole layer is one kernel (the batch-1 kernel for one token, the fused
+# cooperative kernel for 2..8)
 LAUNCHES_PER_DECODE_FORWARD = 1
 # n_tokens > 8 (tensor-core path): router GEMM, top-k, per-expert lists, gather,
 # gate/up GEMM, down GEMM, combine
 LAUNCHES_PER_PREFILL_FORWARD = 7
-# qmoe_forward_q8k: router, top-k, quantise x, gate/up, quantise act, down, combine
-LAUNCHES_PER_Q8K_FORWARD = 7
+# qmoe_forward_q8k up to 8 tokens: routing (one launch), quantise x, gate/up,
+# quantise act, down, combine (7 beyond 8 tokens: router and top-k apart)
+LAUNCHES_PER_Q8K_FORWARD = 6
 # qmoe_forward_fp8 up to 32 tokens: routing (one launch up to 8 tokens, router
 # + top-k beyond), gate/up GEMV, down GEMV, combine; more than 32 tokens (tensor
 # cores): router GEMM, top-k, per-expert lists, gather, gate/up GEMM, down GEMM,
 # combine
 FP8_GEMV_MAX = 32
 # one token at hidden 2048 / ffn 768 (up to 128 experts): the whole FP8 or NVFP4
-# layer is one cooperative kernel
+# layer is one kernel
 LAUNCHES_PER_LOWBIT_T1 = 1
 LAUNCHES_PER_FP8_FORWARD = 4           # otherwise up to 8 tokens (5 for 9..32)
 LAUNCHES_PER_FP8_FORWARD_MANY = 7

@@ -220,18 +220,22 @@ def expert_bytes(H, F, gate_t, up_t, down_t):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_rate(call, units: int, seconds: float, threads: int):
+def cpu_rate(call, units: int, seconds: float, threads: int, durations=None):
     """Units per second of `call` (which processes `units`) run back to back on
     `threads` host threads for about `seconds`.  The oracle is plain C called
     through ctypes, which releases the interpreter lock for the call, and it
-    keeps no global state, so the threads run it side by side.  Returns (rate,
-    calls, elapsed)."""
+    keeps no global state, so the threads run it side by side.  With
+    `durations` (a list), every call's own wall time in seconds is appended to
+    it.  Returns (rate, calls, elapsed)."""
     counts = [0] * threads
     t0 = time.perf_counter()
 
     def work(i):
         while time.perf_counter() - t0 < seconds:
+            c0 = time.perf_counter()
             call()
+            if durations is not None:
+                durations.append(time.perf_counter() - c0)
             counts[i] += 1
 
     ts = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
@@ -245,13 +249,19 @@ def cpu_rate(call, units: int, seconds: float, threads: int):
 
 def cpu_baseline(call, units: int, seconds: float, what: str):
     """The oracle on one thread and on every core: the all-core rate is the
-    baseline value, the single-thread rate is kept beside it."""
+    baseline value, the single-thread rate is kept beside it, with the median
+    and the minimum of the single-thread call times (each call one repetition
+    of the sample)."""
     call()
-    one, n1, e1 = cpu_rate(call, units, seconds / 2, 1)
+    one_calls = []
+    one, n1, e1 = cpu_rate(call, units, seconds / 2, 1, one_calls)
     th = cores()
     allc, na, ea = cpu_rate(call, units, seconds / 2, th)
     return {"value": allc, "unit": "tokens/s/layer", "cores": th, "kind": "oracle",
             "single_thread_value": one,
+            "single_thread_call_ms": {"median": 1e3 * float(np.median(one_calls)),
+                                      "min": 1e3 * float(np.min(one_calls)),
+                                      "repetitions": len(one_calls)},
             "sample": f"{what}: {n1} calls on 1 thread in {e1:.1f} s, {na} calls on {th} "
                       f"threads in {ea:.1f} s"}
 

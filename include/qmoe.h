@@ -82,7 +82,7 @@ typedef struct {
     int n_heads;         /* attention q heads (decode step only, else 0) */
     int n_kv_heads;      /* attention kv heads, divides n_heads */
     int head_dim;        /* 128 for qwen3moe (a multiple of 64, <= 256) */
-    int max_ctx;         /* KV-cache positions per layer */
+    int max_ctx;         /* KV-cache positions per layer, 1..262144 */
     float rope_base;     /* NEOX RoPE base */
     float rms_eps;       /* RMSNorm epsilon (all four norms) */
     void* stream;        /* cudaStream_t the work is enqueued on (NULL = legacy default) */

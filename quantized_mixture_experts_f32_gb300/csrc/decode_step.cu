@@ -423,47 +423,106 @@ size_t attn_smem(int group, int hd) {
            sizeof(__half) * ATT_CHUNK * hd;
 }
 
-// merge the splits of one q head (block per q head): split weights
-// exp(m_c - M) once in shared memory, then each thread sums a slice of the
-// splits for one dim with all its loads in flight, slices combined in order
+// merge the splits of one q head (block per q head).  Every load a thread
+// needs is issued before any of them is used, so the merge costs one round
+// trip to L2 instead of a chain of them: thread (d2, sl) holds the partial
+// accumulators of dims 2*d2, 2*d2+1 for splits sl, sl+S, ... in registers
+// while the split statistics (running max, sum of exp) are loaded beside them
+// and reduced over the block; the split weights exp(m_c - M) then go through
+// shared memory, each thread sums its splits in order and the S slices are
+// combined in order.
 constexpr int MRG_THREADS = 256;
+constexpr int MRG_LD = 16;            // splits per thread held in registers at once
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = red[0];
+    for (int i = 1; i < MRG_THREADS / 32; ++i) t = is_max ? fmaxf(t, red[i]) : t + red[i];
+    return t;
+}
 
 __global__ void __launch_bounds__(MRG_THREADS) attn_merge(const float* __restrict__ part,
                                                           int nsplit, int nvalid, int hd,
                                                           float* __restrict__ out) {
-    extern __shared__ float wsh[];                     // nvalid weights, then slice sums
-    __shared__ float tot_s[2];
+    extern __shared__ float wsh[];                     // nvalid m_c (then weights), nvalid l_c,
+                                                       // then S * hd slice sums
+    __shared__ float red_m[MRG_THREADS / 32], red_l[MRG_THREADS / 32];
     const int h = blockIdx.x, tid = threadIdx.x;
+    const int pitch = hd + 2;                          // per split: m, l, acc[hd]
+    const int hd2 = hd / 2;
+    const int S = MRG_THREADS / hd2;                   // slices of splits (hd <= 256: S >= 2)
+    const int d2 = tid % hd2, sl = tid / hd2;
+    const bool has = sl < S;                           // hd = 192 leaves 64 threads idle here
+    float* ls = wsh + nvalid;
+    float* acc_s = ls + nvalid;
     griddep_wait_launch();
-    const float* ph = part + (size_t)h * nsplit * (hd + 2);
-    float* acc_s = wsh + nvalid;
-    if (tid < 32) {
-        float m = -INFINITY;
-        for (int c = tid; c < nvalid; c += 32) m = fmaxf(m, ph[(size_t)c * (hd + 2)]);
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.f;
-        for (int c = tid; c < nvalid; c += 32) {
-            const float w = expf(ph[(size_t)c * (hd + 2)] - m);
-            wsh[c] = w;
-            l = fmaf(w, ph[(size_t)c * (hd + 2) + 1], l);
-        }
-        l = warp_sum(l);
-        if (tid == 0) tot_s[0] = l;
+    const float* ph = part + (size_t)h * nsplit * pitch;
+    // the accumulators of this thread's first MRG_LD splits ...
+    float2 av[MRG_LD];
+#pragma unroll
+    for (int j = 0; j < MRG_LD; ++j) {
+        const int c = sl + j * S;
+        av[j] = has && c < nvalid ? *reinterpret_cast<const float2*>(ph + (size_t)c * pitch + 2 + 2 * d2)
+                                  : make_float2(0.f, 0.f);
     }
-    __syncthreads();
-    const int S = MRG_THREADS / hd;                    // slices of splits
-    const int d = tid % hd, sl = tid / hd;
-    if (sl < S) {
-        float a = 0.f;
-#pragma unroll 8
-        for (int c = sl; c < nvalid; c += S) a = fmaf(wsh[c], ph[(size_t)c * (hd + 2) + 2 + d], a);
-        acc_s[sl * hd + d] = a;
+    // ... and the split statistics, in flight together
+    float m = -INFINITY;
+    for (int c = tid; c < nvalid; c += MRG_THREADS) {
+        const float2 v = *reinterpret_cast<const float2*>(ph + (size_t)c * pitch);
+        wsh[c] = v.x;
+        ls[c] = v.y;
+        m = fmaxf(m, v.x);
+    }
+    const float M = block_reduce(m, true, red_m);
+    float l = 0.f;
+    for (int c = tid; c < nvalid; c += MRG_THREADS) {
+        const float w = expf(wsh[c] - M);
+        wsh[c] = w;
+        l = fmaf(w, ls[c], l);
+    }
+    const float tot = block_reduce(l, false, red_l);  // its barrier also publishes the weights
+    float2 a = make_float2(0.f, 0.f);
+    if (has) {
+#pragma unroll
+        for (int j = 0; j < MRG_LD; ++j) {
+            const int c = sl + j * S;
+            if (c < nvalid) {
+                a.x = fmaf(wsh[c], av[j].x, a.x);
+                a.y = fmaf(wsh[c], av[j].y, a.y);
+            }
+        }
+        // splits beyond the first MRG_LD * S (contexts over 4096 at head_dim 128)
+        for (int c0 = sl + MRG_LD * S; c0 < nvalid; c0 += MRG_LD * S) {
+#pragma unroll
+            for (int j = 0; j < MRG_LD; ++j) {
+                const int c = c0 + j * S;
+                av[j] = c < nvalid ? *reinterpret_cast<const float2*>(ph + (size_t)c * pitch + 2 + 2 * d2)
+                                   : make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < MRG_LD; ++j) {
+                const int c = c0 + j * S;
+                if (c < nvalid) {
+                    a.x = fmaf(wsh[c], av[j].x, a.x);
+                    a.y = fmaf(wsh[c], av[j].y, a.y);
+                }
+            }
+        }
+        acc_s[sl * hd + 2 * d2] = a.x;
+        acc_s[sl * hd + 2 * d2 + 1] = a.y;
     }
     __syncthreads();
     if (tid < hd) {
-        float a = 0.f;
-        for (int k = 0; k < S; ++k) a += acc_s[k * hd + tid];
-        out[(size_t)h * hd + tid] = a / tot_s[0];
+        float r = 0.f;
+        for (int k = 0; k < S; ++k) r += acc_s[k * hd + tid];
+        out[(size_t)h * hd + tid] = r / tot;
     }
 }
 
@@ -508,7 +567,7 @@ cudaError_t launch_attention_block(const AttnShape& a, const LayerAttn& L, const
     if (hpt <= 1) QMOE_ATT(1); else if (hpt <= 2) QMOE_ATT(2); else if (hpt <= 4) QMOE_ATT(4); else QMOE_ATT(8);
 #undef QMOE_ATT
     if (e != cudaSuccess) return e;
-    e = launch_pdl(attn_merge, dim3(a.nq), dim3(MRG_THREADS), sizeof(float) * (nvalid + MRG_THREADS), st,
+    e = launch_pdl(attn_merge, dim3(a.nq), dim3(MRG_THREADS), sizeof(float) * (2 * nvalid + 2 * MRG_THREADS), st,
                    (const float*)part, nsplit, nvalid, a.hd, att);
     if (e != cudaSuccess) return e;
     // B7: h_out = h + Wo att

@@ -108,7 +108,7 @@ bool config_ok(const qmoe_config* c, char* why, size_t n) {
         if (c->head_dim < 64 || c->head_dim > 256 || c->head_dim % 64) { snprintf(why, n, "head_dim=%d must be a multiple of 64 in 64..256", c->head_dim); return false; }
         if ((c->n_heads * c->head_dim) % 256) { snprintf(why, n, "n_heads*head_dim=%d is not a multiple of 256", c->n_heads * c->head_dim); return false; }
         if ((c->n_kv_heads * c->head_dim) % 256 && c->n_kv_heads * c->head_dim % 32) { snprintf(why, n, "bad kv dim"); return false; }
-        if (c->max_ctx < 1) { snprintf(why, n, "max_ctx=%d must be >= 1", c->max_ctx); return false; }
+        if (c->max_ctx < 1 || c->max_ctx > (1 << 18)) { snprintf(why, n, "max_ctx=%d outside 1..262144 (the attention merge keeps two floats per 64 positions in shared memory)", c->max_ctx); return false; }
         if (!(c->rope_base > 0.f) || !(c->rms_eps > 0.f)) { snprintf(why, n, "rope_base and rms_eps must be positive"); return false; }
         if (c->hidden > 4096 || c->n_heads * c->head_dim > 4096) { snprintf(why, n, "decode step serves hidden and n_heads*head_dim up to 4096"); return false; }
         if (!qmoe::attention_supported(c->n_heads, c->n_kv_heads, c->head_dim)) { snprintf(why, n, "attention shape n_heads=%d n_kv_heads=%d head_dim=%d not served (at most 32 q heads per kv head)", c->n_heads, c->n_kv_heads, c->head_dim); return false; }

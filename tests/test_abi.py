@@ -53,6 +53,14 @@ def test_workspace_bytes_and_bad_configs(q):
         assert q.qmoe_workspace_bytes(bad) == 0
 
 
+def test_max_ctx_bound(q):
+    # the split-K attention merge keeps two floats per 64 positions in shared
+    # memory: contexts up to 2^18 positions are served, longer ones refused
+    geo = dict(n_heads=32, n_kv_heads=4, head_dim=128, rope_base=1e7, rms_eps=1e-6)
+    assert q.qmoe_workspace_bytes(q.make_config(2048, 128, 8, 768, 1, max_ctx=1 << 18, **geo)) > 0
+    assert q.qmoe_workspace_bytes(q.make_config(2048, 128, 8, 768, 1, max_ctx=(1 << 18) + 1, **geo)) == 0
+
+
 def test_create_rejects_bad_config_before_touching_cuda(q):
     with pytest.raises(q.QmoeError) as ei:
         q.qmoe_create(q.make_config(2048, 128, 17, 768, 1))

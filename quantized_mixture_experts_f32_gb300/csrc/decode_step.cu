@@ -232,21 +232,23 @@ __global__ void rope_table(const double* __restrict__ inv_freq, int half, int po
     }
 }
 
-// Per-head RMSNorm (weights nw) and NEOX RoPE (table cs) of one head vector
-// held by a warp: lane owns dims lane + 32 i, i < hd/32, so the rotated pairs
-// (d, d + hd/2) sit in the same lane.
-__device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
-                                               const float* __restrict__ nw, float eps, int hd,
-                                               const float2* __restrict__ cs,
+// One head vector into a warp: lane owns dims lane + 32 i, i < hd/32, so the
+// pairs (d, d + hd/2) that RoPE rotates together sit in the same lane.
+__device__ __forceinline__ void load_head(const float* __restrict__ src, int hd, float (&v)[ATT_DPL]) {
+    const int lane = threadIdx.x & 31, n = hd / 32;
+#pragma unroll
+    for (int i = 0; i < ATT_DPL; ++i) v[i] = i < n ? src[lane + 32 * i] : 0.f;
+}
+
+// Per-head RMSNorm (weights nw) and NEOX RoPE (table cs) of a head vector held
+// as load_head leaves it (v is overwritten)
+__device__ __forceinline__ void norm_rope_vals(float (&v)[ATT_DPL], const float* __restrict__ nw,
+                                               float eps, int hd, const float2* __restrict__ cs,
                                                float (&o)[ATT_DPL]) {
     const int lane = threadIdx.x & 31, n = hd / 32;
-    float v[ATT_DPL];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < ATT_DPL; ++i) {
-        v[i] = i < n ? src[lane + 32 * i] : 0.f;
-        ss = fmaf(v[i], v[i], ss);
-    }
+    for (int i = 0; i < ATT_DPL; ++i) ss = fmaf(v[i], v[i], ss);
     ss = warp_sum(ss);
     const float r = rsqrtf(ss / (float)hd + eps);
 #pragma unroll
@@ -261,6 +263,16 @@ __device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
             o[i + n / 2] = b * t.x + a * t.y;
         }
     }
+}
+
+// both, for a head vector read from src
+__device__ __forceinline__ void norm_rope_warp(const float* __restrict__ src,
+                                               const float* __restrict__ nw, float eps, int hd,
+                                               const float2* __restrict__ cs,
+                                               float (&o)[ATT_DPL]) {
+    float v[ATT_DPL];
+    load_head(src, hd, v);
+    norm_rope_vals(v, nw, eps, hd, cs, o);
 }
 
 // Split-K (flash-decoding) GQA attention with the per-head Q/K RMSNorm, RoPE
@@ -281,7 +293,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
     __half* __restrict__ k_cache, __half* __restrict__ v_cache, int pos, int hd, int nq, int nkv,
     int max_ctx, int nsplit, float* __restrict__ part) {
     extern __shared__ __align__(16) float sm[];
-    const int kvh = blockIdx.x, c = blockIdx.y;
+    // chunks in reverse block order: the CTA that owns position pos (and does
+    // the KV append on top of its chunk) is among the first to be scheduled
+    const int kvh = blockIdx.x, c = gridDim.y - 1 - blockIdx.y;
     const int group = nq / nkv;
     const int p0 = c * ATT_CHUNK, p1 = min(p0 + ATT_CHUNK, pos + 1);
     const int np = p1 - p0;
@@ -321,6 +335,14 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
     // q, k and v are the previous kernel's output (the tile above holds only
     // slots of earlier positions, and the slot at pos is overwritten below)
     griddep_wait_launch();
+    // the chunk owner's warp 0 loads the new token's k and v together with its
+    // q head, so the append costs no round trip of its own
+    const bool owner = pos >= p0 && pos < p1;
+    float knew[ATT_DPL], vnew[ATT_DPL];
+    if (owner && warp == 0) {
+        load_head(k_raw + (size_t)kvh * hd, hd, knew);
+        load_head(v_raw + (size_t)kvh * hd, hd, vnew);
+    }
     // q heads of this kv head: RMSNorm + RoPE (warp per head)
     for (int g = warp; g < group; g += nw) {
         float o[ATT_DPL];
@@ -330,10 +352,10 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
             if (i < hd / 32) qs[g * hd + lane + 32 * i] = o[i];
     }
     __syncthreads();                                   // tile staged (row pos - p0 is stale)
-    if (pos >= p0 && pos < p1 && warp == 0) {
+    if (owner && warp == 0) {
         // the new token's k and v: cache slot pos and tile row pos - p0
         float o[ATT_DPL];
-        norm_rope_warp(k_raw + (size_t)kvh * hd, k_norm, eps, hd, rope_cs, o);
+        norm_rope_vals(knew, k_norm, eps, hd, rope_cs, o);
         __half* kc = k_cache + ((size_t)kvh * max_ctx + pos) * hd;
         __half* vc = v_cache + ((size_t)kvh * max_ctx + pos) * hd;
         __half* kt = reinterpret_cast<__half*>(ks + (pos - p0) * kw);
@@ -343,7 +365,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_partial(
             if (i < hd / 32) {
                 const int d = lane + 32 * i;
                 const __half kh = __float2half_rn(o[i]);
-                const __half vh = __float2half_rn(v_raw[(size_t)kvh * hd + d]);
+                const __half vh = __float2half_rn(vnew[i]);
                 kc[d] = kh;
                 vc[d] = vh;
                 kt[d] = kh;

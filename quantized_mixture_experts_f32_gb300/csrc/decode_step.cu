@@ -76,7 +76,7 @@ __device__ __forceinline__ void griddep_wait_launch() {
 }
 
 template <int RPW, int NT>
-__global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
+__global__ void __launch_bounds__(GV_WARPS * 32, 2) q4k_gemv(const GemvArgs a) {
     extern __shared__ float sx[];
     float* xsum = sx + xpad(a.cols);
     __shared__ float red[GV_WARPS];
@@ -113,6 +113,11 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
     // x is the previous kernel's output: wait for it only now, with the weight
     // loads already in flight
     griddep_wait_launch();
+    // the residual rows, in flight with x (read at the end, they would add a
+    // round trip after the dot products)
+    float resv[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) resv[i] = lane == 0 && wp[i] && rp[i] ? rp[i][rr[i]] : 0.f;
     // x (and the norm weights) in flight at once: cols <= 4096, 4 float4 per thread
     constexpr int XLD = 4096 / 4 / (GV_WARPS * 32);
     float4 xv[XLD], wv[XLD];
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) q4k_gemv(const GemvArgs a) {
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0 && wp[i]) yp[i][rr[i]] = acc + (rp[i] ? rp[i][rr[i]] : 0.f);
+        if (lane == 0 && wp[i]) yp[i][rr[i]] = acc + resv[i];
     }
 }
 

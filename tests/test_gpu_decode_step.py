@@ -3,8 +3,8 @@
 A decode step runs every qwen3moe decoder layer on one token: RMSNorm, Q/K/V,
 per-head Q/K RMSNorm, NEOX RoPE, fp16 KV append, GQA attention, O-proj +
 residual, RMSNorm, MoE FFN + residual.  Checked: the final hidden state (max
-relative error 2e-3), the expert ids of every layer (exact, up to F32
-near-ties), and the KV-cache slot each layer writes (fp16, within one half-ulp
+relative error 2e-3), the expert ids of every layer (exact), and the KV-cache
+slot each layer writes (fp16, within one half-ulp
 of the oracle's rounding of its own value, plus the fp32-vs-fp64 difference).
 """
 import numpy as np
@@ -75,19 +75,19 @@ def _run(q, geo, pos, n_layers):
 
 
 def _oracle(geo, smalls, h0, pos, gpu_ids):
+    """The step as the oracle defines it: the pinned decoder layer applied
+    layer after layer, each on its own weights and KV cache.  The expert ids
+    of every layer must equal the kernel's exactly: at these fixed seeds the
+    K-th and (K+1)-th logits of every layer are at least 1.3e-4 * max|logit|
+    apart on the 48-layer workload and 3.6e-2 on the small geometry (pinned on
+    the CPU in tests/test_oracle_layer.py), far above the fp32 error of the
+    logits."""
     h = h0.astype(np.float64)
     outs = []
     for l, small in enumerate(smalls):
         ex = synth.step_layer_experts(geo, l)
         r = oracle.decode_layer(geo, small, ex, h, pos)
-        if not np.array_equal(r["ids"], gpu_ids[l]):
-            # accept only a swap at an F32 near-tie, then follow the kernel's choice
-            lg = r["logits"].astype(np.float64)
-            changed = set(r["ids"].tolist()) ^ set(gpu_ids[l].tolist())
-            kth = lg[r["ids"]].min()
-            assert all(abs(lg[e] - kth) <= 1e-5 * np.abs(lg).max() for e in changed), \
-                (l, r["ids"], gpu_ids[l])
-            r = oracle.decode_layer(geo, small, ex, h, pos, force=gpu_ids[l])
+        assert np.array_equal(r["ids"], gpu_ids[l]), (l, r["ids"], gpu_ids[l])
         outs.append(r)
         h = r["h"]
     return h, outs

@@ -152,3 +152,22 @@ def test_head_dim_is_independent_of_hidden_over_heads(oracle_lib):
     assert geo["n_heads"] * geo["head_dim"] == 4096 != geo["H"]
     small = synth.step_layer_small(dict(SMALL, H=256, n_heads=4, head_dim=128), 0)
     assert small["wq"].shape[0] == 4 * 128 and small["wo"].shape[1] == synth.row_bytes("Q4_K", 512)
+
+
+@pytest.mark.parametrize("pos", [0, 17, 39])
+def test_step_test_seeds_have_no_topk_near_tie(oracle_lib, pos):
+    """The GPU decode-step test demands the kernel's expert ids exactly; that is
+    sound only if no layer of its small workload has its K-th and (K+1)-th
+    router logits within the fp32 error of each other.  Here they are at least
+    1e-2 * max|logit| apart (about 1e4 times the fp32 rounding of a logit)."""
+    from tests.test_gpu_decode_step import SMALL as STEP_SMALL
+    geo = STEP_SMALL
+    h = synth.step_input(geo).astype(np.float64)
+    for l in range(geo["n_layers"]):
+        small = synth.step_layer_small(geo, l)
+        ex = synth.step_layer_experts(geo, l)
+        r = oracle_lib.decode_layer(geo, small, ex, h, pos)
+        lg = np.sort(r["logits"].astype(np.float64))[::-1]
+        K = geo["K"]
+        assert lg[K - 1] - lg[K] > 1e-2 * np.abs(lg).max(), (pos, l)
+        h = r["h"]

@@ -927,6 +927,13 @@ def main():
     ws, rank, local, pg = dist_init()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
+    try:
+        # device memory in use before this run allocates anything: its own CUDA
+        # context plus whatever other processes hold on the GPU
+        free0, total0 = torch.cuda.mem_get_info(dev)
+        gpu_mem = {"total_mib": total0 >> 20, "used_before_run_mib": (total0 - free0) >> 20}
+    except Exception as e:  # recorded, never fatal
+        gpu_mem = {"error": str(e)}
     import quantized_mixture_experts_f32_gb300 as q
     stream = torch.cuda.Stream(dev)
     if args.workload == "step48":
@@ -958,6 +965,7 @@ def main():
                 "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": args.steps * res["launches"],
         "clocks": res["clocks"],
+        "gpu_memory": gpu_mem,
     }
     if "dtype" in res:
         line["dtype"] = res["dtype"]

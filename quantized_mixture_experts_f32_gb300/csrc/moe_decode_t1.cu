@@ -78,7 +78,7 @@ __host__ __device__ __forceinline__ int apad1(int f) { return f + 4 * (f >> 7); 
 
 struct T1Layout {
     int off_bar, off_misc, off_red, off_lg, off_key, off_sel, off_wts, off_x, off_xq, off_xsum,
-        off_xscale, off_ys, off_res, off_gu, off_dn, total;
+        off_xscale, off_ys, off_gu, off_dn, total;
     int nrs_max, nrd_max, dn_seg, act_pitch, uq_row;
 };
 
@@ -111,7 +111,6 @@ __host__ __device__ inline T1Layout t1_layout(int H, int E, int K, int F, int G,
     L.off_xsum = o;   o += (H / 16) * 4;
     L.off_xscale = o; o += (H / 16) * 4;
     L.off_ys = o;     o += al1(K * L.nrd_max * 4, 16);
-    L.off_res = o;    o += al1(L.nrd_max * 4, 16);
     o = al1(o, 128);
     L.off_gu = o;
     o += 2 * K * L.nrs_max * rbg > K * L.nrd_max * uq_row ? 2 * K * L.nrs_max * rbg : K * L.nrd_max * uq_row;
@@ -268,7 +267,6 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
     float* xsum = reinterpret_cast<float*>(sm + L.off_xsum);
     float* xscale = reinterpret_cast<float*>(sm + L.off_xscale);
     float* ys = reinterpret_cast<float*>(sm + L.off_ys);
-    float* res_s = reinterpret_cast<float*>(sm + L.off_res);                 // [nrd] residual rows
     uint8_t* gu_s = sm + L.off_gu;
     uint8_t* dn_s = sm + L.off_dn;
 
@@ -311,10 +309,6 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
         const int q = tid + i * TN;
         xr[i] = q < HQ ? __ldg(reinterpret_cast<const float4*>(p.x) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // the residual of this CTA's output rows, in flight with x (read at the
-    // very end, it would add one more round trip to the layer; out may alias
-    // it, but no row is written before every CTA has passed this point)
-    for (int r = tid; r < nrd; r += TN) res_s[r] = (p.res ? p.res : p.x)[h0 + r];
     if (p.norm_w) {
         float ss = 0.f;
 #pragma unroll
@@ -976,8 +970,9 @@ __global__ void __launch_bounds__(TN, 1) moe_decode_t1(const __grid_constant__ T
     if (tid == 0) T1_TRACE(6);
     if (!abort_b && misc[MS_ABORT] == 0) {
         // out[h] = res[h] + sum_j w_j y_j[h], slot order
+        const float* res = p.res ? p.res : p.x;
         for (int r = tid; r < nrd; r += TN) {
-            float o = res_s[r];
+            float o = res[h0 + r];
             for (int j = 0; j < K; ++j) o = fmaf(wts[j], ys[j * L.nrd_max + r], o);
             p.out[h0 + r] = o;
         }
